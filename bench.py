@@ -1,0 +1,487 @@
+"""Benchmark of the scan primitives on one GB300 (or N replicas under torchrun).
+
+One step = forward + backward of every scan primitive at its benchmark shape:
+  matrix_affine_scan lab      B=128 T=64   H=8  k=8
+  matrix_scan long-T Givens   B=16  T=1024 H=8  k=8
+  parallel_scan_log minGRU    B=64  T=4096 D=1024
+  matrix_affine_scan scaled   B=32  T=8192 H=64 k=8
+Inputs are seeded synthetic tensors resident in HBM; the two small shapes fit in
+L2, so L2 is flushed (a 512 MiB write) before each of their calls.  Each call is
+bracketed by CUDA events on the launching stream; the step's device time is the
+sum of its eight calls.  value = algorithmic bytes of a step / that time (GB/s).
+
+Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle on the
+host cores instead (bounded sample of the same workloads).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd scan µs and achieved HBM GB/s (% of peak) per op and shape"
+WORKLOAD_IDS = (1, 2, 3, 4)
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def op_bytes(w, direction):
+    """Bytes each argument contributes when read or written once (fp32)."""
+    B, T, H, k = w.B, w.T, w.H, w.k
+    if w.op == "mas":
+        steps = B * T * H
+        init = B * H * k * 4
+        if direction == "fwd":  # read A, b; write h; read h0
+            return steps * 4 * (k * k + 2 * k) + (init if w.h0 != "none" else 0)
+        # read A, grad_h, h; write dA, db; read h0 (if any); write dh0
+        return steps * 4 * (2 * k * k + 3 * k) + (init if w.h0 != "none" else 0) + init
+    if w.op == "ms":
+        steps = B * T * H
+        return steps * 4 * (2 * k * k if direction == "fwd" else 4 * k * k)
+    elems = B * T * H  # H holds D for parallel_scan_log
+    init = B * H * 4
+    if direction == "fwd":  # read lc, lv; write h; read log_h0
+        return elems * 12 + init
+    return elems * 24 + 2 * init  # read lc, lv, g, h; write dlc, dlv; read log_h0, write d_log_h0
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scan_linear_recurrences_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, only if
+    it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    e = d.get("kernels", {}).get(kernel)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- GPU arm
+class Runner:
+    """Holds one workload's device buffers and runs its fwd / bwd calls."""
+
+    def __init__(self, w, torch, b, api, device):
+        self.w = w
+        self.t = torch
+        d = w.make(device=device)
+        self.inp = d
+        B, T, H, k = w.B, w.T, w.H, w.k
+        e = lambda *s: torch.empty(s, dtype=torch.float32, device=device)
+        if w.op == "mas":
+            self.h = e(B, T, H, k)
+            self.dA, self.db, self.dh0 = e(B, T, H, k, k), e(B, T, H, k), e(B, H, k)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, B, T, H, k, device)
+            self.ws_b, self.nb = api.workspace(b.MGS_OP_MATRIX_AFFINE_SCAN_BWD, B, T, H, k, device)
+        elif w.op == "ms":
+            self.P, self.dA = e(B, T, H, k, k), e(B, T, H, k, k)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_MATRIX_SCAN_FWD, B, T, H, k, device)
+            self.ws_b, self.nb = api.workspace(b.MGS_OP_MATRIX_SCAN_BWD, B, T, H, k, device)
+        else:
+            self.h = e(B, T, H)
+            self.dlc, self.dlv, self.dl0 = e(B, T, H), e(B, T, H), e(B, H)
+        self.b = b
+
+    def fwd(self, stream):
+        w, d, b = self.w, self.inp, self.b
+        if w.op == "mas":
+            b.mgs_matrix_affine_scan_fwd(d["A"], d["b"], d["h0"], self.h, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
+        elif w.op == "ms":
+            b.mgs_matrix_scan_fwd(d["A"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
+        else:
+            b.mgs_parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, None,
+                                        w.B, w.T, w.H, None, 0, stream)
+
+    def bwd(self, stream):
+        w, d, b = self.w, self.inp, self.b
+        if w.op == "mas":
+            b.mgs_matrix_affine_scan_bwd(d["A"], d["h0"], self.h, d["grad_h"], self.dA, self.db, self.dh0,
+                                         w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
+        elif w.op == "ms":
+            b.mgs_matrix_scan_bwd(d["A"], self.P, d["grad_P"], self.dA, w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
+        else:
+            b.mgs_parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, d["grad_h"],
+                                        self.dlc, self.dlv, self.dl0, w.B, w.T, w.H, None, 0, stream)
+
+    # e2e: host buffers in pinned memory, copies inside the timed region
+    def host_setup(self):
+        t = self.t
+        self.host_in = {k: v.cpu().pin_memory() for k, v in self.inp.items() if v is not None}
+        outs = self.outputs()
+        self.host_out = [t.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        self.h2d = sum(v.numel() * 4 for v in self.host_in.values())
+        self.d2h = sum(o.numel() * 4 for o in outs)
+
+    def outputs(self):
+        if self.w.op == "mas":
+            return [self.h, self.dA, self.db, self.dh0]
+        if self.w.op == "ms":
+            return [self.P, self.dA]
+        return [self.h, self.dlc, self.dlv, self.dl0]
+
+    def e2e_step(self, stream):
+        for k, v in self.host_in.items():
+            self.inp[k].copy_(v, non_blocking=True)
+        self.fwd(stream)
+        self.bwd(stream)
+        for dst, src in zip(self.host_out, self.outputs()):
+            dst.copy_(src, non_blocking=True)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+
+    from scan_linear_recurrences_gb300 import _binding as b
+    from scan_linear_recurrences_gb300 import api, inputs
+    from scan_linear_recurrences_gb300.build import build
+    build()
+    b.lib()
+
+    ids = [int(x) for x in args.workloads.split(",")]
+    runners = [Runner(inputs.WORKLOADS[i], torch, b, api, device) for i in ids]
+    small = {r.w.cid: (r.w.op != "psl" and r.w.B * r.w.T * r.w.H * r.w.k * r.w.k * 4 * 3 < (256 << 20)) for r in runners}
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    sid = stream.cuda_stream
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def one_step(evs):
+        for r in runners:
+            if small[r.w.cid]:
+                flush.zero_()
+            e0, e1, e2 = evs[r.w.cid]
+            e0.record(stream)
+            r.fwd(sid)
+            e1.record(stream)
+            r.bwd(sid)
+            e2.record(stream)
+
+    for _ in range(args.warmup):
+        one_step({r.w.cid: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for r in runners})
+    b.mgs_check(sid)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    all_evs = []
+    barrier()
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        evs = {r.w.cid: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for r in runners}
+        one_step(evs)
+        all_evs.append(evs)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    b.mgs_check(sid)
+
+    # per-op times (ms)
+    per = {}
+    for r in runners:
+        f = [ev[r.w.cid][0].elapsed_time(ev[r.w.cid][1]) for ev in all_evs]
+        bw = [ev[r.w.cid][1].elapsed_time(ev[r.w.cid][2]) for ev in all_evs]
+        per[r.w.cid] = (f, bw)
+    step_ms = [sum(per[c][0][i] + per[c][1][i] for c in per) for i in range(args.steps)]
+    local_ms = statistics.mean(step_ms)
+    if world > 1:
+        tt = torch.tensor([local_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    else:
+        ms_step = local_ms
+
+    peak, peak_kind = measured_peak()
+    step_bytes = sum(op_bytes(r.w, "fwd") + op_bytes(r.w, "bwd") for r in runners)
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+
+    ops = {}
+    dominant = None
+    for r in runners:
+        w = r.w
+        f, bw = per[w.cid]
+        fm, bm = statistics.median(f), statistics.median(bw)
+        fb, bb_ = op_bytes(w, "fwd"), op_bytes(w, "bwd")
+        key = f"{w.op}_c{w.cid}"
+        ops[key] = {
+            "shape": w.name, "fwd_us": round(fm * 1e3, 2), "bwd_us": round(bm * 1e3, 2),
+            "fwd_bwd_us": round((fm + bm) * 1e3, 2),
+            "fwd_GBps": round(fb / (fm * 1e-3) / 1e9, 1), "bwd_GBps": round(bb_ / (bm * 1e-3) / 1e9, 1),
+            "fwd_bwd_GBps": round((fb + bb_) / ((fm + bm) * 1e-3) / 1e9, 1),
+            "fwd_bwd_pct_of_peak": round(100 * (fb + bb_) / ((fm + bm) * 1e-3) / 1e9 / peak, 1),
+            "l2": "flushed" if small[w.cid] else "inputs larger than L2",
+        }
+        for direction, tms, nbytes in (("fwd", statistics.mean(f), fb), ("bwd", statistics.mean(bw), bb_)):
+            if dominant is None or tms > dominant[1]:
+                dominant = (f"{w.op}_{direction}_c{w.cid}", tms, nbytes, w, direction)
+
+    kname, kms, kbytes, kw, kdir = dominant
+    achieved = kbytes / (kms * 1e-3) / 1e9
+    kernel_symbol = {"mas": "mas", "ms": "ms", "psl": "psl"}[kw.op] + f"_{kdir}_kernel"
+    traffic = committed_traffic(f"{kernel_symbol}@c{kw.cid}")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": kernel_symbol, "workload": kw.name,
+                "algorithmic_bytes_per_launch": kbytes, "peak_kind": f"{peak_kind} hbm_gbs (copy, burst)"}
+
+    # e2e through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        for r in runners:
+            r.host_setup()
+        for _ in range(1):
+            for r in runners:
+                r.e2e_step(sid)
+        barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        n_e2e = max(1, min(args.steps, 3))
+        for _ in range(n_e2e):
+            for r in runners:
+                r.e2e_step(sid)
+        ev1.record(stream)
+        barrier()
+        e2e_ms = ev0.elapsed_time(ev1) / n_e2e
+        if world > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        b.mgs_check(sid)
+        e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": sum(r.h2d for r in runners), "d2h_bytes_per_step": sum(r.d2h for r in runners),
+               "ms_per_step": round(e2e_ms, 3)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(runners, budget_s=args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": " + ".join(r.w.name for r in runners) + ", fwd+bwd each",
+                       "l2": "flushed before the two L2-resident shapes; the others exceed L2",
+                       "step_bytes": step_bytes, "wall_s_timed_region": round(wall, 4)},
+            "ops": ops, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * 2 * len(runners), "clocks": clocks,
+            "impl": "libmgscan",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU (oracle) legs
+def _oracle_sample(w, rows, device_inputs=None):
+    """Float64 oracle inputs for `rows` batch rows of workload w."""
+    import torch
+    d = device_inputs if device_inputs is not None else w.make(device="cpu")
+    return {k: (v[:rows].cpu() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def _time_oracle(w, s):
+    import numpy as np
+    import oracle
+    f64 = lambda x: None if x is None else np.ascontiguousarray(x.double().numpy())
+    if w.op == "mas":
+        A, bb, h0, g = f64(s["A"]), f64(s["b"]), f64(s["h0"]), f64(s["grad_h"])
+        t0 = time.perf_counter(); oracle.mas_fwd(A, bb, h0); t1 = time.perf_counter()
+        oracle.mas_bwd(A, bb, h0 if h0 is not None else np.zeros((A.shape[0], w.H, w.k)), g)
+        t2 = time.perf_counter()
+    elif w.op == "ms":
+        A, G = f64(s["A"]), f64(s["grad_P"])
+        t0 = time.perf_counter(); oracle.ms_fwd(A); t1 = time.perf_counter()
+        oracle.ms_bwd(A, G); t2 = time.perf_counter()
+    else:
+        lc, lv, l0, g = f64(s["log_coeffs"]), f64(s["log_values"]), f64(s["log_h0"]), f64(s["grad_h"])
+        t0 = time.perf_counter(); oracle.psl_fwd(lc, lv, l0); t1 = time.perf_counter()
+        oracle.psl_bwd(lc, lv, l0, g); t2 = time.perf_counter()
+    return t2 - t0
+
+
+def _sample_rows(w, budget_rows):
+    return max(1, min(w.B, budget_rows.get(w.cid, w.B)))
+
+
+# rows of each workload the CPU leg processes (bounded: roughly 10-30 s on 16 cores)
+CPU_ROWS = {1: 128, 2: 16, 3: 8, 4: 4}
+
+
+def cpu_baseline(runners, budget_s=30.0, rows=None):
+    import oracle
+    from dataclasses import replace
+    rows = rows or CPU_ROWS
+    total_b, total_t, parts = 0, 0.0, []
+    for r in runners:
+        w = r.w
+        n = _sample_rows(w, rows)
+        s = _oracle_sample(w, n, r.inp)
+        ws = replace(w, B=n)
+        dt = _time_oracle(ws, s)
+        nb = op_bytes(ws, "fwd") + op_bytes(ws, "bwd")
+        total_b += nb
+        total_t += dt
+        parts.append(f"{w.op}_c{w.cid}: {n}/{w.B} batch rows ({dt:.2f} s)")
+    return {"value": round(total_b / total_t / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": "; ".join(parts) + "; float64 oracle, OpenMP over lanes",
+            "seconds": round(total_t, 2)}
+
+
+def run_reference(args):
+    """The float64 CPU oracle timed as the reference arm (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from dataclasses import replace
+    from scan_linear_recurrences_gb300 import inputs
+    oracle.build()
+    ids = [int(x) for x in args.workloads.split(",")]
+    ws = [inputs.WORKLOADS[i] for i in ids]
+    # each step processes this many batch rows per workload (bounded sample)
+    rows = {1: 32, 2: 4, 3: 2, 4: 1}
+    samples = []
+    for w in ws:
+        n = _sample_rows(w, rows)
+        wsub = replace(w, B=n)  # same recipe and seed, fewer batch rows
+        samples.append((wsub, wsub.make(device="cpu")))
+    for _ in range(args.warmup):
+        for wsub, s in samples:
+            _time_oracle(wsub, s)
+    times = []
+    for _ in range(args.steps):
+        times.append(sum(_time_oracle(wsub, s) for wsub, s in samples))
+    step_bytes = sum(op_bytes(wsub, "fwd") + op_bytes(wsub, "bwd") for wsub, _ in samples)
+    ms_step = statistics.mean(times) * 1e3
+    value = step_bytes / (ms_step * 1e-3) / 1e9
+    sample = "; ".join(f"{w.op}_c{w.cid}: {w.B} batch rows" for w, _ in samples)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": " + ".join(w.name for w in ws) + ", fwd+bwd each (row sample per step)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="libmgscan", choices=["libmgscan", "reference"])
+    ap.add_argument("--workloads", default=",".join(str(i) for i in WORKLOAD_IDS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+/*
+ * libmgscan: scan primitives of the minGRU family on one NVIDIA GB300 (sm_103a).
+ *
+ * The operations are the scan primitives named on the mingru-scans pages
+ * ("mingru-scans" home page, scan-op speedup table; "Run the benchmarks",
+ * Step 2 timing matrix): matrix_affine_scan, matrix_scan and
+ * parallel_scan_log, each with a forward and a backward pass.  The pages name
+ * them without formulas; the recurrences are the standard ones for those
+ * names and are stated at each entry point below.  parallel_scan_log is
+ * Heinsen's log-space scan (arXiv:2311.06281, cited in the home page's
+ * lineage paragraph).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers to contiguous, row-major fp32
+ *   buffers owned by the caller.  The library never allocates, frees, prints
+ *   or aborts.  Every pointer passed must be 16-byte aligned.
+ * - Time index: outputs hold t = 1..T at positions 0..T-1; the initial state
+ *   (h_0 or P_0 = I) is never part of an output.
+ * - Block layout for the matrix ops, with d = H*k channels split into H
+ *   independent k x k blocks per token:
+ *       A, dA, P, grad_P   [B][T][H][k][k]   (A[..][i][j] multiplies h[j]
+ *                                              into output row i)
+ *       b, h, grad_h, db   [B][T][H][k]
+ *       h0, dh0            [B][H][k]
+ *   parallel_scan_log layout (D diagonal channels):
+ *       log_coeffs, log_values, h, log_h, grad_h, d_log_coeffs,
+ *       d_log_values       [B][T][D];   log_h0, d_log_h0   [B][D]
+ * - Supported block sizes k: 4, 8, 16 for any H; 1 and 2 when H*k is a
+ *   multiple of 4.  Other k return MGS_ERR_UNSUPPORTED.
+ *   parallel_scan_log needs D to be a multiple of 4.
+ * - B, T, H, D must be >= 0; T == 0 or an empty batch is a successful no-op.
+ * - Outputs must not overlap any input or each other (MGS_ERR_INVALID_ARG).
+ * - Calls are asynchronous on `stream` (NULL = the legacy default stream).  A
+ *   returned MGS_OK means the work was validated and enqueued.  Faults found
+ *   on the device (a bounded wait that gave up) are recorded in a per-device
+ *   error word and reported by mgs_check().
+ * - Workspace: entry points that take `workspace` need a caller-allocated
+ *   device buffer of at least mgs_workspace_size(op, ...) bytes, 256-byte
+ *   aligned (MGS_ERR_WORKSPACE otherwise).  The size depends only on the op and
+ *   shape.  When the size is 0, workspace may be NULL.  Calls that share one
+ *   workspace must be ordered on the same stream.
+ */
+#ifndef MGSCAN_H
+#define MGSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mgs_status {
+    MGS_OK = 0,
+    MGS_ERR_INVALID_ARG = 1, /* null required pointer, negative size, overlap, overflow */
+    MGS_ERR_UNSUPPORTED = 2, /* k or D outside the supported set, misaligned pointer   */
+    MGS_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned            */
+    MGS_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed           */
+    MGS_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see mgs_check)    */
+} mgs_status;
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st *mgs_stream_t;
+
+/* Operation ids for mgs_workspace_size. */
+enum {
+    MGS_OP_MATRIX_AFFINE_SCAN_FWD = 1,
+    MGS_OP_MATRIX_AFFINE_SCAN_BWD = 2,
+    MGS_OP_MATRIX_SCAN_FWD = 3,
+    MGS_OP_MATRIX_SCAN_BWD = 4,
+    MGS_OP_PARALLEL_SCAN_LOG_FWD = 5,
+    MGS_OP_PARALLEL_SCAN_LOG_BWD = 6
+};
+
+/* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
+ * matrix ops and D for parallel_scan_log; k is ignored for the latter).
+ * Returns 0 when no workspace is needed, and also for invalid shapes (the
+ * entry point then reports the error). */
+size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k);
+
+/* matrix_affine_scan, forward ("mingru-scans" home page, scan-op table,
+ * matrix_affine_scan row; the recurrence behind RotationMinGRU and
+ * GivensMinGRU):
+ *     h_t = A_t h_{t-1} + b_t,   t = 1..T,   per (batch, head) lane,
+ * with h_0 = h0, or zeros when h0 is NULL.
+ * In: A [B][T][H][k][k], b [B][T][H][k], h0 [B][H][k] (nullable).
+ * Out: h [B][T][H][k]. */
+mgs_status mgs_matrix_affine_scan_fwd(const float *A, const float *b, const float *h0, float *h,
+                                      int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                      size_t workspace_bytes, mgs_stream_t stream);
+
+/* matrix_affine_scan, backward: gradients of L = sum_t <grad_h_t, h_t> through
+ * the forward above.  With lambda_t = dL/dh_t,
+ *     lambda_T = grad_h_T,   lambda_t = grad_h_t + A_{t+1}^T lambda_{t+1},
+ *     db_t = lambda_t,   dA_t = lambda_t h_{t-1}^T,   dh0 = A_1^T lambda_1.
+ * In: A, h0 (nullable: zero initial state), h = the forward output (saved),
+ *     grad_h.  b is not needed.
+ * Out: dA [B][T][H][k][k], db [B][T][H][k], dh0 [B][H][k] (nullable: not
+ *     written). */
+mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const float *h,
+                                      const float *grad_h, float *dA, float *db, float *dh0,
+                                      int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                      size_t workspace_bytes, mgs_stream_t stream);
+
+/* matrix_scan, forward ("mingru-scans" home page, scan-op table, matrix_scan
+ * row): prefix products
+ *     P_t = A_t P_{t-1},   P_0 = I,   per (batch, head) lane.
+ * In: A [B][T][H][k][k].  Out: P [B][T][H][k][k].
+ * Long sequences with few lanes are split into time chunks that exchange
+ * carries through the workspace (see mgs_workspace_size). */
+mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,
+                               void *workspace, size_t workspace_bytes, mgs_stream_t stream);
+
+/* matrix_scan, backward: gradient of L = sum_t <grad_P_t, P_t>_F.  With
+ * Lambda_t = dL/dP_t,
+ *     Lambda_T = grad_P_T,   Lambda_t = grad_P_t + A_{t+1}^T Lambda_{t+1},
+ *     dA_t = Lambda_t P_{t-1}^T   (P_0 = I).
+ * In: A, P = the forward output (saved), grad_P.  Out: dA. */
+mgs_status mgs_matrix_scan_bwd(const float *A, const float *P, const float *grad_P, float *dA,
+                               int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                               size_t workspace_bytes, mgs_stream_t stream);
+
+/* parallel_scan_log, forward ("mingru-scans" home page, scan-op table,
+ * parallel_scan_log row; Heinsen's log-space scan behind MinGRU and
+ * SignedMinGRU), per (batch, channel) lane:
+ *     log h_t = log(exp(log_coeffs_t + log h_{t-1}) + exp(log_values_t)),
+ *     log h_0 = log_h0 (NULL: h_0 = 0),   h_t = exp(log h_t),
+ * i.e. h_t = exp(a*_t + logcumsumexp_{s<=t}(log_values_s - a*_s)) with
+ * a*_t = sum_{s<=t} log_coeffs_s, evaluated as a max-shifted log-sum-exp
+ * recurrence so no cumulative sum loses precision.
+ * In: log_coeffs, log_values [B][T][D], log_h0 [B][D] (nullable).
+ * Out: h [B][T][D]; log_h [B][T][D] (nullable: not written). */
+mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_values,
+                                     const float *log_h0, float *h, float *log_h, int64_t B,
+                                     int64_t T, int64_t D, void *workspace, size_t workspace_bytes,
+                                     mgs_stream_t stream);
+
+/* parallel_scan_log, backward: gradients of L = sum_t grad_h_t * h_t.  With
+ * a_t = exp(log_coeffs_t) and lambda_t = dL/dh_t,
+ *     lambda_T = grad_h_T,   lambda_t = grad_h_t + a_{t+1} lambda_{t+1},
+ *     d_log_values_t = lambda_t exp(log_values_t),
+ *     d_log_coeffs_t = lambda_t a_t h_{t-1},
+ *     d_log_h0 = lambda_1 a_1 h_0.
+ * In: log_coeffs, log_values, log_h0 (nullable: h_0 = 0), h = the forward
+ *     output (saved; must not be NULL), grad_h.
+ * Out: d_log_coeffs, d_log_values [B][T][D]; d_log_h0 [B][D] (nullable; must
+ *     be NULL when log_h0 is NULL). */
+mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_values,
+                                     const float *log_h0, const float *h, const float *grad_h,
+                                     float *d_log_coeffs, float *d_log_values, float *d_log_h0,
+                                     int64_t B, int64_t T, int64_t D, void *workspace,
+                                     size_t workspace_bytes, mgs_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns MGS_ERR_TIMEOUT if a kernel's bounded wait gave up since the
+ * last check, MGS_ERR_CUDA if the synchronisation failed, else MGS_OK. */
+mgs_status mgs_check(mgs_stream_t stream);
+
+/* Sets the limit, in nanoseconds, after which a device-side wait gives up
+ * (default 1e9, i.e. one second).  Applies to launches made after the call on
+ * any device.  Values below 1000 are raised to 1000. */
+void mgs_set_wait_timeout_ns(uint64_t ns);
+
+/* Diagnostic: launches one warp that waits, with the library's bounded wait,
+ * on the device flag `*flag` (a device int) until it becomes nonzero.  When
+ * nothing sets the flag, the wait gives up after the timeout and the error
+ * word records it; mgs_check() then returns MGS_ERR_TIMEOUT.  Used to test
+ * failure detection without faulting or hanging the GPU. */
+mgs_status mgs_debug_wait_flag(const int *flag, mgs_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *mgs_status_string(mgs_status status);
+
+/* Library version as an integer, major*10000 + minor*100 + patch. */
+int mgs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MGSCAN_H */

@@ -1,0 +1,172 @@
+"""Tensor-level API over the C ABI: shape checks, output/workspace allocation
+with torch (device memory is torch's job here), then one libmgscan call.
+
+Also provides ``torch.autograd.Function`` wrappers whose forward and backward
+are the library's fwd/bwd entry points, for use inside models.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as _b
+
+
+def _check(t, name, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (the library runs only on the GPU)")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be float32")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def workspace(op, B, T, H_or_D, k, device):
+    """A workspace tensor of the size the op needs (None when it needs none)."""
+    n = _b.mgs_workspace_size(op, B, T, H_or_D, k)
+    if n == 0:
+        return None, 0
+    return torch.empty(n, dtype=torch.uint8, device=device), n
+
+
+# ---------------------------------------------------------------- matrix_affine_scan
+def matrix_affine_scan_fwd(A, b, h0=None, out=None, stream=None):
+    """h_t = A_t h_{t-1} + b_t.  A [B,T,H,k,k], b [B,T,H,k], h0 [B,H,k] or None."""
+    B, T, H, k = b.shape
+    _check(A, "A", (B, T, H, k, k)); _check(b, "b")
+    if h0 is not None:
+        _check(h0, "h0", (B, H, k))
+    h = out if out is not None else torch.empty_like(b)
+    ws, nws = workspace(_b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, B, T, H, k, b.device)
+    _b.mgs_matrix_affine_scan_fwd(A, b, h0, h, B, T, H, k, ws, nws, stream)
+    return h
+
+
+def matrix_affine_scan_bwd(A, h0, h, grad_h, need_dh0=True, stream=None):
+    """Returns (dA, db, dh0) for L = sum <grad_h, h>; dh0 is None unless requested."""
+    B, T, H, k = h.shape
+    _check(A, "A", (B, T, H, k, k)); _check(h, "h"); _check(grad_h, "grad_h", (B, T, H, k))
+    if h0 is not None:
+        _check(h0, "h0", (B, H, k))
+    dA = torch.empty_like(A)
+    db = torch.empty_like(h)
+    dh0 = torch.empty((B, H, k), dtype=torch.float32, device=h.device) if need_dh0 else None
+    ws, nws = workspace(_b.MGS_OP_MATRIX_AFFINE_SCAN_BWD, B, T, H, k, h.device)
+    _b.mgs_matrix_affine_scan_bwd(A, h0, h, grad_h, dA, db, dh0, B, T, H, k, ws, nws, stream)
+    return dA, db, dh0
+
+
+# ---------------------------------------------------------------- matrix_scan
+def matrix_scan_fwd(A, out=None, stream=None):
+    """P_t = A_t P_{t-1}, P_0 = I.  A [B,T,H,k,k]."""
+    B, T, H, k, _ = A.shape
+    _check(A, "A", (B, T, H, k, k))
+    P = out if out is not None else torch.empty_like(A)
+    ws, nws = workspace(_b.MGS_OP_MATRIX_SCAN_FWD, B, T, H, k, A.device)
+    _b.mgs_matrix_scan_fwd(A, P, B, T, H, k, ws, nws, stream)
+    return P
+
+
+def matrix_scan_bwd(A, P, grad_P, stream=None):
+    B, T, H, k, _ = A.shape
+    _check(A, "A", (B, T, H, k, k)); _check(P, "P", A.shape); _check(grad_P, "grad_P", A.shape)
+    dA = torch.empty_like(A)
+    ws, nws = workspace(_b.MGS_OP_MATRIX_SCAN_BWD, B, T, H, k, A.device)
+    _b.mgs_matrix_scan_bwd(A, P, grad_P, dA, B, T, H, k, ws, nws, stream)
+    return dA
+
+
+# ---------------------------------------------------------------- parallel_scan_log
+def parallel_scan_log_fwd(log_coeffs, log_values, log_h0=None, want_log=False, stream=None):
+    """Heinsen log-space scan; returns h (and log h when want_log)."""
+    B, T, D = log_coeffs.shape
+    _check(log_coeffs, "log_coeffs"); _check(log_values, "log_values", (B, T, D))
+    if log_h0 is not None:
+        _check(log_h0, "log_h0", (B, D))
+    h = torch.empty_like(log_coeffs)
+    lh = torch.empty_like(log_coeffs) if want_log else None
+    _b.mgs_parallel_scan_log_fwd(log_coeffs, log_values, log_h0, h, lh, B, T, D, None, 0, stream)
+    return (h, lh) if want_log else h
+
+
+def parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, stream=None):
+    """Returns (d_log_coeffs, d_log_values, d_log_h0 or None)."""
+    B, T, D = log_coeffs.shape
+    for t, n in ((log_coeffs, "log_coeffs"), (log_values, "log_values"), (h, "h"), (grad_h, "grad_h")):
+        _check(t, n, (B, T, D))
+    if log_h0 is not None:
+        _check(log_h0, "log_h0", (B, D))
+    dlc = torch.empty_like(log_coeffs)
+    dlv = torch.empty_like(log_values)
+    dl0 = torch.empty_like(log_h0) if log_h0 is not None else None
+    _b.mgs_parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, dlc, dlv, dl0, B, T, D,
+                                 None, 0, stream)
+    return dlc, dlv, dl0
+
+
+# ---------------------------------------------------------------- autograd wrappers
+class MatrixAffineScan(torch.autograd.Function):
+    """h = matrix_affine_scan(A, b, h0) with the library's fused backward."""
+
+    @staticmethod
+    def forward(ctx, A, b, h0=None):
+        A, b = A.contiguous(), b.contiguous()
+        h0c = h0.contiguous() if h0 is not None else None
+        h = matrix_affine_scan_fwd(A, b, h0c)
+        ctx.save_for_backward(A, h0c if h0c is not None else torch.empty(0, device=b.device), h)
+        ctx.has_h0 = h0 is not None
+        return h
+
+    @staticmethod
+    def backward(ctx, grad_h):
+        A, h0, h = ctx.saved_tensors
+        h0 = h0 if ctx.has_h0 else None
+        dA, db, dh0 = matrix_affine_scan_bwd(A, h0, h, grad_h.contiguous(), need_dh0=ctx.has_h0)
+        return dA, db, dh0
+
+
+class MatrixScan(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, A):
+        A = A.contiguous()
+        P = matrix_scan_fwd(A)
+        ctx.save_for_backward(A, P)
+        return P
+
+    @staticmethod
+    def backward(ctx, grad_P):
+        A, P = ctx.saved_tensors
+        return matrix_scan_bwd(A, P, grad_P.contiguous())
+
+
+class ParallelScanLog(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, log_coeffs, log_values, log_h0=None):
+        lc, lv = log_coeffs.contiguous(), log_values.contiguous()
+        l0 = log_h0.contiguous() if log_h0 is not None else None
+        h = parallel_scan_log_fwd(lc, lv, l0)
+        ctx.save_for_backward(lc, lv, l0 if l0 is not None else torch.empty(0, device=lc.device), h)
+        ctx.has_h0 = log_h0 is not None
+        return h
+
+    @staticmethod
+    def backward(ctx, grad_h):
+        lc, lv, l0, h = ctx.saved_tensors
+        l0 = l0 if ctx.has_h0 else None
+        dlc, dlv, dl0 = parallel_scan_log_bwd(lc, lv, l0, h, grad_h.contiguous())
+        return dlc, dlv, dl0
+
+
+def matrix_affine_scan(A, b, h0=None):
+    return MatrixAffineScan.apply(A, b, h0)
+
+
+def matrix_scan(A):
+    return MatrixScan.apply(A)
+
+
+def parallel_scan_log(log_coeffs, log_values, log_h0=None):
+    return ParallelScanLog.apply(log_coeffs, log_values, log_h0)

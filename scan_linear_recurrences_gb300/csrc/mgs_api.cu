@@ -1,0 +1,342 @@
+// C ABI of libmgscan (declared in include/mgscan.h): argument validation,
+// the per-device error word, and dispatch to the kernel launchers.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "../../include/mgscan.h"
+#include "mgs_launch.h"
+
+#define MGS_VERSION_INT 100  // 0.1.0
+
+namespace {
+
+// Error word written by kernels whose bounded waits give up (one per device:
+// a __device__ variable exists once in every device context that loads the
+// library).  Host code never dereferences its name; it asks the runtime for
+// the device address, once per device.
+__device__ unsigned g_mgs_error_word = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_addr[kMaxDevices] = {};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+mgs_status current_ctl(mgs::DevCtl *ctl) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MGS_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_err_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_mgs_error_word) != cudaSuccess) return MGS_ERR_CUDA;
+        g_err_addr[dev] = static_cast<unsigned *>(p);
+    }
+    ctl->err = g_err_addr[dev];
+    ctl->timeout_ns = g_timeout_ns.load();
+    return MGS_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// n = a*b*c*... with overflow detection (all factors >= 0).
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    if (a == 0 || b == 0) { *out = 0; return true; }
+    if (a > INT64_MAX / b) return false;
+    *out = a * b;
+    return true;
+}
+
+struct Range {
+    uintptr_t lo, hi;
+};
+Range rng(const void *p, int64_t count) {
+    uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return {a, a + uintptr_t(count) * sizeof(float)};
+}
+bool overlap(Range x, Range y) { return x.lo < y.hi && y.lo < x.hi; }
+
+// Every output must be disjoint from every input and from the other outputs.
+bool disjoint(std::initializer_list<std::pair<const void *, int64_t>> outs,
+              std::initializer_list<std::pair<const void *, int64_t>> ins) {
+    for (auto o = outs.begin(); o != outs.end(); ++o) {
+        if (o->first == nullptr || o->second == 0) continue;
+        Range ro = rng(o->first, o->second);
+        for (auto &i : ins)
+            if (i.first != nullptr && i.second != 0 && overlap(ro, rng(i.first, i.second))) return false;
+        for (auto o2 = o + 1; o2 != outs.end(); ++o2)
+            if (o2->first != nullptr && o2->second != 0 && overlap(ro, rng(o2->first, o2->second)))
+                return false;
+    }
+    return true;
+}
+
+bool k_supported(int k, int64_t H) {
+    if (k == 4 || k == 8 || k == 16) return true;
+    if (k == 1 || k == 2) return (H * k) % 4 == 0;
+    return false;
+}
+
+struct BlockSizes {
+    int64_t mat, vec, init;  // element counts: [B,T,H,k,k], [B,T,H,k], [B,H,k]
+};
+
+// Validates (B, T, H, k) for the matrix ops and computes element counts.
+mgs_status block_sizes(int64_t B, int64_t T, int64_t H, int k, BlockSizes *s) {
+    if (B < 0 || T < 0 || H < 0 || k <= 0) return MGS_ERR_INVALID_ARG;
+    if (!k_supported(k, H)) return MGS_ERR_UNSUPPORTED;
+    int64_t bth, bh;
+    if (!mul_ok(B, T, &bth) || !mul_ok(bth, H, &bth) || !mul_ok(B, H, &bh)) return MGS_ERR_INVALID_ARG;
+    if (!mul_ok(bth, int64_t(k) * k, &s->mat) || !mul_ok(bth, k, &s->vec) || !mul_ok(bh, k, &s->init))
+        return MGS_ERR_INVALID_ARG;
+    if (s->mat > (INT64_MAX / 8)) return MGS_ERR_INVALID_ARG;
+    return MGS_OK;
+}
+
+mgs_status check_ptrs(std::initializer_list<const void *> required,
+                      std::initializer_list<const void *> optional) {
+    for (const void *p : required)
+        if (p == nullptr) return MGS_ERR_INVALID_ARG;
+    for (const void *p : required)
+        if (!aligned16(p)) return MGS_ERR_UNSUPPORTED;
+    for (const void *p : optional)
+        if (p != nullptr && !aligned16(p)) return MGS_ERR_UNSUPPORTED;
+    return MGS_OK;
+}
+
+mgs_status check_ws(size_t need, const void *ws, size_t ws_bytes) {
+    if (need == 0) return MGS_OK;
+    if (ws == nullptr || ws_bytes < need) return MGS_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MGS_ERR_WORKSPACE;
+    return MGS_OK;
+}
+
+mgs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGS_OK : MGS_ERR_CUDA; }
+
+}  // namespace
+
+namespace mgs {
+
+cudaError_t ensure_smem_attr(const void *fn, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<const void *, int>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(fn, dev);
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes > 48 * 1024 ? 227 * 1024 : 48 * 1024);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
+
+}  // namespace mgs
+
+extern "C" {
+
+size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
+    BlockSizes s;
+    switch (op) {
+        case MGS_OP_MATRIX_SCAN_FWD:
+        case MGS_OP_MATRIX_SCAN_BWD:
+            if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
+            return mgs::ms_workspace_bytes(B, T, H_or_D, k, op == MGS_OP_MATRIX_SCAN_BWD);
+        default:
+            return 0;
+    }
+}
+
+mgs_status mgs_matrix_affine_scan_fwd(const float *A, const float *b, const float *h0, float *h,
+                                      int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                      size_t workspace_bytes, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.vec == 0) return MGS_OK;
+    if ((st = check_ptrs({A, b, h}, {h0})) != MGS_OK) return st;
+    if (!disjoint({{h, s.vec}}, {{A, s.mat}, {b, s.vec}, {h0, h0 ? s.init : 0}})) return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_mas_fwd(k, A, b, h0, h, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const float *h,
+                                      const float *grad_h, float *dA, float *db, float *dh0,
+                                      int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                      size_t workspace_bytes, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.init == 0) return MGS_OK;
+    if (s.vec == 0) {
+        // T == 0: lambda is empty, the initial-state gradient is zero
+        if (dh0 == nullptr) return MGS_OK;
+        if ((st = check_ptrs({dh0}, {})) != MGS_OK) return st;
+        return from_cuda(cudaMemsetAsync(dh0, 0, size_t(s.init) * sizeof(float),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if ((st = check_ptrs({A, h, grad_h, dA, db}, {h0, dh0})) != MGS_OK) return st;
+    if (!disjoint({{dA, s.mat}, {db, s.vec}, {dh0, dh0 ? s.init : 0}},
+                  {{A, s.mat}, {h0, h0 ? s.init : 0}, {h, s.vec}, {grad_h, s.vec}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_mas_bwd(k, A, h0, h, grad_h, dA, db, dh0, B, T, H, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,
+                               void *workspace, size_t workspace_bytes, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.mat == 0) return MGS_OK;
+    if ((st = check_ptrs({A, P}, {})) != MGS_OK) return st;
+    if (!disjoint({{P, s.mat}}, {{A, s.mat}})) return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(mgs::ms_workspace_bytes(B, T, H, k, false), workspace, workspace_bytes)) != MGS_OK)
+        return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_ms_fwd(k, A, P, B, T, H, workspace, workspace_bytes, ctl,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_matrix_scan_bwd(const float *A, const float *P, const float *grad_P, float *dA,
+                               int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                               size_t workspace_bytes, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.mat == 0) return MGS_OK;
+    if ((st = check_ptrs({A, P, grad_P, dA}, {})) != MGS_OK) return st;
+    if (!disjoint({{dA, s.mat}}, {{A, s.mat}, {P, s.mat}, {grad_P, s.mat}})) return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(mgs::ms_workspace_bytes(B, T, H, k, true), workspace, workspace_bytes)) != MGS_OK)
+        return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_ms_bwd(k, A, P, grad_P, dA, B, T, H, workspace, workspace_bytes, ctl,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static mgs_status psl_sizes(int64_t B, int64_t T, int64_t D, int64_t *n, int64_t *n0) {
+    if (B < 0 || T < 0 || D < 0) return MGS_ERR_INVALID_ARG;
+    if (D % 4 != 0) return MGS_ERR_UNSUPPORTED;
+    int64_t bt;
+    if (!mul_ok(B, T, &bt) || !mul_ok(bt, D, n) || !mul_ok(B, D, n0)) return MGS_ERR_INVALID_ARG;
+    if (*n > INT64_MAX / 8) return MGS_ERR_INVALID_ARG;
+    return MGS_OK;
+}
+
+mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_values,
+                                     const float *log_h0, float *h, float *log_h, int64_t B,
+                                     int64_t T, int64_t D, void *workspace, size_t workspace_bytes,
+                                     mgs_stream_t stream) {
+    int64_t n, n0;
+    mgs_status st = psl_sizes(B, T, D, &n, &n0);
+    if (st != MGS_OK) return st;
+    if (n == 0) return MGS_OK;
+    if ((st = check_ptrs({log_coeffs, log_values, h}, {log_h0, log_h})) != MGS_OK) return st;
+    if (!disjoint({{h, n}, {log_h, log_h ? n : 0}},
+                  {{log_coeffs, n}, {log_values, n}, {log_h0, log_h0 ? n0 : 0}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_psl_fwd(log_coeffs, log_values, log_h0, h, log_h, B, T, D, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_values,
+                                     const float *log_h0, const float *h, const float *grad_h,
+                                     float *d_log_coeffs, float *d_log_values, float *d_log_h0,
+                                     int64_t B, int64_t T, int64_t D, void *workspace,
+                                     size_t workspace_bytes, mgs_stream_t stream) {
+    int64_t n, n0;
+    mgs_status st = psl_sizes(B, T, D, &n, &n0);
+    if (st != MGS_OK) return st;
+    if (d_log_h0 != nullptr && log_h0 == nullptr) return MGS_ERR_INVALID_ARG;
+    if (n0 == 0) return MGS_OK;
+    if (n == 0) {
+        if (d_log_h0 == nullptr) return MGS_OK;
+        if ((st = check_ptrs({d_log_h0}, {})) != MGS_OK) return st;
+        return from_cuda(cudaMemsetAsync(d_log_h0, 0, size_t(n0) * sizeof(float),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if ((st = check_ptrs({log_coeffs, log_values, h, grad_h, d_log_coeffs, d_log_values},
+                         {log_h0, d_log_h0})) != MGS_OK)
+        return st;
+    if (!disjoint({{d_log_coeffs, n}, {d_log_values, n}, {d_log_h0, d_log_h0 ? n0 : 0}},
+                  {{log_coeffs, n}, {log_values, n}, {log_h0, log_h0 ? n0 : 0}, {h, n}, {grad_h, n}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_psl_bwd(log_coeffs, log_values, log_h0, h, grad_h, d_log_coeffs,
+                                         d_log_values, d_log_h0, B, T, D, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_check(mgs_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MGS_ERR_CUDA;
+    mgs::DevCtl ctl;
+    mgs_status st = current_ctl(&ctl);
+    if (st != MGS_OK) return st;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, ctl.err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MGS_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemset(ctl.err, 0, sizeof(unsigned)) != cudaSuccess) return MGS_ERR_CUDA;
+        return MGS_ERR_TIMEOUT;
+    }
+    return MGS_OK;
+}
+
+void mgs_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns < 1000 ? 1000 : ns); }
+
+const char *mgs_status_string(mgs_status status) {
+    switch (status) {
+        case MGS_OK: return "MGS_OK";
+        case MGS_ERR_INVALID_ARG: return "MGS_ERR_INVALID_ARG";
+        case MGS_ERR_UNSUPPORTED: return "MGS_ERR_UNSUPPORTED";
+        case MGS_ERR_WORKSPACE: return "MGS_ERR_WORKSPACE";
+        case MGS_ERR_CUDA: return "MGS_ERR_CUDA";
+        case MGS_ERR_TIMEOUT: return "MGS_ERR_TIMEOUT";
+        default: return "MGS_ERR_UNKNOWN";
+    }
+}
+
+int mgs_version(void) { return MGS_VERSION_INT; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- diagnostic wait
+namespace {
+__global__ void debug_wait_flag_kernel(const int *flag, mgs::DevCtl ctl) {
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = mgs::global_ns();
+    while (true) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v != 0) return;
+        if (mgs::global_ns() - t0 > ctl.timeout_ns) {
+            mgs::record_error(ctl, mgs::ERR_FLAG_TIMEOUT);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+}  // namespace
+
+extern "C" mgs_status mgs_debug_wait_flag(const int *flag, mgs_stream_t stream) {
+    if (flag == nullptr) return MGS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(flag) & 3u) != 0) return MGS_ERR_UNSUPPORTED;
+    mgs::DevCtl ctl;
+    mgs_status st = current_ctl(&ctl);
+    if (st != MGS_OK) return st;
+    debug_wait_flag_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(flag, ctl);
+    return from_cuda(cudaGetLastError());
+}

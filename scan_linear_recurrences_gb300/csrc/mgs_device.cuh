@@ -1,0 +1,158 @@
+// Device helpers shared by the scan kernels: mbarrier-tracked 1-D bulk copies
+// (the Hopper/Blackwell TMA bulk path, no tensor map needed), bounded waits
+// that record an error instead of hanging, and warp-level utilities.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mgs {
+
+// Bits of the per-device error word.
+enum : unsigned {
+    ERR_MBAR_TIMEOUT = 1u,     // a bulk-copy barrier wait gave up
+    ERR_FLAG_TIMEOUT = 2u,     // a look-back / flag wait gave up
+    ERR_DRAIN_TIMEOUT = 4u,    // waiting for in-flight copies after an error gave up
+};
+
+// Launch-wide parameters every kernel receives.
+struct DevCtl {
+    unsigned *err;        // per-device error word (device address)
+    uint64_t timeout_ns;  // bounded-wait limit
+};
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_error(const DevCtl &c, unsigned bits) {
+    atomicOr(c.err, bits);
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete; gives up after the launch's
+// timeout and returns false (the caller records the error and drains).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// L2 eviction hint for data streamed once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` as tx bytes.
+// Both addresses must be 16-byte aligned and `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Streaming (evict-first) vector stores for outputs written once.
+__device__ __forceinline__ void st_cs(float *p, float v) { __stcs(p, v); }
+__device__ __forceinline__ void st_cs4(float *p, float4 v) { __stcs(reinterpret_cast<float4 *>(p), v); }
+
+// After a failed wait: waits (bounded) for every stage that still has copies in
+// flight, so the warp never exits with TMA writes pending into its shared memory.
+static __device__ __noinline__ void drain_ring(uint64_t *bar, int ns, uint32_t inflight, uint32_t phase,
+                                        DevCtl c, int lane) {
+    bool ok = true;
+    for (int s = 0; s < ns; ++s)
+        if (inflight & (1u << s))
+            if (!mbar_wait_bounded(&bar[s], (phase >> s) & 1u, c.timeout_ns)) ok = false;
+    if (!ok && lane == 0) record_error(c, ERR_DRAIN_TIMEOUT);
+    __syncwarp();
+}
+
+// Per-warp ring of NS stages with one full-barrier each.  Lane 0 produces (bulk
+// copies), the whole warp consumes.  After a failed wait, drain() waits (again
+// bounded) for every stage that still has copies in flight so the warp never
+// exits with TMA writes pending into its shared memory.
+template <int NS>
+struct WarpRing {
+    uint64_t *bar;         // NS barriers in shared memory
+    uint32_t inflight;     // bit s set: stage s has an armed, unconsumed phase
+    uint32_t phase;        // bit s: parity expected next on stage s
+
+    __device__ __forceinline__ void init(uint64_t *bars, int lane) {
+        bar = bars;
+        inflight = 0;
+        phase = 0;
+        if (lane == 0) {
+            for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+            fence_barrier_init();
+        }
+        __syncwarp();
+    }
+    // Marks stage s armed (called by all lanes, uniformly, after lane 0 issued).
+    __device__ __forceinline__ void armed(int s) { inflight |= (1u << s); }
+
+    // All lanes wait for stage s; returns false on timeout.
+    __device__ __forceinline__ bool wait(int s, const DevCtl &c) {
+        bool ok = mbar_wait_bounded(&bar[s], (phase >> s) & 1u, c.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            phase ^= (1u << s);
+            inflight &= ~(1u << s);
+        }
+        return ok;
+    }
+
+    __device__ __forceinline__ void drain(const DevCtl &c, int lane) {
+        drain_ring(bar, NS, inflight, phase, c, lane);
+    }
+};
+
+}  // namespace mgs

@@ -1,0 +1,39 @@
+// Internal launcher interface between the C ABI (mgs_api.cu) and the kernel
+// translation units.  Not installed; the public interface is include/mgscan.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mgs_device.cuh"
+
+namespace mgs {
+
+// matrix_affine_scan
+cudaError_t launch_mas_fwd(int K, const float *A, const float *b, const float *h0, float *h,
+                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *h,
+                           const float *gh, float *dA, float *db, float *dh0, int64_t B,
+                           int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+
+// matrix_scan
+size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);
+cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,
+                          void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
+cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G, float *dA,
+                          int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes,
+                          const DevCtl &ctl, cudaStream_t s);
+
+// parallel_scan_log
+cudaError_t launch_psl_fwd(const float *lc, const float *lv, const float *lh0, float *h,
+                           float *logh, int64_t B, int64_t T, int64_t D, const DevCtl &ctl,
+                           cudaStream_t s);
+cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, const float *h,
+                           const float *gh, float *dlc, float *dlv, float *dlh0, int64_t B,
+                           int64_t T, int64_t D, const DevCtl &ctl, cudaStream_t s);
+
+// Sets the dynamic shared-memory limit of `fn` once per device.
+cudaError_t ensure_smem_attr(const void *fn, int bytes);
+
+}  // namespace mgs

@@ -1,0 +1,32 @@
+"""Comparison helpers for the GPU parity tests.
+
+Tolerance (fp32 kernels against the float64 oracle, per output tensor):
+    relative L2  ||y - y_ref||_2 / ||y_ref||_2  <= 1e-5
+    max abs      max |y - y_ref|                <= 1e-4 * sqrt(T)
+"""
+import math
+
+import numpy as np
+
+REL_L2 = 1e-5
+ABS_PER_SQRT_T = 1e-4
+
+
+def errors(gpu, ref):
+    g = gpu.detach().double().cpu().numpy() if hasattr(gpu, "detach") else np.asarray(gpu, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    if r.size == 0:
+        return 0.0, 0.0
+    d = g - r
+    nref = np.linalg.norm(r.ravel())
+    rel = np.linalg.norm(d.ravel()) / nref if nref > 0 else np.linalg.norm(d.ravel())
+    return float(rel), float(np.abs(d).max())
+
+
+def assert_close(name, gpu, ref, T, rel_tol=REL_L2, abs_tol=None):
+    rel, mx = errors(gpu, ref)
+    lim = abs_tol if abs_tol is not None else ABS_PER_SQRT_T * math.sqrt(max(T, 1))
+    assert np.isfinite(rel) and rel <= rel_tol and mx <= lim, \
+        f"{name}: rel_l2={rel:.3e} (<= {rel_tol:.1e}), max_abs={mx:.3e} (<= {lim:.2e})"
+    return rel, mx

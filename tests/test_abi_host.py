@@ -1,0 +1,99 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/mgscan.h declares, and rejects bad arguments with the documented status
+before touching the device (fake, never-dereferenced addresses)."""
+import os
+import re
+
+import pytest
+
+from scan_linear_recurrences_gb300 import _binding as b
+from scan_linear_recurrences_gb300.build import LIB, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mgscan.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return b.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mgs_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in mgscan.h but not exported by {LIB}"
+    assert set(names) == set(b.exported_symbols())
+
+
+def test_version_and_status_strings(L):
+    assert b.mgs_version() == 100
+    for code, name in b.STATUS_NAMES.items():
+        assert b.mgs_status_string(code) == name
+
+
+FAKE = 1 << 40  # aligned, never dereferenced: every case below fails validation first
+
+
+def _st(fn, *args):
+    try:
+        fn(*args, stream=0)
+        return b.MGS_OK
+    except b.MGSError as e:
+        return e.status
+
+
+def test_mas_validation(L):
+    A, bb, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    assert _st(b.mgs_matrix_affine_scan_fwd, None, bb, None, h, 2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_matrix_affine_scan_fwd, A, bb, None, h, -1, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_matrix_affine_scan_fwd, A, bb, None, h, 2, 8, 4, 3) == b.MGS_ERR_UNSUPPORTED
+    assert _st(b.mgs_matrix_affine_scan_fwd, A, bb, None, h, 2, 8, 3, 1) == b.MGS_ERR_UNSUPPORTED  # H*k % 4
+    assert _st(b.mgs_matrix_affine_scan_fwd, A + 4, bb, None, h, 2, 8, 4, 8) == b.MGS_ERR_UNSUPPORTED
+    # output overlapping an input
+    assert _st(b.mgs_matrix_affine_scan_fwd, A, bb, None, bb + 64, 2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    # empty problems are successful no-ops, even with null pointers
+    assert _st(b.mgs_matrix_affine_scan_fwd, None, None, None, None, 0, 8, 4, 8) == b.MGS_OK
+    assert _st(b.mgs_matrix_affine_scan_fwd, None, None, None, None, 2, 8, 0, 8) == b.MGS_OK
+    # overflow of B*T*H*k*k
+    assert _st(b.mgs_matrix_affine_scan_fwd, A, bb, None, h, 1 << 40, 1 << 20, 4, 8) == b.MGS_ERR_INVALID_ARG
+    # backward: dA overlapping h
+    assert _st(b.mgs_matrix_affine_scan_bwd, A, None, h, FAKE + (3 << 30), h, FAKE + (4 << 30), None,
+               2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_matrix_affine_scan_bwd, A, None, None, FAKE + (3 << 30), FAKE + (5 << 30),
+               FAKE + (4 << 30), None, 2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+
+
+def test_ms_and_psl_validation(L):
+    A, P = FAKE, FAKE + (1 << 30)
+    assert _st(b.mgs_matrix_scan_fwd, A, A, 2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_matrix_scan_fwd, A, P, 2, 8, 4, 5) == b.MGS_ERR_UNSUPPORTED
+    assert _st(b.mgs_matrix_scan_bwd, A, P, None, FAKE + (2 << 30), 2, 8, 4, 8) == b.MGS_ERR_INVALID_ARG
+    lc, lv, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    assert _st(b.mgs_parallel_scan_log_fwd, lc, lv, None, h, None, 2, 8, 6) == b.MGS_ERR_UNSUPPORTED  # D % 4
+    assert _st(b.mgs_parallel_scan_log_fwd, lc, lv, None, lv, None, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_parallel_scan_log_fwd, lc, lv, None, h, h, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+    # d_log_h0 without log_h0 has no meaning
+    assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, h, FAKE + (3 << 30), FAKE + (4 << 30),
+               FAKE + (5 << 30), FAKE + (6 << 30), 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, None, FAKE + (3 << 30), FAKE + (4 << 30),
+               FAKE + (5 << 30), None, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+
+
+def test_workspace_size_queries(L):
+    for op in range(1, 7):
+        assert b.mgs_workspace_size(op, 2, 16, 8, 8) >= 0
+    assert b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, -1, 16, 8, 8) == 0
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "nope.so"))
+    monkeypatch.setattr(b, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        b.lib()

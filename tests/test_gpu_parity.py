@@ -1,0 +1,202 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the float64
+oracle on the same seeded float32 inputs, at small sizes that span several
+ring stages and ragged tails, at the benchmark's full sizes on sampled batch
+rows, and on the degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from scan_linear_recurrences_gb300 import _binding as b
+from scan_linear_recurrences_gb300 import api, inputs
+from scan_linear_recurrences_gb300.build import build
+
+from ._parity import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    build()
+    b.lib()
+    yield
+    b.mgs_check()
+
+
+def _cuda(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+# ---------------------------------------------------------------- matrix_affine_scan
+def _run_mas(B, T, H, k, seed, h0_mode, sample=None):
+    d = _cuda(inputs.mas_inputs(B, T, H, k, seed, device="cpu", h0=h0_mode))
+    h = api.matrix_affine_scan_fwd(d["A"], d["b"], d["h0"])
+    dA, db, dh0 = api.matrix_affine_scan_bwd(d["A"], d["h0"], h, d["grad_h"], need_dh0=True)
+    b.mgs_check()
+    sel = slice(None) if sample is None else sample
+    A, bb, g = d["A"][sel].cpu(), d["b"][sel].cpu(), d["grad_h"][sel].cpu()
+    h0 = d["h0"][sel].cpu() if d["h0"] is not None else torch.zeros((A.shape[0], H, k))
+    href = oracle.mas_fwd(A, bb, h0)
+    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
+    assert_close("h", h[sel], href, T)
+    assert_close("dA", dA[sel], dAr, T)
+    assert_close("db", db[sel], dbr, T)
+    assert_close("dh0", dh0[sel], dh0r, T)
+
+
+@pytest.mark.parametrize("cid", [0, 1])
+def test_mas_configs_full(cid):
+    w = inputs.WORKLOADS[cid]
+    _run_mas(w.B, w.T, w.H, w.k, w.seed, w.h0)
+
+
+@pytest.mark.parametrize("B,T,H,k,h0", [
+    (1, 1, 1, 8, "normal"),     # single step
+    (3, 37, 5, 8, "normal"),    # ragged T (not a multiple of the stage), partial head group
+    (2, 70, 9, 8, "zeros"),     # explicit zero initial state
+    (2, 45, 3, 4, "normal"),
+    (2, 33, 3, 16, "normal"),
+    (2, 50, 6, 2, "normal"),
+    (2, 81, 12, 1, "normal"),   # k = 1: the diagonal (linear_scan) case
+    (1, 300, 4, 8, "none"),
+])
+def test_mas_shapes(B, T, H, k, h0):
+    _run_mas(B, T, H, k, seed=100 + B * T + H + k, h0_mode=h0)
+
+
+def test_mas_config4_sampled_rows():
+    """Full benchmark size (B=32, T=8192, H=64, k=8) in the launch
+    configuration the benchmark times; the oracle checks three batch rows."""
+    w = inputs.WORKLOADS[4]
+    d = w.make(device="cuda")
+    h = api.matrix_affine_scan_fwd(d["A"], d["b"], d["h0"])
+    dA, db, dh0 = api.matrix_affine_scan_bwd(d["A"], d["h0"], h, d["grad_h"])
+    b.mgs_check()
+    rows = [0, 13, w.B - 1]
+    A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
+    assert_close("h", h[rows], oracle.mas_fwd(A, bb, h0), w.T)
+    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
+    assert_close("dA", dA[rows], dAr, w.T)
+    assert_close("db", db[rows], dbr, w.T)
+    assert_close("dh0", dh0[rows], dh0r, w.T)
+
+
+def test_mas_empty_and_T0():
+    dev = "cuda"
+    A = torch.empty((2, 0, 3, 8, 8), device=dev)
+    bb = torch.empty((2, 0, 3, 8), device=dev)
+    h = api.matrix_affine_scan_fwd(A, bb, None)
+    assert h.shape == (2, 0, 3, 8)
+    h0 = torch.randn((2, 3, 8), device=dev)
+    dh0 = torch.full((2, 3, 8), float("nan"), device=dev)
+    b.mgs_matrix_affine_scan_bwd(A, h0, bb, bb, A, bb, dh0, 2, 0, 3, 8)
+    b.mgs_check()
+    assert torch.equal(dh0, torch.zeros_like(dh0))
+
+
+# ---------------------------------------------------------------- matrix_scan
+def _run_ms(B, T, H, k, seed):
+    d = _cuda(inputs.ms_inputs(B, T, H, k, seed))
+    P = api.matrix_scan_fwd(d["A"])
+    dA = api.matrix_scan_bwd(d["A"], P, d["grad_P"])
+    b.mgs_check()
+    assert_close("P", P, oracle.ms_fwd(d["A"].cpu()), T)
+    assert_close("dA", dA, oracle.ms_bwd(d["A"].cpu(), d["grad_P"].cpu()), T)
+
+
+def test_ms_config2_full():
+    w = inputs.WORKLOADS[2]
+    _run_ms(w.B, w.T, w.H, w.k, w.seed)
+
+
+@pytest.mark.parametrize("B,T,H,k", [
+    (1, 1, 1, 8), (2, 13, 5, 8), (2, 21, 3, 4), (2, 17, 3, 16), (1, 40, 2, 2), (2, 30, 8, 1), (1, 333, 2, 8),
+])
+def test_ms_shapes(B, T, H, k):
+    _run_ms(B, T, H, k, seed=200 + B * T + H + k)
+
+
+# ---------------------------------------------------------------- parallel_scan_log
+def _run_psl(B, T, D, seed, with_h0=True, rows=None):
+    d = _cuda(inputs.psl_inputs(B, T, D, seed, device="cpu", with_h0=with_h0))
+    return _check_psl(d, T, rows)
+
+
+def _check_psl(d, T, rows=None):
+    h, lh = api.parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], want_log=True)
+    dlc, dlv, dl0 = api.parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], h, d["grad_h"])
+    b.mgs_check()
+    sel = slice(None) if rows is None else rows
+    lc, lv, g = (d[k][sel].cpu() for k in ("log_coeffs", "log_values", "grad_h"))
+    l0 = d["log_h0"][sel].cpu() if d["log_h0"] is not None else None
+    href, lhref = oracle.psl_fwd(lc, lv, l0, want_log=True)
+    assert_close("h", h[sel], href, T)
+    assert_close("log_h", lh[sel], lhref, T)
+    dlcr, dlvr, dl0r = oracle.psl_bwd(lc, lv, l0, g)
+    assert_close("d_log_coeffs", dlc[sel], dlcr, T)
+    assert_close("d_log_values", dlv[sel], dlvr, T)
+    if l0 is not None:
+        assert_close("d_log_h0", dl0[sel], dl0r, T)
+
+
+@pytest.mark.parametrize("B,T,D,h0", [
+    (2, 1, 4, True), (3, 50, 132, True), (2, 257, 1024, True), (2, 100, 260, False), (1, 2000, 128, True),
+])
+def test_psl_shapes(B, T, D, h0):
+    _run_psl(B, T, D, seed=300 + B * T + D, with_h0=h0)
+
+
+def test_psl_config3_sampled_rows():
+    w = inputs.WORKLOADS[3]
+    d = w.make(device="cuda")
+    _check_psl(d, w.T, rows=[0, 33, w.B - 1])
+
+
+def test_psl_zero_coefficients_and_empty():
+    # log_coeffs = -inf: h_t = exp(log_values_t); gradients through the coefficient vanish
+    B, T, D = 2, 20, 8
+    lc = torch.full((B, T, D), float("-inf"), device="cuda")
+    lv = torch.randn((B, T, D), device="cuda")
+    l0 = torch.randn((B, D), device="cuda")
+    h = api.parallel_scan_log_fwd(lc, lv, l0)
+    b.mgs_check()
+    assert_close("h", h, oracle.psl_fwd(lc.cpu(), lv.cpu(), l0.cpu()), T)
+    empty = torch.empty((0, 5, 8), device="cuda")
+    assert api.parallel_scan_log_fwd(empty, empty).shape == (0, 5, 8)
+
+
+# ---------------------------------------------------------------- autograd wrappers
+def test_autograd_wrappers_match_oracle():
+    d = _cuda(inputs.mas_inputs(2, 30, 3, 8, seed=7, h0="normal"))
+    A = d["A"].clone().requires_grad_(True)
+    bb = d["b"].clone().requires_grad_(True)
+    h0 = d["h0"].clone().requires_grad_(True)
+    h = api.matrix_affine_scan(A, bb, h0)
+    (h * d["grad_h"]).sum().backward()
+    dAr, dbr, dh0r = oracle.mas_bwd(d["A"].cpu(), d["b"].cpu(), d["h0"].cpu(), d["grad_h"].cpu())
+    assert_close("dA", A.grad, dAr, 30)
+    assert_close("db", bb.grad, dbr, 30)
+    assert_close("dh0", h0.grad, dh0r, 30)
+
+
+# ---------------------------------------------------------------- failure detection
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A wait on a flag that nothing sets gives up after the timeout, the error
+    word reports it, and the device keeps working afterwards."""
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    b.mgs_set_wait_timeout_ns(20_000_000)  # 20 ms
+    try:
+        b.mgs_debug_wait_flag(flag)
+        with pytest.raises(b.MGSError) as ei:
+            b.mgs_check()
+        assert ei.value.status == b.MGS_ERR_TIMEOUT
+        b.mgs_check()  # cleared
+        flag.fill_(1)
+        b.mgs_debug_wait_flag(flag)
+        b.mgs_check()
+    finally:
+        b.mgs_set_wait_timeout_ns(1_000_000_000)
+    _run_mas(1, 16, 4, 8, seed=1, h0_mode="normal")
