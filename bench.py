@@ -229,7 +229,12 @@ def run_gpu(args):
     b.lib()
 
     ids = [int(x) for x in args.workloads.split(",")]
-    runners = [Runner(inputs.WORKLOADS[i], torch, b, api, device) for i in ids]
+    ws = [inputs.WORKLOADS[i] for i in ids]
+    if args.batch_rows:
+        # profiling only: a smaller case of the same kernels (fewer batch rows)
+        from dataclasses import replace
+        ws = [replace(w, B=min(w.B, args.batch_rows)) for w in ws]
+    runners = [Runner(w, torch, b, api, device) for w in ws]
     small = {r.w.cid: (r.w.op != "psl" and r.w.B * r.w.T * r.w.H * r.w.k * r.w.k * 4 * 3 < (256 << 20)) for r in runners}
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
@@ -474,6 +479,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--batch-rows", type=int, default=0,
+                    help="profiling: cap every workload's batch rows (smaller case, same kernels)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         ap.error("--warmup must be at least 3")
