@@ -7,6 +7,8 @@
 #include <set>
 #include <utility>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/mgscan.h"
 #include "mgs_launch.h"
 
@@ -92,6 +94,8 @@ mgs_status block_sizes(int64_t B, int64_t T, int64_t H, int k, BlockSizes *s) {
     if (!mul_ok(bth, int64_t(k) * k, &s->mat) || !mul_ok(bth, k, &s->vec) || !mul_ok(bh, k, &s->init))
         return MGS_ERR_INVALID_ARG;
     if (s->mat > (INT64_MAX / 8)) return MGS_ERR_INVALID_ARG;
+    // tensor-map row coordinates are 32-bit
+    if (B * T > INT32_MAX || H > INT32_MAX / 256) return MGS_ERR_UNSUPPORTED;
     return MGS_OK;
 }
 
@@ -118,6 +122,32 @@ mgs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGS_OK : MGS_ERR
 }  // namespace
 
 namespace mgs {
+
+cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,
+                      const uint64_t *byte_strides, const uint32_t *box) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (encode == nullptr) return cudaErrorNotSupported;
+    cuuint64_t gdim[3], gstr[2];
+    cuuint32_t bdim[3], estr[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; ++i) gstr[i] = byte_strides[i];
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<float *>(base), gdim,
+                        gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t ensure_smem_attr(const void *fn, int bytes) {
     static std::mutex mu;
@@ -229,6 +259,7 @@ static mgs_status psl_sizes(int64_t B, int64_t T, int64_t D, int64_t *n, int64_t
     int64_t bt;
     if (!mul_ok(B, T, &bt) || !mul_ok(bt, D, n) || !mul_ok(B, D, n0)) return MGS_ERR_INVALID_ARG;
     if (*n > INT64_MAX / 8) return MGS_ERR_INVALID_ARG;
+    if (B * T > INT32_MAX || D > INT32_MAX) return MGS_ERR_UNSUPPORTED;  // 32-bit map coordinates
     return MGS_OK;
 }
 

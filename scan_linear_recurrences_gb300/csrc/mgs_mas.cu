@@ -5,17 +5,16 @@
 // Design (one GB300 SM runs several of these warps side by side):
 //  * A warp owns 32/k consecutive heads of one batch row ("lanes"); k threads
 //    per lane, thread i owning row i of every A_t and coordinate i of h.
-//  * Inputs stream through a per-warp ring of NS stages x TS time steps in
-//    shared memory, filled by 1-D TMA bulk copies (cp.async.bulk) that lane 0
-//    issues and an mbarrier per stage tracks.  The copies for one (b, t) are
-//    contiguous (the warp's heads are adjacent), so each is 128*k bytes of A.
+//  * Inputs stream through a per-warp ring of NS stages in shared memory.  Each
+//    stage holds TS time steps of every input; one tiled TMA load
+//    (cp.async.bulk.tensor) per input fills it, tracked by one mbarrier.
 //  * Forward: h_{t-1} is all-gathered inside the k-thread group with k
 //    shuffles, then k FMAs give h_t[i]; the store is coalesced (128 B/warp).
 //  * Backward walks t downwards: lambda_t = g_t + mu_{t+1}; db_t, the dA_t row
 //    lambda_t[i] h_{t-1}^T and the next mu_t = A_t^T lambda_t (a butterfly
 //    reduce-scatter over the group, k-1 shuffles) all come from registers, so
 //    nothing beyond the outputs is written.
-#include "mgs_launch.h"
+#include "mgs_tiles.cuh"
 
 namespace mgs {
 namespace {
@@ -28,16 +27,15 @@ struct MasShape {
     // time steps per stage: about 8-10 KB of A per stage
     static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? 8 : 16);
     static constexpr int NS = 4;                // stages in flight
+    using TA = HeadTile<K * K, LPW>;
+    using TV = HeadTile<K, LPW>;
 };
 
-constexpr int kWarpsPerBlock = 1;
-
-__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-
-// Per-warp shared memory: ring (NS*TS steps of STEPF floats) then NS barriers.
-template <int STEPF, int TS, int NS>
-struct RingLayout {
-    static constexpr size_t ring_bytes = size_t(NS) * TS * STEPF * sizeof(float);
+// Per-warp shared memory: NS stages of STAGEF floats, then NS barriers.
+template <int STAGEF, int NS>
+struct Ring {
+    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);
+    static constexpr size_t ring_bytes = NS * stage_bytes;
     static constexpr size_t warp_bytes = align_up(ring_bytes + NS * sizeof(uint64_t), 128);
 };
 
@@ -93,43 +91,41 @@ __device__ __forceinline__ float group_reduce_scatter(const float (&p)[K], int r
 
 // ---------------------------------------------------------------- forward
 template <int K>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    mas_fwd_kernel(const float *__restrict__ A, const float *__restrict__ bv,
+__global__ void __launch_bounds__(32)
+    mas_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float *__restrict__ h0, float *__restrict__ h, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MasShape<K>;
-    constexpr int STEPF = S::AF + S::VF;
-    using L = RingLayout<STEPF, S::TS, S::NS>;
+    constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
+    using R = Ring<STAGEF, S::NS>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw + size_t(warp) * L::warp_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + size_t(warp) * L::warp_bytes + L::ring_bytes);
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
-    const int64_t head0 = (g % groups_per_b) * S::LPW;
+    const int head0 = int(g % groups_per_b) * S::LPW;
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, row = lane % K, gbase = lane & ~(K - 1);
     const bool active = sub < nl;
-    const uint32_t a_bytes = uint32_t(nl) * K * K * 4u, v_bytes = uint32_t(nl) * K * 4u;
     const int64_t nblk = (T + S::TS - 1) / S::TS;
+    const int row0 = int(bi * T);
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
     auto issue = [&](int s, int64_t j) {  // lane 0 only
-        const int64_t t0 = j * S::TS;
-        const int n = int(min64(S::TS, T - t0));
-        mbar_arrive_expect_tx(&bars[s], uint32_t(n) * (a_bytes + v_bytes));
-        for (int u = 0; u < n; ++u) {
-            const int64_t r = (bi * T + t0 + u) * H + head0;
-            float *st = ring + (size_t(s) * S::TS + u) * STEPF;
-            bulk_g2s(st, A + r * K * K, a_bytes, &bars[s], pol);
-            bulk_g2s(st + S::AF, bv + r * K, v_bytes, &bars[s], pol);
-        }
+        float *st = ring + size_t(s) * STAGEF;
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        S::TA::load(st, &tmA, head0, row0 + int(j * S::TS), &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmB, head0, row0 + int(j * S::TS), &bars[s], pol);
     };
 
     const int npro = int(min64(S::NS, nblk));
@@ -139,6 +135,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
     float hprev = (h0 != nullptr && active) ? h0[(bi * H + head0 + sub) * K + row] : 0.f;
     float *hout = h + (bi * T * H + head0 + sub) * K + row;  // + t*H*K per step
+    const int64_t hstride = H * K;
 
     for (int64_t j = 0; j < nblk; ++j) {
         const int s = int(j % S::NS);
@@ -147,15 +144,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
             rg.drain(ctl, lane);
             return;
         }
-        const int64_t t0 = j * S::TS;
-        const int n = int(min64(S::TS, T - t0));
-        const float *st = ring + size_t(s) * S::TS * STEPF;
+        const int n = int(min64(S::TS, T - j * S::TS));
+        const float *sa = ring + size_t(s) * STAGEF + (sub * K + row) * K;
+        const float *sb = ring + size_t(s) * STAGEF + A_STAGE + sub * K + row;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 float a[K];
-                lds_row<K>(st + u * STEPF + (sub * K + row) * K, a);
-                float acc0 = st[u * STEPF + S::AF + sub * K + row];
+                lds_row<K>(sa + u * S::AF, a);
+                float acc0 = sb[u * S::VF];
                 float acc1 = 0.f;
 #pragma unroll
                 for (int c = 0; c < K; ++c) {
@@ -166,7 +163,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                         acc0 = fmaf(a[c], x, acc0);
                 }
                 hprev = acc0 + acc1;
-                if (active) st_cs(hout + (t0 + u) * H * K, hprev);
+                if (active) st_cs(hout, hprev);
+                hout += hstride;
             }
         }
         __syncwarp();
@@ -182,48 +180,49 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 
 // ---------------------------------------------------------------- backward
 template <int K>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    mas_bwd_kernel(const float *__restrict__ A, const float *__restrict__ h0,
-                   const float *__restrict__ h, const float *__restrict__ gh,
-                   float *__restrict__ dA, float *__restrict__ db, float *__restrict__ dh0,
-                   int64_t B, int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
+__global__ void __launch_bounds__(32)
+    mas_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                   const __grid_constant__ CUtensorMap tmH, const float *__restrict__ h0,
+                   float *__restrict__ dA, float *__restrict__ db, float *__restrict__ dh0, int64_t B,
+                   int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MasShape<K>;
-    constexpr int STEPF = S::AF + 2 * S::VF;  // A_t, g_t, h_{t-1}
-    using L = RingLayout<STEPF, S::TS, S::NS>;
+    constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
+    constexpr int STAGEF = A_STAGE + 2 * V_STAGE;  // A_t, g_t, h_{t-1}
+    using R = Ring<STAGEF, S::NS>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw + size_t(warp) * L::warp_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + size_t(warp) * L::warp_bytes + L::ring_bytes);
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
-    const int64_t head0 = (g % groups_per_b) * S::LPW;
+    const int head0 = int(g % groups_per_b) * S::LPW;
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, row = lane % K;
     const bool active = sub < nl;
-    const uint32_t a_bytes = uint32_t(nl) * K * K * 4u, v_bytes = uint32_t(nl) * K * 4u;
     const int64_t nblk = (T + S::TS - 1) / S::TS;
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-
-    // block j covers t = T-1-j*TS down to max(0, T-(j+1)*TS); step u -> t = T-1-j*TS-u
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmH);
+    }
+    // Block j covers t = T-1-j*TS down to max(0, T-(j+1)*TS).  Its boxes start
+    // at row bi*T + T-(j+1)*TS (possibly before this batch row: unused, and
+    // zero-filled when negative) so step u (t = T-1-j*TS-u) sits at box row
+    // TS-1-u.  The h box starts one row earlier and holds h_{t-1}.
     auto issue = [&](int s, int64_t j) {  // lane 0 only
-        const int64_t tt = T - 1 - j * S::TS;
-        const int n = int(min64(S::TS, tt + 1));
-        const int with_h = (tt - n + 1 >= 1) ? n : n - 1;  // t = 0 takes h0 instead
-        mbar_arrive_expect_tx(&bars[s], uint32_t(n) * (a_bytes + v_bytes) + uint32_t(with_h) * v_bytes);
-        for (int u = 0; u < n; ++u) {
-            const int64_t t = tt - u;
-            const int64_t r = (bi * T + t) * H + head0;
-            float *st = ring + (size_t(s) * S::TS + u) * STEPF;
-            bulk_g2s(st, A + r * K * K, a_bytes, &bars[s], pol);
-            bulk_g2s(st + S::AF, gh + r * K, v_bytes, &bars[s], pol);
-            if (t >= 1) bulk_g2s(st + S::AF + S::VF, h + (r - H) * K, v_bytes, &bars[s], pol);
-        }
+        float *st = ring + size_t(s) * STAGEF;
+        const int r0 = int(bi * T + T - (j + 1) * S::TS);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        S::TA::load(st, &tmA, head0, r0, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmG, head0, r0, &bars[s], pol);
+        S::TV::load(st + A_STAGE + V_STAGE, &tmH, head0, r0 - 1, &bars[s], pol);
     };
 
     const int npro = int(min64(S::NS, nblk));
@@ -232,7 +231,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
     float mu = 0.f;  // (A_{t+1}^T lambda_{t+1})[row], zero past the end
-    const int64_t lane_off = bi * T * H + head0 + sub;  // (b, t=0, head) row index
+    const int64_t hk = H * K;
+    float *dbp = db + (bi * T * H + head0 + sub) * K + row;          // + t*H*K
+    float *dAp = dA + (bi * T * H + head0 + sub) * K * K + row * K;  // + t*H*K*K
 
     for (int64_t j = 0; j < nblk; ++j) {
         const int s = int(j % S::NS);
@@ -243,16 +244,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         }
         const int64_t tt = T - 1 - j * S::TS;
         const int n = int(min64(S::TS, tt + 1));
-        const float *st = ring + size_t(s) * S::TS * STEPF;
+        const float *st = ring + size_t(s) * STAGEF;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 const int64_t t = tt - u;
-                const float *su = st + u * STEPF;
-                const float lam = su[S::AF + sub * K + row] + mu;
+                const int q = S::TS - 1 - u;  // box row of step u
+                const float lam = st[A_STAGE + q * S::VF + sub * K + row] + mu;
                 float hp[K];
                 if (t >= 1) {
-                    lds_row<K>(su + S::AF + S::VF + sub * K, hp);
+                    lds_row<K>(st + A_STAGE + V_STAGE + q * S::VF + sub * K, hp);
                 } else if (h0 != nullptr && active) {
 #pragma unroll
                     for (int c = 0; c < K; ++c) hp[c] = h0[(bi * H + head0 + sub) * K + c];
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                     for (int c = 0; c < K; ++c) hp[c] = 0.f;
                 }
                 float a[K];
-                lds_row<K>(su + (sub * K + row) * K, a);
+                lds_row<K>(st + q * S::AF + (sub * K + row) * K, a);
                 float p[K], dar[K];
 #pragma unroll
                 for (int c = 0; c < K; ++c) {
@@ -270,9 +271,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                 }
                 mu = group_reduce_scatter<K>(p, row);
                 if (active) {
-                    const int64_t r = lane_off + t * H;
-                    st_cs(db + r * K + row, lam);
-                    stg_row_cs<K>(dA + r * K * K + row * K, dar);
+                    st_cs(dbp + t * hk, lam);
+                    stg_row_cs<K>(dAp + t * hk * K, dar);
                 }
             }
         }
@@ -292,15 +292,17 @@ template <int K>
 cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
                       int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
     using S = MasShape<K>;
-    using L = RingLayout<S::AF + S::VF, S::TS, S::NS>;
+    using R = Ring<S::TS * (S::AF + S::VF), S::NS>;
+    CUtensorMap tA, tB;
+    cudaError_t e;
+    if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tB, b, B * T, H, S::TS)) != cudaSuccess) return e;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
-    const int64_t warps = B * gpb;
-    const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)mas_fwd_kernel<K>, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    mas_fwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(A, b, h0, h, B, T, H, gpb, ctl);
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_fwd_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_fwd_kernel<K><<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tB, h0, h, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
@@ -309,15 +311,18 @@ cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const flo
                       float *db, float *dh0, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
                       cudaStream_t s) {
     using S = MasShape<K>;
-    using L = RingLayout<S::AF + 2 * S::VF, S::TS, S::NS>;
+    using R = Ring<S::TS * (S::AF + 2 * S::VF), S::NS>;
+    CUtensorMap tA, tG, tH;
+    cudaError_t e;
+    if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tG, gh, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tH, h, B * T, H, S::TS)) != cudaSuccess) return e;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
-    const int64_t warps = B * gpb;
-    const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)mas_bwd_kernel<K>, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t blocks = (warps + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    mas_bwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(A, h0, h, gh, dA, db, dh0, B, T, H, gpb, ctl);
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_bwd_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_bwd_kernel<K><<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tG, tH, h0, dA, db, dh0, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 

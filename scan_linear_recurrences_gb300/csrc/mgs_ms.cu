@@ -7,7 +7,7 @@
 // (backward), so the k x k product per step is a broadcast read of A_t from
 // shared memory and k^2 register FMAs with no shuffles.  Inputs stream through
 // the same per-warp TMA bulk-copy ring as matrix_affine_scan.
-#include "mgs_launch.h"
+#include "mgs_tiles.cuh"
 
 namespace mgs {
 namespace {
@@ -18,10 +18,10 @@ struct MsShape {
     static constexpr int MF = LPW * K * K;  // floats of one k x k tensor per time step
     static constexpr int TS = K >= 16 ? 2 : (K >= 8 ? 4 : 8);
     static constexpr int NS = 4;
+    using TM = HeadTile<K * K, LPW>;
 };
 
 constexpr int kWarpsPerBlock = 1;
-__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <int STEPF, int TS, int NS, int EXTRAF>
 struct MsLayout {
@@ -82,8 +82,8 @@ __device__ __forceinline__ void smem_matvec_t(const float *M, const float (&x)[K
 // ---------------------------------------------------------------- forward
 template <int K>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    ms_fwd_kernel(const float *__restrict__ A, float *__restrict__ P, int64_t B, int64_t T,
-                  int64_t H, int64_t groups_per_b, DevCtl ctl) {
+    ms_fwd_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P, int64_t B,
+                  int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MsShape<K>;
     constexpr int STEPF = S::MF;
     using L = MsLayout<STEPF, S::TS, S::NS, 0>;
@@ -101,20 +101,15 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, col = lane % K;
     const bool active = sub < nl;
-    const uint32_t m_bytes = uint32_t(nl) * K * K * 4u;
     const int64_t nblk = (T + S::TS - 1) / S::TS;
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {
-        const int64_t t0 = j * S::TS;
-        const int n = int(min64(S::TS, T - t0));
-        mbar_arrive_expect_tx(&bars[s], uint32_t(n) * m_bytes);
-        for (int u = 0; u < n; ++u) {
-            const int64_t r = (bi * T + t0 + u) * H + head0;
-            bulk_g2s(ring + (size_t(s) * S::TS + u) * STEPF, A + r * K * K, m_bytes, &bars[s], pol);
-        }
+    if (lane == 0) prefetch_tmap(&tmA);
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        mbar_arrive_expect_tx(&bars[s], uint32_t(S::TS * STEPF * 4));
+        S::TM::load(ring + size_t(s) * S::TS * STEPF, &tmA, int(head0), int(bi * T + j * S::TS), &bars[s], pol);
     };
     const int npro = int(min64(S::NS, nblk));
     if (lane == 0)
@@ -164,9 +159,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // ---------------------------------------------------------------- backward
 template <int K>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    ms_bwd_kernel(const float *__restrict__ A, const float *__restrict__ P,
-                  const float *__restrict__ G, float *__restrict__ dA, int64_t B, int64_t T,
-                  int64_t H, int64_t groups_per_b, DevCtl ctl) {
+    ms_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                  const __grid_constant__ CUtensorMap tmP, float *__restrict__ dA, int64_t B,
+                  int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MsShape<K>;
     constexpr int STEPF = 3 * S::MF;  // A_t, G_t, P_{t-1}
     constexpr int XF = S::MF;         // Lambda exchange buffer, [lane][row][col]
@@ -186,25 +181,25 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, col = lane % K;
     const bool active = sub < nl;
-    const uint32_t m_bytes = uint32_t(nl) * K * K * 4u;
     const int64_t nblk = (T + S::TS - 1) / S::TS;
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {
-        const int64_t tt = T - 1 - j * S::TS;
-        const int n = int(min64(S::TS, tt + 1));
-        const int with_p = (tt - n + 1 >= 1) ? n : n - 1;
-        mbar_arrive_expect_tx(&bars[s], uint32_t(2 * n + with_p) * m_bytes);
-        for (int u = 0; u < n; ++u) {
-            const int64_t t = tt - u;
-            const int64_t r = (bi * T + t) * H + head0;
-            float *st = ring + (size_t(s) * S::TS + u) * STEPF;
-            bulk_g2s(st, A + r * K * K, m_bytes, &bars[s], pol);
-            bulk_g2s(st + S::MF, G + r * K * K, m_bytes, &bars[s], pol);
-            if (t >= 1) bulk_g2s(st + 2 * S::MF, P + (r - H) * K * K, m_bytes, &bars[s], pol);
-        }
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmP);
+    }
+    // Block j covers t = T-1-j*TS down to max(0, T-(j+1)*TS); box row of step u
+    // is TS-1-u; the P box starts one row earlier and holds P_{t-1}.
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * S::TS * STEPF;
+        const int r0 = int(bi * T + T - (j + 1) * S::TS);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(S::TS * STEPF * 4));
+        S::TM::load(st, &tmA, int(head0), r0, &bars[s], pol);
+        S::TM::load(st + S::TS * S::MF, &tmG, int(head0), r0, &bars[s], pol);
+        S::TM::load(st + 2 * S::TS * S::MF, &tmP, int(head0), r0 - 1, &bars[s], pol);
     };
     const int npro = int(min64(S::NS, nblk));
     if (lane == 0)
@@ -230,9 +225,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 const int64_t t = tt - u;
-                const float *At = st + u * STEPF + sub * K * K;
-                const float *Gt = At + S::MF;
-                const float *Pp = At + 2 * S::MF;
+                const int q = S::TS - 1 - u;  // box row of step u
+                const float *At = st + q * S::MF + sub * K * K;
+                const float *Gt = At + S::TS * S::MF;
+                const float *Pp = At + 2 * S::TS * S::MF;
                 float lc[K];  // column `col` of Lambda_t
 #pragma unroll
                 for (int i = 0; i < K; ++i) lc[i] = Gt[i * K + col] + mu[i];
@@ -283,11 +279,14 @@ cudaError_t ms_fwd_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, 
     using L = MsLayout<S::MF, S::TS, S::NS, 0>;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
     const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)ms_fwd_kernel<K>, smem);
+    CUtensorMap tA;
+    cudaError_t e = S::TM::make(&tA, A, B * T, H, S::TS);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attr((const void *)ms_fwd_kernel<K>, smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (B * gpb + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    ms_fwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(A, P, B, T, H, gpb, ctl);
+    ms_fwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(tA, P, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
@@ -298,11 +297,16 @@ cudaError_t ms_bwd_t(const float *A, const float *P, const float *G, float *dA, 
     using L = MsLayout<3 * S::MF, S::TS, S::NS, S::MF>;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
     const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)ms_bwd_kernel<K>, smem);
+    CUtensorMap tA, tG, tP;
+    cudaError_t e;
+    if ((e = S::TM::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TM::make(&tG, G, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TM::make(&tP, P, B * T, H, S::TS)) != cudaSuccess) return e;
+    e = ensure_smem_attr((const void *)ms_bwd_kernel<K>, smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (B * gpb + kWarpsPerBlock - 1) / kWarpsPerBlock;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    ms_bwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(A, P, G, dA, B, T, H, gpb, ctl);
+    ms_bwd_kernel<K><<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(tA, tG, tP, dA, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 

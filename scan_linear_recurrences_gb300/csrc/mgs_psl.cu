@@ -8,93 +8,106 @@
 // which equals Heinsen's exp(a*_t + logcumsumexp(log_values - a*)) without
 // ever forming the cumulative sum a*_t (whose fp32 cancellation at T = 4096
 // would cost about three decimal digits).  logaddexp is max-shifted:
-// max(x, y) + log1p(exp(-|x - y|)).
+// max(x, y) + log(1 + exp(-|x - y|)).  The state is carried in base 2
+// (L = log2 h), so each step is two multiplies by log2(e), the hardware
+// ex2/lg2 pair and a final ex2 for h_t.
+//
+// Error budget of the base-2 form: converting an input x to base 2 rounds
+// x*log2(e) (relative error 2^-24), i.e. an absolute error of about
+// 6e-8*|x| in the exponent; ex2 and lg2 add a few 1e-7.  For |log_values|,
+// |log_coeffs|, |log h| up to 50 every step's relative error in h stays
+// below about 4e-6, and the recurrence contracts it (the weight of the
+// carried term is below 1).
 // Backward walks t downwards in linear space (a_t = exp(log_coeffs_t) in (0, 1]
 // for gates), lambda_t = g_t + a_{t+1} lambda_{t+1}.
 //
 // A warp owns 128 adjacent channels of one batch row (4 per thread, float4);
-// each time step's rows arrive by 1-D TMA bulk copies into a per-warp ring.
+// each stage of TS time steps arrives by one tiled TMA load per input tensor.
 #include <math_constants.h>
 
-#include "mgs_launch.h"
+#include "mgs_tiles.cuh"
 
 namespace mgs {
 namespace {
 
 constexpr int kChan = 128;  // channels per warp
-constexpr int kWarpsPerBlock = 1;
-__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
-template <int NT, int TS, int NS>  // NT row-tensors per step
-struct PslLayout {
-    static constexpr int STEPF = NT * kChan;
-    static constexpr size_t ring_bytes = size_t(NS) * TS * STEPF * sizeof(float);
+template <int NT, int TS, int NS>  // NT row tensors per stage
+struct PslRing {
+    static constexpr int BOXF = TS * kChan;  // floats per tensor box
+    static constexpr int STAGEF = NT * BOXF;
+    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);
+    static constexpr size_t ring_bytes = NS * stage_bytes;
     static constexpr size_t warp_bytes = align_up(ring_bytes + NS * sizeof(uint64_t), 128);
 };
 
 constexpr int kFwdTS = 8, kFwdNS = 4;  // 2 tensors x 512 B x 8 steps = 8 KB per stage
 constexpr int kBwdTS = 4, kBwdNS = 4;  // 4 tensors x 512 B x 4 steps = 8 KB per stage
 
-// The correction term log1p(exp(-|x - y|)) lies in [0, log 2]; computing it
-// with the MUFU approximations (__expf, __logf) costs an absolute error of
-// about 2e-7 in log h_t whatever the magnitude of x and y, i.e. a relative
-// error of that size in h_t, well inside the fp32 parity bound.
-__device__ __forceinline__ float logaddexp_f(float x, float y) {
+// log2(2^x + 2^y); both -inf gives -inf (avoids inf - inf).
+__device__ __forceinline__ float logaddexp2_f(float x, float y) {
     const float m = fmaxf(x, y);
-    const float r = m + __logf(1.f + __expf(-fabsf(x - y)));
-    // both -inf: the sum of two zeros is zero (avoid inf - inf)
+    const float r = m + lg2_approx(1.f + ex2_approx(-fabsf(x - y)));
     return (m == -CUDART_INF_F) ? m : r;
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
 
+cudaError_t make_rows_map(CUtensorMap *m, const float *base, int64_t rows, int64_t D, int TS) {
+    const uint64_t dims[2] = {uint64_t(D), uint64_t(rows)};
+    const uint64_t str[1] = {uint64_t(D) * 4u};
+    const uint32_t box[2] = {uint32_t(kChan), uint32_t(TS)};
+    return make_tmap(m, base, 2, dims, str, box);
+}
+
 // ---------------------------------------------------------------- forward
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    psl_fwd_kernel(const float *__restrict__ lc, const float *__restrict__ lv,
-                   const float *__restrict__ lh0, float *__restrict__ h,
-                   float *__restrict__ logh, int64_t B, int64_t T, int64_t D,
-                   int64_t groups_per_b, DevCtl ctl) {
-    using L = PslLayout<2, kFwdTS, kFwdNS>;
+__global__ void __launch_bounds__(32)
+    psl_fwd_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmV,
+                   const float *__restrict__ lh0, float *__restrict__ h, float *__restrict__ logh,
+                   int64_t B, int64_t T, int64_t D, int64_t groups_per_b, DevCtl ctl) {
+    using R = PslRing<2, kFwdTS, kFwdNS>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw + size_t(warp) * L::warp_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + size_t(warp) * L::warp_bytes + L::ring_bytes);
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
-    const int64_t c0 = (g % groups_per_b) * kChan;
-    const int nc = int(min64(kChan, D - c0));
-    const bool active = 4 * lane < nc;
-    const uint32_t row_bytes = uint32_t(nc) * 4u;
+    const int c0 = int(g % groups_per_b) * kChan;
+    const bool active = c0 + 4 * lane < D;
     const int64_t nblk = (T + kFwdTS - 1) / kFwdTS;
+    const int row0 = int(bi * T);
 
     WarpRing<kFwdNS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {
-        const int64_t t0 = j * kFwdTS;
-        const int n = int(min64(kFwdTS, T - t0));
-        mbar_arrive_expect_tx(&bars[s], uint32_t(n) * 2u * row_bytes);
-        for (int u = 0; u < n; ++u) {
-            const int64_t off = (bi * T + t0 + u) * D + c0;
-            float *st = ring + (size_t(s) * kFwdTS + u) * L::STEPF;
-            bulk_g2s(st, lc + off, row_bytes, &bars[s], pol);
-            bulk_g2s(st + kChan, lv + off, row_bytes, &bars[s], pol);
-        }
+    if (lane == 0) {
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmV);
+    }
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * R::STAGEF;
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        tma_load_2d(st, &tmC, c0, row0 + int(j * kFwdTS), &bars[s], pol);
+        tma_load_2d(st + R::BOXF, &tmV, c0, row0 + int(j * kFwdTS), &bars[s], pol);
     };
     const int npro = int(min64(kFwdNS, nblk));
     if (lane == 0)
         for (int s = 0; s < npro; ++s) issue(s, s);
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
-    float4 Lg;  // log h_{t-1} for the thread's four channels
+    float4 L;  // log2 h_{t-1} for the thread's four channels
     if (lh0 != nullptr && active) {
-        Lg = ld4(lh0 + bi * D + c0 + 4 * lane);
+        const float4 l = ld4(lh0 + bi * D + c0 + 4 * lane);
+        L = make_float4(l.x * kLog2e, l.y * kLog2e, l.z * kLog2e, l.w * kLog2e);
     } else {
-        Lg = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+        L = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
     }
-    const int64_t out0 = bi * T * D + c0 + 4 * lane;
+    float *hp = h + bi * T * D + c0 + 4 * lane;
+    float *lp = (logh != nullptr) ? logh + bi * T * D + c0 + 4 * lane : nullptr;
 
     for (int64_t j = 0; j < nblk; ++j) {
         const int s = int(j % kFwdNS);
@@ -103,21 +116,26 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
             rg.drain(ctl, lane);
             return;
         }
-        const int64_t t0 = j * kFwdTS;
-        const int n = int(min64(kFwdTS, T - t0));
-        const float *st = ring + size_t(s) * kFwdTS * L::STEPF;
-#pragma unroll 4
-        for (int u = 0; u < n; ++u) {
-            const float4 a = ld4(st + u * L::STEPF + 4 * lane);
-            const float4 v = ld4(st + u * L::STEPF + kChan + 4 * lane);
-            Lg.x = logaddexp_f(a.x + Lg.x, v.x);
-            Lg.y = logaddexp_f(a.y + Lg.y, v.y);
-            Lg.z = logaddexp_f(a.z + Lg.z, v.z);
-            Lg.w = logaddexp_f(a.w + Lg.w, v.w);
-            if (active) {
-                const int64_t o = out0 + (t0 + u) * D;
-                st_cs4(h + o, make_float4(expf(Lg.x), expf(Lg.y), expf(Lg.z), expf(Lg.w)));
-                if (logh != nullptr) st_cs4(logh + o, Lg);
+        const int n = int(min64(kFwdTS, T - j * kFwdTS));
+        const float *sc = ring + size_t(s) * R::STAGEF + 4 * lane;
+        const float *sv = sc + R::BOXF;
+#pragma unroll
+        for (int u = 0; u < kFwdTS; ++u) {
+            if (u < n) {
+                const float4 a = ld4(sc + u * kChan);
+                const float4 v = ld4(sv + u * kChan);
+                L.x = logaddexp2_f(fmaf(a.x, kLog2e, L.x), v.x * kLog2e);
+                L.y = logaddexp2_f(fmaf(a.y, kLog2e, L.y), v.y * kLog2e);
+                L.z = logaddexp2_f(fmaf(a.z, kLog2e, L.z), v.z * kLog2e);
+                L.w = logaddexp2_f(fmaf(a.w, kLog2e, L.w), v.w * kLog2e);
+                if (active) {
+                    st_cs4(hp, make_float4(ex2_approx(L.x), ex2_approx(L.y), ex2_approx(L.z), ex2_approx(L.w)));
+                    if (lp != nullptr) {
+                        st_cs4(lp, make_float4(L.x * kLn2, L.y * kLn2, L.z * kLn2, L.w * kLn2));
+                        lp += D;
+                    }
+                }
+                hp += D;
             }
         }
         __syncwarp();
@@ -132,44 +150,44 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 }
 
 // ---------------------------------------------------------------- backward
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
-    psl_bwd_kernel(const float *__restrict__ lc, const float *__restrict__ lv,
-                   const float *__restrict__ lh0, const float *__restrict__ h,
-                   const float *__restrict__ gh, float *__restrict__ dlc,
-                   float *__restrict__ dlv, float *__restrict__ dlh0, int64_t B, int64_t T,
-                   int64_t D, int64_t groups_per_b, DevCtl ctl) {
-    using L = PslLayout<4, kBwdTS, kBwdNS>;  // lc_t, lv_t, g_t, h_{t-1}
+__global__ void __launch_bounds__(32)
+    psl_bwd_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
+                   const float *__restrict__ lh0, float *__restrict__ dlc, float *__restrict__ dlv,
+                   float *__restrict__ dlh0, int64_t B, int64_t T, int64_t D, int64_t groups_per_b,
+                   DevCtl ctl) {
+    using R = PslRing<4, kBwdTS, kBwdNS>;  // log_coeffs_t, log_values_t, g_t, h_{t-1}
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw + size_t(warp) * L::warp_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + size_t(warp) * L::warp_bytes + L::ring_bytes);
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
-    const int64_t c0 = (g % groups_per_b) * kChan;
-    const int nc = int(min64(kChan, D - c0));
-    const bool active = 4 * lane < nc;
-    const uint32_t row_bytes = uint32_t(nc) * 4u;
+    const int c0 = int(g % groups_per_b) * kChan;
+    const bool active = c0 + 4 * lane < D;
     const int64_t nblk = (T + kBwdTS - 1) / kBwdTS;
 
     WarpRing<kBwdNS> rg;
     rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {
-        const int64_t tt = T - 1 - j * kBwdTS;
-        const int n = int(min64(kBwdTS, tt + 1));
-        const int with_h = (tt - n + 1 >= 1) ? n : n - 1;
-        mbar_arrive_expect_tx(&bars[s], uint32_t(3 * n + with_h) * row_bytes);
-        for (int u = 0; u < n; ++u) {
-            const int64_t t = tt - u;
-            const int64_t off = (bi * T + t) * D + c0;
-            float *st = ring + (size_t(s) * kBwdTS + u) * L::STEPF;
-            bulk_g2s(st, lc + off, row_bytes, &bars[s], pol);
-            bulk_g2s(st + kChan, lv + off, row_bytes, &bars[s], pol);
-            bulk_g2s(st + 2 * kChan, gh + off, row_bytes, &bars[s], pol);
-            if (t >= 1) bulk_g2s(st + 3 * kChan, h + off - D, row_bytes, &bars[s], pol);
-        }
+    if (lane == 0) {
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmH);
+    }
+    // Block j covers t = T-1-j*TS down to max(0, T-(j+1)*TS); box row of step
+    // u is TS-1-u; the h box starts one row earlier and holds h_{t-1}.
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * R::STAGEF;
+        const int r0 = int(bi * T + T - (j + 1) * kBwdTS);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        tma_load_2d(st, &tmC, c0, r0, &bars[s], pol);
+        tma_load_2d(st + R::BOXF, &tmV, c0, r0, &bars[s], pol);
+        tma_load_2d(st + 2 * R::BOXF, &tmG, c0, r0, &bars[s], pol);
+        tma_load_2d(st + 3 * R::BOXF, &tmH, c0, r0 - 1, &bars[s], pol);
     };
     const int npro = int(min64(kBwdNS, nblk));
     if (lane == 0)
@@ -179,7 +197,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     float4 h0v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lh0 != nullptr && active) {
         const float4 l = ld4(lh0 + bi * D + c0 + 4 * lane);
-        h0v = make_float4(expf(l.x), expf(l.y), expf(l.z), expf(l.w));
+        h0v = make_float4(ex2_approx(l.x * kLog2e), ex2_approx(l.y * kLog2e), ex2_approx(l.z * kLog2e),
+                          ex2_approx(l.w * kLog2e));
     }
     float4 nx = make_float4(0.f, 0.f, 0.f, 0.f);  // a_{t+1} lambda_{t+1}
     const int64_t out0 = bi * T * D + c0 + 4 * lane;
@@ -193,21 +212,24 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         }
         const int64_t tt = T - 1 - j * kBwdTS;
         const int n = int(min64(kBwdTS, tt + 1));
-        const float *st = ring + size_t(s) * kBwdTS * L::STEPF;
-#pragma unroll 4
-        for (int u = 0; u < n; ++u) {
-            const int64_t t = tt - u;
-            const float *su = st + u * L::STEPF + 4 * lane;
-            const float4 c = ld4(su), v = ld4(su + kChan), gg = ld4(su + 2 * kChan);
-            const float4 hp = (t >= 1) ? ld4(su + 3 * kChan) : h0v;
-            const float4 a = make_float4(expf(c.x), expf(c.y), expf(c.z), expf(c.w));
-            const float4 lam = make_float4(gg.x + nx.x, gg.y + nx.y, gg.z + nx.z, gg.w + nx.w);
-            nx = make_float4(a.x * lam.x, a.y * lam.y, a.z * lam.z, a.w * lam.w);
-            if (active) {
-                const int64_t o = out0 + t * D;
-                st_cs4(dlv + o, make_float4(lam.x * expf(v.x), lam.y * expf(v.y), lam.z * expf(v.z),
-                                            lam.w * expf(v.w)));
-                st_cs4(dlc + o, make_float4(nx.x * hp.x, nx.y * hp.y, nx.z * hp.z, nx.w * hp.w));
+        const float *st = ring + size_t(s) * R::STAGEF + 4 * lane;
+#pragma unroll
+        for (int u = 0; u < kBwdTS; ++u) {
+            if (u < n) {
+                const int64_t t = tt - u;
+                const int q = (kBwdTS - 1 - u) * kChan;
+                const float4 c = ld4(st + q), v = ld4(st + R::BOXF + q), gg = ld4(st + 2 * R::BOXF + q);
+                const float4 hp = (t >= 1) ? ld4(st + 3 * R::BOXF + q) : h0v;
+                const float4 a = make_float4(ex2_approx(c.x * kLog2e), ex2_approx(c.y * kLog2e),
+                                             ex2_approx(c.z * kLog2e), ex2_approx(c.w * kLog2e));
+                const float4 lam = make_float4(gg.x + nx.x, gg.y + nx.y, gg.z + nx.z, gg.w + nx.w);
+                nx = make_float4(a.x * lam.x, a.y * lam.y, a.z * lam.z, a.w * lam.w);
+                if (active) {
+                    const int64_t o = out0 + t * D;
+                    st_cs4(dlv + o, make_float4(lam.x * ex2_approx(v.x * kLog2e), lam.y * ex2_approx(v.y * kLog2e),
+                                                lam.z * ex2_approx(v.z * kLog2e), lam.w * ex2_approx(v.w * kLog2e)));
+                    st_cs4(dlc + o, make_float4(nx.x * hp.x, nx.y * hp.y, nx.z * hp.z, nx.w * hp.w));
+                }
             }
         }
         __syncwarp();
@@ -230,28 +252,36 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 cudaError_t launch_psl_fwd(const float *lc, const float *lv, const float *lh0, float *h,
                            float *logh, int64_t B, int64_t T, int64_t D, const DevCtl &ctl,
                            cudaStream_t s) {
-    using L = PslLayout<2, kFwdTS, kFwdNS>;
+    using R = PslRing<2, kFwdTS, kFwdNS>;
+    CUtensorMap tC, tV;
+    cudaError_t e;
+    if ((e = make_rows_map(&tC, lc, B * T, D, kFwdTS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tV, lv, B * T, D, kFwdTS)) != cudaSuccess) return e;
     const int64_t gpb = (D + kChan - 1) / kChan;
-    const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)psl_fwd_kernel, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t blocks = (B * gpb + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    psl_fwd_kernel<<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(lc, lv, lh0, h, logh, B, T, D, gpb, ctl);
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)psl_fwd_kernel, smem)) != cudaSuccess) return e;
+    psl_fwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tC, tV, lh0, h, logh, B, T, D, gpb, ctl);
     return cudaGetLastError();
 }
 
 cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, const float *h,
                            const float *gh, float *dlc, float *dlv, float *dlh0, int64_t B,
                            int64_t T, int64_t D, const DevCtl &ctl, cudaStream_t s) {
-    using L = PslLayout<4, kBwdTS, kBwdNS>;
+    using R = PslRing<4, kBwdTS, kBwdNS>;
+    CUtensorMap tC, tV, tG, tH;
+    cudaError_t e;
+    if ((e = make_rows_map(&tC, lc, B * T, D, kBwdTS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tV, lv, B * T, D, kBwdTS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tG, gh, B * T, D, kBwdTS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tH, h, B * T, D, kBwdTS)) != cudaSuccess) return e;
     const int64_t gpb = (D + kChan - 1) / kChan;
-    const int smem = int(L::warp_bytes * kWarpsPerBlock);
-    cudaError_t e = ensure_smem_attr((const void *)psl_bwd_kernel, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t blocks = (B * gpb + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    psl_bwd_kernel<<<dim3(unsigned(blocks)), kWarpsPerBlock * 32, smem, s>>>(lc, lv, lh0, h, gh, dlc, dlv, dlh0, B, T, D, gpb, ctl);
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)psl_bwd_kernel, smem)) != cudaSuccess) return e;
+    psl_bwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tC, tV, tG, tH, lh0, dlc, dlv, dlh0, B, T, D, gpb, ctl);
     return cudaGetLastError();
 }
 
