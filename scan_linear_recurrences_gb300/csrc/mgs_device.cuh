@@ -83,6 +83,31 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     }
 }
 
+// Flag publication for cross-warp carries: data stores, then a gpu-scope
+// fence by every writer lane, then one release store of the flag; readers
+// acquire the flag (each reading lane on its own) before touching the data.
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *flag is nonzero; returns the value, or 0 after the timeout.
+__device__ __forceinline__ unsigned wait_flag_bounded(const unsigned *flag, uint64_t timeout_ns) {
+    unsigned v = ld_acquire_gpu(flag);
+    if (v != 0) return v;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        __nanosleep(64);
+        v = ld_acquire_gpu(flag);
+        if (v != 0) return v;
+        if (global_ns() - t0 > timeout_ns) return 0;
+    }
+}
+
 // L2 eviction hint for data streamed once.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -310,33 +310,527 @@ cudaError_t ms_bwd_t(const float *A, const float *P, const float *G, float *dA, 
     return cudaGetLastError();
 }
 
-}  // namespace
+// ================================================================ time-chunked path
+// With few lanes (B*H/(32/k) warps well below the SM count) the sequential
+// per-lane loop leaves the GPU idle.  The chunked kernels split T into C
+// chunks of L steps; one warp handles one (lane group, chunk) item:
+//   pass 1  the chunk's aggregate from the identity (forward: the product
+//           A_end...A_start; backward: the affine map mu_out = M mu_in + C),
+//   publish the aggregate, then decoupled look-back (Merrill & Garland 2016)
+//           over the predecessors' flags to get the carry, publish the
+//           inclusive value,
+//   pass 2  the exact recurrence from the carry, writing outputs.
+// Items are taken from an atomic ticket in carry order (all chunk-0 items,
+// then chunk 1, ...), so every item waited on belongs to a warp that is
+// already running: the look-back always makes progress.  Waits are bounded
+// and report ERR_FLAG_TIMEOUT instead of hanging.  Pass 2 re-reads the
+// chunk's inputs a few microseconds after pass 1, from L2.
 
-size_t ms_workspace_bytes(int64_t, int64_t, int64_t, int, bool) { return 0; }
+template <int K>
+struct MsChunkShape {
+    static constexpr int LPW = 32 / K;
+    static constexpr int MF = LPW * K * K;
+    static constexpr int FTS = K >= 16 ? 2 : 4;  // steps per stage, forward
+    static constexpr int BTS = 2;                // steps per stage, backward
+    static constexpr int NS = 4;
+    using TM = HeadTile<K * K, LPW>;
+};
 
-cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,
-                          void *, size_t, const DevCtl &ctl, cudaStream_t s) {
-    switch (K) {
-        case 1: return ms_fwd_t<1>(A, P, B, T, H, ctl, s);
-        case 2: return ms_fwd_t<2>(A, P, B, T, H, ctl, s);
-        case 4: return ms_fwd_t<4>(A, P, B, T, H, ctl, s);
-        case 8: return ms_fwd_t<8>(A, P, B, T, H, ctl, s);
-        case 16: return ms_fwd_t<16>(A, P, B, T, H, ctl, s);
-        default: return cudaErrorInvalidValue;
+struct MsPlan {
+    int64_t G;  // lane groups (warps per chunk index)
+    int64_t C;  // chunks per lane group
+    int64_t L;  // chunk length in steps (multiple of 4)
+};
+
+// Shape-only plan (the workspace size must not depend on the device).
+MsPlan ms_plan(int64_t B, int64_t T, int64_t H, int K) {
+    const int64_t lpw = 32 / K;
+    MsPlan p;
+    p.G = B * ((H + lpw - 1) / lpw);
+    p.C = 1;
+    p.L = T;
+    if (p.G >= 256 || T < 64) return p;
+    int64_t c = (1024 + p.G - 1) / p.G;
+    c = min64(c, (T + 31) / 32);
+    if (c < 2) return p;
+    int64_t L = (T + c - 1) / c;
+    L = (L + 3) / 4 * 4;
+    p.L = L;
+    p.C = (T + L - 1) / L;
+    return p;
+}
+
+// Workspace: [ticket | flags (G*C) | nmat matrices of LPW*K*K floats per item]
+struct MsWs {
+    unsigned *ticket, *flags;
+    float *mats;  // mats + (m * items + item) * MF
+    int64_t items;
+    __host__ __device__ static size_t header_bytes(const MsPlan &p) { return align_up(256 + size_t(p.G * p.C) * 4, 256); }
+    static size_t bytes(const MsPlan &p, int K, int nmat) {
+        return header_bytes(p) + size_t(nmat) * size_t(p.G * p.C) * (32 / K) * K * K * 4;
+    }
+    __host__ __device__ MsWs(unsigned char *ws, int64_t items_)
+        : ticket(reinterpret_cast<unsigned *>(ws)), flags(reinterpret_cast<unsigned *>(ws + 256)),
+          mats(nullptr), items(items_) {}
+};
+
+enum : unsigned { FLAG_AGG = 1u, FLAG_INCL = 2u };
+
+// Column `col` of M (lane `sub`'s k x k matrix number m of item) from the
+// workspace, bypassing L1.
+template <int K>
+__device__ __forceinline__ void ld_ws_col(const float *mat, int col, float (&x)[K]) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) x[i] = __ldcg(mat + i * K + col);
+}
+template <int K>
+__device__ __forceinline__ void st_ws_col(float *mat, int col, const float (&x)[K]) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) __stcg(mat + i * K + col, x[i]);
+}
+
+// y = X x, where X is held one column per thread of the k-group (this thread
+// holds column `col` in xc): X goes through the warp's exchange buffer.
+template <int K>
+__device__ __forceinline__ void group_matvec(float *xw, int col, const float (&xc)[K], const float (&x)[K],
+                                             float (&y)[K]) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) xw[i * K + col] = xc[i];
+    __syncwarp();
+    smem_matvec<K>(xw, x, y);
+    __syncwarp();
+}
+
+// Publishes `value` for this item: every lane fences its data, lane 0 releases.
+__device__ __forceinline__ void publish(unsigned *flag, unsigned value, int lane) {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release_gpu(flag, value);
+}
+
+// Lane 0 waits for a nonzero flag (bounded) and every lane acquires it.
+__device__ __forceinline__ unsigned lookback_flag(const unsigned *flag, int lane, const DevCtl &ctl) {
+    unsigned f = 0;
+    if (lane == 0) f = wait_flag_bounded(flag, ctl.timeout_ns);
+    f = __shfl_sync(0xffffffffu, f, 0);
+    if (f != 0) f = ld_acquire_gpu(flag);
+    return f;
+}
+
+template <int K>
+__global__ void __launch_bounds__(32)
+    ms_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P,
+                        unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb,
+                        int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MsChunkShape<K>;
+    constexpr int TS = S::FTS, NS = S::NS, BOXF = TS * S::MF;
+    using Lay = MsLayout<S::MF, TS, NS, S::MF>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    float *xch = reinterpret_cast<float *>(smem_raw + Lay::ring_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + Lay::ring_bytes + Lay::extra_bytes);
+
+    const int lane = threadIdx.x;
+    const int64_t G = B * gpb, items = G * C;
+    MsWs w(ws, items);
+    float *agg = reinterpret_cast<float *>(ws + MsWs::header_bytes(MsPlan{G, C, Lc}));
+    float *incl = agg + items * S::MF;
+    unsigned item = 0;
+    if (lane == 0) item = atomicAdd(w.ticket, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (int64_t(item) >= items) return;
+
+    const int64_t c = int64_t(item) / G, g = int64_t(item) % G;
+    const int64_t bi = g / gpb;
+    const int head0 = int(g % gpb) * S::LPW;
+    const int nl = int(min64(S::LPW, H - head0));
+    const int sub = lane / K, col = lane % K;
+    const bool active = sub < nl;
+    const int64_t tb = c * Lc, len = min64(Lc, T - tb);
+    const int64_t n1 = (len + TS - 1) / TS;
+    const bool two_pass = c > 0;
+    const int64_t nb = two_pass ? 2 * n1 : n1;
+    float *xw = xch + sub * K * K;
+    const int64_t slot = (g * C + c) * S::MF + sub * K * K;
+
+    WarpRing<NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) prefetch_tmap(&tmA);
+    auto block_t0 = [&](int64_t jj) { return tb + ((two_pass && jj >= n1) ? jj - n1 : jj) * TS; };
+    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+        mbar_arrive_expect_tx(&bars[s], uint32_t(BOXF * 4));
+        S::TM::load(ring + size_t(s) * BOXF, &tmA, head0, int(bi * T + block_t0(jj)), &bars[s], pol);
+    };
+    const int npro = int(min64(NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float m[K];  // pass 1: column of the chunk product; pass 2: column of P_t
+#pragma unroll
+    for (int i = 0; i < K; ++i) m[i] = (i == col) ? 1.f : 0.f;
+    float *pout = P + (bi * T * H + head0 + sub) * K * K + col;
+    bool failed = false;
+
+    for (int64_t jj = 0; jj < nb; ++jj) {
+        const int s = int(jj % NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int64_t t0 = block_t0(jj);
+        const int n = int(min64(TS, tb + len - t0));
+        const bool store = !(two_pass && jj < n1);
+        const float *st = ring + size_t(s) * BOXF + sub * K * K;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                float nm[K];
+                smem_matvec<K>(st + u * S::MF, m, nm);
+#pragma unroll
+                for (int i = 0; i < K; ++i) m[i] = nm[i];
+                if (store && active) {
+                    float *dst = pout + (t0 + u) * H * K * K;
+#pragma unroll
+                    for (int i = 0; i < K; ++i) st_cs(dst + i * K, m[i]);
+                }
+            }
+        }
+        __syncwarp();
+        if (jj + NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, jj + NS);
+            }
+            rg.armed(s);
+        }
+        if (two_pass && jj == n1 - 1) {
+            // publish the aggregate, look back for the exclusive prefix E
+            st_ws_col<K>(agg + slot, col, m);
+            publish(&w.flags[g * C + c], FLAG_AGG, lane);
+            float e[K];
+#pragma unroll
+            for (int i = 0; i < K; ++i) e[i] = (i == col) ? 1.f : 0.f;
+            for (int64_t p = c - 1; p >= 0; --p) {
+                const unsigned f = lookback_flag(&w.flags[g * C + p], lane, ctl);
+                if (f == 0) {
+                    failed = true;
+                    break;
+                }
+                const float *X = (f == FLAG_INCL ? incl : agg) + (g * C + p) * S::MF + sub * K * K;
+                float xc[K], ne[K];
+                ld_ws_col<K>(X, col, xc);
+                // E <- E X: column col of E X is E (X e_col)
+                group_matvec<K>(xw, col, e, xc, ne);
+#pragma unroll
+                for (int i = 0; i < K; ++i) e[i] = ne[i];
+                if (f == FLAG_INCL) break;
+            }
+            if (failed) {
+                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
+                rg.drain(ctl, lane);
+                return;
+            }
+            // inclusive = aggregate * E; pass 2 starts from E
+            float inc[K];
+            group_matvec<K>(xw, col, m, e, inc);
+            st_ws_col<K>(incl + slot, col, inc);
+            publish(&w.flags[g * C + c], FLAG_INCL, lane);
+#pragma unroll
+            for (int i = 0; i < K; ++i) m[i] = e[i];
+        }
+    }
+    if (!two_pass) {  // chunk 0: its last P is the inclusive prefix
+        st_ws_col<K>(incl + slot, col, m);
+        publish(&w.flags[g * C + c], FLAG_INCL, lane);
     }
 }
 
-cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G, float *dA,
-                          int64_t B, int64_t T, int64_t H, void *, size_t, const DevCtl &ctl,
-                          cudaStream_t s) {
-    switch (K) {
-        case 1: return ms_bwd_t<1>(A, P, G, dA, B, T, H, ctl, s);
-        case 2: return ms_bwd_t<2>(A, P, G, dA, B, T, H, ctl, s);
-        case 4: return ms_bwd_t<4>(A, P, G, dA, B, T, H, ctl, s);
-        case 8: return ms_bwd_t<8>(A, P, G, dA, B, T, H, ctl, s);
-        case 16: return ms_bwd_t<16>(A, P, G, dA, B, T, H, ctl, s);
-        default: return cudaErrorInvalidValue;
+template <int K>
+__global__ void __launch_bounds__(32)
+    ms_bwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                        const __grid_constant__ CUtensorMap tmP, float *__restrict__ dA,
+                        unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb,
+                        int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MsChunkShape<K>;
+    constexpr int TS = S::BTS, NS = S::NS, BOXF = TS * S::MF;
+    using Lay = MsLayout<3 * S::MF, TS, NS, S::MF>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    float *xch = reinterpret_cast<float *>(smem_raw + Lay::ring_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + Lay::ring_bytes + Lay::extra_bytes);
+
+    const int lane = threadIdx.x;
+    const int64_t G = B * gpb, items = G * C;
+    MsWs w(ws, items);
+    float *aggM = reinterpret_cast<float *>(ws + MsWs::header_bytes(MsPlan{G, C, Lc}));
+    float *aggC = aggM + items * S::MF;
+    float *incl = aggC + items * S::MF;
+    unsigned item = 0;
+    if (lane == 0) item = atomicAdd(w.ticket, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (int64_t(item) >= items) return;
+
+    // carries flow from the end of the sequence: tickets go to the last chunk first
+    const int64_t c = C - 1 - int64_t(item) / G, g = int64_t(item) % G;
+    const int64_t bi = g / gpb;
+    const int head0 = int(g % gpb) * S::LPW;
+    const int nl = int(min64(S::LPW, H - head0));
+    const int sub = lane / K, col = lane % K;
+    const bool active = sub < nl;
+    const int64_t tb = c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t n1 = (len + TS - 1) / TS;
+    const bool two_pass = c < C - 1;
+    const int64_t nb = two_pass ? 2 * n1 : n1;
+    float *xw = xch + sub * K * K;
+    const int64_t slot = (g * C + c) * S::MF + sub * K * K;
+
+    WarpRing<NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmP);
     }
+    // block jb of a pass covers t = te-1-jb*TS down to max(tb, te-(jb+1)*TS);
+    // box rows start at te-(jb+1)*TS, step u at box row TS-1-u.
+    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+        const bool p1 = two_pass && jj < n1;
+        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
+        const int r0 = int(bi * T + te - (jb + 1) * TS);
+        float *st = ring + size_t(s) * 3 * BOXF;
+        mbar_arrive_expect_tx(&bars[s], uint32_t((p1 ? 2 : 3) * BOXF * 4));
+        S::TM::load(st, &tmA, head0, r0, &bars[s], pol);
+        S::TM::load(st + BOXF, &tmG, head0, r0, &bars[s], pol);
+        if (!p1) S::TM::load(st + 2 * BOXF, &tmP, head0, r0 - 1, &bars[s], pol);
+    };
+    const int npro = int(min64(NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mu[K], mm[K];  // pass 1: (C, M) columns of the chunk map; pass 2: mu column
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        mu[i] = 0.f;
+        mm[i] = (i == col) ? 1.f : 0.f;
+    }
+    bool failed = false;
+
+    for (int64_t jj = 0; jj < nb; ++jj) {
+        const int s = int(jj % NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const bool p1 = two_pass && jj < n1;
+        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
+        const int64_t tt = te - 1 - jb * TS;
+        const int n = int(min64(TS, tt - tb + 1));
+        const float *st = ring + size_t(s) * 3 * BOXF;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                const int64_t t = tt - u;
+                const int q = TS - 1 - u;
+                const float *At = st + q * S::MF + sub * K * K;
+                const float *Gt = At + BOXF;
+                float lc[K];
+#pragma unroll
+                for (int i = 0; i < K; ++i) lc[i] = Gt[i * K + col] + mu[i];
+                if (p1) {
+                    float nm[K];
+                    smem_matvec_t<K>(At, lc, mu);
+                    smem_matvec_t<K>(At, mm, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) mm[i] = nm[i];
+                } else {
+                    const float *Pp = At + 2 * BOXF;
+#pragma unroll
+                    for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
+                    __syncwarp();
+                    float lrow[K], darow[K];
+#pragma unroll
+                    for (int jx = 0; jx < K; ++jx) lrow[jx] = xw[col * K + jx];
+                    if (t >= 1) {
+                        smem_matvec<K>(Pp, lrow, darow);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < K; ++x) darow[x] = lrow[x];
+                    }
+                    smem_matvec_t<K>(At, lc, mu);
+                    __syncwarp();
+                    if (active) {
+                        float *dst = dA + ((bi * T + t) * H + head0 + sub) * K * K + col * K;
+                        if constexpr (K >= 4) {
+#pragma unroll
+                            for (int x = 0; x < K / 4; ++x)
+                                st_cs4(dst + 4 * x, make_float4(darow[4 * x], darow[4 * x + 1], darow[4 * x + 2], darow[4 * x + 3]));
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < K; ++x) st_cs(dst + x, darow[x]);
+                        }
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (jj + NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, jj + NS);
+            }
+            rg.armed(s);
+        }
+        if (two_pass && jj == n1 - 1) {
+            // publish (M, C); look back towards the end for mu_in
+            st_ws_col<K>(aggM + slot, col, mm);
+            st_ws_col<K>(aggC + slot, col, mu);
+            publish(&w.flags[g * C + c], FLAG_AGG, lane);
+            float macc[K], cacc[K];
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                macc[i] = (i == col) ? 1.f : 0.f;
+                cacc[i] = 0.f;
+            }
+            float muin[K];
+            for (int64_t p = c + 1; p < C; ++p) {
+                const unsigned f = lookback_flag(&w.flags[g * C + p], lane, ctl);
+                if (f == 0) {
+                    failed = true;
+                    break;
+                }
+                const int64_t ps = (g * C + p) * S::MF + sub * K * K;
+                if (f == FLAG_INCL) {
+                    float xc[K], y[K];
+                    ld_ws_col<K>(incl + ps, col, xc);
+                    group_matvec<K>(xw, col, macc, xc, y);  // Macc * mu_out(p)
+#pragma unroll
+                    for (int i = 0; i < K; ++i) muin[i] = y[i] + cacc[i];
+                    break;
+                }
+                float mp[K], cp[K], y1[K], y2[K];
+                ld_ws_col<K>(aggM + ps, col, mp);
+                ld_ws_col<K>(aggC + ps, col, cp);
+#pragma unroll
+                for (int i = 0; i < K; ++i) xw[i * K + col] = macc[i];
+                __syncwarp();
+                smem_matvec<K>(xw, cp, y1);  // Macc C_p
+                smem_matvec<K>(xw, mp, y2);  // Macc M_p
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < K; ++i) {
+                    cacc[i] = y1[i] + cacc[i];
+                    macc[i] = y2[i];
+                }
+            }
+            if (failed) {
+                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
+                rg.drain(ctl, lane);
+                return;
+            }
+            // mu_out = M mu_in + C
+            float y[K], out[K];
+            group_matvec<K>(xw, col, mm, muin, y);
+#pragma unroll
+            for (int i = 0; i < K; ++i) out[i] = y[i] + mu[i];
+            st_ws_col<K>(incl + slot, col, out);
+            publish(&w.flags[g * C + c], FLAG_INCL, lane);
+#pragma unroll
+            for (int i = 0; i < K; ++i) mu[i] = muin[i];
+        }
+    }
+    if (!two_pass) {  // last chunk: its final mu is mu_out
+        st_ws_col<K>(incl + slot, col, mu);
+        publish(&w.flags[g * C + c], FLAG_INCL, lane);
+    }
+}
+
+template <int K>
+cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const MsPlan &pl,
+                           unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
+    using S = MsChunkShape<K>;
+    using Lay = MsLayout<S::MF, S::FTS, S::NS, S::MF>;
+    CUtensorMap tA;
+    cudaError_t e;
+    if ((e = S::TM::make(&tA, A, B * T, H, S::FTS)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, MsWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    const int smem = int(Lay::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)ms_fwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
+    const int64_t items = pl.G * pl.C;
+    ms_fwd_chunk_kernel<K><<<dim3(unsigned(items)), 32, smem, s>>>(tA, P, ws, B, T, H, (H + S::LPW - 1) / S::LPW,
+                                                                   pl.C, pl.L, ctl);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float *dA, int64_t B, int64_t T,
+                           int64_t H, const MsPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
+    using S = MsChunkShape<K>;
+    using Lay = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF>;
+    CUtensorMap tA, tG, tP;
+    cudaError_t e;
+    if ((e = S::TM::make(&tA, A, B * T, H, S::BTS)) != cudaSuccess) return e;
+    if ((e = S::TM::make(&tG, G, B * T, H, S::BTS)) != cudaSuccess) return e;
+    if ((e = S::TM::make(&tP, P, B * T, H, S::BTS)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, MsWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    const int smem = int(Lay::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)ms_bwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
+    const int64_t items = pl.G * pl.C;
+    ms_bwd_chunk_kernel<K><<<dim3(unsigned(items)), 32, smem, s>>>(tA, tG, tP, dA, ws, B, T, H,
+                                                                   (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd) {
+    const MsPlan p = ms_plan(B, T, H, K);
+    if (p.C <= 1) return 0;
+    return MsWs::bytes(p, K, bwd ? 3 : 2);
+}
+
+#define MS_DISPATCH(K_, CALL)            \
+    switch (K_) {                        \
+        case 1: return CALL(1);          \
+        case 2: return CALL(2);          \
+        case 4: return CALL(4);          \
+        case 8: return CALL(8);          \
+        case 16: return CALL(16);        \
+        default: return cudaErrorInvalidValue; \
+    }
+
+cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,
+                          void *ws, size_t, const DevCtl &ctl, cudaStream_t s) {
+    const MsPlan pl = ms_plan(B, T, H, K);
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    if (pl.C > 1) {
+#define CALL_FC(k) ms_fwd_chunk_t<k>(A, P, B, T, H, pl, w, ctl, s)
+        MS_DISPATCH(K, CALL_FC)
+#undef CALL_FC
+    }
+#define CALL_F(k) ms_fwd_t<k>(A, P, B, T, H, ctl, s)
+    MS_DISPATCH(K, CALL_F)
+#undef CALL_F
+}
+
+cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G, float *dA,
+                          int64_t B, int64_t T, int64_t H, void *ws, size_t, const DevCtl &ctl,
+                          cudaStream_t s) {
+    const MsPlan pl = ms_plan(B, T, H, K);
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    if (pl.C > 1) {
+#define CALL_BC(k) ms_bwd_chunk_t<k>(A, P, G, dA, B, T, H, pl, w, ctl, s)
+        MS_DISPATCH(K, CALL_BC)
+#undef CALL_BC
+    }
+#define CALL_B(k) ms_bwd_t<k>(A, P, G, dA, B, T, H, ctl, s)
+    MS_DISPATCH(K, CALL_B)
+#undef CALL_B
 }
 
 }  // namespace mgs

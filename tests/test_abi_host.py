@@ -90,6 +90,20 @@ def test_workspace_size_queries(L):
     for op in range(1, 7):
         assert b.mgs_workspace_size(op, 2, 16, 8, 8) >= 0
     assert b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, -1, 16, 8, 8) == 0
+    # many lanes or short sequences: single pass, no workspace
+    assert b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, 128, 64, 8, 8) == 0
+    # few lanes, long sequence: time chunks exchange carries through the workspace
+    nf = b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, 16, 1024, 8, 8)
+    nb = b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_BWD, 16, 1024, 8, 8)
+    assert 0 < nf < nb
+
+
+def test_workspace_errors(L):
+    A, P = FAKE, FAKE + (1 << 30)
+    n = b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, 16, 1024, 8, 8)
+    assert _st(b.mgs_matrix_scan_fwd, A, P, 16, 1024, 8, 8, None, 0) == b.MGS_ERR_WORKSPACE
+    assert _st(b.mgs_matrix_scan_fwd, A, P, 16, 1024, 8, 8, FAKE + (3 << 30), n - 1) == b.MGS_ERR_WORKSPACE
+    assert _st(b.mgs_matrix_scan_fwd, A, P, 16, 1024, 8, 8, FAKE + (3 << 30) + 16, n) == b.MGS_ERR_WORKSPACE
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

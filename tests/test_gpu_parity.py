@@ -113,10 +113,26 @@ def test_ms_config2_full():
 
 
 @pytest.mark.parametrize("B,T,H,k", [
-    (1, 1, 1, 8), (2, 13, 5, 8), (2, 21, 3, 4), (2, 17, 3, 16), (1, 40, 2, 2), (2, 30, 8, 1), (1, 333, 2, 8),
+    (1, 1, 1, 8), (2, 13, 5, 8), (2, 21, 3, 4), (2, 17, 3, 16), (1, 40, 2, 2), (2, 30, 8, 1),
+    # long sequences with few lanes take the time-chunked look-back path
+    (1, 333, 2, 8), (2, 1000, 3, 4), (1, 515, 3, 16), (1, 257, 4, 1), (1, 130, 2, 2), (3, 4099, 5, 8),
 ])
 def test_ms_shapes(B, T, H, k):
     _run_ms(B, T, H, k, seed=200 + B * T + H + k)
+
+
+def test_ms_chunked_repeat_reuses_workspace():
+    """Two calls in a row on one workspace (flags and ticket are re-zeroed per call)."""
+    d = _cuda(inputs.ms_inputs(2, 700, 4, 8, seed=17))
+    n = b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, 2, 700, 4, 8)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    P1 = torch.empty_like(d["A"]); P2 = torch.empty_like(d["A"])
+    b.mgs_matrix_scan_fwd(d["A"], P1, 2, 700, 4, 8, ws, n)
+    b.mgs_matrix_scan_fwd(d["A"], P2, 2, 700, 4, 8, ws, n)
+    b.mgs_check()
+    assert torch.equal(P1, P2)
+    assert_close("P", P1, oracle.ms_fwd(d["A"].cpu()), 700)
 
 
 # ---------------------------------------------------------------- parallel_scan_log
