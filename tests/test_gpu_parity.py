@@ -122,7 +122,9 @@ def test_ms_shapes(B, T, H, k):
 
 
 def test_ms_chunked_repeat_reuses_workspace():
-    """Two calls in a row on one workspace (flags and ticket are re-zeroed per call)."""
+    """Two calls in a row on one workspace (flags and ticket are re-zeroed per
+    call).  The look-back combines whichever predecessor value is ready first,
+    so the two results agree to rounding, not bit for bit."""
     d = _cuda(inputs.ms_inputs(2, 700, 4, 8, seed=17))
     n = b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, 2, 700, 4, 8)
     assert n > 0
@@ -131,8 +133,10 @@ def test_ms_chunked_repeat_reuses_workspace():
     b.mgs_matrix_scan_fwd(d["A"], P1, 2, 700, 4, 8, ws, n)
     b.mgs_matrix_scan_fwd(d["A"], P2, 2, 700, 4, 8, ws, n)
     b.mgs_check()
-    assert torch.equal(P1, P2)
-    assert_close("P", P1, oracle.ms_fwd(d["A"].cpu()), 700)
+    ref = oracle.ms_fwd(d["A"].cpu())
+    assert_close("P first call", P1, ref, 700)
+    assert_close("P second call", P2, ref, 700)
+    assert_close("P calls agree", P2, P1.double().cpu().numpy(), 700, rel_tol=2e-6)
 
 
 # ---------------------------------------------------------------- parallel_scan_log
