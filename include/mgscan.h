@@ -112,6 +112,32 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
 mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,
                                void *workspace, size_t workspace_bytes, mgs_stream_t stream);
 
+/* Size of the device scratch array behind mgs_matrix_scan_fwd_noalloc. */
+#define MGS_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* matrix_scan forward that allocates nothing and takes no workspace.
+ * No counterpart on the mingru-scans pages: this entry point exists for callers
+ * that hold only their input and output buffers and cannot call cudaMalloc,
+ * for instance a host program whose device memory is owned by another
+ * runtime's pool allocator (a raw cudaMalloc there fails or fragments the
+ * pool), or a latency-bound loop that cannot afford the device-wide
+ * synchronisation cudaMalloc/cudaFree imply.
+ * Same operation, layouts and results as mgs_matrix_scan_fwd, without the
+ * workspace arguments.  When the shape needs scratch (few lanes, long
+ * sequence: see mgs_workspace_size with MGS_OP_MATRIX_SCAN_FWD), it uses a
+ * file-scope device array of MGS_NOALLOC_SCRATCH_BYTES inside the library
+ * instead; every GPU that loads the library holds that array until the
+ * process exits.  Shapes needing more
+ * scratch than that return MGS_ERR_WORKSPACE and do nothing.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture.
+ * All calls on a device share the one array, which keeps the previous call's
+ * contents; each call clears the part that must start at zero (an async
+ * memset on `stream`).  Calls that overlap on the GPU, e.g. on two unordered
+ * streams, race on the array: order them. */
+mgs_status mgs_matrix_scan_fwd_noalloc(const float *A, float *P, int64_t B, int64_t T, int64_t H,
+                                       int k, mgs_stream_t stream);
+
 /* matrix_scan, backward: gradient of L = sum_t <grad_P_t, P_t>_F.  With
  * Lambda_t = dL/dP_t,
  *     Lambda_T = grad_P_T,   Lambda_t = grad_P_t + A_{t+1}^T Lambda_{t+1},

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "mgs_matrix_affine_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_matrix_affine_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_matrix_scan_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
+    "mgs_matrix_scan_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "mgs_matrix_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_parallel_scan_log_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "mgs_parallel_scan_log_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
@@ -129,6 +130,15 @@ def mgs_matrix_affine_scan_bwd(A, h0, h, grad_h, dA, db, dh0, B, T, H, k, worksp
 def mgs_matrix_scan_fwd(A, P, B, T, H, k, workspace=None, workspace_bytes=0, stream=None):
     return _call("mgs_matrix_scan_fwd", _ptr(A), _ptr(P), B, T, H, k, _ptr(workspace), workspace_bytes,
                  _stream(stream))
+
+
+def mgs_matrix_scan_fwd_noalloc(A, P, B, T, H, k, stream=None):
+    """matrix_scan forward using the library's built-in device scratch; for
+    callers that cannot allocate device memory (see include/mgscan.h)."""
+    return _call("mgs_matrix_scan_fwd_noalloc", _ptr(A), _ptr(P), B, T, H, k, _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20  # MGS_NOALLOC_SCRATCH_BYTES in include/mgscan.h
 
 
 def mgs_matrix_scan_bwd(A, P, grad_P, dA, B, T, H, k, workspace=None, workspace_bytes=0, stream=None):

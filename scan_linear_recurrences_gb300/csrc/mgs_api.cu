@@ -236,6 +236,21 @@ mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, i
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mgs_status mgs_matrix_scan_fwd_noalloc(const float *A, float *P, int64_t B, int64_t T, int64_t H,
+                                       int k, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.mat == 0) return MGS_OK;
+    if ((st = check_ptrs({A, P}, {})) != MGS_OK) return st;
+    if (!disjoint({{P, s.mat}}, {{A, s.mat}})) return MGS_ERR_INVALID_ARG;
+    if (mgs::ms_workspace_bytes(B, T, H, k, false) > mgs::ms_static_scratch_bytes()) return MGS_ERR_WORKSPACE;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_ms_fwd_static_scratch(k, A, P, B, T, H, ctl,
+                                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mgs_status mgs_matrix_scan_bwd(const float *A, const float *P, const float *grad_P, float *dA,
                                int64_t B, int64_t T, int64_t H, int k, void *workspace,
                                size_t workspace_bytes, mgs_stream_t stream) {

@@ -21,6 +21,12 @@ cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);
 cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,
                           void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
+// matrix_scan forward with the library's own static device scratch (see
+// mgs_matrix_scan_fwd_noalloc); returns cudaErrorInvalidValue if the shape
+// needs more scratch than the array holds.
+cudaError_t launch_ms_fwd_static_scratch(int K, const float *A, float *P, int64_t B, int64_t T,
+                                         int64_t H, const DevCtl &ctl, cudaStream_t s);
+size_t ms_static_scratch_bytes();
 cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G, float *dA,
                           int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes,
                           const DevCtl &ctl, cudaStream_t s);

@@ -7,6 +7,9 @@
 // (backward), so the k x k product per step is a broadcast read of A_t from
 // shared memory and k^2 register FMAs with no shuffles.  Inputs stream through
 // the same per-warp TMA bulk-copy ring as matrix_affine_scan.
+#include <mutex>
+
+#include "../../include/mgscan.h"
 #include "mgs_tiles.cuh"
 
 namespace mgs {
@@ -831,6 +834,52 @@ cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G,
 #define CALL_B(k) ms_bwd_t<k>(A, P, G, dA, B, T, H, ctl, s)
     MS_DISPATCH(K, CALL_B)
 #undef CALL_B
+}
+
+}  // namespace mgs
+
+// ================================================================ no-allocation scratch
+// Scratch for mgs_matrix_scan_fwd_noalloc: one file-scope array per device
+// context that loads the library.  Host code never uses the array's name as
+// an address (in host code it is only a stand-in); the device address comes
+// from cudaGetSymbolAddress, looked up once per device with that device
+// current, and is passed to the kernel like any caller workspace.
+namespace {
+static __device__ __align__(256) unsigned char g_ms_noalloc_scratch[MGS_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mu;
+unsigned char *g_scratch_addr[64] = {};
+
+cudaError_t noalloc_scratch_address(unsigned char **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_ms_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_addr[dev] = static_cast<unsigned char *>(p);
+    }
+    *out = g_scratch_addr[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+namespace mgs {
+
+size_t ms_static_scratch_bytes() { return MGS_NOALLOC_SCRATCH_BYTES; }
+
+cudaError_t launch_ms_fwd_static_scratch(int K, const float *A, float *P, int64_t B, int64_t T,
+                                         int64_t H, const DevCtl &ctl, cudaStream_t s) {
+    const size_t need = ms_workspace_bytes(B, T, H, K, false);
+    if (need == 0) return launch_ms_fwd(K, A, P, B, T, H, nullptr, 0, ctl, s);
+    if (need > MGS_NOALLOC_SCRATCH_BYTES) return cudaErrorInvalidValue;
+    unsigned char *scratch = nullptr;
+    cudaError_t e = noalloc_scratch_address(&scratch);
+    if (e != cudaSuccess) return e;
+    return launch_ms_fwd(K, A, P, B, T, H, scratch, MGS_NOALLOC_SCRATCH_BYTES, ctl, s);
 }
 
 }  // namespace mgs
