@@ -67,28 +67,71 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# sources each kernel family is built from (a change to any of them makes
+# recorded ncu counters stale)
+KERNEL_SOURCES = {"mas": ["mgs_mas.cu"], "ms": ["mgs_ms.cu"], "psl": ["mgs_psl.cu"]}
+COMMON_SOURCES = ["mgs_device.cuh", "mgs_tiles.cuh", "mgs_launch.h"]
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash(op):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scan_linear_recurrences_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[op] + COMMON_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, only if
-    it was taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+def committed_traffic(op, key):
+    """DRAM bytes per launch of kernel `key` from the committed ncu record, only
+    if it was taken on the current sources of that kernel family."""
     try:
-        with open(p) as f:
+        with open(TRAFFIC_JSON) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash():
+    e = d.get("kernels", {}).get(key)
+    if e is None or e.get("source_hash") != kernel_source_hash(op):
         return None
-    e = d.get("kernels", {}).get(kernel)
-    return None if e is None else e.get("dram_bytes_per_launch")
+    return e.get("dram_bytes_per_launch")
+
+
+def record_traffic(csv_path, rows, workloads):
+    """Turns an ncu CSV (dram__bytes_read/write.sum per launch, taken with
+    --batch-rows `rows`) into profiles/traffic.json, scaling each kernel's
+    bytes to a full launch by the batch rows processed."""
+    import csv
+    from scan_linear_recurrences_gb300 import inputs
+    with open(csv_path) as f:
+        table = list(csv.reader(f))
+    hi = next(i for i, r in enumerate(table) if "Kernel Name" in r)
+    hdr = table[hi]
+    ki, mi, vi = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value")
+    by_op = {inputs.WORKLOADS[i].op: inputs.WORKLOADS[i] for i in workloads}
+    acc = {}
+    for r in table[hi + 1:]:
+        if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        name = r[ki].split("(")[0].split("::")[-1].split("<")[0].strip()
+        op = name.split("_")[0]
+        w = by_op[op]
+        key = f"{name}@c{w.cid}"
+        acc.setdefault(key, {"op": op, "w": w, "read": [], "write": []})
+        acc[key]["read" if "read" in r[mi] else "write"].append(float(r[vi].replace(",", "")))
+    out = {"how": f"ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum on --batch-rows {rows}, "
+                  "scaled to the full batch; writes still dirty in L2 at kernel end are not counted",
+           "kernels": {}}
+    for key, a in acc.items():
+        w = a["w"]
+        scale = w.B / min(w.B, rows)
+        rd, wr = statistics.mean(a["read"]), statistics.mean(a["write"])
+        out["kernels"][key] = {"dram_bytes_per_launch": round((rd + wr) * scale),
+                               "read_bytes": round(rd * scale), "write_bytes": round(wr * scale),
+                               "source_hash": kernel_source_hash(a["op"]), "scale": scale}
+    with open(TRAFFIC_JSON, "w") as f:
+        json.dump(out, f, indent=1)
+    return out
 
 
 # ---------------------------------------------------------------- clocks
@@ -317,8 +360,9 @@ def run_gpu(args):
 
     kname, kms, kbytes, kw, kdir = dominant
     achieved = kbytes / (kms * 1e-3) / 1e9
-    kernel_symbol = {"mas": "mas", "ms": "ms", "psl": "psl"}[kw.op] + f"_{kdir}_kernel"
-    traffic = committed_traffic(f"{kernel_symbol}@c{kw.cid}")
+    chunked = kw.op == "ms" and b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, kw.B, kw.T, kw.H, kw.k) > 0
+    kernel_symbol = f"{kw.op}_{kdir}_{'chunk_' if chunked else ''}kernel"
+    traffic = committed_traffic(kw.op, f"{kernel_symbol}@c{kw.cid}")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": kernel_symbol, "workload": kw.name,
@@ -353,7 +397,7 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(runners, budget_s=args.cpu_budget)
+        cpu = cpu_baseline(runners, min_s=args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -404,27 +448,30 @@ def _sample_rows(w, budget_rows):
     return max(1, min(w.B, budget_rows.get(w.cid, w.B)))
 
 
-# rows of each workload the CPU leg processes (bounded: roughly 10-30 s on 16 cores)
-CPU_ROWS = {1: 128, 2: 16, 3: 8, 4: 4}
+# batch rows of each workload one CPU pass processes; passes repeat until the
+# CPU leg has run for at least `min_s` seconds (about 10-30 s in total)
+CPU_ROWS = {1: 128, 2: 16, 3: 16, 4: 8}
 
 
-def cpu_baseline(runners, budget_s=30.0, rows=None):
+def cpu_baseline(runners, min_s=10.0, rows=None):
     import oracle
     from dataclasses import replace
     rows = rows or CPU_ROWS
-    total_b, total_t, parts = 0, 0.0, []
+    samples = []
     for r in runners:
         w = r.w
         n = _sample_rows(w, rows)
-        s = _oracle_sample(w, n, r.inp)
-        ws = replace(w, B=n)
-        dt = _time_oracle(ws, s)
-        nb = op_bytes(ws, "fwd") + op_bytes(ws, "bwd")
-        total_b += nb
-        total_t += dt
-        parts.append(f"{w.op}_c{w.cid}: {n}/{w.B} batch rows ({dt:.2f} s)")
+        samples.append((replace(w, B=n), _oracle_sample(w, n, r.inp), w))
+    total_b, total_t, passes = 0, 0.0, 0
+    while total_t < min_s and passes < 50:
+        for ws, s, _ in samples:
+            total_t += _time_oracle(ws, s)
+            total_b += op_bytes(ws, "fwd") + op_bytes(ws, "bwd")
+        passes += 1
+    parts = [f"{w.op}_c{w.cid}: {ws.B}/{w.B} batch rows" for ws, _, w in samples]
     return {"value": round(total_b / total_t / 1e9, 3), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": "; ".join(parts) + "; float64 oracle, OpenMP over lanes",
+            "kind": "oracle",
+            "sample": "; ".join(parts) + f"; {passes} passes of fwd+bwd; float64 oracle, OpenMP over lanes",
             "seconds": round(total_t, 2)}
 
 
@@ -478,10 +525,16 @@ def main():
     ap.add_argument("--workloads", default=",".join(str(i) for i in WORKLOAD_IDS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum CPU-baseline time")
     ap.add_argument("--batch-rows", type=int, default=0,
                     help="profiling: cap every workload's batch rows (smaller case, same kernels)")
+    ap.add_argument("--record-traffic", default=None,
+                    help="write profiles/traffic.json from this ncu CSV (taken with --batch-rows)")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.batch_rows,
+                                        [int(x) for x in args.workloads.split(",")]), indent=1))
+        return
     if args.warmup < 3 and args.impl != "reference":
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
