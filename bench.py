@@ -182,6 +182,24 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ---------------------------------------------------------------- multi-rank aggregation
+def max_over_ranks(x, world, device="cpu"):
+    """Largest value of x across the ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes_per_rank, world, ms_step_max):
+    """Weak scaling: every rank processes its own copy of the step's work, so
+    the job moves world * step_bytes in the slowest rank's step time."""
+    return step_bytes_per_rank * world / (ms_step_max * 1e-3) / 1e9
+
+
 # ---------------------------------------------------------------- GPU arm
 class Runner:
     """Holds one workload's device buffers and runs its fwd / bwd calls."""
@@ -326,17 +344,11 @@ def run_gpu(args):
         bw = [ev[r.w.cid][1].elapsed_time(ev[r.w.cid][2]) for ev in all_evs]
         per[r.w.cid] = (f, bw)
     step_ms = [sum(per[c][0][i] + per[c][1][i] for c in per) for i in range(args.steps)]
-    local_ms = statistics.mean(step_ms)
-    if world > 1:
-        tt = torch.tensor([local_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    else:
-        ms_step = local_ms
+    ms_step = max_over_ranks(statistics.mean(step_ms), world, device)
 
     peak, peak_kind = measured_peak()
     step_bytes = sum(op_bytes(r.w, "fwd") + op_bytes(r.w, "bwd") for r in runners)
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbps(step_bytes, world, ms_step)
 
     ops = {}
     dominant = None
@@ -385,13 +397,9 @@ def run_gpu(args):
                 r.e2e_step(sid)
         ev1.record(stream)
         barrier()
-        e2e_ms = ev0.elapsed_time(ev1) / n_e2e
-        if world > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / n_e2e, world, device)
         b.mgs_check(sid)
-        e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        e2e = {"value": round(whole_job_gbps(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                "h2d_bytes_per_step": sum(r.h2d for r in runners), "d2h_bytes_per_step": sum(r.d2h for r in runners),
                "ms_per_step": round(e2e_ms, 3)}
 
