@@ -71,13 +71,14 @@ def measured_peak():
 # recorded ncu counters stale)
 KERNEL_SOURCES = {"mas": ["mgs_mas.cu"], "ms": ["mgs_ms.cu"], "psl": ["mgs_psl.cu"]}
 COMMON_SOURCES = ["mgs_device.cuh", "mgs_tiles.cuh", "mgs_launch.h"]
+CHUNK_SOURCES = {"ms": ["mgs_chunk.cuh"], "mas": ["mgs_chunk.cuh"], "psl": []}
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
 def kernel_source_hash(op):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "scan_linear_recurrences_gb300", "csrc")
-    for f in KERNEL_SOURCES[op] + COMMON_SOURCES:
+    for f in KERNEL_SOURCES[op] + CHUNK_SOURCES[op] + COMMON_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

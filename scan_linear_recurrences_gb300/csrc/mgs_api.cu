@@ -170,6 +170,10 @@ extern "C" {
 size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
     BlockSizes s;
     switch (op) {
+        case MGS_OP_MATRIX_AFFINE_SCAN_FWD:
+        case MGS_OP_MATRIX_AFFINE_SCAN_BWD:
+            if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
+            return mgs::mas_workspace_bytes(B, T, H_or_D, k);
         case MGS_OP_MATRIX_SCAN_FWD:
         case MGS_OP_MATRIX_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
@@ -188,10 +192,11 @@ mgs_status mgs_matrix_affine_scan_fwd(const float *A, const float *b, const floa
     if (s.vec == 0) return MGS_OK;
     if ((st = check_ptrs({A, b, h}, {h0})) != MGS_OK) return st;
     if (!disjoint({{h, s.vec}}, {{A, s.mat}, {b, s.vec}, {h0, h0 ? s.init : 0}})) return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::mas_workspace_bytes(B, T, H, k), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_mas_fwd(k, A, b, h0, h, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(mgs::launch_mas_fwd(k, A, b, h0, h, B, T, H, workspace, workspace_bytes, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const float *h,
@@ -213,11 +218,11 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
     if (!disjoint({{dA, s.mat}, {db, s.vec}, {dh0, dh0 ? s.init : 0}},
                   {{A, s.mat}, {h0, h0 ? s.init : 0}, {h, s.vec}, {grad_h, s.vec}}))
         return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::mas_workspace_bytes(B, T, H, k), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_mas_bwd(k, A, h0, h, grad_h, dA, db, dh0, B, T, H, ctl,
-                                         reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(mgs::launch_mas_bwd(k, A, h0, h, grad_h, dA, db, dh0, B, T, H, workspace, workspace_bytes,
+                                         ctl, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,

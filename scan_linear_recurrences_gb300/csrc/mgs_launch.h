@@ -11,11 +11,14 @@
 namespace mgs {
 
 // matrix_affine_scan
+size_t mas_workspace_bytes(int64_t B, int64_t T, int64_t H, int K);
 cudaError_t launch_mas_fwd(int K, const float *A, const float *b, const float *h0, float *h,
-                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+                           int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes,
+                           const DevCtl &ctl, cudaStream_t s);
 cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *h,
                            const float *gh, float *dA, float *db, float *dh0, int64_t B,
-                           int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+                           int64_t T, int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl,
+                           cudaStream_t s);
 
 // matrix_scan
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);

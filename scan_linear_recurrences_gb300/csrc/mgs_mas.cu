@@ -14,7 +14,7 @@
 //    lambda_t[i] h_{t-1}^T and the next mu_t = A_t^T lambda_t (a butterfly
 //    reduce-scatter over the group, k-1 shuffles) all come from registers, so
 //    nothing beyond the outputs is written.
-#include "mgs_tiles.cuh"
+#include "mgs_chunk.cuh"
 
 namespace mgs {
 namespace {
@@ -326,31 +326,454 @@ cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const flo
     return cudaGetLastError();
 }
 
+// ================================================================ time-chunked path
+// Few lanes and a long sequence: T is split into C chunks and one warp handles
+// one (lane group, chunk) item, as for matrix_scan.  The forward aggregate of a
+// chunk is the affine map h_end = M h_in + c with M = A_e ... A_s (built one
+// column per thread: M[:, j] <- A_t M[:, j], broadcast reads of A_t, no
+// shuffles) and c the chunk's own recurrence from h = 0.  The backward
+// aggregate is mu_out = M mu_in + C with M = A_s^T ... A_e^T.  The look-back
+// keeps its running map by rows (thread r holds row r), reading each
+// predecessor's (M, c) or inclusive value straight from the workspace (L2).
+// Workspace slots per item: 0 = M, 1 = c (first LPW*k floats), 2 = inclusive.
+
+template <int K>
+struct MasChunkShape {
+    static constexpr int LPW = 32 / K;
+    static constexpr int AF = LPW * K * K, VF = LPW * K;
+    static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? 8 : 16);
+    static constexpr int NS = 4;
+    using TA = HeadTile<K * K, LPW>;
+    using TV = HeadTile<K, LPW>;
+};
+
+template <int STAGEF, int NS, int XF>
+struct ChunkRing {
+    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);
+    static constexpr size_t ring_bytes = NS * stage_bytes;
+    static constexpr size_t xch_offset = ring_bytes;
+    static constexpr size_t bar_offset = align_up(ring_bytes + size_t(XF) * sizeof(float), 16);
+    static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128);
+};
+
+// Look-back for a row-held affine carry.  On return `hin` (this thread's row
+// element) is the carry entering the item; `dir` = -1 walks to earlier chunks
+// (forward scan), +1 to later chunks (backward scan).  Returns false on timeout.
+template <int K>
+__device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t c, int dir, int sub, int r,
+                                int lane, const DevCtl &ctl, float &hin) {
+    float macc[K];
+#pragma unroll
+    for (int m = 0; m < K; ++m) macc[m] = (m == r) ? 1.f : 0.f;
+    float vacc = 0.f;
+    for (int64_t p = c + dir; p >= 0 && p < C; p += dir) {
+        const int64_t ip = g * C + p;
+        const unsigned f = lookback_flag(&w.flags[ip], lane, ctl);
+        if (f == 0) return false;
+        if (f == FLAG_INCL) {
+            const float *hp = w.slot(2, ip) + sub * K;
+            float acc = vacc;
+#pragma unroll
+            for (int m = 0; m < K; ++m) acc = fmaf(macc[m], __ldcg(hp + m), acc);
+            hin = acc;
+            return true;
+        }
+        const float *Mp = w.slot(0, ip) + sub * K * K;
+        const float *cp = w.slot(1, ip) + sub * K;
+        float nrow[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) nrow[j] = 0.f;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            vacc = fmaf(macc[m], __ldcg(cp + m), vacc);
+#pragma unroll
+            for (int j = 0; j < K; ++j) nrow[j] = fmaf(macc[m], __ldcg(Mp + m * K + j), nrow[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) macc[j] = nrow[j];
+    }
+    hin = vacc;  // no predecessor in that direction: the carry is the identity's offset (zero)
+    return true;
+}
+
+// Inclusive value of this item: out[r] = sum_m M[r][m] hin[m] + cv, with M held
+// by columns (mcol) and hin by rows; both go through the exchange buffer.
+template <int K>
+__device__ __forceinline__ float affine_apply(float *xw, int r, int gbase, const float (&mcol)[K], float hin,
+                                              float cv) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) xw[i * K + r] = mcol[i];
+    __syncwarp();
+    float acc = cv;
+#pragma unroll
+    for (int m = 0; m < K; ++m) acc = fmaf(xw[r * K + m], __shfl_sync(0xffffffffu, hin, gbase + m), acc);
+    __syncwarp();
+    return acc;
+}
+
+template <int K>
+__global__ void __launch_bounds__(32)
+    mas_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const float *__restrict__ h0, float *__restrict__ h, unsigned char *__restrict__ ws,
+                         int64_t B, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MasChunkShape<K>;
+    constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
+    using R = ChunkRing<STAGEF, S::NS, S::AF>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    float *xch = reinterpret_cast<float *>(smem_raw + R::xch_offset);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::bar_offset);
+
+    const int lane = threadIdx.x;
+    const int64_t G = B * gpb;
+    const ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::AF);
+    unsigned item = 0;
+    if (lane == 0) item = atomicAdd(w.ticket, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (int64_t(item) >= G * C) return;
+
+    const int64_t c = int64_t(item) / G, g = int64_t(item) % G, iself = g * C + c;
+    const int64_t bi = g / gpb;
+    const int head0 = int(g % gpb) * S::LPW;
+    const int nl = int(min64(S::LPW, H - head0));
+    const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
+    const bool active = sub < nl;
+    const int64_t tb = c * Lc, len = min64(Lc, T - tb);
+    const int64_t n1 = (len + S::TS - 1) / S::TS;
+    const bool two_pass = c > 0;
+    const int64_t nb = two_pass ? 2 * n1 : n1;
+    float *xw = xch + sub * K * K;
+
+    WarpRing<S::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    auto block_t0 = [&](int64_t jj) { return tb + ((two_pass && jj >= n1) ? jj - n1 : jj) * S::TS; };
+    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+        float *st = ring + size_t(s) * STAGEF;
+        const int row = int(bi * T + block_t0(jj));
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        S::TA::load(st, &tmA, head0, row, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmB, head0, row, &bars[s], pol);
+    };
+    const int npro = int(min64(S::NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float cv = 0.f;  // pass 1: row r of the chunk offset c
+    float mcol[K];   // pass 1: column r of the chunk matrix M
+#pragma unroll
+    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
+    float hprev = (!two_pass && h0 != nullptr && active) ? h0[(bi * H + head0 + sub) * K + r] : 0.f;
+    const int64_t hstride = H * K;
+
+    for (int64_t jj = 0; jj < nb; ++jj) {
+        const int s = int(jj % S::NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int64_t t0 = block_t0(jj);
+        const int n = int(min64(S::TS, tb + len - t0));
+        const bool p1 = two_pass && jj < n1;
+        const float *st = ring + size_t(s) * STAGEF;
+#pragma unroll
+        for (int u = 0; u < S::TS; ++u) {
+            if (u < n) {
+                const float *Ablk = st + u * S::AF + sub * K * K;
+                float a[K];
+                lds_row<K>(Ablk + r * K, a);
+                const float bval = st[A_STAGE + u * S::VF + sub * K + r];
+                const float x_in = p1 ? cv : hprev;
+                float acc0 = bval, acc1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < K; ++j) {
+                    const float x = __shfl_sync(0xffffffffu, x_in, gbase + j);
+                    if (j & 1) acc1 = fmaf(a[j], x, acc1);
+                    else acc0 = fmaf(a[j], x, acc0);
+                }
+                if (p1) {
+                    cv = acc0 + acc1;
+                    float nm[K];
+                    smem_matvec<K>(Ablk, mcol, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+                } else {
+                    hprev = acc0 + acc1;
+                    if (active) st_cs(h + (bi * T * H + head0 + sub) * K + r + (t0 + u) * hstride, hprev);
+                }
+            }
+        }
+        __syncwarp();
+        if (jj + S::NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, jj + S::NS);
+            }
+            rg.armed(s);
+        }
+        if (two_pass && jj == n1 - 1) {
+            st_ws_col<K>(w.slot(0, iself) + sub * K * K, r, mcol);
+            __stcg(w.slot(1, iself) + sub * K + r, cv);
+            publish(&w.flags[iself], FLAG_AGG, lane);
+            float hin = 0.f;
+            if (!lookback_affine<K>(w, g, C, c, -1, sub, r, lane, ctl, hin)) {
+                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
+                rg.drain(ctl, lane);
+                return;
+            }
+            // h at the end of the chunk = M h_in + c
+            const float hend = affine_apply<K>(xw, r, gbase, mcol, hin, cv);
+            __stcg(w.slot(2, iself) + sub * K + r, hend);
+            publish(&w.flags[iself], FLAG_INCL, lane);
+            hprev = hin;
+        }
+    }
+    if (!two_pass) {  // chunk 0: its final state is the inclusive value
+        __stcg(w.slot(2, iself) + sub * K + r, hprev);
+        publish(&w.flags[iself], FLAG_INCL, lane);
+    }
+}
+
+template <int K>
+__global__ void __launch_bounds__(32)
+    mas_bwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                         const __grid_constant__ CUtensorMap tmH, const float *__restrict__ h0,
+                         float *__restrict__ dA, float *__restrict__ db, float *__restrict__ dh0,
+                         unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb, int64_t C,
+                         int64_t Lc, DevCtl ctl) {
+    using S = MasChunkShape<K>;
+    constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
+    constexpr int STAGEF = A_STAGE + 2 * V_STAGE;
+    using R = ChunkRing<STAGEF, S::NS, S::AF>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    float *xch = reinterpret_cast<float *>(smem_raw + R::xch_offset);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::bar_offset);
+
+    const int lane = threadIdx.x;
+    const int64_t G = B * gpb;
+    const ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::AF);
+    unsigned item = 0;
+    if (lane == 0) item = atomicAdd(w.ticket, 1u);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    if (int64_t(item) >= G * C) return;
+
+    // carries flow from the end: tickets go to the last chunk first
+    const int64_t c = C - 1 - int64_t(item) / G, g = int64_t(item) % G, iself = g * C + c;
+    const int64_t bi = g / gpb;
+    const int head0 = int(g % gpb) * S::LPW;
+    const int nl = int(min64(S::LPW, H - head0));
+    const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
+    const bool active = sub < nl;
+    const int64_t tb = c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t n1 = (len + S::TS - 1) / S::TS;
+    const bool two_pass = c < C - 1;
+    const int64_t nb = two_pass ? 2 * n1 : n1;
+    float *xw = xch + sub * K * K;
+
+    WarpRing<S::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmH);
+    }
+    // block jb of a pass covers t = te-1-jb*TS down to max(tb, te-(jb+1)*TS);
+    // boxes start at row te-(jb+1)*TS; the h box one row earlier holds h_{t-1}
+    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+        const bool p1 = two_pass && jj < n1;
+        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
+        const int r0 = int(bi * T + te - (jb + 1) * S::TS);
+        float *st = ring + size_t(s) * STAGEF;
+        mbar_arrive_expect_tx(&bars[s], uint32_t((A_STAGE + (p1 ? 1 : 2) * V_STAGE) * 4));
+        S::TA::load(st, &tmA, head0, r0, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmG, head0, r0, &bars[s], pol);
+        if (!p1) S::TV::load(st + A_STAGE + V_STAGE, &tmH, head0, r0 - 1, &bars[s], pol);
+    };
+    const int npro = int(min64(S::NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mu = 0.f;  // pass 1: row r of the chunk offset C; pass 2: (A_{t+1}^T lambda_{t+1})[r]
+    float mcol[K];   // pass 1: column r of M = A_s^T ... A_e^T
+#pragma unroll
+    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
+    const int64_t hk = H * K;
+    float *dbp = db + (bi * T * H + head0 + sub) * K + r;
+    float *dAp = dA + (bi * T * H + head0 + sub) * K * K + r * K;
+
+    for (int64_t jj = 0; jj < nb; ++jj) {
+        const int s = int(jj % S::NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const bool p1 = two_pass && jj < n1;
+        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
+        const int64_t tt = te - 1 - jb * S::TS;
+        const int n = int(min64(S::TS, tt - tb + 1));
+        const float *st = ring + size_t(s) * STAGEF;
+#pragma unroll
+        for (int u = 0; u < S::TS; ++u) {
+            if (u < n) {
+                const int64_t t = tt - u;
+                const int q = S::TS - 1 - u;
+                const float *Ablk = st + q * S::AF + sub * K * K;
+                const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
+                float a[K];
+                lds_row<K>(Ablk + r * K, a);
+                float p[K];
+#pragma unroll
+                for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
+                mu = group_reduce_scatter<K>(p, r);
+                if (p1) {
+                    float nm[K];
+                    smem_matvec_t<K>(Ablk, mcol, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+                } else {
+                    float hp[K];
+                    if (t >= 1) {
+                        lds_row<K>(st + A_STAGE + V_STAGE + q * S::VF + sub * K, hp);
+                    } else if (h0 != nullptr && active) {
+#pragma unroll
+                        for (int x = 0; x < K; ++x) hp[x] = h0[(bi * H + head0 + sub) * K + x];
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < K; ++x) hp[x] = 0.f;
+                    }
+                    float dar[K];
+#pragma unroll
+                    for (int x = 0; x < K; ++x) dar[x] = lam * hp[x];
+                    if (active) {
+                        st_cs(dbp + t * hk, lam);
+                        stg_row_cs<K>(dAp + t * hk * K, dar);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (jj + S::NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, jj + S::NS);
+            }
+            rg.armed(s);
+        }
+        if (two_pass && jj == n1 - 1) {
+            st_ws_col<K>(w.slot(0, iself) + sub * K * K, r, mcol);
+            __stcg(w.slot(1, iself) + sub * K + r, mu);
+            publish(&w.flags[iself], FLAG_AGG, lane);
+            float muin = 0.f;
+            if (!lookback_affine<K>(w, g, C, c, +1, sub, r, lane, ctl, muin)) {
+                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
+                rg.drain(ctl, lane);
+                return;
+            }
+            const float muout = affine_apply<K>(xw, r, gbase, mcol, muin, mu);
+            __stcg(w.slot(2, iself) + sub * K + r, muout);
+            publish(&w.flags[iself], FLAG_INCL, lane);
+            mu = muin;
+        }
+    }
+    if (!two_pass) {  // last chunk: its final mu is the inclusive value
+        __stcg(w.slot(2, iself) + sub * K + r, mu);
+        publish(&w.flags[iself], FLAG_INCL, lane);
+    }
+    if (c == 0 && dh0 != nullptr && active) dh0[(bi * H + head0 + sub) * K + r] = mu;
+}
+
+template <int K>
+cudaError_t mas_fwd_chunk_t(const float *A, const float *b, const float *h0, float *h, int64_t B, int64_t T,
+                            int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
+    using S = MasChunkShape<K>;
+    using R = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::AF>;
+    CUtensorMap tA, tB;
+    cudaError_t e;
+    if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tB, b, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_fwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_fwd_chunk_kernel<K><<<dim3(unsigned(pl.G * pl.C)), 32, smem, s>>>(tA, tB, h0, h, ws, B, T, H,
+                                                                          (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
+    return cudaGetLastError();
+}
+
+template <int K>
+cudaError_t mas_bwd_chunk_t(const float *A, const float *h0, const float *h, const float *gh, float *dA,
+                            float *db, float *dh0, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
+                            unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
+    using S = MasChunkShape<K>;
+    using R = ChunkRing<S::TS * (S::AF + 2 * S::VF), S::NS, S::AF>;
+    CUtensorMap tA, tG, tH;
+    cudaError_t e;
+    if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tG, gh, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tH, h, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    const int smem = int(R::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_bwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_bwd_chunk_kernel<K><<<dim3(unsigned(pl.G * pl.C)), 32, smem, s>>>(
+        tA, tG, tH, h0, dA, db, dh0, ws, B, T, H, (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_mas_fwd(int K, const float *A, const float *b, const float *h0, float *h,
-                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
-    switch (K) {
-        case 1: return mas_fwd_t<1>(A, b, h0, h, B, T, H, ctl, s);
-        case 2: return mas_fwd_t<2>(A, b, h0, h, B, T, H, ctl, s);
-        case 4: return mas_fwd_t<4>(A, b, h0, h, B, T, H, ctl, s);
-        case 8: return mas_fwd_t<8>(A, b, h0, h, B, T, H, ctl, s);
-        case 16: return mas_fwd_t<16>(A, b, h0, h, B, T, H, ctl, s);
-        default: return cudaErrorInvalidValue;
+size_t mas_workspace_bytes(int64_t B, int64_t T, int64_t H, int K) {
+    const ChunkPlan p = plan_chunks(B, T, H, K);
+    if (p.C <= 1) return 0;
+    return ChunkWs::bytes(p, K, 3);
+}
+
+#define MAS_DISPATCH(K_, CALL)                 \
+    switch (K_) {                              \
+        case 1: return CALL(1);                \
+        case 2: return CALL(2);                \
+        case 4: return CALL(4);                \
+        case 8: return CALL(8);                \
+        case 16: return CALL(16);              \
+        default: return cudaErrorInvalidValue; \
     }
+
+cudaError_t launch_mas_fwd(int K, const float *A, const float *b, const float *h0, float *h,
+                           int64_t B, int64_t T, int64_t H, void *ws, size_t, const DevCtl &ctl,
+                           cudaStream_t s) {
+    const ChunkPlan pl = plan_chunks(B, T, H, K);
+    if (pl.C > 1) {
+        unsigned char *w = static_cast<unsigned char *>(ws);
+#define CALL_FC(k) mas_fwd_chunk_t<k>(A, b, h0, h, B, T, H, pl, w, ctl, s)
+        MAS_DISPATCH(K, CALL_FC)
+#undef CALL_FC
+    }
+#define CALL_F(k) mas_fwd_t<k>(A, b, h0, h, B, T, H, ctl, s)
+    MAS_DISPATCH(K, CALL_F)
+#undef CALL_F
 }
 
 cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *h,
                            const float *gh, float *dA, float *db, float *dh0, int64_t B,
-                           int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
-    switch (K) {
-        case 1: return mas_bwd_t<1>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
-        case 2: return mas_bwd_t<2>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
-        case 4: return mas_bwd_t<4>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
-        case 8: return mas_bwd_t<8>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
-        case 16: return mas_bwd_t<16>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
-        default: return cudaErrorInvalidValue;
+                           int64_t T, int64_t H, void *ws, size_t, const DevCtl &ctl, cudaStream_t s) {
+    const ChunkPlan pl = plan_chunks(B, T, H, K);
+    if (pl.C > 1) {
+        unsigned char *w = static_cast<unsigned char *>(ws);
+#define CALL_BC(k) mas_bwd_chunk_t<k>(A, h0, h, gh, dA, db, dh0, B, T, H, pl, w, ctl, s)
+        MAS_DISPATCH(K, CALL_BC)
+#undef CALL_BC
     }
+#define CALL_B(k) mas_bwd_t<k>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s)
+    MAS_DISPATCH(K, CALL_B)
+#undef CALL_B
 }
 
 }  // namespace mgs

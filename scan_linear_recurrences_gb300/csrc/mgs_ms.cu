@@ -10,7 +10,7 @@
 #include <mutex>
 
 #include "../../include/mgscan.h"
-#include "mgs_tiles.cuh"
+#include "mgs_chunk.cuh"
 
 namespace mgs {
 namespace {
@@ -32,55 +32,6 @@ struct MsLayout {
     static constexpr size_t extra_bytes = size_t(EXTRAF) * sizeof(float);
     static constexpr size_t warp_bytes = align_up(ring_bytes + extra_bytes + NS * sizeof(uint64_t), 128);
 };
-
-// y = M x for a k x k row-major M in shared memory (broadcast reads).
-template <int K>
-__device__ __forceinline__ void smem_matvec(const float *M, const float (&x)[K], float (&y)[K]) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-        float r[K];
-        if constexpr (K >= 4) {
-#pragma unroll
-            for (int c = 0; c < K / 4; ++c) {
-                float4 q = reinterpret_cast<const float4 *>(M + i * K)[c];
-                r[4 * c] = q.x; r[4 * c + 1] = q.y; r[4 * c + 2] = q.z; r[4 * c + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < K; ++c) r[c] = M[i * K + c];
-        }
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int m = 0; m < K; ++m) {
-            if (m & 1) s1 = fmaf(r[m], x[m], s1);
-            else s0 = fmaf(r[m], x[m], s0);
-        }
-        y[i] = s0 + s1;
-    }
-}
-
-// y = M^T x for a k x k row-major M in shared memory: y[m] = sum_i M[i][m] x[i].
-template <int K>
-__device__ __forceinline__ void smem_matvec_t(const float *M, const float (&x)[K], float (&y)[K]) {
-#pragma unroll
-    for (int m = 0; m < K; ++m) y[m] = 0.f;
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-        float r[K];
-        if constexpr (K >= 4) {
-#pragma unroll
-            for (int c = 0; c < K / 4; ++c) {
-                float4 q = reinterpret_cast<const float4 *>(M + i * K)[c];
-                r[4 * c] = q.x; r[4 * c + 1] = q.y; r[4 * c + 2] = q.z; r[4 * c + 3] = q.w;
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < K; ++c) r[c] = M[i * K + c];
-        }
-#pragma unroll
-        for (int m = 0; m < K; ++m) y[m] = fmaf(r[m], x[i], y[m]);
-    }
-}
 
 // ---------------------------------------------------------------- forward
 template <int K>
@@ -339,87 +290,6 @@ struct MsChunkShape {
     using TM = HeadTile<K * K, LPW>;
 };
 
-struct MsPlan {
-    int64_t G;  // lane groups (warps per chunk index)
-    int64_t C;  // chunks per lane group
-    int64_t L;  // chunk length in steps (multiple of 4)
-};
-
-// Shape-only plan (the workspace size must not depend on the device).
-MsPlan ms_plan(int64_t B, int64_t T, int64_t H, int K) {
-    const int64_t lpw = 32 / K;
-    MsPlan p;
-    p.G = B * ((H + lpw - 1) / lpw);
-    p.C = 1;
-    p.L = T;
-    if (p.G >= 256 || T < 64) return p;
-    int64_t c = (1024 + p.G - 1) / p.G;
-    c = min64(c, (T + 31) / 32);
-    if (c < 2) return p;
-    int64_t L = (T + c - 1) / c;
-    L = (L + 3) / 4 * 4;
-    p.L = L;
-    p.C = (T + L - 1) / L;
-    return p;
-}
-
-// Workspace: [ticket | flags (G*C) | nmat matrices of LPW*K*K floats per item]
-struct MsWs {
-    unsigned *ticket, *flags;
-    float *mats;  // mats + (m * items + item) * MF
-    int64_t items;
-    __host__ __device__ static size_t header_bytes(const MsPlan &p) { return align_up(256 + size_t(p.G * p.C) * 4, 256); }
-    static size_t bytes(const MsPlan &p, int K, int nmat) {
-        return header_bytes(p) + size_t(nmat) * size_t(p.G * p.C) * (32 / K) * K * K * 4;
-    }
-    __host__ __device__ MsWs(unsigned char *ws, int64_t items_)
-        : ticket(reinterpret_cast<unsigned *>(ws)), flags(reinterpret_cast<unsigned *>(ws + 256)),
-          mats(nullptr), items(items_) {}
-};
-
-enum : unsigned { FLAG_AGG = 1u, FLAG_INCL = 2u };
-
-// Column `col` of M (lane `sub`'s k x k matrix number m of item) from the
-// workspace, bypassing L1.
-template <int K>
-__device__ __forceinline__ void ld_ws_col(const float *mat, int col, float (&x)[K]) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) x[i] = __ldcg(mat + i * K + col);
-}
-template <int K>
-__device__ __forceinline__ void st_ws_col(float *mat, int col, const float (&x)[K]) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) __stcg(mat + i * K + col, x[i]);
-}
-
-// y = X x, where X is held one column per thread of the k-group (this thread
-// holds column `col` in xc): X goes through the warp's exchange buffer.
-template <int K>
-__device__ __forceinline__ void group_matvec(float *xw, int col, const float (&xc)[K], const float (&x)[K],
-                                             float (&y)[K]) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) xw[i * K + col] = xc[i];
-    __syncwarp();
-    smem_matvec<K>(xw, x, y);
-    __syncwarp();
-}
-
-// Publishes `value` for this item: every lane fences its data, lane 0 releases.
-__device__ __forceinline__ void publish(unsigned *flag, unsigned value, int lane) {
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release_gpu(flag, value);
-}
-
-// Lane 0 waits for a nonzero flag (bounded) and every lane acquires it.
-__device__ __forceinline__ unsigned lookback_flag(const unsigned *flag, int lane, const DevCtl &ctl) {
-    unsigned f = 0;
-    if (lane == 0) f = wait_flag_bounded(flag, ctl.timeout_ns);
-    f = __shfl_sync(0xffffffffu, f, 0);
-    if (f != 0) f = ld_acquire_gpu(flag);
-    return f;
-}
-
 template <int K>
 __global__ void __launch_bounds__(32)
     ms_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P,
@@ -435,8 +305,8 @@ __global__ void __launch_bounds__(32)
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb, items = G * C;
-    MsWs w(ws, items);
-    float *agg = reinterpret_cast<float *>(ws + MsWs::header_bytes(MsPlan{G, C, Lc}));
+    ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::MF);
+    float *agg = w.slot(0, 0);
     float *incl = agg + items * S::MF;
     unsigned item = 0;
     if (lane == 0) item = atomicAdd(w.ticket, 1u);
@@ -567,8 +437,8 @@ __global__ void __launch_bounds__(32)
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb, items = G * C;
-    MsWs w(ws, items);
-    float *aggM = reinterpret_cast<float *>(ws + MsWs::header_bytes(MsPlan{G, C, Lc}));
+    ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::MF);
+    float *aggM = w.slot(0, 0);
     float *aggC = aggM + items * S::MF;
     float *incl = aggC + items * S::MF;
     unsigned item = 0;
@@ -754,14 +624,14 @@ __global__ void __launch_bounds__(32)
 }
 
 template <int K>
-cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const MsPlan &pl,
+cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
                            unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
     using Lay = MsLayout<S::MF, S::FTS, S::NS, S::MF>;
     CUtensorMap tA;
     cudaError_t e;
     if ((e = S::TM::make(&tA, A, B * T, H, S::FTS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, MsWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
     const int smem = int(Lay::warp_bytes);
     if ((e = ensure_smem_attr((const void *)ms_fwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
     const int64_t items = pl.G * pl.C;
@@ -772,7 +642,7 @@ cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64
 
 template <int K>
 cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float *dA, int64_t B, int64_t T,
-                           int64_t H, const MsPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
+                           int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
     using Lay = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF>;
     CUtensorMap tA, tG, tP;
@@ -780,7 +650,7 @@ cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float
     if ((e = S::TM::make(&tA, A, B * T, H, S::BTS)) != cudaSuccess) return e;
     if ((e = S::TM::make(&tG, G, B * T, H, S::BTS)) != cudaSuccess) return e;
     if ((e = S::TM::make(&tP, P, B * T, H, S::BTS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, MsWs::header_bytes(pl), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
     const int smem = int(Lay::warp_bytes);
     if ((e = ensure_smem_attr((const void *)ms_bwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
     const int64_t items = pl.G * pl.C;
@@ -792,9 +662,9 @@ cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float
 }  // namespace
 
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd) {
-    const MsPlan p = ms_plan(B, T, H, K);
+    const ChunkPlan p = plan_chunks(B, T, H, K);
     if (p.C <= 1) return 0;
-    return MsWs::bytes(p, K, bwd ? 3 : 2);
+    return ChunkWs::bytes(p, K, bwd ? 3 : 2);
 }
 
 #define MS_DISPATCH(K_, CALL)            \
@@ -809,7 +679,7 @@ size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd) {
 
 cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,
                           void *ws, size_t, const DevCtl &ctl, cudaStream_t s) {
-    const MsPlan pl = ms_plan(B, T, H, K);
+    const ChunkPlan pl = plan_chunks(B, T, H, K);
     unsigned char *w = static_cast<unsigned char *>(ws);
     if (pl.C > 1) {
 #define CALL_FC(k) ms_fwd_chunk_t<k>(A, P, B, T, H, pl, w, ctl, s)
@@ -824,7 +694,7 @@ cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T,
 cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G, float *dA,
                           int64_t B, int64_t T, int64_t H, void *ws, size_t, const DevCtl &ctl,
                           cudaStream_t s) {
-    const MsPlan pl = ms_plan(B, T, H, K);
+    const ChunkPlan pl = plan_chunks(B, T, H, K);
     unsigned char *w = static_cast<unsigned char *>(ws);
     if (pl.C > 1) {
 #define CALL_BC(k) ms_bwd_chunk_t<k>(A, P, G, dA, B, T, H, pl, w, ctl, s)

@@ -62,9 +62,18 @@ def test_mas_configs_full(cid):
     (2, 50, 6, 2, "normal"),
     (2, 81, 12, 1, "normal"),   # k = 1: the diagonal (linear_scan) case
     (1, 300, 4, 8, "none"),
+    # few lanes, long sequences: the time-chunked look-back path
+    (1, 1000, 3, 16, "normal"), (2, 515, 5, 4, "normal"), (1, 2048, 8, 8, "none"), (3, 4099, 2, 2, "normal"),
 ])
 def test_mas_shapes(B, T, H, k, h0):
     _run_mas(B, T, H, k, seed=100 + B * T + H + k, h0_mode=h0)
+
+
+def test_mas_long_T_shape_of_the_pages():
+    """The pages' long-T benchmark shape (B=16, T=1024) with d=64 as H=8 blocks
+    of k=8: 32 lane groups, so the sequence is split into time chunks."""
+    assert b.mgs_workspace_size(b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, 16, 1024, 8, 8) > 0
+    _run_mas(16, 1024, 8, 8, seed=4242, h0_mode="normal")
 
 
 def test_mas_config4_sampled_rows():
@@ -137,6 +146,28 @@ def test_ms_chunked_repeat_reuses_workspace():
     assert_close("P first call", P1, ref, 700)
     assert_close("P second call", P2, ref, 700)
     assert_close("P calls agree", P2, P1.double().cpu().numpy(), 700, rel_tol=2e-6)
+
+
+@pytest.mark.timeout(300)
+def test_chunked_lookback_repeated_calls_stay_correct():
+    """Many back-to-back chunked calls: a predecessor's flag may advance from
+    aggregate to inclusive while a warp reads it; every call must still finish
+    and match the oracle."""
+    B, T, H, k = 2, 2050, 3, 8
+    dm = _cuda(inputs.mas_inputs(B, T, H, k, seed=77, h0="normal"))
+    ds = _cuda(inputs.ms_inputs(B, T, H, k, seed=78))
+    href = oracle.mas_fwd(dm["A"].cpu(), dm["b"].cpu(), dm["h0"].cpu())
+    dAr, _, _ = oracle.mas_bwd(dm["A"].cpu(), dm["b"].cpu(), dm["h0"].cpu(), dm["grad_h"].cpu())
+    Pref = oracle.ms_fwd(ds["A"].cpu())
+    for _ in range(25):
+        h = api.matrix_affine_scan_fwd(dm["A"], dm["b"], dm["h0"])
+        dA, _, _ = api.matrix_affine_scan_bwd(dm["A"], dm["h0"], h, dm["grad_h"])
+        P = api.matrix_scan_fwd(ds["A"])
+        dAs = api.matrix_scan_bwd(ds["A"], P, ds["grad_P"])
+    b.mgs_check()
+    assert_close("h", h, href, T)
+    assert_close("dA", dA, dAr, T)
+    assert_close("P", P, Pref, T)
 
 
 # ---------------------------------------------------------------- parallel_scan_log
