@@ -404,6 +404,32 @@ def run_gpu(args):
                "h2d_bytes_per_step": sum(r.h2d for r in runners), "d2h_bytes_per_step": sum(r.d2h for r in runners),
                "ms_per_step": round(e2e_ms, 3)}
 
+    extra = {}
+    if not args.no_extra:
+        for w in inputs.EXTRA_WORKLOADS.values():
+            r = Runner(w, torch, b, api, device)
+            fs, bs = [], []
+            for it in range(args.warmup + 10):
+                flush.zero_()
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+                r.fwd(sid)
+                e1.record(stream)
+                r.bwd(sid)
+                e2.record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    fs.append(e0.elapsed_time(e1))
+                    bs.append(e1.elapsed_time(e2))
+            fm, bm = statistics.median(fs), statistics.median(bs)
+            nbytes = op_bytes(w, "fwd") + op_bytes(w, "bwd")
+            extra[f"{w.op}_c{w.cid}"] = {"shape": w.name, "fwd_us": round(fm * 1e3, 2), "bwd_us": round(bm * 1e3, 2),
+                                         "fwd_bwd_us": round((fm + bm) * 1e3, 2),
+                                         "fwd_bwd_GBps": round(nbytes / ((fm + bm) * 1e-3) / 1e9, 1),
+                                         "l2": "flushed"}
+            del r
+        b.mgs_check(sid)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(runners, min_s=args.cpu_seconds)
@@ -416,7 +442,7 @@ def run_gpu(args):
             "config": {"workload": " + ".join(r.w.name for r in runners) + ", fwd+bwd each",
                        "l2": "flushed before the two L2-resident shapes; the others exceed L2",
                        "step_bytes": step_bytes, "wall_s_timed_region": round(wall, 4)},
-            "ops": ops, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "ops": ops, "extra_ops_not_in_step": extra, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * 2 * len(runners), "clocks": clocks,
             "impl": "libmgscan",
         }
@@ -534,6 +560,7 @@ def main():
     ap.add_argument("--workloads", default=",".join(str(i) for i in WORKLOAD_IDS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the report-only extra shapes")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum CPU-baseline time")
     ap.add_argument("--batch-rows", type=int, default=0,
                     help="profiling: cap every workload's batch rows (smaller case, same kernels)")

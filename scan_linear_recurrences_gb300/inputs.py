@@ -195,3 +195,10 @@ WORKLOADS = {
     3: Workload(3, "psl", "parallel_scan_log minGRU B=64 T=4096 D=1024", 64, 4096, 1024, 1, "log"),
     4: Workload(4, "mas", "matrix_affine_scan scaled B=32 T=8192 H=64 k=8", 32, 8192, 64, 8, "normal"),
 }
+
+# The pages' other benchmark shapes (lab B=128 T=64, long-T B=16 T=1024) for the
+# ops the table above covers at one shape only; reported beside the step.
+EXTRA_WORKLOADS = {
+    5: Workload(5, "mas", "matrix_affine_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "normal"),
+    6: Workload(6, "ms", "matrix_scan lab Givens B=128 T=64 H=8 k=8", 128, 64, 8, 8, "none"),
+}
