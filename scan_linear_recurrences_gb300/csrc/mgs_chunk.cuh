@@ -64,7 +64,9 @@ struct ChunkPlan {
 
 // Shape-only plan (the workspace size must not depend on the device): chunk
 // only when there are fewer than 256 lane groups and T >= 64, aiming at about
-// 1024 (group, chunk) items with chunks of at least 32 steps.
+// 1024 (group, chunk) items, with chunks of 32 to 64 steps so that the second
+// pass over a chunk, a few microseconds after the first, still finds its
+// inputs in L2 (about a thousand resident items x 64 KB stays well inside L2).
 __host__ __device__ inline ChunkPlan plan_chunks(int64_t B, int64_t T, int64_t H, int K) {
     const int64_t lpw = 32 / K;
     ChunkPlan p;
@@ -72,13 +74,16 @@ __host__ __device__ inline ChunkPlan plan_chunks(int64_t B, int64_t T, int64_t H
     p.C = 1;
     p.L = T;
     if (p.G >= 256 || T < 64) return p;
-    int64_t c = (1024 + p.G - 1) / p.G;
-    c = min64(c, (T + 31) / 32);
-    if (c < 2) return p;
-    int64_t L = (T + c - 1) / c;
+    const int64_t c0 = (1024 + p.G - 1) / p.G;
+    int64_t L = (T + c0 - 1) / c0;
+    L = L < 32 ? 32 : (L > 64 ? 64 : L);
     L = (L + 3) / 4 * 4;
     p.L = L;
     p.C = (T + L - 1) / L;
+    if (p.C < 2) {
+        p.C = 1;
+        p.L = T;
+    }
     return p;
 }
 
@@ -159,6 +164,91 @@ __device__ __forceinline__ unsigned lookback_flag(const unsigned *flag, int lane
         }
     }
     return __all_sync(0xffffffffu, ok) ? f : 0u;
+}
+
+// Windowed look-back.  Scans the items of one lane group before (dir = -1) or
+// after (dir = +1) chunk c, 32 at a time (lane j reads the flag of chunk
+// c + dir*(1 + j)), for the nearest one whose inclusive value is published,
+// waiting (bounded) until every chunk between it and c has published at least
+// its aggregate.  Returns that chunk index, or -1 after the timeout; the result
+// is uniform across the warp.  Each lane acquires the flag it reads and the
+// closing __syncwarp (which orders memory among the warp's lanes) lets every
+// lane read the data of all the chunks in the window.
+__device__ __forceinline__ int64_t find_inclusive(const unsigned *flags, int64_t c, int dir, int64_t C, int lane,
+                                                  const DevCtl &ctl) {
+    const uint64_t t0 = global_ns();
+    for (int64_t base = c + dir; base >= 0 && base < C; base += int64_t(dir) * 32) {
+        const int64_t p = base + int64_t(dir) * lane;
+        const bool valid = p >= 0 && p < C;
+        unsigned f = valid ? ld_acquire_gpu(flags + p) : 0u;
+        while (true) {
+            const unsigned incl = __ballot_sync(0xffffffffu, valid && f == FLAG_INCL);
+            const int first = incl ? __ffs(int(incl)) - 1 : 32;
+            const bool need = valid && lane < first;
+            const unsigned missing = __ballot_sync(0xffffffffu, need && f == 0u);
+            if (missing == 0u) {
+                if (first < 32) {
+                    __syncwarp();
+                    return base + int64_t(dir) * first;
+                }
+                break;  // 32 aggregates: look further
+            }
+            const bool late = (lane == 0) && (global_ns() - t0 > ctl.timeout_ns);
+            if (__any_sync(0xffffffffu, late)) return -1;
+            __nanosleep(64);
+            if (need && f == 0u) f = ld_acquire_gpu(flags + p);
+        }
+    }
+    return -1;
+}
+
+// K consecutive floats from global memory through L2 (16-byte loads when K >= 4).
+template <int K>
+__device__ __forceinline__ void lds_row_global(const float *p, float (&r)[K]) {
+    if constexpr (K >= 4) {
+#pragma unroll
+        for (int c = 0; c < K / 4; ++c) {
+            const float4 q = __ldcg(reinterpret_cast<const float4 *>(p) + c);
+            r[4 * c] = q.x; r[4 * c + 1] = q.y; r[4 * c + 2] = q.z; r[4 * c + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < K; ++c) r[c] = __ldcg(p + c);
+    }
+}
+
+// K consecutive floats from shared memory (16-byte loads when K >= 4).
+template <int K>
+__device__ __forceinline__ void lds_row_smem(const float *p, float (&r)[K]) {
+    if constexpr (K >= 4) {
+#pragma unroll
+        for (int c = 0; c < K / 4; ++c) {
+            const float4 q = reinterpret_cast<const float4 *>(p)[c];
+            r[4 * c] = q.x; r[4 * c + 1] = q.y; r[4 * c + 2] = q.z; r[4 * c + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < K; ++c) r[c] = p[c];
+    }
+}
+
+// k x k row-major matrix from the workspace into registers (L2, 16-byte loads).
+template <int K>
+__device__ __forceinline__ void ld_ws_mat(const float *m, float (&r)[K][K]) {
+    if constexpr (K >= 4) {
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+#pragma unroll
+            for (int c = 0; c < K / 4; ++c) {
+                const float4 q = __ldcg(reinterpret_cast<const float4 *>(m + i * K) + c);
+                r[i][4 * c] = q.x; r[i][4 * c + 1] = q.y; r[i][4 * c + 2] = q.z; r[i][4 * c + 3] = q.w;
+            }
+    } else {
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+#pragma unroll
+            for (int j = 0; j < K; ++j) r[i][j] = __ldcg(m + i * K + j);
+    }
 }
 
 }  // namespace mgs

@@ -356,43 +356,42 @@ struct ChunkRing {
     static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128);
 };
 
-// Look-back for a row-held affine carry.  On return `hin` (this thread's row
-// element) is the carry entering the item; `dir` = -1 walks to earlier chunks
-// (forward scan), +1 to later chunks (backward scan).  Returns false on timeout.
+// Look-back for a row-held affine carry.  Finds the nearest chunk in direction
+// `dir` (-1: earlier, forward scan; +1: later, backward scan) whose inclusive
+// value is published, then applies the aggregates (M_p, c_p) of the chunks
+// between it and this one, nearest to it first: x <- M_p x + c_p.  Thread r
+// holds row element r; each step needs row r of M_p and x gathered across the
+// k-group.  The next chunk's row is loaded while the current one is applied.
+// Returns false (uniformly) on timeout.
 template <int K>
 __device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t c, int dir, int sub, int r,
-                                int lane, const DevCtl &ctl, float &hin) {
-    float macc[K];
-#pragma unroll
-    for (int m = 0; m < K; ++m) macc[m] = (m == r) ? 1.f : 0.f;
-    float vacc = 0.f;
-    for (int64_t p = c + dir; p >= 0 && p < C; p += dir) {
-        const int64_t ip = g * C + p;
-        const unsigned f = lookback_flag(&w.flags[ip], lane, ctl);
-        if (f == 0) return false;
-        if (f == FLAG_INCL) {
-            const float *hp = w.slot(2, ip) + sub * K;
-            float acc = vacc;
-#pragma unroll
-            for (int m = 0; m < K; ++m) acc = fmaf(macc[m], __ldcg(hp + m), acc);
-            hin = acc;
-            return true;
-        }
-        const float *Mp = w.slot(0, ip) + sub * K * K;
-        const float *cp = w.slot(1, ip) + sub * K;
-        float nrow[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) nrow[j] = 0.f;
-#pragma unroll
-        for (int m = 0; m < K; ++m) {
-            vacc = fmaf(macc[m], __ldcg(cp + m), vacc);
-#pragma unroll
-            for (int j = 0; j < K; ++j) nrow[j] = fmaf(macc[m], __ldcg(Mp + m * K + j), nrow[j]);
-        }
-#pragma unroll
-        for (int j = 0; j < K; ++j) macc[j] = nrow[j];
+                                int gbase, int lane, const DevCtl &ctl, float &hin) {
+    const int64_t ps = find_inclusive(w.flags + g * C, c, dir, C, lane, ctl);
+    if (ps < 0) return false;
+    float x = __ldcg(w.slot(2, g * C + ps) + sub * K + r);
+    int64_t p = ps - dir;
+    float mrow[K], cp = 0.f;
+    if (p != c) {
+        lds_row_global<K>(w.slot(0, g * C + p) + sub * K * K + r * K, mrow);
+        cp = __ldcg(w.slot(1, g * C + p) + sub * K + r);
     }
-    hin = vacc;  // no predecessor in that direction: the carry is the identity's offset (zero)
+    while (p != c) {
+        const int64_t pn = p - dir;
+        float nrow[K], ncp = 0.f;
+        if (pn != c) {
+            lds_row_global<K>(w.slot(0, g * C + pn) + sub * K * K + r * K, nrow);
+            ncp = __ldcg(w.slot(1, g * C + pn) + sub * K + r);
+        }
+        float acc = cp;
+#pragma unroll
+        for (int m = 0; m < K; ++m) acc = fmaf(mrow[m], __shfl_sync(0xffffffffu, x, gbase + m), acc);
+        x = acc;
+#pragma unroll
+        for (int m = 0; m < K; ++m) mrow[m] = nrow[m];
+        cp = ncp;
+        p = pn;
+    }
+    hin = x;
     return true;
 }
 
@@ -522,7 +521,7 @@ __global__ void __launch_bounds__(32)
             __stcg(w.slot(1, iself) + sub * K + r, cv);
             publish(&w.flags[iself], FLAG_AGG, lane);
             float hin = 0.f;
-            if (!lookback_affine<K>(w, g, C, c, -1, sub, r, lane, ctl, hin)) {
+            if (!lookback_affine<K>(w, g, C, c, -1, sub, r, gbase, lane, ctl, hin)) {
                 if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
                 rg.drain(ctl, lane);
                 return;
@@ -674,7 +673,7 @@ __global__ void __launch_bounds__(32)
             __stcg(w.slot(1, iself) + sub * K + r, mu);
             publish(&w.flags[iself], FLAG_AGG, lane);
             float muin = 0.f;
-            if (!lookback_affine<K>(w, g, C, c, +1, sub, r, lane, ctl, muin)) {
+            if (!lookback_affine<K>(w, g, C, c, +1, sub, r, gbase, lane, ctl, muin)) {
                 if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
                 rg.drain(ctl, lane);
                 return;

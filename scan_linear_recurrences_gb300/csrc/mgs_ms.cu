@@ -290,6 +290,63 @@ struct MsChunkShape {
     using TM = HeadTile<K * K, LPW>;
 };
 
+// Applies, starting from the inclusive value X0 (k x k, row-major, this lane's
+// slot in the workspace), the aggregates of chunks p = p_first, p_first+step,
+// ... up to (not including) p_end: X <- M_p X (+ C_p when Cs is given), where
+// M_p = Ms[(item0 + p) * mf] and C_p likewise.  Thread i of the k-group keeps
+// row i of X; the rows go through the exchange buffer each step, and row i of
+// the next aggregate is loaded while the current one is applied.  Returns
+// column `col` of the result in out.
+template <int K>
+__device__ void fold_rows(const float *X0, const float *Ms, int64_t mf, int64_t item0, int64_t p_first,
+                          int64_t p_end, int step, const float *Cs, float *xw, int col, float (&out)[K]) {
+    const int i = col;  // this thread's row
+    float xr[K];
+    lds_row_global<K>(X0 + i * K, xr);
+    float mr[K], cr[K];
+    int64_t p = p_first;
+    if (p != p_end) {
+        lds_row_global<K>(Ms + (item0 + p) * mf + i * K, mr);
+        if (Cs) lds_row_global<K>(Cs + (item0 + p) * mf + i * K, cr);
+    }
+    while (p != p_end) {
+        const int64_t pn = p + step;
+        float mn[K], cn[K];
+        if (pn != p_end) {
+            lds_row_global<K>(Ms + (item0 + pn) * mf + i * K, mn);
+            if (Cs) lds_row_global<K>(Cs + (item0 + pn) * mf + i * K, cn);
+        }
+#pragma unroll
+        for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
+        __syncwarp();
+        float nr[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) nr[j] = Cs ? cr[j] : 0.f;
+#pragma unroll
+        for (int m = 0; m < K; ++m) {
+            float xm[K];
+            lds_row_smem<K>(xw + m * K, xm);
+#pragma unroll
+            for (int j = 0; j < K; ++j) nr[j] = fmaf(mr[m], xm[j], nr[j]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            xr[j] = nr[j];
+            mr[j] = mn[j];
+            if (Cs) cr[j] = cn[j];
+        }
+        p = pn;
+    }
+    // rows -> column `col`
+#pragma unroll
+    for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
+    __syncwarp();
+#pragma unroll
+    for (int m = 0; m < K; ++m) out[m] = xw[m * K + col];
+    __syncwarp();
+}
+
 template <int K>
 __global__ void __launch_bounds__(32)
     ms_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P,
@@ -383,23 +440,15 @@ __global__ void __launch_bounds__(32)
             // publish the aggregate, look back for the exclusive prefix E
             st_ws_col<K>(agg + slot, col, m);
             publish(&w.flags[g * C + c], FLAG_AGG, lane);
+            // E = P at the end of chunk c-1: the nearest published inclusive
+            // prefix, then the aggregates after it, oldest first: E <- Agg_p E
             float e[K];
-#pragma unroll
-            for (int i = 0; i < K; ++i) e[i] = (i == col) ? 1.f : 0.f;
-            for (int64_t p = c - 1; p >= 0; --p) {
-                const unsigned f = lookback_flag(&w.flags[g * C + p], lane, ctl);
-                if (f == 0) {
-                    failed = true;
-                    break;
-                }
-                const float *X = (f == FLAG_INCL ? incl : agg) + (g * C + p) * S::MF + sub * K * K;
-                float xc[K], ne[K];
-                ld_ws_col<K>(X, col, xc);
-                // E <- E X: column col of E X is E (X e_col)
-                group_matvec<K>(xw, col, e, xc, ne);
-#pragma unroll
-                for (int i = 0; i < K; ++i) e[i] = ne[i];
-                if (f == FLAG_INCL) break;
+            const int64_t ps = find_inclusive(w.flags + g * C, c, -1, C, lane, ctl);
+            if (ps < 0) {
+                failed = true;
+            } else {
+                const float *inc0 = incl + (g * C + ps) * S::MF + sub * K * K;
+                fold_rows<K>(inc0, agg + sub * K * K, S::MF, g * C, ps + 1, c, +1, nullptr, xw, col, e);
             }
             if (failed) {
                 if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
@@ -564,42 +613,17 @@ __global__ void __launch_bounds__(32)
             st_ws_col<K>(aggM + slot, col, mm);
             st_ws_col<K>(aggC + slot, col, mu);
             publish(&w.flags[g * C + c], FLAG_AGG, lane);
-            float macc[K], cacc[K];
-#pragma unroll
-            for (int i = 0; i < K; ++i) {
-                macc[i] = (i == col) ? 1.f : 0.f;
-                cacc[i] = 0.f;
-            }
+            // mu_in = mu_out of chunk c+1: the nearest published inclusive value
+            // after c, then the aggregates between, farthest first:
+            // mu <- M_p mu + C_p
             float muin[K];
-            for (int64_t p = c + 1; p < C; ++p) {
-                const unsigned f = lookback_flag(&w.flags[g * C + p], lane, ctl);
-                if (f == 0) {
-                    failed = true;
-                    break;
-                }
-                const int64_t ps = (g * C + p) * S::MF + sub * K * K;
-                if (f == FLAG_INCL) {
-                    float xc[K], y[K];
-                    ld_ws_col<K>(incl + ps, col, xc);
-                    group_matvec<K>(xw, col, macc, xc, y);  // Macc * mu_out(p)
-#pragma unroll
-                    for (int i = 0; i < K; ++i) muin[i] = y[i] + cacc[i];
-                    break;
-                }
-                float mp[K], cp[K], y1[K], y2[K];
-                ld_ws_col<K>(aggM + ps, col, mp);
-                ld_ws_col<K>(aggC + ps, col, cp);
-#pragma unroll
-                for (int i = 0; i < K; ++i) xw[i * K + col] = macc[i];
-                __syncwarp();
-                smem_matvec<K>(xw, cp, y1);  // Macc C_p
-                smem_matvec<K>(xw, mp, y2);  // Macc M_p
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < K; ++i) {
-                    cacc[i] = y1[i] + cacc[i];
-                    macc[i] = y2[i];
-                }
+            const int64_t ps = find_inclusive(w.flags + g * C, c, +1, C, lane, ctl);
+            if (ps < 0) {
+                failed = true;
+            } else {
+                const float *inc0 = incl + (g * C + ps) * S::MF + sub * K * K;
+                fold_rows<K>(inc0, aggM + sub * K * K, S::MF, g * C, ps - 1, c, -1, aggC + sub * K * K, xw, col,
+                             muin);
             }
             if (failed) {
                 if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
