@@ -67,6 +67,15 @@ struct ChunkPlan {
 // 1024 (group, chunk) items, with chunks of 32 to 64 steps so that the second
 // pass over a chunk, a few microseconds after the first, still finds its
 // inputs in L2 (about a thousand resident items x 64 KB stays well inside L2).
+#ifndef MGS_CHUNK_ITEMS
+#define MGS_CHUNK_ITEMS 1024
+#endif
+#ifndef MGS_CHUNK_LMIN
+#define MGS_CHUNK_LMIN 32
+#endif
+#ifndef MGS_CHUNK_LMAX
+#define MGS_CHUNK_LMAX 64
+#endif
 __host__ __device__ inline ChunkPlan plan_chunks(int64_t B, int64_t T, int64_t H, int K) {
     const int64_t lpw = 32 / K;
     ChunkPlan p;
@@ -74,9 +83,9 @@ __host__ __device__ inline ChunkPlan plan_chunks(int64_t B, int64_t T, int64_t H
     p.C = 1;
     p.L = T;
     if (p.G >= 256 || T < 64) return p;
-    const int64_t c0 = (1024 + p.G - 1) / p.G;
+    const int64_t c0 = (MGS_CHUNK_ITEMS + p.G - 1) / p.G;
     int64_t L = (T + c0 - 1) / c0;
-    L = L < 32 ? 32 : (L > 64 ? 64 : L);
+    L = L < MGS_CHUNK_LMIN ? MGS_CHUNK_LMIN : (L > MGS_CHUNK_LMAX ? MGS_CHUNK_LMAX : L);
     L = (L + 3) / 4 * 4;
     p.L = L;
     p.C = (T + L - 1) / L;
