@@ -50,6 +50,13 @@ def op_bytes(w, direction):
     if w.op == "ms":
         steps = B * T * H
         return steps * 4 * (2 * k * k if direction == "fwd" else 4 * k * k)
+    if w.op == "lin":
+        elems = B * T * H  # H holds D
+        init = B * H * 4
+        if direction == "fwd":  # read a, b; write h; read h0
+            return elems * 12 + (init if w.h0 != "none" else 0)
+        # read a, grad_h, h; write da, db; read h0, write dh0
+        return elems * 20 + (init if w.h0 != "none" else 0) + init
     elems = B * T * H  # H holds D for parallel_scan_log
     init = B * H * 4
     if direction == "fwd":  # read lc, lv; write h; read log_h0
@@ -217,6 +224,11 @@ class Runner:
             self.dA, self.db, self.dh0 = e(B, T, H, k, k), e(B, T, H, k), e(B, H, k)
             self.ws_f, self.nf = api.workspace(b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, B, T, H, k, device)
             self.ws_b, self.nb = api.workspace(b.MGS_OP_MATRIX_AFFINE_SCAN_BWD, B, T, H, k, device)
+        elif w.op == "lin":
+            self.h = e(B, T, H)
+            self.da, self.db, self.dh0 = e(B, T, H), e(B, T, H), e(B, H)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_LINEAR_SCAN_FWD, B, T, H, 1, device)
+            self.ws_b, self.nb = api.workspace(b.MGS_OP_LINEAR_SCAN_BWD, B, T, H, 1, device)
         elif w.op == "ms":
             self.P, self.dA = e(B, T, H, k, k), e(B, T, H, k, k)
             self.ws_f, self.nf = api.workspace(b.MGS_OP_MATRIX_SCAN_FWD, B, T, H, k, device)
@@ -230,6 +242,8 @@ class Runner:
         w, d, b = self.w, self.inp, self.b
         if w.op == "mas":
             b.mgs_matrix_affine_scan_fwd(d["A"], d["b"], d["h0"], self.h, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
+        elif w.op == "lin":
+            b.mgs_linear_scan_fwd(d["a"], d["b"], d["h0"], self.h, w.B, w.T, w.H, self.ws_f, self.nf, stream)
         elif w.op == "ms":
             b.mgs_matrix_scan_fwd(d["A"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
         else:
@@ -241,6 +255,9 @@ class Runner:
         if w.op == "mas":
             b.mgs_matrix_affine_scan_bwd(d["A"], d["h0"], self.h, d["grad_h"], self.dA, self.db, self.dh0,
                                          w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
+        elif w.op == "lin":
+            b.mgs_linear_scan_bwd(d["a"], d["h0"], self.h, d["grad_h"], self.da, self.db, self.dh0,
+                                  w.B, w.T, w.H, self.ws_b, self.nb, stream)
         elif w.op == "ms":
             b.mgs_matrix_scan_bwd(d["A"], self.P, d["grad_P"], self.dA, w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
         else:
@@ -261,6 +278,8 @@ class Runner:
             return [self.h, self.dA, self.db, self.dh0]
         if self.w.op == "ms":
             return [self.P, self.dA]
+        if self.w.op == "lin":
+            return [self.h, self.da, self.db, self.dh0]
         return [self.h, self.dlc, self.dlv, self.dl0]
 
     def e2e_step(self, stream):

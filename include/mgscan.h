@@ -70,7 +70,9 @@ enum {
     MGS_OP_MATRIX_SCAN_FWD = 3,
     MGS_OP_MATRIX_SCAN_BWD = 4,
     MGS_OP_PARALLEL_SCAN_LOG_FWD = 5,
-    MGS_OP_PARALLEL_SCAN_LOG_BWD = 6
+    MGS_OP_PARALLEL_SCAN_LOG_BWD = 6,
+    MGS_OP_LINEAR_SCAN_FWD = 7,
+    MGS_OP_LINEAR_SCAN_BWD = 8
 };
 
 /* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
@@ -177,6 +179,29 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
                                      float *d_log_coeffs, float *d_log_values, float *d_log_h0,
                                      int64_t B, int64_t T, int64_t D, void *workspace,
                                      size_t workspace_bytes, mgs_stream_t stream);
+
+/* linear_scan, forward ("mingru-scans" home page, scan-op table, linear_scan
+ * row): the diagonal linear recurrence in linear space, per (batch, channel)
+ * lane,
+ *     h_t = a_t * h_{t-1} + b_t,   h_0 = h0 (zeros when NULL),
+ * with signed coefficients allowed (the negative-eigenvalue gates of
+ * SignedMinGRU, home page lineage paragraph).  It is matrix_affine_scan with
+ * k = 1 and H = D, and runs on those kernels.
+ * In: a, b [B][T][D], h0 [B][D] (nullable).  Out: h [B][T][D].  D must be a
+ * multiple of 4.  Workspace: mgs_workspace_size(MGS_OP_LINEAR_SCAN_FWD, ...). */
+mgs_status mgs_linear_scan_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B,
+                               int64_t T, int64_t D, void *workspace, size_t workspace_bytes,
+                               mgs_stream_t stream);
+
+/* linear_scan, backward: gradients of L = sum_t <grad_h_t, h_t>.  With
+ * lambda_t = dL/dh_t,
+ *     lambda_T = grad_h_T,   lambda_t = grad_h_t + a_{t+1} lambda_{t+1},
+ *     db_t = lambda_t,   da_t = lambda_t h_{t-1},   dh0 = a_1 lambda_1.
+ * In: a, h0 (nullable), h = the forward output (saved), grad_h.
+ * Out: da, db [B][T][D], dh0 [B][D] (nullable: not written). */
+mgs_status mgs_linear_scan_bwd(const float *a, const float *h0, const float *h, const float *grad_h,
+                               float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t D,
+                               void *workspace, size_t workspace_bytes, mgs_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns MGS_ERR_TIMEOUT if a kernel's bounded wait gave up since the

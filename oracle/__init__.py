@@ -56,9 +56,11 @@ def _load():
             lib.oracle_ms_bwd.argtypes = [dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_psl_fwd.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64]
             lib.oracle_psl_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64]
+            lib.oracle_linear_fwd.argtypes = [dp, dp, dp, dp, i64, i64, i64]
+            lib.oracle_linear_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64]
             lib.oracle_num_threads.restype = ctypes.c_int
             for f in ("oracle_mas_fwd", "oracle_mas_bwd", "oracle_ms_fwd", "oracle_ms_bwd",
-                      "oracle_psl_fwd", "oracle_psl_bwd"):
+                      "oracle_psl_fwd", "oracle_psl_bwd", "oracle_linear_fwd", "oracle_linear_bwd"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -150,3 +152,25 @@ def psl_bwd(log_coeffs, log_values, log_h0, grad_h):
     dl0 = np.empty((B, D), dtype=np.float64) if l0 is not None else None
     _load().oracle_psl_bwd(_p(lc), _p(lv), _p(l0), _p(g), _p(dlc), _p(dlv), _p(dl0), B, T, D)
     return dlc, dlv, dl0
+
+
+# ---------------------------------------------------------------- linear_scan
+def linear_fwd(a, b, h0=None):
+    """h_t = a_t h_{t-1} + b_t elementwise.  a, b [B,T,D], h0 [B,D] or None -> h."""
+    a, b, h0 = _f64(a), _f64(b), _f64(h0)
+    B, T, D = a.shape
+    assert b.shape == (B, T, D) and (h0 is None or h0.shape == (B, D))
+    h = np.empty((B, T, D), dtype=np.float64)
+    _load().oracle_linear_fwd(_p(a), _p(b), _p(h0), _p(h), B, T, D)
+    return h
+
+
+def linear_bwd(a, b, h0, grad_h, want_dh0=True):
+    """Gradients of sum grad_h * h -> (da, db, dh0 or None)."""
+    a, b, h0, g = _f64(a), _f64(b), _f64(h0), _f64(grad_h)
+    B, T, D = a.shape
+    da = np.empty_like(a)
+    db = np.empty_like(a)
+    dh0 = np.empty((B, D), dtype=np.float64) if want_dh0 else None
+    _load().oracle_linear_bwd(_p(a), _p(b), _p(h0), _p(g), _p(da), _p(db), _p(dh0), B, T, D)
+    return da, db, dh0

@@ -305,6 +305,60 @@ void oracle_psl_bwd(const double *lc, const double *lv, const double *log_h0,
     }
 }
 
+/* ------------------------------------------------------------------ */
+/* linear_scan                                                          */
+/* ------------------------------------------------------------------ */
+
+/* Forward of the diagonal linear recurrence, per (batch, channel) lane:
+ *   h_t = a_t h_{t-1} + b_t,  h_0 = h0 (zeros when NULL).
+ * Signed coefficients are allowed.  Layout [B][T][D], h0 [B][D]. */
+void oracle_linear_fwd(const double *a, const double *bv, const double *h0, double *h,
+                       int64_t B, int64_t T, int64_t D)
+{
+    int64_t lanes = B * D;
+#pragma omp parallel for schedule(static)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / D, d = lane % D;
+        double x = h0 ? h0[bb * D + d] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t idx = (bb * T + t) * D + d;
+            x = a[idx] * x + bv[idx];
+            h[idx] = x;
+        }
+    }
+}
+
+/* Backward for L = sum_t g_t h_t:  lambda_T = g_T,
+ * lambda_t = g_t + a_{t+1} lambda_{t+1};  db_t = lambda_t;
+ * da_t = lambda_t h_{t-1};  dh0 = a_1 lambda_1 (dh0 may be NULL).
+ * The forward states are recomputed from (a, b, h0). */
+void oracle_linear_bwd(const double *a, const double *bv, const double *h0, const double *gh,
+                       double *da, double *db, double *dh0, int64_t B, int64_t T, int64_t D)
+{
+    int64_t lanes = B * D;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / D, d = lane % D;
+        double *hs = (double *)malloc(sizeof(double) * (size_t)(T + 1));
+        hs[0] = h0 ? h0[bb * D + d] : 0.0;
+        for (int64_t t = 1; t <= T; ++t) {
+            int64_t idx = (bb * T + (t - 1)) * D + d;
+            hs[t] = a[idx] * hs[t - 1] + bv[idx];
+        }
+        double nxt = 0.0; /* a_{t+1} lambda_{t+1} */
+        for (int64_t t = T; t >= 1; --t) {
+            int64_t idx = (bb * T + (t - 1)) * D + d;
+            double lam = gh[idx] + nxt;
+            db[idx] = lam;
+            da[idx] = lam * hs[t - 1];
+            nxt = a[idx] * lam;
+        }
+        if (dh0)
+            dh0[bb * D + d] = nxt;
+        free(hs);
+    }
+}
+
 /* Number of host threads the OpenMP loops above use. */
 int oracle_num_threads(void)
 {

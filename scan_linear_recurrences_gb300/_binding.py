@@ -30,6 +30,8 @@ MGS_OP_MATRIX_SCAN_FWD = 3
 MGS_OP_MATRIX_SCAN_BWD = 4
 MGS_OP_PARALLEL_SCAN_LOG_FWD = 5
 MGS_OP_PARALLEL_SCAN_LOG_BWD = 6
+MGS_OP_LINEAR_SCAN_FWD = 7
+MGS_OP_LINEAR_SCAN_BWD = 8
 
 
 class MGSError(RuntimeError):
@@ -56,6 +58,8 @@ _SIGNATURES = {
     "mgs_matrix_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_parallel_scan_log_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "mgs_parallel_scan_log_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "mgs_linear_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "mgs_linear_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "mgs_check": (_int, [_vp]),
     "mgs_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "mgs_debug_wait_flag": (_int, [_vp, _vp]),
@@ -157,6 +161,16 @@ def mgs_parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, d_log_c
     return _call("mgs_parallel_scan_log_bwd", _ptr(log_coeffs), _ptr(log_values), _ptr(log_h0), _ptr(h),
                  _ptr(grad_h), _ptr(d_log_coeffs), _ptr(d_log_values), _ptr(d_log_h0), B, T, D,
                  _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mgs_linear_scan_fwd(a, b, h0, h, B, T, D, workspace=None, workspace_bytes=0, stream=None):
+    return _call("mgs_linear_scan_fwd", _ptr(a), _ptr(b), _ptr(h0), _ptr(h), B, T, D, _ptr(workspace),
+                 workspace_bytes, _stream(stream))
+
+
+def mgs_linear_scan_bwd(a, h0, h, grad_h, da, db, dh0, B, T, D, workspace=None, workspace_bytes=0, stream=None):
+    return _call("mgs_linear_scan_bwd", _ptr(a), _ptr(h0), _ptr(h), _ptr(grad_h), _ptr(da), _ptr(db), _ptr(dh0),
+                 B, T, D, _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def mgs_check(stream=None):

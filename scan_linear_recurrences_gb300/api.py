@@ -107,6 +107,33 @@ def parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, stream=None
     return dlc, dlv, dl0
 
 
+# ---------------------------------------------------------------- linear_scan
+def linear_scan_fwd(a, b, h0=None, stream=None):
+    """h_t = a_t * h_{t-1} + b_t elementwise.  a, b [B,T,D], h0 [B,D] or None."""
+    B, T, D = a.shape
+    _check(a, "a"); _check(b, "b", (B, T, D))
+    if h0 is not None:
+        _check(h0, "h0", (B, D))
+    h = torch.empty_like(b)
+    ws, nws = workspace(_b.MGS_OP_LINEAR_SCAN_FWD, B, T, D, 1, b.device)
+    _b.mgs_linear_scan_fwd(a, b, h0, h, B, T, D, ws, nws, stream)
+    return h
+
+
+def linear_scan_bwd(a, h0, h, grad_h, need_dh0=True, stream=None):
+    """Returns (da, db, dh0 or None) for L = sum grad_h * h."""
+    B, T, D = a.shape
+    for t, n in ((a, "a"), (h, "h"), (grad_h, "grad_h")):
+        _check(t, n, (B, T, D))
+    if h0 is not None:
+        _check(h0, "h0", (B, D))
+    da, db = torch.empty_like(a), torch.empty_like(a)
+    dh0 = torch.empty((B, D), dtype=torch.float32, device=a.device) if need_dh0 else None
+    ws, nws = workspace(_b.MGS_OP_LINEAR_SCAN_BWD, B, T, D, 1, a.device)
+    _b.mgs_linear_scan_bwd(a, h0, h, grad_h, da, db, dh0, B, T, D, ws, nws, stream)
+    return da, db, dh0
+
+
 # ---------------------------------------------------------------- autograd wrappers
 class MatrixAffineScan(torch.autograd.Function):
     """h = matrix_affine_scan(A, b, h0) with the library's fused backward."""
@@ -158,6 +185,28 @@ class ParallelScanLog(torch.autograd.Function):
         l0 = l0 if ctx.has_h0 else None
         dlc, dlv, dl0 = parallel_scan_log_bwd(lc, lv, l0, h, grad_h.contiguous())
         return dlc, dlv, dl0
+
+
+class LinearScan(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, a, b, h0=None):
+        a, b = a.contiguous(), b.contiguous()
+        h0c = h0.contiguous() if h0 is not None else None
+        h = linear_scan_fwd(a, b, h0c)
+        ctx.save_for_backward(a, h0c if h0c is not None else torch.empty(0, device=a.device), h)
+        ctx.has_h0 = h0 is not None
+        return h
+
+    @staticmethod
+    def backward(ctx, grad_h):
+        a, h0, h = ctx.saved_tensors
+        h0 = h0 if ctx.has_h0 else None
+        da, db, dh0 = linear_scan_bwd(a, h0, h, grad_h.contiguous(), need_dh0=ctx.has_h0)
+        return da, db, dh0
+
+
+def linear_scan(a, b, h0=None):
+    return LinearScan.apply(a, b, h0)
 
 
 def matrix_affine_scan(A, b, h0=None):

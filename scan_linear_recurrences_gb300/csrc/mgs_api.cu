@@ -174,6 +174,10 @@ size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
         case MGS_OP_MATRIX_AFFINE_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
             return mgs::mas_workspace_bytes(B, T, H_or_D, k);
+        case MGS_OP_LINEAR_SCAN_FWD:
+        case MGS_OP_LINEAR_SCAN_BWD:
+            if (block_sizes(B, T, H_or_D, 1, &s) != MGS_OK) return 0;
+            return mgs::mas_workspace_bytes(B, T, H_or_D, 1);
         case MGS_OP_MATRIX_SCAN_FWD:
         case MGS_OP_MATRIX_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
@@ -330,6 +334,23 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
     return from_cuda(mgs::launch_psl_bwd(log_coeffs, log_values, log_h0, h, grad_h, d_log_coeffs,
                                          d_log_values, d_log_h0, B, T, D, ctl,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// linear_scan is matrix_affine_scan with 1 x 1 blocks: [B][T][D] is
+// [B][T][H=D][1][1], so it validates and runs exactly as that op with k = 1.
+mgs_status mgs_linear_scan_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B,
+                               int64_t T, int64_t D, void *workspace, size_t workspace_bytes,
+                               mgs_stream_t stream) {
+    if (D >= 0 && D % 4 != 0) return MGS_ERR_UNSUPPORTED;
+    return mgs_matrix_affine_scan_fwd(a, b, h0, h, B, T, D, 1, workspace, workspace_bytes, stream);
+}
+
+mgs_status mgs_linear_scan_bwd(const float *a, const float *h0, const float *h, const float *grad_h,
+                               float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t D,
+                               void *workspace, size_t workspace_bytes, mgs_stream_t stream) {
+    if (D >= 0 && D % 4 != 0) return MGS_ERR_UNSUPPORTED;
+    return mgs_matrix_affine_scan_bwd(a, h0, h, grad_h, da, db, dh0, B, T, D, 1, workspace, workspace_bytes,
+                                      stream);
 }
 
 mgs_status mgs_check(mgs_stream_t stream) {

@@ -164,11 +164,31 @@ def psl_inputs(B, T, D, seed, device="cpu", with_h0=True):
     return dict(log_coeffs=lc, log_values=lv, log_h0=l0, grad_h=gh)
 
 
+def linear_inputs(B, T, D, seed, device="cpu", with_h0=True):
+    """linear_scan inputs with signed gates: a = tanh(N(0,1)) in (-1, 1),
+    b = sigmoid(N(0,1)) * N(0,1), h0 ~ N(0,1) (drawn first) or absent,
+    grad_h ~ N(0,1); dict(a, b [B,T,D], h0 [B,D] or None, grad_h)."""
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    f64 = dict(dtype=torch.float64, device=dev)
+    h0 = torch.randn((B, D), generator=g, **f64).float() if with_h0 else None
+    a = torch.empty((B, T, D), dtype=torch.float32, device=dev)
+    b = torch.empty((B, T, D), dtype=torch.float32, device=dev)
+    gh = torch.empty((B, T, D), dtype=torch.float32, device=dev)
+    for t0 in range(0, T, TIME_BLOCK):
+        tb = min(TIME_BLOCK, T - t0)
+        a[:, t0:t0 + tb] = torch.tanh(torch.randn((B, tb, D), generator=g, **f64)).float()
+        z = torch.sigmoid(torch.randn((B, tb, D), generator=g, **f64))
+        b[:, t0:t0 + tb] = (z * torch.randn((B, tb, D), generator=g, **f64)).float()
+        gh[:, t0:t0 + tb] = torch.randn((B, tb, D), generator=g, **f64).float()
+    return dict(a=a, b=b, h0=h0, grad_h=gh)
+
+
 @dataclass(frozen=True)
 class Workload:
     """One benchmarked shape."""
     cid: int
-    op: str          # "mas" | "ms" | "psl"
+    op: str          # "mas" | "ms" | "psl" | "lin"
     name: str
     B: int
     T: int
@@ -185,6 +205,8 @@ class Workload:
             return mas_inputs(self.B, self.T, self.H, self.k, self.seed, device, h0=self.h0)
         if self.op == "ms":
             return ms_inputs(self.B, self.T, self.H, self.k, self.seed, device)
+        if self.op == "lin":
+            return linear_inputs(self.B, self.T, self.H, self.seed, device, with_h0=True)
         return psl_inputs(self.B, self.T, self.H, self.seed, device, with_h0=True)
 
 
@@ -201,4 +223,6 @@ WORKLOADS = {
 EXTRA_WORKLOADS = {
     5: Workload(5, "mas", "matrix_affine_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "normal"),
     6: Workload(6, "ms", "matrix_scan lab Givens B=128 T=64 H=8 k=8", 128, 64, 8, 8, "none"),
+    7: Workload(7, "lin", "linear_scan lab B=128 T=64 D=64", 128, 64, 64, 1, "normal"),
+    8: Workload(8, "lin", "linear_scan long-T B=16 T=1024 D=64", 16, 1024, 64, 1, "normal"),
 }

@@ -86,8 +86,17 @@ def test_ms_and_psl_validation(L):
                FAKE + (5 << 30), None, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
 
 
+def test_linear_scan_validation(L):
+    a, bb, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    assert _st(b.mgs_linear_scan_fwd, a, bb, None, h, 2, 8, 6) == b.MGS_ERR_UNSUPPORTED  # D % 4
+    assert _st(b.mgs_linear_scan_fwd, a, bb, None, bb, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+    assert _st(b.mgs_linear_scan_fwd, None, None, None, None, 0, 8, 8) == b.MGS_OK
+    assert b.mgs_workspace_size(b.MGS_OP_LINEAR_SCAN_FWD, 1, 4096, 64, 1) > 0  # few lanes: chunked
+    assert b.mgs_workspace_size(b.MGS_OP_LINEAR_SCAN_FWD, 64, 4096, 1024, 1) == 0
+
+
 def test_workspace_size_queries(L):
-    for op in range(1, 7):
+    for op in range(1, 9):
         assert b.mgs_workspace_size(op, 2, 16, 8, 8) >= 0
     assert b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, -1, 16, 8, 8) == 0
     # many lanes or short sequences: single pass, no workspace

@@ -219,7 +219,38 @@ def test_psl_zero_coefficients_and_empty():
     assert api.parallel_scan_log_fwd(empty, empty).shape == (0, 5, 8)
 
 
+# ---------------------------------------------------------------- linear_scan
+@pytest.mark.parametrize("B,T,D,h0", [
+    (2, 1, 4, True), (3, 77, 132, True), (2, 300, 64, True), (1, 2000, 32, False), (4, 500, 1024, True),
+    (16, 1024, 64, True), (128, 64, 64, True),
+])
+def test_linear_scan(B, T, D, h0):
+    d = _cuda(inputs.linear_inputs(B, T, D, seed=500 + B * T + D, with_h0=h0))
+    h = api.linear_scan_fwd(d["a"], d["b"], d["h0"])
+    da, db, dh0 = api.linear_scan_bwd(d["a"], d["h0"], h, d["grad_h"], need_dh0=True)
+    b.mgs_check()
+    a, bb, g = d["a"].cpu(), d["b"].cpu(), d["grad_h"].cpu()
+    hz = d["h0"].cpu() if d["h0"] is not None else torch.zeros((B, D))
+    assert_close("h", h, oracle.linear_fwd(a, bb, hz), T)
+    dar, dbr, dh0r = oracle.linear_bwd(a, bb, hz, g)
+    assert_close("da", da, dar, T)
+    assert_close("db", db, dbr, T)
+    assert_close("dh0", dh0, dh0r, T)
+
+
 # ---------------------------------------------------------------- autograd wrappers
+def test_linear_scan_autograd():
+    d = _cuda(inputs.linear_inputs(2, 90, 8, seed=8))
+    a = d["a"].clone().requires_grad_(True)
+    bb = d["b"].clone().requires_grad_(True)
+    h0 = d["h0"].clone().requires_grad_(True)
+    (api.linear_scan(a, bb, h0) * d["grad_h"]).sum().backward()
+    dar, dbr, dh0r = oracle.linear_bwd(d["a"].cpu(), d["b"].cpu(), d["h0"].cpu(), d["grad_h"].cpu())
+    assert_close("da", a.grad, dar, 90)
+    assert_close("db", bb.grad, dbr, 90)
+    assert_close("dh0", h0.grad, dh0r, 90)
+
+
 def test_autograd_wrappers_match_oracle():
     d = _cuda(inputs.mas_inputs(2, 30, 3, 8, seed=7, h0="normal"))
     A = d["A"].clone().requires_grad_(True)

@@ -25,6 +25,8 @@ MUTATIONS = [
     ("psl_fwd_wrong_sign", "log1p(exp(-fabs(x - y)))", "log1p(exp(fabs(x - y)))", 0),
     ("psl_bwd_dlc_uses_h_t", "dlc[idx] = lam * a * hs[t - 1];", "dlc[idx] = lam * a * hs[t];", 0),
     ("psl_bwd_dropped_carry", "lam = gh[idx] + nxt;", "lam = gh[idx];", 0),
+    ("linear_fwd_dropped_b", "x = a[idx] * x + bv[idx];", "x = a[idx] * x;", 0),
+    ("linear_bwd_da_uses_h_t", "da[idx] = lam * hs[t - 1];", "da[idx] = lam * hs[t];", 0),
 ]
 
 

@@ -379,3 +379,48 @@ def test_empty_shapes():
     assert oracle.ms_fwd(A).shape == A.shape
     lc = np.zeros((0, 5, 3))
     assert oracle.psl_fwd(lc, lc, np.zeros((0, 3))).shape == (0, 5, 3)
+
+
+# --------------------------------------------------------------- linear_scan
+def test_linear_scan_equals_k1_block_scan_and_closed_form():
+    """k = 1 matrix_affine_scan is the same recurrence (separate oracle loops);
+    constant a gives the geometric closed form; signed a is allowed."""
+    B, T, D = 2, 60, 5
+    a = rng.uniform(-0.95, 0.95, (B, T, D))
+    b = rng.standard_normal((B, T, D))
+    h0 = rng.standard_normal((B, D))
+    h = oracle.linear_fwd(a, b, h0)
+    hm = oracle.mas_fwd(a[..., None, None], b[..., None], h0[..., None])[..., 0]
+    np.testing.assert_allclose(h, hm, rtol=1e-13, atol=1e-14)
+    ac = np.full((B, T, D), -0.7)
+    bc = np.broadcast_to(b[:, :1], (B, T, D)).copy()
+    t = np.broadcast_to(np.arange(1, T + 1)[None, :, None], (B, T, D))
+    ref = (-0.7) ** t * h0[:, None] + bc * (1 - (-0.7) ** t) / (1 + 0.7)
+    np.testing.assert_allclose(oracle.linear_fwd(ac, bc, h0), ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(oracle.linear_fwd(a, b, None), oracle.linear_fwd(a, b, np.zeros((B, D))))
+
+
+def test_linear_scan_bwd_finite_differences_and_tangent():
+    B, T, D = 1, 6, 3
+    a = rng.uniform(-0.9, 0.9, (B, T, D))
+    b = rng.standard_normal((B, T, D))
+    h0 = rng.standard_normal((B, D))
+    g = rng.standard_normal((B, T, D))
+    da, db, dh0 = oracle.linear_bwd(a, b, h0, g)
+    L = lambda a_, b_, h_: float(np.sum(g * oracle.linear_fwd(a_, b_, h_)))
+    np.testing.assert_allclose(da, _fd(lambda x: L(x, b, h0), a), rtol=1e-7, atol=1e-8)
+    np.testing.assert_allclose(db, _fd(lambda x: L(a, x, h0), b), rtol=1e-7, atol=1e-8)
+    np.testing.assert_allclose(dh0, _fd(lambda x: L(a, b, x), h0), rtol=1e-7, atol=1e-8)
+    # forward-mode tangent in da at a medium size
+    B, T, D = 2, 300, 4
+    a = rng.uniform(-0.99, 0.99, (B, T, D))
+    b = rng.standard_normal((B, T, D)); h0 = rng.standard_normal((B, D)); g = rng.standard_normal((B, T, D))
+    V = rng.standard_normal(a.shape)
+    h = oracle.linear_fwd(a, b, h0)
+    hprev = np.concatenate([h0[:, None], h[:, :-1]], axis=1)
+    dh = np.zeros((B, D)); tangent = 0.0
+    for tt in range(T):
+        dh = a[:, tt] * dh + V[:, tt] * hprev[:, tt]
+        tangent += np.sum(g[:, tt] * dh)
+    da, _, _ = oracle.linear_bwd(a, b, h0, g)
+    assert abs(tangent - np.sum(da * V)) <= 1e-10 * np.sum(np.abs(da * V))
