@@ -124,7 +124,7 @@ mgs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MGS_OK : MGS_ERR
 namespace mgs {
 
 cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,
-                      const uint64_t *byte_strides, const uint32_t *box) {
+                      const uint64_t *byte_strides, const uint32_t *box, bool swizzle128) {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     std::call_once(once, [] {
@@ -144,7 +144,8 @@ cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint6
     }
     for (int i = 0; i + 1 < rank; ++i) gstr[i] = byte_strides[i];
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, cuuint32_t(rank), const_cast<float *>(base), gdim,
-                        gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -45,7 +45,7 @@ cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, c
 // Encodes a tiled fp32 tensor map over `base` (rank 2 or 3).  dims and box are
 // innermost first; byte_strides has rank-1 entries (strides of dims 1..).
 cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,
-                      const uint64_t *byte_strides, const uint32_t *box);
+                      const uint64_t *byte_strides, const uint32_t *box, bool swizzle128 = false);
 
 // Sets the dynamic shared-memory limit of `fn` once per device.
 cudaError_t ensure_smem_attr(const void *fn, int bytes);

@@ -27,16 +27,19 @@ struct MasShape {
     // time steps per stage: about 8-10 KB of A per stage
     static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? 8 : 16);
     static constexpr int NS = 4;                // stages in flight
-    using TA = HeadTile<K * K, LPW>;
+    using TA = MatTile<K, false>;
     using TV = HeadTile<K, LPW>;
 };
 
-// Per-warp shared memory: NS stages of STAGEF floats, then NS barriers.
-template <int STAGEF, int NS>
+// Per-warp shared memory: NS stages of STAGEF floats (each starting on an
+// ALIGN-byte boundary, the A box first), then NS barriers; ALIGN bytes of
+// slack let the kernel align the dynamic base at run time.
+template <int STAGEF, int NS, size_t ALIGN>
 struct Ring {
-    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);
-    static constexpr size_t ring_bytes = NS * stage_bytes;
-    static constexpr size_t warp_bytes = align_up(ring_bytes + NS * sizeof(uint64_t), 128);
+    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);   // transferred per stage
+    static constexpr size_t stage_stride = align_up(stage_bytes, ALIGN);
+    static constexpr size_t ring_bytes = NS * stage_stride;
+    static constexpr size_t warp_bytes = align_up(ring_bytes + NS * sizeof(uint64_t), 128) + ALIGN;
 };
 
 // Loads K consecutive floats from shared memory (16-byte aligned when K >= 4).
@@ -97,14 +100,16 @@ __global__ void __launch_bounds__(32)
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MasShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
-    using R = Ring<STAGEF, S::NS>;
+    using R = Ring<STAGEF, S::NS, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
     const int lane = threadIdx.x;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * S::LPW;
@@ -122,7 +127,7 @@ __global__ void __launch_bounds__(32)
         prefetch_tmap(&tmB);
     }
     auto issue = [&](int s, int64_t j) {  // lane 0 only
-        float *st = ring + size_t(s) * STAGEF;
+        float *st = ring + size_t(s) * SSTR;
         mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
         S::TA::load(st, &tmA, head0, row0 + int(j * S::TS), &bars[s], pol);
         S::TV::load(st + A_STAGE, &tmB, head0, row0 + int(j * S::TS), &bars[s], pol);
@@ -145,13 +150,13 @@ __global__ void __launch_bounds__(32)
             return;
         }
         const int n = int(min64(S::TS, T - j * S::TS));
-        const float *sa = ring + size_t(s) * STAGEF + (sub * K + row) * K;
-        const float *sb = ring + size_t(s) * STAGEF + A_STAGE + sub * K + row;
+        const float *st = ring + size_t(s) * SSTR;
+        const float *sb = st + A_STAGE + sub * K + row;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 float a[K];
-                lds_row<K>(sa + u * S::AF, a);
+                TileRef<K, false>{st, u, sub}.row(row, a);
                 float acc0 = sb[u * S::VF];
                 float acc1 = 0.f;
 #pragma unroll
@@ -188,14 +193,16 @@ __global__ void __launch_bounds__(32)
     using S = MasShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
     constexpr int STAGEF = A_STAGE + 2 * V_STAGE;  // A_t, g_t, h_{t-1}
-    using R = Ring<STAGEF, S::NS>;
+    using R = Ring<STAGEF, S::NS, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
     const int lane = threadIdx.x;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::ring_bytes);
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::ring_bytes);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * S::LPW;
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(32)
     // zero-filled when negative) so step u (t = T-1-j*TS-u) sits at box row
     // TS-1-u.  The h box starts one row earlier and holds h_{t-1}.
     auto issue = [&](int s, int64_t j) {  // lane 0 only
-        float *st = ring + size_t(s) * STAGEF;
+        float *st = ring + size_t(s) * SSTR;
         const int r0 = int(bi * T + T - (j + 1) * S::TS);
         mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
         S::TA::load(st, &tmA, head0, r0, &bars[s], pol);
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(32)
         }
         const int64_t tt = T - 1 - j * S::TS;
         const int n = int(min64(S::TS, tt + 1));
-        const float *st = ring + size_t(s) * STAGEF;
+        const float *st = ring + size_t(s) * SSTR;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(32)
                     for (int c = 0; c < K; ++c) hp[c] = 0.f;
                 }
                 float a[K];
-                lds_row<K>(st + q * S::AF + (sub * K + row) * K, a);
+                TileRef<K, false>{st, q, sub}.row(row, a);
                 float p[K], dar[K];
 #pragma unroll
                 for (int c = 0; c < K; ++c) {
@@ -292,7 +299,7 @@ template <int K>
 cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
                       int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
     using S = MasShape<K>;
-    using R = Ring<S::TS * (S::AF + S::VF), S::NS>;
+    using R = Ring<S::TS * (S::AF + S::VF), S::NS, S::TA::kAlign>;
     CUtensorMap tA, tB;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
@@ -311,7 +318,7 @@ cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const flo
                       float *db, float *dh0, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
                       cudaStream_t s) {
     using S = MasShape<K>;
-    using R = Ring<S::TS * (S::AF + 2 * S::VF), S::NS>;
+    using R = Ring<S::TS * (S::AF + 2 * S::VF), S::NS, S::TA::kAlign>;
     CUtensorMap tA, tG, tH;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
@@ -343,17 +350,18 @@ struct MasChunkShape {
     static constexpr int AF = LPW * K * K, VF = LPW * K;
     static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? 8 : 16);
     static constexpr int NS = 4;
-    using TA = HeadTile<K * K, LPW>;
+    using TA = MatTile<K>;
     using TV = HeadTile<K, LPW>;
 };
 
-template <int STAGEF, int NS, int XF>
+template <int STAGEF, int NS, int XF, size_t ALIGN>
 struct ChunkRing {
-    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);
-    static constexpr size_t ring_bytes = NS * stage_bytes;
+    static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);  // transferred per full stage
+    static constexpr size_t stage_stride = align_up(stage_bytes, ALIGN);
+    static constexpr size_t ring_bytes = NS * stage_stride;
     static constexpr size_t xch_offset = ring_bytes;
     static constexpr size_t bar_offset = align_up(ring_bytes + size_t(XF) * sizeof(float), 16);
-    static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128);
+    static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128) + ALIGN;
 };
 
 // Look-back for a row-held affine carry.  Finds the nearest chunk in direction
@@ -417,11 +425,13 @@ __global__ void __launch_bounds__(32)
                          int64_t B, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
     using S = MasChunkShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
-    using R = ChunkRing<STAGEF, S::NS, S::AF>;
+    using R = ChunkRing<STAGEF, S::NS, S::AF, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    float *xch = reinterpret_cast<float *>(smem_raw + R::xch_offset);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::bar_offset);
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    float *xch = reinterpret_cast<float *>(sbase + R::xch_offset);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb;
@@ -452,7 +462,7 @@ __global__ void __launch_bounds__(32)
     }
     auto block_t0 = [&](int64_t jj) { return tb + ((two_pass && jj >= n1) ? jj - n1 : jj) * S::TS; };
     auto issue = [&](int s, int64_t jj) {  // lane 0 only
-        float *st = ring + size_t(s) * STAGEF;
+        float *st = ring + size_t(s) * SSTR;
         const int row = int(bi * T + block_t0(jj));
         mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
         S::TA::load(st, &tmA, head0, row, &bars[s], pol);
@@ -480,13 +490,13 @@ __global__ void __launch_bounds__(32)
         const int64_t t0 = block_t0(jj);
         const int n = int(min64(S::TS, tb + len - t0));
         const bool p1 = two_pass && jj < n1;
-        const float *st = ring + size_t(s) * STAGEF;
+        const float *st = ring + size_t(s) * SSTR;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
-                const float *Ablk = st + u * S::AF + sub * K * K;
+                const TileRef<K> Ablk{st, u, sub};
                 float a[K];
-                lds_row<K>(Ablk + r * K, a);
+                Ablk.row(r, a);
                 const float bval = st[A_STAGE + u * S::VF + sub * K + r];
                 const float x_in = p1 ? cv : hprev;
                 float acc0 = bval, acc1 = 0.f;
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(32)
                 if (p1) {
                     cv = acc0 + acc1;
                     float nm[K];
-                    smem_matvec<K>(Ablk, mcol, nm);
+                    tile_matvec(Ablk, mcol, nm);
 #pragma unroll
                     for (int i = 0; i < K; ++i) mcol[i] = nm[i];
                 } else {
@@ -549,11 +559,13 @@ __global__ void __launch_bounds__(32)
     using S = MasChunkShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
     constexpr int STAGEF = A_STAGE + 2 * V_STAGE;
-    using R = ChunkRing<STAGEF, S::NS, S::AF>;
+    using R = ChunkRing<STAGEF, S::NS, S::AF, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    float *xch = reinterpret_cast<float *>(smem_raw + R::xch_offset);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + R::bar_offset);
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    float *xch = reinterpret_cast<float *>(sbase + R::xch_offset);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb;
@@ -590,7 +602,7 @@ __global__ void __launch_bounds__(32)
         const bool p1 = two_pass && jj < n1;
         const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
         const int r0 = int(bi * T + te - (jb + 1) * S::TS);
-        float *st = ring + size_t(s) * STAGEF;
+        float *st = ring + size_t(s) * SSTR;
         mbar_arrive_expect_tx(&bars[s], uint32_t((A_STAGE + (p1 ? 1 : 2) * V_STAGE) * 4));
         S::TA::load(st, &tmA, head0, r0, &bars[s], pol);
         S::TV::load(st + A_STAGE, &tmG, head0, r0, &bars[s], pol);
@@ -620,23 +632,23 @@ __global__ void __launch_bounds__(32)
         const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
         const int64_t tt = te - 1 - jb * S::TS;
         const int n = int(min64(S::TS, tt - tb + 1));
-        const float *st = ring + size_t(s) * STAGEF;
+        const float *st = ring + size_t(s) * SSTR;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 const int64_t t = tt - u;
                 const int q = S::TS - 1 - u;
-                const float *Ablk = st + q * S::AF + sub * K * K;
+                const TileRef<K> Ablk{st, q, sub};
                 const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
                 float a[K];
-                lds_row<K>(Ablk + r * K, a);
+                Ablk.row(r, a);
                 float p[K];
 #pragma unroll
                 for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
                 mu = group_reduce_scatter<K>(p, r);
                 if (p1) {
                     float nm[K];
-                    smem_matvec_t<K>(Ablk, mcol, nm);
+                    tile_matvec_t(Ablk, mcol, nm);
 #pragma unroll
                     for (int i = 0; i < K; ++i) mcol[i] = nm[i];
                 } else {
@@ -695,7 +707,7 @@ template <int K>
 cudaError_t mas_fwd_chunk_t(const float *A, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                             int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MasChunkShape<K>;
-    using R = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::AF>;
+    using R = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::AF, S::TA::kAlign>;
     CUtensorMap tA, tB;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
@@ -713,7 +725,7 @@ cudaError_t mas_bwd_chunk_t(const float *A, const float *h0, const float *h, con
                             float *db, float *dh0, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
                             unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MasChunkShape<K>;
-    using R = ChunkRing<S::TS * (S::AF + 2 * S::VF), S::NS, S::AF>;
+    using R = ChunkRing<S::TS * (S::AF + 2 * S::VF), S::NS, S::AF, S::TA::kAlign>;
     CUtensorMap tA, tG, tH;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;

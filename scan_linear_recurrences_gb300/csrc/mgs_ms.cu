@@ -21,16 +21,19 @@ struct MsShape {
     static constexpr int MF = LPW * K * K;  // floats of one k x k tensor per time step
     static constexpr int TS = K >= 16 ? 2 : (K >= 8 ? 4 : 8);
     static constexpr int NS = 4;
-    using TM = HeadTile<K * K, LPW>;
+    using TM = MatTile<K, false>;
 };
 
 constexpr int kWarpsPerBlock = 1;
 
-template <int STEPF, int TS, int NS, int EXTRAF>
+// Per-warp shared memory: the ring (stages of 1 or 3 swizzled k x k boxes,
+// each a multiple of 1024 bytes for k >= 8), an exchange buffer, the barriers,
+// and ALIGN bytes of slack so the kernel can align the base at run time.
+template <int STEPF, int TS, int NS, int EXTRAF, size_t ALIGN>
 struct MsLayout {
     static constexpr size_t ring_bytes = size_t(NS) * TS * STEPF * sizeof(float);
     static constexpr size_t extra_bytes = size_t(EXTRAF) * sizeof(float);
-    static constexpr size_t warp_bytes = align_up(ring_bytes + extra_bytes + NS * sizeof(uint64_t), 128);
+    static constexpr size_t warp_bytes = align_up(ring_bytes + extra_bytes + NS * sizeof(uint64_t), 128) + ALIGN;
 };
 
 // ---------------------------------------------------------------- forward
@@ -40,13 +43,13 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                   int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
     using S = MsShape<K>;
     constexpr int STEPF = S::MF;
-    using L = MsLayout<STEPF, S::TS, S::NS, 0>;
+    using L = MsLayout<STEPF, S::TS, S::NS, 0, S::TM::kAlign>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
     if (g >= B * groups_per_b) return;
-    unsigned char *base = smem_raw + size_t(warp) * L::warp_bytes;
+    unsigned char *base = align_smem(smem_raw + size_t(warp) * L::warp_bytes, S::TM::kAlign);
     float *ring = reinterpret_cast<float *>(base);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + L::ring_bytes + L::extra_bytes);
 
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
                 float nc[K];
-                smem_matvec<K>(st + u * STEPF + sub * K * K, pc, nc);
+                tile_matvec(TileRef<K, false>{st, u, sub}, pc, nc);
 #pragma unroll
                 for (int i = 0; i < K; ++i) pc[i] = nc[i];
                 if (active) {
@@ -119,13 +122,13 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     using S = MsShape<K>;
     constexpr int STEPF = 3 * S::MF;  // A_t, G_t, P_{t-1}
     constexpr int XF = S::MF;         // Lambda exchange buffer, [lane][row][col]
-    using L = MsLayout<STEPF, S::TS, S::NS, XF>;
+    using L = MsLayout<STEPF, S::TS, S::NS, XF, S::TM::kAlign>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t g = int64_t(blockIdx.x) * kWarpsPerBlock + warp;
     if (g >= B * groups_per_b) return;
-    unsigned char *base = smem_raw + size_t(warp) * L::warp_bytes;
+    unsigned char *base = align_smem(smem_raw + size_t(warp) * L::warp_bytes, S::TM::kAlign);
     float *ring = reinterpret_cast<float *>(base);
     float *xch = reinterpret_cast<float *>(base + L::ring_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + L::ring_bytes + L::extra_bytes);
@@ -180,12 +183,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
             if (u < n) {
                 const int64_t t = tt - u;
                 const int q = S::TS - 1 - u;  // box row of step u
-                const float *At = st + q * S::MF + sub * K * K;
-                const float *Gt = At + S::TS * S::MF;
-                const float *Pp = At + 2 * S::TS * S::MF;
+                const TileRef<K, false> At{st, q, sub}, Gt{st + S::TS * S::MF, q, sub}, Pp{st + 2 * S::TS * S::MF, q, sub};
                 float lc[K];  // column `col` of Lambda_t
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt[i * K + col] + mu[i];
+                for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
                 // exchange Lambda_t so this thread can form row `col` of dA_t
 #pragma unroll
                 for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
@@ -195,12 +196,12 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                 for (int jj = 0; jj < K; ++jj) lrow[jj] = xw[col * K + jj];
                 float darow[K];
                 if (t >= 1) {
-                    smem_matvec<K>(Pp, lrow, darow);  // dA[row][m] = sum_j L[row][j] P[m][j]
+                    tile_matvec(Pp, lrow, darow);  // dA[row][m] = sum_j L[row][j] P[m][j]
                 } else {
 #pragma unroll
                     for (int m = 0; m < K; ++m) darow[m] = lrow[m];  // P_0 = I
                 }
-                smem_matvec_t<K>(At, lc, mu);
+                tile_matvec_t(At, lc, mu);
                 __syncwarp();
                 if (active) {
                     float *dst = dA + ((bi * T + t) * H + head0 + sub) * K * K + col * K;
@@ -230,7 +231,7 @@ template <int K>
 cudaError_t ms_fwd_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
                      cudaStream_t s) {
     using S = MsShape<K>;
-    using L = MsLayout<S::MF, S::TS, S::NS, 0>;
+    using L = MsLayout<S::MF, S::TS, S::NS, 0, S::TM::kAlign>;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
     const int smem = int(L::warp_bytes * kWarpsPerBlock);
     CUtensorMap tA;
@@ -248,7 +249,7 @@ template <int K>
 cudaError_t ms_bwd_t(const float *A, const float *P, const float *G, float *dA, int64_t B,
                      int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
     using S = MsShape<K>;
-    using L = MsLayout<3 * S::MF, S::TS, S::NS, S::MF>;
+    using L = MsLayout<3 * S::MF, S::TS, S::NS, S::MF, S::TM::kAlign>;
     const int64_t gpb = (H + S::LPW - 1) / S::LPW;
     const int smem = int(L::warp_bytes * kWarpsPerBlock);
     CUtensorMap tA, tG, tP;
@@ -287,7 +288,7 @@ struct MsChunkShape {
     static constexpr int FTS = K >= 16 ? 2 : 4;  // steps per stage, forward
     static constexpr int BTS = 2;                // steps per stage, backward
     static constexpr int NS = 4;
-    using TM = HeadTile<K * K, LPW>;
+    using TM = MatTile<K>;
 };
 
 // Applies, starting from the inclusive value X0 (k x k, row-major, this lane's
@@ -354,11 +355,12 @@ __global__ void __launch_bounds__(32)
                         int64_t C, int64_t Lc, DevCtl ctl) {
     using S = MsChunkShape<K>;
     constexpr int TS = S::FTS, NS = S::NS, BOXF = TS * S::MF;
-    using Lay = MsLayout<S::MF, TS, NS, S::MF>;
+    using Lay = MsLayout<S::MF, TS, NS, S::MF, S::TM::kAlign>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    float *xch = reinterpret_cast<float *>(smem_raw + Lay::ring_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + Lay::ring_bytes + Lay::extra_bytes);
+    unsigned char *sbase = align_smem(smem_raw, S::TM::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    float *xch = reinterpret_cast<float *>(sbase + Lay::ring_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb, items = G * C;
@@ -413,12 +415,12 @@ __global__ void __launch_bounds__(32)
         const int64_t t0 = block_t0(jj);
         const int n = int(min64(TS, tb + len - t0));
         const bool store = !(two_pass && jj < n1);
-        const float *st = ring + size_t(s) * BOXF + sub * K * K;
+        const float *st = ring + size_t(s) * BOXF;
 #pragma unroll
         for (int u = 0; u < TS; ++u) {
             if (u < n) {
                 float nm[K];
-                smem_matvec<K>(st + u * S::MF, m, nm);
+                tile_matvec(TileRef<K>{st, u, sub}, m, nm);
 #pragma unroll
                 for (int i = 0; i < K; ++i) m[i] = nm[i];
                 if (store && active) {
@@ -478,11 +480,12 @@ __global__ void __launch_bounds__(32)
                         int64_t C, int64_t Lc, DevCtl ctl) {
     using S = MsChunkShape<K>;
     constexpr int TS = S::BTS, NS = S::NS, BOXF = TS * S::MF;
-    using Lay = MsLayout<3 * S::MF, TS, NS, S::MF>;
+    using Lay = MsLayout<3 * S::MF, TS, NS, S::MF, S::TM::kAlign>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    float *ring = reinterpret_cast<float *>(smem_raw);
-    float *xch = reinterpret_cast<float *>(smem_raw + Lay::ring_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + Lay::ring_bytes + Lay::extra_bytes);
+    unsigned char *sbase = align_smem(smem_raw, S::TM::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    float *xch = reinterpret_cast<float *>(sbase + Lay::ring_bytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
 
     const int lane = threadIdx.x;
     const int64_t G = B * gpb, items = G * C;
@@ -559,19 +562,17 @@ __global__ void __launch_bounds__(32)
             if (u < n) {
                 const int64_t t = tt - u;
                 const int q = TS - 1 - u;
-                const float *At = st + q * S::MF + sub * K * K;
-                const float *Gt = At + BOXF;
+                const TileRef<K> At{st, q, sub}, Gt{st + BOXF, q, sub}, Pp{st + 2 * BOXF, q, sub};
                 float lc[K];
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt[i * K + col] + mu[i];
+                for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
                 if (p1) {
                     float nm[K];
-                    smem_matvec_t<K>(At, lc, mu);
-                    smem_matvec_t<K>(At, mm, nm);
+                    tile_matvec_t(At, lc, mu);
+                    tile_matvec_t(At, mm, nm);
 #pragma unroll
                     for (int i = 0; i < K; ++i) mm[i] = nm[i];
                 } else {
-                    const float *Pp = At + 2 * BOXF;
 #pragma unroll
                     for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
                     __syncwarp();
@@ -579,12 +580,12 @@ __global__ void __launch_bounds__(32)
 #pragma unroll
                     for (int jx = 0; jx < K; ++jx) lrow[jx] = xw[col * K + jx];
                     if (t >= 1) {
-                        smem_matvec<K>(Pp, lrow, darow);
+                        tile_matvec(Pp, lrow, darow);
                     } else {
 #pragma unroll
                         for (int x = 0; x < K; ++x) darow[x] = lrow[x];
                     }
-                    smem_matvec_t<K>(At, lc, mu);
+                    tile_matvec_t(At, lc, mu);
                     __syncwarp();
                     if (active) {
                         float *dst = dA + ((bi * T + t) * H + head0 + sub) * K * K + col * K;
@@ -651,7 +652,7 @@ template <int K>
 cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
                            unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
-    using Lay = MsLayout<S::MF, S::FTS, S::NS, S::MF>;
+    using Lay = MsLayout<S::MF, S::FTS, S::NS, S::MF, S::TM::kAlign>;
     CUtensorMap tA;
     cudaError_t e;
     if ((e = S::TM::make(&tA, A, B * T, H, S::FTS)) != cudaSuccess) return e;
@@ -668,7 +669,7 @@ template <int K>
 cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float *dA, int64_t B, int64_t T,
                            int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
-    using Lay = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF>;
+    using Lay = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF, S::TM::kAlign>;
     CUtensorMap tA, tG, tP;
     cudaError_t e;
     if ((e = S::TM::make(&tA, A, B * T, H, S::BTS)) != cudaSuccess) return e;
