@@ -141,11 +141,16 @@ __device__ __forceinline__ void group_matvec(float *xw, int col, const float (&x
     __syncwarp();
 }
 
-// Publishes `value` for this item: every lane fences its data, lane 0 releases.
+// Publishes `value` for this item once the whole warp has stored its data.
+// The warp barrier orders every lane's data stores before lane 0's fence and
+// release store (one fence per warp rather than one per lane).
 __device__ __forceinline__ void publish(unsigned *flag, unsigned value, int lane) {
-    __threadfence();
     __syncwarp();
-    if (lane == 0) st_release_gpu(flag, value);
+    if (lane == 0) {
+        __threadfence();
+        st_release_gpu(flag, value);
+    }
+    __syncwarp();
 }
 
 // Lane 0 waits (bounded) for a nonzero flag and broadcasts the value it saw;

@@ -19,14 +19,20 @@
 namespace mgs {
 namespace {
 
-template <int K>
+#ifndef MGS_MAS_FWD_NS
+#define MGS_MAS_FWD_NS 4
+#endif
+#ifndef MGS_MAS_FWD_TS8
+#define MGS_MAS_FWD_TS8 8
+#endif
+template <int K, bool FWD = false>
 struct MasShape {
     static constexpr int LPW = 32 / K;          // lanes (heads) per warp
     static constexpr int AF = LPW * K * K;      // floats of A per time step
     static constexpr int VF = LPW * K;          // floats of one per-lane vector per time step
     // time steps per stage: about 8-10 KB of A per stage
-    static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? 8 : 16);
-    static constexpr int NS = 4;                // stages in flight
+    static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? (FWD ? MGS_MAS_FWD_TS8 : 8) : 16);
+    static constexpr int NS = FWD ? MGS_MAS_FWD_NS : 4;  // stages in flight
     using TA = MatTile<K, false>;
     using TV = HeadTile<K, LPW>;
 };
@@ -98,7 +104,7 @@ __global__ void __launch_bounds__(32)
     mas_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float *__restrict__ h0, float *__restrict__ h, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
-    using S = MasShape<K>;
+    using S = MasShape<K, true>;
     constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
     using R = Ring<STAGEF, S::NS, S::TA::kAlign>;
     constexpr int SSTR = int(R::stage_stride / sizeof(float));
@@ -298,7 +304,7 @@ __global__ void __launch_bounds__(32)
 template <int K>
 cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
                       int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
-    using S = MasShape<K>;
+    using S = MasShape<K, true>;
     using R = Ring<S::TS * (S::AF + S::VF), S::NS, S::TA::kAlign>;
     CUtensorMap tA, tB;
     cudaError_t e;
