@@ -509,6 +509,33 @@ def run_gpu(args):
                                          "fwd_bwd_GBps": round(nbytes / ((fm + bm) * 1e-3) / 1e9, 1),
                                          "l2": "flushed"}
             del r
+        # parallel_scan_log backward in recompute mode (h not saved) on the
+        # minGRU shape: DRAM bytes are 28 per element (log_coeffs and
+        # log_values read by both passes, grad_h read, two gradients written)
+        for r in runners:
+            w = r.w
+            if w.op != "psl":
+                continue
+            d = r.inp
+            ws, nws = api.workspace(b.MGS_OP_PARALLEL_SCAN_LOG_BWD, w.B, w.T, w.H, 0, device)
+            ts = []
+            for it in range(args.warmup + 10):
+                flush.zero_()
+                e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+                e0.record(stream)
+                b.mgs_parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], None, d["grad_h"],
+                                            r.dlc, r.dlv, r.dl0, w.B, w.T, w.H, ws, nws, sid)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    ts.append(e0.elapsed_time(e1))
+            bm = statistics.median(ts)
+            nbytes = w.B * w.T * w.H * 28 + 2 * w.B * w.H * 4 + 2 * nws
+            extra[f"psl_c{w.cid}_bwd_recompute"] = {
+                "shape": w.name, "bwd_us": round(bm * 1e3, 2), "workspace_bytes": nws,
+                "GBps": round(nbytes / (bm * 1e-3) / 1e9, 1),
+                "bytes": "28 per element + checkpoints", "l2": "flushed"}
+            del ws
         b.mgs_check(sid)
 
     cpu = None

@@ -78,7 +78,8 @@ enum {
 /* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
  * matrix ops and D for parallel_scan_log; k is ignored for the latter).
  * Returns 0 when no workspace is needed, and also for invalid shapes (the
- * entry point then reports the error). */
+ * entry point then reports the error).  MGS_OP_PARALLEL_SCAN_LOG_BWD gives the
+ * bytes of the recompute mode (h == NULL); with h saved it needs none. */
 size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k);
 
 /* matrix_affine_scan, forward ("mingru-scans" home page, scan-op table,
@@ -171,9 +172,17 @@ mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_v
  *     d_log_coeffs_t = lambda_t a_t h_{t-1},
  *     d_log_h0 = lambda_1 a_1 h_0.
  * In: log_coeffs, log_values, log_h0 (nullable: h_0 = 0), h = the forward
- *     output (saved; must not be NULL), grad_h.
+ *     output (nullable, see below), grad_h.
  * Out: d_log_coeffs, d_log_values [B][T][D]; d_log_h0 [B][D] (nullable; must
- *     be NULL when log_h0 is NULL). */
+ *     be NULL when log_h0 is NULL).
+ * With h saved, no workspace is needed.  With h == NULL the forward is
+ * recomputed inside the call (the pages' log op recomputes its forward in
+ * backward): one forward pass stores log2 h every 16 steps in the workspace,
+ * then each 16-step segment's h is rebuilt from its checkpoint as the reverse
+ * sweep reaches it.  That needs mgs_workspace_size(MGS_OP_PARALLEL_SCAN_LOG_BWD,
+ * B, T, D, 0) = 4 * B * ceil(T / 16) * D bytes, 256-byte aligned (else
+ * MGS_ERR_WORKSPACE), reads log_coeffs and log_values twice, and gives the
+ * same results as passing the h this library's forward wrote. */
 mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_values,
                                      const float *log_h0, const float *h, const float *grad_h,
                                      float *d_log_coeffs, float *d_log_values, float *d_log_h0,

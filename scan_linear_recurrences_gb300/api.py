@@ -93,17 +93,24 @@ def parallel_scan_log_fwd(log_coeffs, log_values, log_h0=None, want_log=False, s
 
 
 def parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, stream=None):
-    """Returns (d_log_coeffs, d_log_values, d_log_h0 or None)."""
+    """Returns (d_log_coeffs, d_log_values, d_log_h0 or None).
+
+    h is the saved forward output, or None to recompute it inside the call
+    (checkpoints every 16 steps in a workspace of 4*B*ceil(T/16)*D bytes)."""
     B, T, D = log_coeffs.shape
-    for t, n in ((log_coeffs, "log_coeffs"), (log_values, "log_values"), (h, "h"), (grad_h, "grad_h")):
+    for t, n in ((log_coeffs, "log_coeffs"), (log_values, "log_values"), (grad_h, "grad_h")):
         _check(t, n, (B, T, D))
+    if h is not None:
+        _check(h, "h", (B, T, D))
     if log_h0 is not None:
         _check(log_h0, "log_h0", (B, D))
     dlc = torch.empty_like(log_coeffs)
     dlv = torch.empty_like(log_values)
     dl0 = torch.empty_like(log_h0) if log_h0 is not None else None
+    ws, nws = (None, 0) if h is not None else \
+        workspace(_b.MGS_OP_PARALLEL_SCAN_LOG_BWD, B, T, D, 0, log_coeffs.device)
     _b.mgs_parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, dlc, dlv, dl0, B, T, D,
-                                 None, 0, stream)
+                                 ws, nws, stream)
     return dlc, dlv, dl0
 
 
@@ -171,20 +178,23 @@ class MatrixScan(torch.autograd.Function):
 
 class ParallelScanLog(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, log_coeffs, log_values, log_h0=None):
+    def forward(ctx, log_coeffs, log_values, log_h0=None, recompute=False):
         lc, lv = log_coeffs.contiguous(), log_values.contiguous()
         l0 = log_h0.contiguous() if log_h0 is not None else None
         h = parallel_scan_log_fwd(lc, lv, l0)
-        ctx.save_for_backward(lc, lv, l0 if l0 is not None else torch.empty(0, device=lc.device), h)
+        empty = torch.empty(0, device=lc.device)
+        ctx.save_for_backward(lc, lv, l0 if l0 is not None else empty, empty if recompute else h)
         ctx.has_h0 = log_h0 is not None
+        ctx.recompute = recompute
         return h
 
     @staticmethod
     def backward(ctx, grad_h):
         lc, lv, l0, h = ctx.saved_tensors
         l0 = l0 if ctx.has_h0 else None
+        h = None if ctx.recompute else h
         dlc, dlv, dl0 = parallel_scan_log_bwd(lc, lv, l0, h, grad_h.contiguous())
-        return dlc, dlv, dl0
+        return dlc, dlv, dl0, None
 
 
 class LinearScan(torch.autograd.Function):
@@ -217,5 +227,6 @@ def matrix_scan(A):
     return MatrixScan.apply(A)
 
 
-def parallel_scan_log(log_coeffs, log_values, log_h0=None):
-    return ParallelScanLog.apply(log_coeffs, log_values, log_h0)
+def parallel_scan_log(log_coeffs, log_values, log_h0=None, recompute=False):
+    """recompute=True keeps no copy of h for backward; backward rebuilds it."""
+    return ParallelScanLog.apply(log_coeffs, log_values, log_h0, recompute)

@@ -168,6 +168,8 @@ cudaError_t ensure_smem_attr(const void *fn, int bytes) {
 
 extern "C" {
 
+static mgs_status psl_sizes(int64_t B, int64_t T, int64_t D, int64_t *n, int64_t *n0);
+
 size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
     BlockSizes s;
     switch (op) {
@@ -183,6 +185,11 @@ size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
         case MGS_OP_MATRIX_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
             return mgs::ms_workspace_bytes(B, T, H_or_D, k, op == MGS_OP_MATRIX_SCAN_BWD);
+        case MGS_OP_PARALLEL_SCAN_LOG_BWD: {
+            int64_t n, n0;
+            if (psl_sizes(B, T, H_or_D, &n, &n0) != MGS_OK || n == 0) return 0;
+            return mgs::psl_recompute_workspace_bytes(B, T, H_or_D);
+        }
         default:
             return 0;
     }
@@ -323,15 +330,21 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
         return from_cuda(cudaMemsetAsync(d_log_h0, 0, size_t(n0) * sizeof(float),
                                          reinterpret_cast<cudaStream_t>(stream)));
     }
-    if ((st = check_ptrs({log_coeffs, log_values, h, grad_h, d_log_coeffs, d_log_values},
-                         {log_h0, d_log_h0})) != MGS_OK)
+    if ((st = check_ptrs({log_coeffs, log_values, grad_h, d_log_coeffs, d_log_values},
+                         {log_h0, h, d_log_h0})) != MGS_OK)
         return st;
     if (!disjoint({{d_log_coeffs, n}, {d_log_values, n}, {d_log_h0, d_log_h0 ? n0 : 0}},
-                  {{log_coeffs, n}, {log_values, n}, {log_h0, log_h0 ? n0 : 0}, {h, n}, {grad_h, n}}))
+                  {{log_coeffs, n}, {log_values, n}, {log_h0, log_h0 ? n0 : 0}, {h, h ? n : 0},
+                   {grad_h, n}}))
         return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    const size_t need = (h == nullptr) ? mgs::psl_recompute_workspace_bytes(B, T, D) : 0;
+    if ((st = check_ws(need, workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    if (h == nullptr)
+        return from_cuda(mgs::launch_psl_bwd_recompute(log_coeffs, log_values, log_h0, grad_h, d_log_coeffs,
+                                                       d_log_values, d_log_h0, workspace, B, T, D, ctl,
+                                                       reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(mgs::launch_psl_bwd(log_coeffs, log_values, log_h0, h, grad_h, d_log_coeffs,
                                          d_log_values, d_log_h0, B, T, D, ctl,
                                          reinterpret_cast<cudaStream_t>(stream)));

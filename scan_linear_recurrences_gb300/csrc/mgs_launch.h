@@ -38,6 +38,10 @@ cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G,
 cudaError_t launch_psl_fwd(const float *lc, const float *lv, const float *lh0, float *h,
                            float *logh, int64_t B, int64_t T, int64_t D, const DevCtl &ctl,
                            cudaStream_t s);
+size_t psl_recompute_workspace_bytes(int64_t B, int64_t T, int64_t D);
+cudaError_t launch_psl_bwd_recompute(const float *lc, const float *lv, const float *lh0, const float *gh,
+                                     float *dlc, float *dlv, float *dlh0, void *ws, int64_t B, int64_t T,
+                                     int64_t D, const DevCtl &ctl, cudaStream_t s);
 cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, const float *h,
                            const float *gh, float *dlc, float *dlv, float *dlh0, int64_t B,
                            int64_t T, int64_t D, const DevCtl &ctl, cudaStream_t s);

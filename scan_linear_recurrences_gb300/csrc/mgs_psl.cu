@@ -264,6 +264,192 @@ __global__ void __launch_bounds__(32)
     }
 }
 
+
+// ---------------------------------------------------------------- backward, recomputing h
+// Backward without the saved forward output (the pages' log-space op
+// recomputes its forward).  Phase A runs the forward recurrence once over the
+// whole sequence and writes log2 h at the start of every kRcS-step segment to
+// the workspace.  Phase B walks the segments from the last to the first: each
+// segment's log_coeffs, log_values and grad_h arrive by TMA into one of two
+// buffers (the next segment's loads are in flight while this one is used), h
+// over the segment is recomputed from its checkpoint into registers, and the
+// reverse sweep of the saved-h kernel runs over it.  DRAM traffic is 28
+// bytes per element (log_coeffs and log_values are read twice) against 24 with
+// the saved h; what it saves is keeping h.
+constexpr int kRcS = 16;   // steps per segment (checkpoint spacing)
+constexpr int kRcNA = 3;   // phase-A stages
+
+struct RcLayout {
+    static constexpr int BOXF = kRcS * kChan;                        // floats per tensor box
+    static constexpr size_t a_bytes = size_t(kRcNA) * 2 * BOXF * 4;  // phase A: lc, lv per stage
+    static constexpr size_t b_bytes = size_t(2) * 3 * BOXF * 4;      // phase B: 2 x (lc, lv, g)
+    static constexpr size_t ring_bytes = a_bytes > b_bytes ? a_bytes : b_bytes;
+    static constexpr size_t warp_bytes = align_up(ring_bytes + (kRcNA + 2) * sizeof(uint64_t), 128);
+};
+
+__global__ void __launch_bounds__(32)
+    psl_bwd_recompute_kernel(const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmV,
+                             const __grid_constant__ CUtensorMap tmG, const float *__restrict__ lh0,
+                             float *__restrict__ dlc, float *__restrict__ dlv, float *__restrict__ dlh0,
+                             float *__restrict__ ckpt, int64_t B, int64_t T, int64_t D, int64_t groups_per_b,
+                             DevCtl ctl) {
+    using L = RcLayout;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
+    if (g >= B * groups_per_b) return;
+    float *ring = reinterpret_cast<float *>(smem_raw);
+    uint64_t *barsA = reinterpret_cast<uint64_t *>(smem_raw + L::ring_bytes);
+    uint64_t *barsB = barsA + kRcNA;
+
+    const int64_t bi = g / groups_per_b;
+    const int c0 = int(g % groups_per_b) * kChan;
+    const bool active = c0 + 4 * lane < D;
+    const int64_t nseg = (T + kRcS - 1) / kRcS;
+    const int row0 = int(bi * T);
+    float *ck = ckpt + bi * nseg * D + c0 + 4 * lane;  // checkpoint of segment j at ck + j*D
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+        prefetch_tmap(&tmC);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+    }
+
+    // ---- phase A: forward, checkpoints
+    float4 Lg;
+    if (lh0 != nullptr && active) {
+        const float4 l = ld4(lh0 + bi * D + c0 + 4 * lane);
+        Lg = make_float4(l.x * kLog2e, l.y * kLog2e, l.z * kLog2e, l.w * kLog2e);
+    } else {
+        Lg = make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+    }
+    const float4 L0 = Lg;
+    if (active) *reinterpret_cast<float4 *>(ck) = Lg;
+    {
+        WarpRing<kRcNA> ra;
+        ra.init(barsA, lane);
+        auto issueA = [&](int s, int64_t j) {  // lane 0 only
+            float *st = ring + size_t(s) * 2 * L::BOXF;
+            mbar_arrive_expect_tx(&barsA[s], uint32_t(2 * L::BOXF * 4));
+            tma_load_2d(st, &tmC, c0, row0 + int(j * kRcS), &barsA[s], pol);
+            tma_load_2d(st + L::BOXF, &tmV, c0, row0 + int(j * kRcS), &barsA[s], pol);
+        };
+        const int npro = int(min64(kRcNA, nseg));
+        if (lane == 0)
+            for (int s = 0; s < npro; ++s) issueA(s, s);
+        for (int s = 0; s < npro; ++s) ra.armed(s);
+        for (int64_t j = 0; j < nseg; ++j) {
+            const int s = int(j % kRcNA);
+            if (!ra.wait(s, ctl)) {
+                if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+                ra.drain(ctl, lane);
+                return;
+            }
+            const int n = int(min64(kRcS, T - j * kRcS));
+            const float *sc = ring + size_t(s) * 2 * L::BOXF + 4 * lane;
+            const float *sv = sc + L::BOXF;
+#pragma unroll
+            for (int u = 0; u < kRcS; ++u) {
+                if (u < n) {
+                    const float4 a = ld4(sc + u * kChan), v = ld4(sv + u * kChan);
+                    Lg.x = logaddexp2_f(fmaf(a.x, kLog2e, Lg.x), v.x * kLog2e);
+                    Lg.y = logaddexp2_f(fmaf(a.y, kLog2e, Lg.y), v.y * kLog2e);
+                    Lg.z = logaddexp2_f(fmaf(a.z, kLog2e, Lg.z), v.z * kLog2e);
+                    Lg.w = logaddexp2_f(fmaf(a.w, kLog2e, Lg.w), v.w * kLog2e);
+                }
+            }
+            __syncwarp();
+            if (j + kRcNA < nseg) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    issueA(s, j + kRcNA);
+                }
+                ra.armed(s);
+            }
+            if (j + 1 < nseg && active) *reinterpret_cast<float4 *>(ck + (j + 1) * D) = Lg;
+        }
+    }
+
+    // ---- phase B: segments from the last to the first
+    __syncwarp();
+    if (lane == 0) fence_proxy_async_smem();  // phase-A reads of the ring precede phase-B copies into it
+    WarpRing<2> rb;
+    rb.init(barsB, lane);
+    auto issueB = [&](int buf, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(buf) * 3 * L::BOXF;
+        mbar_arrive_expect_tx(&barsB[buf], uint32_t(3 * L::BOXF * 4));
+        tma_load_2d(st, &tmC, c0, row0 + int(j * kRcS), &barsB[buf], pol);
+        tma_load_2d(st + L::BOXF, &tmV, c0, row0 + int(j * kRcS), &barsB[buf], pol);
+        tma_load_2d(st + 2 * L::BOXF, &tmG, c0, row0 + int(j * kRcS), &barsB[buf], pol);
+    };
+    const int nprob = int(min64(2, nseg));
+    if (lane == 0)
+        for (int b2 = 0; b2 < nprob; ++b2) issueB(b2, nseg - 1 - b2);
+    for (int b2 = 0; b2 < nprob; ++b2) rb.armed(b2);
+
+    float4 nx = make_float4(0.f, 0.f, 0.f, 0.f);  // a_{t+1} lambda_{t+1}
+    for (int64_t jj = 0; jj < nseg; ++jj) {
+        const int64_t j = nseg - 1 - jj;
+        const int buf = int(jj & 1);
+        if (!rb.wait(buf, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rb.drain(ctl, lane);
+            return;
+        }
+        const int n = int(min64(kRcS, T - j * kRcS));
+        const float *sc = ring + size_t(buf) * 3 * L::BOXF + 4 * lane;
+        const float *sv = sc + L::BOXF;
+        const float *sg = sc + 2 * L::BOXF;
+        const float4 Ls = active ? ld4(ck + j * D) : L0;
+        // h over the segment, from its checkpoint
+        float4 hreg[kRcS];
+        float4 Lr = Ls;
+#pragma unroll
+        for (int u = 0; u < kRcS; ++u) {
+            if (u < n) {
+                const float4 a = ld4(sc + u * kChan), v = ld4(sv + u * kChan);
+                Lr.x = logaddexp2_f(fmaf(a.x, kLog2e, Lr.x), v.x * kLog2e);
+                Lr.y = logaddexp2_f(fmaf(a.y, kLog2e, Lr.y), v.y * kLog2e);
+                Lr.z = logaddexp2_f(fmaf(a.z, kLog2e, Lr.z), v.z * kLog2e);
+                Lr.w = logaddexp2_f(fmaf(a.w, kLog2e, Lr.w), v.w * kLog2e);
+                hreg[u] = make_float4(ex2_approx(Lr.x), ex2_approx(Lr.y), ex2_approx(Lr.z), ex2_approx(Lr.w));
+            }
+        }
+        const float4 hstart = make_float4(ex2_approx(Ls.x), ex2_approx(Ls.y), ex2_approx(Ls.z), ex2_approx(Ls.w));
+        // reverse sweep over the segment
+#pragma unroll
+        for (int u = kRcS - 1; u >= 0; --u) {
+            if (u < n) {
+                const float4 c = ld4(sc + u * kChan), v = ld4(sv + u * kChan), gg = ld4(sg + u * kChan);
+                const float4 hp = (u >= 1) ? hreg[u >= 1 ? u - 1 : 0] : hstart;
+                const float4 a = make_float4(ex2_approx(c.x * kLog2e), ex2_approx(c.y * kLog2e),
+                                             ex2_approx(c.z * kLog2e), ex2_approx(c.w * kLog2e));
+                const float4 lam = make_float4(gg.x + nx.x, gg.y + nx.y, gg.z + nx.z, gg.w + nx.w);
+                nx = make_float4(a.x * lam.x, a.y * lam.y, a.z * lam.z, a.w * lam.w);
+                if (active) {
+                    const int64_t o = (bi * T + j * kRcS + u) * D + c0 + 4 * lane;
+                    st_cs4(dlv + o, make_float4(lam.x * ex2_approx(v.x * kLog2e), lam.y * ex2_approx(v.y * kLog2e),
+                                                lam.z * ex2_approx(v.z * kLog2e), lam.w * ex2_approx(v.w * kLog2e)));
+                    st_cs4(dlc + o, make_float4(nx.x * hp.x, nx.y * hp.y, nx.z * hp.z, nx.w * hp.w));
+                }
+            }
+        }
+        __syncwarp();
+        if (jj + 2 < nseg) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issueB(buf, j - 2);
+            }
+            rb.armed(buf);
+        }
+    }
+    if (dlh0 != nullptr && active) {
+        const float4 h0v = make_float4(ex2_approx(L0.x), ex2_approx(L0.y), ex2_approx(L0.z), ex2_approx(L0.w));
+        *reinterpret_cast<float4 *>(dlh0 + bi * D + c0 + 4 * lane) =
+            make_float4(nx.x * h0v.x, nx.y * h0v.y, nx.z * h0v.z, nx.w * h0v.w);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_psl_fwd(const float *lc, const float *lv, const float *lh0, float *h,
@@ -299,6 +485,29 @@ cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, c
     const int smem = int(R::warp_bytes);
     if ((e = ensure_smem_attr((const void *)psl_bwd_kernel, smem)) != cudaSuccess) return e;
     psl_bwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tC, tV, tG, tH, lh0, dlc, dlv, dlh0, B, T, D, gpb, ctl);
+    return cudaGetLastError();
+}
+
+size_t psl_recompute_workspace_bytes(int64_t B, int64_t T, int64_t D) {
+    const int64_t nseg = (T + kRcS - 1) / kRcS;
+    return size_t(B) * size_t(nseg) * size_t(D) * sizeof(float);
+}
+
+cudaError_t launch_psl_bwd_recompute(const float *lc, const float *lv, const float *lh0, const float *gh,
+                                     float *dlc, float *dlv, float *dlh0, void *ws, int64_t B, int64_t T,
+                                     int64_t D, const DevCtl &ctl, cudaStream_t s) {
+    CUtensorMap tC, tV, tG;
+    cudaError_t e;
+    if ((e = make_rows_map(&tC, lc, B * T, D, kRcS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tV, lv, B * T, D, kRcS)) != cudaSuccess) return e;
+    if ((e = make_rows_map(&tG, gh, B * T, D, kRcS)) != cudaSuccess) return e;
+    const int64_t gpb = (D + kChan - 1) / kChan;
+    const int64_t blocks = B * gpb;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const int smem = int(RcLayout::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)psl_bwd_recompute_kernel, smem)) != cudaSuccess) return e;
+    psl_bwd_recompute_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tC, tV, tG, lh0, dlc, dlv, dlh0,
+                                                                     static_cast<float *>(ws), B, T, D, gpb, ctl);
     return cudaGetLastError();
 }
 

@@ -82,8 +82,26 @@ def test_ms_and_psl_validation(L):
     # d_log_h0 without log_h0 has no meaning
     assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, h, FAKE + (3 << 30), FAKE + (4 << 30),
                FAKE + (5 << 30), FAKE + (6 << 30), 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+    # h == NULL: the recompute mode, which needs its checkpoint workspace
     assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, None, FAKE + (3 << 30), FAKE + (4 << 30),
-               FAKE + (5 << 30), None, 2, 8, 8) == b.MGS_ERR_INVALID_ARG
+               FAKE + (5 << 30), None, 2, 8, 8) == b.MGS_ERR_WORKSPACE
+    assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, None, FAKE + (3 << 30), FAKE + (4 << 30),
+               FAKE + (5 << 30), None, 2, 8, 8, FAKE + (6 << 30), 63) == b.MGS_ERR_WORKSPACE
+    # still validated: outputs overlapping inputs
+    assert _st(b.mgs_parallel_scan_log_bwd, lc, lv, None, None, FAKE + (3 << 30), lv,
+               FAKE + (5 << 30), None, 2, 8, 8, FAKE + (6 << 30), 64) == b.MGS_ERR_INVALID_ARG
+
+
+def test_psl_recompute_workspace_size(L):
+    op = b.MGS_OP_PARALLEL_SCAN_LOG_BWD
+    # 4 bytes per channel per 16-step segment: log2 h at each segment start
+    assert b.mgs_workspace_size(op, 2, 8, 8, 0) == 4 * 2 * 1 * 8
+    assert b.mgs_workspace_size(op, 2, 16, 8, 0) == 4 * 2 * 1 * 8
+    assert b.mgs_workspace_size(op, 2, 17, 8, 0) == 4 * 2 * 2 * 8
+    assert b.mgs_workspace_size(op, 64, 4096, 1024, 0) == 4 * 64 * 256 * 1024
+    assert b.mgs_workspace_size(op, 2, 0, 8, 0) == 0
+    assert b.mgs_workspace_size(op, 2, 16, 6, 0) == 0  # D % 4: the call reports it
+    assert b.mgs_workspace_size(b.MGS_OP_PARALLEL_SCAN_LOG_FWD, 64, 4096, 1024, 0) == 0
 
 
 def test_linear_scan_validation(L):

@@ -219,6 +219,63 @@ def test_psl_zero_coefficients_and_empty():
     assert api.parallel_scan_log_fwd(empty, empty).shape == (0, 5, 8)
 
 
+@pytest.mark.parametrize("B,T,D,h0", [
+    (2, 1, 4, True), (3, 15, 132, True), (2, 16, 8, False), (2, 17, 1024, True), (3, 50, 260, False),
+    (2, 257, 1024, True), (1, 2000, 128, True), (5, 33, 36, True),
+])
+def test_psl_recompute_backward(B, T, D, h0):
+    """h == NULL: checkpoints every 16 steps, segments rebuilt in reverse; ragged
+    last segments, T below one segment and partial 128-channel groups."""
+    d = _cuda(inputs.psl_inputs(B, T, D, seed=700 + B * T + D, with_h0=h0))
+    lc, lv, l0, g = d["log_coeffs"], d["log_values"], d["log_h0"], d["grad_h"]
+    h = api.parallel_scan_log_fwd(lc, lv, l0)
+    saved = api.parallel_scan_log_bwd(lc, lv, l0, h, g)
+    rec = api.parallel_scan_log_bwd(lc, lv, l0, None, g)
+    b.mgs_check()
+    dlcr, dlvr, dl0r = oracle.psl_bwd(lc.cpu(), lv.cpu(), l0.cpu() if h0 else None, g.cpu())
+    assert_close("d_log_coeffs", rec[0], dlcr, T)
+    assert_close("d_log_values", rec[1], dlvr, T)
+    if h0:
+        assert_close("d_log_h0", rec[2], dl0r, T)
+    else:
+        assert rec[2] is None
+    # the recomputed h follows the forward kernel's arithmetic step for step
+    for name, x, y in zip(("d_log_coeffs", "d_log_values", "d_log_h0"), rec, saved):
+        if y is not None:
+            assert_close(name + " (vs saved h)", x, y.double().cpu().numpy(), T, rel_tol=1e-6, abs_tol=1e-5)
+
+
+def test_psl_recompute_config3_sampled_rows():
+    w = inputs.WORKLOADS[3]
+    d = w.make(device="cuda")
+    dlc, dlv, dl0 = api.parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], None, d["grad_h"])
+    b.mgs_check()
+    rows = [0, 33, w.B - 1]
+    dlcr, dlvr, dl0r = oracle.psl_bwd(*(d[k][rows].cpu() for k in ("log_coeffs", "log_values", "log_h0",
+                                                                   "grad_h")))
+    assert_close("d_log_coeffs", dlc[rows], dlcr, w.T)
+    assert_close("d_log_values", dlv[rows], dlvr, w.T)
+    assert_close("d_log_h0", dl0[rows], dl0r, w.T)
+
+
+def test_psl_recompute_autograd_and_T0():
+    d = _cuda(inputs.psl_inputs(2, 70, 12, seed=9))
+    lc = d["log_coeffs"].clone().requires_grad_(True)
+    lv = d["log_values"].clone().requires_grad_(True)
+    l0 = d["log_h0"].clone().requires_grad_(True)
+    (api.parallel_scan_log(lc, lv, l0, recompute=True) * d["grad_h"]).sum().backward()
+    dlcr, dlvr, dl0r = oracle.psl_bwd(*(d[k].cpu() for k in ("log_coeffs", "log_values", "log_h0", "grad_h")))
+    assert_close("d_log_coeffs", lc.grad, dlcr, 70)
+    assert_close("d_log_values", lv.grad, dlvr, 70)
+    assert_close("d_log_h0", l0.grad, dl0r, 70)
+    # T = 0: d_log_h0 = 0, nothing else written
+    e = torch.empty((2, 0, 12), device="cuda")
+    z = torch.randn((2, 12), device="cuda")
+    _, _, dz = api.parallel_scan_log_bwd(e, e, z, None, e)
+    b.mgs_check()
+    assert torch.equal(dz, torch.zeros_like(z))
+
+
 # ---------------------------------------------------------------- linear_scan
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 77, 132, True), (2, 300, 64, True), (1, 2000, 32, False), (4, 500, 1024, True),
