@@ -1,4 +1,5 @@
-"""Float64 CPU oracle for matrix_affine_scan, matrix_scan and parallel_scan_log.
+"""Float64 CPU oracle for matrix_affine_scan, matrix_scan, parallel_scan_log,
+linear_scan and the Givens-mesh (angle-parameterised) affine and matrix scans.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -58,9 +59,14 @@ def _load():
             lib.oracle_psl_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64]
             lib.oracle_linear_fwd.argtypes = [dp, dp, dp, dp, i64, i64, i64]
             lib.oracle_linear_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64]
+            lib.oracle_gas_fwd.argtypes = [dp, dp, dp, dp, dp, i64, i64, i64, i64]
+            lib.oracle_gas_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64]
+            lib.oracle_gms_fwd.argtypes = [dp, dp, i64, i64, i64, i64]
+            lib.oracle_gms_bwd.argtypes = [dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_num_threads.restype = ctypes.c_int
             for f in ("oracle_mas_fwd", "oracle_mas_bwd", "oracle_ms_fwd", "oracle_ms_bwd",
-                      "oracle_psl_fwd", "oracle_psl_bwd", "oracle_linear_fwd", "oracle_linear_bwd"):
+                      "oracle_psl_fwd", "oracle_psl_bwd", "oracle_linear_fwd", "oracle_linear_bwd",
+                      "oracle_gas_fwd", "oracle_gas_bwd", "oracle_gms_fwd", "oracle_gms_bwd"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -174,3 +180,62 @@ def linear_bwd(a, b, h0, grad_h, want_dh0=True):
     dh0 = np.empty((B, D), dtype=np.float64) if want_dh0 else None
     _load().oracle_linear_bwd(_p(a), _p(b), _p(h0), _p(g), _p(da), _p(db), _p(dh0), B, T, D)
     return da, db, dh0
+
+
+# ---------------------------------------------------------------- Givens mesh
+def n_angles(K):
+    """Angles of the K-coordinate brick-wall mesh: K(K-1)/2."""
+    return K * (K - 1) // 2
+
+
+def _k_of(N):
+    K = int(round((1 + (1 + 8 * N) ** 0.5) / 2))
+    assert n_angles(K) == N, f"{N} is not K(K-1)/2"
+    return K
+
+
+def gas_fwd(theta, a, b, h0=None):
+    """h_t = G(theta_t) diag(a_t) h_{t-1} + b_t.  theta [B,T,H,N], a [B,T,H,K] or None,
+    b [B,T,H,K], h0 [B,H,K] or None -> h [B,T,H,K]."""
+    th, a, b, h0 = _f64(theta), _f64(a), _f64(b), _f64(h0)
+    B, T, H, K = b.shape
+    assert th.shape == (B, T, H, n_angles(K)) and (a is None or a.shape == b.shape)
+    assert h0 is None or h0.shape == (B, H, K)
+    h = np.empty((B, T, H, K), dtype=np.float64)
+    _load().oracle_gas_fwd(_p(th), _p(a), _p(b), _p(h0), _p(h), B, T, H, K)
+    return h
+
+
+def gas_bwd(theta, a, b, h0, grad_h):
+    """Gradients of sum <grad_h, h> -> (dtheta, da or None, db, dh0 or None)."""
+    th, a, b, h0, g = _f64(theta), _f64(a), _f64(b), _f64(h0), _f64(grad_h)
+    B, T, H, K = b.shape
+    assert th.shape == (B, T, H, n_angles(K)) and g.shape == b.shape
+    dth = np.empty_like(th)
+    da = np.empty_like(b) if a is not None else None
+    db = np.empty_like(b)
+    dh0 = np.empty((B, H, K), dtype=np.float64) if h0 is not None else None
+    _load().oracle_gas_bwd(_p(th), _p(a), _p(b), _p(h0), _p(g), _p(dth), _p(da), _p(db), _p(dh0),
+                           B, T, H, K)
+    return dth, da, db, dh0
+
+
+def gms_fwd(theta):
+    """P_t = G(theta_t) P_{t-1}, P_0 = I.  theta [B,T,H,N] -> P [B,T,H,K,K]."""
+    th = _f64(theta)
+    B, T, H, N = th.shape
+    K = _k_of(N)
+    P = np.empty((B, T, H, K, K), dtype=np.float64)
+    _load().oracle_gms_fwd(_p(th), _p(P), B, T, H, K)
+    return P
+
+
+def gms_bwd(theta, grad_P):
+    """Gradient of sum <grad_P, P>_F with respect to the angles -> dtheta [B,T,H,N]."""
+    th, G = _f64(theta), _f64(grad_P)
+    B, T, H, N = th.shape
+    K = _k_of(N)
+    assert G.shape == (B, T, H, K, K)
+    dth = np.empty_like(th)
+    _load().oracle_gms_bwd(_p(th), _p(G), _p(dth), B, T, H, K)
+    return dth

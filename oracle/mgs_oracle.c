@@ -20,6 +20,9 @@
  *   parallel_scan_log   h_t = e^{lc_t} h_{t-1} + e^{lv_t}  in log space,
  *                       Heinsen (2023, arXiv:2311.06281), cited on the
  *                       home page's lineage paragraph.
+ *   Givens affine scan  matrix_affine_scan with A_t = G(theta_t) diag(a_t),
+ *   Givens matrix scan  matrix_scan with A_t = G(theta_t): the brick-wall
+ *                       rotation mesh of GivensMinGRU, fed by its angles.
  * Backward passes are the adjoint (reverse-mode) recurrences of those maps.
  *
  * Layouts (row-major, contiguous, double):
@@ -356,6 +359,272 @@ void oracle_linear_bwd(const double *a, const double *bv, const double *h0, cons
         if (dh0)
             dh0[bb * D + d] = nxt;
         free(hs);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Givens-mesh (angle-parameterised) matrix_affine_scan / matrix_scan   */
+/* ------------------------------------------------------------------ */
+
+/* The GivensMinGRU transition ("mingru-scans" home page, lineage paragraph:
+ * the brick-wall mesh of Clements et al. 2016 / EUNN, built from Golub & Van
+ * Loan's plane rotations; "Run the benchmarks", Step 3: the angle-fused
+ * backward).  For K coordinates the mesh has K layers; layer l = 1..K rotates
+ * the disjoint pairs (p, p+1) with p = 0, 2, 4, ... for odd l and p = 1, 3,
+ * 5, ... for even l (p+1 < K, no wrap-around), K(K-1)/2 angles in all,
+ * consumed layer by layer, pairs ascending.  The rotation of angle th on pair
+ * (p, p+1) maps (x_p, x_{p+1}) to (cos th x_p - sin th x_{p+1},
+ * sin th x_p + cos th x_{p+1}).  G(theta) = L_K ... L_1 (layer 1 first).
+ *
+ * givens_matrix builds M = G(theta) diag(a) (diag(a) = I when a is NULL) by
+ * left-multiplying the layers onto diag(a) one rotation at a time.  When
+ * deriv >= 0, the rotation of angle `deriv` is replaced by its derivative
+ * with respect to that angle, [[-sin, -cos], [cos, -sin]] on its pair and zero
+ * on every other row, so M becomes dM/dtheta_deriv. */
+static void givens_matrix(const double *th, const double *a, int64_t K, int64_t deriv, double *M)
+{
+    for (int64_t i = 0; i < K; ++i)
+        for (int64_t j = 0; j < K; ++j)
+            M[i * K + j] = (i == j) ? (a ? a[j] : 1.0) : 0.0;
+    int64_t idx = 0;
+    for (int64_t l = 1; l <= K; ++l) {
+        for (int64_t p = (l % 2 == 1) ? 0 : 1; p + 1 < K; p += 2, ++idx) {
+            double c = cos(th[idx]), s = sin(th[idx]);
+            if (idx == deriv) {
+                for (int64_t col = 0; col < K; ++col) {
+                    double x = M[p * K + col], y = M[(p + 1) * K + col];
+                    for (int64_t r = 0; r < K; ++r)
+                        if (r != p && r != p + 1)
+                            M[r * K + col] = 0.0;
+                    M[p * K + col] = -s * x - c * y;
+                    M[(p + 1) * K + col] = c * x - s * y;
+                }
+            } else {
+                for (int64_t col = 0; col < K; ++col) {
+                    double x = M[p * K + col], y = M[(p + 1) * K + col];
+                    M[p * K + col] = c * x - s * y;
+                    M[(p + 1) * K + col] = s * x + c * y;
+                }
+            }
+        }
+    }
+}
+
+/* Forward of the Givens affine scan, per (batch, head) lane:
+ *   h_t = G(theta_t) diag(a_t) h_{t-1} + b_t,  h_0 = h0 (zeros when NULL),
+ * i.e. matrix_affine_scan with A_t = G(theta_t) diag(a_t) (a NULL: A_t =
+ * G(theta_t)).  Layouts: theta [B][T][H][N], N = K(K-1)/2; a, b, h
+ * [B][T][H][K]; h0 [B][H][K]. */
+void oracle_gas_fwd(const double *theta, const double *a, const double *bv, const double *h0,
+                    double *h, int64_t B, int64_t T, int64_t H, int64_t K)
+{
+    int64_t N = K * (K - 1) / 2, lanes = B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / H, hd = lane % H;
+        double *M = (double *)malloc(sizeof(double) * (size_t)(K * K));
+        double *prev = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int64_t i = 0; i < K; ++i)
+            prev[i] = h0 ? h0[(bb * H + hd) * K + i] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t st = (bb * T + t) * H + hd;
+            givens_matrix(theta + st * N, a ? a + st * K : NULL, K, -1, M);
+            double *ht = h + st * K;
+            for (int64_t i = 0; i < K; ++i) {
+                double s = bv[st * K + i];
+                for (int64_t j = 0; j < K; ++j)
+                    s += M[i * K + j] * prev[j];
+                ht[i] = s;
+            }
+            memcpy(prev, ht, sizeof(double) * (size_t)K);
+        }
+        free(M);
+        free(prev);
+    }
+}
+
+/* Backward of the Givens affine scan for L = sum_t <g_t, h_t>, by the chain
+ * rule through A_t = G(theta_t) diag(a_t):
+ *   lambda_T = g_T,  lambda_t = g_t + A_{t+1}^T lambda_{t+1},  db_t = lambda_t,
+ *   dA_t = lambda_t h_{t-1}^T,
+ *   dtheta_t[n] = <dA_t, dA_t/dtheta_n>_F,  da_t[j] = sum_r dA_t[r][j] G_t[r][j],
+ *   dh0 = A_1^T lambda_1.
+ * The states h_t are recomputed from the inputs.  a, da may be NULL (then
+ * A_t = G(theta_t) and da is not produced); dh0 may be NULL. */
+void oracle_gas_bwd(const double *theta, const double *a, const double *bv, const double *h0,
+                    const double *gh, double *dtheta, double *da, double *db, double *dh0,
+                    int64_t B, int64_t T, int64_t H, int64_t K)
+{
+    int64_t N = K * (K - 1) / 2, lanes = B * H, KK = K * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / H, hd = lane % H;
+        double *states = (double *)malloc(sizeof(double) * (size_t)((T + 1) * K));
+        double *M = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *dM = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *dAt = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *lam = (double *)malloc(sizeof(double) * (size_t)K);
+        double *nxt = (double *)malloc(sizeof(double) * (size_t)K);
+        for (int64_t i = 0; i < K; ++i)
+            states[i] = h0 ? h0[(bb * H + hd) * K + i] : 0.0;
+        for (int64_t t = 1; t <= T; ++t) {
+            int64_t st = (bb * T + (t - 1)) * H + hd;
+            givens_matrix(theta + st * N, a ? a + st * K : NULL, K, -1, M);
+            for (int64_t i = 0; i < K; ++i) {
+                double s = bv[st * K + i];
+                for (int64_t j = 0; j < K; ++j)
+                    s += M[i * K + j] * states[(t - 1) * K + j];
+                states[t * K + i] = s;
+            }
+        }
+        for (int64_t i = 0; i < K; ++i)
+            nxt[i] = 0.0;
+        for (int64_t t = T; t >= 1; --t) {
+            int64_t st = (bb * T + (t - 1)) * H + hd;
+            const double *th = theta + st * N;
+            const double *at = a ? a + st * K : NULL;
+            for (int64_t i = 0; i < K; ++i) {
+                lam[i] = gh[st * K + i] + nxt[i];
+                db[st * K + i] = lam[i];
+            }
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t j = 0; j < K; ++j)
+                    dAt[i * K + j] = lam[i] * states[(t - 1) * K + j];
+            for (int64_t n = 0; n < N; ++n) {
+                givens_matrix(th, at, K, n, dM);
+                double s = 0.0;
+                for (int64_t e = 0; e < KK; ++e)
+                    s += dAt[e] * dM[e];
+                dtheta[st * N + n] = s;
+            }
+            if (da) {
+                givens_matrix(th, NULL, K, -1, M);
+                for (int64_t j = 0; j < K; ++j) {
+                    double s = 0.0;
+                    for (int64_t r = 0; r < K; ++r)
+                        s += dAt[r * K + j] * M[r * K + j];
+                    da[st * K + j] = s;
+                }
+            }
+            givens_matrix(th, at, K, -1, M);
+            for (int64_t j = 0; j < K; ++j) {
+                double s = 0.0;
+                for (int64_t i = 0; i < K; ++i)
+                    s += M[i * K + j] * lam[i];
+                nxt[j] = s;
+            }
+        }
+        if (dh0)
+            for (int64_t i = 0; i < K; ++i)
+                dh0[(bb * H + hd) * K + i] = nxt[i];
+        free(states);
+        free(M);
+        free(dM);
+        free(dAt);
+        free(lam);
+        free(nxt);
+    }
+}
+
+/* Forward of the Givens matrix scan: P_t = G(theta_t) P_{t-1}, P_0 = I.
+ * theta [B][T][H][N] -> P [B][T][H][K][K]. */
+void oracle_gms_fwd(const double *theta, double *P, int64_t B, int64_t T, int64_t H, int64_t K)
+{
+    int64_t N = K * (K - 1) / 2, lanes = B * H, KK = K * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / H, hd = lane % H;
+        double *M = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *prev = (double *)malloc(sizeof(double) * (size_t)KK);
+        for (int64_t i = 0; i < K; ++i)
+            for (int64_t j = 0; j < K; ++j)
+                prev[i * K + j] = (i == j) ? 1.0 : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t st = (bb * T + t) * H + hd;
+            givens_matrix(theta + st * N, NULL, K, -1, M);
+            double *Pt = P + st * KK;
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t j = 0; j < K; ++j) {
+                    double s = 0.0;
+                    for (int64_t m = 0; m < K; ++m)
+                        s += M[i * K + m] * prev[m * K + j];
+                    Pt[i * K + j] = s;
+                }
+            memcpy(prev, Pt, sizeof(double) * (size_t)KK);
+        }
+        free(M);
+        free(prev);
+    }
+}
+
+/* Backward of the Givens matrix scan for L = sum_t <G_t, P_t>_F:
+ *   Lambda_T = G_T,  Lambda_t = G_t + A_{t+1}^T Lambda_{t+1},  A_t = G(theta_t),
+ *   dA_t = Lambda_t P_{t-1}^T (P_0 = I),  dtheta_t[n] = <dA_t, dA_t/dtheta_n>_F.
+ * gP [B][T][H][K][K] -> dtheta [B][T][H][N]; prefix products recomputed. */
+void oracle_gms_bwd(const double *theta, const double *gP, double *dtheta, int64_t B, int64_t T,
+                    int64_t H, int64_t K)
+{
+    int64_t N = K * (K - 1) / 2, lanes = B * H, KK = K * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / H, hd = lane % H;
+        double *prods = (double *)malloc(sizeof(double) * (size_t)((T + 1) * KK));
+        double *M = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *dM = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *dAt = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *lam = (double *)malloc(sizeof(double) * (size_t)KK);
+        double *nxt = (double *)malloc(sizeof(double) * (size_t)KK);
+        for (int64_t i = 0; i < K; ++i)
+            for (int64_t j = 0; j < K; ++j)
+                prods[i * K + j] = (i == j) ? 1.0 : 0.0;
+        for (int64_t t = 1; t <= T; ++t) {
+            int64_t st = (bb * T + (t - 1)) * H + hd;
+            givens_matrix(theta + st * N, NULL, K, -1, M);
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t j = 0; j < K; ++j) {
+                    double s = 0.0;
+                    for (int64_t m = 0; m < K; ++m)
+                        s += M[i * K + m] * prods[(t - 1) * KK + m * K + j];
+                    prods[t * KK + i * K + j] = s;
+                }
+        }
+        for (int64_t e = 0; e < KK; ++e)
+            nxt[e] = 0.0;
+        for (int64_t t = T; t >= 1; --t) {
+            int64_t st = (bb * T + (t - 1)) * H + hd;
+            const double *th = theta + st * N;
+            const double *Pprev = prods + (t - 1) * KK;
+            for (int64_t e = 0; e < KK; ++e)
+                lam[e] = gP[st * KK + e] + nxt[e];
+            for (int64_t i = 0; i < K; ++i)
+                for (int64_t m = 0; m < K; ++m) {
+                    double s = 0.0;
+                    for (int64_t j = 0; j < K; ++j)
+                        s += lam[i * K + j] * Pprev[m * K + j];
+                    dAt[i * K + m] = s;
+                }
+            for (int64_t n = 0; n < N; ++n) {
+                givens_matrix(th, NULL, K, n, dM);
+                double s = 0.0;
+                for (int64_t e = 0; e < KK; ++e)
+                    s += dAt[e] * dM[e];
+                dtheta[st * N + n] = s;
+            }
+            givens_matrix(th, NULL, K, -1, M);
+            for (int64_t m = 0; m < K; ++m)
+                for (int64_t j = 0; j < K; ++j) {
+                    double s = 0.0;
+                    for (int64_t i = 0; i < K; ++i)
+                        s += M[i * K + m] * lam[i * K + j];
+                    nxt[m * K + j] = s;
+                }
+        }
+        free(prods);
+        free(M);
+        free(dM);
+        free(dAt);
+        free(lam);
+        free(nxt);
     }
 }
 

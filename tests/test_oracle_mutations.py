@@ -27,7 +27,19 @@ MUTATIONS = [
     ("psl_bwd_dropped_carry", "lam = gh[idx] + nxt;", "lam = gh[idx];", 0),
     ("linear_fwd_dropped_b", "x = a[idx] * x + bv[idx];", "x = a[idx] * x;", 0),
     ("linear_bwd_da_uses_h_t", "da[idx] = lam * hs[t - 1];", "da[idx] = lam * hs[t];", 0),
+    ("givens_rotation_sign", "M[p * K + col] = c * x - s * y;", "M[p * K + col] = c * x + s * y;", 0),
+    ("givens_layer_parity", "(l % 2 == 1) ? 0 : 1", "(l % 2 == 1) ? 1 : 0", 0),
+    ("givens_layer_order", "for (int64_t l = 1; l <= K; ++l) {", "for (int64_t l = K; l >= 1; --l) {", 0),
+    ("givens_deriv_sign", "M[p * K + col] = -s * x - c * y;", "M[p * K + col] = s * x - c * y;", 0),
+    ("givens_deriv_keeps_other_rows", "M[r * K + col] = 0.0;", "M[r * K + col] = M[r * K + col];", 0),
+    ("gas_fwd_drops_a", "givens_matrix(theta + st * N, a ? a + st * K : NULL, K, -1, M);",
+     "givens_matrix(theta + st * N, NULL, K, -1, M);", 0),
+    ("gas_bwd_da_uses_A", "givens_matrix(th, NULL, K, -1, M);", "givens_matrix(th, at, K, -1, M);", 0),
+    ("gas_bwd_dropped_carry", "lam[i] = gh[st * K + i] + nxt[i];", "lam[i] = gh[st * K + i];", 0),
+    ("gms_bwd_P_not_transposed", "s += lam[i * K + j] * Pprev[m * K + j];",
+     "s += lam[i * K + j] * Pprev[j * K + m];", 1),
 ]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_givens_pins.py"]
 
 
 def _mutate(text, old, new, occ):
@@ -48,7 +60,7 @@ def test_pins_reject_planted_mistake(tmp_path, name, old, new, occ):
     subprocess.run(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11", "-o", str(so), str(c), "-lm"],
                    check=True)
     env = dict(os.environ, MGS_ORACLE_LIB=str(so))
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(HERE, "test_oracle_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider"]
+                       + [os.path.join(HERE, f) for f in PIN_FILES],
                        env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutation {name} survived the pins:\n{r.stdout[-2000:]}"
