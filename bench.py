@@ -57,6 +57,18 @@ def op_bytes(w, direction):
             return elems * 12 + (init if w.h0 != "none" else 0)
         # read a, grad_h, h; write da, db; read h0, write dh0
         return elems * 20 + (init if w.h0 != "none" else 0) + init
+    if w.op == "gas":  # angles N = k(k-1)/2 per step instead of the k x k matrix
+        steps, n = B * T * H, k * (k - 1) // 2
+        init = B * H * k * 4
+        if direction == "fwd":  # read theta, a, b; write h; read h0
+            return steps * 4 * (n + 3 * k) + (init if w.h0 != "none" else 0)
+        # read theta, a, grad_h, h; write d_theta, da, db; read h0, write dh0
+        return steps * 4 * (2 * n + 5 * k) + (init if w.h0 != "none" else 0) + init
+    if w.op == "gms":
+        steps, n = B * T * H, k * (k - 1) // 2
+        if direction == "fwd":  # read theta; write P
+            return steps * 4 * (n + k * k)
+        return steps * 4 * (2 * n + 2 * k * k)  # read theta, P, grad_P; write d_theta
     elems = B * T * H  # H holds D for parallel_scan_log
     init = B * H * 4
     if direction == "fwd":  # read lc, lv; write h; read log_h0
@@ -235,6 +247,11 @@ class Runner:
             self.P, self.dA = e(B, T, H, k, k), e(B, T, H, k, k)
             self.ws_f, self.nf = api.workspace(b.MGS_OP_MATRIX_SCAN_FWD, B, T, H, k, device)
             self.ws_b, self.nb = api.workspace(b.MGS_OP_MATRIX_SCAN_BWD, B, T, H, k, device)
+        elif w.op == "gas":
+            self.h = e(B, T, H, k)
+            self.dth, self.da, self.db, self.dh0 = e(B, T, H, k * (k - 1) // 2), e(B, T, H, k), e(B, T, H, k), e(B, H, k)
+        elif w.op == "gms":
+            self.P, self.dth = e(B, T, H, k, k), e(B, T, H, k * (k - 1) // 2)
         else:
             self.h = e(B, T, H)
             self.dlc, self.dlv, self.dl0 = e(B, T, H), e(B, T, H), e(B, H)
@@ -261,6 +278,11 @@ class Runner:
             b.mgs_linear_scan_fwd(d["a"], d["b"], d["h0"], self.h, w.B, w.T, w.H, self.ws_f, self.nf, stream)
         elif w.op == "ms":
             b.mgs_matrix_scan_fwd(d["A"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
+        elif w.op == "gas":
+            b.mgs_givens_affine_scan_fwd(d["theta"], d["a"], d["b"], d["h0"], self.h, w.B, w.T, w.H, w.k,
+                                         None, 0, stream)
+        elif w.op == "gms":
+            b.mgs_givens_matrix_scan_fwd(d["theta"], self.P, w.B, w.T, w.H, w.k, None, 0, stream)
         else:
             b.mgs_parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, None,
                                         w.B, w.T, w.H, None, 0, stream)
@@ -275,6 +297,12 @@ class Runner:
                                   w.B, w.T, w.H, self.ws_b, self.nb, stream)
         elif w.op == "ms":
             b.mgs_matrix_scan_bwd(d["A"], self.P, d["grad_P"], self.dA, w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
+        elif w.op == "gas":
+            b.mgs_givens_affine_scan_bwd(d["theta"], d["a"], d["h0"], self.h, d["grad_h"], self.dth, self.da,
+                                         self.db, self.dh0, w.B, w.T, w.H, w.k, None, 0, stream)
+        elif w.op == "gms":
+            b.mgs_givens_matrix_scan_bwd(d["theta"], self.P, d["grad_P"], self.dth, w.B, w.T, w.H, w.k, None, 0,
+                                         stream)
         else:
             b.mgs_parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, d["grad_h"],
                                         self.dlc, self.dlv, self.dl0, w.B, w.T, w.H, None, 0, stream)

@@ -72,7 +72,11 @@ enum {
     MGS_OP_PARALLEL_SCAN_LOG_FWD = 5,
     MGS_OP_PARALLEL_SCAN_LOG_BWD = 6,
     MGS_OP_LINEAR_SCAN_FWD = 7,
-    MGS_OP_LINEAR_SCAN_BWD = 8
+    MGS_OP_LINEAR_SCAN_BWD = 8,
+    MGS_OP_GIVENS_AFFINE_SCAN_FWD = 9,
+    MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10,
+    MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11,
+    MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12
 };
 
 /* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
@@ -211,6 +215,59 @@ mgs_status mgs_linear_scan_fwd(const float *a, const float *b, const float *h0, 
 mgs_status mgs_linear_scan_bwd(const float *a, const float *h0, const float *h, const float *grad_h,
                                float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t D,
                                void *workspace, size_t workspace_bytes, mgs_stream_t stream);
+
+/* Givens-mesh scans: matrix_affine_scan and matrix_scan whose k x k
+ * transition is GivensMinGRU's brick-wall rotation mesh, given by its angles
+ * ("mingru-scans" home page, lineage paragraph: the Clements et al. 2016 mesh
+ * of Golub & Van Loan plane rotations; "Run the benchmarks", Step 3: the
+ * angle-fused backward).  Only k = 8 is supported (else MGS_ERR_UNSUPPORTED);
+ * N = k(k-1)/2 = 28 angles per (batch, step, head).
+ *
+ * G(theta) = L_k ... L_1: layer l = 1..k rotates the disjoint coordinate pairs
+ * (0,1),(2,3),.. (odd l) or (1,2),(3,4),.. (even l), no wrap-around; the
+ * angles are consumed layer by layer, pairs ascending, and the rotation of
+ * angle th on (p, p+1) maps (x_p, x_{p+1}) to
+ * (cos th x_p - sin th x_{p+1}, sin th x_p + cos th x_{p+1}).
+ * Neither direction forms A_t or dA_t in memory.  No workspace is needed
+ * (mgs_workspace_size returns 0 for these ops); the workspace arguments are
+ * accepted for uniformity.
+ *
+ * Affine forward:  h_t = G(theta_t) diag(a_t) h_{t-1} + b_t, h_0 = h0 (zeros
+ * when NULL); a NULL means A_t = G(theta_t).
+ * In: theta [B][T][H][28], a [B][T][H][8] (nullable), b [B][T][H][8],
+ *     h0 [B][H][8] (nullable).  Out: h [B][T][H][8]. */
+mgs_status mgs_givens_affine_scan_fwd(const float *theta, const float *a, const float *b,
+                                      const float *h0, float *h, int64_t B, int64_t T, int64_t H,
+                                      int k, void *workspace, size_t workspace_bytes,
+                                      mgs_stream_t stream);
+
+/* Affine backward: gradients of L = sum_t <grad_h_t, h_t> with respect to the
+ * angles, a, b and h0.  With lambda_t = dL/dh_t (lambda_t = grad_h_t +
+ * A_{t+1}^T lambda_{t+1}): db_t = lambda_t; d_theta_t[n] = <lambda_t h_{t-1}^T,
+ * dA_t/dtheta_n>; da_t[j] = (G_t^T lambda_t)[j] h_{t-1}[j]; dh0 = A_1^T lambda_1.
+ * In: theta, a (nullable, as in the forward), h0 (nullable), h = the forward
+ *     output (saved), grad_h.  b is not needed.
+ * Out: d_theta [B][T][H][28]; da [B][T][H][8] (nullable; must be NULL when a
+ *     is NULL); db [B][T][H][8]; dh0 [B][H][8] (nullable). */
+mgs_status mgs_givens_affine_scan_bwd(const float *theta, const float *a, const float *h0,
+                                      const float *h, const float *grad_h, float *d_theta, float *da,
+                                      float *db, float *dh0, int64_t B, int64_t T, int64_t H, int k,
+                                      void *workspace, size_t workspace_bytes, mgs_stream_t stream);
+
+/* Matrix forward: P_t = G(theta_t) P_{t-1}, P_0 = I.
+ * In: theta [B][T][H][28].  Out: P [B][T][H][8][8]. */
+mgs_status mgs_givens_matrix_scan_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H,
+                                      int k, void *workspace, size_t workspace_bytes,
+                                      mgs_stream_t stream);
+
+/* Matrix backward: gradient of L = sum_t <grad_P_t, P_t>_F with respect to the
+ * angles, d_theta_t[n] = <Lambda_t P_{t-1}^T, dA_t/dtheta_n> with Lambda_t =
+ * grad_P_t + A_{t+1}^T Lambda_{t+1}.
+ * In: theta, P = the forward output (saved), grad_P [B][T][H][8][8].
+ * Out: d_theta [B][T][H][28]. */
+mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const float *grad_P,
+                                      float *d_theta, int64_t B, int64_t T, int64_t H, int k,
+                                      void *workspace, size_t workspace_bytes, mgs_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns MGS_ERR_TIMEOUT if a kernel's bounded wait gave up since the

@@ -32,6 +32,10 @@ MGS_OP_PARALLEL_SCAN_LOG_FWD = 5
 MGS_OP_PARALLEL_SCAN_LOG_BWD = 6
 MGS_OP_LINEAR_SCAN_FWD = 7
 MGS_OP_LINEAR_SCAN_BWD = 8
+MGS_OP_GIVENS_AFFINE_SCAN_FWD = 9
+MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10
+MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11
+MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12
 
 
 class MGSError(RuntimeError):
@@ -60,6 +64,11 @@ _SIGNATURES = {
     "mgs_parallel_scan_log_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "mgs_linear_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "mgs_linear_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "mgs_givens_affine_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
+    "mgs_givens_affine_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int,
+                                          _vp, _sz, _vp]),
+    "mgs_givens_matrix_scan_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
+    "mgs_givens_matrix_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_check": (_int, [_vp]),
     "mgs_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "mgs_debug_wait_flag": (_int, [_vp, _vp]),
@@ -171,6 +180,29 @@ def mgs_linear_scan_fwd(a, b, h0, h, B, T, D, workspace=None, workspace_bytes=0,
 def mgs_linear_scan_bwd(a, h0, h, grad_h, da, db, dh0, B, T, D, workspace=None, workspace_bytes=0, stream=None):
     return _call("mgs_linear_scan_bwd", _ptr(a), _ptr(h0), _ptr(h), _ptr(grad_h), _ptr(da), _ptr(db), _ptr(dh0),
                  B, T, D, _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mgs_givens_affine_scan_fwd(theta, a, b, h0, h, B, T, H, k, workspace=None, workspace_bytes=0, stream=None):
+    return _call("mgs_givens_affine_scan_fwd", _ptr(theta), _ptr(a), _ptr(b), _ptr(h0), _ptr(h), B, T, H, k,
+                 _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mgs_givens_affine_scan_bwd(theta, a, h0, h, grad_h, d_theta, da, db, dh0, B, T, H, k, workspace=None,
+                               workspace_bytes=0, stream=None):
+    return _call("mgs_givens_affine_scan_bwd", _ptr(theta), _ptr(a), _ptr(h0), _ptr(h), _ptr(grad_h),
+                 _ptr(d_theta), _ptr(da), _ptr(db), _ptr(dh0), B, T, H, k, _ptr(workspace), workspace_bytes,
+                 _stream(stream))
+
+
+def mgs_givens_matrix_scan_fwd(theta, P, B, T, H, k, workspace=None, workspace_bytes=0, stream=None):
+    return _call("mgs_givens_matrix_scan_fwd", _ptr(theta), _ptr(P), B, T, H, k, _ptr(workspace),
+                 workspace_bytes, _stream(stream))
+
+
+def mgs_givens_matrix_scan_bwd(theta, P, grad_P, d_theta, B, T, H, k, workspace=None, workspace_bytes=0,
+                               stream=None):
+    return _call("mgs_givens_matrix_scan_bwd", _ptr(theta), _ptr(P), _ptr(grad_P), _ptr(d_theta), B, T, H, k,
+                 _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def mgs_check(stream=None):

@@ -114,6 +114,58 @@ def parallel_scan_log_bwd(log_coeffs, log_values, log_h0, h, grad_h, stream=None
     return dlc, dlv, dl0
 
 
+# ---------------------------------------------------------------- Givens-mesh scans
+GIVENS_K = 8
+GIVENS_N = GIVENS_K * (GIVENS_K - 1) // 2
+
+
+def givens_affine_scan_fwd(theta, a, b, h0=None, stream=None):
+    """h_t = G(theta_t) diag(a_t) h_{t-1} + b_t.  theta [B,T,H,28], a [B,T,H,8] or None,
+    b [B,T,H,8], h0 [B,H,8] or None."""
+    B, T, H, k = b.shape
+    _check(theta, "theta", (B, T, H, k * (k - 1) // 2)); _check(b, "b")
+    if a is not None:
+        _check(a, "a", (B, T, H, k))
+    if h0 is not None:
+        _check(h0, "h0", (B, H, k))
+    h = torch.empty_like(b)
+    _b.mgs_givens_affine_scan_fwd(theta, a, b, h0, h, B, T, H, k, None, 0, stream)
+    return h
+
+
+def givens_affine_scan_bwd(theta, a, h0, h, grad_h, need_dh0=True, stream=None):
+    """Returns (d_theta, da or None, db, dh0 or None) for L = sum <grad_h, h>."""
+    B, T, H, k = h.shape
+    _check(theta, "theta", (B, T, H, k * (k - 1) // 2)); _check(h, "h"); _check(grad_h, "grad_h", (B, T, H, k))
+    if a is not None:
+        _check(a, "a", (B, T, H, k))
+    if h0 is not None:
+        _check(h0, "h0", (B, H, k))
+    dth = torch.empty_like(theta)
+    da = torch.empty_like(a) if a is not None else None
+    db = torch.empty_like(h)
+    dh0 = torch.empty((B, H, k), dtype=torch.float32, device=h.device) if need_dh0 else None
+    _b.mgs_givens_affine_scan_bwd(theta, a, h0, h, grad_h, dth, da, db, dh0, B, T, H, k, None, 0, stream)
+    return dth, da, db, dh0
+
+
+def givens_matrix_scan_fwd(theta, k=GIVENS_K, stream=None):
+    """P_t = G(theta_t) P_{t-1}, P_0 = I.  theta [B,T,H,28] -> P [B,T,H,8,8]."""
+    B, T, H, n = theta.shape
+    _check(theta, "theta", (B, T, H, k * (k - 1) // 2))
+    P = torch.empty((B, T, H, k, k), dtype=torch.float32, device=theta.device)
+    _b.mgs_givens_matrix_scan_fwd(theta, P, B, T, H, k, None, 0, stream)
+    return P
+
+
+def givens_matrix_scan_bwd(theta, P, grad_P, stream=None):
+    B, T, H, k, _ = P.shape
+    _check(theta, "theta", (B, T, H, k * (k - 1) // 2)); _check(P, "P"); _check(grad_P, "grad_P", P.shape)
+    dth = torch.empty_like(theta)
+    _b.mgs_givens_matrix_scan_bwd(theta, P, grad_P, dth, B, T, H, k, None, 0, stream)
+    return dth
+
+
 # ---------------------------------------------------------------- linear_scan
 def linear_scan_fwd(a, b, h0=None, stream=None):
     """h_t = a_t * h_{t-1} + b_t elementwise.  a, b [B,T,D], h0 [B,D] or None."""
@@ -213,6 +265,50 @@ class LinearScan(torch.autograd.Function):
         h0 = h0 if ctx.has_h0 else None
         da, db, dh0 = linear_scan_bwd(a, h0, h, grad_h.contiguous(), need_dh0=ctx.has_h0)
         return da, db, dh0
+
+
+class GivensAffineScan(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, theta, a, b, h0=None):
+        theta, b = theta.contiguous(), b.contiguous()
+        a = a.contiguous() if a is not None else None
+        h0c = h0.contiguous() if h0 is not None else None
+        h = givens_affine_scan_fwd(theta, a, b, h0c)
+        empty = torch.empty(0, device=b.device)
+        ctx.save_for_backward(theta, a if a is not None else empty, h0c if h0c is not None else empty, h)
+        ctx.has_a, ctx.has_h0 = a is not None, h0 is not None
+        return h
+
+    @staticmethod
+    def backward(ctx, grad_h):
+        theta, a, h0, h = ctx.saved_tensors
+        a = a if ctx.has_a else None
+        h0 = h0 if ctx.has_h0 else None
+        dth, da, db, dh0 = givens_affine_scan_bwd(theta, a, h0, h, grad_h.contiguous(), need_dh0=ctx.has_h0)
+        return dth, da, db, dh0
+
+
+class GivensMatrixScan(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, theta):
+        theta = theta.contiguous()
+        P = givens_matrix_scan_fwd(theta)
+        ctx.save_for_backward(theta, P)
+        return P
+
+    @staticmethod
+    def backward(ctx, grad_P):
+        theta, P = ctx.saved_tensors
+        return givens_matrix_scan_bwd(theta, P, grad_P.contiguous())
+
+
+def givens_affine_scan(theta, a, b, h0=None):
+    """GivensMinGRU's angle-fused recurrence h_t = G(theta_t) diag(a_t) h_{t-1} + b_t (a may be None)."""
+    return GivensAffineScan.apply(theta, a, b, h0)
+
+
+def givens_matrix_scan(theta):
+    return GivensMatrixScan.apply(theta)
 
 
 def linear_scan(a, b, h0=None):

@@ -99,6 +99,24 @@ mgs_status block_sizes(int64_t B, int64_t T, int64_t H, int k, BlockSizes *s) {
     return MGS_OK;
 }
 
+struct GivensSizes {
+    int64_t ang, vec, mat, init;  // element counts: [B,T,H,N], [B,T,H,k], [B,T,H,k,k], [B,H,k]
+};
+
+// Validates (B, T, H, k) for the Givens-mesh ops (k = 8 only).
+mgs_status givens_sizes(int64_t B, int64_t T, int64_t H, int k, GivensSizes *s) {
+    if (B < 0 || T < 0 || H < 0 || k <= 0) return MGS_ERR_INVALID_ARG;
+    if (k != 8) return MGS_ERR_UNSUPPORTED;
+    int64_t bth, bh;
+    if (!mul_ok(B, T, &bth) || !mul_ok(bth, H, &bth) || !mul_ok(B, H, &bh)) return MGS_ERR_INVALID_ARG;
+    if (!mul_ok(bth, 64, &s->mat) || !mul_ok(bth, 28, &s->ang) || !mul_ok(bth, 8, &s->vec) ||
+        !mul_ok(bh, 8, &s->init))
+        return MGS_ERR_INVALID_ARG;
+    if (s->mat > (INT64_MAX / 8)) return MGS_ERR_INVALID_ARG;
+    if (B * T > INT32_MAX || H > INT32_MAX / 256) return MGS_ERR_UNSUPPORTED;  // 32-bit map coordinates
+    return MGS_OK;
+}
+
 mgs_status check_ptrs(std::initializer_list<const void *> required,
                       std::initializer_list<const void *> optional) {
     for (const void *p : required)
@@ -365,6 +383,79 @@ mgs_status mgs_linear_scan_bwd(const float *a, const float *h0, const float *h, 
     if (D >= 0 && D % 4 != 0) return MGS_ERR_UNSUPPORTED;
     return mgs_matrix_affine_scan_bwd(a, h0, h, grad_h, da, db, dh0, B, T, D, 1, workspace, workspace_bytes,
                                       stream);
+}
+
+mgs_status mgs_givens_affine_scan_fwd(const float *theta, const float *a, const float *b,
+                                      const float *h0, float *h, int64_t B, int64_t T, int64_t H,
+                                      int k, void *workspace, size_t workspace_bytes,
+                                      mgs_stream_t stream) {
+    GivensSizes s;
+    mgs_status st = givens_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.vec == 0) return MGS_OK;
+    if ((st = check_ptrs({theta, b, h}, {a, h0})) != MGS_OK) return st;
+    if (!disjoint({{h, s.vec}}, {{theta, s.ang}, {a, a ? s.vec : 0}, {b, s.vec}, {h0, h0 ? s.init : 0}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_gas_fwd(theta, a, b, h0, h, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_givens_affine_scan_bwd(const float *theta, const float *a, const float *h0,
+                                      const float *h, const float *grad_h, float *d_theta, float *da,
+                                      float *db, float *dh0, int64_t B, int64_t T, int64_t H, int k,
+                                      void *workspace, size_t workspace_bytes, mgs_stream_t stream) {
+    GivensSizes s;
+    mgs_status st = givens_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (da != nullptr && a == nullptr) return MGS_ERR_INVALID_ARG;
+    if (s.init == 0) return MGS_OK;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (s.vec == 0) {  // T = 0: dh0 = 0
+        if (dh0 == nullptr) return MGS_OK;
+        if ((st = check_ptrs({dh0}, {})) != MGS_OK) return st;
+        return from_cuda(cudaMemsetAsync(dh0, 0, size_t(s.init) * sizeof(float), cs));
+    }
+    if ((st = check_ptrs({theta, h, grad_h, d_theta, db}, {a, h0, da, dh0})) != MGS_OK) return st;
+    if (!disjoint({{d_theta, s.ang}, {da, da ? s.vec : 0}, {db, s.vec}, {dh0, dh0 ? s.init : 0}},
+                  {{theta, s.ang}, {a, a ? s.vec : 0}, {h0, h0 ? s.init : 0}, {h, s.vec}, {grad_h, s.vec}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_gas_bwd(theta, a, h0, h, grad_h, d_theta, da, db, dh0, B, T, H, ctl, cs));
+}
+
+mgs_status mgs_givens_matrix_scan_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H,
+                                      int k, void *workspace, size_t workspace_bytes,
+                                      mgs_stream_t stream) {
+    GivensSizes s;
+    mgs_status st = givens_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.mat == 0) return MGS_OK;
+    if ((st = check_ptrs({theta, P}, {})) != MGS_OK) return st;
+    if (!disjoint({{P, s.mat}}, {{theta, s.ang}})) return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_gms_fwd(theta, P, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const float *grad_P,
+                                      float *d_theta, int64_t B, int64_t T, int64_t H, int k,
+                                      void *workspace, size_t workspace_bytes, mgs_stream_t stream) {
+    GivensSizes s;
+    mgs_status st = givens_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.mat == 0) return MGS_OK;
+    if ((st = check_ptrs({theta, P, grad_P, d_theta}, {})) != MGS_OK) return st;
+    if (!disjoint({{d_theta, s.ang}}, {{theta, s.ang}, {P, s.mat}, {grad_P, s.mat}})) return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_gms_bwd(theta, P, grad_P, d_theta, B, T, H, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_check(mgs_stream_t stream) {

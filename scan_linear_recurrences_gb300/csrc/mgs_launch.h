@@ -46,6 +46,17 @@ cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, c
                            const float *gh, float *dlc, float *dlv, float *dlh0, int64_t B,
                            int64_t T, int64_t D, const DevCtl &ctl, cudaStream_t s);
 
+// Givens-mesh affine and matrix scans (k = 8)
+cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, const float *h0, float *h,
+                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, const float *h, const float *gh,
+                           float *dth, float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t H,
+                           const DevCtl &ctl, cudaStream_t s);
+cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
+                           cudaStream_t s);
+cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
+                           int64_t H, const DevCtl &ctl, cudaStream_t s);
+
 // Encodes a tiled fp32 tensor map over `base` (rank 2 or 3).  dims and box are
 // innermost first; byte_strides has rank-1 entries (strides of dims 1..).
 cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,

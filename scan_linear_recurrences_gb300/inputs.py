@@ -26,6 +26,12 @@ memory stays bounded; within a block the draws are in the order listed):
   (1,2),(3,4),...; no wrap), each angle ~ U(-pi, pi), k(k-1)/2 angles per
   matrix; rotation on (i, i+1) maps (x_i, x_{i+1}) to
   (c x_i - s x_{i+1}, s x_i + c x_{i+1}).  grad_P = N(0,1)^{k x k}.
+* Givens affine scan (GivensMinGRU transition from its angles): h0 as for
+  matrix_affine_scan; per block theta ~ U(-pi, pi)^{k(k-1)/2}, a =
+  sigmoid(N(0,1))^k (drawn even when the op is run without a), z =
+  sigmoid(N(0,1))^k, n = N(0,1)^k, b = z * n, grad_h = N(0,1)^k.
+* Givens matrix scan: per block theta ~ U(-pi, pi)^{k(k-1)/2} (the angles
+  of the matrix_scan recipe above), grad_P = N(0,1)^{k x k}.
 * parallel_scan_log (minGRU gates): log_h0 = log g(N(0,1)) drawn first; then
   per block u ~ N(0,1), x ~ N(0,1), grad_h ~ N(0,1);
   log_coeffs = log(1 - sigmoid(u)) = -softplus(u),
@@ -144,6 +150,49 @@ def ms_inputs(B, T, H, k, seed, device="cpu"):
     return dict(A=A, grad_P=gP)
 
 
+def givens_affine_inputs(B, T, H, k, seed, device="cpu", h0="none", with_a=True):
+    """Givens affine scan inputs: dict(theta [B,T,H,k(k-1)/2], a [B,T,H,k] or
+    None, b [B,T,H,k], h0 [B,H,k] or None, grad_h [B,T,H,k]), float32."""
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    f64 = dict(dtype=torch.float64, device=dev)
+    nang = k * (k - 1) // 2
+    th = torch.empty((B, T, H, nang), dtype=torch.float32, device=dev)
+    a = torch.empty((B, T, H, k), dtype=torch.float32, device=dev)
+    b = torch.empty((B, T, H, k), dtype=torch.float32, device=dev)
+    gh = torch.empty((B, T, H, k), dtype=torch.float32, device=dev)
+    if h0 == "normal":
+        h0_t = torch.randn((B, H, k), generator=g, **f64).float()
+    elif h0 == "none":
+        h0_t = None
+    else:
+        raise ValueError(h0)
+    for t0 in range(0, T, TIME_BLOCK):
+        tb = min(TIME_BLOCK, T - t0)
+        th[:, t0:t0 + tb] = ((torch.rand((B, tb, H, nang), generator=g, **f64) * 2.0 - 1.0) * math.pi).float()
+        a[:, t0:t0 + tb] = torch.sigmoid(torch.randn((B, tb, H, k), generator=g, **f64)).float()
+        z = torch.sigmoid(torch.randn((B, tb, H, k), generator=g, **f64))
+        n = torch.randn((B, tb, H, k), generator=g, **f64)
+        b[:, t0:t0 + tb] = (z * n).float()
+        gh[:, t0:t0 + tb] = torch.randn((B, tb, H, k), generator=g, **f64).float()
+    return dict(theta=th, a=a if with_a else None, b=b, h0=h0_t, grad_h=gh)
+
+
+def givens_matrix_inputs(B, T, H, k, seed, device="cpu"):
+    """Givens matrix scan inputs: dict(theta [B,T,H,k(k-1)/2], grad_P [B,T,H,k,k])."""
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    f64 = dict(dtype=torch.float64, device=dev)
+    nang = k * (k - 1) // 2
+    th = torch.empty((B, T, H, nang), dtype=torch.float32, device=dev)
+    gP = torch.empty((B, T, H, k, k), dtype=torch.float32, device=dev)
+    for t0 in range(0, T, TIME_BLOCK):
+        tb = min(TIME_BLOCK, T - t0)
+        th[:, t0:t0 + tb] = ((torch.rand((B, tb, H, nang), generator=g, **f64) * 2.0 - 1.0) * math.pi).float()
+        gP[:, t0:t0 + tb] = torch.randn((B, tb, H, k, k), generator=g, **f64).float()
+    return dict(theta=th, grad_P=gP)
+
+
 def psl_inputs(B, T, D, seed, device="cpu", with_h0=True):
     """parallel_scan_log inputs with the minGRU gate distribution:
     dict(log_coeffs, log_values [B,T,D], log_h0 [B,D] or None, grad_h [B,T,D])."""
@@ -188,7 +237,7 @@ def linear_inputs(B, T, D, seed, device="cpu", with_h0=True):
 class Workload:
     """One benchmarked shape."""
     cid: int
-    op: str          # "mas" | "ms" | "psl" | "lin"
+    op: str          # "mas" | "ms" | "psl" | "lin" | "gas" | "gms"
     name: str
     B: int
     T: int
@@ -207,6 +256,10 @@ class Workload:
             return ms_inputs(self.B, self.T, self.H, self.k, self.seed, device)
         if self.op == "lin":
             return linear_inputs(self.B, self.T, self.H, self.seed, device, with_h0=True)
+        if self.op == "gas":
+            return givens_affine_inputs(self.B, self.T, self.H, self.k, self.seed, device, h0=self.h0)
+        if self.op == "gms":
+            return givens_matrix_inputs(self.B, self.T, self.H, self.k, self.seed, device)
         return psl_inputs(self.B, self.T, self.H, self.seed, device, with_h0=True)
 
 
@@ -225,4 +278,10 @@ EXTRA_WORKLOADS = {
     6: Workload(6, "ms", "matrix_scan lab Givens B=128 T=64 H=8 k=8", 128, 64, 8, 8, "none"),
     7: Workload(7, "lin", "linear_scan lab B=128 T=64 D=64", 128, 64, 64, 1, "normal"),
     8: Workload(8, "lin", "linear_scan long-T B=16 T=1024 D=64", 16, 1024, 64, 1, "normal"),
+    # GivensMinGRU's angle-fused scans at the pages' memory-benchmark shape
+    # (B=128, T=64, d=64 = 8 heads of k=8) and the long-sequence shape
+    9: Workload(9, "gas", "givens_affine_scan lab B=128 T=64 H=8 k=8", 128, 64, 8, 8, "normal"),
+    10: Workload(10, "gas", "givens_affine_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "normal"),
+    11: Workload(11, "gms", "givens_matrix_scan lab B=128 T=64 H=8 k=8", 128, 64, 8, 8, "none"),
+    12: Workload(12, "gms", "givens_matrix_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "none"),
 }
