@@ -18,15 +18,18 @@
 // HBM bytes per step (k = 8) drop from 4(k^2 + 2k) = 320 to 4(28 + 3k) = 208
 // forward and from 608 to 4(2*28 + 5k) = 384 backward for the affine scan.
 //
-// Mapping.  Affine scan: one thread per (batch, head) lane holds the whole
-// state in registers, so the rotations need no exchange between threads; a
-// warp takes LPW consecutive heads of one batch row (LPW chosen per shape so
-// that there are enough warps to fill the GPU).  Matrix scan: eight threads
-// per lane, thread j owning column j of P_t, four lanes per warp.  In both,
-// each stage of TS steps arrives by tiled TMA loads into a per-warp ring, and
-// the whole warp first turns the stage's angles into cosines and sines (from
-// the half-angle tangent, so that the rotations carry no systematic norm
-// error), which the recurrence threads then read.
+// Mapping.  Each block is one recurrence warp and three angle warps.  The
+// angles cost far more than the rotations (28 cosine/sine pairs per lane and
+// step against 112 multiply-adds), but they do not depend on the state, so
+// the angle warps convert stage j+1's angles (to cosines and sines, from the
+// half-angle tangent so that the rotations carry no systematic norm error)
+// while the recurrence warp runs stage j.  Affine scan: one thread of the
+// recurrence warp per (batch, head) lane holds the whole state in registers,
+// so the rotations need no exchange between threads; a block takes LPW
+// consecutive heads of one batch row (LPW chosen per shape so that there are
+// enough blocks to fill the GPU).  Matrix scan: eight threads per lane,
+// thread j owning column j of P_t, four lanes per block.  Each stage of TS
+// steps arrives by tiled TMA loads into a per-block ring.
 #include "mgs_tiles.cuh"
 
 namespace mgs {
@@ -35,10 +38,12 @@ namespace {
 constexpr int GK = 8;                  // coordinates per head
 constexpr int GN = GK * (GK - 1) / 2;  // angles per head and step
 constexpr int kItems = 64;             // (lane, step) items per affine-scan stage
-constexpr int kGasNS = 3;              // affine-scan stages in flight
-constexpr int kGmsLanes = 4;           // heads per warp in the matrix scan
-constexpr int kGmsFwdTS = 16, kGmsFwdNS = 3;
-constexpr int kGmsBwdTS = 8, kGmsBwdNS = 2;
+constexpr int kNS = 3;                 // stages in flight
+constexpr int kBlock = 128;            // threads per block: 1 recurrence warp + 3 angle warps
+constexpr int kProd = kBlock - 32;     // angle threads
+constexpr int kGasMaxLanes = 8;        // affine-scan lanes per recurrence warp, at most
+constexpr int kGmsLanes = 4;           // heads per block in the matrix scan (8 threads each)
+constexpr int kGmsFwdTS = 16, kGmsBwdTS = 8;
 
 // Index of the first angle of layer l (0-based): layers alternate 4 and 3 pairs.
 __host__ __device__ constexpr int layer_base(int l) { return (l / 2) * 7 + (l % 2) * 4; }
@@ -95,32 +100,37 @@ __device__ __forceinline__ void mesh_apply(float (&x)[GK], const float (&cs)[GN]
 // relative growth of the state, four times the parity tolerance.  The ratio
 // t = sin/cos of the half angle cancels any common scale error of sincosf,
 // and its angle error has no measurable mean.
+// 1/x for normal positive x below 2^126: the hardware approximation refined
+// by one Newton-Raphson step, r1 = r0 + r0 (1 - x r0) with the residual taken
+// by a fused multiply-add, which leaves only the final rounding (to nearest).
+__device__ __forceinline__ float recip_nr(float x) {
+    float r0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(x));
+    return fmaf(r0, fmaf(-x, r0, 1.f), r0);
+}
+
 __device__ __forceinline__ void unbiased_cos_sin(float theta, float &c, float &s) {
     float sh, ch;
     sincosf(0.5f * theta, &sh, &ch);
-    const float t = __fdiv_rn(sh, ch);
-    if (fabsf(t) > 1e18f) {  // half angle at a pole of tan: theta = pi (mod 2 pi)
-        c = -1.f;
-        s = 0.f;
-        return;
-    }
-    const float r = __frcp_rn(fmaf(t, t, 1.f));
+    // |cos| of the half angle: at least 2^-100 away from a pole (theta = pi
+    // mod 2 pi gives |t| <= 1e30, where c = -1 and s = 0 to fp32 precision)
+    const float ach = fmaxf(fabsf(ch), 1e-30f);
+    const float t = fminf(fmaxf(copysignf(sh * recip_nr(ach), sh * ch), -1e18f), 1e18f);
+    const float r = recip_nr(fmaf(t, t, 1.f));
     c = fmaf(-t, t, 1.f) * r;
     s = (2.f * t) * r;
 }
 
-// The n angles at th (n a multiple of 4, 16-byte aligned) -> cosines in place
-// and sines to sn; the whole warp shares the work.
-__device__ __forceinline__ void stage_sincos(float *th, float *sn, int n, int lane) {
-    for (int i = 4 * lane; i < n; i += 128) {
-        const float4 t = *reinterpret_cast<const float4 *>(th + i);
-        float4 c, s;
-        unbiased_cos_sin(t.x, c.x, s.x);
-        unbiased_cos_sin(t.y, c.y, s.y);
-        unbiased_cos_sin(t.z, c.z, s.z);
-        unbiased_cos_sin(t.w, c.w, s.w);
-        *reinterpret_cast<float4 *>(th + i) = c;
-        *reinterpret_cast<float4 *>(sn + i) = s;
+// Angles [lo, hi) of a stage converted by the block's angle threads (pt = 0 ..
+// kProd-1): cosines in place, sines to sn; consecutive threads take
+// consecutive words.
+__device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi, int pt) {
+#pragma unroll 2
+    for (int i = lo + pt; i < hi; i += kProd) {
+        float c, s;
+        unbiased_cos_sin(th[i], c, s);
+        th[i] = c;
+        sn[i] = s;
     }
 }
 
@@ -133,35 +143,75 @@ cudaError_t make_head_map(CUtensorMap *m, const float *base, int64_t rows, int64
     return make_tmap(m, base, 3, dims, str, box);
 }
 
-// Per-warp shared memory of the affine scan: kGasNS stages of
-// [theta ts*lpw*GN][vector inputs nv x ts*lpw*GK], a sine scratch of
-// ts*lpw*GN floats, then the barriers.
+// Block pipeline shared by the four kernels.  A block is one recurrence warp
+// (warp 0) and three angle warps.  Iteration `it` of the main loop:
+//   angle warps: wait for stage it's bulk copies, convert its angles;
+//   warp 0:      run the recurrence over stage it-1 (converted last time);
+//   all:         __syncthreads; then stage it-1's slot is refilled with the
+//                block kNS ahead.
+// The angle warps own the ring's barriers: only they wait on the copies, and
+// the block barrier hands the landed (and converted) data on to warp 0.  A
+// wait that gives up sets the block's abort word, so every thread leaves at
+// the same barrier, after the angle warps have drained the copies in flight.
+struct BlockRing {
+    WarpRing<kNS> rg;
+    uint64_t *bars;
+    int *abort_word;
+    __device__ __forceinline__ void init(uint64_t *b, int *ab, int tid) {
+        bars = b;
+        abort_word = ab;
+        if (tid == 0) {
+            for (int s = 0; s < kNS; ++s) mbar_init(&bars[s], 1);
+            fence_barrier_init();
+            *abort_word = 0;
+        }
+        __syncthreads();
+        rg.bar = bars;
+        rg.inflight = 0;
+        rg.phase = 0;
+    }
+};
+
+#define MGS_BLOCK_ABORT_CHECK(br, producer, lane)                 \
+    if (*(br).abort_word != 0) {                                  \
+        if (producer) (br).rg.drain(ctl, lane);                   \
+        return;                                                   \
+    }
+
+// Per-block shared memory of the affine scan: kNS stages of
+// [theta ts*lpw*GN][vector inputs nv x ts*lpw*GK], two sine buffers of
+// ts*lpw*GN floats, the barriers and the abort word.
 struct GasSmem {
     int th_f, vec_f, stage_f, ring_f, sin_f;
     __host__ __device__ GasSmem(int lpw, int ts, int nv) {
         th_f = ts * lpw * GN;
         vec_f = ts * lpw * GK;
         stage_f = int(align_up(size_t(th_f + nv * vec_f), 32));
-        ring_f = kGasNS * stage_f;
+        ring_f = kNS * stage_f;
         sin_f = th_f;
     }
-    __host__ __device__ size_t bytes() const { return size_t(ring_f + sin_f) * 4 + kGasNS * sizeof(uint64_t); }
+    __host__ __device__ size_t bytes() const {
+        return size_t(ring_f + 2 * sin_f) * 4 + kNS * sizeof(uint64_t) + 16;
+    }
 };
 
 // ---------------------------------------------------------------- affine forward
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kBlock)
     gas_fwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const float *__restrict__ h0, float *__restrict__ h,
                    int64_t B, int64_t T, int64_t H, int64_t groups_per_b, int lpw, int ts, int has_a,
                    DevCtl ctl) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const GasSmem L(lpw, ts, has_a ? 2 : 1);
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     float *ring = reinterpret_cast<float *>(smem_raw);
-    float *sn = ring + L.ring_f;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sn + L.sin_f);
+    float *snb = ring + L.ring_f;  // two sine buffers
+    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * L.sin_f);
+    BlockRing br;
+    br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * lpw;
@@ -170,16 +220,8 @@ __global__ void __launch_bounds__(32)
     const int row0 = int(bi * T);
     const int b_off = L.th_f + (has_a ? L.vec_f : 0);
     const uint32_t stage_tx = uint32_t(L.th_f + (has_a ? 2 : 1) * L.vec_f) * 4u;
-
-    WarpRing<kGasNS> rg;
-    rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) {
-        prefetch_tmap(&tmTh);
-        prefetch_tmap(&tmB);
-        if (has_a) prefetch_tmap(&tmA);
-    }
-    auto issue = [&](int s, int64_t j) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
         float *st = ring + size_t(s) * L.stage_f;
         const int r = row0 + int(j * ts);
         mbar_arrive_expect_tx(&bars[s], stage_tx);
@@ -187,12 +229,17 @@ __global__ void __launch_bounds__(32)
         if (has_a) tma_load_3d(st + L.th_f, &tmA, 0, head0, r, &bars[s], pol);
         tma_load_3d(st + b_off, &tmB, 0, head0, r, &bars[s], pol);
     };
-    const int npro = int(min64(kGasNS, nblk));
-    if (lane == 0)
+    const int npro = int(min64(kNS, nblk));
+    if (tid == kBlock - 1) {
+        prefetch_tmap(&tmTh);
+        prefetch_tmap(&tmB);
+        if (has_a) prefetch_tmap(&tmA);
         for (int s = 0; s < npro; ++s) issue(s, s);
-    for (int s = 0; s < npro; ++s) rg.armed(s);
+    }
+    if (producer)
+        for (int s = 0; s < npro; ++s) br.rg.armed(s);
 
-    const bool active = lane < nl;
+    const bool active = !producer && lane < nl;
     float x[GK];
     if (active && h0 != nullptr) {
         lds_vec<GK>(h0 + (bi * H + head0 + lane) * GK, x);  // 16-byte aligned global loads
@@ -202,23 +249,27 @@ __global__ void __launch_bounds__(32)
     }
     float *hp = h + ((bi * T) * H + head0 + lane) * GK;
 
-    for (int64_t j = 0; j < nblk; ++j) {
-        const int s = int(j % kGasNS);
-        if (!rg.wait(s, ctl)) {
-            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
-            rg.drain(ctl, lane);
-            return;
+    for (int64_t it = 0; it <= nblk; ++it) {
+        if (producer && it < nblk) {
+            const int s = int(it % kNS);
+            if (br.rg.wait(s, ctl)) {
+                angle_range(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0,
+                            int(min64(ts, T - it * ts)) * lpw * GN, tid - 32);
+            } else {
+                if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+                *br.abort_word = 1;
+            }
         }
-        const int n = int(min64(ts, T - j * ts));
-        float *st = ring + size_t(s) * L.stage_f;
-        stage_sincos(st, sn, n * lpw * GN, lane);
-        __syncwarp();
-        if (active) {
+        if (active && it >= 1) {
+            const int64_t j = it - 1;
+            const float *st = ring + size_t(j % kNS) * L.stage_f;
+            const float *sc = snb + (j & 1) * L.sin_f;
+            const int n = int(min64(ts, T - j * ts));
             for (int u = 0; u < n; ++u) {
                 const int item = u * lpw + lane;
                 float cs[GN], sv[GN], bv[GK];
                 lds_vec<GN>(st + item * GN, cs);
-                lds_vec<GN>(sn + item * GN, sv);
+                lds_vec<GN>(sc + item * GN, sv);
                 lds_vec<GK>(st + b_off + item * GK, bv);
                 if (has_a) {
                     float av[GK];
@@ -233,13 +284,15 @@ __global__ void __launch_bounds__(32)
                 hp += H * GK;
             }
         }
-        __syncwarp();
-        if (j + kGasNS < nblk) {
-            if (lane == 0) {
+        __syncthreads();
+        MGS_BLOCK_ABORT_CHECK(br, producer, lane);
+        if (it >= 1 && it - 1 + kNS < nblk) {
+            const int s = int((it - 1) % kNS);
+            if (tid == kBlock - 1) {
                 fence_proxy_async_smem();
-                issue(s, j + kGasNS);
+                issue(s, it - 1 + kNS);
             }
-            rg.armed(s);
+            if (producer) br.rg.armed(s);
         }
     }
 }
@@ -252,7 +305,7 @@ __global__ void __launch_bounds__(32)
 //   every angle's gradient on the way,
 //   da_t = mu_0 * h_{t-1},  carry = a_t * mu_0 (= A_t^T lambda_t);
 // dh0 = the last carry.
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kBlock)
     gas_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
                    const float *__restrict__ h0, float *__restrict__ dth, float *__restrict__ da,
@@ -261,12 +314,15 @@ __global__ void __launch_bounds__(32)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int nv = has_a ? 3 : 2;  // a, g, h_{t-1}
     const GasSmem L(lpw, ts, nv);
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     float *ring = reinterpret_cast<float *>(smem_raw);
-    float *sn = ring + L.ring_f;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sn + L.sin_f);
+    float *snb = ring + L.ring_f;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * L.sin_f);
+    BlockRing br;
+    br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * lpw;
@@ -274,19 +330,10 @@ __global__ void __launch_bounds__(32)
     const int64_t nblk = (T + ts - 1) / ts;
     const int g_off = L.th_f + (has_a ? L.vec_f : 0), h_off = g_off + L.vec_f;
     const uint32_t stage_tx = uint32_t(L.th_f + nv * L.vec_f) * 4u;
-
-    WarpRing<kGasNS> rg;
-    rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) {
-        prefetch_tmap(&tmTh);
-        prefetch_tmap(&tmG);
-        prefetch_tmap(&tmH);
-        if (has_a) prefetch_tmap(&tmA);
-    }
     // Block j covers in-batch rows T-(j+1)*ts .. T-1-j*ts (rows below 0 are
     // skipped); the h box starts one row earlier and holds h_{t-1}.
-    auto issue = [&](int s, int64_t j) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
         float *st = ring + size_t(s) * L.stage_f;
         const int r = int(bi * T + T - (j + 1) * ts);
         mbar_arrive_expect_tx(&bars[s], stage_tx);
@@ -295,12 +342,22 @@ __global__ void __launch_bounds__(32)
         tma_load_3d(st + g_off, &tmG, 0, head0, r, &bars[s], pol);
         tma_load_3d(st + h_off, &tmH, 0, head0, r - 1, &bars[s], pol);
     };
-    const int npro = int(min64(kGasNS, nblk));
-    if (lane == 0)
+    const int npro = int(min64(kNS, nblk));
+    if (tid == kBlock - 1) {
+        prefetch_tmap(&tmTh);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmH);
+        if (has_a) prefetch_tmap(&tmA);
         for (int s = 0; s < npro; ++s) issue(s, s);
-    for (int s = 0; s < npro; ++s) rg.armed(s);
+    }
+    if (producer)
+        for (int s = 0; s < npro; ++s) br.rg.armed(s);
+    auto first_row = [&](int64_t j) -> int {  // first valid box row of block j
+        const int64_t tb = T - (j + 1) * ts;
+        return int(tb < 0 ? -tb : 0);
+    };
 
-    const bool active = lane < nl;
+    const bool active = !producer && lane < nl;
     float h0v[GK], carry[GK];
 #pragma unroll
     for (int i = 0; i < GK; ++i) {
@@ -309,25 +366,28 @@ __global__ void __launch_bounds__(32)
     }
     if (active && h0 != nullptr) lds_vec<GK>(h0 + (bi * H + head0 + lane) * GK, h0v);
 
-    for (int64_t j = 0; j < nblk; ++j) {
-        const int s = int(j % kGasNS);
-        if (!rg.wait(s, ctl)) {
-            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
-            rg.drain(ctl, lane);
-            return;
+    for (int64_t it = 0; it <= nblk; ++it) {
+        if (producer && it < nblk) {
+            const int s = int(it % kNS);
+            if (br.rg.wait(s, ctl)) {
+                angle_range(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, first_row(it) * lpw * GN,
+                            ts * lpw * GN, tid - 32);
+            } else {
+                if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+                *br.abort_word = 1;
+            }
         }
-        const int64_t tb = T - (j + 1) * ts;       // in-batch row of box row 0
-        const int u0 = int(tb < 0 ? -tb : 0);      // first valid box row
-        float *st = ring + size_t(s) * L.stage_f;
-        stage_sincos(st + u0 * lpw * GN, sn + u0 * lpw * GN, (ts - u0) * lpw * GN, lane);
-        __syncwarp();
-        if (active) {
-            for (int u = ts - 1; u >= u0; --u) {
+        if (active && it >= 1) {
+            const int64_t j = it - 1;
+            const int64_t tb = T - (j + 1) * ts;  // in-batch row of box row 0
+            const float *st = ring + size_t(j % kNS) * L.stage_f;
+            const float *sc = snb + (j & 1) * L.sin_f;
+            for (int u = ts - 1; u >= first_row(j); --u) {
                 const int64_t t = tb + u;
                 const int item = u * lpw + lane;
                 float cs[GN], sv[GN], lam[GK], hp[GK];
                 lds_vec<GN>(st + item * GN, cs);
-                lds_vec<GN>(sn + item * GN, sv);
+                lds_vec<GN>(sc + item * GN, sv);
                 lds_vec<GK>(st + g_off + item * GK, lam);
                 if (t >= 1) {
                     lds_vec<GK>(st + h_off + item * GK, hp);
@@ -384,13 +444,15 @@ __global__ void __launch_bounds__(32)
                 for (int i = 0; i < GK; ++i) carry[i] = av[i] * lam[i];
             }
         }
-        __syncwarp();
-        if (j + kGasNS < nblk) {
-            if (lane == 0) {
+        __syncthreads();
+        MGS_BLOCK_ABORT_CHECK(br, producer, lane);
+        if (it >= 1 && it - 1 + kNS < nblk) {
+            const int s = int((it - 1) % kNS);
+            if (tid == kBlock - 1) {
                 fence_proxy_async_smem();
-                issue(s, j + kGasNS);
+                issue(s, it - 1 + kNS);
             }
-            rg.armed(s);
+            if (producer) br.rg.armed(s);
         }
     }
     if (active && dh0 != nullptr) {
@@ -401,118 +463,123 @@ __global__ void __launch_bounds__(32)
 }
 
 // ---------------------------------------------------------------- matrix forward
-// Thread j of a lane's 8-thread group carries column j of P_t.
-__global__ void __launch_bounds__(32)
+// Warp 0's thread j of a lane's 8-thread group carries column j of P_t.
+__global__ void __launch_bounds__(kBlock)
     gms_fwd_kernel(const __grid_constant__ CUtensorMap tmTh, float *__restrict__ P, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
-    constexpr int TS = kGmsFwdTS, NS = kGmsFwdNS;
+    constexpr int TS = kGmsFwdTS;
     constexpr int STAGEF = TS * kGmsLanes * GN;  // one theta box (a multiple of 32 floats)
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     float *ring = reinterpret_cast<float *>(smem_raw);
-    float *sn = ring + NS * STAGEF;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sn + STAGEF);
+    float *snb = ring + kNS * STAGEF;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * STAGEF);
+    BlockRing br;
+    br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * kGmsLanes;
     const int sub = lane >> 3, col = lane & 7;
-    const bool active = head0 + sub < H;
+    const bool active = !producer && head0 + sub < H;
     const int64_t nblk = (T + TS - 1) / TS;
     const int row0 = int(bi * T);
-
-    WarpRing<NS> rg;
-    rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) prefetch_tmap(&tmTh);
-    auto issue = [&](int s, int64_t j) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
         mbar_arrive_expect_tx(&bars[s], uint32_t(STAGEF * 4));
         tma_load_3d(ring + size_t(s) * STAGEF, &tmTh, 0, head0, row0 + int(j * TS), &bars[s], pol);
     };
-    const int npro = int(min64(NS, nblk));
-    if (lane == 0)
+    const int npro = int(min64(kNS, nblk));
+    if (tid == kBlock - 1) {
+        prefetch_tmap(&tmTh);
         for (int s = 0; s < npro; ++s) issue(s, s);
-    for (int s = 0; s < npro; ++s) rg.armed(s);
+    }
+    if (producer)
+        for (int s = 0; s < npro; ++s) br.rg.armed(s);
 
     float v[GK];
 #pragma unroll
     for (int i = 0; i < GK; ++i) v[i] = (i == col) ? 1.f : 0.f;
     float *pp = P + ((bi * T) * H + head0 + sub) * (GK * GK) + col;
 
-    for (int64_t j = 0; j < nblk; ++j) {
-        const int s = int(j % NS);
-        if (!rg.wait(s, ctl)) {
-            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
-            rg.drain(ctl, lane);
-            return;
+    for (int64_t it = 0; it <= nblk; ++it) {
+        if (producer && it < nblk) {
+            const int s = int(it % kNS);
+            if (br.rg.wait(s, ctl)) {
+                angle_range(ring + size_t(s) * STAGEF, snb + (it & 1) * STAGEF, 0,
+                            int(min64(TS, T - it * TS)) * kGmsLanes * GN, tid - 32);
+            } else {
+                if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+                *br.abort_word = 1;
+            }
         }
-        const int n = int(min64(TS, T - j * TS));
-        float *st = ring + size_t(s) * STAGEF;
-        stage_sincos(st, sn, n * kGmsLanes * GN, lane);
-        __syncwarp();
-        for (int u = 0; u < n; ++u) {
-            const int item = u * kGmsLanes + sub;
-            float cs[GN], sv[GN];
-            lds_vec<GN>(st + item * GN, cs);
-            lds_vec<GN>(sn + item * GN, sv);
-            mesh_apply(v, cs, sv);
-            if (active) {
+        if (!producer && it >= 1) {
+            const int64_t j = it - 1;
+            const float *st = ring + size_t(j % kNS) * STAGEF;
+            const float *sc = snb + (j & 1) * STAGEF;
+            const int n = int(min64(TS, T - j * TS));
+            for (int u = 0; u < n; ++u) {
+                const int item = u * kGmsLanes + sub;
+                float cs[GN], sv[GN];
+                lds_vec<GN>(st + item * GN, cs);
+                lds_vec<GN>(sc + item * GN, sv);
+                mesh_apply(v, cs, sv);
+                if (active) {
 #pragma unroll
-                for (int i = 0; i < GK; ++i) st_cs(pp + i * GK, v[i]);
+                    for (int i = 0; i < GK; ++i) st_cs(pp + i * GK, v[i]);
+                }
+                pp += H * GK * GK;
             }
-            pp += H * GK * GK;
         }
-        __syncwarp();
-        if (j + NS < nblk) {
-            if (lane == 0) {
+        __syncthreads();
+        MGS_BLOCK_ABORT_CHECK(br, producer, lane);
+        if (it >= 1 && it - 1 + kNS < nblk) {
+            const int s = int((it - 1) % kNS);
+            if (tid == kBlock - 1) {
                 fence_proxy_async_smem();
-                issue(s, j + NS);
+                issue(s, it - 1 + kNS);
             }
-            rg.armed(s);
+            if (producer) br.rg.armed(s);
         }
     }
 }
 
 // ---------------------------------------------------------------- matrix backward
-// Per step and column j (t downwards): Lambda = G_t[:, j] + carry; x = P_t[:, j];
-// both go back through the layers by transposed rotations (x recovers the
-// column before each layer, exact up to rounding since the mesh is
-// orthogonal), each thread adding its column's share of every angle's
+// Per step and column j (t downwards, warp 0): Lambda = G_t[:, j] + carry;
+// x = P_t[:, j]; both go back through the layers by transposed rotations (x
+// recovers the column before each layer, exact up to rounding since the mesh
+// is orthogonal), each thread adding its column's share of every angle's
 // gradient; the eight shares are summed by a butterfly reduce-scatter that
 // leaves angles 4j .. 4j+3 with thread j.  carry = A_t^T Lambda[:, j].
-__global__ void __launch_bounds__(32)
+__global__ void __launch_bounds__(kBlock)
     gms_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmG, float *__restrict__ dth, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
-    constexpr int TS = kGmsBwdTS, NS = kGmsBwdNS;
+    constexpr int TS = kGmsBwdTS;
     using TM = MatTile<GK, true>;  // swizzled: conflict-free column reads
     constexpr int MATF = TS * TM::MF, THF = TS * kGmsLanes * GN;
     constexpr int STAGEF = int(align_up(size_t(2 * MATF + THF), TM::kAlign / 4));
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const int lane = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     unsigned char *sbase = align_smem(smem_raw, TM::kAlign);
     float *ring = reinterpret_cast<float *>(sbase);
-    float *sn = ring + NS * STAGEF;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sn + THF);
+    float *snb = ring + kNS * STAGEF;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * THF);
+    BlockRing br;
+    br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
     const int64_t bi = g / groups_per_b;
     const int head0 = int(g % groups_per_b) * kGmsLanes;
     const int sub = lane >> 3, col = lane & 7;
-    const bool active = head0 + sub < H;
+    const bool active = !producer && head0 + sub < H;
     const int64_t nblk = (T + TS - 1) / TS;
-
-    WarpRing<NS> rg;
-    rg.init(bars, lane);
     const uint64_t pol = policy_evict_first();
-    if (lane == 0) {
-        prefetch_tmap(&tmTh);
-        prefetch_tmap(&tmP);
-        prefetch_tmap(&tmG);
-    }
-    auto issue = [&](int s, int64_t j) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
         float *st = ring + size_t(s) * STAGEF;
         const int r = int(bi * T + T - (j + 1) * TS);
         mbar_arrive_expect_tx(&bars[s], uint32_t((2 * MATF + THF) * 4));
@@ -520,90 +587,107 @@ __global__ void __launch_bounds__(32)
         TM::load(st + MATF, &tmG, head0, r, &bars[s], pol);
         tma_load_3d(st + 2 * MATF, &tmTh, 0, head0, r, &bars[s], pol);
     };
-    const int npro = int(min64(NS, nblk));
-    if (lane == 0)
+    const int npro = int(min64(kNS, nblk));
+    if (tid == kBlock - 1) {
+        prefetch_tmap(&tmTh);
+        prefetch_tmap(&tmP);
+        prefetch_tmap(&tmG);
         for (int s = 0; s < npro; ++s) issue(s, s);
-    for (int s = 0; s < npro; ++s) rg.armed(s);
+    }
+    if (producer)
+        for (int s = 0; s < npro; ++s) br.rg.armed(s);
+    auto first_row = [&](int64_t j) -> int {
+        const int64_t tb = T - (j + 1) * TS;
+        return int(tb < 0 ? -tb : 0);
+    };
 
     float carry[GK];
 #pragma unroll
     for (int i = 0; i < GK; ++i) carry[i] = 0.f;
 
-    for (int64_t j = 0; j < nblk; ++j) {
-        const int s = int(j % NS);
-        if (!rg.wait(s, ctl)) {
-            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
-            rg.drain(ctl, lane);
-            return;
+    for (int64_t it = 0; it <= nblk; ++it) {
+        if (producer && it < nblk) {
+            const int s = int(it % kNS);
+            if (br.rg.wait(s, ctl)) {
+                angle_range(ring + size_t(s) * STAGEF + 2 * MATF, snb + (it & 1) * THF,
+                            first_row(it) * kGmsLanes * GN, THF, tid - 32);
+            } else {
+                if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+                *br.abort_word = 1;
+            }
         }
-        const int64_t tb = T - (j + 1) * TS;
-        const int u0 = int(tb < 0 ? -tb : 0);
-        float *st = ring + size_t(s) * STAGEF;
-        float *sth = st + 2 * MATF;
-        stage_sincos(sth + u0 * kGmsLanes * GN, sn + u0 * kGmsLanes * GN, (TS - u0) * kGmsLanes * GN, lane);
-        __syncwarp();
-        for (int u = TS - 1; u >= u0; --u) {
-            const int64_t t = tb + u;
-            const TileRef<GK, true> Pt{st, u, sub}, Gt{st + MATF, u, sub};
-            const int item = u * kGmsLanes + sub;
-            float cs[GN], sv[GN], lam[GK], x[GK];
-            lds_vec<GN>(sth + item * GN, cs);
-            lds_vec<GN>(sn + item * GN, sv);
+        if (!producer && it >= 1) {
+            const int64_t j = it - 1;
+            const int64_t tb = T - (j + 1) * TS;
+            const float *st = ring + size_t(j % kNS) * STAGEF;
+            const float *sth = st + 2 * MATF;
+            const float *sc = snb + (j & 1) * THF;
+            for (int u = TS - 1; u >= first_row(j); --u) {
+                const int64_t t = tb + u;
+                const TileRef<GK, true> Pt{st, u, sub}, Gt{st + MATF, u, sub};
+                const int item = u * kGmsLanes + sub;
+                float cs[GN], sv[GN], lam[GK], x[GK];
+                lds_vec<GN>(sth + item * GN, cs);
+                lds_vec<GN>(sc + item * GN, sv);
 #pragma unroll
-            for (int i = 0; i < GK; ++i) {
-                lam[i] = Gt.at(i, col) + carry[i];
-                x[i] = Pt.at(i, col);
-            }
-            float d[32];
-#pragma unroll
-            for (int l = GK - 1; l >= 0; --l) {
-#pragma unroll
-                for (int q = 0; q < layer_pairs(l); ++q) {
-                    const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-                    d[n] = fmaf(lam[p + 1], x[p], -lam[p] * x[p + 1]);
-                    rot_bwd(x[p], x[p + 1], cs[n], sv[n]);
-                    rot_bwd(lam[p], lam[p + 1], cs[n], sv[n]);
+                for (int i = 0; i < GK; ++i) {
+                    lam[i] = Gt.at(i, col) + carry[i];
+                    x[i] = Pt.at(i, col);
                 }
-            }
+                float d[32];
 #pragma unroll
-            for (int n = GN; n < 32; ++n) d[n] = 0.f;
-            // butterfly reduce-scatter over the 8 columns: 32 -> 4 values
+                for (int l = GK - 1; l >= 0; --l) {
 #pragma unroll
-            for (int o = 4, half = 16; o >= 1; o >>= 1, half >>= 1) {
-                const bool up = (col & o) != 0;
-#pragma unroll
-                for (int c = 0; c < half; ++c) {
-                    const float send = up ? d[c] : d[c + half];
-                    const float keep = up ? d[c + half] : d[c];
-                    d[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    for (int q = 0; q < layer_pairs(l); ++q) {
+                        const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+                        d[n] = fmaf(lam[p + 1], x[p], -lam[p] * x[p + 1]);
+                        rot_bwd(x[p], x[p + 1], cs[n], sv[n]);
+                        rot_bwd(lam[p], lam[p + 1], cs[n], sv[n]);
+                    }
                 }
-            }
-            if (active && col < GN / 4)
-                st_cs4(dth + ((bi * T + t) * H + head0 + sub) * GN + 4 * col, make_float4(d[0], d[1], d[2], d[3]));
 #pragma unroll
-            for (int i = 0; i < GK; ++i) carry[i] = lam[i];
+                for (int n = GN; n < 32; ++n) d[n] = 0.f;
+                // butterfly reduce-scatter over the 8 columns: 32 -> 4 values
+#pragma unroll
+                for (int o = 4, half = 16; o >= 1; o >>= 1, half >>= 1) {
+                    const bool up = (col & o) != 0;
+#pragma unroll
+                    for (int c = 0; c < half; ++c) {
+                        const float send = up ? d[c] : d[c + half];
+                        const float keep = up ? d[c + half] : d[c];
+                        d[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                if (active && col < GN / 4)
+                    st_cs4(dth + ((bi * T + t) * H + head0 + sub) * GN + 4 * col,
+                           make_float4(d[0], d[1], d[2], d[3]));
+#pragma unroll
+                for (int i = 0; i < GK; ++i) carry[i] = lam[i];
+            }
         }
-        __syncwarp();
-        if (j + NS < nblk) {
-            if (lane == 0) {
+        __syncthreads();
+        MGS_BLOCK_ABORT_CHECK(br, producer, lane);
+        if (it >= 1 && it - 1 + kNS < nblk) {
+            const int s = int((it - 1) % kNS);
+            if (tid == kBlock - 1) {
                 fence_proxy_async_smem();
-                issue(s, j + NS);
+                issue(s, it - 1 + kNS);
             }
-            rg.armed(s);
+            if (producer) br.rg.armed(s);
         }
     }
 }
 
-// Lanes per warp for the affine scan: the fewest (each lane is one thread)
-// that still gives about one warp per SM sub-partition or fewer, capped by
-// the heads of one batch row.
-int gas_lanes_per_warp(int64_t B, int64_t H) {
+// Lanes per recurrence warp for the affine scan: as many as keep at least
+// one block per SM, at most kGasMaxLanes (beyond that the angle warps, which
+// convert 28 angles per lane and step, fall behind the recurrence), and no
+// more than the heads of one batch row.
+int gas_lanes_per_block(int64_t B, int64_t H) {
     int sms = 148;
     int dev = 0;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (B * H + 4 * sms - 1) / (4 * int64_t(sms));
     int lpw = 1;
-    while (lpw < want && lpw < 32) lpw *= 2;
+    while (lpw < kGasMaxLanes && B * H / (2 * lpw) >= sms) lpw *= 2;
     while (lpw > 1 && lpw / 2 >= H) lpw /= 2;
     return lpw;
 }
@@ -612,7 +696,7 @@ int gas_lanes_per_warp(int64_t B, int64_t H) {
 
 cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, const float *h0, float *h,
                            int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
-    const int lpw = gas_lanes_per_warp(B, H), ts = kItems / lpw;
+    const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
     CUtensorMap tTh, tA, tB;
     cudaError_t e;
@@ -627,15 +711,15 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(GasSmem(lpw, ts, a ? 2 : 1).bytes());
     if ((e = ensure_smem_attr((const void *)gas_fwd_kernel, smem)) != cudaSuccess) return e;
-    gas_fwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts,
-                                                            a != nullptr, ctl);
+    gas_fwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts,
+                                                                a != nullptr, ctl);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, const float *h, const float *gh,
                            float *dth, float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t H,
                            const DevCtl &ctl, cudaStream_t s) {
-    const int lpw = gas_lanes_per_warp(B, H), ts = kItems / lpw;
+    const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
     CUtensorMap tTh, tA, tG, tH;
     cudaError_t e;
@@ -651,8 +735,8 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(GasSmem(lpw, ts, a ? 3 : 2).bytes());
     if ((e = ensure_smem_attr((const void *)gas_bwd_kernel, smem)) != cudaSuccess) return e;
-    gas_bwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H, gpb,
-                                                            lpw, ts, a != nullptr, ctl);
+    gas_bwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H,
+                                                                gpb, lpw, ts, a != nullptr, ctl);
     return cudaGetLastError();
 }
 
@@ -664,9 +748,9 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
     const int64_t gpb = (H + kGmsLanes - 1) / kGmsLanes, blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     constexpr int STAGEF = kGmsFwdTS * kGmsLanes * GN;
-    const int smem = int((kGmsFwdNS + 1) * STAGEF * 4 + kGmsFwdNS * sizeof(uint64_t));
+    const int smem = int((kNS + 2) * STAGEF * 4 + kNS * sizeof(uint64_t) + 16);
     if ((e = ensure_smem_attr((const void *)gms_fwd_kernel, smem)) != cudaSuccess) return e;
-    gms_fwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tTh, P, B, T, H, gpb, ctl);
+    gms_fwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, P, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
@@ -682,9 +766,9 @@ cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, f
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     constexpr int MATF = kGmsBwdTS * TM::MF, THF = kGmsBwdTS * kGmsLanes * GN;
     constexpr int STAGEF = int(align_up(size_t(2 * MATF + THF), TM::kAlign / 4));
-    const int smem = int(size_t(kGmsBwdNS * STAGEF + THF) * 4 + kGmsBwdNS * sizeof(uint64_t) + TM::kAlign);
+    const int smem = int(size_t(kNS * STAGEF + 2 * THF) * 4 + kNS * sizeof(uint64_t) + 16 + TM::kAlign);
     if ((e = ensure_smem_attr((const void *)gms_bwd_kernel, smem)) != cudaSuccess) return e;
-    gms_bwd_kernel<<<dim3(unsigned(blocks)), 32, smem, s>>>(tTh, tP, tG, dth, B, T, H, gpb, ctl);
+    gms_bwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tP, tG, dth, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 

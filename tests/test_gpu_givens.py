@@ -61,11 +61,12 @@ def _run_gas(B, T, H, seed, h0, with_a, rows=None):
 @pytest.mark.parametrize("B,T,H,h0,with_a", [
     (1, 1, 1, "normal", True),
     (2, 7, 3, "none", True),
-    (3, 130, 5, "normal", False),     # 1 lane per warp, 64-step stages, ragged
-    (128, 64, 8, "normal", True),     # the pages' lab shape: 2 lanes per warp
-    (2, 45, 1000, "normal", True),    # 4 lanes per warp, partial head groups
-    (64, 20, 64, "none", True),       # 8 lanes per warp
-    (40, 9, 256, "normal", True),     # 32 lanes per warp, 2-step stages, ragged
+    (3, 130, 5, "normal", False),     # 1 lane per block, 64-step stages, ragged
+    (5, 33, 100, "normal", True),     # 2 lanes per block, partial head group
+    (128, 64, 8, "normal", True),     # the pages' lab shape: 4 lanes per block
+    (2, 45, 1000, "normal", True),    # 8 lanes per block, partial head groups
+    (64, 20, 64, "none", True),       # 8 lanes per block, 8-step stages, ragged
+    (40, 9, 256, "normal", True),     # 8 lanes per block, a block shorter than a stage
 ])
 def test_givens_affine_scan(B, T, H, h0, with_a):
     _run_gas(B, T, H, seed=900 + B * T + H, h0=h0, with_a=with_a)
