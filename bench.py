@@ -87,10 +87,11 @@ def measured_peak():
 
 
 # sources each kernel family is built from (a change to any of them makes
-# recorded ncu counters stale)
-KERNEL_SOURCES = {"mas": ["mgs_mas.cu"], "ms": ["mgs_ms.cu"], "psl": ["mgs_psl.cu"]}
-COMMON_SOURCES = ["mgs_device.cuh", "mgs_tiles.cuh", "mgs_launch.h"]
-CHUNK_SOURCES = {"ms": ["mgs_chunk.cuh"], "mas": ["mgs_chunk.cuh"], "psl": []}
+# recorded ncu counters stale; mgs_launch.h holds only host declarations)
+KERNEL_SOURCES = {"mas": ["mgs_mas.cu"], "ms": ["mgs_ms.cu"], "psl": ["mgs_psl.cu"],
+                  "gas": ["mgs_givens.cu"], "gms": ["mgs_givens.cu"]}
+COMMON_SOURCES = ["mgs_device.cuh", "mgs_tiles.cuh"]
+CHUNK_SOURCES = {"ms": ["mgs_chunk.cuh"], "mas": ["mgs_chunk.cuh"], "psl": [], "gas": [], "gms": []}
 TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
 
 
@@ -221,6 +222,51 @@ def whole_job_gbps(step_bytes_per_rank, world, ms_step_max):
 
 
 # ---------------------------------------------------------------- GPU arm
+def givens_peak_memory(torch, api, device, B=128, T=64, H=8, k=8):
+    """Peak device memory of one forward+backward through the Givens affine
+    scan at the pages' memory-benchmark shape (B=128, T=64, d=64, k=8): the
+    angle-fused op against the generic path that first builds A = G(theta)
+    diag(a) with eager autograd ops and then runs matrix_affine_scan.  Memory
+    held before the call (the inputs) is not counted."""
+    from scan_linear_recurrences_gb300 import inputs
+
+    d = inputs.givens_affine_inputs(B, T, H, k, seed=BASE_SEED_GIVENS_MEMORY, device=device, h0="normal")
+    g = d["grad_h"]
+
+    def mesh_eager(theta):
+        M = torch.eye(k, device=device).expand(B, T, H, k, k)
+        n = 0
+        for layer in range(k):
+            for p in range(layer % 2, k - 1, 2):
+                c, s = torch.cos(theta[..., n, None]), torch.sin(theta[..., n, None])
+                x, y = M[..., p, :], M[..., p + 1, :]
+                rows = list(M.unbind(-2))
+                rows[p], rows[p + 1] = c * x - s * y, s * x + c * y
+                M = torch.stack(rows, dim=-2)
+                n += 1
+        return M
+
+    def run(fused):
+        leaves = {n: d[n].clone().requires_grad_(True) for n in ("theta", "a", "b", "h0")}
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats(device)
+        base = torch.cuda.memory_allocated(device)
+        if fused:
+            h = api.givens_affine_scan(leaves["theta"], leaves["a"], leaves["b"], leaves["h0"])
+        else:
+            A = mesh_eager(leaves["theta"]) * leaves["a"].unsqueeze(-2)
+            h = api.matrix_affine_scan(A, leaves["b"], leaves["h0"])
+        (h * g).sum().backward()
+        torch.cuda.synchronize()
+        return (torch.cuda.max_memory_allocated(device) - base) / 1e6
+
+    return {"shape": f"B={B} T={T} H={H} k={k} (d=64)", "angle_fused_MB": round(run(True), 2),
+            "eager_mesh_then_matrix_affine_scan_MB": round(run(False), 2)}
+
+
+BASE_SEED_GIVENS_MEMORY = 20261202 + 99
+
+
 class Runner:
     """Holds one workload's device buffers and runs its fwd / bwd calls."""
 
@@ -384,7 +430,8 @@ def run_gpu(args):
     b.lib()
 
     ids = [int(x) for x in args.workloads.split(",")]
-    ws = [inputs.WORKLOADS[i] for i in ids]
+    # the report-only shapes may be named too (profiling their kernels alone)
+    ws = [inputs.WORKLOADS[i] if i in inputs.WORKLOADS else inputs.EXTRA_WORKLOADS[i] for i in ids]
     if args.batch_rows:
         # profiling only: a smaller case of the same kernels (fewer batch rows)
         from dataclasses import replace
@@ -565,6 +612,7 @@ def run_gpu(args):
                 "bytes": "28 per element + checkpoints", "l2": "flushed"}
             del ws
         b.mgs_check(sid)
+        extra["givens_peak_memory"] = givens_peak_memory(torch, api, device)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
