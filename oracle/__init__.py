@@ -1,5 +1,6 @@
 """Float64 CPU oracle for matrix_affine_scan, matrix_scan, parallel_scan_log,
-linear_scan and the Givens-mesh (angle-parameterised) affine and matrix scans.
+linear_scan, the Givens-mesh (angle-parameterised) affine and matrix scans and
+the delta rule (DeltaNet) forward.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -63,10 +64,12 @@ def _load():
             lib.oracle_gas_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_gms_fwd.argtypes = [dp, dp, i64, i64, i64, i64]
             lib.oracle_gms_bwd.argtypes = [dp, dp, dp, i64, i64, i64, i64]
+            lib.oracle_delta_fwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, i64, i64, i64, i64]
             lib.oracle_num_threads.restype = ctypes.c_int
             for f in ("oracle_mas_fwd", "oracle_mas_bwd", "oracle_ms_fwd", "oracle_ms_bwd",
                       "oracle_psl_fwd", "oracle_psl_bwd", "oracle_linear_fwd", "oracle_linear_bwd",
-                      "oracle_gas_fwd", "oracle_gas_bwd", "oracle_gms_fwd", "oracle_gms_bwd"):
+                      "oracle_gas_fwd", "oracle_gas_bwd", "oracle_gms_fwd", "oracle_gms_bwd",
+                      "oracle_delta_fwd"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -239,3 +242,17 @@ def gms_bwd(theta, grad_P):
     dth = np.empty_like(th)
     _load().oracle_gms_bwd(_p(th), _p(G), _p(dth), B, T, H, K)
     return dth
+
+
+# ---------------------------------------------------------------- delta rule
+def delta_fwd(q, k, v, beta, S0=None, want_state=False):
+    """S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T, o_t = S_t q_t.
+    q, k, v [B,T,H,D], beta [B,T,H], S0 [B,H,D,D] or None -> o (and S_T)."""
+    q, k, v, beta, S0 = _f64(q), _f64(k), _f64(v), _f64(beta), _f64(S0)
+    B, T, H, D = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and beta.shape == (B, T, H)
+    assert S0 is None or S0.shape == (B, H, D, D)
+    o = np.empty_like(q)
+    ST = np.empty((B, H, D, D), dtype=np.float64) if want_state else None
+    _load().oracle_delta_fwd(_p(q), _p(k), _p(v), _p(beta), _p(S0), _p(o), _p(ST), B, T, H, D)
+    return (o, ST) if want_state else o

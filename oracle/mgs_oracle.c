@@ -23,6 +23,8 @@
  *   Givens affine scan  matrix_affine_scan with A_t = G(theta_t) diag(a_t),
  *   Givens matrix scan  matrix_scan with A_t = G(theta_t): the brick-wall
  *                       rotation mesh of GivensMinGRU, fed by its angles.
+ *   delta rule          S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T,
+ *                       o_t = S_t q_t (DeltaNet, behind DeltaMinGRU).
  * Backward passes are the adjoint (reverse-mode) recurrences of those maps.
  *
  * Layouts (row-major, contiguous, double):
@@ -625,6 +627,57 @@ void oracle_gms_bwd(const double *theta, const double *gP, double *dtheta, int64
         free(dAt);
         free(lam);
         free(nxt);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* delta rule (DeltaNet), forward                                       */
+/* ------------------------------------------------------------------ */
+
+/* DeltaMinGRU's recurrence ("mingru-scans" home page, lineage paragraph:
+ * DeltaMinGRU reimplements DeltaNet, Yang et al. 2024, arXiv:2406.06484,
+ * whose chunked WY form is its parallel forward).  The delta rule, per
+ * (batch, head) lane, with a d_v x d_k state S (here d_v = d_k = D):
+ *   S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T,   o_t = S_t q_t,
+ * S_0 = S0 (zeros when NULL).  Layouts: q, k, v, o [B][T][H][D];
+ * beta [B][T][H]; S0, S_T [B][H][D][D] with S[i][j], i the value index.
+ * S_T (the state after step T) is written when not NULL. */
+void oracle_delta_fwd(const double *q, const double *k, const double *v, const double *beta,
+                      const double *S0, double *o, double *ST, int64_t B, int64_t T, int64_t H,
+                      int64_t D)
+{
+    int64_t lanes = B * H, DD = D * D;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+        int64_t bb = lane / H, hd = lane % H;
+        double *S = (double *)malloc(sizeof(double) * (size_t)DD);
+        double *Sk = (double *)malloc(sizeof(double) * (size_t)D);
+        for (int64_t e = 0; e < DD; ++e)
+            S[e] = S0 ? S0[(bb * H + hd) * DD + e] : 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t st = (bb * T + t) * H + hd;
+            const double *kt = k + st * D, *vt = v + st * D, *qt = q + st * D;
+            double bt = beta[st];
+            for (int64_t i = 0; i < D; ++i) {
+                double s = 0.0;
+                for (int64_t j = 0; j < D; ++j)
+                    s += S[i * D + j] * kt[j];
+                Sk[i] = s;
+            }
+            for (int64_t i = 0; i < D; ++i)
+                for (int64_t j = 0; j < D; ++j)
+                    S[i * D + j] += bt * (vt[i] - Sk[i]) * kt[j];
+            for (int64_t i = 0; i < D; ++i) {
+                double s = 0.0;
+                for (int64_t j = 0; j < D; ++j)
+                    s += S[i * D + j] * qt[j];
+                o[st * D + i] = s;
+            }
+        }
+        if (ST)
+            memcpy(ST + (bb * H + hd) * DD, S, sizeof(double) * (size_t)DD);
+        free(S);
+        free(Sk);
     }
 }
 

@@ -38,8 +38,16 @@ MUTATIONS = [
     ("gas_bwd_dropped_carry", "lam[i] = gh[st * K + i] + nxt[i];", "lam[i] = gh[st * K + i];", 0),
     ("gms_bwd_P_not_transposed", "s += lam[i * K + j] * Pprev[m * K + j];",
      "s += lam[i * K + j] * Pprev[j * K + m];", 1),
+    ("delta_dropped_beta", "S[i * D + j] += bt * (vt[i] - Sk[i]) * kt[j];",
+     "S[i * D + j] += (vt[i] - Sk[i]) * kt[j];", 0),
+    ("delta_no_erase", "S[i * D + j] += bt * (vt[i] - Sk[i]) * kt[j];",
+     "S[i * D + j] += bt * vt[i] * kt[j];", 0),
+    ("delta_state_transposed", "s += S[i * D + j] * kt[j];", "s += S[j * D + i] * kt[j];", 0),
+    ("delta_state_never_updated", "for (int64_t i = 0; i < D; ++i)\n                for (int64_t j = 0; j < D; ++j)\n"
+     "                    S[i * D + j] += bt", "for (int64_t i = 0; i < 0; ++i)\n                for (int64_t j = 0; j < D; ++j)\n"
+     "                    S[i * D + j] += bt", 0),
 ]
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_givens_pins.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_givens_pins.py", "test_oracle_delta_pins.py"]
 
 
 def _mutate(text, old, new, occ):
