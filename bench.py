@@ -64,6 +64,9 @@ def op_bytes(w, direction):
             return steps * 4 * (n + 3 * k) + (init if w.h0 != "none" else 0)
         # read theta, a, grad_h, h; write d_theta, da, db; read h0, write dh0
         return steps * 4 * (2 * n + 5 * k) + (init if w.h0 != "none" else 0) + init
+    if w.op == "delta":  # forward only: read q, k, v, beta, S0; write o, S_T (k holds D)
+        elems, state = B * T * H * k, B * H * k * k
+        return (4 * elems + B * T * H + 2 * state) * 4 if direction == "fwd" else 0
     if w.op == "gms":
         steps, n = B * T * H, k * (k - 1) // 2
         if direction == "fwd":  # read theta; write P
@@ -267,6 +270,31 @@ def givens_peak_memory(torch, api, device, B=128, T=64, H=8, k=8):
 BASE_SEED_GIVENS_MEMORY = 20261202 + 99
 
 
+def delta_flops(w, C=64):
+    """Floating-point operations of the chunked WY forward per call: per
+    64-step chunk the products K K^T, Q K^T, the forward substitution for
+    [W | U], W S^T, Q S^T, tril(Q K^T) U' and U'^T K, i.e. 4 C^2 D + 3 C D^2
+    multiply-adds (2 flops each); chunks are counted whole."""
+    D = w.k
+    chunks = -(-w.T // C)
+    return 2 * (4 * C * C * D + 3 * C * D * D) * chunks * w.B * w.H
+
+
+def fp32_fma_peak_tflops():
+    """fp32 peak of the CUDA cores from unit counts and clock: SMs x 128 FMA
+    lanes x 2 flops x the maximum SM clock (MEASURED_PEAKS.json sm_max_mhz,
+    else the nominal 2070 MHz)."""
+    import torch
+    mhz = 2070.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    except Exception:
+        pass
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
 class Runner:
     """Holds one workload's device buffers and runs its fwd / bwd calls."""
 
@@ -298,6 +326,8 @@ class Runner:
             self.dth, self.da, self.db, self.dh0 = e(B, T, H, k * (k - 1) // 2), e(B, T, H, k), e(B, T, H, k), e(B, H, k)
         elif w.op == "gms":
             self.P, self.dth = e(B, T, H, k, k), e(B, T, H, k * (k - 1) // 2)
+        elif w.op == "delta":
+            self.o, self.ST = e(B, T, H, k), e(B, H, k, k)
         else:
             self.h = e(B, T, H)
             self.dlc, self.dlv, self.dl0 = e(B, T, H), e(B, T, H), e(B, H)
@@ -329,6 +359,9 @@ class Runner:
                                          None, 0, stream)
         elif w.op == "gms":
             b.mgs_givens_matrix_scan_fwd(d["theta"], self.P, w.B, w.T, w.H, w.k, None, 0, stream)
+        elif w.op == "delta":
+            b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], self.o, self.ST, w.B, w.T, w.H, w.k,
+                                 None, 0, stream)
         else:
             b.mgs_parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, None,
                                         w.B, w.T, w.H, None, 0, stream)
@@ -349,6 +382,8 @@ class Runner:
         elif w.op == "gms":
             b.mgs_givens_matrix_scan_bwd(d["theta"], self.P, d["grad_P"], self.dth, w.B, w.T, w.H, w.k, None, 0,
                                          stream)
+        elif w.op == "delta":
+            pass  # forward only (the pages' DeltaMinGRU row is its chunked-WY forward)
         else:
             b.mgs_parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, d["grad_h"],
                                         self.dlc, self.dlv, self.dl0, w.B, w.T, w.H, None, 0, stream)
@@ -579,6 +614,15 @@ def run_gpu(args):
                     bs.append(e1.elapsed_time(e2))
             fm, bm = statistics.median(fs), statistics.median(bs)
             nbytes = op_bytes(w, "fwd") + op_bytes(w, "bwd")
+            if w.op == "delta":
+                flops = delta_flops(w)
+                extra[f"{w.op}_c{w.cid}"] = {
+                    "shape": w.name, "fwd_us": round(fm * 1e3, 2), "fwd_GBps": round(nbytes / (fm * 1e-3) / 1e9, 1),
+                    "fwd_TFLOPs": round(flops / (fm * 1e-3) / 1e12, 2), "flops_per_call": flops,
+                    "pct_of_fp32_fma_peak": round(100 * flops / (fm * 1e-3) / 1e12 / fp32_fma_peak_tflops(), 1),
+                    "l2": "flushed"}
+                del r
+                continue
             extra[f"{w.op}_c{w.cid}"] = {"shape": w.name, "fwd_us": round(fm * 1e3, 2), "bwd_us": round(bm * 1e3, 2),
                                          "fwd_bwd_us": round((fm + bm) * 1e3, 2),
                                          "fwd_bwd_GBps": round(nbytes / ((fm + bm) * 1e-3) / 1e9, 1),

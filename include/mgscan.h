@@ -76,7 +76,8 @@ enum {
     MGS_OP_GIVENS_AFFINE_SCAN_FWD = 9,
     MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10,
     MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11,
-    MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12
+    MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12,
+    MGS_OP_DELTA_SCAN_FWD = 13
 };
 
 /* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
@@ -268,6 +269,22 @@ mgs_status mgs_givens_matrix_scan_fwd(const float *theta, float *P, int64_t B, i
 mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const float *grad_P,
                                       float *d_theta, int64_t B, int64_t T, int64_t H, int k,
                                       void *workspace, size_t workspace_bytes, mgs_stream_t stream);
+
+/* Delta rule (DeltaNet), forward ("mingru-scans" home page, lineage
+ * paragraph: DeltaMinGRU reimplements DeltaNet, Yang et al. 2024,
+ * arXiv:2406.06484, whose chunked WY representation is its parallel forward),
+ * per (batch, head) lane with a D x D state S (S[i][j], i the value index):
+ *     S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T,   o_t = S_t q_t,
+ * S_0 = S0 (zeros when NULL).  Computed chunk by chunk (64 steps) in the WY
+ * form.  Only D = 64 is supported (else MGS_ERR_UNSUPPORTED).
+ * In: q, k, v [B][T][H][D]; beta [B][T][H] (4-byte aligned); S0 [B][H][D][D]
+ *     (nullable).
+ * Out: o [B][T][H][D]; S_T [B][H][D][D] (nullable: not written), the state
+ *     after step T (S0, or zeros, when T = 0).
+ * No workspace is needed (mgs_workspace_size returns 0 for this op). */
+mgs_status mgs_delta_scan_fwd(const float *q, const float *k, const float *v, const float *beta,
+                              const float *S0, float *o, float *S_T, int64_t B, int64_t T, int64_t H,
+                              int D, void *workspace, size_t workspace_bytes, mgs_stream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns MGS_ERR_TIMEOUT if a kernel's bounded wait gave up since the

@@ -36,6 +36,7 @@ MGS_OP_GIVENS_AFFINE_SCAN_FWD = 9
 MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10
 MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11
 MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12
+MGS_OP_DELTA_SCAN_FWD = 13
 
 
 class MGSError(RuntimeError):
@@ -69,6 +70,7 @@ _SIGNATURES = {
                                           _vp, _sz, _vp]),
     "mgs_givens_matrix_scan_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_givens_matrix_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
+    "mgs_delta_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_check": (_int, [_vp]),
     "mgs_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
     "mgs_debug_wait_flag": (_int, [_vp, _vp]),
@@ -203,6 +205,11 @@ def mgs_givens_matrix_scan_bwd(theta, P, grad_P, d_theta, B, T, H, k, workspace=
                                stream=None):
     return _call("mgs_givens_matrix_scan_bwd", _ptr(theta), _ptr(P), _ptr(grad_P), _ptr(d_theta), B, T, H, k,
                  _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mgs_delta_scan_fwd(q, k, v, beta, S0, o, S_T, B, T, H, D, workspace=None, workspace_bytes=0, stream=None):
+    return _call("mgs_delta_scan_fwd", _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_T),
+                 B, T, H, D, _ptr(workspace), workspace_bytes, _stream(stream))
 
 
 def mgs_check(stream=None):

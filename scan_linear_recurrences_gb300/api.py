@@ -166,6 +166,21 @@ def givens_matrix_scan_bwd(theta, P, grad_P, stream=None):
     return dth
 
 
+# ---------------------------------------------------------------- delta rule
+def delta_scan_fwd(q, k, v, beta, S0=None, want_state=False, stream=None):
+    """DeltaNet's delta rule: S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T,
+    o_t = S_t q_t.  q, k, v [B,T,H,64], beta [B,T,H], S0 [B,H,64,64] or None.
+    Returns o (and the final state when want_state)."""
+    B, T, H, D = q.shape
+    _check(q, "q"); _check(k, "k", q.shape); _check(v, "v", q.shape); _check(beta, "beta", (B, T, H))
+    if S0 is not None:
+        _check(S0, "S0", (B, H, D, D))
+    o = torch.empty_like(q)
+    ST = torch.empty((B, H, D, D), dtype=torch.float32, device=q.device) if want_state else None
+    _b.mgs_delta_scan_fwd(q, k, v, beta, S0, o, ST, B, T, H, D, None, 0, stream)
+    return (o, ST) if want_state else o
+
+
 # ---------------------------------------------------------------- linear_scan
 def linear_scan_fwd(a, b, h0=None, stream=None):
     """h_t = a_t * h_{t-1} + b_t elementwise.  a, b [B,T,D], h0 [B,D] or None."""

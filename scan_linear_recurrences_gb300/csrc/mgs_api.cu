@@ -458,6 +458,39 @@ mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const 
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mgs_status mgs_delta_scan_fwd(const float *q, const float *k, const float *v, const float *beta,
+                              const float *S0, float *o, float *S_T, int64_t B, int64_t T, int64_t H,
+                              int D, void *workspace, size_t workspace_bytes, mgs_stream_t stream) {
+    if (B < 0 || T < 0 || H < 0 || D <= 0) return MGS_ERR_INVALID_ARG;
+    if (D != 64) return MGS_ERR_UNSUPPORTED;
+    int64_t nb, n, ns;
+    if (!mul_ok(B, T, &nb) || !mul_ok(nb, H, &nb) || !mul_ok(nb, D, &n) || !mul_ok(B, H, &ns) ||
+        !mul_ok(ns, int64_t(D) * D, &ns))
+        return MGS_ERR_INVALID_ARG;
+    if (n > INT64_MAX / 8 || ns > INT64_MAX / 8) return MGS_ERR_INVALID_ARG;
+    if (B * T > INT32_MAX || H > INT32_MAX) return MGS_ERR_UNSUPPORTED;  // 32-bit map coordinates
+    if (ns == 0) return MGS_OK;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    mgs_status st;
+    if (n == 0) {  // T = 0: the final state is the initial one
+        if (S_T == nullptr) return MGS_OK;
+        if ((st = check_ptrs({S_T}, {S0})) != MGS_OK) return st;
+        if (!disjoint({{S_T, ns}}, {{S0, S0 ? ns : 0}})) return MGS_ERR_INVALID_ARG;
+        return from_cuda(S0 ? cudaMemcpyAsync(S_T, S0, size_t(ns) * sizeof(float), cudaMemcpyDeviceToDevice, cs)
+                            : cudaMemsetAsync(S_T, 0, size_t(ns) * sizeof(float), cs));
+    }
+    if ((st = check_ptrs({q, k, v, o}, {S0, S_T})) != MGS_OK) return st;
+    if (beta == nullptr) return MGS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(beta) & 3u) != 0) return MGS_ERR_UNSUPPORTED;
+    if (!disjoint({{o, n}, {S_T, S_T ? ns : 0}},
+                  {{q, n}, {k, n}, {v, n}, {beta, nb}, {S0, S0 ? ns : 0}}))
+        return MGS_ERR_INVALID_ARG;
+    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_delta_fwd(q, k, v, beta, S0, o, S_T, B, T, H, ctl, cs));
+}
+
 mgs_status mgs_check(mgs_stream_t stream) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return MGS_ERR_CUDA;
     mgs::DevCtl ctl;

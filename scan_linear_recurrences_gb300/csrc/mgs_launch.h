@@ -57,6 +57,11 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
 cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
                            int64_t H, const DevCtl &ctl, cudaStream_t s);
 
+// delta rule forward (head dimension 64)
+cudaError_t launch_delta_fwd(const float *q, const float *k, const float *v, const float *beta, const float *S0,
+                             float *o, float *ST, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
+                             cudaStream_t s);
+
 // Encodes a tiled fp32 tensor map over `base` (rank 2 or 3).  dims and box are
 // innermost first; byte_strides has rank-1 entries (strides of dims 1..).
 cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,

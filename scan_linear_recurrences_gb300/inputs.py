@@ -32,6 +32,9 @@ memory stays bounded; within a block the draws are in the order listed):
   sigmoid(N(0,1))^k, n = N(0,1)^k, b = z * n, grad_h = N(0,1)^k.
 * Givens matrix scan: per block theta ~ U(-pi, pi)^{k(k-1)/2} (the angles
   of the matrix_scan recipe above), grad_P = N(0,1)^{k x k}.
+* delta rule (DeltaNet, behind DeltaMinGRU): S0 = N(0,1)^{DxD}/sqrt(D) drawn
+  first when requested; per block q ~ N(0,1)^D normalised, k likewise, v =
+  N(0,1)^D, beta = sigmoid(N(0,1)) per (b, t, head).
 * parallel_scan_log (minGRU gates): log_h0 = log g(N(0,1)) drawn first; then
   per block u ~ N(0,1), x ~ N(0,1), grad_h ~ N(0,1);
   log_coeffs = log(1 - sigmoid(u)) = -softplus(u),
@@ -193,6 +196,29 @@ def givens_matrix_inputs(B, T, H, k, seed, device="cpu"):
     return dict(theta=th, grad_P=gP)
 
 
+def delta_inputs(B, T, H, D, seed, device="cpu", with_S0=True):
+    """Delta-rule inputs (DeltaNet conventions): q, k = unit vectors (N(0,1)^D
+    normalised), v = N(0,1)^D, beta = sigmoid(N(0,1)); S0 = N(0,1)^{DxD}/sqrt(D)
+    drawn first when requested.  dict(q, k, v [B,T,H,D], beta [B,T,H], S0)."""
+    dev = torch.device(device)
+    g = _gen(seed, dev)
+    f64 = dict(dtype=torch.float64, device=dev)
+    S0 = (torch.randn((B, H, D, D), generator=g, **f64) / math.sqrt(D)).float() if with_S0 else None
+    q = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty_like(q)
+    beta = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    for t0 in range(0, T, TIME_BLOCK):
+        tb = min(TIME_BLOCK, T - t0)
+        qq = torch.randn((B, tb, H, D), generator=g, **f64)
+        kk = torch.randn((B, tb, H, D), generator=g, **f64)
+        q[:, t0:t0 + tb] = (qq / qq.norm(dim=-1, keepdim=True)).float()
+        k[:, t0:t0 + tb] = (kk / kk.norm(dim=-1, keepdim=True)).float()
+        v[:, t0:t0 + tb] = torch.randn((B, tb, H, D), generator=g, **f64).float()
+        beta[:, t0:t0 + tb] = torch.sigmoid(torch.randn((B, tb, H), generator=g, **f64)).float()
+    return dict(q=q, k=k, v=v, beta=beta, S0=S0)
+
+
 def psl_inputs(B, T, D, seed, device="cpu", with_h0=True):
     """parallel_scan_log inputs with the minGRU gate distribution:
     dict(log_coeffs, log_values [B,T,D], log_h0 [B,D] or None, grad_h [B,T,D])."""
@@ -237,7 +263,7 @@ def linear_inputs(B, T, D, seed, device="cpu", with_h0=True):
 class Workload:
     """One benchmarked shape."""
     cid: int
-    op: str          # "mas" | "ms" | "psl" | "lin" | "gas" | "gms"
+    op: str          # "mas" | "ms" | "psl" | "lin" | "gas" | "gms" | "delta"
     name: str
     B: int
     T: int
@@ -260,6 +286,8 @@ class Workload:
             return givens_affine_inputs(self.B, self.T, self.H, self.k, self.seed, device, h0=self.h0)
         if self.op == "gms":
             return givens_matrix_inputs(self.B, self.T, self.H, self.k, self.seed, device)
+        if self.op == "delta":
+            return delta_inputs(self.B, self.T, self.H, self.k, self.seed, device, with_S0=True)
         return psl_inputs(self.B, self.T, self.H, self.seed, device, with_h0=True)
 
 
@@ -284,4 +312,10 @@ EXTRA_WORKLOADS = {
     10: Workload(10, "gas", "givens_affine_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "normal"),
     11: Workload(11, "gms", "givens_matrix_scan lab B=128 T=64 H=8 k=8", 128, 64, 8, 8, "none"),
     12: Workload(12, "gms", "givens_matrix_scan long-T B=16 T=1024 H=8 k=8", 16, 1024, 8, 8, "none"),
+    # DeltaMinGRU's delta rule (forward only), head dimension 64 (k holds D):
+    # the pages' lab and long-T shapes with one head of d=64, and a throughput
+    # shape with enough (batch, head) lanes to fill the GPU
+    13: Workload(13, "delta", "delta_scan lab B=128 T=64 H=1 D=64", 128, 64, 1, 64, "normal"),
+    14: Workload(14, "delta", "delta_scan long-T B=16 T=1024 H=1 D=64", 16, 1024, 1, 64, "normal"),
+    15: Workload(15, "delta", "delta_scan scaled B=16 T=4096 H=16 D=64", 16, 4096, 16, 64, "normal"),
 }
