@@ -7,13 +7,17 @@
 // A chunk of C = 64 steps with state S on entry is, in matrix form (rows are
 // time steps, K, V, Q are C x D):
 //   A   = strict_tril(diag(beta) K K^T)
-//   (I + A) [W | U] = diag(beta) [K | V]       (forward substitution)
-//   U'  = U - W S^T
+//   (I + A) [W | U] = diag(beta) [K | V],   U' = U - W S^T
 //   O   = Q S^T + tril(Q K^T) U'
 //   S  <- S + U'^T K
 // which is the recurrence exactly (the WY representation of the product of
-// the chunk's rank-one updates).  The state is kept key-major (S^T) in shared
-// memory so that every product reads its operands by rows.
+// the chunk's rank-one updates).  Since (I + A) is the same for W and U, U'
+// is obtained from one solve, (I + A) U' = diag(beta) (V - K S^T), and W is
+// never formed.  The solve is blocked by 16 rows: the four 16 x 16 diagonal
+// blocks of (I + A) are inverted by forward substitution (one warp each), then
+// U'_b = D_b (R_b - A_{b,<b} U'_{<b}) block after block.  The state is kept
+// key-major (S^T) in shared memory so that every product reads its operands
+// by rows.
 //
 // One 256-thread block per lane walks its chunks in order; each chunk's Q, K
 // and V arrive by tiled TMA loads (a 68-float box over 64-float rows, so the
@@ -35,7 +39,9 @@ constexpr int kThreads = 256;
 constexpr int kStages = 2;
 
 // Shared memory layout (floats): stages [Q K V] x kStages, then ST, KT, A, QK,
-// W, U, beta (64), barriers.
+// D (the inverted diagonal blocks, rows 16b..16b+15, columns 0..15), U (R,
+// then U' in place; also the 16-row panel of the blocked solve), beta (64),
+// barriers.
 struct DeltaSmem {
     static constexpr int stage = 3 * MATF;
     static constexpr int st = kStages * stage;
@@ -79,12 +85,14 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 // acc[nt] += op(A)[m0.., :] B[:, n0 + 8 nt ..] over k = 0..63 for one warp's
 // 16 x (8 NT) block of the result.  AT = false: A row-major [m][k];
 // AT = true: A stored [k][m].  B row-major [k][n].  Stride LD.
+// Only k < kend and n-tiles nt < ntl take part (the zero triangles of the
+// masked products are skipped; both limits are warp-uniform).
 template <bool AT, int NT>
 __device__ __forceinline__ void mma64(const float *__restrict__ A, const float *__restrict__ B, float (&acc)[NT][4],
-                                      int m0, int n0, int lane) {
+                                      int m0, int n0, int lane, int kend = DD, int ntl = NT) {
     const int g = lane >> 2, q = lane & 3;
 #pragma unroll 2
-    for (int k0 = 0; k0 < DD; k0 += 8) {
+    for (int k0 = 0; k0 < kend; k0 += 8) {
         float av[4];
         if constexpr (AT) {
             av[0] = A[(k0 + q) * LD + m0 + g];
@@ -102,6 +110,7 @@ __device__ __forceinline__ void mma64(const float *__restrict__ A, const float *
         for (int i = 0; i < 4; ++i) split_tf32(av[i], ab[i], as[i]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
+            if (nt >= ntl) break;
             const int n = n0 + 8 * nt + g;
             uint32_t bb[2], bs[2];
             split_tf32(B[(k0 + q) * LD + n], bb[0], bs[0]);
@@ -145,12 +154,13 @@ __global__ void __launch_bounds__(kThreads)
     using L = DeltaSmem;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *sm = reinterpret_cast<float *>(smem_raw);
-    float *ST = sm + L::st, *KT = sm + L::kt, *Am = sm + L::a, *QK = sm + L::qk, *W = sm + L::w, *U = sm + L::u;
+    float *ST = sm + L::st, *KT = sm + L::kt, *Am = sm + L::a, *QK = sm + L::qk, *U = sm + L::u;
+    float *Wd = sm + L::w;           // inverted diagonal blocks D_b
+    float *Pn = KT;                  // 16-row panel of the blocked solve (KT is free by then)
     float *sb = sm + L::beta;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::bars);
     int *abort_word = reinterpret_cast<int *>(bars + kStages);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int m0 = 16 * (warp >> 1), n0 = 32 * (warp & 1);  // this warp's 16 x 32 block of a product
     const int64_t lane_id = blockIdx.x;  // (batch, head)
     if (lane_id >= B * H) return;
     const int64_t bi = lane_id / H, hd = lane_id % H;
@@ -229,105 +239,131 @@ __global__ void __launch_bounds__(kThreads)
             KT[j * LD + t] = K[t * LD + j];
         }
         __syncthreads();
-        // A = strict_tril(diag(beta) K K^T)
+        // Phase 1.  Warps 0-3 (rows 16w..): A = strict_tril(diag(beta) K K^T)
+        // and R = diag(beta) (V - K S^T).  Warps 4-7 (rows 16(w-4)..):
+        // QK = tril(Q K^T) and Q S^T, the latter kept in registers as the
+        // start of O.
+        const bool lo = warp < 4;
+        const int mr = 16 * (warp & 3);  // this warp's 16 rows in phases 1 and 4
+        float oacc[8][4];                // warps 4-7: Q S^T, then O; warps 0-3: K^T U'
+        zero_frag(oacc);
         {
-            float acc[4][4];
-            zero_frag(acc);
-            mma64<false>(K, KT, acc, m0, n0, lane);
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = frag_row(m0, lane, e), s2 = frag_col(n0, lane, nt, e);
-                    acc[nt][e] = (s2 < t) ? sb[t] * acc[nt][e] : 0.f;
-                }
-            store_frag(Am, acc, m0, n0, lane);
-        }
-        __syncthreads();
-        if (tid < 2 * DD) {
-            // forward substitution, one column of [W | U] per thread, the
-            // column held in registers (fully unrolled, so every index is a
-            // constant): X[t] = beta_t Y[t] - sum_{s<t} A[t][s] X[s]
-            const int col = tid & 63;
-            const float *Y = tid < DD ? K : V;
-            float *X = tid < DD ? W : U;
-            float xr[CH];
-#pragma unroll
-            for (int t = 0; t < CH; ++t) {
-                float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-                const float *ar = Am + t * LD;
-#pragma unroll
-                for (int s4 = 0; s4 + 4 <= t; s4 += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(ar + s4);
-                    p0 = fmaf(a4.x, xr[s4 + 0], p0);
-                    p1 = fmaf(a4.y, xr[s4 + 1], p1);
-                    p2 = fmaf(a4.z, xr[s4 + 2], p2);
-                    p3 = fmaf(a4.w, xr[s4 + 3], p3);
-                }
-#pragma unroll
-                for (int s1 = t & ~3; s1 < t; ++s1) p0 = fmaf(ar[s1], xr[s1], p0);
-                xr[t] = fmaf(sb[t], Y[t * LD + col], -((p0 + p1) + (p2 + p3)));
-                X[t * LD + col] = xr[t];
-            }
-        } else {
-            // meanwhile: QK = tril(Q K^T), by the other four warps (16 rows each)
-            const int mq = 16 * (warp - 4);
+            // the triangular products take rows 16w (warps 0-3) and 16(7-w)
+            // (warps 4-7), so that the two warps of each SM sub-partition
+            // (w and w+4) share out the same number of tiles
+            const int mt = lo ? mr : 48 - mr;
             float acc[8][4];
             zero_frag(acc);
-            mma64<false>(Q, KT, acc, mq, 0, lane);
+            // only columns up to the diagonal: n-tiles below mt/8 + 2
+            mma64<false>(lo ? K : Q, KT, acc, mt, 0, lane, DD, mt / 8 + 2);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (frag_col(0, lane, nt, e) > frag_row(mq, lane, e)) acc[nt][e] = 0.f;
-            store_frag(QK, acc, mq, 0, lane);
-        }
-        __syncthreads();
-        // U' = U - W S^T  (in place of U)
-        {
-            float acc[4][4];
-            zero_frag(acc);
-            mma64<false>(W, ST, acc, m0, n0, lane);
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float2 *p = reinterpret_cast<float2 *>(U + frag_row(m0, lane, 2 * h) * LD +
-                                                           frag_col(n0, lane, nt, 0));
-                    const float2 u = *p;
-                    *p = make_float2(u.x - acc[nt][2 * h], u.y - acc[nt][2 * h + 1]);
+                for (int e = 0; e < 4; ++e) {
+                    const int t = frag_row(mt, lane, e), s2 = frag_col(0, lane, nt, e);
+                    acc[nt][e] = lo ? ((s2 < t) ? sb[t] * acc[nt][e] : 0.f) : ((s2 <= t) ? acc[nt][e] : 0.f);
                 }
+            store_frag(lo ? Am : QK, acc, mt, 0, lane);
+            mma64<false>(lo ? K : Q, ST, oacc, mr, 0, lane);
+            if (lo) {
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = frag_row(mr, lane, 2 * h), i = frag_col(0, lane, nt, 0);
+                        const float2 v2 = *reinterpret_cast<const float2 *>(V + t * LD + i);
+                        *reinterpret_cast<float2 *>(U + t * LD + i) =
+                            make_float2(sb[t] * (v2.x - oacc[nt][2 * h]), sb[t] * (v2.y - oacc[nt][2 * h + 1]));
+                    }
+                zero_frag(oacc);
+            }
         }
         __syncthreads();
-        // O = Q S^T + tril(Q K^T) U'; new state contribution K^T U'
-        float dS[4][4];
-        {
-            float acc[4][4];
-            zero_frag(acc);
-            mma64<false>(Q, ST, acc, m0, n0, lane);
-            mma64<false>(QK, U, acc, m0, n0, lane);
+        // Phase 2.  D_b = (I + A_bb)^{-1}, b = warp (0-3), lane j < 16 builds
+        // column j by forward substitution.
+        if (warp < 4 && lane < 16) {
+            const int b0 = 16 * warp;
+            float dcol[16];
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int r = 0; r < 16; ++r) {
+                float acc = (r == lane) ? 1.f : 0.f;
+#pragma unroll
+                for (int q = 0; q < r; ++q) acc = fmaf(-Am[(b0 + r) * LD + b0 + q], dcol[q], acc);
+                dcol[r] = acc;
+                Wd[(b0 + r) * LD + lane] = acc;
+            }
+        }
+        __syncthreads();
+        // Phase 3.  Blocked solve, U' in place of R: for b = 0..3,
+        // P = R_b - A_{b,<b} U'_{<b};  U'_b = D_b P.  Thread: column tid % 64,
+        // rows 4 (tid / 64) .. +3 of the block.
+        {
+            const int col = tid & 63, r0 = 4 * (tid >> 6);
+            for (int b = 0; b < 4; ++b) {
+                const int b0 = 16 * b;
+                float p[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) p[r] = U[(b0 + r0 + r) * LD + col];
+                for (int s4 = 0; s4 < b0; s4 += 4) {
+                    const float u0 = U[(s4 + 0) * LD + col], u1 = U[(s4 + 1) * LD + col];
+                    const float u2 = U[(s4 + 2) * LD + col], u3 = U[(s4 + 3) * LD + col];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + (b0 + r0 + r) * LD + s4);
+                        p[r] = fmaf(-a4.x, u0, p[r]);
+                        p[r] = fmaf(-a4.y, u1, p[r]);
+                        p[r] = fmaf(-a4.z, u2, p[r]);
+                        p[r] = fmaf(-a4.w, u3, p[r]);
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) Pn[(r0 + r) * LD + col] = p[r];
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; q4 += 4) {
+                        const float4 d4 = *reinterpret_cast<const float4 *>(Wd + (b0 + r0 + r) * LD + q4);
+                        acc = fmaf(d4.x, Pn[(q4 + 0) * LD + col], acc);
+                        acc = fmaf(d4.y, Pn[(q4 + 1) * LD + col], acc);
+                        acc = fmaf(d4.z, Pn[(q4 + 2) * LD + col], acc);
+                        acc = fmaf(d4.w, Pn[(q4 + 3) * LD + col], acc);
+                    }
+                    U[(b0 + r0 + r) * LD + col] = acc;
+                }
+                __syncthreads();
+            }
+        }
+        // Phase 4.  Warps 4-7: O = Q S^T + tril(Q K^T) U' (k only up to the
+        // diagonal); warps 0-3: rows 16w.. of K^T U' (the state update).
+        if (lo) {
+            mma64<true>(K, U, oacc, mr, 0, lane);  // oacc[j][i] = sum_t K[t][j] U'[t][i]
+        } else {
+            mma64<false>(QK, U, oacc, mr, 0, lane, mr + 16);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int t = frag_row(m0, lane, 2 * h);
+                    const int t = frag_row(mr, lane, 2 * h);
                     if (t < n)
                         *reinterpret_cast<float2 *>(o + ((bi * T + c * CH + t) * H + hd) * DD +
-                                                    frag_col(n0, lane, nt, 0)) =
-                            make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+                                                    frag_col(0, lane, nt, 0)) =
+                            make_float2(oacc[nt][2 * h], oacc[nt][2 * h + 1]);
                 }
-            zero_frag(dS);
-            mma64<true>(K, U, dS, m0, n0, lane);  // dS[j][i] = sum_t K[t][j] U'[t][i]
         }
         __syncthreads();  // every read of ST and of this stage is done
+        if (lo) {
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float2 *p = reinterpret_cast<float2 *>(ST + frag_row(m0, lane, 2 * h) * LD + frag_col(n0, lane, nt, 0));
-                const float2 v = *p;
-                *p = make_float2(v.x + dS[nt][2 * h], v.y + dS[nt][2 * h + 1]);
-            }
+                for (int h = 0; h < 2; ++h) {
+                    float2 *pp =
+                        reinterpret_cast<float2 *>(ST + frag_row(mr, lane, 2 * h) * LD + frag_col(0, lane, nt, 0));
+                    const float2 v = *pp;
+                    *pp = make_float2(v.x + oacc[nt][2 * h], v.y + oacc[nt][2 * h + 1]);
+                }
+        }
         if (c + kStages < nch) {
             if (tid == 0) {
                 fence_proxy_async_smem();
