@@ -324,8 +324,12 @@ class Runner:
         elif w.op == "gas":
             self.h = e(B, T, H, k)
             self.dth, self.da, self.db, self.dh0 = e(B, T, H, k * (k - 1) // 2), e(B, T, H, k), e(B, T, H, k), e(B, H, k)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_GIVENS_AFFINE_SCAN_FWD, B, T, H, k, device)
+            self.ws_b, self.nb = api.workspace(b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, B, T, H, k, device)
         elif w.op == "gms":
             self.P, self.dth = e(B, T, H, k, k), e(B, T, H, k * (k - 1) // 2)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_GIVENS_MATRIX_SCAN_FWD, B, T, H, k, device)
+            self.ws_b, self.nb = api.workspace(b.MGS_OP_GIVENS_MATRIX_SCAN_BWD, B, T, H, k, device)
         elif w.op == "delta":
             self.o, self.ST = e(B, T, H, k), e(B, H, k, k)
         else:
@@ -356,9 +360,9 @@ class Runner:
             b.mgs_matrix_scan_fwd(d["A"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
         elif w.op == "gas":
             b.mgs_givens_affine_scan_fwd(d["theta"], d["a"], d["b"], d["h0"], self.h, w.B, w.T, w.H, w.k,
-                                         None, 0, stream)
+                                         self.ws_f, self.nf, stream)
         elif w.op == "gms":
-            b.mgs_givens_matrix_scan_fwd(d["theta"], self.P, w.B, w.T, w.H, w.k, None, 0, stream)
+            b.mgs_givens_matrix_scan_fwd(d["theta"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
         elif w.op == "delta":
             b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], self.o, self.ST, w.B, w.T, w.H, w.k,
                                  None, 0, stream)
@@ -378,10 +382,10 @@ class Runner:
             b.mgs_matrix_scan_bwd(d["A"], self.P, d["grad_P"], self.dA, w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
         elif w.op == "gas":
             b.mgs_givens_affine_scan_bwd(d["theta"], d["a"], d["h0"], self.h, d["grad_h"], self.dth, self.da,
-                                         self.db, self.dh0, w.B, w.T, w.H, w.k, None, 0, stream)
+                                         self.db, self.dh0, w.B, w.T, w.H, w.k, self.ws_b, self.nb, stream)
         elif w.op == "gms":
-            b.mgs_givens_matrix_scan_bwd(d["theta"], self.P, d["grad_P"], self.dth, w.B, w.T, w.H, w.k, None, 0,
-                                         stream)
+            b.mgs_givens_matrix_scan_bwd(d["theta"], self.P, d["grad_P"], self.dth, w.B, w.T, w.H, w.k, self.ws_b,
+                                         self.nb, stream)
         elif w.op == "delta":
             pass  # forward only (the pages' DeltaMinGRU row is its chunked-WY forward)
         else:

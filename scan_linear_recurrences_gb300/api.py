@@ -129,7 +129,8 @@ def givens_affine_scan_fwd(theta, a, b, h0=None, stream=None):
     if h0 is not None:
         _check(h0, "h0", (B, H, k))
     h = torch.empty_like(b)
-    _b.mgs_givens_affine_scan_fwd(theta, a, b, h0, h, B, T, H, k, None, 0, stream)
+    ws, nws = workspace(_b.MGS_OP_GIVENS_AFFINE_SCAN_FWD, B, T, H, k, b.device)
+    _b.mgs_givens_affine_scan_fwd(theta, a, b, h0, h, B, T, H, k, ws, nws, stream)
     return h
 
 
@@ -145,7 +146,8 @@ def givens_affine_scan_bwd(theta, a, h0, h, grad_h, need_dh0=True, stream=None):
     da = torch.empty_like(a) if a is not None else None
     db = torch.empty_like(h)
     dh0 = torch.empty((B, H, k), dtype=torch.float32, device=h.device) if need_dh0 else None
-    _b.mgs_givens_affine_scan_bwd(theta, a, h0, h, grad_h, dth, da, db, dh0, B, T, H, k, None, 0, stream)
+    ws, nws = workspace(_b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, B, T, H, k, h.device)
+    _b.mgs_givens_affine_scan_bwd(theta, a, h0, h, grad_h, dth, da, db, dh0, B, T, H, k, ws, nws, stream)
     return dth, da, db, dh0
 
 
@@ -154,7 +156,8 @@ def givens_matrix_scan_fwd(theta, k=GIVENS_K, stream=None):
     B, T, H, n = theta.shape
     _check(theta, "theta", (B, T, H, k * (k - 1) // 2))
     P = torch.empty((B, T, H, k, k), dtype=torch.float32, device=theta.device)
-    _b.mgs_givens_matrix_scan_fwd(theta, P, B, T, H, k, None, 0, stream)
+    ws, nws = workspace(_b.MGS_OP_GIVENS_MATRIX_SCAN_FWD, B, T, H, k, theta.device)
+    _b.mgs_givens_matrix_scan_fwd(theta, P, B, T, H, k, ws, nws, stream)
     return P
 
 
@@ -162,7 +165,8 @@ def givens_matrix_scan_bwd(theta, P, grad_P, stream=None):
     B, T, H, k, _ = P.shape
     _check(theta, "theta", (B, T, H, k * (k - 1) // 2)); _check(P, "P"); _check(grad_P, "grad_P", P.shape)
     dth = torch.empty_like(theta)
-    _b.mgs_givens_matrix_scan_bwd(theta, P, grad_P, dth, B, T, H, k, None, 0, stream)
+    ws, nws = workspace(_b.MGS_OP_GIVENS_MATRIX_SCAN_BWD, B, T, H, k, theta.device)
+    _b.mgs_givens_matrix_scan_bwd(theta, P, grad_P, dth, B, T, H, k, ws, nws, stream)
     return dth
 
 

@@ -203,6 +203,14 @@ size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
         case MGS_OP_MATRIX_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
             return mgs::ms_workspace_bytes(B, T, H_or_D, k, op == MGS_OP_MATRIX_SCAN_BWD);
+        case MGS_OP_GIVENS_AFFINE_SCAN_FWD:
+        case MGS_OP_GIVENS_AFFINE_SCAN_BWD:
+        case MGS_OP_GIVENS_MATRIX_SCAN_FWD:
+        case MGS_OP_GIVENS_MATRIX_SCAN_BWD: {
+            GivensSizes gs;
+            if (givens_sizes(B, T, H_or_D, k, &gs) != MGS_OK || gs.vec == 0) return 0;
+            return mgs::givens_workspace_bytes(op - MGS_OP_GIVENS_AFFINE_SCAN_FWD, B, T, H_or_D);
+        }
         case MGS_OP_PARALLEL_SCAN_LOG_BWD: {
             int64_t n, n0;
             if (psl_sizes(B, T, H_or_D, &n, &n0) != MGS_OK || n == 0) return 0;
@@ -396,10 +404,11 @@ mgs_status mgs_givens_affine_scan_fwd(const float *theta, const float *a, const 
     if ((st = check_ptrs({theta, b, h}, {a, h0})) != MGS_OK) return st;
     if (!disjoint({{h, s.vec}}, {{theta, s.ang}, {a, a ? s.vec : 0}, {b, s.vec}, {h0, h0 ? s.init : 0}}))
         return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::givens_workspace_bytes(0, B, T, H), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_gas_fwd(theta, a, b, h0, h, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(mgs::launch_gas_fwd(theta, a, b, h0, h, B, T, H, workspace, workspace_bytes, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_givens_affine_scan_bwd(const float *theta, const float *a, const float *h0,
@@ -421,10 +430,11 @@ mgs_status mgs_givens_affine_scan_bwd(const float *theta, const float *a, const 
     if (!disjoint({{d_theta, s.ang}, {da, da ? s.vec : 0}, {db, s.vec}, {dh0, dh0 ? s.init : 0}},
                   {{theta, s.ang}, {a, a ? s.vec : 0}, {h0, h0 ? s.init : 0}, {h, s.vec}, {grad_h, s.vec}}))
         return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::givens_workspace_bytes(1, B, T, H), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_gas_bwd(theta, a, h0, h, grad_h, d_theta, da, db, dh0, B, T, H, ctl, cs));
+    return from_cuda(mgs::launch_gas_bwd(theta, a, h0, h, grad_h, d_theta, da, db, dh0, B, T, H, workspace,
+                                         workspace_bytes, ctl, cs));
 }
 
 mgs_status mgs_givens_matrix_scan_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H,
@@ -436,10 +446,11 @@ mgs_status mgs_givens_matrix_scan_fwd(const float *theta, float *P, int64_t B, i
     if (s.mat == 0) return MGS_OK;
     if ((st = check_ptrs({theta, P}, {})) != MGS_OK) return st;
     if (!disjoint({{P, s.mat}}, {{theta, s.ang}})) return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::givens_workspace_bytes(2, B, T, H), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_gms_fwd(theta, P, B, T, H, ctl, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(mgs::launch_gms_fwd(theta, P, B, T, H, workspace, workspace_bytes, ctl,
+                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const float *grad_P,
@@ -451,10 +462,10 @@ mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const 
     if (s.mat == 0) return MGS_OK;
     if ((st = check_ptrs({theta, P, grad_P, d_theta}, {})) != MGS_OK) return st;
     if (!disjoint({{d_theta, s.ang}}, {{theta, s.ang}, {P, s.mat}, {grad_P, s.mat}})) return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    if ((st = check_ws(mgs::givens_workspace_bytes(3, B, T, H), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_gms_bwd(theta, P, grad_P, d_theta, B, T, H, ctl,
+    return from_cuda(mgs::launch_gms_bwd(theta, P, grad_P, d_theta, B, T, H, workspace, workspace_bytes, ctl,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -678,6 +678,156 @@ __global__ void __launch_bounds__(kBlock)
     }
 }
 
+// ---------------------------------------------------------------- few lanes, long sequences
+// With few (batch, head) lanes and a long sequence, each lane of the kernels
+// above walks a long serial chain on one thread.  There the library instead
+// materialises A_t = G(theta_t) diag(a_t) in the caller's workspace (one
+// thread per step, fully parallel), runs the time-chunked matrix kernels on it,
+// and turns their output back into angle gradients (again one thread per step).
+
+// A_t = G(theta_t) diag(a_t) (a NULL: G(theta_t)), row-major 8 x 8 per step.
+__global__ void __launch_bounds__(128)
+    givens_materialise_kernel(const float *__restrict__ theta, const float *__restrict__ a, float *__restrict__ A,
+                              int64_t steps) {
+    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (st >= steps) return;
+    float cs[GN], sv[GN];
+#pragma unroll
+    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
+    float av[GK];
+    if (a != nullptr) {
+        lds_vec<GK>(a + st * GK, av);
+    } else {
+#pragma unroll
+        for (int i = 0; i < GK; ++i) av[i] = 1.f;
+    }
+    float m[GK][GK];  // m[j] = column j
+#pragma unroll
+    for (int j = 0; j < GK; ++j) {
+#pragma unroll
+        for (int i = 0; i < GK; ++i) m[j][i] = (i == j) ? av[j] : 0.f;
+        mesh_apply(m[j], cs, sv);
+    }
+    float *out = A + st * (GK * GK);
+#pragma unroll
+    for (int i = 0; i < GK; ++i) {
+        float row[GK];
+#pragma unroll
+        for (int j = 0; j < GK; ++j) row[j] = m[j][i];
+        stg_vec_cs<GK>(out + i * GK, row);
+    }
+}
+
+// Angle (and gate) gradients of the affine scan from lambda_t (= db_t) and
+// h_{t-1}: the per-step body of gas_bwd_kernel without the carry.
+__global__ void __launch_bounds__(128)
+    gas_grad_kernel(const float *__restrict__ theta, const float *__restrict__ a, const float *__restrict__ lam_in,
+                    const float *__restrict__ h, const float *__restrict__ h0, float *__restrict__ dth,
+                    float *__restrict__ da, int64_t B, int64_t T, int64_t H) {
+    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;  // (b, t, head)
+    if (st >= B * T * H) return;
+    const int64_t hd = st % H, t = (st / H) % T, bi = st / (H * T);
+    float cs[GN], sv[GN];
+#pragma unroll
+    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
+    float lam[GK], hp[GK], av[GK];
+    lds_vec<GK>(lam_in + st * GK, lam);
+    if (t >= 1) {
+        lds_vec<GK>(h + (st - H) * GK, hp);
+    } else if (h0 != nullptr) {
+        lds_vec<GK>(h0 + (bi * H + hd) * GK, hp);
+    } else {
+#pragma unroll
+        for (int i = 0; i < GK; ++i) hp[i] = 0.f;
+    }
+    if (a != nullptr) {
+        lds_vec<GK>(a + st * GK, av);
+    } else {
+#pragma unroll
+        for (int i = 0; i < GK; ++i) av[i] = 1.f;
+    }
+    float xl[GK][GK];
+#pragma unroll
+    for (int i = 0; i < GK; ++i) xl[0][i] = av[i] * hp[i];
+#pragma unroll
+    for (int l = 0; l < GK; ++l) {
+        if (l > 0) {
+#pragma unroll
+            for (int i = 0; i < GK; ++i) xl[l][i] = xl[l - 1][i];
+        }
+#pragma unroll
+        for (int q = 0; q < layer_pairs(l); ++q) {
+            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+            rot_fwd(xl[l][p], xl[l][p + 1], cs[n], sv[n]);
+        }
+    }
+    float dthv[GN];
+#pragma unroll
+    for (int l = GK - 1; l >= 0; --l) {
+#pragma unroll
+        for (int q = 0; q < layer_pairs(l); ++q) {
+            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+            dthv[n] = fmaf(lam[p + 1], xl[l][p], -lam[p] * xl[l][p + 1]);
+            rot_bwd(lam[p], lam[p + 1], cs[n], sv[n]);
+        }
+    }
+    stg_vec_cs<GN>(dth + st * GN, dthv);
+    if (da != nullptr) {
+        float dav[GK];
+#pragma unroll
+        for (int i = 0; i < GK; ++i) dav[i] = lam[i] * hp[i];
+        stg_vec_cs<GK>(da + st * GK, dav);
+    }
+}
+
+// Angle gradients of the matrix scan from dA_t: d theta_n = <dA_t, dG/dtheta_n>
+// = sum_j mu_j^T (dG/dtheta_n) e_j, one column j at a time: e_j forward
+// through the layers (each layer's output kept), dA_t[:, j] back through them.
+__global__ void __launch_bounds__(128)
+    gms_grad_kernel(const float *__restrict__ theta, const float *__restrict__ dA, float *__restrict__ dth,
+                    int64_t steps) {
+    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (st >= steps) return;
+    float cs[GN], sv[GN];
+#pragma unroll
+    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
+    float dthv[GN];
+#pragma unroll
+    for (int n = 0; n < GN; ++n) dthv[n] = 0.f;
+    const float *g = dA + st * (GK * GK);
+#pragma unroll 1
+    for (int j = 0; j < GK; ++j) {
+        float xl[GK][GK], mu[GK];
+#pragma unroll
+        for (int i = 0; i < GK; ++i) {
+            xl[0][i] = (i == j) ? 1.f : 0.f;
+            mu[i] = g[i * GK + j];
+        }
+#pragma unroll
+        for (int l = 0; l < GK; ++l) {
+            if (l > 0) {
+#pragma unroll
+                for (int i = 0; i < GK; ++i) xl[l][i] = xl[l - 1][i];
+            }
+#pragma unroll
+            for (int q = 0; q < layer_pairs(l); ++q) {
+                const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+                rot_fwd(xl[l][p], xl[l][p + 1], cs[n], sv[n]);
+            }
+        }
+#pragma unroll
+        for (int l = GK - 1; l >= 0; --l) {
+#pragma unroll
+            for (int q = 0; q < layer_pairs(l); ++q) {
+                const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+                dthv[n] = fmaf(mu[p + 1], xl[l][p], fmaf(-mu[p], xl[l][p + 1], dthv[n]));
+                rot_bwd(mu[p], mu[p + 1], cs[n], sv[n]);
+            }
+        }
+    }
+    stg_vec_cs<GN>(dth + st * GN, dthv);
+}
+
 // Lanes per recurrence warp for the affine scan: as many as keep at least
 // one block per SM, at most kGasMaxLanes (beyond that the angle warps, which
 // convert 28 angles per lane and step, fall behind the recurrence), and no
@@ -692,10 +842,37 @@ int gas_lanes_per_block(int64_t B, int64_t H) {
     return lpw;
 }
 
+// The few-lane path is taken when the matrix kernels would split T into
+// chunks (fewer than 256 groups of 4 lanes) and T is at least 256.
+bool few_lane_path(int64_t B, int64_t T, int64_t H) { return T >= 256 && mas_workspace_bytes(B, T, H, GK) > 0; }
+
+size_t mat_bytes(int64_t B, int64_t T, int64_t H) { return align_up(size_t(B * T * H) * GK * GK * 4, 256); }
+
+inline unsigned grid_for(int64_t n, int block) { return unsigned((n + block - 1) / block); }
+
 }  // namespace
 
+size_t givens_workspace_bytes(int op, int64_t B, int64_t T, int64_t H) {
+    if (!few_lane_path(B, T, H)) return 0;
+    switch (op) {
+        case 0: return mat_bytes(B, T, H) + mas_workspace_bytes(B, T, H, GK);             // affine fwd
+        case 1: return 2 * mat_bytes(B, T, H) + mas_workspace_bytes(B, T, H, GK);         // affine bwd
+        case 2: return mat_bytes(B, T, H) + ms_workspace_bytes(B, T, H, GK, false);       // matrix fwd
+        default: return 2 * mat_bytes(B, T, H) + ms_workspace_bytes(B, T, H, GK, true);   // matrix bwd
+    }
+}
+
 cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, const float *h0, float *h,
-                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
+                           int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl,
+                           cudaStream_t s) {
+    if (few_lane_path(B, T, H)) {
+        float *A = static_cast<float *>(ws);
+        const size_t mb = mat_bytes(B, T, H);
+        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, A, B * T * H);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_mas_fwd(GK, A, b, h0, h, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
+    }
     const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
     CUtensorMap tTh, tA, tB;
@@ -718,7 +895,23 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
 
 cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, const float *h, const float *gh,
                            float *dth, float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t H,
-                           const DevCtl &ctl, cudaStream_t s) {
+                           void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
+    if (few_lane_path(B, T, H)) {
+        // lambda_t = db_t and dh0 come from the time-chunked matrix_affine_scan
+        // backward (dA goes to the workspace, unused); the angle and gate
+        // gradients then follow per step from lambda_t and h_{t-1}
+        float *A = static_cast<float *>(ws);
+        const size_t mb = mat_bytes(B, T, H);
+        float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
+        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, A, B * T * H);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if ((e = launch_mas_bwd(GK, A, h0, h, gh, dA, db, dh0, B, T, H, static_cast<char *>(ws) + 2 * mb,
+                                ws_bytes - 2 * mb, ctl, s)) != cudaSuccess)
+            return e;
+        gas_grad_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, db, h, h0, dth, da, B, T, H);
+        return cudaGetLastError();
+    }
     const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
     CUtensorMap tTh, tA, tG, tH;
@@ -740,8 +933,16 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
-                           cudaStream_t s) {
+cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, void *ws,
+                           size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
+    if (few_lane_path(B, T, H)) {
+        float *A = static_cast<float *>(ws);
+        const size_t mb = mat_bytes(B, T, H);
+        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, nullptr, A, B * T * H);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_ms_fwd(GK, A, P, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
+    }
     CUtensorMap tTh;
     cudaError_t e;
     if ((e = make_head_map(&tTh, theta, B * T, H, GN, kGmsLanes, kGmsFwdTS)) != cudaSuccess) return e;
@@ -755,7 +956,20 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
 }
 
 cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
-                           int64_t H, const DevCtl &ctl, cudaStream_t s) {
+                           int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
+    if (few_lane_path(B, T, H)) {
+        float *A = static_cast<float *>(ws);
+        const size_t mb = mat_bytes(B, T, H);
+        float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
+        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, nullptr, A, B * T * H);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if ((e = launch_ms_bwd(GK, A, P, G, dA, B, T, H, static_cast<char *>(ws) + 2 * mb, ws_bytes - 2 * mb, ctl,
+                               s)) != cudaSuccess)
+            return e;
+        gms_grad_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, dA, dth, B * T * H);
+        return cudaGetLastError();
+    }
     using TM = MatTile<GK, true>;
     CUtensorMap tTh, tP, tG;
     cudaError_t e;

@@ -46,16 +46,19 @@ cudaError_t launch_psl_bwd(const float *lc, const float *lv, const float *lh0, c
                            const float *gh, float *dlc, float *dlv, float *dlh0, int64_t B,
                            int64_t T, int64_t D, const DevCtl &ctl, cudaStream_t s);
 
-// Givens-mesh affine and matrix scans (k = 8)
+// Givens-mesh affine and matrix scans (k = 8).  op: 0 affine fwd, 1 affine
+// bwd, 2 matrix fwd, 3 matrix bwd; nonzero only for few lanes and long T.
+size_t givens_workspace_bytes(int op, int64_t B, int64_t T, int64_t H);
 cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, const float *h0, float *h,
-                           int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s);
+                           int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl,
+                           cudaStream_t s);
 cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, const float *h, const float *gh,
                            float *dth, float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t H,
-                           const DevCtl &ctl, cudaStream_t s);
-cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
-                           cudaStream_t s);
+                           void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
+cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, void *ws,
+                           size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
 cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
-                           int64_t H, const DevCtl &ctl, cudaStream_t s);
+                           int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
 
 // delta rule forward (head dimension 64)
 cudaError_t launch_delta_fwd(const float *q, const float *k, const float *v, const float *beta, const float *S0,

@@ -138,3 +138,18 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         b.lib()
+
+
+def test_givens_workspace_only_for_few_lanes_and_long_T(L):
+    for op in (b.MGS_OP_GIVENS_AFFINE_SCAN_FWD, b.MGS_OP_GIVENS_AFFINE_SCAN_BWD,
+               b.MGS_OP_GIVENS_MATRIX_SCAN_FWD, b.MGS_OP_GIVENS_MATRIX_SCAN_BWD):
+        assert b.mgs_workspace_size(op, 128, 64, 8, 8) == 0      # lab shape: angle-fused kernels
+        assert b.mgs_workspace_size(op, 64, 1024, 64, 8) == 0    # many lanes
+        assert b.mgs_workspace_size(op, 16, 128, 8, 8) == 0      # T < 256
+        assert b.mgs_workspace_size(op, 16, 1024, 8, 4) == 0     # k != 8: the call reports it
+        n = b.mgs_workspace_size(op, 16, 1024, 8, 8)              # long-T shape: A formed in the workspace
+        assert n >= 16 * 1024 * 8 * 256
+    steps = 16 * 1024 * 8
+    assert b.mgs_workspace_size(b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, 16, 1024, 8, 8) >= 2 * steps * 256
+    th, bb, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    assert _st(b.mgs_givens_affine_scan_fwd, th, None, bb, None, h, 16, 1024, 8, 8) == b.MGS_ERR_WORKSPACE

@@ -72,6 +72,15 @@ def test_givens_affine_scan(B, T, H, h0, with_a):
     _run_gas(B, T, H, seed=900 + B * T + H, h0=h0, with_a=with_a)
 
 
+@pytest.mark.parametrize("B,T,H,h0,with_a", [
+    (2, 300, 3, "normal", True),      # few lanes, long T: A formed in the workspace, time-chunked
+    (1, 517, 4, "none", False),       # ragged chunks, no gate, zero initial state
+    (40, 300, 64, "normal", True),    # many lanes, long T: angle-fused kernels
+])
+def test_givens_affine_scan_long_sequences(B, T, H, h0, with_a):
+    _run_gas(B, T, H, seed=980 + B * T + H, h0=h0, with_a=with_a, rows=[0, B - 1])
+
+
 def test_givens_affine_scan_long_T_shape():
     w = inputs.EXTRA_WORKLOADS[10]
     _run_gas(w.B, w.T, w.H, seed=w.seed, h0=w.h0, with_a=True, rows=[0, 7, w.B - 1])
@@ -91,6 +100,11 @@ def _run_gms(B, T, H, seed, rows=None):
 @pytest.mark.parametrize("B,T,H", [(1, 1, 1), (2, 50, 3), (3, 33, 9), (128, 64, 8), (2, 300, 4)])
 def test_givens_matrix_scan(B, T, H):
     _run_gms(B, T, H, seed=950 + B * T + H)
+
+
+@pytest.mark.parametrize("B,T,H", [(2, 300, 3), (1, 517, 5)])
+def test_givens_matrix_scan_few_lanes_long_T(B, T, H):
+    _run_gms(B, T, H, seed=990 + B * T + H)
 
 
 def test_givens_matrix_scan_long_T_shape():
