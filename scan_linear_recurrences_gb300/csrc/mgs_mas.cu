@@ -375,35 +375,40 @@ struct ChunkRing {
 // value is published, then applies the aggregates (M_p, c_p) of the chunks
 // between it and this one, nearest to it first: x <- M_p x + c_p.  Thread r
 // holds row element r; each step needs row r of M_p and x gathered across the
-// k-group.  The next chunk's row is loaded while the current one is applied.
+// k-group.  The rows of the next kFoldAhead aggregates are in flight while one
+// is applied (each is an L2 round trip, long against the k FMAs of a step).
 // Returns false (uniformly) on timeout.
+constexpr int kFoldAhead = 4;
+
 template <int K>
 __device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t c, int dir, int sub, int r,
                                 int gbase, int lane, const DevCtl &ctl, float &hin) {
     const int64_t ps = find_inclusive(w.flags + g * C, c, dir, C, lane, ctl);
     if (ps < 0) return false;
     float x = __ldcg(w.slot(2, g * C + ps) + sub * K + r);
-    int64_t p = ps - dir;
-    float mrow[K], cp = 0.f;
-    if (p != c) {
+    // aggregates p_k = ps - dir (k + 1), k = 0 .. cnt-1 (the last is next to c)
+    const int64_t cnt = (c - ps) * (-dir) - 1;
+    auto load = [&](int64_t k, float (&mrow)[K], float &cp) {
+        const int64_t p = ps - dir * (k + 1);
         lds_row_global<K>(w.slot(0, g * C + p) + sub * K * K + r * K, mrow);
         cp = __ldcg(w.slot(1, g * C + p) + sub * K + r);
-    }
-    while (p != c) {
-        const int64_t pn = p - dir;
-        float nrow[K], ncp = 0.f;
-        if (pn != c) {
-            lds_row_global<K>(w.slot(0, g * C + pn) + sub * K * K + r * K, nrow);
-            ncp = __ldcg(w.slot(1, g * C + pn) + sub * K + r);
+    };
+    float mq[kFoldAhead][K], cq[kFoldAhead];
+#pragma unroll
+    for (int d = 0; d < kFoldAhead; ++d)
+        if (d < cnt) load(d, mq[d], cq[d]);
+    for (int64_t k0 = 0; k0 < cnt; k0 += kFoldAhead) {
+#pragma unroll
+        for (int d = 0; d < kFoldAhead; ++d) {
+            const int64_t k = k0 + d;
+            if (k < cnt) {  // warp-uniform
+                float acc = cq[d];
+#pragma unroll
+                for (int m = 0; m < K; ++m) acc = fmaf(mq[d][m], __shfl_sync(0xffffffffu, x, gbase + m), acc);
+                x = acc;
+                if (k + kFoldAhead < cnt) load(k + kFoldAhead, mq[d], cq[d]);
+            }
         }
-        float acc = cp;
-#pragma unroll
-        for (int m = 0; m < K; ++m) acc = fmaf(mrow[m], __shfl_sync(0xffffffffu, x, gbase + m), acc);
-        x = acc;
-#pragma unroll
-        for (int m = 0; m < K; ++m) mrow[m] = nrow[m];
-        cp = ncp;
-        p = pn;
     }
     hin = x;
     return true;

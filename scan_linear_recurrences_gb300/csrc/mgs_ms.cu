@@ -296,48 +296,51 @@ struct MsChunkShape {
 // ... up to (not including) p_end: X <- M_p X (+ C_p when Cs is given), where
 // M_p = Ms[(item0 + p) * mf] and C_p likewise.  Thread i of the k-group keeps
 // row i of X; the rows go through the exchange buffer each step, and row i of
-// the next aggregate is loaded while the current one is applied.  Returns
-// column `col` of the result in out.
+// the next kFoldAhead aggregates is in flight while one is applied (each is an
+// L2 round trip, long against a step's k^2 FMAs).  Returns column `col` of the
+// result in out.
+constexpr int kFoldAhead = 4;
+
 template <int K>
 __device__ void fold_rows(const float *X0, const float *Ms, int64_t mf, int64_t item0, int64_t p_first,
                           int64_t p_end, int step, const float *Cs, float *xw, int col, float (&out)[K]) {
     const int i = col;  // this thread's row
     float xr[K];
     lds_row_global<K>(X0 + i * K, xr);
-    float mr[K], cr[K];
-    int64_t p = p_first;
-    if (p != p_end) {
+    const int64_t cnt = (p_end - p_first) / step;
+    float mq[kFoldAhead][K], cq[kFoldAhead][K];
+    auto load = [&](int64_t k, float (&mr)[K], float (&cr)[K]) {
+        const int64_t p = p_first + k * step;
         lds_row_global<K>(Ms + (item0 + p) * mf + i * K, mr);
         if (Cs) lds_row_global<K>(Cs + (item0 + p) * mf + i * K, cr);
-    }
-    while (p != p_end) {
-        const int64_t pn = p + step;
-        float mn[K], cn[K];
-        if (pn != p_end) {
-            lds_row_global<K>(Ms + (item0 + pn) * mf + i * K, mn);
-            if (Cs) lds_row_global<K>(Cs + (item0 + pn) * mf + i * K, cn);
+    };
+#pragma unroll
+    for (int d = 0; d < kFoldAhead; ++d)
+        if (d < cnt) load(d, mq[d], cq[d]);
+    for (int64_t k0 = 0; k0 < cnt; k0 += kFoldAhead) {
+#pragma unroll
+        for (int d = 0; d < kFoldAhead; ++d) {
+            const int64_t k = k0 + d;
+            if (k < cnt) {  // warp-uniform
+#pragma unroll
+                for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
+                __syncwarp();
+                float nr[K];
+#pragma unroll
+                for (int j = 0; j < K; ++j) nr[j] = Cs ? cq[d][j] : 0.f;
+#pragma unroll
+                for (int m = 0; m < K; ++m) {
+                    float xm[K];
+                    lds_row_smem<K>(xw + m * K, xm);
+#pragma unroll
+                    for (int j = 0; j < K; ++j) nr[j] = fmaf(mq[d][m], xm[j], nr[j]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < K; ++j) xr[j] = nr[j];
+                if (k + kFoldAhead < cnt) load(k + kFoldAhead, mq[d], cq[d]);
+            }
         }
-#pragma unroll
-        for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
-        __syncwarp();
-        float nr[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) nr[j] = Cs ? cr[j] : 0.f;
-#pragma unroll
-        for (int m = 0; m < K; ++m) {
-            float xm[K];
-            lds_row_smem<K>(xw + m * K, xm);
-#pragma unroll
-            for (int j = 0; j < K; ++j) nr[j] = fmaf(mr[m], xm[j], nr[j]);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            xr[j] = nr[j];
-            mr[j] = mn[j];
-            if (Cs) cr[j] = cn[j];
-        }
-        p = pn;
     }
     // rows -> column `col`
 #pragma unroll
