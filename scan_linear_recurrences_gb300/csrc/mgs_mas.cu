@@ -375,10 +375,12 @@ struct ChunkRing {
 // value is published, then applies the aggregates (M_p, c_p) of the chunks
 // between it and this one, nearest to it first: x <- M_p x + c_p.  Thread r
 // holds row element r; each step needs row r of M_p and x gathered across the
-// k-group.  The rows of the next kFoldAhead aggregates are in flight while one
+// k-group.  The rows of the next 8 aggregates are in flight while one
 // is applied (each is an L2 round trip, long against the k FMAs of a step).
 // Returns false (uniformly) on timeout.
-constexpr int kFoldAhead = 4;
+// (4 for k = 16, where 8 would not fit in registers)
+template <int K>
+constexpr int fold_ahead() { return K >= 16 ? 4 : 8; }
 
 template <int K>
 __device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t c, int dir, int sub, int r,
@@ -393,6 +395,7 @@ __device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t 
         lds_row_global<K>(w.slot(0, g * C + p) + sub * K * K + r * K, mrow);
         cp = __ldcg(w.slot(1, g * C + p) + sub * K + r);
     };
+    constexpr int kFoldAhead = fold_ahead<K>();
     float mq[kFoldAhead][K], cq[kFoldAhead];
 #pragma unroll
     for (int d = 0; d < kFoldAhead; ++d)

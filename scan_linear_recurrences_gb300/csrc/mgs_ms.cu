@@ -296,10 +296,12 @@ struct MsChunkShape {
 // ... up to (not including) p_end: X <- M_p X (+ C_p when Cs is given), where
 // M_p = Ms[(item0 + p) * mf] and C_p likewise.  Thread i of the k-group keeps
 // row i of X; the rows go through the exchange buffer each step, and row i of
-// the next kFoldAhead aggregates is in flight while one is applied (each is an
+// the next 8 aggregates is in flight while one is applied (each is an
 // L2 round trip, long against a step's k^2 FMAs).  Returns column `col` of the
 // result in out.
-constexpr int kFoldAhead = 4;
+// (4 for k = 16, where 8 would not fit in registers)
+template <int K>
+constexpr int fold_ahead() { return K >= 16 ? 4 : 8; }
 
 template <int K>
 __device__ void fold_rows(const float *X0, const float *Ms, int64_t mf, int64_t item0, int64_t p_first,
@@ -308,6 +310,7 @@ __device__ void fold_rows(const float *X0, const float *Ms, int64_t mf, int64_t 
     float xr[K];
     lds_row_global<K>(X0 + i * K, xr);
     const int64_t cnt = (p_end - p_first) / step;
+    constexpr int kFoldAhead = fold_ahead<K>();
     float mq[kFoldAhead][K], cq[kFoldAhead][K];
     auto load = [&](int64_t k, float (&mr)[K], float (&cr)[K]) {
         const int64_t p = p_first + k * step;
