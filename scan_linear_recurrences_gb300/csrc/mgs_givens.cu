@@ -124,9 +124,23 @@ __device__ __forceinline__ void unbiased_cos_sin(float theta, float &c, float &s
 // Angles [lo, hi) of a stage converted by the block's angle threads (pt = 0 ..
 // kProd-1): cosines in place, sines to sn; consecutive threads take
 // consecutive words.
+// Four angles per thread and round are independent chains, which the
+// scheduler interleaves (one chain alone is a long run of dependent ops).
 __device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi, int pt) {
-#pragma unroll 2
-    for (int i = lo + pt; i < hi; i += kProd) {
+    int i = lo + pt;
+    for (; i + 3 * kProd < hi; i += 4 * kProd) {
+        float x[4], c[4], s[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = th[i + q * kProd];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unbiased_cos_sin(x[q], c[q], s[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            th[i + q * kProd] = c[q];
+            sn[i + q * kProd] = s[q];
+        }
+    }
+    for (; i < hi; i += kProd) {
         float c, s;
         unbiased_cos_sin(th[i], c, s);
         th[i] = c;
