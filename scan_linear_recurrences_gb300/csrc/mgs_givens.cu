@@ -699,15 +699,48 @@ __global__ void __launch_bounds__(kBlock)
 // thread per step, fully parallel), runs the time-chunked matrix kernels on it,
 // and turns their output back into angle gradients (again one thread per step).
 
+// The materialising kernel takes kStepBlock consecutive steps per block.  Its
+// angles are staged through shared memory: one coalesced sweep of the
+// block's 28 x kStepBlock angles in, the conversion to cosines and sines spread
+// over all threads with consecutive threads on consecutive words, and each
+// thread then reads its step's 28 pairs back (a 112-byte stride: 8-thread
+// phases of 16-byte reads hit distinct banks).
+constexpr int kStepBlock = 128;
+
+__device__ __forceinline__ void stage_step_angles(const float *__restrict__ theta, int64_t s0, int nsteps,
+                                                  float *cs_sm, float *sn_sm) {
+    const int n = nsteps * GN;  // a multiple of 4; theta + s0 * GN is 16-byte aligned
+    const float4 *src = reinterpret_cast<const float4 *>(theta + s0 * GN);
+    for (int i = threadIdx.x; i < n / 4; i += blockDim.x) reinterpret_cast<float4 *>(cs_sm)[i] = __ldcs(src + i);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += 4 * blockDim.x) {
+        float c[4], sv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i + q * blockDim.x < n) unbiased_cos_sin(cs_sm[i + q * blockDim.x], c[q], sv[q]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (i + q * blockDim.x < n) {
+                cs_sm[i + q * blockDim.x] = c[q];
+                sn_sm[i + q * blockDim.x] = sv[q];
+            }
+    }
+    __syncthreads();
+}
+
 // A_t = G(theta_t) diag(a_t) (a NULL: G(theta_t)), row-major 8 x 8 per step.
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kStepBlock)
     givens_materialise_kernel(const float *__restrict__ theta, const float *__restrict__ a, float *__restrict__ A,
                               int64_t steps) {
-    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (st >= steps) return;
+    __shared__ __align__(16) float cs_sm[kStepBlock * GN], sn_sm[kStepBlock * GN];
+    const int64_t s0 = int64_t(blockIdx.x) * kStepBlock;
+    const int nsteps = int(min64(kStepBlock, steps - s0));
+    stage_step_angles(theta, s0, nsteps, cs_sm, sn_sm);
+    if (int(threadIdx.x) >= nsteps) return;
+    const int64_t st = s0 + threadIdx.x;
     float cs[GN], sv[GN];
-#pragma unroll
-    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
+    lds_vec<GN>(cs_sm + threadIdx.x * GN, cs);
+    lds_vec<GN>(sn_sm + threadIdx.x * GN, sv);
     float av[GK];
     if (a != nullptr) {
         lds_vec<GK>(a + st * GK, av);
@@ -882,7 +915,7 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     if (few_lane_path(B, T, H)) {
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, a, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_mas_fwd(GK, A, b, h0, h, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
@@ -917,7 +950,7 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
         float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, a, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if ((e = launch_mas_bwd(GK, A, h0, h, gh, dA, db, dh0, B, T, H, static_cast<char *>(ws) + 2 * mb,
@@ -952,7 +985,7 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
     if (few_lane_path(B, T, H)) {
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, nullptr, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, nullptr, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_ms_fwd(GK, A, P, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
@@ -975,7 +1008,7 @@ cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, f
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
         float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, nullptr, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, nullptr, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if ((e = launch_ms_bwd(GK, A, P, G, dA, B, T, H, static_cast<char *>(ws) + 2 * mb, ws_bytes - 2 * mb, ctl,
