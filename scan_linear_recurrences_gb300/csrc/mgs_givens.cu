@@ -841,8 +841,10 @@ __global__ void __launch_bounds__(128)
     float dthv[GN];
 #pragma unroll
     for (int n = 0; n < GN; ++n) dthv[n] = 0.f;
-    const float *g = dA + st * (GK * GK);
-#pragma unroll 1
+    // the step's whole dA (256 contiguous bytes) in sixteen 16-byte loads
+    float g[GK * GK];
+    lds_vec<GK * GK>(dA + st * (GK * GK), g);
+#pragma unroll
     for (int j = 0; j < GK; ++j) {
         float xl[GK][GK], mu[GK];
 #pragma unroll
