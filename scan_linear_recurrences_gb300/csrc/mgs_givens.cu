@@ -194,18 +194,21 @@ struct BlockRing {
 
 // Per-block shared memory of the affine scan: kNS stages of
 // [theta ts*lpw*GN][vector inputs nv x ts*lpw*GK], two sine buffers of
-// ts*lpw*GN floats, the barriers and the abort word.
+// ts*lpw*GN floats, in the backward two buffers of rotated pairs of
+// 2*ts*lpw*GN floats, the barriers and the abort word.
+// The backward adds two buffers of the rotated-state pairs (xp_f floats each).
 struct GasSmem {
-    int th_f, vec_f, stage_f, ring_f, sin_f;
-    __host__ __device__ GasSmem(int lpw, int ts, int nv) {
+    int th_f, vec_f, stage_f, ring_f, sin_f, xp_f;
+    __host__ __device__ GasSmem(int lpw, int ts, int nv, bool with_xp = false) {
         th_f = ts * lpw * GN;
         vec_f = ts * lpw * GK;
         stage_f = int(align_up(size_t(th_f + nv * vec_f), 32));
         ring_f = kNS * stage_f;
         sin_f = th_f;
+        xp_f = with_xp ? 2 * th_f : 0;
     }
     __host__ __device__ size_t bytes() const {
-        return size_t(ring_f + 2 * sin_f) * 4 + kNS * sizeof(uint64_t) + 16;
+        return size_t(ring_f + 2 * sin_f + 2 * xp_f) * 4 + kNS * sizeof(uint64_t) + 16;
     }
 };
 
@@ -314,11 +317,15 @@ __global__ void __launch_bounds__(kBlock)
 // ---------------------------------------------------------------- affine backward
 // Walks t downwards.  Per step and lane:
 //   lambda = g_t + carry,  db_t = lambda,
-//   x = a_t * h_{t-1} rotated layer by layer (each layer's output kept),
+//   x = a_t * h_{t-1} rotated layer by layer (each rotation's output pair kept),
 //   mu = lambda taken back through the layers (transposed rotations), giving
 //   every angle's gradient on the way,
 //   da_t = mu_0 * h_{t-1},  carry = a_t * mu_0 (= A_t^T lambda_t);
-// dh0 = the last carry.
+// dh0 = the last carry.  The forward pass through the layers depends only on
+// inputs (h_{t-1}, a_t, theta_t), not on the carry, so the angle warps run it
+// for the next stage together with its angle conversion and leave the 28
+// rotated pairs per step in shared memory; the recurrence warp's chain per
+// step is then only the transposed rotations of mu.
 __global__ void __launch_bounds__(kBlock)
     gas_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
@@ -327,14 +334,15 @@ __global__ void __launch_bounds__(kBlock)
                    int64_t groups_per_b, int lpw, int ts, int has_a, DevCtl ctl) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int nv = has_a ? 3 : 2;  // a, g, h_{t-1}
-    const GasSmem L(lpw, ts, nv);
+    const GasSmem L(lpw, ts, nv, true);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *snb = ring + L.ring_f;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * L.sin_f);
+    float *xpb = snb + 2 * L.sin_f;  // two buffers of rotated pairs, 2 GN floats per item
+    uint64_t *bars = reinterpret_cast<uint64_t *>(xpb + 2 * L.xp_f);
     BlockRing br;
     br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
@@ -383,12 +391,56 @@ __global__ void __launch_bounds__(kBlock)
     for (int64_t it = 0; it <= nblk; ++it) {
         if (producer && it < nblk) {
             const int s = int(it % kNS);
+            float *st = ring + size_t(s) * L.stage_f;
+            float *sn = snb + (it & 1) * L.sin_f;
             if (br.rg.wait(s, ctl)) {
-                angle_range(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, first_row(it) * lpw * GN,
-                            ts * lpw * GN, tid - 32);
+                angle_range(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
                 *br.abort_word = 1;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kProd) : "memory");  // angle warps only
+            if (*br.abort_word == 0) {
+                // the forward pass through the layers of every step of the
+                // stage: x = a_t * h_{t-1}, each rotation's output pair kept
+                const int64_t tb = T - (it + 1) * ts;
+                float *xp = xpb + (it & 1) * L.xp_f;
+                for (int q = first_row(it) * lpw + tid - 32; q < ts * lpw; q += kProd) {
+                    const int u = q / lpw, l = q % lpw;
+                    float cs[GN], sv[GN], hv[GK], av[GK];
+                    lds_vec<GN>(st + q * GN, cs);
+                    lds_vec<GN>(sn + q * GN, sv);
+                    if (tb + u >= 1) {
+                        lds_vec<GK>(st + h_off + q * GK, hv);
+                    } else if (h0 != nullptr && head0 + l < H) {
+                        lds_vec<GK>(h0 + (bi * H + head0 + l) * GK, hv);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < GK; ++i) hv[i] = 0.f;
+                    }
+                    if (has_a) {
+                        lds_vec<GK>(st + L.th_f + q * GK, av);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < GK; ++i) av[i] = 1.f;
+                    }
+                    float x[GK], pr[2 * GN];
+#pragma unroll
+                    for (int i = 0; i < GK; ++i) x[i] = av[i] * hv[i];
+#pragma unroll
+                    for (int ll = 0; ll < GK; ++ll)
+#pragma unroll
+                        for (int qq = 0; qq < layer_pairs(ll); ++qq) {
+                            const int p = (ll & 1) + 2 * qq, n = layer_base(ll) + qq;
+                            rot_fwd(x[p], x[p + 1], cs[n], sv[n]);
+                            pr[2 * n] = x[p];
+                            pr[2 * n + 1] = x[p + 1];
+                        }
+#pragma unroll
+                    for (int c4 = 0; c4 < 2 * GN; c4 += 4)
+                        *reinterpret_cast<float4 *>(xp + q * 2 * GN + c4) =
+                            make_float4(pr[c4], pr[c4 + 1], pr[c4 + 2], pr[c4 + 3]);
+                }
             }
         }
         if (active && it >= 1) {
@@ -396,12 +448,14 @@ __global__ void __launch_bounds__(kBlock)
             const int64_t tb = T - (j + 1) * ts;  // in-batch row of box row 0
             const float *st = ring + size_t(j % kNS) * L.stage_f;
             const float *sc = snb + (j & 1) * L.sin_f;
+            const float *xp = xpb + (j & 1) * L.xp_f;
             for (int u = ts - 1; u >= first_row(j); --u) {
                 const int64_t t = tb + u;
                 const int item = u * lpw + lane;
-                float cs[GN], sv[GN], lam[GK], hp[GK];
+                float cs[GN], sv[GN], lam[GK], hp[GK], pr[2 * GN];
                 lds_vec<GN>(st + item * GN, cs);
                 lds_vec<GN>(sc + item * GN, sv);
+                lds_vec<2 * GN>(xp + item * 2 * GN, pr);
                 lds_vec<GK>(st + g_off + item * GK, lam);
                 if (t >= 1) {
                     lds_vec<GK>(st + h_off + item * GK, hp);
@@ -420,30 +474,15 @@ __global__ void __launch_bounds__(kBlock)
 #pragma unroll
                     for (int i = 0; i < GK; ++i) av[i] = 1.f;
                 }
-                // forward through the mesh, keeping every layer's output
-                float xl[GK][GK];
-#pragma unroll
-                for (int i = 0; i < GK; ++i) xl[0][i] = av[i] * hp[i];
-#pragma unroll
-                for (int l = 0; l < GK; ++l) {
-                    if (l > 0) {
-#pragma unroll
-                        for (int i = 0; i < GK; ++i) xl[l][i] = xl[l - 1][i];
-                    }
-#pragma unroll
-                    for (int q = 0; q < layer_pairs(l); ++q) {
-                        const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-                        rot_fwd(xl[l][p], xl[l][p + 1], cs[n], sv[n]);
-                    }
-                }
-                // adjoint back through the layers
+                // adjoint back through the layers, with the rotated pairs the
+                // angle warps kept
                 float dthv[GN];
 #pragma unroll
                 for (int l = GK - 1; l >= 0; --l) {
 #pragma unroll
                     for (int q = 0; q < layer_pairs(l); ++q) {
                         const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-                        dthv[n] = fmaf(lam[p + 1], xl[l][p], -lam[p] * xl[l][p + 1]);
+                        dthv[n] = fmaf(lam[p + 1], pr[2 * n], -lam[p] * pr[2 * n + 1]);
                         rot_bwd(lam[p], lam[p + 1], cs[n], sv[n]);
                     }
                 }
@@ -975,7 +1014,7 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
     }
     const int64_t gpb = (H + lpw - 1) / lpw, blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const int smem = int(GasSmem(lpw, ts, a ? 3 : 2).bytes());
+    const int smem = int(GasSmem(lpw, ts, a ? 3 : 2, true).bytes());
     if ((e = ensure_smem_attr((const void *)gas_bwd_kernel, smem)) != cudaSuccess) return e;
     gas_bwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H,
                                                                 gpb, lpw, ts, a != nullptr, ctl);
