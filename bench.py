@@ -332,6 +332,7 @@ class Runner:
             self.ws_b, self.nb = api.workspace(b.MGS_OP_GIVENS_MATRIX_SCAN_BWD, B, T, H, k, device)
         elif w.op == "delta":
             self.o, self.ST = e(B, T, H, k), e(B, H, k, k)
+            self.ws_f, self.nf = api.workspace(b.MGS_OP_DELTA_SCAN_FWD, B, T, H, k, device)
         else:
             self.h = e(B, T, H)
             self.dlc, self.dlv, self.dl0 = e(B, T, H), e(B, T, H), e(B, H)
@@ -365,7 +366,7 @@ class Runner:
             b.mgs_givens_matrix_scan_fwd(d["theta"], self.P, w.B, w.T, w.H, w.k, self.ws_f, self.nf, stream)
         elif w.op == "delta":
             b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], self.o, self.ST, w.B, w.T, w.H, w.k,
-                                 None, 0, stream)
+                                 self.ws_f, self.nf, stream)
         else:
             b.mgs_parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], self.h, None,
                                         w.B, w.T, w.H, None, 0, stream)
@@ -554,6 +555,8 @@ def run_gpu(args):
     achieved = kbytes / (kms * 1e-3) / 1e9
     chunked = kw.op == "ms" and b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, kw.B, kw.T, kw.H, kw.k) > 0
     kernel_symbol = f"{kw.op}_{kdir}_{'chunk_' if chunked else ''}kernel"
+    if kw.op == "delta":
+        kernel_symbol = "delta_wy_kernel+delta_state_kernel"
     traffic = committed_traffic(kw.op, f"{kernel_symbol}@c{kw.cid}")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,

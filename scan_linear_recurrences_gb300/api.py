@@ -181,7 +181,8 @@ def delta_scan_fwd(q, k, v, beta, S0=None, want_state=False, stream=None):
         _check(S0, "S0", (B, H, D, D))
     o = torch.empty_like(q)
     ST = torch.empty((B, H, D, D), dtype=torch.float32, device=q.device) if want_state else None
-    _b.mgs_delta_scan_fwd(q, k, v, beta, S0, o, ST, B, T, H, D, None, 0, stream)
+    ws, nws = workspace(_b.MGS_OP_DELTA_SCAN_FWD, B, T, H, D, q.device)
+    _b.mgs_delta_scan_fwd(q, k, v, beta, S0, o, ST, B, T, H, D, ws, nws, stream)
     return (o, ST) if want_state else o
 
 

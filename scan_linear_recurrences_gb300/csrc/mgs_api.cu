@@ -211,6 +211,13 @@ size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
             if (givens_sizes(B, T, H_or_D, k, &gs) != MGS_OK || gs.vec == 0) return 0;
             return mgs::givens_workspace_bytes(op - MGS_OP_GIVENS_AFFINE_SCAN_FWD, B, T, H_or_D);
         }
+        case MGS_OP_DELTA_SCAN_FWD: {
+            int64_t ns;
+            if (B < 0 || T < 0 || H_or_D < 0 || k != 64 || !mul_ok(B, T, &ns) || !mul_ok(ns, H_or_D, &ns) ||
+                !mul_ok(B, H_or_D, &ns) || !mul_ok(ns, (T + 63) / 64, &ns) || ns > INT64_MAX / (3 * 64 * 64 * 4))
+                return 0;
+            return mgs::delta_workspace_bytes(B, T, H_or_D);
+        }
         case MGS_OP_PARALLEL_SCAN_LOG_BWD: {
             int64_t n, n0;
             if (psl_sizes(B, T, H_or_D, &n, &n0) != MGS_OK || n == 0) return 0;
@@ -496,10 +503,16 @@ mgs_status mgs_delta_scan_fwd(const float *q, const float *k, const float *v, co
     if (!disjoint({{o, n}, {S_T, S_T ? ns : 0}},
                   {{q, n}, {k, n}, {v, n}, {beta, nb}, {S0, S0 ? ns : 0}}))
         return MGS_ERR_INVALID_ARG;
-    if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
+    int64_t chunks;
+    if (!mul_ok(B * H, (T + 63) / 64, &chunks) || chunks > INT32_MAX / (3 * 64)) return MGS_ERR_UNSUPPORTED;
+    const size_t need = mgs::delta_workspace_bytes(B, T, H);
+    if ((st = check_ws(need, workspace, workspace_bytes)) != MGS_OK) return st;
+    if (!disjoint({{static_cast<float *>(workspace), int64_t(need / sizeof(float))}},
+                  {{q, n}, {k, n}, {v, n}, {beta, nb}, {S0, S0 ? ns : 0}, {o, n}, {S_T, S_T ? ns : 0}}))
+        return MGS_ERR_INVALID_ARG;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    return from_cuda(mgs::launch_delta_fwd(q, k, v, beta, S0, o, S_T, B, T, H, ctl, cs));
+    return from_cuda(mgs::launch_delta_fwd(q, k, v, beta, S0, o, S_T, B, T, H, workspace, ctl, cs));
 }
 
 mgs_status mgs_check(mgs_stream_t stream) {

@@ -7,25 +7,33 @@
 // A chunk of C = 64 steps with state S on entry is, in matrix form (rows are
 // time steps, K, V, Q are C x D):
 //   A   = strict_tril(diag(beta) K K^T)
-//   (I + A) [W | U] = diag(beta) [K | V],   U' = U - W S^T
-//   O   = Q S^T + tril(Q K^T) U'
+//   (I + A) [W | U] = diag(beta) [K | V],   P = tril(Q K^T)
+//   U'  = U - W S^T
+//   O   = Q S^T + P U'
 //   S  <- S + U'^T K
 // which is the recurrence exactly (the WY representation of the product of
-// the chunk's rank-one updates).  Since (I + A) is the same for W and U, U'
-// is obtained from one solve, (I + A) U' = diag(beta) (V - K S^T), and W is
-// never formed.  The solve is blocked by 16 rows: the four 16 x 16 diagonal
-// blocks of (I + A) are inverted by forward substitution (one warp each), then
-// U'_b = D_b (R_b - A_{b,<b} U'_{<b}) block after block.  The state is kept
-// key-major (S^T) in shared memory so that every product reads its operands
-// by rows.
+// the chunk's rank-one updates).  W, U and P depend on the chunk's inputs
+// only, so they are formed for every chunk at once (delta_wy_kernel, one
+// block per chunk); only the last three lines carry the state from chunk to
+// chunk.  Those lines act on each value index i (row i of S, column i of U',
+// O) separately, so the state pass (delta_state_kernel) splits every lane
+// into blocks of 8, 16, 32 or 64 value columns (narrower when lanes are few,
+// so that more blocks run) that walk the lane's chunks in order, each holding
+// its slice of S^T.
 //
-// One 256-thread block per lane walks its chunks in order; each chunk's Q, K
-// and V arrive by tiled TMA loads (a 68-float box over 64-float rows, so the
-// last 4 floats of every shared row are the tensor map's zero fill: a padded
-// layout that keeps the products' shared reads free of bank conflicts), two
-// chunks in flight.  The 64 x 64 x 64 products run on the tensor cores
-// (mma.sync tf32 with a three-term split for fp32 accuracy), each warp owning a
-// 16 x 32 block of the result; the forward substitution runs on the fp32 pipes.
+// [W | U] = T' [K | V] with T' = (I + A)^{-1} diag(beta), lower triangular.
+// T' is formed by 16 x 16 blocks: the diagonal blocks D_b = (I + A_bb)^{-1}
+// by forward substitution (one warp each), T'_bb = D_b diag(beta_b), then
+// E_bm = D_b A_bm for the six blocks below the diagonal, then the blocks of
+// T' below the diagonal one subdiagonal at a time,
+//   T'_bc = -sum_{c <= m < b} E_bm T'_mc,
+// which is (I + A) T' = diag(beta) solved by blocks.  Q, K, V (and in the
+// state pass W, P and the slice of U) arrive by tiled TMA loads; a box
+// wider than the 64-float rows leaves the last floats of every shared row as
+// the tensor map's zero fill, a padded layout that keeps the products' shared
+// reads free of bank conflicts.  The 64 x 64 products run on the tensor cores
+// (mma.sync tf32 with a three-term split for fp32 accuracy); the small
+// triangular blocks on the fp32 pipes.
 #include "mgs_tiles.cuh"
 
 namespace mgs {
@@ -36,24 +44,57 @@ constexpr int CH = 64;         // chunk length
 constexpr int LD = 68;         // padded row stride (floats)
 constexpr int MATF = CH * LD;  // floats per padded 64 x 64 matrix
 constexpr int kThreads = 256;
-constexpr int kStages = 2;
+constexpr int kStages = 3;      // at most this many chunks in flight in the state pass
+constexpr int DLD = 20;         // row stride of the 16 x 16 blocks (D_b, level sums)
+constexpr int WSM = CH * DD;    // floats of one stored 64 x 64 matrix (W, U or P)
 
-// Shared memory layout (floats): stages [Q K V] x kStages, then ST, KT, A, QK,
-// D (the inverted diagonal blocks, rows 16b..16b+15, columns 0..15), U (R,
-// then U' in place; also the 16-row panel of the blocked solve), beta (64),
-// barriers.
-struct DeltaSmem {
-    static constexpr int stage = 3 * MATF;
-    static constexpr int st = kStages * stage;
-    static constexpr int kt = st + MATF;
-    static constexpr int a = kt + MATF;
-    static constexpr int qk = a + MATF;
-    static constexpr int w = qk + MATF;
-    static constexpr int u = w + MATF;
-    static constexpr int beta = u + MATF;
-    static constexpr int bars = beta + CH;  // 8-byte aligned (all offsets are multiples of 4 floats)
-    static constexpr size_t bytes = size_t(bars) * 4 + kStages * sizeof(uint64_t) + 16;  // + abort word
+// State blocks of NT n-tiles (8 NT value columns); the shared stride of their
+// 64 x 8 NT operands is 8 mod 32 floats, so that a fragment's reads
+// (rows k0 + q, columns g) fall in 32 different banks.
+template <int NT>
+struct StateCols {
+    static constexpr int VS = 8 * NT;
+    static constexpr int LDB = NT == 1 ? 8 : VS + 8;
 };
+
+// Shared memory of delta_wy_kernel (floats): Q, K, V, A, T' (padded
+// 64 x 68), D (64 x DLD: rows 16b..16b+15, columns 0..15), E (6 blocks of
+// 16 x DLD, block b(b-1)/2 + m holding E_bm), beta (64), the barrier and the
+// abort word.
+struct WySmem {
+    static constexpr int q = 0;
+    static constexpr int k = MATF;
+    static constexpr int v = 2 * MATF;
+    static constexpr int a = 3 * MATF;
+    static constexpr int t = 4 * MATF;
+    static constexpr int dinv = 5 * MATF;
+    static constexpr int xs = dinv + CH * DLD;
+    static constexpr int beta = xs + 6 * 16 * DLD;
+    static constexpr int bars = beta + CH;  // 8-byte aligned (all offsets are multiples of 4 floats)
+    static constexpr size_t bytes = size_t(bars) * 4 + sizeof(uint64_t) + 16;
+};
+
+// Shared memory of delta_state_kernel (floats): nst stages of [W P Q K]
+// (padded 64 x 68) and the block's columns of U (64 x LDB); the block's slice
+// of S^T (64 x LDB, key-major), U' (64 x LDB), then kStages barriers and the
+// abort word.
+struct StateSmem {
+    int stage, st, up, bars;
+    size_t bytes;
+    __host__ __device__ StateSmem(int nst, int ldb) {
+        stage = 4 * MATF + CH * ldb;
+        st = nst * stage;
+        up = st + DD * ldb;
+        bars = up + CH * ldb;
+        bytes = size_t(bars) * 4 + kStages * sizeof(uint64_t) + 16;
+    }
+};
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 
 // ---- 64 x 64 x 64 products on the tensor cores (mma.sync m16n8k8, tf32).
 // fp32 accuracy from three tf32 products per multiply: with x = xb + xs
@@ -82,12 +123,13 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// acc[nt] += op(A)[m0.., :] B[:, n0 + 8 nt ..] over k = 0..63 for one warp's
-// 16 x (8 NT) block of the result.  AT = false: A row-major [m][k];
-// AT = true: A stored [k][m].  B row-major [k][n].  Stride LD.
-// Only k < kend and n-tiles nt < ntl take part (the zero triangles of the
-// masked products are skipped; both limits are warp-uniform).
-template <bool AT, int NT>
+// acc[nt] += op(A)[m0.., :] op(B)[:, n0 + 8 nt ..] over k = 0..63 for one
+// warp's 16 x (8 NT) block of the result.  AT = false: A row-major [m][k];
+// AT = true: A stored [k][m].  BT = false: B row-major [k][n]; BT = true: B
+// stored [n][k].  Stride LD.  Only k < kend and n-tiles nt < ntl take part
+// (the zero triangles of the masked products are skipped; both limits are
+// warp-uniform).
+template <bool AT, int NT, bool BT = false>
 __device__ __forceinline__ void mma64(const float *__restrict__ A, const float *__restrict__ B, float (&acc)[NT][4],
                                       int m0, int n0, int lane, int kend = DD, int ntl = NT) {
     const int g = lane >> 2, q = lane & 3;
@@ -113,13 +155,73 @@ __device__ __forceinline__ void mma64(const float *__restrict__ A, const float *
             if (nt >= ntl) break;
             const int n = n0 + 8 * nt + g;
             uint32_t bb[2], bs[2];
-            split_tf32(B[(k0 + q) * LD + n], bb[0], bs[0]);
-            split_tf32(B[(k0 + q + 4) * LD + n], bb[1], bs[1]);
+            if constexpr (BT) {
+                split_tf32(B[n * LD + k0 + q], bb[0], bs[0]);
+                split_tf32(B[n * LD + k0 + q + 4], bb[1], bs[1]);
+            } else {
+                split_tf32(B[(k0 + q) * LD + n], bb[0], bs[0]);
+                split_tf32(B[(k0 + q + 4) * LD + n], bb[1], bs[1]);
+            }
             mma_tf32(acc[nt], as, bb);
             mma_tf32(acc[nt], ab, bs);
             mma_tf32(acc[nt], ab, bb);
         }
     }
+}
+
+// acc[nt] += op(A)[m0.., 0..kend) B[0..kend, 8 nt..] for one warp's
+// 16 x 8 NT block, A as in mma64 (stride LD), B row-major [k][n] of stride
+// LDB.  With a single n-tile the three terms of the split go to three
+// accumulators (shorter dependency chains), summed at the end.
+template <bool AT, int NT, int LDB>
+__device__ __forceinline__ void mma_tile(const float *__restrict__ A, const float *__restrict__ B,
+                                         float (&acc)[NT][4], int m0, int lane, int kend = DD) {
+    const int g = lane >> 2, q = lane & 3;
+    constexpr int NA = NT == 1 ? 3 : 1;
+    float c[NA][NT][4];
+#pragma unroll
+    for (int t = 0; t < NA; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[t][nt][e] = 0.f;
+#pragma unroll(NT > 2 ? 2 : 8)
+    for (int k0 = 0; k0 < DD; k0 += 8) {
+        if (k0 >= kend) break;
+        float av[4];
+        if constexpr (AT) {
+            av[0] = A[(k0 + q) * LD + m0 + g];
+            av[1] = A[(k0 + q) * LD + m0 + g + 8];
+            av[2] = A[(k0 + q + 4) * LD + m0 + g];
+            av[3] = A[(k0 + q + 4) * LD + m0 + g + 8];
+        } else {
+            av[0] = A[(m0 + g) * LD + k0 + q];
+            av[1] = A[(m0 + g + 8) * LD + k0 + q];
+            av[2] = A[(m0 + g) * LD + k0 + q + 4];
+            av[3] = A[(m0 + g + 8) * LD + k0 + q + 4];
+        }
+        uint32_t ab[4], as[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_tf32(av[i], ab[i], as[i]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            uint32_t bb[2], bs[2];
+            split_tf32(B[(k0 + q) * LDB + 8 * nt + g], bb[0], bs[0]);
+            split_tf32(B[(k0 + q + 4) * LDB + 8 * nt + g], bb[1], bs[1]);
+            mma_tf32(c[0][nt], as, bb);
+            mma_tf32(c[NA > 1 ? 1 : 0][nt], ab, bs);
+            mma_tf32(c[NA > 2 ? 2 : 0][nt], ab, bb);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float sum = c[0][nt][e];
+#pragma unroll
+            for (int t = 1; t < NA; ++t) sum += c[t][nt][e];
+            acc[nt][e] += sum;
+        }
 }
 
 template <int NT>
@@ -146,68 +248,265 @@ __device__ __forceinline__ void store_frag(float *C, const float (&acc)[NT][4], 
                 make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
 }
 
-__global__ void __launch_bounds__(kThreads)
-    delta_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const float *__restrict__ beta,
-                     const float *__restrict__ S0, float *__restrict__ o, float *__restrict__ ST_out, int64_t B,
-                     int64_t T, int64_t H, DevCtl ctl) {
-    using L = DeltaSmem;
+// Stores a warp's 16 x 64 accumulator block (rows m0..) as rows of 64 floats.
+__device__ __forceinline__ void store_frag_global(float *__restrict__ C, const float (&acc)[8][4], int m0, int lane) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            *reinterpret_cast<float2 *>(C + frag_row(m0, lane, 2 * h) * DD + frag_col(0, lane, nt, 0)) =
+                make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
+}
+
+// One block per chunk (chunks of a lane consecutive): W, U and P of the chunk
+// into the workspace, each 64 x 64 row-major (rows past the sequence end are
+// zero).
+__global__ void __launch_bounds__(kThreads, 2)
+    delta_wy_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const float *__restrict__ beta, float *__restrict__ ws,
+                    int64_t B, int64_t T, int64_t H, DevCtl ctl) {
+    using L = WySmem;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     float *sm = reinterpret_cast<float *>(smem_raw);
-    float *ST = sm + L::st, *KT = sm + L::kt, *Am = sm + L::a, *QK = sm + L::qk, *U = sm + L::u;
-    float *Wd = sm + L::w;           // inverted diagonal blocks D_b
-    float *Pn = KT;                  // 16-row panel of the blocked solve (KT is free by then)
-    float *sb = sm + L::beta;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::bars);
-    int *abort_word = reinterpret_cast<int *>(bars + kStages);
+    float *Q = sm + L::q, *K = sm + L::k, *V = sm + L::v, *Am = sm + L::a, *Tm = sm + L::t;
+    float *Dv = sm + L::dinv, *Xs = sm + L::xs, *sb = sm + L::beta;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::bars);
+    int *abort_word = reinterpret_cast<int *>(bar + 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t lane_id = blockIdx.x;  // (batch, head)
-    if (lane_id >= B * H) return;
-    const int64_t bi = lane_id / H, hd = lane_id % H;
     const int64_t nch = (T + CH - 1) / CH;
-    const int row0 = int(bi * T);
+    const int64_t ci = blockIdx.x;
+    if (ci >= B * H * nch) return;
+    const int64_t lane_id = ci / nch, c = ci % nch;
+    const int64_t bi = lane_id / H, hd = lane_id % H;
+    const int n = int(min64(CH, T - c * CH));
+    const int r = int(bi * T + c * CH);
+    float *Wg = ws + ci * 3 * WSM, *Ug = Wg + WSM, *Pg = Wg + 2 * WSM;
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+        mbar_init(bar, 1);
         fence_barrier_init();
         *abort_word = 0;
     }
     __syncthreads();
-    const uint64_t pol = policy_evict_first();
+    WarpRing<1> rg;
+    rg.bar = bar;
+    rg.inflight = 0;
+    rg.phase = 0;
+    if (tid == 0) {
+        // Q and K are read again by the state pass: kept in L2 at normal priority
+        const uint64_t keep = policy_evict_normal(), once = policy_evict_first();
+        mbar_arrive_expect_tx(bar, uint32_t(3 * MATF * 4));
+        tma_load_3d(Q, &tmQ, 0, int(hd), r, bar, keep);
+        tma_load_3d(K, &tmK, 0, int(hd), r, bar, keep);
+        tma_load_3d(V, &tmV, 0, int(hd), r, bar, once);
+    }
+    rg.armed(0);
+    if (tid < CH) sb[tid] = tid < n ? beta[(int64_t(r) + tid) * H + hd] : 0.f;
+    if (!rg.wait(0, ctl) && lane == 0) {
+        record_error(ctl, ERR_MBAR_TIMEOUT);
+        *abort_word = 1;
+    }
+    __syncthreads();
+    if (*abort_word != 0) {
+        rg.drain(ctl, lane);
+        return;
+    }
+    // rows past the sequence end (the next sequence's, or fill) contribute nothing
+    if (n < CH)
+        for (int e = tid; e < (CH - n) * LD; e += kThreads) {
+            Q[n * LD + e] = 0.f;
+            K[n * LD + e] = 0.f;
+            V[n * LD + e] = 0.f;
+        }
+    __syncthreads();
+    // Row blocks 16w (warps 0-3) and 16(7-w) (warps 4-7) in the triangular
+    // products, so that the two warps of each SM sub-partition share out the
+    // same number of tiles.
+    const bool lo = warp < 4;
+    const int mt = lo ? 16 * warp : 48 - 16 * (warp - 4);
+    // Phase 1.  Warps 0-3: A = strict_tril(diag(beta) K K^T); warps 4-7:
+    // P = tril(Q K^T), straight to the workspace.
+    {
+        float acc[8][4];
+        zero_frag(acc);
+        // only columns up to the diagonal: n-tiles below mt/8 + 2
+        mma64<false, 8, true>(lo ? K : Q, K, acc, mt, 0, lane, DD, mt / 8 + 2);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int t = frag_row(mt, lane, e), s2 = frag_col(0, lane, nt, e);
+                acc[nt][e] = lo ? ((s2 < t) ? sb[t] * acc[nt][e] : 0.f) : ((s2 <= t) ? acc[nt][e] : 0.f);
+            }
+        if (lo)
+            store_frag(Am, acc, mt, 0, lane);
+        else
+            store_frag_global(Pg, acc, mt, lane);
+    }
+    __syncthreads();
+    // Phase 2.  Warps 0-3: D_b = (I + A_bb)^{-1}, b = warp, lane j < 16 builds
+    // column j by forward substitution; T'_bb = D_b diag(beta_b).  The column
+    // is kept in registers and stored after it is complete, so that no shared
+    // store sits between the loads of the chain.
+    if (lo && lane < 16) {
+        const int b0 = 16 * warp;
+        float dcol[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            float arow[16];
+#pragma unroll
+            for (int q4 = 0; q4 < rr; q4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Am + (b0 + rr) * LD + b0 + q4);
+                arow[q4] = a4.x;
+                arow[q4 + 1] = a4.y;
+                arow[q4 + 2] = a4.z;
+                arow[q4 + 3] = a4.w;
+            }
+            float acc = (rr == lane) ? 1.f : 0.f;
+#pragma unroll
+            for (int q = 0; q < rr; ++q) acc = fmaf(-arow[q], dcol[q], acc);
+            dcol[rr] = acc;
+        }
+        const float bj = sb[b0 + lane];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            Dv[(b0 + rr) * DLD + lane] = dcol[rr];
+            Tm[(b0 + rr) * LD + b0 + lane] = dcol[rr] * bj;
+        }
+    }
+    __syncthreads();
+    // Phase 3.  E_bm = D_b A_bm for the six blocks below the diagonal (pair
+    // j = b(b-1)/2 + m), then T'_bc = -sum_{c <= m < b} E_bm T'_mc one
+    // subdiagonal d = b - c at a time.  Thread: element (tid / 16, tid % 16)
+    // of every block of the step.
+    const int er = tid >> 4, ec = tid & 15;
+    {
+        float acc[6];
+#pragma unroll
+        for (int j = 0; j < 6; ++j) acc[j] = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 16; q4 += 4) {
+#pragma unroll
+            for (int j = 0; j < 6; ++j) {
+                const int b = j < 1 ? 1 : j < 3 ? 2 : 3, m = j - b * (b - 1) / 2;
+                const float4 d4 = *reinterpret_cast<const float4 *>(Dv + (16 * b + er) * DLD + q4);
+                const float *a = Am + (16 * b + q4) * LD + 16 * m + ec;
+                acc[j] = fmaf(d4.x, a[0], acc[j]);
+                acc[j] = fmaf(d4.y, a[LD], acc[j]);
+                acc[j] = fmaf(d4.z, a[2 * LD], acc[j]);
+                acc[j] = fmaf(d4.w, a[3 * LD], acc[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 6; ++j) Xs[(16 * j + er) * DLD + ec] = acc[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int d = 1; d < 4; ++d) {
+        constexpr int kMaxB = 3;
+        float acc[kMaxB];
+#pragma unroll
+        for (int cb = 0; cb < kMaxB; ++cb) acc[cb] = 0.f;
+#pragma unroll
+        for (int cb = 0; cb < 4 - d; ++cb) {
+            const int b = cb + d;
+#pragma unroll
+            for (int m = cb; m < b; ++m) {
+                const float *e = Xs + (16 * (b * (b - 1) / 2 + m) + er) * DLD;
+                const float *t = Tm + 16 * m * LD + 16 * cb + ec;
+#pragma unroll
+                for (int q4 = 0; q4 < 16; q4 += 4) {
+                    const float4 e4 = *reinterpret_cast<const float4 *>(e + q4);
+                    acc[cb] = fmaf(e4.x, t[(q4 + 0) * LD], acc[cb]);
+                    acc[cb] = fmaf(e4.y, t[(q4 + 1) * LD], acc[cb]);
+                    acc[cb] = fmaf(e4.z, t[(q4 + 2) * LD], acc[cb]);
+                    acc[cb] = fmaf(e4.w, t[(q4 + 3) * LD], acc[cb]);
+                }
+            }
+        }
+#pragma unroll
+        for (int cb = 0; cb < 4 - d; ++cb) Tm[(16 * (cb + d) + er) * LD + 16 * cb + ec] = -acc[cb];
+        __syncthreads();
+    }
+    // Phase 4.  Warps 0-3: W = T' K; warps 4-7: U = T' V (k only up to the
+    // diagonal block), straight to the workspace.
+    {
+        float acc[8][4];
+        zero_frag(acc);
+        mma64<false, 8>(Tm, lo ? K : V, acc, mt, 0, lane, mt + 16);
+        store_frag_global(lo ? Wg : Ug, acc, mt, lane);
+    }
+}
+
+// One block per (lane, 8 NT value columns i0..): walks the lane's chunks in
+// order with the slice S^T[:, i0..] in shared memory.  Per chunk:
+//   warps 0-3: U'[16w..] = U[16w.., i] - W[16w..] S^T[:, i]
+//   warps 4-7: O = Q[16(w-4)..] S^T[:, i], then O += P U' (k up to the diagonal)
+//   warps 0-3: S^T[16w.., i] += K^T U'
+template <int NT>
+__global__ void __launch_bounds__(kThreads)
+    delta_state_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
+                       const float *__restrict__ S0, float *__restrict__ o, float *__restrict__ ST_out, int64_t B,
+                       int64_t T, int64_t H, int nst, DevCtl ctl) {
+    constexpr int VS = StateCols<NT>::VS, LDB = StateCols<NT>::LDB, NVB = DD / VS;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const StateSmem L(nst, LDB);
+    float *sm = reinterpret_cast<float *>(smem_raw);
+    float *STc = sm + L.st, *Up = sm + L.up;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+    int *abort_word = reinterpret_cast<int *>(bars + kStages);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t blk = blockIdx.x;
+    if (blk >= B * H * NVB) return;
+    const int64_t lane_id = blk / NVB;
+    const int i0 = int(blk % NVB) * VS;
+    const int64_t bi = lane_id / H, hd = lane_id % H;
+    const int64_t nch = (T + CH - 1) / CH;
+
+    if (tid == 0) {
+        for (int s = 0; s < nst; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+        *abort_word = 0;
+    }
+    __syncthreads();
+    // the lane's state blocks read the same W, P, Q, K (and U rows)
+    const uint64_t pol = policy_evict_normal();
     auto issue = [&](int s, int64_t c) {  // thread 0 only
-        float *st = sm + s * L::stage;
-        const int r = row0 + int(c * CH);
-        mbar_arrive_expect_tx(&bars[s], uint32_t(3 * MATF * 4));
-        tma_load_3d(st, &tmQ, 0, int(hd), r, &bars[s], pol);
-        tma_load_3d(st + MATF, &tmK, 0, int(hd), r, &bars[s], pol);
-        tma_load_3d(st + 2 * MATF, &tmV, 0, int(hd), r, &bars[s], pol);
+        float *st = sm + s * L.stage;
+        const int r = int(bi * T + c * CH);
+        const int wr = int((lane_id * nch + c) * 3 * CH);  // workspace row of the chunk's W
+        mbar_arrive_expect_tx(&bars[s], uint32_t(L.stage * 4));
+        tma_load_2d(st, &tmW, 0, wr, &bars[s], pol);
+        tma_load_2d(st + MATF, &tmW, 0, wr + 2 * CH, &bars[s], pol);
+        tma_load_3d(st + 2 * MATF, &tmQ, 0, int(hd), r, &bars[s], pol);
+        tma_load_3d(st + 3 * MATF, &tmK, 0, int(hd), r, &bars[s], pol);
+        tma_load_2d(st + 4 * MATF, &tmU, i0, wr + CH, &bars[s], pol);
     };
-    // Every thread tracks the ring (all wait on the same barriers).
-    WarpRing<kStages> rg;
+    WarpRing<kStages> rg;  // every thread tracks the ring (all wait on the same barriers)
     rg.bar = bars;
     rg.inflight = 0;
     rg.phase = 0;
-    const int npro = int(min64(kStages, nch));
+    const int npro = int(min64(nst, nch));
     if (tid == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmU);
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
         for (int s = 0; s < npro; ++s) issue(s, s);
     }
     for (int s = 0; s < npro; ++s) rg.armed(s);
-
-    float beta_next = (tid < CH && tid < T) ? beta[(bi * T + tid) * H + hd] : 0.f;
-    // initial state, key-major: ST[j][i] = S0[i][j]
-    for (int e = tid; e < DD * DD; e += kThreads) {
+    // the slice of the initial state, key-major: STc[j][i] = S0[i0 + i][j]
+    for (int e = tid; e < DD * VS; e += kThreads) {
         const int i = e >> 6, j = e & 63;
-        ST[j * LD + i] = S0 != nullptr ? S0[lane_id * DD * DD + e] : 0.f;
+        STc[j * LDB + i] = S0 != nullptr ? S0[lane_id * DD * DD + (i0 + i) * DD + j] : 0.f;
     }
 
+    const bool lo = warp < 4;
+    const int m0 = 16 * (warp & 3);
     for (int64_t c = 0; c < nch; ++c) {
-        const int s = int(c % kStages);
+        const int s = int(c % nst);
         const int n = int(min64(CH, T - c * CH));
-        // a wait that gives up in any warp makes the whole block leave at the
-        // next barrier, after each warp has drained the copies it still counts
         if (!rg.wait(s, ctl) && lane == 0) {
             record_error(ctl, ERR_MBAR_TIMEOUT);
             *abort_word = 1;
@@ -217,166 +516,67 @@ __global__ void __launch_bounds__(kThreads)
             rg.drain(ctl, lane);
             return;
         }
-        float *Q = sm + s * L::stage, *K = Q + MATF, *V = K + MATF;
-        // beta of the chunk (0 past the sequence end; loaded one chunk ahead);
-        // the rows of Q, K and V past the end (the next sequence's, or fill)
-        // are zeroed so that they contribute exactly nothing
-        if (tid < CH) {
-            sb[tid] = beta_next;
-            const int64_t tn = (c + 1) * CH + tid;
-            beta_next = tn < T ? beta[(bi * T + tn) * H + hd] : 0.f;
-        }
+        float *st = sm + s * L.stage;
+        const float *W = st, *P = st + MATF, *Q = st + 2 * MATF, *Uc = st + 4 * MATF;
+        float *K = st + 3 * MATF;
+        // rows of K past the sequence end meet rows of U' that are exactly zero;
+        // zeroed so that whatever they hold contributes nothing
         if (n < CH)
-            for (int e = tid; e < (CH - n) * LD; e += kThreads) {
-                Q[n * LD + e] = 0.f;
-                K[n * LD + e] = 0.f;
-                V[n * LD + e] = 0.f;
-            }
-        __syncthreads();
-        // KT[j][t] = K[t][j]
-        for (int e = tid; e < CH * DD; e += kThreads) {
-            const int t = e & 63, j = e >> 6;
-            KT[j * LD + t] = K[t * LD + j];
-        }
-        __syncthreads();
-        // Phase 1.  Warps 0-3 (rows 16w..): A = strict_tril(diag(beta) K K^T)
-        // and R = diag(beta) (V - K S^T).  Warps 4-7 (rows 16(w-4)..):
-        // QK = tril(Q K^T) and Q S^T, the latter kept in registers as the
-        // start of O.
-        const bool lo = warp < 4;
-        const int mr = 16 * (warp & 3);  // this warp's 16 rows in phases 1 and 4
-        float oacc[8][4];                // warps 4-7: Q S^T, then O; warps 0-3: K^T U'
-        zero_frag(oacc);
-        {
-            // the triangular products take rows 16w (warps 0-3) and 16(7-w)
-            // (warps 4-7), so that the two warps of each SM sub-partition
-            // (w and w+4) share out the same number of tiles
-            const int mt = lo ? mr : 48 - mr;
-            float acc[8][4];
-            zero_frag(acc);
-            // only columns up to the diagonal: n-tiles below mt/8 + 2
-            mma64<false>(lo ? K : Q, KT, acc, mt, 0, lane, DD, mt / 8 + 2);
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = frag_row(mt, lane, e), s2 = frag_col(0, lane, nt, e);
-                    acc[nt][e] = lo ? ((s2 < t) ? sb[t] * acc[nt][e] : 0.f) : ((s2 <= t) ? acc[nt][e] : 0.f);
-                }
-            store_frag(lo ? Am : QK, acc, mt, 0, lane);
-            mma64<false>(lo ? K : Q, ST, oacc, mr, 0, lane);
-            if (lo) {
-#pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int t = frag_row(mr, lane, 2 * h), i = frag_col(0, lane, nt, 0);
-                        const float2 v2 = *reinterpret_cast<const float2 *>(V + t * LD + i);
-                        *reinterpret_cast<float2 *>(U + t * LD + i) =
-                            make_float2(sb[t] * (v2.x - oacc[nt][2 * h]), sb[t] * (v2.y - oacc[nt][2 * h + 1]));
-                    }
-                zero_frag(oacc);
-            }
-        }
-        __syncthreads();
-        // Phase 2.  D_b = (I + A_bb)^{-1}, b = warp (0-3), lane j < 16 builds
-        // column j by forward substitution.
-        if (warp < 4 && lane < 16) {
-            const int b0 = 16 * warp;
-            float dcol[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == lane) ? 1.f : 0.f;
-#pragma unroll
-                for (int q = 0; q < r; ++q) acc = fmaf(-Am[(b0 + r) * LD + b0 + q], dcol[q], acc);
-                dcol[r] = acc;
-                Wd[(b0 + r) * LD + lane] = acc;
-            }
-        }
-        __syncthreads();
-        // Phase 3.  Blocked solve, U' in place of R: for b = 0..3,
-        // P = R_b - A_{b,<b} U'_{<b};  U'_b = D_b P.  Thread: column tid % 64,
-        // rows 4 (tid / 64) .. +3 of the block.
-        {
-            const int col = tid & 63, r0 = 4 * (tid >> 6);
-            for (int b = 0; b < 4; ++b) {
-                const int b0 = 16 * b;
-                float p[4];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) p[r] = U[(b0 + r0 + r) * LD + col];
-                for (int s4 = 0; s4 < b0; s4 += 4) {
-                    const float u0 = U[(s4 + 0) * LD + col], u1 = U[(s4 + 1) * LD + col];
-                    const float u2 = U[(s4 + 2) * LD + col], u3 = U[(s4 + 3) * LD + col];
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(Am + (b0 + r0 + r) * LD + s4);
-                        p[r] = fmaf(-a4.x, u0, p[r]);
-                        p[r] = fmaf(-a4.y, u1, p[r]);
-                        p[r] = fmaf(-a4.z, u2, p[r]);
-                        p[r] = fmaf(-a4.w, u3, p[r]);
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < 4; ++r) Pn[(r0 + r) * LD + col] = p[r];
-                __syncthreads();
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int q4 = 0; q4 < 16; q4 += 4) {
-                        const float4 d4 = *reinterpret_cast<const float4 *>(Wd + (b0 + r0 + r) * LD + q4);
-                        acc = fmaf(d4.x, Pn[(q4 + 0) * LD + col], acc);
-                        acc = fmaf(d4.y, Pn[(q4 + 1) * LD + col], acc);
-                        acc = fmaf(d4.z, Pn[(q4 + 2) * LD + col], acc);
-                        acc = fmaf(d4.w, Pn[(q4 + 3) * LD + col], acc);
-                    }
-                    U[(b0 + r0 + r) * LD + col] = acc;
-                }
-                __syncthreads();
-            }
-        }
-        // Phase 4.  Warps 4-7: O = Q S^T + tril(Q K^T) U' (k only up to the
-        // diagonal); warps 0-3: rows 16w.. of K^T U' (the state update).
-        if (lo) {
-            mma64<true>(K, U, oacc, mr, 0, lane);  // oacc[j][i] = sum_t K[t][j] U'[t][i]
-        } else {
-            mma64<false>(QK, U, oacc, mr, 0, lane, mr + 16);
-#pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = frag_row(mr, lane, 2 * h);
-                    if (t < n)
-                        *reinterpret_cast<float2 *>(o + ((bi * T + c * CH + t) * H + hd) * DD +
-                                                    frag_col(0, lane, nt, 0)) =
-                            make_float2(oacc[nt][2 * h], oacc[nt][2 * h + 1]);
-                }
-        }
-        __syncthreads();  // every read of ST and of this stage is done
+            for (int e = tid; e < (CH - n) * LD; e += kThreads) K[n * LD + e] = 0.f;
+        float acc[NT][4];
+        zero_frag(acc);
+        mma_tile<false, NT, LDB>(lo ? W : Q, STc, acc, m0, lane);
         if (lo) {
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float2 *pp =
-                        reinterpret_cast<float2 *>(ST + frag_row(mr, lane, 2 * h) * LD + frag_col(0, lane, nt, 0));
+                    const int t = frag_row(m0, lane, 2 * h), i = frag_col(0, lane, nt, 0);
+                    const float2 u2 = *reinterpret_cast<const float2 *>(Uc + t * LDB + i);
+                    *reinterpret_cast<float2 *>(Up + t * LDB + i) =
+                        make_float2(u2.x - acc[nt][2 * h], u2.y - acc[nt][2 * h + 1]);
+                }
+        }
+        __syncthreads();
+        if (lo) {
+            float dS[NT][4];
+            zero_frag(dS);
+            mma_tile<true, NT, LDB>(K, Up, dS, m0, lane);  // dS[j][i] = sum_t K[t][j] U'[t][i]
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float2 *pp = reinterpret_cast<float2 *>(STc + frag_row(m0, lane, 2 * h) * LDB +
+                                                            frag_col(0, lane, nt, 0));
                     const float2 v = *pp;
-                    *pp = make_float2(v.x + oacc[nt][2 * h], v.y + oacc[nt][2 * h + 1]);
+                    *pp = make_float2(v.x + dS[nt][2 * h], v.y + dS[nt][2 * h + 1]);
+                }
+        } else {
+            mma_tile<false, NT, LDB>(P, Up, acc, m0, lane, m0 + 16);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = frag_row(m0, lane, 2 * h);
+                    if (t < n)
+                        *reinterpret_cast<float2 *>(o + ((bi * T + c * CH + t) * H + hd) * DD + i0 +
+                                                    frag_col(0, lane, nt, 0)) =
+                            make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
                 }
         }
-        if (c + kStages < nch) {
+        __syncthreads();  // every read of this stage, of U' and of the state slice is done
+        if (c + nst < nch) {
             if (tid == 0) {
                 fence_proxy_async_smem();
-                issue(s, c + kStages);
+                issue(s, c + nst);
             }
             rg.armed(s);
         }
-        __syncthreads();
     }
     if (ST_out != nullptr) {
-        for (int e = tid; e < DD * DD; e += kThreads) {
+        for (int e = tid; e < DD * VS; e += kThreads) {
             const int i = e >> 6, j = e & 63;
-            ST_out[lane_id * DD * DD + e] = ST[j * LD + i];
+            ST_out[lane_id * DD * DD + (i0 + i) * DD + j] = STc[j * LDB + i];
         }
     }
 }
@@ -390,22 +590,63 @@ cudaError_t make_chunk_map(CUtensorMap *m, const float *base, int64_t rows, int6
     return make_tmap(m, base, 3, dims, str, box);
 }
 
+// The workspace as rows of 64 floats (W, U, P of every chunk): boxes of
+// box_x x 64 floats; a box wider than the columns left in the row ends in the
+// tensor map's zero fill (the padded layouts above).
+cudaError_t make_ws_map(CUtensorMap *m, const float *ws, int64_t rows, int box_x) {
+    const uint64_t dims[2] = {uint64_t(DD), uint64_t(rows)};
+    const uint64_t str[1] = {uint64_t(DD) * 4u};
+    const uint32_t box[2] = {uint32_t(box_x), uint32_t(CH)};
+    return make_tmap(m, ws, 2, dims, str, box);
+}
+
+template <int NT>
+cudaError_t launch_state(const CUtensorMap &tQ, const CUtensorMap &tK, const CUtensorMap &tW, float *w,
+                         int64_t chunks, const float *S0, float *o, float *ST, int64_t B, int64_t T, int64_t H,
+                         int nst, const DevCtl &ctl, cudaStream_t s) {
+    constexpr int LDB = StateCols<NT>::LDB, NVB = DD / StateCols<NT>::VS;
+    if (nst == 2 && (T + CH - 1) / CH > 2 && StateSmem(3, LDB).bytes <= 227 * 1024) nst = 3;
+    CUtensorMap tU;
+    cudaError_t e;
+    if ((e = make_ws_map(&tU, w, chunks * 3 * CH, LDB)) != cudaSuccess) return e;
+    const int smem = int(StateSmem(nst, LDB).bytes);
+    if ((e = ensure_smem_attr((const void *)delta_state_kernel<NT>, smem)) != cudaSuccess) return e;
+    delta_state_kernel<NT><<<dim3(unsigned(B * H * NVB)), kThreads, smem, s>>>(tQ, tK, tW, tU, S0, o, ST, B, T, H,
+                                                                               nst, ctl);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
+size_t delta_workspace_bytes(int64_t B, int64_t T, int64_t H) {
+    return size_t(B) * size_t(H) * size_t((T + CH - 1) / CH) * 3 * WSM * sizeof(float);
+}
+
 cudaError_t launch_delta_fwd(const float *q, const float *k, const float *v, const float *beta, const float *S0,
-                             float *o, float *ST, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
+                             float *o, float *ST, int64_t B, int64_t T, int64_t H, void *ws, const DevCtl &ctl,
                              cudaStream_t s) {
-    CUtensorMap tQ, tK, tV;
+    const int64_t nch = (T + CH - 1) / CH, chunks = B * H * nch, lanes = B * H;
+    if (chunks > 0x7fffffff / (3 * CH) || lanes * 8 > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    float *w = static_cast<float *>(ws);
+    CUtensorMap tQ, tK, tV, tW;
     cudaError_t e;
     if ((e = make_chunk_map(&tQ, q, B * T, H)) != cudaSuccess) return e;
     if ((e = make_chunk_map(&tK, k, B * T, H)) != cudaSuccess) return e;
     if ((e = make_chunk_map(&tV, v, B * T, H)) != cudaSuccess) return e;
-    const int64_t blocks = B * H;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const int smem = int(DeltaSmem::bytes);
-    if ((e = ensure_smem_attr((const void *)delta_fwd_kernel, smem)) != cudaSuccess) return e;
-    delta_fwd_kernel<<<dim3(unsigned(blocks)), kThreads, smem, s>>>(tQ, tK, tV, beta, S0, o, ST, B, T, H, ctl);
-    return cudaGetLastError();
+    if ((e = make_ws_map(&tW, w, chunks * 3 * CH, LD)) != cudaSuccess) return e;
+    const int smem_a = int(WySmem::bytes);
+    if ((e = ensure_smem_attr((const void *)delta_wy_kernel, smem_a)) != cudaSuccess) return e;
+    delta_wy_kernel<<<dim3(unsigned(chunks)), kThreads, smem_a, s>>>(tQ, tK, tV, beta, w, B, T, H, ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // State blocks as wide as the lane count allows while still giving about
+    // one block per SM (the per-chunk products are cheapest per column in the
+    // widest blocks; narrow ones shorten the chain when lanes are few).  As
+    // many stages in flight as the chunks and shared memory allow.
+    const int nst = int(min64(nch, 2));
+    if (lanes >= 152) return launch_state<8>(tQ, tK, tW, w, chunks, S0, o, ST, B, T, H, nst, ctl, s);
+    if (lanes >= 76) return launch_state<4>(tQ, tK, tW, w, chunks, S0, o, ST, B, T, H, nst, ctl, s);
+    if (lanes >= 38) return launch_state<2>(tQ, tK, tW, w, chunks, S0, o, ST, B, T, H, nst, ctl, s);
+    return launch_state<1>(tQ, tK, tW, w, chunks, S0, o, ST, B, T, H, nst, ctl, s);
 }
 
 }  // namespace mgs

@@ -60,9 +60,11 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
 cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
                            int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s);
 
-// delta rule forward (head dimension 64)
+// delta rule forward (head dimension 64); the workspace holds W, U and P of
+// every 64-step chunk
+size_t delta_workspace_bytes(int64_t B, int64_t T, int64_t H);
 cudaError_t launch_delta_fwd(const float *q, const float *k, const float *v, const float *beta, const float *S0,
-                             float *o, float *ST, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
+                             float *o, float *ST, int64_t B, int64_t T, int64_t H, void *ws, const DevCtl &ctl,
                              cudaStream_t s);
 
 // Encodes a tiled fp32 tensor map over `base` (rank 2 or 3).  dims and box are

@@ -153,3 +153,15 @@ def test_givens_workspace_only_for_few_lanes_and_long_T(L):
     assert b.mgs_workspace_size(b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, 16, 1024, 8, 8) >= 2 * steps * 256
     th, bb, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
     assert _st(b.mgs_givens_affine_scan_fwd, th, None, bb, None, h, 16, 1024, 8, 8) == b.MGS_ERR_WORKSPACE
+
+
+def test_delta_workspace_size(L):
+    # W, U and tril(Q K^T) of every lane's 64-step chunks, 64 x 64 floats each
+    op = b.MGS_OP_DELTA_SCAN_FWD
+    per_chunk = 3 * 64 * 64 * 4
+    assert b.mgs_workspace_size(op, 128, 64, 1, 64) == 128 * per_chunk
+    assert b.mgs_workspace_size(op, 16, 1024, 1, 64) == 16 * 16 * per_chunk
+    assert b.mgs_workspace_size(op, 2, 70, 3, 64) == 2 * 3 * 2 * per_chunk   # ragged tail: a whole chunk
+    assert b.mgs_workspace_size(op, 2, 0, 3, 64) == 0
+    assert b.mgs_workspace_size(op, 2, 64, 3, 32) == 0                       # D != 64: the call reports it
+    assert b.mgs_workspace_size(op, -1, 64, 3, 64) == 0

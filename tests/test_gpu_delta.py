@@ -74,3 +74,18 @@ def test_delta_degenerate_and_errors():
         b.mgs_delta_scan_fwd(x, x.clone(), x.clone(), torch.zeros((1, 4, 1), device="cuda"), None,
                              torch.empty_like(x), None, 1, 4, 1, 32)
     assert err.value.status == b.MGS_ERR_UNSUPPORTED
+    # the workspace: required, and disjoint from the outputs
+    o = torch.empty_like(d["q"])
+    with pytest.raises(b.MGSError) as err:
+        b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], o, None, 2, 70, 2, 64)
+    assert err.value.status == b.MGS_ERR_WORKSPACE
+    ws, nws = api.workspace(b.MGS_OP_DELTA_SCAN_FWD, 2, 70, 2, 64, "cuda")
+    assert nws == 2 * 2 * 2 * 3 * 64 * 64 * 4
+    with pytest.raises(b.MGSError) as err:
+        b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], o, None, 2, 70, 2, 64, ws, nws // 2)
+    assert err.value.status == b.MGS_ERR_WORKSPACE
+    big = torch.empty(nws // 4 + o.numel(), device="cuda")
+    with pytest.raises(b.MGSError) as err:
+        b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], big[:o.numel()].view(o.shape), None,
+                             2, 70, 2, 64, big, nws)
+    assert err.value.status == b.MGS_ERR_INVALID_ARG
