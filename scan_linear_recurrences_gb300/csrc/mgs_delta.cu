@@ -76,8 +76,8 @@ struct WySmem {
 
 // Shared memory of delta_state_kernel (floats): nst stages of [W P Q K]
 // (padded 64 x 68) and the block's columns of U (64 x LDB); the block's slice
-// of S^T (64 x LDB, key-major), U' (64 x LDB), then kStages barriers and the
-// abort word.
+// of S^T (64 x LDB, key-major), U' (64 x LDB), then kStages "full" and
+// kStages "empty" barriers and the abort word.
 struct StateSmem {
     int stage, st, up, bars;
     size_t bytes;
@@ -86,9 +86,18 @@ struct StateSmem {
         st = nst * stage;
         up = st + DD * ldb;
         bars = up + CH * ldb;
-        bytes = size_t(bars) * 4 + kStages * sizeof(uint64_t) + 16;
+        bytes = size_t(bars) * 4 + 2 * kStages * sizeof(uint64_t) + 16;
     }
 };
+
+constexpr int kStateThreads = kThreads + 32;  // eight compute warps and one copy warp
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the eight compute warps only (the copy warp runs on its own).
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kThreads) : "memory"); }
 
 __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
@@ -276,8 +285,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int64_t nch = (T + CH - 1) / CH;
     const int64_t ci = blockIdx.x;
     if (ci >= B * H * nch) return;
-    const int64_t lane_id = ci / nch, c = ci % nch;
-    const int64_t bi = lane_id / H, hd = lane_id % H;
+    // 32-bit divisions (the grid, the chunk count and H are below 2^31)
+    const int lane32 = int(blockIdx.x) / int(nch);
+    const int64_t lane_id = lane32, c = int64_t(blockIdx.x) - int64_t(lane32) * nch;
+    const int64_t bi = lane32 / int(H), hd = lane32 - int(bi) * int(H);
     const int n = int(min64(CH, T - c * CH));
     const int r = int(bi * T + c * CH);
     float *Wg = ws + ci * 3 * WSM, *Ug = Wg + WSM, *Pg = Wg + 2 * WSM;
@@ -443,8 +454,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 //   warps 0-3: U'[16w..] = U[16w.., i] - W[16w..] S^T[:, i]
 //   warps 4-7: O = Q[16(w-4)..] S^T[:, i], then O += P U' (k up to the diagonal)
 //   warps 0-3: S^T[16w.., i] += K^T U'
+// Warp 8 is the copy warp: it refills a stage by TMA once all eight compute
+// warps have arrived on its "empty" barrier (after their last read of it),
+// so issuing the copies never holds up the compute warps.  Only the copy
+// warp issues copies, so only it drains them when the block gives up.
 template <int NT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kStateThreads)
     delta_state_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmU,
                        const float *__restrict__ S0, float *__restrict__ o, float *__restrict__ ST_out, int64_t B,
@@ -454,48 +469,70 @@ __global__ void __launch_bounds__(kThreads)
     const StateSmem L(nst, LDB);
     float *sm = reinterpret_cast<float *>(smem_raw);
     float *STc = sm + L.st, *Up = sm + L.up;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
-    int *abort_word = reinterpret_cast<int *>(bars + kStages);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + L.bars), *empty = full + kStages;
+    volatile int *abort_word = reinterpret_cast<volatile int *>(empty + kStages);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t blk = blockIdx.x;
     if (blk >= B * H * NVB) return;
     const int64_t lane_id = blk / NVB;
     const int i0 = int(blk % NVB) * VS;
-    const int64_t bi = lane_id / H, hd = lane_id % H;
+    const int64_t bi = int(lane_id) / int(H), hd = int(lane_id) - int(bi) * int(H);  // 32-bit: lanes < 2^31
     const int64_t nch = (T + CH - 1) / CH;
 
     if (tid == 0) {
-        for (int s = 0; s < nst; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kThreads / 32);
+        }
         fence_barrier_init();
         *abort_word = 0;
     }
     __syncthreads();
-    // the lane's state blocks read the same W, P, Q, K (and U rows)
-    const uint64_t pol = policy_evict_normal();
-    auto issue = [&](int s, int64_t c) {  // thread 0 only
-        float *st = sm + s * L.stage;
-        const int r = int(bi * T + c * CH);
-        const int wr = int((lane_id * nch + c) * 3 * CH);  // workspace row of the chunk's W
-        mbar_arrive_expect_tx(&bars[s], uint32_t(L.stage * 4));
-        tma_load_2d(st, &tmW, 0, wr, &bars[s], pol);
-        tma_load_2d(st + MATF, &tmW, 0, wr + 2 * CH, &bars[s], pol);
-        tma_load_3d(st + 2 * MATF, &tmQ, 0, int(hd), r, &bars[s], pol);
-        tma_load_3d(st + 3 * MATF, &tmK, 0, int(hd), r, &bars[s], pol);
-        tma_load_2d(st + 4 * MATF, &tmU, i0, wr + CH, &bars[s], pol);
-    };
-    WarpRing<kStages> rg;  // every thread tracks the ring (all wait on the same barriers)
-    rg.bar = bars;
-    rg.inflight = 0;
-    rg.phase = 0;
-    const int npro = int(min64(nst, nch));
-    if (tid == 0) {
-        prefetch_tmap(&tmW);
-        prefetch_tmap(&tmU);
-        prefetch_tmap(&tmQ);
-        prefetch_tmap(&tmK);
-        for (int s = 0; s < npro; ++s) issue(s, s);
+
+    if (warp == kThreads / 32) {  // the copy warp
+        if (lane == 0) {
+            // the lane's state blocks read the same W, P, Q, K (and U rows)
+            const uint64_t pol = policy_evict_normal();
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmU);
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmK);
+            // stage s and the parity of its "empty" phase to wait for, kept as
+            // counters (no 64-bit division by the run-time stage count)
+            int s = 0;
+            uint32_t eph = 0;
+            int64_t last = -1;
+            for (int64_t c = 0; c < nch; ++c, s = (s + 1 == nst) ? 0 : s + 1) {
+                if (c >= nst) {
+                    // The abort word is written only by compute warps, before a
+                    // barrier of theirs, so that all eight read the same value
+                    // after it; this warp just stops issuing, and their bounded
+                    // waits for the missing stage give up together.
+                    const bool ok = mbar_wait_bounded(&empty[s], eph, ctl.timeout_ns);
+                    if (!ok) record_error(ctl, ERR_MBAR_TIMEOUT);
+                    if (!ok || *abort_word != 0) break;
+                    if (s + 1 == nst) eph ^= 1u;
+                }
+                float *st = sm + s * L.stage;
+                const int r = int(bi * T + c * CH);
+                const int wr = int((lane_id * nch + c) * 3 * CH);  // workspace row of the chunk's W
+                mbar_arrive_expect_tx(&full[s], uint32_t(L.stage * 4));
+                tma_load_2d(st, &tmW, 0, wr, &full[s], pol);
+                tma_load_2d(st + MATF, &tmW, 0, wr + 2 * CH, &full[s], pol);
+                tma_load_3d(st + 2 * MATF, &tmQ, 0, int(hd), r, &full[s], pol);
+                tma_load_3d(st + 3 * MATF, &tmK, 0, int(hd), r, &full[s], pol);
+                tma_load_2d(st + 4 * MATF, &tmU, i0, wr + CH, &full[s], pol);
+                last = c;
+            }
+            // the block's shared memory outlives every copy this warp started
+            bool ok = true;
+            for (int64_t c = last - nst + 1; c <= last; ++c)
+                if (c >= 0 && !mbar_wait_bounded(&full[c % nst], uint32_t((c / nst) & 1), ctl.timeout_ns)) ok = false;
+            if (!ok) record_error(ctl, ERR_DRAIN_TIMEOUT);
+        }
+        return;
     }
-    for (int s = 0; s < npro; ++s) rg.armed(s);
+
     // the slice of the initial state, key-major: STc[j][i] = S0[i0 + i][j]
     for (int e = tid; e < DD * VS; e += kThreads) {
         const int i = e >> 6, j = e & 63;
@@ -504,23 +541,24 @@ __global__ void __launch_bounds__(kThreads)
 
     const bool lo = warp < 4;
     const int m0 = 16 * (warp & 3);
+    int s = 0;          // stage of chunk c
+    uint32_t fph = 0;   // parity of its "full" phase
     for (int64_t c = 0; c < nch; ++c) {
-        const int s = int(c % nst);
-        const int n = int(min64(CH, T - c * CH));
-        if (!rg.wait(s, ctl) && lane == 0) {
+        const int n = c + 1 < nch ? CH : int(T - c * CH);
+        bool ok = mbar_wait_bounded(&full[s], fph, ctl.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok && lane == 0) {
             record_error(ctl, ERR_MBAR_TIMEOUT);
             *abort_word = 1;
         }
-        __syncthreads();
-        if (*abort_word != 0) {
-            rg.drain(ctl, lane);
-            return;
-        }
+        compute_sync();  // also orders the previous chunk's state update before this chunk's reads
+        if (*abort_word != 0) return;
         float *st = sm + s * L.stage;
         const float *W = st, *P = st + MATF, *Q = st + 2 * MATF, *Uc = st + 4 * MATF;
         float *K = st + 3 * MATF;
         // rows of K past the sequence end meet rows of U' that are exactly zero;
-        // zeroed so that whatever they hold contributes nothing
+        // zeroed so that whatever they hold contributes nothing (only the last
+        // chunk is short, and its stage is not refilled)
         if (n < CH)
             for (int e = tid; e < (CH - n) * LD; e += kThreads) K[n * LD + e] = 0.f;
         float acc[NT][4];
@@ -537,11 +575,13 @@ __global__ void __launch_bounds__(kThreads)
                         make_float2(u2.x - acc[nt][2 * h], u2.y - acc[nt][2 * h + 1]);
                 }
         }
-        __syncthreads();
+        compute_sync();
         if (lo) {
             float dS[NT][4];
             zero_frag(dS);
             mma_tile<true, NT, LDB>(K, Up, dS, m0, lane);  // dS[j][i] = sum_t K[t][j] U'[t][i]
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);  // this warp's reads of the stage are done
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -553,6 +593,8 @@ __global__ void __launch_bounds__(kThreads)
                 }
         } else {
             mma_tile<false, NT, LDB>(P, Up, acc, m0, lane, m0 + 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -564,13 +606,12 @@ __global__ void __launch_bounds__(kThreads)
                             make_float2(acc[nt][2 * h], acc[nt][2 * h + 1]);
                 }
         }
-        __syncthreads();  // every read of this stage, of U' and of the state slice is done
-        if (c + nst < nch) {
-            if (tid == 0) {
-                fence_proxy_async_smem();
-                issue(s, c + nst);
-            }
-            rg.armed(s);
+        // U' is rewritten in the next chunk's first phase: every read of it
+        // here must be done first
+        compute_sync();
+        if (++s == nst) {
+            s = 0;
+            fph ^= 1u;
         }
     }
     if (ST_out != nullptr) {
@@ -611,8 +652,8 @@ cudaError_t launch_state(const CUtensorMap &tQ, const CUtensorMap &tK, const CUt
     if ((e = make_ws_map(&tU, w, chunks * 3 * CH, LDB)) != cudaSuccess) return e;
     const int smem = int(StateSmem(nst, LDB).bytes);
     if ((e = ensure_smem_attr((const void *)delta_state_kernel<NT>, smem)) != cudaSuccess) return e;
-    delta_state_kernel<NT><<<dim3(unsigned(B * H * NVB)), kThreads, smem, s>>>(tQ, tK, tW, tU, S0, o, ST, B, T, H,
-                                                                               nst, ctl);
+    delta_state_kernel<NT><<<dim3(unsigned(B * H * NVB)), kStateThreads, smem, s>>>(tQ, tK, tW, tU, S0, o, ST, B,
+                                                                                    T, H, nst, ctl);
     return cudaGetLastError();
 }
 
