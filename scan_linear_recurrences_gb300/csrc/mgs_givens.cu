@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(kBlock)
     const int g_off = L.th_f + (has_a ? L.vec_f : 0), h_off = g_off + L.vec_f;
     const uint32_t stage_tx = uint32_t(L.th_f + nv * L.vec_f) * 4u;
     const uint64_t pol = policy_evict_first();
+    const int lpw_log2 = __ffs(lpw) - 1;
     // Block j covers in-batch rows T-(j+1)*ts .. T-1-j*ts (rows below 0 are
     // skipped); the h box starts one row earlier and holds h_{t-1}.
     auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(kBlock)
                 const int64_t tb = T - (it + 1) * ts;
                 float *xp = xpb + (it & 1) * L.xp_f;
                 for (int q = first_row(it) * lpw + tid - 32; q < ts * lpw; q += kProd) {
-                    const int u = q / lpw, l = q % lpw;
+                    const int u = q >> lpw_log2, l = q & (lpw - 1);  // lpw is a power of two
                     float cs[GN], sv[GN], hv[GK], av[GK];
                     lds_vec<GN>(st + q * GN, cs);
                     lds_vec<GN>(sn + q * GN, sv);
@@ -812,7 +813,18 @@ __global__ void __launch_bounds__(128)
                     float *__restrict__ da, int64_t B, int64_t T, int64_t H) {
     const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;  // (b, t, head)
     if (st >= B * T * H) return;
-    const int64_t hd = st % H, t = (st / H) % T, bi = st / (H * T);
+    int64_t hd, t, bi;
+    if (B * T * H <= 0x7fffffff) {  // 32-bit divisions where the index fits
+        const int s32 = int(st), q = s32 / int(H), b32 = q / int(T);
+        hd = s32 - q * int(H);
+        t = q - b32 * int(T);
+        bi = b32;
+    } else {
+        const int64_t q = st / H;
+        hd = st - q * H;
+        bi = q / T;
+        t = q - bi * T;
+    }
     float cs[GN], sv[GN];
 #pragma unroll
     for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
