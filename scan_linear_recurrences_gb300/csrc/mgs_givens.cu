@@ -739,13 +739,16 @@ __global__ void __launch_bounds__(kBlock)
 // thread per step, fully parallel), runs the time-chunked matrix kernels on it,
 // and turns their output back into angle gradients (again one thread per step).
 
-// The materialising kernel takes kStepBlock consecutive steps per block.  Its
-// angles are staged through shared memory: one coalesced sweep of the
-// block's 28 x kStepBlock angles in, the conversion to cosines and sines spread
-// over all threads with consecutive threads on consecutive words, and each
-// thread then reads its step's 28 pairs back (a 112-byte stride: 8-thread
-// phases of 16-byte reads hit distinct banks).
-constexpr int kStepBlock = 128;
+// The per-column kernels (forming A, the matrix scan's angle gradients) take
+// kColSteps consecutive steps per block, eight threads per step, thread j on
+// column j.  Their angles are staged through shared memory: one coalesced
+// sweep of the block's 28 x kColSteps angles in, the conversion to cosines
+// and sines spread over all threads with consecutive threads on consecutive
+// words, and each thread then reads its step's 28 pairs back (the eight
+// threads of a step read the same words; the four steps of a warp are 112
+// bytes apart, in distinct banks).
+constexpr int kColSteps = 32;
+constexpr int kColBlock = kColSteps * GK;
 
 __device__ __forceinline__ void stage_step_angles(const float *__restrict__ theta, int64_t s0, int nsteps,
                                                   float *cs_sm, float *sn_sm) {
@@ -768,41 +771,30 @@ __device__ __forceinline__ void stage_step_angles(const float *__restrict__ thet
     __syncthreads();
 }
 
-// A_t = G(theta_t) diag(a_t) (a NULL: G(theta_t)), row-major 8 x 8 per step.
-__global__ void __launch_bounds__(kStepBlock)
+// A_t = G(theta_t) diag(a_t) (a NULL: G(theta_t)), row-major 8 x 8 per step:
+// thread j of a step forms column j = a_j G(theta_t) e_j.
+__global__ void __launch_bounds__(kColBlock)
     givens_materialise_kernel(const float *__restrict__ theta, const float *__restrict__ a, float *__restrict__ A,
                               int64_t steps) {
-    __shared__ __align__(16) float cs_sm[kStepBlock * GN], sn_sm[kStepBlock * GN];
-    const int64_t s0 = int64_t(blockIdx.x) * kStepBlock;
-    const int nsteps = int(min64(kStepBlock, steps - s0));
+    __shared__ __align__(16) float cs_sm[kColSteps * GN], sn_sm[kColSteps * GN];
+    const int64_t s0 = int64_t(blockIdx.x) * kColSteps;
+    const int nsteps = int(min64(kColSteps, steps - s0));
     stage_step_angles(theta, s0, nsteps, cs_sm, sn_sm);
-    if (int(threadIdx.x) >= nsteps) return;
-    const int64_t st = s0 + threadIdx.x;
+    const int u = threadIdx.x >> 3, j = threadIdx.x & 7;
+    if (u >= nsteps) return;
+    const int64_t st = s0 + u;
     float cs[GN], sv[GN];
-    lds_vec<GN>(cs_sm + threadIdx.x * GN, cs);
-    lds_vec<GN>(sn_sm + threadIdx.x * GN, sv);
-    float av[GK];
-    if (a != nullptr) {
-        lds_vec<GK>(a + st * GK, av);
-    } else {
+    lds_vec<GN>(cs_sm + u * GN, cs);
+    lds_vec<GN>(sn_sm + u * GN, sv);
+    const float aj = a != nullptr ? a[st * GK + j] : 1.f;
+    float x[GK];
 #pragma unroll
-        for (int i = 0; i < GK; ++i) av[i] = 1.f;
-    }
-    float m[GK][GK];  // m[j] = column j
+    for (int i = 0; i < GK; ++i) x[i] = (i == j) ? aj : 0.f;
+    mesh_apply(x, cs, sv);
+    // for each row, the step's eight threads write its 32 contiguous bytes
+    float *out = A + st * (GK * GK) + j;
 #pragma unroll
-    for (int j = 0; j < GK; ++j) {
-#pragma unroll
-        for (int i = 0; i < GK; ++i) m[j][i] = (i == j) ? av[j] : 0.f;
-        mesh_apply(m[j], cs, sv);
-    }
-    float *out = A + st * (GK * GK);
-#pragma unroll
-    for (int i = 0; i < GK; ++i) {
-        float row[GK];
-#pragma unroll
-        for (int j = 0; j < GK; ++j) row[j] = m[j][i];
-        stg_vec_cs<GK>(out + i * GK, row);
-    }
+    for (int i = 0; i < GK; ++i) st_cs(out + i * GK, x[i]);
 }
 
 // Angle (and gate) gradients of the affine scan from lambda_t (= db_t) and
@@ -878,54 +870,56 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// Angle gradients of the matrix scan from dA_t: d theta_n = <dA_t, dG/dtheta_n>
-// = sum_j mu_j^T (dG/dtheta_n) e_j, one column j at a time: e_j forward
-// through the layers (each layer's output kept), dA_t[:, j] back through them.
-__global__ void __launch_bounds__(128)
-    gms_grad_kernel(const float *__restrict__ theta, const float *__restrict__ dA, float *__restrict__ dth,
-                    int64_t steps) {
-    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (st >= steps) return;
-    float cs[GN], sv[GN];
+// Angle gradients of the matrix scan from dA_t and A_t = G(theta_t) (both in
+// the workspace): d theta_n = <dA_t, dG/dtheta_n> = sum_j mu_j^T (dG/dtheta_n) e_j.
+// Thread j of a step takes column j back through the layers: x = A_t[:, j]
+// (= G e_j; each layer undone by its transposed rotations, exact up to
+// rounding since the mesh is orthogonal) and mu = dA_t[:, j], adding
+// mu_p+1 x_p - mu_p x_p+1 to angle n at its layer; the eight columns' shares
+// are summed by a butterfly reduce-scatter that leaves angles 4j .. 4j+3 with
+// thread j.  Threads past the last step carry zeros through the exchange.
+__global__ void __launch_bounds__(kColBlock)
+    gms_grad_kernel(const float *__restrict__ theta, const float *__restrict__ A, const float *__restrict__ dA,
+                    float *__restrict__ dth, int64_t steps) {
+    __shared__ __align__(16) float cs_sm[kColSteps * GN], sn_sm[kColSteps * GN];
+    const int64_t s0 = int64_t(blockIdx.x) * kColSteps;
+    const int nsteps = int(min64(kColSteps, steps - s0));
+    stage_step_angles(theta, s0, nsteps, cs_sm, sn_sm);
+    const int u = threadIdx.x >> 3, j = threadIdx.x & 7;
+    const bool valid = u < nsteps;
+    const int64_t st = s0 + (valid ? u : 0);
+    float cs[GN], sv[GN], x[GK], mu[GK];
+    lds_vec<GN>(cs_sm + (valid ? u : 0) * GN, cs);
+    lds_vec<GN>(sn_sm + (valid ? u : 0) * GN, sv);
 #pragma unroll
-    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
-    float dthv[GN];
+    for (int i = 0; i < GK; ++i) {
+        x[i] = valid ? A[st * (GK * GK) + i * GK + j] : 0.f;
+        mu[i] = valid ? __ldcs(dA + st * (GK * GK) + i * GK + j) : 0.f;
+    }
+    float d[32];
 #pragma unroll
-    for (int n = 0; n < GN; ++n) dthv[n] = 0.f;
-    // the step's whole dA (256 contiguous bytes) in sixteen 16-byte loads
-    float g[GK * GK];
-    lds_vec<GK * GK>(dA + st * (GK * GK), g);
+    for (int l = GK - 1; l >= 0; --l) {
 #pragma unroll
-    for (int j = 0; j < GK; ++j) {
-        float xl[GK][GK], mu[GK];
-#pragma unroll
-        for (int i = 0; i < GK; ++i) {
-            xl[0][i] = (i == j) ? 1.f : 0.f;
-            mu[i] = g[i * GK + j];
-        }
-#pragma unroll
-        for (int l = 0; l < GK; ++l) {
-            if (l > 0) {
-#pragma unroll
-                for (int i = 0; i < GK; ++i) xl[l][i] = xl[l - 1][i];
-            }
-#pragma unroll
-            for (int q = 0; q < layer_pairs(l); ++q) {
-                const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-                rot_fwd(xl[l][p], xl[l][p + 1], cs[n], sv[n]);
-            }
-        }
-#pragma unroll
-        for (int l = GK - 1; l >= 0; --l) {
-#pragma unroll
-            for (int q = 0; q < layer_pairs(l); ++q) {
-                const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-                dthv[n] = fmaf(mu[p + 1], xl[l][p], fmaf(-mu[p], xl[l][p + 1], dthv[n]));
-                rot_bwd(mu[p], mu[p + 1], cs[n], sv[n]);
-            }
+        for (int q = 0; q < layer_pairs(l); ++q) {
+            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+            d[n] = fmaf(mu[p + 1], x[p], -mu[p] * x[p + 1]);
+            rot_bwd(x[p], x[p + 1], cs[n], sv[n]);
+            rot_bwd(mu[p], mu[p + 1], cs[n], sv[n]);
         }
     }
-    stg_vec_cs<GN>(dth + st * GN, dthv);
+#pragma unroll
+    for (int n = GN; n < 32; ++n) d[n] = 0.f;
+#pragma unroll
+    for (int o = 4, half = 16; o >= 1; o >>= 1, half >>= 1) {
+        const bool up = (j & o) != 0;
+#pragma unroll
+        for (int c = 0; c < half; ++c) {
+            const float send = up ? d[c] : d[c + half];
+            const float keep = up ? d[c + half] : d[c];
+            d[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    if (valid && j < GN / 4) st_cs4(dth + st * GN + 4 * j, make_float4(d[0], d[1], d[2], d[3]));
 }
 
 // Lanes per recurrence warp for the affine scan: as many as keep at least
@@ -968,7 +962,7 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     if (few_lane_path(B, T, H)) {
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, a, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, a, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_mas_fwd(GK, A, b, h0, h, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
@@ -1003,7 +997,7 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
         float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, a, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, a, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if ((e = launch_mas_bwd(GK, A, h0, h, gh, dA, db, dh0, B, T, H, static_cast<char *>(ws) + 2 * mb,
@@ -1038,7 +1032,7 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
     if (few_lane_path(B, T, H)) {
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, nullptr, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, nullptr, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         return launch_ms_fwd(GK, A, P, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
@@ -1061,13 +1055,13 @@ cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, f
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
         float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, kStepBlock), kStepBlock, 0, s>>>(theta, nullptr, A, B * T * H);
+        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, nullptr, A, B * T * H);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if ((e = launch_ms_bwd(GK, A, P, G, dA, B, T, H, static_cast<char *>(ws) + 2 * mb, ws_bytes - 2 * mb, ctl,
                                s)) != cudaSuccess)
             return e;
-        gms_grad_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, dA, dth, B * T * H);
+        gms_grad_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, A, dA, dth, B * T * H);
         return cudaGetLastError();
     }
     using TM = MatTile<GK, true>;
