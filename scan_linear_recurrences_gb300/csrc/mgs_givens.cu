@@ -39,8 +39,13 @@ constexpr int GK = 8;                  // coordinates per head
 constexpr int GN = GK * (GK - 1) / 2;  // angles per head and step
 constexpr int kItems = 64;             // (lane, step) items per affine-scan stage
 constexpr int kNS = 3;                 // stages in flight
-constexpr int kBlock = 128;            // threads per block: 1 recurrence warp + 3 angle warps
-constexpr int kProd = kBlock - 32;     // angle threads
+// Threads per block of the fused kernels: one recurrence warp and the angle
+// warps, three in the forward kernels and four in the backward ones, whose
+// angle warps also run the affine scan's forward pass through the layers
+// (measured at the lab shape: affine backward 31.0 -> 24.8 us with the fourth
+// warp; the forward kernels gain nothing from a fourth or fifth).
+constexpr int kBlockF = 128, kBlockB = 160;
+constexpr int kProdF = kBlockF - 32, kProdB = kBlockB - 32;  // angle threads
 constexpr int kGasMaxLanes = 8;        // affine-scan lanes per recurrence warp, at most
 constexpr int kGmsLanes = 4;           // heads per block in the matrix scan (8 threads each)
 constexpr int kGmsFwdTS = 16, kGmsBwdTS = 8;
@@ -121,12 +126,14 @@ __device__ __forceinline__ void unbiased_cos_sin(float theta, float &c, float &s
     s = (2.f * t) * r;
 }
 
-// Angles [lo, hi) of a stage converted by the block's angle threads (pt = 0 ..
-// kProd-1): cosines in place, sines to sn; consecutive threads take
+// Angles [lo, hi) of a stage converted by the block's NP angle threads
+// (pt = 0 .. NP-1): cosines in place, sines to sn; consecutive threads take
 // consecutive words.
 // Four angles per thread and round are independent chains, which the
 // scheduler interleaves (one chain alone is a long run of dependent ops).
+template <int NP>
 __device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi, int pt) {
+    constexpr int kProd = NP;
     int i = lo + pt;
     for (; i + 3 * kProd < hi; i += 4 * kProd) {
         float x[4], c[4], s[4];
@@ -213,7 +220,7 @@ struct GasSmem {
 };
 
 // ---------------------------------------------------------------- affine forward
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlockF)
     gas_fwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const float *__restrict__ h0, float *__restrict__ h,
                    int64_t B, int64_t T, int64_t H, int64_t groups_per_b, int lpw, int ts, int has_a,
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(kBlock)
     const int b_off = L.th_f + (has_a ? L.vec_f : 0);
     const uint32_t stage_tx = uint32_t(L.th_f + (has_a ? 2 : 1) * L.vec_f) * 4u;
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlockF-1 only
         float *st = ring + size_t(s) * L.stage_f;
         const int r = row0 + int(j * ts);
         mbar_arrive_expect_tx(&bars[s], stage_tx);
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(kBlock)
         tma_load_3d(st + b_off, &tmB, 0, head0, r, &bars[s], pol);
     };
     const int npro = int(min64(kNS, nblk));
-    if (tid == kBlock - 1) {
+    if (tid == kBlockF - 1) {
         prefetch_tmap(&tmTh);
         prefetch_tmap(&tmB);
         if (has_a) prefetch_tmap(&tmA);
@@ -270,7 +277,7 @@ __global__ void __launch_bounds__(kBlock)
         if (producer && it < nblk) {
             const int s = int(it % kNS);
             if (br.rg.wait(s, ctl)) {
-                angle_range(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0,
+                angle_range<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0,
                             int(min64(ts, T - it * ts)) * lpw * GN, tid - 32);
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
@@ -305,7 +312,7 @@ __global__ void __launch_bounds__(kBlock)
         MGS_BLOCK_ABORT_CHECK(br, producer, lane);
         if (it >= 1 && it - 1 + kNS < nblk) {
             const int s = int((it - 1) % kNS);
-            if (tid == kBlock - 1) {
+            if (tid == kBlockF - 1) {
                 fence_proxy_async_smem();
                 issue(s, it - 1 + kNS);
             }
@@ -326,7 +333,7 @@ __global__ void __launch_bounds__(kBlock)
 // for the next stage together with its angle conversion and leave the 28
 // rotated pairs per step in shared memory; the recurrence warp's chain per
 // step is then only the transposed rotations of mu.
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlockB)
     gas_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
                    const float *__restrict__ h0, float *__restrict__ dth, float *__restrict__ da,
@@ -356,7 +363,7 @@ __global__ void __launch_bounds__(kBlock)
     const int lpw_log2 = __ffs(lpw) - 1;
     // Block j covers in-batch rows T-(j+1)*ts .. T-1-j*ts (rows below 0 are
     // skipped); the h box starts one row earlier and holds h_{t-1}.
-    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlockB-1 only
         float *st = ring + size_t(s) * L.stage_f;
         const int r = int(bi * T + T - (j + 1) * ts);
         mbar_arrive_expect_tx(&bars[s], stage_tx);
@@ -366,7 +373,7 @@ __global__ void __launch_bounds__(kBlock)
         tma_load_3d(st + h_off, &tmH, 0, head0, r - 1, &bars[s], pol);
     };
     const int npro = int(min64(kNS, nblk));
-    if (tid == kBlock - 1) {
+    if (tid == kBlockB - 1) {
         prefetch_tmap(&tmTh);
         prefetch_tmap(&tmG);
         prefetch_tmap(&tmH);
@@ -395,18 +402,18 @@ __global__ void __launch_bounds__(kBlock)
             float *st = ring + size_t(s) * L.stage_f;
             float *sn = snb + (it & 1) * L.sin_f;
             if (br.rg.wait(s, ctl)) {
-                angle_range(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
+                angle_range<kProdB>(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
                 *br.abort_word = 1;
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(kProd) : "memory");  // angle warps only
+            asm volatile("bar.sync 1, %0;" ::"r"(kProdB) : "memory");  // angle warps only
             if (*br.abort_word == 0) {
                 // the forward pass through the layers of every step of the
                 // stage: x = a_t * h_{t-1}, each rotation's output pair kept
                 const int64_t tb = T - (it + 1) * ts;
                 float *xp = xpb + (it & 1) * L.xp_f;
-                for (int q = first_row(it) * lpw + tid - 32; q < ts * lpw; q += kProd) {
+                for (int q = first_row(it) * lpw + tid - 32; q < ts * lpw; q += kProdB) {
                     const int u = q >> lpw_log2, l = q & (lpw - 1);  // lpw is a power of two
                     float cs[GN], sv[GN], hv[GK], av[GK];
                     lds_vec<GN>(st + q * GN, cs);
@@ -502,7 +509,7 @@ __global__ void __launch_bounds__(kBlock)
         MGS_BLOCK_ABORT_CHECK(br, producer, lane);
         if (it >= 1 && it - 1 + kNS < nblk) {
             const int s = int((it - 1) % kNS);
-            if (tid == kBlock - 1) {
+            if (tid == kBlockB - 1) {
                 fence_proxy_async_smem();
                 issue(s, it - 1 + kNS);
             }
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(kBlock)
 
 // ---------------------------------------------------------------- matrix forward
 // Warp 0's thread j of a lane's 8-thread group carries column j of P_t.
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlockF)
     gms_fwd_kernel(const __grid_constant__ CUtensorMap tmTh, float *__restrict__ P, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
     constexpr int TS = kGmsFwdTS;
@@ -541,12 +548,12 @@ __global__ void __launch_bounds__(kBlock)
     const int64_t nblk = (T + TS - 1) / TS;
     const int row0 = int(bi * T);
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlockF-1 only
         mbar_arrive_expect_tx(&bars[s], uint32_t(STAGEF * 4));
         tma_load_3d(ring + size_t(s) * STAGEF, &tmTh, 0, head0, row0 + int(j * TS), &bars[s], pol);
     };
     const int npro = int(min64(kNS, nblk));
-    if (tid == kBlock - 1) {
+    if (tid == kBlockF - 1) {
         prefetch_tmap(&tmTh);
         for (int s = 0; s < npro; ++s) issue(s, s);
     }
@@ -562,7 +569,7 @@ __global__ void __launch_bounds__(kBlock)
         if (producer && it < nblk) {
             const int s = int(it % kNS);
             if (br.rg.wait(s, ctl)) {
-                angle_range(ring + size_t(s) * STAGEF, snb + (it & 1) * STAGEF, 0,
+                angle_range<kProdF>(ring + size_t(s) * STAGEF, snb + (it & 1) * STAGEF, 0,
                             int(min64(TS, T - it * TS)) * kGmsLanes * GN, tid - 32);
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
@@ -591,7 +598,7 @@ __global__ void __launch_bounds__(kBlock)
         MGS_BLOCK_ABORT_CHECK(br, producer, lane);
         if (it >= 1 && it - 1 + kNS < nblk) {
             const int s = int((it - 1) % kNS);
-            if (tid == kBlock - 1) {
+            if (tid == kBlockF - 1) {
                 fence_proxy_async_smem();
                 issue(s, it - 1 + kNS);
             }
@@ -607,7 +614,7 @@ __global__ void __launch_bounds__(kBlock)
 // is orthogonal), each thread adding its column's share of every angle's
 // gradient; the eight shares are summed by a butterfly reduce-scatter that
 // leaves angles 4j .. 4j+3 with thread j.  carry = A_t^T Lambda[:, j].
-__global__ void __launch_bounds__(kBlock)
+__global__ void __launch_bounds__(kBlockB)
     gms_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmP,
                    const __grid_constant__ CUtensorMap tmG, float *__restrict__ dth, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kBlock)
     const bool active = !producer && head0 + sub < H;
     const int64_t nblk = (T + TS - 1) / TS;
     const uint64_t pol = policy_evict_first();
-    auto issue = [&](int s, int64_t j) {  // thread kBlock-1 only
+    auto issue = [&](int s, int64_t j) {  // thread kBlockB-1 only
         float *st = ring + size_t(s) * STAGEF;
         const int r = int(bi * T + T - (j + 1) * TS);
         mbar_arrive_expect_tx(&bars[s], uint32_t((2 * MATF + THF) * 4));
@@ -642,7 +649,7 @@ __global__ void __launch_bounds__(kBlock)
         tma_load_3d(st + 2 * MATF, &tmTh, 0, head0, r, &bars[s], pol);
     };
     const int npro = int(min64(kNS, nblk));
-    if (tid == kBlock - 1) {
+    if (tid == kBlockB - 1) {
         prefetch_tmap(&tmTh);
         prefetch_tmap(&tmP);
         prefetch_tmap(&tmG);
@@ -663,7 +670,7 @@ __global__ void __launch_bounds__(kBlock)
         if (producer && it < nblk) {
             const int s = int(it % kNS);
             if (br.rg.wait(s, ctl)) {
-                angle_range(ring + size_t(s) * STAGEF + 2 * MATF, snb + (it & 1) * THF,
+                angle_range<kProdB>(ring + size_t(s) * STAGEF + 2 * MATF, snb + (it & 1) * THF,
                             first_row(it) * kGmsLanes * GN, THF, tid - 32);
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
@@ -723,7 +730,7 @@ __global__ void __launch_bounds__(kBlock)
         MGS_BLOCK_ABORT_CHECK(br, producer, lane);
         if (it >= 1 && it - 1 + kNS < nblk) {
             const int s = int((it - 1) % kNS);
-            if (tid == kBlock - 1) {
+            if (tid == kBlockB - 1) {
                 fence_proxy_async_smem();
                 issue(s, it - 1 + kNS);
             }
@@ -982,7 +989,7 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(GasSmem(lpw, ts, a ? 2 : 1).bytes());
     if ((e = ensure_smem_attr((const void *)gas_fwd_kernel, smem)) != cudaSuccess) return e;
-    gas_fwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts,
+    gas_fwd_kernel<<<dim3(unsigned(blocks)), kBlockF, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts,
                                                                 a != nullptr, ctl);
     return cudaGetLastError();
 }
@@ -1022,7 +1029,7 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(GasSmem(lpw, ts, a ? 3 : 2, true).bytes());
     if ((e = ensure_smem_attr((const void *)gas_bwd_kernel, smem)) != cudaSuccess) return e;
-    gas_bwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H,
+    gas_bwd_kernel<<<dim3(unsigned(blocks)), kBlockB, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H,
                                                                 gpb, lpw, ts, a != nullptr, ctl);
     return cudaGetLastError();
 }
@@ -1045,7 +1052,7 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
     constexpr int STAGEF = kGmsFwdTS * kGmsLanes * GN;
     const int smem = int((kNS + 2) * STAGEF * 4 + kNS * sizeof(uint64_t) + 16);
     if ((e = ensure_smem_attr((const void *)gms_fwd_kernel, smem)) != cudaSuccess) return e;
-    gms_fwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, P, B, T, H, gpb, ctl);
+    gms_fwd_kernel<<<dim3(unsigned(blocks)), kBlockF, smem, s>>>(tTh, P, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
@@ -1076,7 +1083,7 @@ cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, f
     constexpr int STAGEF = int(align_up(size_t(2 * MATF + THF), TM::kAlign / 4));
     const int smem = int(size_t(kNS * STAGEF + 2 * THF) * 4 + kNS * sizeof(uint64_t) + 16 + TM::kAlign);
     if ((e = ensure_smem_attr((const void *)gms_bwd_kernel, smem)) != cudaSuccess) return e;
-    gms_bwd_kernel<<<dim3(unsigned(blocks)), kBlock, smem, s>>>(tTh, tP, tG, dth, B, T, H, gpb, ctl);
+    gms_bwd_kernel<<<dim3(unsigned(blocks)), kBlockB, smem, s>>>(tTh, tP, tG, dth, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
