@@ -662,6 +662,35 @@ def run_gpu(args):
                 "GBps": round(nbytes / (bm * 1e-3) / 1e9, 1),
                 "bytes": "28 per element + checkpoints", "l2": "flushed"}
             del ws
+        # matrix_affine_scan backward in recompute mode (h not saved) on the
+        # scaled shape: per step A and b read by both passes, grad_h read,
+        # dA and db written (4 (2k^2 + 2k + k + k^2 + k) = 896 bytes at k = 8),
+        # plus h0 read, dh0 written and the checkpoints written and read
+        for r in runners:
+            w = r.w
+            if w.op != "mas" or w.cid != 4:
+                continue
+            d = r.inp
+            ws, nws = api.workspace(b.MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE, w.B, w.T, w.H, w.k, device)
+            ts = []
+            for it in range(args.warmup + 10):
+                e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+                e0.record(stream)
+                b.mgs_matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"], r.dA, r.db, r.dh0,
+                                                       w.B, w.T, w.H, w.k, ws, nws, sid)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    ts.append(e0.elapsed_time(e1))
+            bm = statistics.median(ts)
+            k = w.k
+            nbytes = w.B * w.T * w.H * 4 * (3 * k * k + 4 * k) + 2 * w.B * w.H * k * 4 + 2 * nws
+            extra[f"mas_c{w.cid}_bwd_recompute"] = {
+                "shape": w.name, "bwd_us": round(bm * 1e3, 2), "workspace_bytes": nws,
+                "GBps": round(nbytes / (bm * 1e-3) / 1e9, 1), "pct_of_peak": round(100 * nbytes / (bm * 1e-3) / 1e9 /
+                                                                                   measured_peak()[0], 1),
+                "bytes": f"{4 * (3 * k * k + 4 * k)} per step + checkpoints", "l2": "inputs larger than L2"}
+            del ws
         b.mgs_check(sid)
         extra["givens_peak_memory"] = givens_peak_memory(torch, api, device)
 

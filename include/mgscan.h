@@ -77,14 +77,16 @@ enum {
     MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10,
     MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11,
     MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12,
-    MGS_OP_DELTA_SCAN_FWD = 13
+    MGS_OP_DELTA_SCAN_FWD = 13,
+    MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE = 14
 };
 
 /* Bytes of device workspace `op` needs for this shape (H_or_D is H for the
  * matrix ops and D for parallel_scan_log; k is ignored for the latter).
  * Returns 0 when no workspace is needed, and also for invalid shapes (the
  * entry point then reports the error).  MGS_OP_PARALLEL_SCAN_LOG_BWD gives the
- * bytes of the recompute mode (h == NULL); with h saved it needs none. */
+ * bytes of the recompute mode (h == NULL); with h saved it needs none.
+ * MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE is the recompute-mode entry point's. */
 size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k);
 
 /* matrix_affine_scan, forward ("mingru-scans" home page, scan-op table,
@@ -110,6 +112,24 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
                                       const float *grad_h, float *dA, float *db, float *dh0,
                                       int64_t B, int64_t T, int64_t H, int k, void *workspace,
                                       size_t workspace_bytes, mgs_stream_t stream);
+
+/* matrix_affine_scan, backward in recompute mode: the same gradients as
+ * mgs_matrix_affine_scan_bwd without the saved forward output (the pages'
+ * scans keep memory down by recomputing the forward in the backward).  The
+ * call runs the forward over each lane's sequence keeping only h at the start
+ * of every chunk of TS steps (TS = 8 for k = 8) in the workspace, then walks
+ * the chunks downwards, recomputing each chunk's h from its checkpoint before
+ * taking the adjoint back over it.  Reads A and b twice and grad_h once per
+ * step (896 bytes per step at k = 8, against 608 with h saved).
+ * In: A, b (the forward's inputs), h0 (nullable: zero initial state), grad_h.
+ * Out: dA, db, dh0 (nullable: not written), as mgs_matrix_affine_scan_bwd.
+ * Workspace: mgs_workspace_size(MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE, B, T,
+ * H, k) bytes (the checkpoints: 1/TS of the size of h, rounded up per group
+ * of 32/k heads), disjoint from every other argument. */
+mgs_status mgs_matrix_affine_scan_bwd_recompute(const float *A, const float *b, const float *h0,
+                                                const float *grad_h, float *dA, float *db, float *dh0,
+                                                int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                                size_t workspace_bytes, mgs_stream_t stream);
 
 /* matrix_scan, forward ("mingru-scans" home page, scan-op table, matrix_scan
  * row): prefix products

@@ -37,6 +37,7 @@ MGS_OP_GIVENS_AFFINE_SCAN_BWD = 10
 MGS_OP_GIVENS_MATRIX_SCAN_FWD = 11
 MGS_OP_GIVENS_MATRIX_SCAN_BWD = 12
 MGS_OP_DELTA_SCAN_FWD = 13
+MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE = 14
 
 
 class MGSError(RuntimeError):
@@ -58,6 +59,8 @@ _SIGNATURES = {
     "mgs_workspace_size": (_sz, [_int, _i64, _i64, _i64, _int]),
     "mgs_matrix_affine_scan_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_matrix_affine_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
+    "mgs_matrix_affine_scan_bwd_recompute": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
+                                                    _sz, _vp]),
     "mgs_matrix_scan_fwd": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
     "mgs_matrix_scan_fwd_noalloc": (_int, [_vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "mgs_matrix_scan_bwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _sz, _vp]),
@@ -139,6 +142,12 @@ def mgs_matrix_affine_scan_fwd(A, b, h0, h, B, T, H, k, workspace=None, workspac
 def mgs_matrix_affine_scan_bwd(A, h0, h, grad_h, dA, db, dh0, B, T, H, k, workspace=None,
                                workspace_bytes=0, stream=None):
     return _call("mgs_matrix_affine_scan_bwd", _ptr(A), _ptr(h0), _ptr(h), _ptr(grad_h), _ptr(dA),
+                 _ptr(db), _ptr(dh0), B, T, H, k, _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def mgs_matrix_affine_scan_bwd_recompute(A, b, h0, grad_h, dA, db, dh0, B, T, H, k, workspace=None,
+                                         workspace_bytes=0, stream=None):
+    return _call("mgs_matrix_affine_scan_bwd_recompute", _ptr(A), _ptr(b), _ptr(h0), _ptr(grad_h), _ptr(dA),
                  _ptr(db), _ptr(dh0), B, T, H, k, _ptr(workspace), workspace_bytes, _stream(stream))
 
 

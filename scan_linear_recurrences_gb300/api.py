@@ -59,6 +59,21 @@ def matrix_affine_scan_bwd(A, h0, h, grad_h, need_dh0=True, stream=None):
     return dA, db, dh0
 
 
+def matrix_affine_scan_bwd_recompute(A, b, h0, grad_h, need_dh0=True, stream=None):
+    """The same gradients as matrix_affine_scan_bwd without the saved h: the
+    call recomputes the forward from A, b and h0 (checkpoints in a workspace)."""
+    B, T, H, k = b.shape
+    _check(A, "A", (B, T, H, k, k)); _check(b, "b"); _check(grad_h, "grad_h", (B, T, H, k))
+    if h0 is not None:
+        _check(h0, "h0", (B, H, k))
+    dA = torch.empty_like(A)
+    db = torch.empty_like(b)
+    dh0 = torch.empty((B, H, k), dtype=torch.float32, device=b.device) if need_dh0 else None
+    ws, nws = workspace(_b.MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE, B, T, H, k, b.device)
+    _b.mgs_matrix_affine_scan_bwd_recompute(A, b, h0, grad_h, dA, db, dh0, B, T, H, k, ws, nws, stream)
+    return dA, db, dh0
+
+
 # ---------------------------------------------------------------- matrix_scan
 def matrix_scan_fwd(A, out=None, stream=None):
     """P_t = A_t P_{t-1}, P_0 = I.  A [B,T,H,k,k]."""
@@ -215,23 +230,28 @@ def linear_scan_bwd(a, h0, h, grad_h, need_dh0=True, stream=None):
 
 # ---------------------------------------------------------------- autograd wrappers
 class MatrixAffineScan(torch.autograd.Function):
-    """h = matrix_affine_scan(A, b, h0) with the library's fused backward."""
+    """h = matrix_affine_scan(A, b, h0) with the library's fused backward;
+    recompute=True saves b instead of h and the backward rebuilds h."""
 
     @staticmethod
-    def forward(ctx, A, b, h0=None):
+    def forward(ctx, A, b, h0=None, recompute=False):
         A, b = A.contiguous(), b.contiguous()
         h0c = h0.contiguous() if h0 is not None else None
         h = matrix_affine_scan_fwd(A, b, h0c)
-        ctx.save_for_backward(A, h0c if h0c is not None else torch.empty(0, device=b.device), h)
+        ctx.save_for_backward(A, h0c if h0c is not None else torch.empty(0, device=b.device), b if recompute else h)
         ctx.has_h0 = h0 is not None
+        ctx.recompute = recompute
         return h
 
     @staticmethod
     def backward(ctx, grad_h):
-        A, h0, h = ctx.saved_tensors
+        A, h0, x = ctx.saved_tensors
         h0 = h0 if ctx.has_h0 else None
-        dA, db, dh0 = matrix_affine_scan_bwd(A, h0, h, grad_h.contiguous(), need_dh0=ctx.has_h0)
-        return dA, db, dh0
+        if ctx.recompute:
+            dA, db, dh0 = matrix_affine_scan_bwd_recompute(A, x, h0, grad_h.contiguous(), need_dh0=ctx.has_h0)
+        else:
+            dA, db, dh0 = matrix_affine_scan_bwd(A, h0, x, grad_h.contiguous(), need_dh0=ctx.has_h0)
+        return dA, db, dh0, None
 
 
 class MatrixScan(torch.autograd.Function):
@@ -335,8 +355,9 @@ def linear_scan(a, b, h0=None):
     return LinearScan.apply(a, b, h0)
 
 
-def matrix_affine_scan(A, b, h0=None):
-    return MatrixAffineScan.apply(A, b, h0)
+def matrix_affine_scan(A, b, h0=None, recompute=False):
+    """recompute=True keeps b rather than h for backward; backward rebuilds h."""
+    return MatrixAffineScan.apply(A, b, h0, recompute)
 
 
 def matrix_scan(A):

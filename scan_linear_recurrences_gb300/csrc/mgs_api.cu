@@ -199,6 +199,9 @@ size_t mgs_workspace_size(int op, int64_t B, int64_t T, int64_t H_or_D, int k) {
         case MGS_OP_LINEAR_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, 1, &s) != MGS_OK) return 0;
             return mgs::mas_workspace_bytes(B, T, H_or_D, 1);
+        case MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE:
+            if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK || s.vec == 0) return 0;
+            return mgs::mas_rc_workspace_bytes(B, T, H_or_D, k);
         case MGS_OP_MATRIX_SCAN_FWD:
         case MGS_OP_MATRIX_SCAN_BWD:
             if (block_sizes(B, T, H_or_D, k, &s) != MGS_OK) return 0;
@@ -268,6 +271,37 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
     return from_cuda(mgs::launch_mas_bwd(k, A, h0, h, grad_h, dA, db, dh0, B, T, H, workspace, workspace_bytes,
                                          ctl, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mgs_status mgs_matrix_affine_scan_bwd_recompute(const float *A, const float *b, const float *h0,
+                                                const float *grad_h, float *dA, float *db, float *dh0,
+                                                int64_t B, int64_t T, int64_t H, int k, void *workspace,
+                                                size_t workspace_bytes, mgs_stream_t stream) {
+    BlockSizes s;
+    mgs_status st = block_sizes(B, T, H, k, &s);
+    if (st != MGS_OK) return st;
+    if (s.init == 0) return MGS_OK;
+    if (s.vec == 0) {
+        // T == 0: lambda is empty, the initial-state gradient is zero
+        if (dh0 == nullptr) return MGS_OK;
+        if ((st = check_ptrs({dh0}, {})) != MGS_OK) return st;
+        return from_cuda(cudaMemsetAsync(dh0, 0, size_t(s.init) * sizeof(float),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+    }
+    if ((st = check_ptrs({A, b, grad_h, dA, db}, {h0, dh0})) != MGS_OK) return st;
+    if (!disjoint({{dA, s.mat}, {db, s.vec}, {dh0, dh0 ? s.init : 0}},
+                  {{A, s.mat}, {b, s.vec}, {h0, h0 ? s.init : 0}, {grad_h, s.vec}}))
+        return MGS_ERR_INVALID_ARG;
+    const size_t need = mgs::mas_rc_workspace_bytes(B, T, H, k);
+    if ((st = check_ws(need, workspace, workspace_bytes)) != MGS_OK) return st;
+    if (!disjoint({{static_cast<float *>(workspace), int64_t(need / sizeof(float))}},
+                  {{A, s.mat}, {b, s.vec}, {h0, h0 ? s.init : 0}, {grad_h, s.vec}, {dA, s.mat}, {db, s.vec},
+                   {dh0, dh0 ? s.init : 0}}))
+        return MGS_ERR_INVALID_ARG;
+    mgs::DevCtl ctl;
+    if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    return from_cuda(mgs::launch_mas_bwd_recompute(k, A, b, h0, grad_h, dA, db, dh0, B, T, H, workspace, ctl,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,

@@ -19,6 +19,11 @@ cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *
                            const float *gh, float *dA, float *db, float *dh0, int64_t B,
                            int64_t T, int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl,
                            cudaStream_t s);
+// recompute-mode backward (h not saved): checkpoints in the workspace
+size_t mas_rc_workspace_bytes(int64_t B, int64_t T, int64_t H, int K);
+cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, const float *h0, const float *gh,
+                                     float *dA, float *db, float *dh0, int64_t B, int64_t T, int64_t H, void *ws,
+                                     const DevCtl &ctl, cudaStream_t s);
 
 // matrix_scan
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);

@@ -301,6 +301,245 @@ __global__ void __launch_bounds__(32)
     if (dh0 != nullptr && active) dh0[(bi * H + head0 + sub) * K + row] = mu;
 }
 
+// ---------------------------------------------------------------- recompute-mode backward
+// The backward without the saved forward output.  Phase A runs the forward
+// over the warp's whole sequence (A and b streamed as in mas_fwd_kernel),
+// keeping only h at the start of every chunk of RC = TS steps (one stage), in
+// the workspace.  Phase B walks the chunks downwards, each chunk's stage of
+// A, b and g resident in shared memory while the ring's other slots take the
+// next chunks down: the chunk's h is recomputed forward from its checkpoint
+// into shared memory, then the adjoint runs back over the chunk as in
+// mas_bwd_kernel.  Per step A and b are read twice and g once, dA and db are
+// written once; h is never stored.
+template <int K>
+struct MasRc {
+    using S = MasShape<K>;
+    static constexpr int RS = 1;           // stages per chunk
+    static constexpr int RC = RS * S::TS;  // steps per chunk
+    static constexpr int NS = 4;           // ring slots: chunk c in slot c % NS
+    static constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
+    static constexpr int STAGEF = A_STAGE + 2 * V_STAGE;  // A_t, b_t, g_t
+    using R = Ring<STAGEF, NS, S::TA::kAlign>;
+    static constexpr size_t hs_off = align_up(R::ring_bytes + NS * sizeof(uint64_t), 128);
+    // h of a chunk: row 0 the state before it, row u+1 the state after its step u
+    static constexpr size_t warp_bytes = hs_off + size_t(RC + 1) * S::VF * sizeof(float) + S::TA::kAlign;
+};
+
+template <int K>
+__global__ void __launch_bounds__(32)
+    mas_bwd_rc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmG, const float *__restrict__ h0,
+                      float *__restrict__ ck, float *__restrict__ dA, float *__restrict__ db,
+                      float *__restrict__ dh0, int64_t B, int64_t T, int64_t H, int64_t groups_per_b,
+                      DevCtl ctl) {
+    using M = MasRc<K>;
+    using S = typename M::S;
+    using R = typename M::R;
+    constexpr int NS = M::NS, TS = S::TS, RC = M::RC, VF = S::VF;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
+    if (g >= B * groups_per_b) return;
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::ring_bytes);
+    float *hs = reinterpret_cast<float *>(sbase + M::hs_off);
+
+    const int64_t bi = g / groups_per_b;
+    const int head0 = int(g % groups_per_b) * S::LPW;
+    const int nl = int(min64(S::LPW, H - head0));
+    const int sub = lane / K, row = lane % K, gbase = lane & ~(K - 1);
+    const bool active = sub < nl;
+    const int row0 = int(bi * T);
+    const int64_t nblk = (T + TS - 1) / TS;  // phase A stages
+    const int64_t nck = (T + RC - 1) / RC;   // chunks
+    float *ckp = ck + g * nck * VF + lane;   // the group's checkpoints; lane = sub * K + row
+
+    WarpRing<NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmG);
+    }
+
+    // ---- phase A: the forward, checkpoints only
+    auto issue_f = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * SSTR;
+        mbar_arrive_expect_tx(&bars[s], uint32_t((M::A_STAGE + M::V_STAGE) * sizeof(float)));
+        S::TA::load(st, &tmA, head0, row0 + int(j * TS), &bars[s], pol);
+        S::TV::load(st + M::A_STAGE, &tmB, head0, row0 + int(j * TS), &bars[s], pol);
+    };
+    {
+        const int npro = int(min64(NS, nblk));
+        if (lane == 0)
+            for (int s = 0; s < npro; ++s) issue_f(s, s);
+        for (int s = 0; s < npro; ++s) rg.armed(s);
+    }
+    float hprev = (h0 != nullptr && active) ? h0[(bi * H + head0 + sub) * K + row] : 0.f;
+    ckp[0] = hprev;
+    for (int64_t j = 0; j < nblk; ++j) {
+        const int s = int(j % NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int n = int(min64(TS, T - j * TS));
+        const float *st = ring + size_t(s) * SSTR;
+        const float *sb = st + M::A_STAGE + lane;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                float a[K];
+                TileRef<K, false>{st, u, sub}.row(row, a);
+                float acc0 = sb[u * VF];
+                float acc1 = 0.f;
+#pragma unroll
+                for (int c = 0; c < K; ++c) {
+                    const float x = __shfl_sync(0xffffffffu, hprev, gbase + c);
+                    if (c & 1)
+                        acc1 = fmaf(a[c], x, acc1);
+                    else
+                        acc0 = fmaf(a[c], x, acc0);
+                }
+                hprev = acc0 + acc1;
+            }
+        }
+        // chunks end on stage boundaries: h after this stage starts the next chunk
+        if ((j + 1) % M::RS == 0 && (j + 1) * TS < T) ckp[((j + 1) / M::RS) * VF] = hprev;
+        __syncwarp();
+        if (j + NS < nblk) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue_f(s, j + NS);
+            }
+            rg.armed(s);
+        }
+    }
+
+    // ---- phase B: chunks downwards; chunk c in slot c % NS
+    auto issue_b = [&](int s, int64_t c) {  // lane 0 only
+        float *st = ring + size_t(s) * SSTR;
+        const int rr = row0 + int(c * RC);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        S::TA::load(st, &tmA, head0, rr, &bars[s], pol);
+        S::TV::load(st + M::A_STAGE, &tmB, head0, rr, &bars[s], pol);
+        S::TV::load(st + M::A_STAGE + M::V_STAGE, &tmG, head0, rr, &bars[s], pol);
+    };
+    __syncwarp();
+    for (int64_t c = nck - 1; c >= 0 && c >= nck - NS; --c) {
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            issue_b(int(c % NS), c);
+        }
+        rg.armed(int(c % NS));
+    }
+    float mu = 0.f;  // (A_{t+1}^T lambda_{t+1})[row], zero past the end
+    const int64_t hk = H * K;
+    float *dbp = db + (bi * T * H + head0 + sub) * K + row;          // + t*H*K
+    float *dAp = dA + (bi * T * H + head0 + sub) * K * K + row * K;  // + t*H*K*K
+    float hnext = ckp[(nck - 1) * VF];  // each chunk's checkpoint is read one chunk ahead
+    for (int64_t c = nck - 1; c >= 0; --c) {
+        const int s = int(c % NS);
+        float hv = hnext;
+        if (c >= 1) hnext = ckp[(c - 1) * VF];
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int n = int(min64(RC, T - c * RC));
+        const float *st = ring + size_t(s) * SSTR;
+        // the chunk's h, forward from its checkpoint
+        hs[lane] = hv;
+        const float *sb = st + M::A_STAGE + lane;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                float a[K];
+                TileRef<K, false>{st, u, sub}.row(row, a);
+                float acc0 = sb[u * VF];
+                float acc1 = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < K; ++cc) {
+                    const float x = __shfl_sync(0xffffffffu, hv, gbase + cc);
+                    if (cc & 1)
+                        acc1 = fmaf(a[cc], x, acc1);
+                    else
+                        acc0 = fmaf(a[cc], x, acc0);
+                }
+                hv = acc0 + acc1;
+                hs[(u + 1) * VF + lane] = hv;
+            }
+        }
+        __syncwarp();
+        // the adjoint back over the chunk
+#pragma unroll
+        for (int u = TS - 1; u >= 0; --u) {
+            if (u < n) {
+                const int64_t t = c * RC + u;
+                const float lam = st[M::A_STAGE + M::V_STAGE + u * VF + lane] + mu;
+                float hp[K];
+                lds_row<K>(hs + u * VF + sub * K, hp);  // h_{t-1}
+                float a[K];
+                TileRef<K, false>{st, u, sub}.row(row, a);
+                float p[K], dar[K];
+#pragma unroll
+                for (int cc = 0; cc < K; ++cc) {
+                    p[cc] = a[cc] * lam;
+                    dar[cc] = lam * hp[cc];
+                }
+                mu = group_reduce_scatter<K>(p, row);
+                if (active) {
+                    st_cs(dbp + t * hk, lam);
+                    stg_row_cs<K>(dAp + t * hk * K, dar);
+                }
+            }
+        }
+        __syncwarp();  // every read of the chunk's slot and of hs is done
+        if (c >= NS) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue_b(s, c - NS);
+            }
+            rg.armed(s);
+        }
+    }
+    if (dh0 != nullptr && active) dh0[(bi * H + head0 + sub) * K + row] = mu;
+}
+
+template <int K>
+size_t mas_rc_workspace_t(int64_t B, int64_t T, int64_t H) {
+    using M = MasRc<K>;
+    const int64_t gpb = (H + M::S::LPW - 1) / M::S::LPW;
+    return size_t(B) * size_t(gpb) * size_t((T + M::RC - 1) / M::RC) * M::S::VF * sizeof(float);
+}
+
+template <int K>
+cudaError_t mas_bwd_rc_t(const float *A, const float *b, const float *h0, const float *gh, float *dA, float *db,
+                         float *dh0, int64_t B, int64_t T, int64_t H, void *ws, const DevCtl &ctl,
+                         cudaStream_t s) {
+    using M = MasRc<K>;
+    using S = typename M::S;
+    CUtensorMap tA, tB, tG;
+    cudaError_t e;
+    if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tB, b, B * T, H, S::TS)) != cudaSuccess) return e;
+    if ((e = S::TV::make(&tG, gh, B * T, H, S::TS)) != cudaSuccess) return e;
+    const int64_t gpb = (H + S::LPW - 1) / S::LPW;
+    const int64_t blocks = B * gpb;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const int smem = int(M::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_bwd_rc_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_bwd_rc_kernel<K><<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tB, tG, h0, static_cast<float *>(ws), dA, db,
+                                                                  dh0, B, T, H, gpb, ctl);
+    return cudaGetLastError();
+}
+
 template <int K>
 cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
                       int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
@@ -799,6 +1038,25 @@ cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *
 #define CALL_B(k) mas_bwd_t<k>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s)
     MAS_DISPATCH(K, CALL_B)
 #undef CALL_B
+}
+
+size_t mas_rc_workspace_bytes(int64_t B, int64_t T, int64_t H, int K) {
+    switch (K) {
+        case 1: return mas_rc_workspace_t<1>(B, T, H);
+        case 2: return mas_rc_workspace_t<2>(B, T, H);
+        case 4: return mas_rc_workspace_t<4>(B, T, H);
+        case 8: return mas_rc_workspace_t<8>(B, T, H);
+        case 16: return mas_rc_workspace_t<16>(B, T, H);
+        default: return 0;
+    }
+}
+
+cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, const float *h0, const float *gh,
+                                     float *dA, float *db, float *dh0, int64_t B, int64_t T, int64_t H, void *ws,
+                                     const DevCtl &ctl, cudaStream_t s) {
+#define CALL_RC(k) mas_bwd_rc_t<k>(A, b, h0, gh, dA, db, dh0, B, T, H, ws, ctl, s)
+    MAS_DISPATCH(K, CALL_RC)
+#undef CALL_RC
 }
 
 }  // namespace mgs

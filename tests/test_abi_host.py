@@ -165,3 +165,22 @@ def test_delta_workspace_size(L):
     assert b.mgs_workspace_size(op, 2, 0, 3, 64) == 0
     assert b.mgs_workspace_size(op, 2, 64, 3, 32) == 0                       # D != 64: the call reports it
     assert b.mgs_workspace_size(op, -1, 64, 3, 64) == 0
+
+
+def test_mas_recompute_workspace_and_validation(L):
+    # checkpoints: 32 floats per (lane group of 32/k heads, chunk of TS steps)
+    op = b.MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE
+    assert b.mgs_workspace_size(op, 2, 40, 4, 8) == 2 * 1 * 5 * 32 * 4     # TS 8
+    assert b.mgs_workspace_size(op, 2, 40, 4, 16) == 2 * 2 * 10 * 32 * 4   # TS 4
+    assert b.mgs_workspace_size(op, 2, 40, 64, 1) == 2 * 2 * 3 * 32 * 4    # TS 16
+    assert b.mgs_workspace_size(op, 32, 8192, 64, 8) == 32 * 16 * 1024 * 32 * 4
+    assert b.mgs_workspace_size(op, 2, 0, 4, 8) == 0
+    assert b.mgs_workspace_size(op, 2, 40, 4, 3) == 0                      # unsupported k: the call reports it
+    A, bb, g = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    dA, db = FAKE + (3 << 30), FAKE + (4 << 30)
+    f = b.mgs_matrix_affine_scan_bwd_recompute
+    assert _st(f, A, None, None, g, dA, db, None, 2, 40, 4, 8) == b.MGS_ERR_INVALID_ARG     # b required
+    assert _st(f, A, bb, None, g, dA, bb, None, 2, 40, 4, 8) == b.MGS_ERR_INVALID_ARG       # db over b
+    assert _st(f, A, bb, None, g, dA, db, None, 2, 40, 4, 8) == b.MGS_ERR_WORKSPACE         # none given
+    assert _st(f, A, bb, None, g, dA, db, None, 2, 40, 4, 3) == b.MGS_ERR_UNSUPPORTED
+    assert _st(f, None, None, None, None, None, None, None, 2, 40, 0, 8) == b.MGS_OK         # no lanes

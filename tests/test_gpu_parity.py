@@ -106,6 +106,68 @@ def test_mas_empty_and_T0():
     assert torch.equal(dh0, torch.zeros_like(dh0))
 
 
+# ---------------------------------------------------------------- matrix_affine_scan, recompute-mode backward
+@pytest.mark.parametrize("B,T,H,k,h0", [
+    (1, 1, 1, 8, "normal"),      # one step
+    (3, 37, 5, 8, "normal"),     # ragged last chunk, partial head group
+    (2, 8, 4, 8, "none"),        # exactly one chunk
+    (2, 32, 4, 8, "normal"),     # exactly the four ring slots
+    (2, 40, 4, 8, "normal"),     # the ring refilled
+    (2, 70, 9, 8, "zeros"),
+    (2, 45, 3, 4, "normal"), (2, 33, 3, 16, "normal"), (2, 50, 6, 2, "normal"), (2, 81, 12, 1, "normal"),
+    (1, 300, 4, 8, "normal"),
+    (1, 1000, 3, 16, "normal"),  # few lanes, long sequence (one warp per lane group here too)
+])
+def test_mas_recompute_backward(B, T, H, k, h0):
+    """No saved h: checkpoints at every chunk start, chunks rebuilt downwards."""
+    d = _cuda(inputs.mas_inputs(B, T, H, k, seed=900 + B * T + H + k, device="cpu", h0=h0))
+    rec = api.matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"], need_dh0=True)
+    b.mgs_check()
+    A, bb, g = d["A"].cpu(), d["b"].cpu(), d["grad_h"].cpu()
+    h0c = d["h0"].cpu() if d["h0"] is not None else torch.zeros((B, H, k))
+    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0c, g)
+    assert_close("dA", rec[0], dAr, T)
+    assert_close("db", rec[1], dbr, T)
+    assert_close("dh0", rec[2], dh0r, T)
+    if b.mgs_workspace_size(b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, B, T, H, k) == 0:
+        # single-pass shapes: the recomputed h follows the forward kernel's
+        # arithmetic step for step, so the two backwards agree to rounding
+        h = api.matrix_affine_scan_fwd(d["A"], d["b"], d["h0"])
+        saved = api.matrix_affine_scan_bwd(d["A"], d["h0"], h, d["grad_h"], need_dh0=True)
+        b.mgs_check()
+        for name, x, y in zip(("dA", "db", "dh0"), rec, saved):
+            assert_close(name + " (vs saved h)", x, y.double().cpu().numpy(), T, rel_tol=1e-6, abs_tol=1e-5)
+
+
+def test_mas_recompute_config4_sampled_rows():
+    """Full benchmark size (B=32, T=8192, H=64, k=8), recompute mode."""
+    w = inputs.WORKLOADS[4]
+    d = w.make(device="cuda")
+    dA, db, dh0 = api.matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"])
+    b.mgs_check()
+    rows = [0, 19, w.B - 1]
+    A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
+    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
+    assert_close("dA", dA[rows], dAr, w.T)
+    assert_close("db", db[rows], dbr, w.T)
+    assert_close("dh0", dh0[rows], dh0r, w.T)
+
+
+def test_mas_recompute_T0_and_errors():
+    dev = "cuda"
+    A = torch.empty((2, 0, 3, 8, 8), device=dev)
+    bb = torch.empty((2, 0, 3, 8), device=dev)
+    dh0 = torch.full((2, 3, 8), float("nan"), device=dev)
+    b.mgs_matrix_affine_scan_bwd_recompute(A, bb, None, bb, A, bb, dh0, 2, 0, 3, 8)
+    b.mgs_check()
+    assert torch.equal(dh0, torch.zeros_like(dh0))
+    d = _cuda(inputs.mas_inputs(2, 40, 4, 8, seed=5, device="cpu", h0="normal"))
+    dA, db = torch.empty_like(d["A"]), torch.empty_like(d["b"])
+    with pytest.raises(b.MGSError) as err:  # the checkpoints need a workspace
+        b.mgs_matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"], dA, db, None, 2, 40, 4, 8)
+    assert err.value.status == b.MGS_ERR_WORKSPACE
+
+
 # ---------------------------------------------------------------- matrix_scan
 def _run_ms(B, T, H, k, seed):
     d = _cuda(inputs.ms_inputs(B, T, H, k, seed))
@@ -308,12 +370,13 @@ def test_linear_scan_autograd():
     assert_close("dh0", h0.grad, dh0r, 90)
 
 
-def test_autograd_wrappers_match_oracle():
+@pytest.mark.parametrize("recompute", [False, True])
+def test_autograd_wrappers_match_oracle(recompute):
     d = _cuda(inputs.mas_inputs(2, 30, 3, 8, seed=7, h0="normal"))
     A = d["A"].clone().requires_grad_(True)
     bb = d["b"].clone().requires_grad_(True)
     h0 = d["h0"].clone().requires_grad_(True)
-    h = api.matrix_affine_scan(A, bb, h0)
+    h = api.matrix_affine_scan(A, bb, h0, recompute=recompute)
     (h * d["grad_h"]).sum().backward()
     dAr, dbr, dh0r = oracle.mas_bwd(d["A"].cpu(), d["b"].cpu(), d["h0"].cpu(), d["grad_h"].cpu())
     assert_close("dA", A.grad, dAr, 30)
