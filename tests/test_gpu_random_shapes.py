@@ -55,6 +55,12 @@ def test_random_matrix_affine_scan(B, T, H, k, h0):
     assert_close("dA", dA, rA, T)
     assert_close("db", db, rb, T)
     assert_close("dh0", dh0, r0, T)
+    # the recompute-mode backward (no saved h) on the same draw
+    qA, qb, q0 = api.matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"])
+    b.mgs_check()
+    assert_close("dA (recompute)", qA, rA, T)
+    assert_close("db (recompute)", qb, rb, T)
+    assert_close("dh0 (recompute)", q0, r0, T)
 
 
 MS = [(int(R.integers(1, 5)), int(R.integers(1, 300)), int(R.integers(1, 6)), int(R.choice([4, 8, 16])))

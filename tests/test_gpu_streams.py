@@ -37,6 +37,8 @@ def _calls():
         out = {}
         h = api.matrix_affine_scan_fwd(m["A"], m["b"], m["h0"], stream=stream)
         out["mas"] = (h,) + api.matrix_affine_scan_bwd(m["A"], m["h0"], h, m["grad_h"], stream=stream)[:2]
+        out["mas_recompute"] = api.matrix_affine_scan_bwd_recompute(m["A"], m["b"], m["h0"], m["grad_h"],
+                                                                    stream=stream)[:2]
         hc = api.matrix_affine_scan_fwd(mc["A"], mc["b"], mc["h0"], stream=stream)
         out["mas_chunked"] = (hc,) + api.matrix_affine_scan_bwd(mc["A"], mc["h0"], hc, mc["grad_h"], stream=stream)[:2]
         hp = api.parallel_scan_log_fwd(p["log_coeffs"], p["log_values"], p["log_h0"], stream=stream)
