@@ -120,12 +120,16 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
  * of every chunk of TS steps (TS = 8 for k = 8) in the workspace, then walks
  * the chunks downwards, recomputing each chunk's h from its checkpoint before
  * taking the adjoint back over it.  Reads A and b twice and grad_h once per
- * step (896 bytes per step at k = 8, against 608 with h saved).
+ * step (896 bytes per step at k = 8, against 608 with h saved).  Shapes with
+ * few lanes and a long sequence (those where the saved-h backward splits T
+ * into chunks, see mgs_workspace_size) instead run the time-chunked forward
+ * into the workspace and the saved-h backward on it.
  * In: A, b (the forward's inputs), h0 (nullable: zero initial state), grad_h.
  * Out: dA, db, dh0 (nullable: not written), as mgs_matrix_affine_scan_bwd.
  * Workspace: mgs_workspace_size(MGS_OP_MATRIX_AFFINE_SCAN_BWD_RECOMPUTE, B, T,
  * H, k) bytes (the checkpoints: 1/TS of the size of h, rounded up per group
- * of 32/k heads), disjoint from every other argument. */
+ * of 32/k heads; for the few-lane shapes h itself and the chunked kernels'
+ * workspace), disjoint from every other argument. */
 mgs_status mgs_matrix_affine_scan_bwd_recompute(const float *A, const float *b, const float *h0,
                                                 const float *grad_h, float *dA, float *db, float *dh0,
                                                 int64_t B, int64_t T, int64_t H, int k, void *workspace,

@@ -1040,7 +1040,17 @@ cudaError_t launch_mas_bwd(int K, const float *A, const float *h0, const float *
 #undef CALL_B
 }
 
+// Few lane groups and a long sequence (where the saved-h path splits T into
+// chunks): the recompute mode runs the time-chunked forward into the
+// workspace and the time-chunked saved-h backward on it; the workspace holds
+// h (256-byte aligned) followed by the chunked kernels' own workspace.  h is
+// still not kept between the forward and the backward call.
+static size_t rc_h_bytes(int64_t B, int64_t T, int64_t H, int K) {
+    return align_up(size_t(B) * size_t(T) * size_t(H) * size_t(K) * sizeof(float), 256);
+}
+
 size_t mas_rc_workspace_bytes(int64_t B, int64_t T, int64_t H, int K) {
+    if (plan_chunks(B, T, H, K).C > 1) return rc_h_bytes(B, T, H, K) + mas_workspace_bytes(B, T, H, K);
     switch (K) {
         case 1: return mas_rc_workspace_t<1>(B, T, H);
         case 2: return mas_rc_workspace_t<2>(B, T, H);
@@ -1054,6 +1064,14 @@ size_t mas_rc_workspace_bytes(int64_t B, int64_t T, int64_t H, int K) {
 cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, const float *h0, const float *gh,
                                      float *dA, float *db, float *dh0, int64_t B, int64_t T, int64_t H, void *ws,
                                      const DevCtl &ctl, cudaStream_t s) {
+    if (plan_chunks(B, T, H, K).C > 1) {
+        float *h = static_cast<float *>(ws);
+        const size_t hb = rc_h_bytes(B, T, H, K), cb = mas_workspace_bytes(B, T, H, K);
+        void *cw = static_cast<unsigned char *>(ws) + hb;
+        cudaError_t e = launch_mas_fwd(K, A, b, h0, h, B, T, H, cw, cb, ctl, s);
+        if (e != cudaSuccess) return e;
+        return launch_mas_bwd(K, A, h0, h, gh, dA, db, dh0, B, T, H, cw, cb, ctl, s);
+    }
 #define CALL_RC(k) mas_bwd_rc_t<k>(A, b, h0, gh, dA, db, dh0, B, T, H, ws, ctl, s)
     MAS_DISPATCH(K, CALL_RC)
 #undef CALL_RC

@@ -174,6 +174,10 @@ def test_mas_recompute_workspace_and_validation(L):
     assert b.mgs_workspace_size(op, 2, 40, 4, 16) == 2 * 2 * 10 * 32 * 4   # TS 4
     assert b.mgs_workspace_size(op, 2, 40, 64, 1) == 2 * 2 * 3 * 32 * 4    # TS 16
     assert b.mgs_workspace_size(op, 32, 8192, 64, 8) == 32 * 16 * 1024 * 32 * 4
+    # few lanes, long sequence: h plus the time-chunked kernels' workspace
+    chunked = b.mgs_workspace_size(b.MGS_OP_MATRIX_AFFINE_SCAN_BWD, 16, 1024, 8, 8)
+    assert chunked > 0
+    assert b.mgs_workspace_size(op, 16, 1024, 8, 8) == 16 * 1024 * 8 * 8 * 4 + chunked
     assert b.mgs_workspace_size(op, 2, 0, 4, 8) == 0
     assert b.mgs_workspace_size(op, 2, 40, 4, 3) == 0                      # unsupported k: the call reports it
     A, bb, g = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)

@@ -116,7 +116,8 @@ def test_mas_empty_and_T0():
     (2, 70, 9, 8, "zeros"),
     (2, 45, 3, 4, "normal"), (2, 33, 3, 16, "normal"), (2, 50, 6, 2, "normal"), (2, 81, 12, 1, "normal"),
     (1, 300, 4, 8, "normal"),
-    (1, 1000, 3, 16, "normal"),  # few lanes, long sequence (one warp per lane group here too)
+    # few lanes, long sequences: chunked forward into the workspace, chunked backward
+    (1, 1000, 3, 16, "normal"), (16, 1024, 8, 8, "normal"), (3, 4099, 2, 2, "none"),
 ])
 def test_mas_recompute_backward(B, T, H, k, h0):
     """No saved h: checkpoints at every chunk start, chunks rebuilt downwards."""
