@@ -388,9 +388,14 @@ __global__ void __launch_bounds__(32)
     for (int b2 = 0; b2 < nprob; ++b2) rb.armed(b2);
 
     float4 nx = make_float4(0.f, 0.f, 0.f, 0.f);  // a_{t+1} lambda_{t+1}
+    // each segment's checkpoint is read one segment ahead (a global read at the
+    // top of a segment would sit on its critical path)
+    float4 Lnext = active ? ld4(ck + (nseg - 1) * D) : L0;
     for (int64_t jj = 0; jj < nseg; ++jj) {
         const int64_t j = nseg - 1 - jj;
         const int buf = int(jj & 1);
+        const float4 Ls = Lnext;
+        if (j >= 1 && active) Lnext = ld4(ck + (j - 1) * D);
         if (!rb.wait(buf, ctl)) {
             if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
             rb.drain(ctl, lane);
@@ -400,7 +405,6 @@ __global__ void __launch_bounds__(32)
         const float *sc = ring + size_t(buf) * 3 * L::BOXF + 4 * lane;
         const float *sv = sc + L::BOXF;
         const float *sg = sc + 2 * L::BOXF;
-        const float4 Ls = active ? ld4(ck + j * D) : L0;
         // h over the segment, from its checkpoint
         float4 hreg[kRcS];
         float4 Lr = Ls;
