@@ -694,9 +694,11 @@ __global__ void __launch_bounds__(32)
     item = __shfl_sync(0xffffffffu, item, 0);
     if (int64_t(item) >= G * C) return;
 
-    const int64_t c = int64_t(item) / G, g = int64_t(item) % G, iself = g * C + c;
-    const int64_t bi = g / gpb;
-    const int head0 = int(g % gpb) * S::LPW;
+    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
+    const int64_t c = q32, g = item - q32 * unsigned(G), iself = g * C + c;
+    const unsigned b32 = unsigned(g) / unsigned(gpb);
+    const int64_t bi = b32;
+    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
     const bool active = sub < nl;
@@ -829,9 +831,11 @@ __global__ void __launch_bounds__(32)
     if (int64_t(item) >= G * C) return;
 
     // carries flow from the end: tickets go to the last chunk first
-    const int64_t c = C - 1 - int64_t(item) / G, g = int64_t(item) % G, iself = g * C + c;
-    const int64_t bi = g / gpb;
-    const int head0 = int(g % gpb) * S::LPW;
+    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
+    const int64_t c = C - 1 - int64_t(q32), g = item - q32 * unsigned(G), iself = g * C + c;
+    const unsigned b32 = unsigned(g) / unsigned(gpb);
+    const int64_t bi = b32;
+    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
     const int nl = int(min64(S::LPW, H - head0));
     const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
     const bool active = sub < nl;
