@@ -2,7 +2,7 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into
 ``scan_linear_recurrences_gb300/libmgscan.so`` (static CUDA runtime, so the
-library only needs the driver at run time).  Run ``python -m
+library only needs the CUDA driver at run time).  Run ``python -m
 scan_linear_recurrences_gb300.build`` or call :func:`build`.
 """
 from __future__ import annotations
