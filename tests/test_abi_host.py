@@ -188,3 +188,14 @@ def test_mas_recompute_workspace_and_validation(L):
     assert _st(f, A, bb, None, g, dA, db, None, 2, 40, 4, 8) == b.MGS_ERR_WORKSPACE         # none given
     assert _st(f, A, bb, None, g, dA, db, None, 2, 40, 4, 3) == b.MGS_ERR_UNSUPPORTED
     assert _st(f, None, None, None, None, None, None, None, 2, 40, 0, 8) == b.MGS_OK         # no lanes
+
+
+def test_binding_op_ids_match_the_header():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    ids = dict(re.findall(r"\b(MGS_OP_[A-Z_]+)\s*=\s*(\d+)", text))
+    assert len(ids) >= 14
+    for name, value in ids.items():
+        assert getattr(b, name) == int(value), name
+    statuses = dict(re.findall(r"\b(MGS_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", text))
+    for name, value in statuses.items():
+        assert getattr(b, name) == int(value), name
