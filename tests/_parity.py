@@ -24,17 +24,9 @@ def errors(gpu, ref):
     return float(rel), float(np.abs(d).max())
 
 
-def assert_close(name, gpu, ref, T, rel_tol=REL_L2, abs_tol=None, scale_by_rms=False):
-    """scale_by_rms: the max-abs bound is taken relative to the reference's RMS
-    when that exceeds 1.  Used only for recurrences without a contracting gate
-    (a rotation-only transition), whose states and adjoints grow like sqrt(T),
-    so that a fixed absolute bound would test the magnitude, not the error."""
+def assert_close(name, gpu, ref, T, rel_tol=REL_L2, abs_tol=None):
     rel, mx = errors(gpu, ref)
     lim = abs_tol if abs_tol is not None else ABS_PER_SQRT_T * math.sqrt(max(T, 1))
-    if scale_by_rms and abs_tol is None:
-        r = np.asarray(ref, np.float64)
-        rms = float(np.sqrt(np.mean(r * r))) if r.size else 0.0
-        lim *= max(1.0, rms)
     assert np.isfinite(rel) and rel <= rel_tol and mx <= lim, \
         f"{name}: rel_l2={rel:.3e} (<= {rel_tol:.1e}), max_abs={mx:.3e} (<= {lim:.2e})"
     return rel, mx

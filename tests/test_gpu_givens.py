@@ -43,15 +43,12 @@ def _run_gas(B, T, H, seed, h0, with_a, rows=None):
     sel = slice(None) if rows is None else rows
     pick = lambda x: _cpu(x[sel]) if x is not None else None
     href = oracle.gas_fwd(pick(th), pick(a), pick(bb), pick(z0))
-    # without the gate a the transition is a pure rotation: nothing contracts,
-    # h and the adjoints grow like sqrt(T), and max-abs is judged against the RMS
-    sc = a is None
-    assert_close("h", h[sel], href, T, scale_by_rms=sc)
+    assert_close("h", h[sel], href, T)
     z0c = pick(z0) if z0 is not None else torch.zeros((len(href), H, 8))
     dthr, dar, dbr, dh0r = oracle.gas_bwd(pick(th), pick(a), pick(bb), z0c, pick(g))
-    assert_close("d_theta", dth[sel], dthr, T, scale_by_rms=sc)
-    assert_close("db", db[sel], dbr, T, scale_by_rms=sc)
-    assert_close("dh0", dh0[sel], dh0r, T, scale_by_rms=sc)
+    assert_close("d_theta", dth[sel], dthr, T)
+    assert_close("db", db[sel], dbr, T)
+    assert_close("dh0", dh0[sel], dh0r, T)
     if a is not None:
         assert_close("da", da[sel], dar, T)
     else:
