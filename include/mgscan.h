@@ -162,7 +162,9 @@ mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, i
  * process exits.  Shapes needing more
  * scratch than that return MGS_ERR_WORKSPACE and do nothing.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture.
+ * device current; make that first call before any stream capture.  The
+ * address is cached per device context: if the context is destroyed and
+ * created again (cudaDeviceReset), the next call looks it up again.
  * All calls on a device share the one array, which keeps the previous call's
  * contents; each call clears the part that must start at zero (an async
  * memset on `stream`).  Calls that overlap on the GPU, e.g. on two unordered

@@ -22,21 +22,14 @@ namespace {
 // the device address, once per device.
 __device__ unsigned g_mgs_error_word = 0;
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-unsigned *g_err_addr[kMaxDevices] = {};
+mgs::SymbolAddressCache g_err_cache;
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 
 mgs_status current_ctl(mgs::DevCtl *ctl) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MGS_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_err_addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_mgs_error_word) != cudaSuccess) return MGS_ERR_CUDA;
-        g_err_addr[dev] = static_cast<unsigned *>(p);
-    }
-    ctl->err = g_err_addr[dev];
+    void *p = nullptr;
+    if (mgs::cached_symbol_address(g_err_cache, (const void *)&g_mgs_error_word, &p) != cudaSuccess)
+        return MGS_ERR_CUDA;
+    ctl->err = static_cast<unsigned *>(p);
     ctl->timeout_ns = g_timeout_ns.load();
     return MGS_OK;
 }
@@ -168,17 +161,59 @@ cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t ensure_smem_attr(const void *fn, int bytes) {
-    static std::mutex mu;
-    static std::set<std::pair<const void *, int>> done;
+uint64_t current_context_id() {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? uint64_t(id) : 0;
+}
+
+cudaError_t cached_symbol_address(SymbolAddressCache &cache, const void *symbol, void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= SymbolAddressCache::kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(cache.mu);
+    const uint64_t ctx = current_context_id();
+    if (ctx != 0 && cache.ctx[dev] == ctx && cache.addr[dev] != nullptr) {
+        *out = cache.addr[dev];
+        return cudaSuccess;
+    }
+    // the lookup also creates and binds the device's primary context when no
+    // context is current yet, so the id is read again after it
+    void *p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, symbol)) != cudaSuccess) return e;
+    cache.ctx[dev] = current_context_id();
+    cache.addr[dev] = p;
+    *out = p;
+    return cudaSuccess;
+}
+
+cudaError_t ensure_smem_attr(const void *fn, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<const void *, uint64_t>> done;
+    const uint64_t ctx = current_context_id();
     std::lock_guard<std::mutex> lk(mu);
-    auto key = std::make_pair(fn, dev);
-    if (done.count(key)) return cudaSuccess;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes > 48 * 1024 ? 227 * 1024 : 48 * 1024);
-    if (e == cudaSuccess) done.insert(key);
+    auto key = std::make_pair(fn, ctx);
+    if (ctx != 0 && done.count(key)) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         bytes > 48 * 1024 ? 227 * 1024 : 48 * 1024);
+    if (e == cudaSuccess && ctx != 0) done.insert(key);
     return e;
 }
 

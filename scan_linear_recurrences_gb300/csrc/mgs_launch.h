@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "mgs_device.cuh"
@@ -77,7 +78,24 @@ cudaError_t launch_delta_fwd(const float *q, const float *k, const float *v, con
 cudaError_t make_tmap(CUtensorMap *map, const float *base, int rank, const uint64_t *dims,
                       const uint64_t *byte_strides, const uint32_t *box, bool swizzle128 = false);
 
-// Sets the dynamic shared-memory limit of `fn` once per device.
+// Sets the dynamic shared-memory limit of `fn` once per device context.
 cudaError_t ensure_smem_attr(const void *fn, int bytes);
+
+// Unique id of the CUDA context current on the calling thread, 0 when none is
+// current (or the driver does not report one).
+uint64_t current_context_id();
+
+// Device address of a file-scope __device__ variable, looked up with
+// cudaGetSymbolAddress once per device context and cached.  A device's
+// context can be torn down and created again (cudaDeviceReset), after which
+// the variable lives at a new address; the cache is keyed on the context id,
+// so a new context gets a fresh lookup rather than a stale address.
+struct SymbolAddressCache {
+    static constexpr int kMaxDevices = 64;
+    std::mutex mu;
+    uint64_t ctx[kMaxDevices] = {};
+    void *addr[kMaxDevices] = {};
+};
+cudaError_t cached_symbol_address(SymbolAddressCache &cache, const void *symbol, void **out);
 
 }  // namespace mgs

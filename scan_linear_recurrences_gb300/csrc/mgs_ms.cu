@@ -747,28 +747,19 @@ cudaError_t launch_ms_bwd(int K, const float *A, const float *P, const float *G,
 // Scratch for mgs_matrix_scan_fwd_noalloc: one file-scope array per device
 // context that loads the library.  Host code never uses the array's name as
 // an address (in host code it is only a stand-in); the device address comes
-// from cudaGetSymbolAddress, looked up once per device with that device
-// current, and is passed to the kernel like any caller workspace.
+// from cudaGetSymbolAddress, looked up once per device context with that
+// device current (again if the context is torn down and re-created), and is
+// passed to the kernel like any caller workspace.
 namespace {
 static __device__ __align__(256) unsigned char g_ms_noalloc_scratch[MGS_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_scratch_mu;
-unsigned char *g_scratch_addr[64] = {};
+mgs::SymbolAddressCache g_scratch_cache;
 
 cudaError_t noalloc_scratch_address(unsigned char **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_ms_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<unsigned char *>(p);
-    }
-    *out = g_scratch_addr[dev];
-    return cudaSuccess;
+    void *p = nullptr;
+    cudaError_t e = mgs::cached_symbol_address(g_scratch_cache, (const void *)&g_ms_noalloc_scratch, &p);
+    *out = static_cast<unsigned char *>(p);
+    return e;
 }
 }  // namespace
 
