@@ -706,9 +706,11 @@ def run_gpu(args):
             "config": {"workload": " + ".join(r.w.name for r in runners) + ", fwd+bwd each",
                        "l2": "flushed before the two L2-resident shapes; the others exceed L2",
                        "step_bytes": step_bytes, "wall_s_timed_region": round(wall, 4)},
-            "ops": ops, "extra_ops_not_in_step": extra, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            # the report-only shapes first and the per-op lines of the step
+            # last, so that a reader keeping only the end of the line keeps them
+            "extra_ops_not_in_step": extra, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * 2 * len(runners), "clocks": clocks,
-            "impl": "libmgscan",
+            "impl": "libmgscan", "ops": ops,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
