@@ -30,6 +30,7 @@
 // enough blocks to fill the GPU).  Matrix scan: eight threads per lane,
 // thread j owning column j of P_t, four lanes per block.  Each stage of TS
 // steps arrives by tiled TMA loads into a per-block ring.
+#include "mgs_ffsincos.cuh"
 #include "mgs_tiles.cuh"
 
 namespace mgs {
@@ -204,36 +205,78 @@ struct BlockRing {
 // ts*lpw*GN floats, in the backward two buffers of rotated pairs of
 // 2*ts*lpw*GN floats, the barriers and the abort word.
 // The backward adds two buffers of the rotated-state pairs (xp_f floats each).
+// In the exact-orthogonal mode (no gate, see below) two more buffers of
+// ts*lpw*GN floats per stage parity hold the low parts of the cosines and
+// sines, and the table of cos_sin_ff sits in front of the barriers.
 struct GasSmem {
-    int th_f, vec_f, stage_f, ring_f, sin_f, xp_f;
-    __host__ __device__ GasSmem(int lpw, int ts, int nv, bool with_xp = false) {
+    int th_f, vec_f, stage_f, ring_f, sin_f, xp_f, lo_f, tab_f;
+    __host__ __device__ GasSmem(int lpw, int ts, int nv, bool with_xp = false, bool xo = false) {
         th_f = ts * lpw * GN;
         vec_f = ts * lpw * GK;
         stage_f = int(align_up(size_t(th_f + nv * vec_f), 32));
         ring_f = kNS * stage_f;
         sin_f = th_f;
         xp_f = with_xp ? 2 * th_f : 0;
+        lo_f = xo ? 2 * th_f : 0;
+        tab_f = xo ? 4 * SinCosTable::kEntries : 0;
     }
     __host__ __device__ size_t bytes() const {
-        return size_t(ring_f + 2 * sin_f + 2 * xp_f) * 4 + kNS * sizeof(uint64_t) + 16;
+        return size_t(ring_f + 2 * sin_f + 2 * xp_f + 2 * lo_f + tab_f) * 4 + kNS * sizeof(uint64_t) + 16;
     }
 };
 
+// Exact-orthogonal mode.  Without the gate a the transition G(theta) is
+// orthogonal: nothing contracts, the state and the adjoint grow like sqrt(T)
+// and the angle gradients like T, so the rounding of fp32 cosines and sines
+// (each rotation off by up to half an ulp, 3e-8, in angle) accumulates into
+// angle-gradient errors of several 1e-3 at T ~ 500.  There the kernels take
+// the cosines and sines as hi + lo pairs from cos_sin_ff (error ~1e-11) and
+// carry the recurrence state (forward) and the adjoint (backward) as hi + lo
+// pairs, rounding to fp32 only what they store.
+template <int NP>
+__device__ __forceinline__ void angle_range_ff(float *th, float *sn, float *clo, float *slo, int lo, int hi, int pt,
+                                               const float4 *tab) {
+    int i = lo + pt;
+    for (; i + NP < hi; i += 2 * NP) {
+        float c0, c0l, s0, s0l, c1, c1l, s1, s1l;
+        cos_sin_ff(th[i], tab, c0, c0l, s0, s0l);
+        cos_sin_ff(th[i + NP], tab, c1, c1l, s1, s1l);
+        th[i] = c0; sn[i] = s0; clo[i] = c0l; slo[i] = s0l;
+        th[i + NP] = c1; sn[i + NP] = s1; clo[i + NP] = c1l; slo[i + NP] = s1l;
+    }
+    for (; i < hi; i += NP) {
+        float c, cl, sv, sl;
+        cos_sin_ff(th[i], tab, c, cl, sv, sl);
+        th[i] = c; sn[i] = sv; clo[i] = cl; slo[i] = sl;
+    }
+}
+
+// Copies the cos_sin_ff table from the kernel parameters into shared memory
+// (indexed reads of parameter space serialise across a warp).
+__device__ __forceinline__ void load_table(float4 *dst, const SinCosTable &tab, int tid, int nthreads) {
+    for (int i = tid; i < SinCosTable::kEntries; i += nthreads) dst[i] = tab.e[i];
+}
+
 // ---------------------------------------------------------------- affine forward
+// XO: the exact-orthogonal mode (has_a must be 0), see angle_range_ff.
+template <bool XO>
 __global__ void __launch_bounds__(kBlockF)
     gas_fwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const float *__restrict__ h0, float *__restrict__ h,
                    int64_t B, int64_t T, int64_t H, int64_t groups_per_b, int lpw, int ts, int has_a,
-                   DevCtl ctl) {
+                   const __grid_constant__ SinCosTable tab, DevCtl ctl) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    const GasSmem L(lpw, ts, has_a ? 2 : 1);
+    const GasSmem L(lpw, ts, has_a ? 2 : 1, false, XO);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
     if (g >= B * groups_per_b) return;
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *snb = ring + L.ring_f;  // two sine buffers
-    uint64_t *bars = reinterpret_cast<uint64_t *>(snb + 2 * L.sin_f);
+    float *lob = snb + 2 * L.sin_f;  // XO: two buffers of (cosine lo, sine lo)
+    float4 *tabs = reinterpret_cast<float4 *>(lob + 2 * L.lo_f);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tabs + (XO ? SinCosTable::kEntries : 0));
+    if constexpr (XO) load_table(tabs, tab, tid, kBlockF);
     BlockRing br;
     br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
@@ -264,21 +307,29 @@ __global__ void __launch_bounds__(kBlockF)
         for (int s = 0; s < npro; ++s) br.rg.armed(s);
 
     const bool active = !producer && lane < nl;
-    float x[GK];
+    float x[GK], xl[GK];  // state (XO: hi parts; xl the lo parts)
     if (active && h0 != nullptr) {
         lds_vec<GK>(h0 + (bi * H + head0 + lane) * GK, x);  // 16-byte aligned global loads
     } else {
 #pragma unroll
         for (int i = 0; i < GK; ++i) x[i] = 0.f;
     }
+#pragma unroll
+    for (int i = 0; i < GK; ++i) xl[i] = 0.f;
     float *hp = h + ((bi * T) * H + head0 + lane) * GK;
 
     for (int64_t it = 0; it <= nblk; ++it) {
         if (producer && it < nblk) {
             const int s = int(it % kNS);
             if (br.rg.wait(s, ctl)) {
-                angle_range<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0,
-                            int(min64(ts, T - it * ts)) * lpw * GN, tid - 32);
+                const int hi = int(min64(ts, T - it * ts)) * lpw * GN;
+                if constexpr (XO) {
+                    float *lo = lob + (it & 1) * L.lo_f;
+                    angle_range_ff<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, lo, lo + L.sin_f,
+                                           0, hi, tid - 32, tabs);
+                } else {
+                    angle_range<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0, hi, tid - 32);
+                }
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
                 *br.abort_word = 1;
@@ -289,6 +340,27 @@ __global__ void __launch_bounds__(kBlockF)
             const float *st = ring + size_t(j % kNS) * L.stage_f;
             const float *sc = snb + (j & 1) * L.sin_f;
             const int n = int(min64(ts, T - j * ts));
+            if constexpr (XO) {
+                const float *lo = lob + (j & 1) * L.lo_f;
+                for (int u = 0; u < n; ++u) {
+                    const int item = u * lpw + lane;
+                    const float *cp = st + item * GN, *sp = sc + item * GN;
+                    const float *clp = lo + item * GN, *slp = lo + L.sin_f + item * GN;
+                    float bv[GK];
+                    lds_vec<GK>(st + b_off + item * GK, bv);
+#pragma unroll
+                    for (int l = 0; l < GK; ++l)
+#pragma unroll
+                        for (int q = 0; q < layer_pairs(l); ++q) {
+                            const int p = (l & 1) + 2 * q, nn = layer_base(l) + q;
+                            ff_rot_fwd(x[p], xl[p], x[p + 1], xl[p + 1], cp[nn], clp[nn], sp[nn], slp[nn]);
+                        }
+#pragma unroll
+                    for (int i = 0; i < GK; ++i) ff_add(x[i], xl[i], bv[i]);
+                    stg_vec_cs<GK>(hp, x);
+                    hp += H * GK;
+                }
+            } else
             for (int u = 0; u < n; ++u) {
                 const int item = u * lpw + lane;
                 float cs[GN], sv[GN], bv[GK];
@@ -333,15 +405,21 @@ __global__ void __launch_bounds__(kBlockF)
 // for the next stage together with its angle conversion and leave the 28
 // rotated pairs per step in shared memory; the recurrence warp's chain per
 // step is then only the transposed rotations of mu.
+// XO: the exact-orthogonal mode (has_a must be 0): cosines and sines as
+// hi + lo pairs and the adjoint carried as hi + lo pairs; the forward pass
+// through the layers (which only enters the angle gradients, rounded to
+// fp32 anyway) uses the hi parts.
+template <bool XO>
 __global__ void __launch_bounds__(kBlockB)
     gas_bwd_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
                    const float *__restrict__ h0, float *__restrict__ dth, float *__restrict__ da,
                    float *__restrict__ db, float *__restrict__ dh0, int64_t B, int64_t T, int64_t H,
-                   int64_t groups_per_b, int lpw, int ts, int has_a, DevCtl ctl) {
+                   int64_t groups_per_b, int lpw, int ts, int has_a, const __grid_constant__ SinCosTable tab,
+                   DevCtl ctl) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int nv = has_a ? 3 : 2;  // a, g, h_{t-1}
-    const GasSmem L(lpw, ts, nv, true);
+    const GasSmem L(lpw, ts, nv, true, XO);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool producer = warp != 0;
     const int64_t g = blockIdx.x;
@@ -349,7 +427,10 @@ __global__ void __launch_bounds__(kBlockB)
     float *ring = reinterpret_cast<float *>(smem_raw);
     float *snb = ring + L.ring_f;
     float *xpb = snb + 2 * L.sin_f;  // two buffers of rotated pairs, 2 GN floats per item
-    uint64_t *bars = reinterpret_cast<uint64_t *>(xpb + 2 * L.xp_f);
+    float *lob = xpb + 2 * L.xp_f;   // XO: two buffers of (cosine lo, sine lo)
+    float4 *tabs = reinterpret_cast<float4 *>(lob + 2 * L.lo_f);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tabs + (XO ? SinCosTable::kEntries : 0));
+    if constexpr (XO) load_table(tabs, tab, tid, kBlockB);
     BlockRing br;
     br.init(bars, reinterpret_cast<int *>(bars + kNS), tid);
 
@@ -388,11 +469,12 @@ __global__ void __launch_bounds__(kBlockB)
     };
 
     const bool active = !producer && lane < nl;
-    float h0v[GK], carry[GK];
+    float h0v[GK], carry[GK], carryl[GK];  // carryl: XO lo parts
 #pragma unroll
     for (int i = 0; i < GK; ++i) {
         h0v[i] = 0.f;
         carry[i] = 0.f;
+        carryl[i] = 0.f;
     }
     if (active && h0 != nullptr) lds_vec<GK>(h0 + (bi * H + head0 + lane) * GK, h0v);
 
@@ -402,7 +484,13 @@ __global__ void __launch_bounds__(kBlockB)
             float *st = ring + size_t(s) * L.stage_f;
             float *sn = snb + (it & 1) * L.sin_f;
             if (br.rg.wait(s, ctl)) {
-                angle_range<kProdB>(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
+                if constexpr (XO) {
+                    float *lo = lob + (it & 1) * L.lo_f;
+                    angle_range_ff<kProdB>(st, sn, lo, lo + L.sin_f, first_row(it) * lpw * GN, ts * lpw * GN,
+                                           tid - 32, tabs);
+                } else {
+                    angle_range<kProdB>(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
+                }
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
                 *br.abort_word = 1;
@@ -457,6 +545,41 @@ __global__ void __launch_bounds__(kBlockB)
             const float *st = ring + size_t(j % kNS) * L.stage_f;
             const float *sc = snb + (j & 1) * L.sin_f;
             const float *xp = xpb + (j & 1) * L.xp_f;
+            if constexpr (XO) {
+                const float *lo = lob + (j & 1) * L.lo_f;
+                for (int u = ts - 1; u >= first_row(j); --u) {
+                    const int64_t t = tb + u;
+                    const int item = u * lpw + lane;
+                    const float *cp = st + item * GN, *sp = sc + item * GN, *pp = xp + item * 2 * GN;
+                    const float *clp = lo + item * GN, *slp = lo + L.sin_f + item * GN;
+                    float gv[GK], lam[GK], laml[GK];
+                    lds_vec<GK>(st + g_off + item * GK, gv);
+#pragma unroll
+                    for (int i = 0; i < GK; ++i) {
+                        float s_, e_;
+                        ff_two_sum(carry[i], gv[i], s_, e_);
+                        ff_fast_two_sum(s_, e_ + carryl[i], lam[i], laml[i]);
+                    }
+                    const int64_t o = ((bi * T + t) * H + head0 + lane);
+                    stg_vec_cs<GK>(db + o * GK, lam);
+                    float dthv[GN];
+#pragma unroll
+                    for (int l = GK - 1; l >= 0; --l) {
+#pragma unroll
+                        for (int q = 0; q < layer_pairs(l); ++q) {
+                            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
+                            dthv[n] = fmaf(lam[p + 1], pp[2 * n], -lam[p] * pp[2 * n + 1]);
+                            ff_rot_bwd(lam[p], laml[p], lam[p + 1], laml[p + 1], cp[n], clp[n], sp[n], slp[n]);
+                        }
+                    }
+                    stg_vec_cs<GN>(dth + o * GN, dthv);
+#pragma unroll
+                    for (int i = 0; i < GK; ++i) {
+                        carry[i] = lam[i];
+                        carryl[i] = laml[i];
+                    }
+                }
+            } else
             for (int u = ts - 1; u >= first_row(j); --u) {
                 const int64_t t = tb + u;
                 const int item = u * lpw + lane;
@@ -963,10 +1086,18 @@ size_t givens_workspace_bytes(int op, int64_t B, int64_t T, int64_t H) {
     }
 }
 
+const SinCosTable &sincos_table() {
+    static const SinCosTable t = SinCosTable::build();
+    return t;
+}
+
 cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, const float *h0, float *h,
                            int64_t B, int64_t T, int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl,
                            cudaStream_t s) {
-    if (few_lane_path(B, T, H)) {
+    // without the gate the exact-orthogonal kernels run at every shape (the
+    // few-lane path's fp32 matrix kernels cannot carry the extra precision)
+    const bool xo = a == nullptr;
+    if (!xo && few_lane_path(B, T, H)) {
         float *A = static_cast<float *>(ws);
         const size_t mb = mat_bytes(B, T, H);
         givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, a, A, B * T * H);
@@ -987,17 +1118,19 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     }
     const int64_t gpb = (H + lpw - 1) / lpw, blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const int smem = int(GasSmem(lpw, ts, a ? 2 : 1).bytes());
-    if ((e = ensure_smem_attr((const void *)gas_fwd_kernel, smem)) != cudaSuccess) return e;
-    gas_fwd_kernel<<<dim3(unsigned(blocks)), kBlockF, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts,
-                                                                a != nullptr, ctl);
+    const int smem = int(GasSmem(lpw, ts, a ? 2 : 1, false, xo).bytes());
+    const auto kern = xo ? gas_fwd_kernel<true> : gas_fwd_kernel<false>;
+    if ((e = ensure_smem_attr((const void *)kern, smem)) != cudaSuccess) return e;
+    kern<<<dim3(unsigned(blocks)), kBlockF, smem, s>>>(tTh, tA, tB, h0, h, B, T, H, gpb, lpw, ts, a != nullptr,
+                                                       sincos_table(), ctl);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, const float *h, const float *gh,
                            float *dth, float *da, float *db, float *dh0, int64_t B, int64_t T, int64_t H,
                            void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
-    if (few_lane_path(B, T, H)) {
+    const bool xo = a == nullptr;  // as in the forward
+    if (!xo && few_lane_path(B, T, H)) {
         // lambda_t = db_t and dh0 come from the time-chunked matrix_affine_scan
         // backward (dA goes to the workspace, unused); the angle and gate
         // gradients then follow per step from lambda_t and h_{t-1}
@@ -1027,10 +1160,11 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
     }
     const int64_t gpb = (H + lpw - 1) / lpw, blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const int smem = int(GasSmem(lpw, ts, a ? 3 : 2, true).bytes());
-    if ((e = ensure_smem_attr((const void *)gas_bwd_kernel, smem)) != cudaSuccess) return e;
-    gas_bwd_kernel<<<dim3(unsigned(blocks)), kBlockB, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H,
-                                                                gpb, lpw, ts, a != nullptr, ctl);
+    const int smem = int(GasSmem(lpw, ts, a ? 3 : 2, true, xo).bytes());
+    const auto kern = xo ? gas_bwd_kernel<true> : gas_bwd_kernel<false>;
+    if ((e = ensure_smem_attr((const void *)kern, smem)) != cudaSuccess) return e;
+    kern<<<dim3(unsigned(blocks)), kBlockB, smem, s>>>(tTh, tA, tG, tH, h0, dth, da, db, dh0, B, T, H, gpb, lpw, ts,
+                                                       a != nullptr, sincos_table(), ctl);
     return cudaGetLastError();
 }
 
