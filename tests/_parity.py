@@ -30,3 +30,31 @@ def assert_close(name, gpu, ref, T, rel_tol=REL_L2, abs_tol=None):
     assert np.isfinite(rel) and rel <= rel_tol and mx <= lim, \
         f"{name}: rel_l2={rel:.3e} (<= {rel_tol:.1e}), max_abs={mx:.3e} (<= {lim:.2e})"
     return rel, mx
+
+
+class Streamed:
+    """Relative L2 and max-abs of one output tensor compared part by part (for
+    outputs too large to hold in float64 at once): the squared norms and the
+    maximum accumulate over the parts, then check() applies the same bounds
+    as assert_close to the whole tensor."""
+
+    def __init__(self, name):
+        self.name, self.d2, self.r2, self.mx, self.n = name, 0.0, 0.0, 0.0, 0
+
+    def add(self, gpu, ref):
+        g = gpu.detach().double().cpu().numpy() if hasattr(gpu, "detach") else np.asarray(gpu, np.float64)
+        r = np.asarray(ref, np.float64)
+        assert g.shape == r.shape, (g.shape, r.shape)
+        d = g - r
+        self.d2 += float(np.sum(d * d))
+        self.r2 += float(np.sum(r * r))
+        if d.size:
+            self.mx = max(self.mx, float(np.abs(d).max()))
+        self.n += r.size
+
+    def check(self, T, rel_tol=REL_L2):
+        rel = math.sqrt(self.d2 / self.r2) if self.r2 > 0 else math.sqrt(self.d2)
+        lim = ABS_PER_SQRT_T * math.sqrt(max(T, 1))
+        assert np.isfinite(rel) and rel <= rel_tol and self.mx <= lim, \
+            f"{self.name}: rel_l2={rel:.3e} (<= {rel_tol:.1e}), max_abs={self.mx:.3e} (<= {lim:.2e})"
+        return rel, self.mx

@@ -1,7 +1,7 @@
 """GPU parity: the CUDA library (called through its C ABI) against the float64
 oracle on the same seeded float32 inputs, at small sizes that span several
-ring stages and ragged tails, at the benchmark's full sizes on sampled batch
-rows, and on the degenerate cases."""
+ring stages and ragged tails, at the benchmark's full sizes (every element,
+compared in groups of batch rows), and on the degenerate cases."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +11,7 @@ from scan_linear_recurrences_gb300 import _binding as b
 from scan_linear_recurrences_gb300 import api, inputs
 from scan_linear_recurrences_gb300.build import build
 
-from ._parity import assert_close
+from ._parity import Streamed, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -76,21 +76,28 @@ def test_mas_long_T_shape_of_the_pages():
     _run_mas(16, 1024, 8, 8, seed=4242, h0_mode="normal")
 
 
-def test_mas_config4_sampled_rows():
+def test_mas_config4_full():
     """Full benchmark size (B=32, T=8192, H=64, k=8) in the launch
-    configuration the benchmark times; the oracle checks three batch rows."""
+    configuration the benchmark times, every output element compared with the
+    oracle (streamed over groups of 4 batch rows)."""
     w = inputs.WORKLOADS[4]
     d = w.make(device="cuda")
     h = api.matrix_affine_scan_fwd(d["A"], d["b"], d["h0"])
     dA, db, dh0 = api.matrix_affine_scan_bwd(d["A"], d["h0"], h, d["grad_h"])
     b.mgs_check()
-    rows = [0, 13, w.B - 1]
-    A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
-    assert_close("h", h[rows], oracle.mas_fwd(A, bb, h0), w.T)
-    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
-    assert_close("dA", dA[rows], dAr, w.T)
-    assert_close("db", db[rows], dbr, w.T)
-    assert_close("dh0", dh0[rows], dh0r, w.T)
+    acc = {n: Streamed(n) for n in ("h", "dA", "db", "dh0")}
+    for r0 in range(0, w.B, 4):
+        rows = slice(r0, min(w.B, r0 + 4))
+        A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
+        acc["h"].add(h[rows], oracle.mas_fwd(A, bb, h0))
+        dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
+        acc["dA"].add(dA[rows], dAr)
+        acc["db"].add(db[rows], dbr)
+        acc["dh0"].add(dh0[rows], dh0r)
+        del A, bb, h0, g, dAr, dbr, dh0r
+    for a in acc.values():
+        assert a.n > 0
+        a.check(w.T)
 
 
 def test_mas_empty_and_T0():
@@ -140,18 +147,24 @@ def test_mas_recompute_backward(B, T, H, k, h0):
             assert_close(name + " (vs saved h)", x, y.double().cpu().numpy(), T, rel_tol=1e-6, abs_tol=1e-5)
 
 
-def test_mas_recompute_config4_sampled_rows():
-    """Full benchmark size (B=32, T=8192, H=64, k=8), recompute mode."""
+def test_mas_recompute_config4_full():
+    """Full benchmark size (B=32, T=8192, H=64, k=8), recompute mode, every
+    element compared (streamed over groups of 4 batch rows)."""
     w = inputs.WORKLOADS[4]
     d = w.make(device="cuda")
     dA, db, dh0 = api.matrix_affine_scan_bwd_recompute(d["A"], d["b"], d["h0"], d["grad_h"])
     b.mgs_check()
-    rows = [0, 19, w.B - 1]
-    A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
-    dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
-    assert_close("dA", dA[rows], dAr, w.T)
-    assert_close("db", db[rows], dbr, w.T)
-    assert_close("dh0", dh0[rows], dh0r, w.T)
+    acc = {n: Streamed(n) for n in ("dA", "db", "dh0")}
+    for r0 in range(0, w.B, 4):
+        rows = slice(r0, min(w.B, r0 + 4))
+        A, bb, h0, g = (d[k][rows].cpu() for k in ("A", "b", "h0", "grad_h"))
+        dAr, dbr, dh0r = oracle.mas_bwd(A, bb, h0, g)
+        acc["dA"].add(dA[rows], dAr)
+        acc["db"].add(db[rows], dbr)
+        acc["dh0"].add(dh0[rows], dh0r)
+        del A, bb, h0, g, dAr, dbr, dh0r
+    for a in acc.values():
+        a.check(w.T)
 
 
 def test_mas_recompute_T0_and_errors():
@@ -263,10 +276,28 @@ def test_psl_shapes(B, T, D, h0):
     _run_psl(B, T, D, seed=300 + B * T + D, with_h0=h0)
 
 
-def test_psl_config3_sampled_rows():
+def test_psl_config3_full():
+    """Full benchmark size (B=64, T=4096, D=1024), every element of h, log h
+    and the three gradients compared (streamed over groups of 8 batch rows)."""
     w = inputs.WORKLOADS[3]
     d = w.make(device="cuda")
-    _check_psl(d, w.T, rows=[0, 33, w.B - 1])
+    h, lh = api.parallel_scan_log_fwd(d["log_coeffs"], d["log_values"], d["log_h0"], want_log=True)
+    dlc, dlv, dl0 = api.parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], h, d["grad_h"])
+    b.mgs_check()
+    acc = {n: Streamed(n) for n in ("h", "log_h", "d_log_coeffs", "d_log_values", "d_log_h0")}
+    for r0 in range(0, w.B, 8):
+        rows = slice(r0, min(w.B, r0 + 8))
+        lc, lv, l0, g = (d[k][rows].cpu() for k in ("log_coeffs", "log_values", "log_h0", "grad_h"))
+        href, lhref = oracle.psl_fwd(lc, lv, l0, want_log=True)
+        acc["h"].add(h[rows], href)
+        acc["log_h"].add(lh[rows], lhref)
+        dlcr, dlvr, dl0r = oracle.psl_bwd(lc, lv, l0, g)
+        acc["d_log_coeffs"].add(dlc[rows], dlcr)
+        acc["d_log_values"].add(dlv[rows], dlvr)
+        acc["d_log_h0"].add(dl0[rows], dl0r)
+        del lc, lv, l0, g, href, lhref, dlcr, dlvr, dl0r
+    for a in acc.values():
+        a.check(w.T)
 
 
 def test_psl_zero_coefficients_and_empty():
@@ -308,17 +339,24 @@ def test_psl_recompute_backward(B, T, D, h0):
             assert_close(name + " (vs saved h)", x, y.double().cpu().numpy(), T, rel_tol=1e-6, abs_tol=1e-5)
 
 
-def test_psl_recompute_config3_sampled_rows():
+def test_psl_recompute_config3_full():
+    """Full benchmark size, recompute mode (h not saved), every element of the
+    three gradients compared (streamed over groups of 8 batch rows)."""
     w = inputs.WORKLOADS[3]
     d = w.make(device="cuda")
     dlc, dlv, dl0 = api.parallel_scan_log_bwd(d["log_coeffs"], d["log_values"], d["log_h0"], None, d["grad_h"])
     b.mgs_check()
-    rows = [0, 33, w.B - 1]
-    dlcr, dlvr, dl0r = oracle.psl_bwd(*(d[k][rows].cpu() for k in ("log_coeffs", "log_values", "log_h0",
-                                                                   "grad_h")))
-    assert_close("d_log_coeffs", dlc[rows], dlcr, w.T)
-    assert_close("d_log_values", dlv[rows], dlvr, w.T)
-    assert_close("d_log_h0", dl0[rows], dl0r, w.T)
+    acc = {n: Streamed(n) for n in ("d_log_coeffs", "d_log_values", "d_log_h0")}
+    for r0 in range(0, w.B, 8):
+        rows = slice(r0, min(w.B, r0 + 8))
+        dlcr, dlvr, dl0r = oracle.psl_bwd(*(d[k][rows].cpu() for k in ("log_coeffs", "log_values", "log_h0",
+                                                                       "grad_h")))
+        acc["d_log_coeffs"].add(dlc[rows], dlcr)
+        acc["d_log_values"].add(dlv[rows], dlvr)
+        acc["d_log_h0"].add(dl0[rows], dl0r)
+        del dlcr, dlvr, dl0r
+    for a in acc.values():
+        a.check(w.T)
 
 
 def test_psl_recompute_autograd_and_T0():
