@@ -139,8 +139,8 @@ mgs_status mgs_matrix_affine_scan_bwd_recompute(const float *A, const float *b, 
  * row): prefix products
  *     P_t = A_t P_{t-1},   P_0 = I,   per (batch, head) lane.
  * In: A [B][T][H][k][k].  Out: P [B][T][H][k][k].
- * Long sequences with few lanes are split into time chunks that exchange
- * carries through the workspace (see mgs_workspace_size). */
+ * Long sequences with few lanes are split into time chunks whose aggregates
+ * and carries go through the workspace (see mgs_workspace_size). */
 mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, int64_t H, int k,
                                void *workspace, size_t workspace_bytes, mgs_stream_t stream);
 
@@ -166,9 +166,9 @@ mgs_status mgs_matrix_scan_fwd(const float *A, float *P, int64_t B, int64_t T, i
  * address is cached per device context: if the context is destroyed and
  * created again (cudaDeviceReset), the next call looks it up again.
  * All calls on a device share the one array, which keeps the previous call's
- * contents; each call clears the part that must start at zero (an async
- * memset on `stream`).  Calls that overlap on the GPU, e.g. on two unordered
- * streams, race on the array: order them. */
+ * contents; a call writes every part of it that it reads before reading it,
+ * so nothing needs to start at zero.  Calls that overlap on the GPU, e.g. on
+ * two unordered streams, race on the array: order them. */
 mgs_status mgs_matrix_scan_fwd_noalloc(const float *A, float *P, int64_t B, int64_t T, int64_t H,
                                        int k, mgs_stream_t stream);
 

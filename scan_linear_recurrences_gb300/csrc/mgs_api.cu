@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -205,15 +206,18 @@ cudaError_t cached_symbol_address(SymbolAddressCache &cache, const void *symbol,
 }
 
 cudaError_t ensure_smem_attr(const void *fn, int bytes) {
+    // the limit set for each kernel in each device context; raised (to the
+    // opt-in maximum) when a launch needs more than the 48 KB default
     static std::mutex mu;
-    static std::set<std::pair<const void *, uint64_t>> done;
+    static std::map<std::pair<const void *, uint64_t>, int> limit;
     const uint64_t ctx = current_context_id();
+    const int want = bytes > 48 * 1024 ? 227 * 1024 : 48 * 1024;
     std::lock_guard<std::mutex> lk(mu);
     auto key = std::make_pair(fn, ctx);
-    if (ctx != 0 && done.count(key)) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         bytes > 48 * 1024 ? 227 * 1024 : 48 * 1024);
-    if (e == cudaSuccess && ctx != 0) done.insert(key);
+    auto itr = limit.find(key);
+    if (ctx != 0 && itr != limit.end() && itr->second >= want) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (e == cudaSuccess && ctx != 0) limit[key] = want;
     return e;
 }
 

@@ -1,7 +1,21 @@
-// Shared machinery of the time-chunked kernels (matrix_scan and
-// matrix_affine_scan): a shape-only chunk plan, the workspace layout, flag
-// publication and the bounded look-back wait, and small k x k helpers.
+// Shared machinery of the time-chunked path of matrix_scan and
+// matrix_affine_scan (few lanes, long sequences): a shape-only chunk plan, the
+// workspace layout, the carry-chain kernel and small k x k helpers.
+//
+// The path is a reduce-then-scan in three launches on the caller's stream:
+//   1. every chunk but the last in carry order (the first for the backward)
+//      computes its aggregate - the chunk's map from its incoming carry to its
+//      outgoing one - from the identity;
+//   2. one block per lane group bulk-copies that group's aggregates into
+//      shared memory and composes them in carry order, writing the incoming
+//      carry of every chunk;
+//   3. every chunk reruns its recurrence from its carry and writes outputs.
+// Stream order is the only synchronisation: no flags, no waits on other
+// blocks, no zeroing of the workspace, and every run adds in the same order,
+// so results are reproducible bit for bit.
 #pragma once
+
+#include <utility>
 
 #include "mgs_tiles.cuh"
 
@@ -96,26 +110,22 @@ __host__ __device__ inline ChunkPlan plan_chunks(int64_t B, int64_t T, int64_t H
     return p;
 }
 
-// Workspace: [ticket | one flag per item | nmat slots of LPW*K*K floats per item]
-struct ChunkWs {
-    unsigned *ticket, *flags;
-    float *slots;
-    int64_t items;
-    int mf;  // floats per slot
-    __host__ __device__ static size_t header_bytes(const ChunkPlan &p) {
-        return align_up(256 + size_t(p.G * p.C) * 4, 256);
+// Workspace of the chunked path: three arrays of G*C items (lane group g,
+// chunk c at item g*C + c) - the aggregates' matrices, their offsets, and the
+// incoming carries - of mM, mC and mE floats per item, each array starting
+// on a 256-byte boundary.
+struct ScanWs {
+    float *M, *Cv, *E;
+    __host__ __device__ static size_t arr(const ChunkPlan &p, int mf) {
+        return align_up(size_t(p.G * p.C) * size_t(mf) * 4, 256);
     }
-    static size_t bytes(const ChunkPlan &p, int K, int nmat) {
-        return header_bytes(p) + size_t(nmat) * size_t(p.G * p.C) * (32 / K) * K * K * 4;
+    __host__ __device__ static size_t bytes(const ChunkPlan &p, int mM, int mC, int mE) {
+        return arr(p, mM) + arr(p, mC) + arr(p, mE);
     }
-    __device__ ChunkWs(unsigned char *ws, const ChunkPlan &p, int mf_)
-        : ticket(reinterpret_cast<unsigned *>(ws)), flags(reinterpret_cast<unsigned *>(ws + 256)),
-          slots(reinterpret_cast<float *>(ws + header_bytes(p))), items(p.G * p.C), mf(mf_) {}
-    // slot m of item
-    __device__ float *slot(int m, int64_t item) const { return slots + (m * items + item) * mf; }
+    __host__ __device__ ScanWs(unsigned char *ws, const ChunkPlan &p, int mM, int mC)
+        : M(reinterpret_cast<float *>(ws)), Cv(reinterpret_cast<float *>(ws + arr(p, mM))),
+          E(reinterpret_cast<float *>(ws + arr(p, mM) + arr(p, mC))) {}
 };
-
-enum : unsigned { FLAG_AGG = 1u, FLAG_INCL = 2u };
 
 // Column `col` of a k x k row-major matrix in the workspace (bypassing L1).
 template <int K>
@@ -127,93 +137,6 @@ template <int K>
 __device__ __forceinline__ void st_ws_col(float *mat, int col, const float (&x)[K]) {
 #pragma unroll
     for (int i = 0; i < K; ++i) __stcg(mat + i * K + col, x[i]);
-}
-
-// y = X x, where X is held one column per thread of the k-group (this thread
-// holds column `col` in xc): X goes through the warp's exchange buffer.
-template <int K>
-__device__ __forceinline__ void group_matvec(float *xw, int col, const float (&xc)[K], const float (&x)[K],
-                                             float (&y)[K]) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) xw[i * K + col] = xc[i];
-    __syncwarp();
-    smem_matvec<K>(xw, x, y);
-    __syncwarp();
-}
-
-// Publishes `value` for this item once the whole warp has stored its data.
-// The warp barrier orders every lane's data stores before lane 0's fence and
-// release store (one fence per warp rather than one per lane).
-__device__ __forceinline__ void publish(unsigned *flag, unsigned value, int lane) {
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence();
-        st_release_gpu(flag, value);
-    }
-    __syncwarp();
-}
-
-// Lane 0 waits (bounded) for a nonzero flag and broadcasts the value it saw;
-// that broadcast value alone drives control flow, so the warp never diverges
-// even if the flag advances (1 -> 2) meanwhile.  Each lane then acquires the
-// flag itself until it reads a value at least that new (flags only grow), so
-// its own later loads see the data published before that value.  Returns 0,
-// uniformly, on timeout.
-__device__ __forceinline__ unsigned lookback_flag(const unsigned *flag, int lane, const DevCtl &ctl) {
-    unsigned f = 0;
-    if (lane == 0) f = wait_flag_bounded(flag, ctl.timeout_ns);
-    f = __shfl_sync(0xffffffffu, f, 0);
-    if (f == 0) return 0;
-    bool ok = true;
-    unsigned v = ld_acquire_gpu(flag);
-    if (v < f) {
-        const uint64_t t0 = global_ns();
-        while (v < f) {
-            __nanosleep(32);
-            v = ld_acquire_gpu(flag);
-            if (v < f && global_ns() - t0 > ctl.timeout_ns) {
-                ok = false;
-                break;
-            }
-        }
-    }
-    return __all_sync(0xffffffffu, ok) ? f : 0u;
-}
-
-// Windowed look-back.  Scans the items of one lane group before (dir = -1) or
-// after (dir = +1) chunk c, 32 at a time (lane j reads the flag of chunk
-// c + dir*(1 + j)), for the nearest one whose inclusive value is published,
-// waiting (bounded) until every chunk between it and c has published at least
-// its aggregate.  Returns that chunk index, or -1 after the timeout; the result
-// is uniform across the warp.  Each lane acquires the flag it reads and the
-// closing __syncwarp (which orders memory among the warp's lanes) lets every
-// lane read the data of all the chunks in the window.
-__device__ __forceinline__ int64_t find_inclusive(const unsigned *flags, int64_t c, int dir, int64_t C, int lane,
-                                                  const DevCtl &ctl) {
-    const uint64_t t0 = global_ns();
-    for (int64_t base = c + dir; base >= 0 && base < C; base += int64_t(dir) * 32) {
-        const int64_t p = base + int64_t(dir) * lane;
-        const bool valid = p >= 0 && p < C;
-        unsigned f = valid ? ld_acquire_gpu(flags + p) : 0u;
-        while (true) {
-            const unsigned incl = __ballot_sync(0xffffffffu, valid && f == FLAG_INCL);
-            const int first = incl ? __ffs(int(incl)) - 1 : 32;
-            const bool need = valid && lane < first;
-            const unsigned missing = __ballot_sync(0xffffffffu, need && f == 0u);
-            if (missing == 0u) {
-                if (first < 32) {
-                    __syncwarp();
-                    return base + int64_t(dir) * first;
-                }
-                break;  // 32 aggregates: look further
-            }
-            const bool late = (lane == 0) && (global_ns() - t0 > ctl.timeout_ns);
-            if (__any_sync(0xffffffffu, late)) return -1;
-            __nanosleep(64);
-            if (need && f == 0u) f = ld_acquire_gpu(flags + p);
-        }
-    }
-    return -1;
 }
 
 // K consecutive floats from global memory through L2 (16-byte loads when K >= 4).
@@ -263,6 +186,184 @@ __device__ __forceinline__ void ld_ws_mat(const float *m, float (&r)[K][K]) {
 #pragma unroll
             for (int j = 0; j < K; ++j) r[i][j] = __ldcg(m + i * K + j);
     }
+}
+
+
+// ---------------------------------------------------------------- carry chain
+// Launch 2 of the chunked path: one block (one warp) per lane group g, over
+// the group's aggregates in carry order.  DIR = +1 (forward scans):
+//     E_0 = initial state,   E_{p+1} = M_p E_p (+ C_p),   p = 0 .. C-2;
+// DIR = -1 (backward scans):
+//     E_{C-1} = 0,           E_{p-1} = M_p E_p + C_p,     p = C-1 .. 1.
+// MAT: the carries are k x k matrices (matrix_scan), thread (lane, col) of a
+// lane's k-group holding column col; otherwise k-vectors (matrix_affine_scan),
+// every thread of the group holding the whole vector (k^2 FMAs, no shuffles)
+// and storing its own element.  The aggregates come into shared memory by 1-D
+// bulk copies, `nb` per batch in two alternating buffers, so their loads are
+// all in flight at once instead of one memory latency per step.
+// Per item floats: mM = LPW k^2; mC (and mE) = LPW k^2 (MAT) or LPW k.
+template <int K, bool MAT, bool HASC, int DIR>
+__global__ void __launch_bounds__(32)
+    chain_kernel(const float *__restrict__ Ms, const float *__restrict__ Cs, float *__restrict__ Es,
+                 const float *__restrict__ init, int64_t C, int64_t gpb, int64_t H, int nb, DevCtl ctl) {
+    constexpr int LPW = 32 / K;
+    constexpr int mM = LPW * K * K, mC = MAT ? LPW * K * K : LPW * K, mE = mC;
+    constexpr int STEPF = mM + (HASC ? mC : 0);
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *buf = reinterpret_cast<float *>(smem_raw);  // 2 buffers of nb * STEPF floats
+    uint64_t *bars = reinterpret_cast<uint64_t *>(buf + 2 * size_t(nb) * STEPF);
+
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x;
+    const int64_t bi = g / gpb;
+    const int head0 = int(g - bi * gpb) * LPW;
+    const int sub = lane / K, col = lane % K;
+    const bool active = head0 + sub < H;
+    const int64_t nsteps = C - 1;
+    const int64_t nbat = (nsteps + nb - 1) / nb;
+    if (lane == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    // launched as a programmatic dependent of launch 1: wait for its
+    // aggregates, then let launch 3 be scheduled
+    pdl_wait();
+    pdl_trigger();
+    const uint64_t pol = policy_evict_first();
+    // batch bt: steps [bt*nb, bt*nb + n); their aggregates are the contiguous
+    // items g*C + plo .. g*C + plo + n - 1
+    auto batch_n = [&](int64_t bt) { return int(min64(nb, nsteps - bt * nb)); };
+    auto batch_plo = [&](int64_t bt) { return DIR > 0 ? bt * nb : C - bt * nb - batch_n(bt); };
+    auto issue = [&](int64_t bt) {  // lane 0 only
+        const int n = batch_n(bt), b = int(bt & 1);
+        const int64_t it0 = g * C + batch_plo(bt);
+        float *dst = buf + size_t(b) * nb * STEPF;
+        mbar_arrive_expect_tx(&bars[b], uint32_t(n) * STEPF * 4u);
+        bulk_g2s(dst, Ms + it0 * mM, uint32_t(n) * mM * 4u, &bars[b], pol);
+        if constexpr (HASC) bulk_g2s(dst + size_t(n) * mM, Cs + it0 * mC, uint32_t(n) * mC * 4u, &bars[b], pol);
+    };
+    if (lane == 0) {
+        if (nbat > 0) issue(0);
+        if (nbat > 1) issue(1);
+    }
+
+    // the carry of the first chunk in carry order
+    float x[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) x[i] = 0.f;
+    if constexpr (MAT) {
+        if (DIR > 0) {  // P_0 = I
+#pragma unroll
+            for (int i = 0; i < K; ++i) x[i] = (i == col) ? 1.f : 0.f;
+        }
+    } else {
+        if (DIR > 0 && init != nullptr && active) lds_row_global<K>(init + (bi * H + head0 + sub) * K, x);
+    }
+    auto store = [&](int64_t chunk) {
+        if (!active) return;
+        float *e = Es + (g * C + chunk) * mE;
+        if constexpr (MAT) {
+            st_ws_col<K>(e + sub * K * K, col, x);
+        } else {
+            float v = x[0];
+#pragma unroll
+            for (int i = 1; i < K; ++i) v = (i == col) ? x[i] : v;
+            __stcg(e + sub * K + col, v);
+        }
+    };
+    store(DIR > 0 ? 0 : C - 1);
+
+    uint32_t phase = 0;
+    for (int64_t bt = 0; bt < nbat; ++bt) {
+        const int b = int(bt & 1);
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[b], (phase >> b) & 1u, ctl.timeout_ns));
+        if (!ok) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            // the other buffer may still have a copy in flight
+            if (bt + 1 < nbat && !mbar_wait_bounded(&bars[b ^ 1], (phase >> (b ^ 1)) & 1u, ctl.timeout_ns) &&
+                lane == 0)
+                record_error(ctl, ERR_DRAIN_TIMEOUT);
+            __syncwarp();
+            return;
+        }
+        phase ^= 1u << b;
+        const int n = batch_n(bt);
+        const float *sm = buf + size_t(b) * nb * STEPF;
+        const float *sc = sm + size_t(n) * mM;
+        for (int q = 0; q < n; ++q) {
+            const int idx = DIR > 0 ? q : n - 1 - q;  // position of this step's aggregate in the batch
+            const float *Mp = sm + idx * mM + sub * K * K;
+            float y[K];
+#pragma unroll
+            for (int i = 0; i < K; ++i) {
+                float r[K];
+                lds_row_smem<K>(Mp + i * K, r);
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < K; ++m) {
+                    if (m & 1) s1 = fmaf(r[m], x[m], s1);
+                    else s0 = fmaf(r[m], x[m], s0);
+                }
+                y[i] = s0 + s1;
+            }
+            if constexpr (HASC) {
+#pragma unroll
+                for (int i = 0; i < K; ++i)
+                    y[i] += MAT ? sc[idx * mC + sub * K * K + i * K + col] : sc[idx * mC + sub * K + i];
+            }
+#pragma unroll
+            for (int i = 0; i < K; ++i) x[i] = y[i];
+            const int64_t k = bt * nb + q;
+            store(DIR > 0 ? k + 1 : C - 2 - k);
+        }
+        __syncwarp();
+        if (bt + 2 < nbat && lane == 0) {
+            fence_proxy_async_smem();
+            issue(bt + 2);
+        }
+    }
+}
+
+// Launches a one-warp-per-block kernel as a programmatic dependent of the
+// previous kernel in the stream (the kernel calls pdl_wait() before reading
+// what that kernel wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, int smem, cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Aggregates per batch of the chain kernel: about 48 KB of shared memory per
+// buffer, at most the whole chain.
+inline int chain_batch(int64_t C, int step_floats) {
+    const int64_t nb = (48 * 1024) / (int64_t(step_floats) * 4);
+    return int(nb < 1 ? 1 : (nb > C - 1 ? C - 1 : nb));
+}
+inline size_t chain_smem(int nb, int step_floats) { return size_t(2) * nb * step_floats * 4 + 2 * sizeof(uint64_t); }
+
+// Launches the chain kernel for lane-group count G.
+template <int K, bool MAT, bool HASC, int DIR>
+cudaError_t launch_chain(const float *Ms, const float *Cs, float *Es, const float *init, int64_t G, int64_t C,
+                         int64_t gpb, int64_t H, const DevCtl &ctl, cudaStream_t s) {
+    constexpr int LPW = 32 / K;
+    constexpr int stepf = LPW * K * K + (HASC ? (MAT ? LPW * K * K : LPW * K) : 0);
+    const int nb = chain_batch(C, stepf);
+    const int smem = int(chain_smem(nb, stepf));
+    cudaError_t e = ensure_smem_attr((const void *)chain_kernel<K, MAT, HASC, DIR>, smem);
+    if (e != cudaSuccess) return e;
+    if (G > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    return launch_pdl(chain_kernel<K, MAT, HASC, DIR>, dim3(unsigned(G)), smem, s, Ms, Cs, Es, init, C, gpb, H, nb, ctl);
 }
 
 }  // namespace mgs

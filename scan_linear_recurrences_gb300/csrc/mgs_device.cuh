@@ -108,10 +108,25 @@ __device__ __forceinline__ unsigned wait_flag_bounded(const unsigned *flag, uint
     }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before the previous kernel in the stream ends;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible (it returns at once for a normal launch).  pdl_trigger() lets the
+// next such kernel be scheduled once every block of this one has called it
+// or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // L2 eviction hint for data streamed once.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// L2 eviction hint for data read again shortly (by a later launch).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

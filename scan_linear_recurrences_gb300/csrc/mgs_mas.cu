@@ -25,14 +25,15 @@ namespace {
 #ifndef MGS_MAS_FWD_TS8
 #define MGS_MAS_FWD_TS8 8
 #endif
-template <int K, bool FWD = false>
+// NSX: stages in flight when nonzero, else the tuned default.
+template <int K, bool FWD = false, int NSX = 0>
 struct MasShape {
     static constexpr int LPW = 32 / K;          // lanes (heads) per warp
     static constexpr int AF = LPW * K * K;      // floats of A per time step
     static constexpr int VF = LPW * K;          // floats of one per-lane vector per time step
     // time steps per stage: about 8-10 KB of A per stage
     static constexpr int TS = K >= 16 ? 4 : (K >= 8 ? (FWD ? MGS_MAS_FWD_TS8 : 8) : 16);
-    static constexpr int NS = FWD ? MGS_MAS_FWD_NS : 4;  // stages in flight
+    static constexpr int NS = NSX ? NSX : (FWD ? MGS_MAS_FWD_NS : 4);  // stages in flight
     using TA = MatTile<K, false>;
     using TV = HeadTile<K, LPW>;
 };
@@ -99,12 +100,12 @@ __device__ __forceinline__ float group_reduce_scatter(const float (&p)[K], int r
 }
 
 // ---------------------------------------------------------------- forward
-template <int K>
+template <int K, int NSX>
 __global__ void __launch_bounds__(32)
     mas_fwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float *__restrict__ h0, float *__restrict__ h, int64_t B, int64_t T,
                    int64_t H, int64_t groups_per_b, DevCtl ctl) {
-    using S = MasShape<K, true>;
+    using S = MasShape<K, true, NSX>;
     constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
     using R = Ring<STAGEF, S::NS, S::TA::kAlign>;
     constexpr int SSTR = int(R::stage_stride / sizeof(float));
@@ -190,13 +191,13 @@ __global__ void __launch_bounds__(32)
 }
 
 // ---------------------------------------------------------------- backward
-template <int K>
+template <int K, int NSX>
 __global__ void __launch_bounds__(32)
     mas_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
                    const __grid_constant__ CUtensorMap tmH, const float *__restrict__ h0,
                    float *__restrict__ dA, float *__restrict__ db, float *__restrict__ dh0, int64_t B,
                    int64_t T, int64_t H, int64_t groups_per_b, DevCtl ctl) {
-    using S = MasShape<K>;
+    using S = MasShape<K, false, NSX>;
     constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
     constexpr int STAGEF = A_STAGE + 2 * V_STAGE;  // A_t, g_t, h_{t-1}
     using R = Ring<STAGEF, S::NS, S::TA::kAlign>;
@@ -540,10 +541,10 @@ cudaError_t mas_bwd_rc_t(const float *A, const float *b, const float *h0, const 
     return cudaGetLastError();
 }
 
-template <int K>
-cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
-                      int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
-    using S = MasShape<K, true>;
+template <int K, int NSX>
+cudaError_t mas_fwd_launch(const float *A, const float *b, const float *h0, float *h, int64_t B, int64_t T,
+                           int64_t H, const DevCtl &ctl, cudaStream_t s) {
+    using S = MasShape<K, true, NSX>;
     using R = Ring<S::TS * (S::AF + S::VF), S::NS, S::TA::kAlign>;
     CUtensorMap tA, tB;
     cudaError_t e;
@@ -553,16 +554,22 @@ cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h,
     const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(R::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)mas_fwd_kernel<K>, smem)) != cudaSuccess) return e;
-    mas_fwd_kernel<K><<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tB, h0, h, B, T, H, gpb, ctl);
+    const auto kern = mas_fwd_kernel<K, NSX>;
+    if ((e = ensure_smem_attr((const void *)kern, smem)) != cudaSuccess) return e;
+    kern<<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tB, h0, h, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
 template <int K>
-cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const float *gh, float *dA,
-                      float *db, float *dh0, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
-                      cudaStream_t s) {
-    using S = MasShape<K>;
+cudaError_t mas_fwd_t(const float *A, const float *b, const float *h0, float *h, int64_t B,
+                      int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
+    return mas_fwd_launch<K, 0>(A, b, h0, h, B, T, H, ctl, s);
+}
+
+template <int K, int NSX>
+cudaError_t mas_bwd_launch(const float *A, const float *h0, const float *h, const float *gh, float *dA, float *db,
+                           float *dh0, int64_t B, int64_t T, int64_t H, const DevCtl &ctl, cudaStream_t s) {
+    using S = MasShape<K, false, NSX>;
     using R = Ring<S::TS * (S::AF + 2 * S::VF), S::NS, S::TA::kAlign>;
     CUtensorMap tA, tG, tH;
     cudaError_t e;
@@ -573,21 +580,27 @@ cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const flo
     const int64_t blocks = B * gpb;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const int smem = int(R::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)mas_bwd_kernel<K>, smem)) != cudaSuccess) return e;
-    mas_bwd_kernel<K><<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tG, tH, h0, dA, db, dh0, B, T, H, gpb, ctl);
+    const auto kern = mas_bwd_kernel<K, NSX>;
+    if ((e = ensure_smem_attr((const void *)kern, smem)) != cudaSuccess) return e;
+    kern<<<dim3(unsigned(blocks)), 32, smem, s>>>(tA, tG, tH, h0, dA, db, dh0, B, T, H, gpb, ctl);
     return cudaGetLastError();
 }
 
+template <int K>
+cudaError_t mas_bwd_t(const float *A, const float *h0, const float *h, const float *gh, float *dA,
+                      float *db, float *dh0, int64_t B, int64_t T, int64_t H, const DevCtl &ctl,
+                      cudaStream_t s) {
+    return mas_bwd_launch<K, 0>(A, h0, h, gh, dA, db, dh0, B, T, H, ctl, s);
+}
+
 // ================================================================ time-chunked path
-// Few lanes and a long sequence: T is split into C chunks and one warp handles
-// one (lane group, chunk) item, as for matrix_scan.  The forward aggregate of a
-// chunk is the affine map h_end = M h_in + c with M = A_e ... A_s (built one
-// column per thread: M[:, j] <- A_t M[:, j], broadcast reads of A_t, no
-// shuffles) and c the chunk's own recurrence from h = 0.  The backward
-// aggregate is mu_out = M mu_in + C with M = A_s^T ... A_e^T.  The look-back
-// keeps its running map by rows (thread r holds row r), reading each
-// predecessor's (M, c) or inclusive value straight from the workspace (L2).
-// Workspace slots per item: 0 = M, 1 = c (first LPW*k floats), 2 = inclusive.
+// Few lanes and a long sequence: T is split into C chunks, one warp per
+// (lane group, chunk) item, as for matrix_scan (the three launches of
+// mgs_chunk.cuh).  The forward aggregate of a chunk is the affine map
+// h_end = M h_in + c with M = A_e ... A_s (built one column per thread:
+// M[:, j] <- A_t M[:, j], broadcast reads of A_t, no shuffles) and c the
+// chunk's own recurrence from h = 0.  The backward aggregate is
+// mu_out = M mu_in + C with M = A_s^T ... A_e^T.
 
 template <int K>
 struct MasChunkShape {
@@ -599,114 +612,146 @@ struct MasChunkShape {
     using TV = HeadTile<K, LPW>;
 };
 
-template <int STAGEF, int NS, int XF, size_t ALIGN>
+template <int STAGEF, int NS, size_t ALIGN>
 struct ChunkRing {
     static constexpr size_t stage_bytes = size_t(STAGEF) * sizeof(float);  // transferred per full stage
     static constexpr size_t stage_stride = align_up(stage_bytes, ALIGN);
     static constexpr size_t ring_bytes = NS * stage_stride;
-    static constexpr size_t xch_offset = ring_bytes;
-    static constexpr size_t bar_offset = align_up(ring_bytes + size_t(XF) * sizeof(float), 16);
+    static constexpr size_t bar_offset = ring_bytes;
     static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128) + ALIGN;
 };
 
-// Look-back for a row-held affine carry.  Finds the nearest chunk in direction
-// `dir` (-1: earlier, forward scan; +1: later, backward scan) whose inclusive
-// value is published, then applies the aggregates (M_p, c_p) of the chunks
-// between it and this one, nearest to it first: x <- M_p x + c_p.  Thread r
-// holds row element r; each step needs row r of M_p and x gathered across the
-// k-group.  The rows of the next 8 aggregates are in flight while one
-// is applied (each is an L2 round trip, long against the k FMAs of a step).
-// Returns false (uniformly) on timeout.
-// (4 for k = 16, where 8 would not fit in registers)
-template <int K>
-constexpr int fold_ahead() { return K >= 16 ? 4 : 8; }
-
-template <int K>
-__device__ bool lookback_affine(const ChunkWs &w, int64_t g, int64_t C, int64_t c, int dir, int sub, int r,
-                                int gbase, int lane, const DevCtl &ctl, float &hin) {
-    const int64_t ps = find_inclusive(w.flags + g * C, c, dir, C, lane, ctl);
-    if (ps < 0) return false;
-    float x = __ldcg(w.slot(2, g * C + ps) + sub * K + r);
-    // aggregates p_k = ps - dir (k + 1), k = 0 .. cnt-1 (the last is next to c)
-    const int64_t cnt = (c - ps) * (-dir) - 1;
-    auto load = [&](int64_t k, float (&mrow)[K], float &cp) {
-        const int64_t p = ps - dir * (k + 1);
-        lds_row_global<K>(w.slot(0, g * C + p) + sub * K * K + r * K, mrow);
-        cp = __ldcg(w.slot(1, g * C + p) + sub * K + r);
-    };
-    constexpr int kFoldAhead = fold_ahead<K>();
-    float mq[kFoldAhead][K], cq[kFoldAhead];
-#pragma unroll
-    for (int d = 0; d < kFoldAhead; ++d)
-        if (d < cnt) load(d, mq[d], cq[d]);
-    for (int64_t k0 = 0; k0 < cnt; k0 += kFoldAhead) {
-#pragma unroll
-        for (int d = 0; d < kFoldAhead; ++d) {
-            const int64_t k = k0 + d;
-            if (k < cnt) {  // warp-uniform
-                float acc = cq[d];
-#pragma unroll
-                for (int m = 0; m < K; ++m) acc = fmaf(mq[d][m], __shfl_sync(0xffffffffu, x, gbase + m), acc);
-                x = acc;
-                if (k + kFoldAhead < cnt) load(k + kFoldAhead, mq[d], cq[d]);
-            }
-        }
+// Item -> (lane group, chunk) and the lane group's place in the batch.
+struct ChunkItem {
+    int64_t g, c, bi;
+    int head0;
+    __device__ ChunkItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int lpw) {
+        const unsigned q = unsigned(item) / unsigned(nper);  // 32-bit: items, nper and gpb are below 2^32
+        g = q;
+        c = cfirst + (item - int64_t(q) * nper);
+        const unsigned b32 = q / unsigned(gpb);
+        bi = b32;
+        head0 = int(q - b32 * unsigned(gpb)) * lpw;
     }
-    hin = x;
-    return true;
-}
+};
 
-// Inclusive value of this item: out[r] = sum_m M[r][m] hin[m] + cv, with M held
-// by columns (mcol) and hin by rows; both go through the exchange buffer.
-template <int K>
-__device__ __forceinline__ float affine_apply(float *xw, int r, int gbase, const float (&mcol)[K], float hin,
-                                              float cv) {
-#pragma unroll
-    for (int i = 0; i < K; ++i) xw[i * K + r] = mcol[i];
-    __syncwarp();
-    float acc = cv;
-#pragma unroll
-    for (int m = 0; m < K; ++m) acc = fmaf(xw[r * K + m], __shfl_sync(0xffffffffu, hin, gbase + m), acc);
-    __syncwarp();
-    return acc;
-}
+// The chunked path is the reduce-then-scan of mgs_chunk.cuh:
+//   forward:  aggregate h_end = M h_in + c of chunks 0 .. C-2 (M = A_e ... A_s
+//             built one column per thread, c the chunk's recurrence from zero),
+//             carries E_0 = h0, E_{p+1} = M_p E_p + c_p, then every chunk's
+//             recurrence from its carry;
+//   backward: aggregate mu_out = M mu_in + C of chunks 1 .. C-1 (M = A_s^T ...
+//             A_e^T), carries mu_in(C-1) = 0, mu_in(p-1) = M_p mu_in(p) + C_p,
+//             then every chunk's adjoint from its carry.
 
+// Launch 1, forward.
 template <int K>
 __global__ void __launch_bounds__(32)
-    mas_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const float *__restrict__ h0, float *__restrict__ h, unsigned char *__restrict__ ws,
-                         int64_t B, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    mas_fwd_agg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       float *__restrict__ Ms, float *__restrict__ Cs, int64_t T, int64_t gpb, int64_t C, int64_t Lc,
+                       DevCtl ctl) {
     using S = MasChunkShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
-    using R = ChunkRing<STAGEF, S::NS, S::AF, S::TA::kAlign>;
+    using R = ChunkRing<STAGEF, S::NS, S::TA::kAlign>;
     constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
     float *ring = reinterpret_cast<float *>(sbase);
-    float *xch = reinterpret_cast<float *>(sbase + R::xch_offset);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
 
     const int lane = threadIdx.x;
-    const int64_t G = B * gpb;
-    const ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::AF);
-    unsigned item = 0;
-    if (lane == 0) item = atomicAdd(w.ticket, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    if (int64_t(item) >= G * C) return;
-
-    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
-    const int64_t c = q32, g = item - q32 * unsigned(G), iself = g * C + c;
-    const unsigned b32 = unsigned(g) / unsigned(gpb);
-    const int64_t bi = b32;
-    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
-    const int nl = int(min64(S::LPW, H - head0));
+    const ChunkItem it(blockIdx.x, C - 1, 0, gpb, S::LPW);
     const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
-    const bool active = sub < nl;
-    const int64_t tb = c * Lc, len = min64(Lc, T - tb);
-    const int64_t n1 = (len + S::TS - 1) / S::TS;
-    const bool two_pass = c > 0;
-    const int64_t nb = two_pass ? 2 * n1 : n1;
-    float *xw = xch + sub * K * K;
+    const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
+    const int64_t nb = (len + S::TS - 1) / S::TS;
+
+    WarpRing<S::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();  // launch 3 reads the chunk again
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * SSTR;
+        const int row = int(it.bi * T + tb + j * S::TS);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
+        S::TA::load(st, &tmA, it.head0, row, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmB, it.head0, row, &bars[s], pol);
+    };
+    const int npro = int(min64(S::NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float cv = 0.f;  // row r of the chunk offset c
+    float mcol[K];   // column r of the chunk matrix M
+#pragma unroll
+    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % S::NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int n = int(min64(S::TS, len - j * S::TS));
+        const float *st = ring + size_t(s) * SSTR;
+#pragma unroll
+        for (int u = 0; u < S::TS; ++u) {
+            if (u < n) {
+                const TileRef<K> Ablk{st, u, sub};
+                float a[K];
+                Ablk.row(r, a);
+                float acc0 = st[A_STAGE + u * S::VF + sub * K + r], acc1 = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < K; ++jj) {
+                    const float x = __shfl_sync(0xffffffffu, cv, gbase + jj);
+                    if (jj & 1) acc1 = fmaf(a[jj], x, acc1);
+                    else acc0 = fmaf(a[jj], x, acc0);
+                }
+                cv = acc0 + acc1;
+                float nm[K];
+                tile_matvec(Ablk, mcol, nm);
+#pragma unroll
+                for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+            }
+        }
+        __syncwarp();
+        if (j + S::NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + S::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    const int64_t item = it.g * C + it.c;
+    st_ws_col<K>(Ms + item * S::AF + sub * K * K, r, mcol);
+    __stcg(Cs + item * S::VF + sub * K + r, cv);
+}
+
+// Launch 3, forward: h_t from the chunk's carry (all chunks).
+template <int K>
+__global__ void __launch_bounds__(32)
+    mas_fwd_out_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       float *__restrict__ h, const float *__restrict__ Es, int64_t T, int64_t H, int64_t gpb,
+                       int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MasChunkShape<K>;
+    constexpr int A_STAGE = S::TS * S::AF, STAGEF = A_STAGE + S::TS * S::VF;
+    using R = ChunkRing<STAGEF, S::NS, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
+
+    const int lane = threadIdx.x;
+    const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
+    const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
+    const bool active = it.head0 + sub < H;
+    const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
+    const int64_t nb = (len + S::TS - 1) / S::TS;
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
@@ -715,135 +760,171 @@ __global__ void __launch_bounds__(32)
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
     }
-    auto block_t0 = [&](int64_t jj) { return tb + ((two_pass && jj >= n1) ? jj - n1 : jj) * S::TS; };
-    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
         float *st = ring + size_t(s) * SSTR;
-        const int row = int(bi * T + block_t0(jj));
+        const int row = int(it.bi * T + tb + j * S::TS);
         mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
-        S::TA::load(st, &tmA, head0, row, &bars[s], pol);
-        S::TV::load(st + A_STAGE, &tmB, head0, row, &bars[s], pol);
+        S::TA::load(st, &tmA, it.head0, row, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmB, it.head0, row, &bars[s], pol);
     };
     const int npro = int(min64(S::NS, nb));
     if (lane == 0)
         for (int s = 0; s < npro; ++s) issue(s, s);
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
-    float cv = 0.f;  // pass 1: row r of the chunk offset c
-    float mcol[K];   // pass 1: column r of the chunk matrix M
-#pragma unroll
-    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
-    float hprev = (!two_pass && h0 != nullptr && active) ? h0[(bi * H + head0 + sub) * K + r] : 0.f;
+    pdl_wait();  // the carries of launch 2
+    float hprev = __ldcg(Es + (it.g * C + it.c) * S::VF + sub * K + r);
     const int64_t hstride = H * K;
-
-    for (int64_t jj = 0; jj < nb; ++jj) {
-        const int s = int(jj % S::NS);
+    float *hout = h + (it.bi * T * H + it.head0 + sub) * K + r + tb * hstride;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % S::NS);
         if (!rg.wait(s, ctl)) {
             if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
             rg.drain(ctl, lane);
             return;
         }
-        const int64_t t0 = block_t0(jj);
-        const int n = int(min64(S::TS, tb + len - t0));
-        const bool p1 = two_pass && jj < n1;
+        const int n = int(min64(S::TS, len - j * S::TS));
         const float *st = ring + size_t(s) * SSTR;
 #pragma unroll
         for (int u = 0; u < S::TS; ++u) {
             if (u < n) {
-                const TileRef<K> Ablk{st, u, sub};
                 float a[K];
-                Ablk.row(r, a);
-                const float bval = st[A_STAGE + u * S::VF + sub * K + r];
-                const float x_in = p1 ? cv : hprev;
-                float acc0 = bval, acc1 = 0.f;
+                TileRef<K>{st, u, sub}.row(r, a);
+                float acc0 = st[A_STAGE + u * S::VF + sub * K + r], acc1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < K; ++j) {
-                    const float x = __shfl_sync(0xffffffffu, x_in, gbase + j);
-                    if (j & 1) acc1 = fmaf(a[j], x, acc1);
-                    else acc0 = fmaf(a[j], x, acc0);
+                for (int jj = 0; jj < K; ++jj) {
+                    const float x = __shfl_sync(0xffffffffu, hprev, gbase + jj);
+                    if (jj & 1) acc1 = fmaf(a[jj], x, acc1);
+                    else acc0 = fmaf(a[jj], x, acc0);
                 }
-                if (p1) {
-                    cv = acc0 + acc1;
-                    float nm[K];
-                    tile_matvec(Ablk, mcol, nm);
-#pragma unroll
-                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
-                } else {
-                    hprev = acc0 + acc1;
-                    if (active) st_cs(h + (bi * T * H + head0 + sub) * K + r + (t0 + u) * hstride, hprev);
-                }
+                hprev = acc0 + acc1;
+                if (active) st_cs(hout, hprev);
+                hout += hstride;
             }
         }
         __syncwarp();
-        if (jj + S::NS < nb) {
+        if (j + S::NS < nb) {
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(s, jj + S::NS);
+                issue(s, j + S::NS);
             }
             rg.armed(s);
         }
-        if (two_pass && jj == n1 - 1) {
-            st_ws_col<K>(w.slot(0, iself) + sub * K * K, r, mcol);
-            __stcg(w.slot(1, iself) + sub * K + r, cv);
-            publish(&w.flags[iself], FLAG_AGG, lane);
-            float hin = 0.f;
-            if (!lookback_affine<K>(w, g, C, c, -1, sub, r, gbase, lane, ctl, hin)) {
-                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
-                rg.drain(ctl, lane);
-                return;
-            }
-            // h at the end of the chunk = M h_in + c
-            const float hend = affine_apply<K>(xw, r, gbase, mcol, hin, cv);
-            __stcg(w.slot(2, iself) + sub * K + r, hend);
-            publish(&w.flags[iself], FLAG_INCL, lane);
-            hprev = hin;
-        }
-    }
-    if (!two_pass) {  // chunk 0: its final state is the inclusive value
-        __stcg(w.slot(2, iself) + sub * K + r, hprev);
-        publish(&w.flags[iself], FLAG_INCL, lane);
     }
 }
 
+// Launch 1, backward: (M, C) of chunks 1 .. C-1, t walking down the chunk.
 template <int K>
 __global__ void __launch_bounds__(32)
-    mas_bwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
-                         const __grid_constant__ CUtensorMap tmH, const float *__restrict__ h0,
-                         float *__restrict__ dA, float *__restrict__ db, float *__restrict__ dh0,
-                         unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb, int64_t C,
-                         int64_t Lc, DevCtl ctl) {
+    mas_bwd_agg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                       float *__restrict__ Ms, float *__restrict__ Cs, int64_t T, int64_t gpb, int64_t C, int64_t Lc,
+                       DevCtl ctl) {
     using S = MasChunkShape<K>;
     constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
-    constexpr int STAGEF = A_STAGE + 2 * V_STAGE;
-    using R = ChunkRing<STAGEF, S::NS, S::AF, S::TA::kAlign>;
+    constexpr int STAGEF = A_STAGE + V_STAGE;
+    using R = ChunkRing<STAGEF, S::NS, S::TA::kAlign>;
     constexpr int SSTR = int(R::stage_stride / sizeof(float));
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
     float *ring = reinterpret_cast<float *>(sbase);
-    float *xch = reinterpret_cast<float *>(sbase + R::xch_offset);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
 
     const int lane = threadIdx.x;
-    const int64_t G = B * gpb;
-    const ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::AF);
-    unsigned item = 0;
-    if (lane == 0) item = atomicAdd(w.ticket, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    if (int64_t(item) >= G * C) return;
+    const ChunkItem it(blockIdx.x, C - 1, 1, gpb, S::LPW);
+    const int sub = lane / K, r = lane % K;
+    const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t nb = (len + S::TS - 1) / S::TS;
 
-    // carries flow from the end: tickets go to the last chunk first
-    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
-    const int64_t c = C - 1 - int64_t(q32), g = item - q32 * unsigned(G), iself = g * C + c;
-    const unsigned b32 = unsigned(g) / unsigned(gpb);
-    const int64_t bi = b32;
-    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
-    const int nl = int(min64(S::LPW, H - head0));
-    const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
-    const bool active = sub < nl;
-    const int64_t tb = c * Lc, te = min64(T, tb + Lc), len = te - tb;
-    const int64_t n1 = (len + S::TS - 1) / S::TS;
-    const bool two_pass = c < C - 1;
-    const int64_t nb = two_pass ? 2 * n1 : n1;
-    float *xw = xch + sub * K * K;
+    WarpRing<S::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+    }
+    // block j covers t = te-1-j*TS down to max(tb, te-(j+1)*TS); boxes start at
+    // row te-(j+1)*TS, step u at box row TS-1-u
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        const int r0 = int(it.bi * T + te - (j + 1) * S::TS);
+        float *st = ring + size_t(s) * SSTR;
+        mbar_arrive_expect_tx(&bars[s], uint32_t(STAGEF * 4));
+        S::TA::load(st, &tmA, it.head0, r0, &bars[s], pol);
+        S::TV::load(st + A_STAGE, &tmG, it.head0, r0, &bars[s], pol);
+    };
+    const int npro = int(min64(S::NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mu = 0.f;  // row r of the chunk offset C
+    float mcol[K];   // column r of M = A_s^T ... A_e^T
+#pragma unroll
+    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % S::NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int64_t tt = te - 1 - j * S::TS;
+        const int n = int(min64(S::TS, tt - tb + 1));
+        const float *st = ring + size_t(s) * SSTR;
+#pragma unroll
+        for (int u = 0; u < S::TS; ++u) {
+            if (u < n) {
+                const int q = S::TS - 1 - u;
+                const TileRef<K> Ablk{st, q, sub};
+                const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
+                float a[K], p[K], nm[K];
+                Ablk.row(r, a);
+#pragma unroll
+                for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
+                mu = group_reduce_scatter<K>(p, r);
+                tile_matvec_t(Ablk, mcol, nm);
+#pragma unroll
+                for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+            }
+        }
+        __syncwarp();
+        if (j + S::NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + S::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    const int64_t item = it.g * C + it.c;
+    st_ws_col<K>(Ms + item * S::AF + sub * K * K, r, mcol);
+    __stcg(Cs + item * S::VF + sub * K + r, mu);
+}
+
+// Launch 3, backward: db, dA (and dh0 from chunk 0) from the chunk's carry.
+template <int K>
+__global__ void __launch_bounds__(32)
+    mas_bwd_out_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                       const __grid_constant__ CUtensorMap tmH, const float *__restrict__ h0, float *__restrict__ dA,
+                       float *__restrict__ db, float *__restrict__ dh0, const float *__restrict__ Es, int64_t T,
+                       int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MasChunkShape<K>;
+    constexpr int A_STAGE = S::TS * S::AF, V_STAGE = S::TS * S::VF;
+    constexpr int STAGEF = A_STAGE + 2 * V_STAGE;
+    using R = ChunkRing<STAGEF, S::NS, S::TA::kAlign>;
+    constexpr int SSTR = int(R::stage_stride / sizeof(float));
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *sbase = align_smem(smem_raw, S::TA::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + R::bar_offset);
+
+    const int lane = threadIdx.x;
+    const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
+    const int sub = lane / K, r = lane % K;
+    const bool active = it.head0 + sub < H;
+    const int64_t bi = it.bi;
+    const int head0 = it.head0;
+    const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t nb = (len + S::TS - 1) / S::TS;
 
     WarpRing<S::NS> rg;
     rg.init(bars, lane);
@@ -853,41 +934,33 @@ __global__ void __launch_bounds__(32)
         prefetch_tmap(&tmG);
         prefetch_tmap(&tmH);
     }
-    // block jb of a pass covers t = te-1-jb*TS down to max(tb, te-(jb+1)*TS);
-    // boxes start at row te-(jb+1)*TS; the h box one row earlier holds h_{t-1}
-    auto issue = [&](int s, int64_t jj) {  // lane 0 only
-        const bool p1 = two_pass && jj < n1;
-        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
-        const int r0 = int(bi * T + te - (jb + 1) * S::TS);
+    // as in launch 1; the h box starts one row earlier and holds h_{t-1}
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        const int r0 = int(bi * T + te - (j + 1) * S::TS);
         float *st = ring + size_t(s) * SSTR;
-        mbar_arrive_expect_tx(&bars[s], uint32_t((A_STAGE + (p1 ? 1 : 2) * V_STAGE) * 4));
+        mbar_arrive_expect_tx(&bars[s], uint32_t(R::stage_bytes));
         S::TA::load(st, &tmA, head0, r0, &bars[s], pol);
         S::TV::load(st + A_STAGE, &tmG, head0, r0, &bars[s], pol);
-        if (!p1) S::TV::load(st + A_STAGE + V_STAGE, &tmH, head0, r0 - 1, &bars[s], pol);
+        S::TV::load(st + A_STAGE + V_STAGE, &tmH, head0, r0 - 1, &bars[s], pol);
     };
     const int npro = int(min64(S::NS, nb));
     if (lane == 0)
         for (int s = 0; s < npro; ++s) issue(s, s);
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
-    float mu = 0.f;  // pass 1: row r of the chunk offset C; pass 2: (A_{t+1}^T lambda_{t+1})[r]
-    float mcol[K];   // pass 1: column r of M = A_s^T ... A_e^T
-#pragma unroll
-    for (int i = 0; i < K; ++i) mcol[i] = (i == r) ? 1.f : 0.f;
+    pdl_wait();  // the carries of launch 2
+    float mu = __ldcg(Es + (it.g * C + it.c) * S::VF + sub * K + r);  // (A_{t+1}^T lambda_{t+1})[r] past the chunk
     const int64_t hk = H * K;
     float *dbp = db + (bi * T * H + head0 + sub) * K + r;
     float *dAp = dA + (bi * T * H + head0 + sub) * K * K + r * K;
-
-    for (int64_t jj = 0; jj < nb; ++jj) {
-        const int s = int(jj % S::NS);
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % S::NS);
         if (!rg.wait(s, ctl)) {
             if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
             rg.drain(ctl, lane);
             return;
         }
-        const bool p1 = two_pass && jj < n1;
-        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
-        const int64_t tt = te - 1 - jb * S::TS;
+        const int64_t tt = te - 1 - j * S::TS;
         const int n = int(min64(S::TS, tt - tb + 1));
         const float *st = ring + size_t(s) * SSTR;
 #pragma unroll
@@ -897,84 +970,61 @@ __global__ void __launch_bounds__(32)
                 const int q = S::TS - 1 - u;
                 const TileRef<K> Ablk{st, q, sub};
                 const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
-                float a[K];
+                float a[K], p[K], hp[K], dar[K];
                 Ablk.row(r, a);
-                float p[K];
 #pragma unroll
                 for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
                 mu = group_reduce_scatter<K>(p, r);
-                if (p1) {
-                    float nm[K];
-                    tile_matvec_t(Ablk, mcol, nm);
+                if (t >= 1) {
+                    lds_row<K>(st + A_STAGE + V_STAGE + q * S::VF + sub * K, hp);
+                } else if (h0 != nullptr && active) {
 #pragma unroll
-                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+                    for (int x = 0; x < K; ++x) hp[x] = h0[(bi * H + head0 + sub) * K + x];
                 } else {
-                    float hp[K];
-                    if (t >= 1) {
-                        lds_row<K>(st + A_STAGE + V_STAGE + q * S::VF + sub * K, hp);
-                    } else if (h0 != nullptr && active) {
 #pragma unroll
-                        for (int x = 0; x < K; ++x) hp[x] = h0[(bi * H + head0 + sub) * K + x];
-                    } else {
+                    for (int x = 0; x < K; ++x) hp[x] = 0.f;
+                }
 #pragma unroll
-                        for (int x = 0; x < K; ++x) hp[x] = 0.f;
-                    }
-                    float dar[K];
-#pragma unroll
-                    for (int x = 0; x < K; ++x) dar[x] = lam * hp[x];
-                    if (active) {
-                        st_cs(dbp + t * hk, lam);
-                        stg_row_cs<K>(dAp + t * hk * K, dar);
-                    }
+                for (int x = 0; x < K; ++x) dar[x] = lam * hp[x];
+                if (active) {
+                    st_cs(dbp + t * hk, lam);
+                    stg_row_cs<K>(dAp + t * hk * K, dar);
                 }
             }
         }
         __syncwarp();
-        if (jj + S::NS < nb) {
+        if (j + S::NS < nb) {
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(s, jj + S::NS);
+                issue(s, j + S::NS);
             }
             rg.armed(s);
         }
-        if (two_pass && jj == n1 - 1) {
-            st_ws_col<K>(w.slot(0, iself) + sub * K * K, r, mcol);
-            __stcg(w.slot(1, iself) + sub * K + r, mu);
-            publish(&w.flags[iself], FLAG_AGG, lane);
-            float muin = 0.f;
-            if (!lookback_affine<K>(w, g, C, c, +1, sub, r, gbase, lane, ctl, muin)) {
-                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
-                rg.drain(ctl, lane);
-                return;
-            }
-            const float muout = affine_apply<K>(xw, r, gbase, mcol, muin, mu);
-            __stcg(w.slot(2, iself) + sub * K + r, muout);
-            publish(&w.flags[iself], FLAG_INCL, lane);
-            mu = muin;
-        }
     }
-    if (!two_pass) {  // last chunk: its final mu is the inclusive value
-        __stcg(w.slot(2, iself) + sub * K + r, mu);
-        publish(&w.flags[iself], FLAG_INCL, lane);
-    }
-    if (c == 0 && dh0 != nullptr && active) dh0[(bi * H + head0 + sub) * K + r] = mu;
+    if (it.c == 0 && dh0 != nullptr && active) dh0[(bi * H + head0 + sub) * K + r] = mu;
 }
 
 template <int K>
 cudaError_t mas_fwd_chunk_t(const float *A, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                             int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MasChunkShape<K>;
-    using R = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::AF, S::TA::kAlign>;
+    using R = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::TA::kAlign>;
+    const int64_t gpb = (H + S::LPW - 1) / S::LPW;
+    const ScanWs w(ws, pl, S::AF, S::VF);
+    if (pl.G * pl.C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     CUtensorMap tA, tB;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
     if ((e = S::TV::make(&tB, b, B * T, H, S::TS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
     const int smem = int(R::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)mas_fwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
-    mas_fwd_chunk_kernel<K><<<dim3(unsigned(pl.G * pl.C)), 32, smem, s>>>(tA, tB, h0, h, ws, B, T, H,
-                                                                          (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
-    return cudaGetLastError();
+    if ((e = ensure_smem_attr((const void *)mas_fwd_agg_kernel<K>, smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem_attr((const void *)mas_fwd_out_kernel<K>, smem)) != cudaSuccess) return e;
+    mas_fwd_agg_kernel<K><<<dim3(unsigned(pl.G * (pl.C - 1))), 32, smem, s>>>(tA, tB, w.M, w.Cv, T, gpb, pl.C, pl.L,
+                                                                              ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_chain<K, false, true, +1>(w.M, w.Cv, w.E, h0, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess) return e;
+    return launch_pdl(mas_fwd_out_kernel<K>, dim3(unsigned(pl.G * pl.C)), smem, s, tA, tB, h, w.E, T, H, gpb, pl.C,
+                      pl.L, ctl);
 }
 
 template <int K>
@@ -982,18 +1032,26 @@ cudaError_t mas_bwd_chunk_t(const float *A, const float *h0, const float *h, con
                             float *db, float *dh0, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
                             unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MasChunkShape<K>;
-    using R = ChunkRing<S::TS * (S::AF + 2 * S::VF), S::NS, S::AF, S::TA::kAlign>;
+    using RA = ChunkRing<S::TS * (S::AF + S::VF), S::NS, S::TA::kAlign>;
+    using RO = ChunkRing<S::TS * (S::AF + 2 * S::VF), S::NS, S::TA::kAlign>;
+    const int64_t gpb = (H + S::LPW - 1) / S::LPW;
+    const ScanWs w(ws, pl, S::AF, S::VF);
+    if (pl.G * pl.C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     CUtensorMap tA, tG, tH;
     cudaError_t e;
     if ((e = S::TA::make(&tA, A, B * T, H, S::TS)) != cudaSuccess) return e;
     if ((e = S::TV::make(&tG, gh, B * T, H, S::TS)) != cudaSuccess) return e;
     if ((e = S::TV::make(&tH, h, B * T, H, S::TS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
-    const int smem = int(R::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)mas_bwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
-    mas_bwd_chunk_kernel<K><<<dim3(unsigned(pl.G * pl.C)), 32, smem, s>>>(
-        tA, tG, tH, h0, dA, db, dh0, ws, B, T, H, (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
-    return cudaGetLastError();
+    const int sa = int(RA::warp_bytes), so = int(RO::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)mas_bwd_agg_kernel<K>, sa)) != cudaSuccess) return e;
+    if ((e = ensure_smem_attr((const void *)mas_bwd_out_kernel<K>, so)) != cudaSuccess) return e;
+    mas_bwd_agg_kernel<K><<<dim3(unsigned(pl.G * (pl.C - 1))), 32, sa, s>>>(tA, tG, w.M, w.Cv, T, gpb, pl.C, pl.L,
+                                                                            ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_chain<K, false, true, -1>(w.M, w.Cv, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess)
+        return e;
+    return launch_pdl(mas_bwd_out_kernel<K>, dim3(unsigned(pl.G * pl.C)), so, s, tA, tG, tH, h0, dA, db, dh0, w.E, T,
+                      H, gpb, pl.C, pl.L, ctl);
 }
 
 }  // namespace
@@ -1001,7 +1059,7 @@ cudaError_t mas_bwd_chunk_t(const float *A, const float *h0, const float *h, con
 size_t mas_workspace_bytes(int64_t B, int64_t T, int64_t H, int K) {
     const ChunkPlan p = plan_chunks(B, T, H, K);
     if (p.C <= 1) return 0;
-    return ChunkWs::bytes(p, K, 3);
+    return ScanWs::bytes(p, 32 * K, 32, 32);  // per lane group: M (32/k blocks of k x k), c and E (32 floats)
 }
 
 #define MAS_DISPATCH(K_, CALL)                 \

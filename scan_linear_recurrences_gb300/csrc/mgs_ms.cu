@@ -267,19 +267,15 @@ cudaError_t ms_bwd_t(const float *A, const float *P, const float *G, float *dA, 
 
 // ================================================================ time-chunked path
 // With few lanes (B*H/(32/k) warps well below the SM count) the sequential
-// per-lane loop leaves the GPU idle.  The chunked kernels split T into C
-// chunks of L steps; one warp handles one (lane group, chunk) item:
-//   pass 1  the chunk's aggregate from the identity (forward: the product
-//           A_end...A_start; backward: the affine map mu_out = M mu_in + C),
-//   publish the aggregate, then decoupled look-back (Merrill & Garland 2016)
-//           over the predecessors' flags to get the carry, publish the
-//           inclusive value,
-//   pass 2  the exact recurrence from the carry, writing outputs.
-// Items are taken from an atomic ticket in carry order (all chunk-0 items,
-// then chunk 1, ...), so every item waited on belongs to a warp that is
-// already running: the look-back always makes progress.  Waits are bounded
-// and report ERR_FLAG_TIMEOUT instead of hanging.  Pass 2 re-reads the
-// chunk's inputs a few microseconds after pass 1, from L2.
+// per-lane loop leaves the GPU idle.  T is then split into C chunks of L
+// steps and the scan runs as a reduce-then-scan in three launches (see
+// mgs_chunk.cuh): one warp per (lane group, chunk) item computes the chunk's
+// aggregate, one block per lane group chains the aggregates into every
+// chunk's incoming carry, and one warp per item reruns its chunk from the
+// carry, writing outputs.  The inputs of the rerun are still in L2.
+//   forward:  aggregate M = A_e ... A_s, carry E_{c+1} = M_c E_c (E_0 = I);
+//   backward: aggregate (M, C) with mu_out = M mu_in + C, M = A_s^T ... A_e^T,
+//             carry mu_in(c-1) = M_c mu_in(c) + C_c (mu_in(C-1) = 0).
 
 template <int K>
 struct MsChunkShape {
@@ -291,138 +287,63 @@ struct MsChunkShape {
     using TM = MatTile<K>;
 };
 
-// Applies, starting from the inclusive value X0 (k x k, row-major, this lane's
-// slot in the workspace), the aggregates of chunks p = p_first, p_first+step,
-// ... up to (not including) p_end: X <- M_p X (+ C_p when Cs is given), where
-// M_p = Ms[(item0 + p) * mf] and C_p likewise.  Thread i of the k-group keeps
-// row i of X; the rows go through the exchange buffer each step, and row i of
-// the next 8 aggregates is in flight while one is applied (each is an
-// L2 round trip, long against a step's k^2 FMAs).  Returns column `col` of the
-// result in out.
-// (4 for k = 16, where 8 would not fit in registers)
-template <int K>
-constexpr int fold_ahead() { return K >= 16 ? 4 : 8; }
-
-template <int K>
-__device__ void fold_rows(const float *X0, const float *Ms, int64_t mf, int64_t item0, int64_t p_first,
-                          int64_t p_end, int step, const float *Cs, float *xw, int col, float (&out)[K]) {
-    const int i = col;  // this thread's row
-    float xr[K];
-    lds_row_global<K>(X0 + i * K, xr);
-    const int64_t cnt = (p_end - p_first) / step;
-    constexpr int kFoldAhead = fold_ahead<K>();
-    float mq[kFoldAhead][K], cq[kFoldAhead][K];
-    auto load = [&](int64_t k, float (&mr)[K], float (&cr)[K]) {
-        const int64_t p = p_first + k * step;
-        lds_row_global<K>(Ms + (item0 + p) * mf + i * K, mr);
-        if (Cs) lds_row_global<K>(Cs + (item0 + p) * mf + i * K, cr);
-    };
-#pragma unroll
-    for (int d = 0; d < kFoldAhead; ++d)
-        if (d < cnt) load(d, mq[d], cq[d]);
-    for (int64_t k0 = 0; k0 < cnt; k0 += kFoldAhead) {
-#pragma unroll
-        for (int d = 0; d < kFoldAhead; ++d) {
-            const int64_t k = k0 + d;
-            if (k < cnt) {  // warp-uniform
-#pragma unroll
-                for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
-                __syncwarp();
-                float nr[K];
-#pragma unroll
-                for (int j = 0; j < K; ++j) nr[j] = Cs ? cq[d][j] : 0.f;
-#pragma unroll
-                for (int m = 0; m < K; ++m) {
-                    float xm[K];
-                    lds_row_smem<K>(xw + m * K, xm);
-#pragma unroll
-                    for (int j = 0; j < K; ++j) nr[j] = fmaf(mq[d][m], xm[j], nr[j]);
-                }
-                __syncwarp();
-#pragma unroll
-                for (int j = 0; j < K; ++j) xr[j] = nr[j];
-                if (k + kFoldAhead < cnt) load(k + kFoldAhead, mq[d], cq[d]);
-            }
-        }
+// Item -> (lane group, chunk) and the lane group's place in the batch.
+struct ChunkItem {
+    int64_t g, c, bi;
+    int head0;
+    __device__ ChunkItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int lpw) {
+        const unsigned q = unsigned(item) / unsigned(nper);  // 32-bit: items, nper and gpb are below 2^32
+        g = q;
+        c = cfirst + (item - int64_t(q) * nper);
+        const unsigned b32 = q / unsigned(gpb);
+        bi = b32;
+        head0 = int(q - b32 * unsigned(gpb)) * lpw;
     }
-    // rows -> column `col`
-#pragma unroll
-    for (int j = 0; j < K; ++j) xw[i * K + j] = xr[j];
-    __syncwarp();
-#pragma unroll
-    for (int m = 0; m < K; ++m) out[m] = xw[m * K + col];
-    __syncwarp();
-}
+};
 
+// Launch 1, forward: the product of the chunk's A_t (chunks 0 .. C-2).
 template <int K>
 __global__ void __launch_bounds__(32)
-    ms_fwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P,
-                        unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb,
-                        int64_t C, int64_t Lc, DevCtl ctl) {
+    ms_fwd_agg_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ Ms, int64_t T, int64_t gpb,
+                      int64_t C, int64_t Lc, DevCtl ctl) {
     using S = MsChunkShape<K>;
     constexpr int TS = S::FTS, NS = S::NS, BOXF = TS * S::MF;
-    using Lay = MsLayout<S::MF, TS, NS, S::MF, S::TM::kAlign>;
+    using Lay = MsLayout<S::MF, TS, NS, 0, S::TM::kAlign>;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *sbase = align_smem(smem_raw, S::TM::kAlign);
     float *ring = reinterpret_cast<float *>(sbase);
-    float *xch = reinterpret_cast<float *>(sbase + Lay::ring_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
 
     const int lane = threadIdx.x;
-    const int64_t G = B * gpb, items = G * C;
-    ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::MF);
-    float *agg = w.slot(0, 0);
-    float *incl = agg + items * S::MF;
-    unsigned item = 0;
-    if (lane == 0) item = atomicAdd(w.ticket, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    if (int64_t(item) >= items) return;
-
-    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
-    const int64_t c = q32, g = item - q32 * unsigned(G);
-    const unsigned b32 = unsigned(g) / unsigned(gpb);
-    const int64_t bi = b32;
-    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
-    const int nl = int(min64(S::LPW, H - head0));
+    const ChunkItem it(blockIdx.x, C - 1, 0, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
-    const bool active = sub < nl;
-    const int64_t tb = c * Lc, len = min64(Lc, T - tb);
-    const int64_t n1 = (len + TS - 1) / TS;
-    const bool two_pass = c > 0;
-    const int64_t nb = two_pass ? 2 * n1 : n1;
-    float *xw = xch + sub * K * K;
-    const int64_t slot = (g * C + c) * S::MF + sub * K * K;
+    const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
+    const int64_t nb = (len + TS - 1) / TS;
 
     WarpRing<NS> rg;
     rg.init(bars, lane);
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = policy_evict_last();  // launch 3 reads the chunk again
     if (lane == 0) prefetch_tmap(&tmA);
-    auto block_t0 = [&](int64_t jj) { return tb + ((two_pass && jj >= n1) ? jj - n1 : jj) * TS; };
-    auto issue = [&](int s, int64_t jj) {  // lane 0 only
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
         mbar_arrive_expect_tx(&bars[s], uint32_t(BOXF * 4));
-        S::TM::load(ring + size_t(s) * BOXF, &tmA, head0, int(bi * T + block_t0(jj)), &bars[s], pol);
+        S::TM::load(ring + size_t(s) * BOXF, &tmA, it.head0, int(it.bi * T + tb + j * TS), &bars[s], pol);
     };
     const int npro = int(min64(NS, nb));
     if (lane == 0)
         for (int s = 0; s < npro; ++s) issue(s, s);
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
-    float m[K];  // pass 1: column of the chunk product; pass 2: column of P_t
+    float m[K];  // column `col` of the chunk product
 #pragma unroll
     for (int i = 0; i < K; ++i) m[i] = (i == col) ? 1.f : 0.f;
-    float *pout = P + (bi * T * H + head0 + sub) * K * K + col;
-    bool failed = false;
-
-    for (int64_t jj = 0; jj < nb; ++jj) {
-        const int s = int(jj % NS);
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % NS);
         if (!rg.wait(s, ctl)) {
             if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
             rg.drain(ctl, lane);
             return;
         }
-        const int64_t t0 = block_t0(jj);
-        const int n = int(min64(TS, tb + len - t0));
-        const bool store = !(two_pass && jj < n1);
+        const int n = int(min64(TS, len - j * TS));
         const float *st = ring + size_t(s) * BOXF;
 #pragma unroll
         for (int u = 0; u < TS; ++u) {
@@ -431,7 +352,75 @@ __global__ void __launch_bounds__(32)
                 tile_matvec(TileRef<K>{st, u, sub}, m, nm);
 #pragma unroll
                 for (int i = 0; i < K; ++i) m[i] = nm[i];
-                if (store && active) {
+            }
+        }
+        __syncwarp();
+        if (j + NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + NS);
+            }
+            rg.armed(s);
+        }
+    }
+    st_ws_col<K>(Ms + (it.g * C + it.c) * S::MF + sub * K * K, col, m);
+}
+
+// Launch 3, forward: P_t from the chunk's carry (all chunks).
+template <int K>
+__global__ void __launch_bounds__(32)
+    ms_fwd_out_kernel(const __grid_constant__ CUtensorMap tmA, float *__restrict__ P, const float *__restrict__ Es,
+                      int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using S = MsChunkShape<K>;
+    constexpr int TS = S::FTS, NS = S::NS, BOXF = TS * S::MF;
+    using Lay = MsLayout<S::MF, TS, NS, 0, S::TM::kAlign>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *sbase = align_smem(smem_raw, S::TM::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
+
+    const int lane = threadIdx.x;
+    const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
+    const int sub = lane / K, col = lane % K;
+    const bool active = it.head0 + sub < H;
+    const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
+    const int64_t nb = (len + TS - 1) / TS;
+
+    WarpRing<NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    if (lane == 0) prefetch_tmap(&tmA);
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        mbar_arrive_expect_tx(&bars[s], uint32_t(BOXF * 4));
+        S::TM::load(ring + size_t(s) * BOXF, &tmA, it.head0, int(it.bi * T + tb + j * TS), &bars[s], pol);
+    };
+    const int npro = int(min64(NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float m[K];  // column `col` of P_t, from the carry (P at the end of chunk c-1)
+    pdl_wait();   // the carries of launch 2
+    ld_ws_col<K>(Es + (it.g * C + it.c) * S::MF + sub * K * K, col, m);
+    float *pout = P + (it.bi * T * H + it.head0 + sub) * K * K + col;
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int64_t t0 = tb + j * TS;
+        const int n = int(min64(TS, len - j * TS));
+        const float *st = ring + size_t(s) * BOXF;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                float nm[K];
+                tile_matvec(TileRef<K>{st, u, sub}, m, nm);
+#pragma unroll
+                for (int i = 0; i < K; ++i) m[i] = nm[i];
+                if (active) {
                     float *dst = pout + (t0 + u) * H * K * K;
 #pragma unroll
                     for (int i = 0; i < K; ++i) st_cs(dst + i * K, m[i]);
@@ -439,53 +428,107 @@ __global__ void __launch_bounds__(32)
             }
         }
         __syncwarp();
-        if (jj + NS < nb) {
+        if (j + NS < nb) {
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(s, jj + NS);
+                issue(s, j + NS);
             }
             rg.armed(s);
         }
-        if (two_pass && jj == n1 - 1) {
-            // publish the aggregate, look back for the exclusive prefix E
-            st_ws_col<K>(agg + slot, col, m);
-            publish(&w.flags[g * C + c], FLAG_AGG, lane);
-            // E = P at the end of chunk c-1: the nearest published inclusive
-            // prefix, then the aggregates after it, oldest first: E <- Agg_p E
-            float e[K];
-            const int64_t ps = find_inclusive(w.flags + g * C, c, -1, C, lane, ctl);
-            if (ps < 0) {
-                failed = true;
-            } else {
-                const float *inc0 = incl + (g * C + ps) * S::MF + sub * K * K;
-                fold_rows<K>(inc0, agg + sub * K * K, S::MF, g * C, ps + 1, c, +1, nullptr, xw, col, e);
-            }
-            if (failed) {
-                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
-                rg.drain(ctl, lane);
-                return;
-            }
-            // inclusive = aggregate * E; pass 2 starts from E
-            float inc[K];
-            group_matvec<K>(xw, col, m, e, inc);
-            st_ws_col<K>(incl + slot, col, inc);
-            publish(&w.flags[g * C + c], FLAG_INCL, lane);
-#pragma unroll
-            for (int i = 0; i < K; ++i) m[i] = e[i];
-        }
-    }
-    if (!two_pass) {  // chunk 0: its last P is the inclusive prefix
-        st_ws_col<K>(incl + slot, col, m);
-        publish(&w.flags[g * C + c], FLAG_INCL, lane);
     }
 }
 
+// Launch 1, backward: (M, C) of chunks 1 .. C-1, t walking down the chunk.
 template <int K>
 __global__ void __launch_bounds__(32)
-    ms_bwd_chunk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
-                        const __grid_constant__ CUtensorMap tmP, float *__restrict__ dA,
-                        unsigned char *__restrict__ ws, int64_t B, int64_t T, int64_t H, int64_t gpb,
-                        int64_t C, int64_t Lc, DevCtl ctl) {
+    ms_bwd_agg_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                      float *__restrict__ Ms, float *__restrict__ Cs, int64_t T, int64_t gpb, int64_t C, int64_t Lc,
+                      DevCtl ctl) {
+    using S = MsChunkShape<K>;
+    constexpr int TS = S::BTS, NS = S::NS, BOXF = TS * S::MF;
+    using Lay = MsLayout<2 * S::MF, TS, NS, 0, S::TM::kAlign>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    unsigned char *sbase = align_smem(smem_raw, S::TM::kAlign);
+    float *ring = reinterpret_cast<float *>(sbase);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
+
+    const int lane = threadIdx.x;
+    const ChunkItem it(blockIdx.x, C - 1, 1, gpb, S::LPW);
+    const int sub = lane / K, col = lane % K;
+    const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t nb = (len + TS - 1) / TS;
+
+    WarpRing<NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    if (lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmG);
+    }
+    // block j covers t = te-1-j*TS down to max(tb, te-(j+1)*TS); boxes start
+    // at row te-(j+1)*TS, step u at box row TS-1-u
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        const int r0 = int(it.bi * T + te - (j + 1) * TS);
+        float *st = ring + size_t(s) * 2 * BOXF;
+        mbar_arrive_expect_tx(&bars[s], uint32_t(2 * BOXF * 4));
+        S::TM::load(st, &tmA, it.head0, r0, &bars[s], pol);
+        S::TM::load(st + BOXF, &tmG, it.head0, r0, &bars[s], pol);
+    };
+    const int npro = int(min64(NS, nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mu[K], mm[K];  // columns of the chunk map's offset C and matrix M
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        mu[i] = 0.f;
+        mm[i] = (i == col) ? 1.f : 0.f;
+    }
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % NS);
+        if (!rg.wait(s, ctl)) {
+            if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
+            rg.drain(ctl, lane);
+            return;
+        }
+        const int64_t tt = te - 1 - j * TS;
+        const int n = int(min64(TS, tt - tb + 1));
+        const float *st = ring + size_t(s) * 2 * BOXF;
+#pragma unroll
+        for (int u = 0; u < TS; ++u) {
+            if (u < n) {
+                const int q = TS - 1 - u;
+                const TileRef<K> At{st, q, sub}, Gt{st + BOXF, q, sub};
+                float lc[K], nm[K];
+#pragma unroll
+                for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
+                tile_matvec_t(At, lc, mu);
+                tile_matvec_t(At, mm, nm);
+#pragma unroll
+                for (int i = 0; i < K; ++i) mm[i] = nm[i];
+            }
+        }
+        __syncwarp();
+        if (j + NS < nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + NS);
+            }
+            rg.armed(s);
+        }
+    }
+    const int64_t slot = (it.g * C + it.c) * S::MF + sub * K * K;
+    st_ws_col<K>(Ms + slot, col, mm);
+    st_ws_col<K>(Cs + slot, col, mu);
+}
+
+// Launch 3, backward: dA_t from the chunk's carry mu_in (all chunks).
+template <int K>
+__global__ void __launch_bounds__(32)
+    ms_bwd_out_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmG,
+                      const __grid_constant__ CUtensorMap tmP, float *__restrict__ dA, const float *__restrict__ Es,
+                      int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
     using S = MsChunkShape<K>;
     constexpr int TS = S::BTS, NS = S::NS, BOXF = TS * S::MF;
     using Lay = MsLayout<3 * S::MF, TS, NS, S::MF, S::TM::kAlign>;
@@ -496,31 +539,12 @@ __global__ void __launch_bounds__(32)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Lay::ring_bytes + Lay::extra_bytes);
 
     const int lane = threadIdx.x;
-    const int64_t G = B * gpb, items = G * C;
-    ChunkWs w(ws, ChunkPlan{G, C, Lc}, S::MF);
-    float *aggM = w.slot(0, 0);
-    float *aggC = aggM + items * S::MF;
-    float *incl = aggC + items * S::MF;
-    unsigned item = 0;
-    if (lane == 0) item = atomicAdd(w.ticket, 1u);
-    item = __shfl_sync(0xffffffffu, item, 0);
-    if (int64_t(item) >= items) return;
-
-    // carries flow from the end of the sequence: tickets go to the last chunk first
-    const unsigned q32 = item / unsigned(G);  // 32-bit: tickets, G and gpb are below 2^32
-    const int64_t c = C - 1 - int64_t(q32), g = item - q32 * unsigned(G);
-    const unsigned b32 = unsigned(g) / unsigned(gpb);
-    const int64_t bi = b32;
-    const int head0 = int(unsigned(g) - b32 * unsigned(gpb)) * S::LPW;
-    const int nl = int(min64(S::LPW, H - head0));
+    const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
-    const bool active = sub < nl;
-    const int64_t tb = c * Lc, te = min64(T, tb + Lc), len = te - tb;
-    const int64_t n1 = (len + TS - 1) / TS;
-    const bool two_pass = c < C - 1;
-    const int64_t nb = two_pass ? 2 * n1 : n1;
+    const bool active = it.head0 + sub < H;
+    const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
+    const int64_t nb = (len + TS - 1) / TS;
     float *xw = xch + sub * K * K;
-    const int64_t slot = (g * C + c) * S::MF + sub * K * K;
 
     WarpRing<NS> rg;
     rg.init(bars, lane);
@@ -530,41 +554,30 @@ __global__ void __launch_bounds__(32)
         prefetch_tmap(&tmG);
         prefetch_tmap(&tmP);
     }
-    // block jb of a pass covers t = te-1-jb*TS down to max(tb, te-(jb+1)*TS);
-    // box rows start at te-(jb+1)*TS, step u at box row TS-1-u.
-    auto issue = [&](int s, int64_t jj) {  // lane 0 only
-        const bool p1 = two_pass && jj < n1;
-        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
-        const int r0 = int(bi * T + te - (jb + 1) * TS);
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        const int r0 = int(it.bi * T + te - (j + 1) * TS);
         float *st = ring + size_t(s) * 3 * BOXF;
-        mbar_arrive_expect_tx(&bars[s], uint32_t((p1 ? 2 : 3) * BOXF * 4));
-        S::TM::load(st, &tmA, head0, r0, &bars[s], pol);
-        S::TM::load(st + BOXF, &tmG, head0, r0, &bars[s], pol);
-        if (!p1) S::TM::load(st + 2 * BOXF, &tmP, head0, r0 - 1, &bars[s], pol);
+        mbar_arrive_expect_tx(&bars[s], uint32_t(3 * BOXF * 4));
+        S::TM::load(st, &tmA, it.head0, r0, &bars[s], pol);
+        S::TM::load(st + BOXF, &tmG, it.head0, r0, &bars[s], pol);
+        S::TM::load(st + 2 * BOXF, &tmP, it.head0, r0 - 1, &bars[s], pol);
     };
     const int npro = int(min64(NS, nb));
     if (lane == 0)
         for (int s = 0; s < npro; ++s) issue(s, s);
     for (int s = 0; s < npro; ++s) rg.armed(s);
 
-    float mu[K], mm[K];  // pass 1: (C, M) columns of the chunk map; pass 2: mu column
-#pragma unroll
-    for (int i = 0; i < K; ++i) {
-        mu[i] = 0.f;
-        mm[i] = (i == col) ? 1.f : 0.f;
-    }
-    bool failed = false;
-
-    for (int64_t jj = 0; jj < nb; ++jj) {
-        const int s = int(jj % NS);
+    float mu[K];  // column `col` of A_{t+1}^T Lambda_{t+1}, from the carry
+    pdl_wait();    // the carries of launch 2
+    ld_ws_col<K>(Es + (it.g * C + it.c) * S::MF + sub * K * K, col, mu);
+    for (int64_t j = 0; j < nb; ++j) {
+        const int s = int(j % NS);
         if (!rg.wait(s, ctl)) {
             if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
             rg.drain(ctl, lane);
             return;
         }
-        const bool p1 = two_pass && jj < n1;
-        const int64_t jb = (two_pass && jj >= n1) ? jj - n1 : jj;
-        const int64_t tt = te - 1 - jb * TS;
+        const int64_t tt = te - 1 - j * TS;
         const int n = int(min64(TS, tt - tb + 1));
         const float *st = ring + size_t(s) * 3 * BOXF;
 #pragma unroll
@@ -576,85 +589,41 @@ __global__ void __launch_bounds__(32)
                 float lc[K];
 #pragma unroll
                 for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
-                if (p1) {
-                    float nm[K];
-                    tile_matvec_t(At, lc, mu);
-                    tile_matvec_t(At, mm, nm);
 #pragma unroll
-                    for (int i = 0; i < K; ++i) mm[i] = nm[i];
+                for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
+                __syncwarp();
+                float lrow[K], darow[K];
+#pragma unroll
+                for (int x = 0; x < K; ++x) lrow[x] = xw[col * K + x];
+                if (t >= 1) {
+                    tile_matvec(Pp, lrow, darow);  // dA[row][m] = sum_j L[row][j] P_{t-1}[m][j]
                 } else {
 #pragma unroll
-                    for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
-                    __syncwarp();
-                    float lrow[K], darow[K];
+                    for (int x = 0; x < K; ++x) darow[x] = lrow[x];  // P_0 = I
+                }
+                tile_matvec_t(At, lc, mu);
+                __syncwarp();
+                if (active) {
+                    float *dst = dA + ((it.bi * T + t) * H + it.head0 + sub) * K * K + col * K;
+                    if constexpr (K >= 4) {
 #pragma unroll
-                    for (int jx = 0; jx < K; ++jx) lrow[jx] = xw[col * K + jx];
-                    if (t >= 1) {
-                        tile_matvec(Pp, lrow, darow);
+                        for (int x = 0; x < K / 4; ++x)
+                            st_cs4(dst + 4 * x, make_float4(darow[4 * x], darow[4 * x + 1], darow[4 * x + 2], darow[4 * x + 3]));
                     } else {
 #pragma unroll
-                        for (int x = 0; x < K; ++x) darow[x] = lrow[x];
-                    }
-                    tile_matvec_t(At, lc, mu);
-                    __syncwarp();
-                    if (active) {
-                        float *dst = dA + ((bi * T + t) * H + head0 + sub) * K * K + col * K;
-                        if constexpr (K >= 4) {
-#pragma unroll
-                            for (int x = 0; x < K / 4; ++x)
-                                st_cs4(dst + 4 * x, make_float4(darow[4 * x], darow[4 * x + 1], darow[4 * x + 2], darow[4 * x + 3]));
-                        } else {
-#pragma unroll
-                            for (int x = 0; x < K; ++x) st_cs(dst + x, darow[x]);
-                        }
+                        for (int x = 0; x < K; ++x) st_cs(dst + x, darow[x]);
                     }
                 }
             }
         }
         __syncwarp();
-        if (jj + NS < nb) {
+        if (j + NS < nb) {
             if (lane == 0) {
                 fence_proxy_async_smem();
-                issue(s, jj + NS);
+                issue(s, j + NS);
             }
             rg.armed(s);
         }
-        if (two_pass && jj == n1 - 1) {
-            // publish (M, C); look back towards the end for mu_in
-            st_ws_col<K>(aggM + slot, col, mm);
-            st_ws_col<K>(aggC + slot, col, mu);
-            publish(&w.flags[g * C + c], FLAG_AGG, lane);
-            // mu_in = mu_out of chunk c+1: the nearest published inclusive value
-            // after c, then the aggregates between, farthest first:
-            // mu <- M_p mu + C_p
-            float muin[K];
-            const int64_t ps = find_inclusive(w.flags + g * C, c, +1, C, lane, ctl);
-            if (ps < 0) {
-                failed = true;
-            } else {
-                const float *inc0 = incl + (g * C + ps) * S::MF + sub * K * K;
-                fold_rows<K>(inc0, aggM + sub * K * K, S::MF, g * C, ps - 1, c, -1, aggC + sub * K * K, xw, col,
-                             muin);
-            }
-            if (failed) {
-                if (lane == 0) record_error(ctl, ERR_FLAG_TIMEOUT);
-                rg.drain(ctl, lane);
-                return;
-            }
-            // mu_out = M mu_in + C
-            float y[K], out[K];
-            group_matvec<K>(xw, col, mm, muin, y);
-#pragma unroll
-            for (int i = 0; i < K; ++i) out[i] = y[i] + mu[i];
-            st_ws_col<K>(incl + slot, col, out);
-            publish(&w.flags[g * C + c], FLAG_INCL, lane);
-#pragma unroll
-            for (int i = 0; i < K; ++i) mu[i] = muin[i];
-        }
-    }
-    if (!two_pass) {  // last chunk: its final mu is mu_out
-        st_ws_col<K>(incl + slot, col, mu);
-        publish(&w.flags[g * C + c], FLAG_INCL, lane);
     }
 }
 
@@ -662,36 +631,48 @@ template <int K>
 cudaError_t ms_fwd_chunk_t(const float *A, float *P, int64_t B, int64_t T, int64_t H, const ChunkPlan &pl,
                            unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
-    using Lay = MsLayout<S::MF, S::FTS, S::NS, S::MF, S::TM::kAlign>;
+    using Lay = MsLayout<S::MF, S::FTS, S::NS, 0, S::TM::kAlign>;
+    const int64_t gpb = (H + S::LPW - 1) / S::LPW;
+    const ScanWs w(ws, pl, S::MF, 0);
+    if (pl.G * pl.C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     CUtensorMap tA;
     cudaError_t e;
     if ((e = S::TM::make(&tA, A, B * T, H, S::FTS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
     const int smem = int(Lay::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)ms_fwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
-    const int64_t items = pl.G * pl.C;
-    ms_fwd_chunk_kernel<K><<<dim3(unsigned(items)), 32, smem, s>>>(tA, P, ws, B, T, H, (H + S::LPW - 1) / S::LPW,
-                                                                   pl.C, pl.L, ctl);
-    return cudaGetLastError();
+    if ((e = ensure_smem_attr((const void *)ms_fwd_agg_kernel<K>, smem)) != cudaSuccess) return e;
+    if ((e = ensure_smem_attr((const void *)ms_fwd_out_kernel<K>, smem)) != cudaSuccess) return e;
+    ms_fwd_agg_kernel<K><<<dim3(unsigned(pl.G * (pl.C - 1))), 32, smem, s>>>(tA, w.M, T, gpb, pl.C, pl.L, ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_chain<K, true, false, +1>(w.M, nullptr, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess)
+        return e;
+    return launch_pdl(ms_fwd_out_kernel<K>, dim3(unsigned(pl.G * pl.C)), smem, s, tA, P, w.E, T, H, gpb, pl.C, pl.L,
+                      ctl);
 }
 
 template <int K>
 cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float *dA, int64_t B, int64_t T,
                            int64_t H, const ChunkPlan &pl, unsigned char *ws, const DevCtl &ctl, cudaStream_t s) {
     using S = MsChunkShape<K>;
-    using Lay = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF, S::TM::kAlign>;
+    using LayA = MsLayout<2 * S::MF, S::BTS, S::NS, 0, S::TM::kAlign>;
+    using LayO = MsLayout<3 * S::MF, S::BTS, S::NS, S::MF, S::TM::kAlign>;
+    const int64_t gpb = (H + S::LPW - 1) / S::LPW;
+    const ScanWs w(ws, pl, S::MF, S::MF);
+    if (pl.G * pl.C > 0x7fffffff) return cudaErrorInvalidConfiguration;
     CUtensorMap tA, tG, tP;
     cudaError_t e;
     if ((e = S::TM::make(&tA, A, B * T, H, S::BTS)) != cudaSuccess) return e;
     if ((e = S::TM::make(&tG, G, B * T, H, S::BTS)) != cudaSuccess) return e;
     if ((e = S::TM::make(&tP, P, B * T, H, S::BTS)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(ws, 0, ChunkWs::header_bytes(pl), s)) != cudaSuccess) return e;
-    const int smem = int(Lay::warp_bytes);
-    if ((e = ensure_smem_attr((const void *)ms_bwd_chunk_kernel<K>, smem)) != cudaSuccess) return e;
-    const int64_t items = pl.G * pl.C;
-    ms_bwd_chunk_kernel<K><<<dim3(unsigned(items)), 32, smem, s>>>(tA, tG, tP, dA, ws, B, T, H,
-                                                                   (H + S::LPW - 1) / S::LPW, pl.C, pl.L, ctl);
-    return cudaGetLastError();
+    const int sa = int(LayA::warp_bytes), so = int(LayO::warp_bytes);
+    if ((e = ensure_smem_attr((const void *)ms_bwd_agg_kernel<K>, sa)) != cudaSuccess) return e;
+    if ((e = ensure_smem_attr((const void *)ms_bwd_out_kernel<K>, so)) != cudaSuccess) return e;
+    ms_bwd_agg_kernel<K><<<dim3(unsigned(pl.G * (pl.C - 1))), 32, sa, s>>>(tA, tG, w.M, w.Cv, T, gpb, pl.C, pl.L,
+                                                                           ctl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_chain<K, true, true, -1>(w.M, w.Cv, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess)
+        return e;
+    return launch_pdl(ms_bwd_out_kernel<K>, dim3(unsigned(pl.G * pl.C)), so, s, tA, tG, tP, dA, w.E, T, H, gpb, pl.C,
+                      pl.L, ctl);
 }
 
 }  // namespace
@@ -699,7 +680,8 @@ cudaError_t ms_bwd_chunk_t(const float *A, const float *P, const float *G, float
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd) {
     const ChunkPlan p = plan_chunks(B, T, H, K);
     if (p.C <= 1) return 0;
-    return ChunkWs::bytes(p, K, bwd ? 3 : 2);
+    const int mf = 32 * K;  // floats of one k x k matrix per lane group
+    return ScanWs::bytes(p, mf, bwd ? mf : 0, mf);
 }
 
 #define MS_DISPATCH(K_, CALL)            \

@@ -8,7 +8,7 @@ output (every element written).
 
 The shapes reach the places where an out-of-bounds store could hide: ragged
 last TMA boxes (T not a multiple of the stage), partial head or channel
-groups of a warp, ragged last chunks of the time-chunked look-back path, the
+groups of a warp, ragged last chunks of the time-chunked path, the
 few-lane long-sequence Givens path that forms A in its workspace, and the
 delta rule's ragged last 64-step chunk."""
 import math

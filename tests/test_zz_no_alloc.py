@@ -48,7 +48,7 @@ def test_noalloc_matches_the_oracle_on_two_calls(B, T, H, k, uses_scratch):
 def test_noalloc_rejects_shapes_beyond_the_scratch():
     build()
     # k = 16, one lane group, very long sequence: more carry scratch than the array holds
-    B, T, H, k = 1, 65536, 2, 16
+    B, T, H, k = 1, 131072, 2, 16
     assert b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, B, T, H, k) > b.NOALLOC_SCRATCH_BYTES
     fake = 1 << 40  # never dereferenced: the size check comes first
     with pytest.raises(b.MGSError) as ei:
