@@ -263,7 +263,7 @@ def givens_peak_memory(torch, api, device, B=128, T=64, H=8, k=8):
         torch.cuda.synchronize()
         return (torch.cuda.max_memory_allocated(device) - base) / 1e6
 
-    return {"shape": f"B={B} T={T} H={H} k={k} (d=64)", "angle_fused_MB": round(run(True), 2),
+    return {"shape": f"B={B} T={T} H={H} k={k} (d={H * k})", "angle_fused_MB": round(run(True), 2),
             "eager_mesh_then_matrix_affine_scan_MB": round(run(False), 2)}
 
 
@@ -692,7 +692,9 @@ def run_gpu(args):
                 "bytes": f"{4 * (3 * k * k + 4 * k)} per step + checkpoints", "l2": "inputs larger than L2"}
             del ws
         b.mgs_check(sid)
+        # the pages' memory shape, and the long-sequence shape (time-chunked, still from the angles)
         extra["givens_peak_memory"] = givens_peak_memory(torch, api, device)
+        extra["givens_peak_memory_long_T"] = givens_peak_memory(torch, api, device, B=16, T=1024)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -255,15 +255,18 @@ mgs_status mgs_linear_scan_bwd(const float *a, const float *h0, const float *h, 
  * angles are consumed layer by layer, pairs ascending, and the rotation of
  * angle th on (p, p+1) maps (x_p, x_{p+1}) to
  * (cos th x_p - sin th x_{p+1}, sin th x_p + cos th x_{p+1}).
- * With enough (batch, head) lanes, or T < 256, neither direction forms A_t or
- * dA_t in memory and no workspace is needed.  With few lanes and a long
+ * Neither direction ever forms A_t or dA_t in memory.  With enough (batch,
+ * head) lanes, or T < 256, no workspace is needed.  With few lanes and a long
  * sequence (when matrix_affine_scan would split T into chunks, and T >= 256)
- * the serial chain per lane would dominate, so the call instead forms A_t in
- * the workspace (and dA_t for the backward), runs the time-chunked matrix
- * kernels and derives the angle gradients from their output: then
- * mgs_workspace_size(MGS_OP_GIVENS_*, B, T, H, 8) is nonzero (about 256 bytes
- * per step, 512 for the backward, plus the chunk carries) and a smaller or
- * misaligned workspace gives MGS_ERR_WORKSPACE.
+ * the serial chain per lane would dominate, so T is split into chunks as in
+ * the matrix scans' chunked paths, each chunk's aggregate built from the
+ * angles: mgs_workspace_size(MGS_OP_GIVENS_*, B, T, H, 8) is then nonzero -
+ * the per-chunk aggregates and carries only, the same bytes as
+ * MGS_OP_MATRIX_AFFINE_SCAN_* (affine) or MGS_OP_MATRIX_SCAN_* (matrix) for
+ * that shape - and a smaller or misaligned workspace gives
+ * MGS_ERR_WORKSPACE.  Without the gate a (the orthogonal case) the call runs
+ * the per-lane kernels in extended precision at every shape and leaves the
+ * workspace unused.
  *
  * Affine forward:  h_t = G(theta_t) diag(a_t) h_{t-1} + b_t, h_0 = h0 (zeros
  * when NULL); a NULL means A_t = G(theta_t).

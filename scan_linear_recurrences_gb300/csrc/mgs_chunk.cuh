@@ -127,6 +127,21 @@ struct ScanWs {
           E(reinterpret_cast<float *>(ws + arr(p, mM) + arr(p, mC))) {}
 };
 
+// Item -> (lane group, chunk) of the chunked path and the lane group's place
+// in the batch (nper items per lane group, chunks from cfirst).
+struct ChunkItem {
+    int64_t g, c, bi;
+    int head0;
+    __device__ ChunkItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int lpw) {
+        const unsigned q = unsigned(item) / unsigned(nper);  // 32-bit: items, nper and gpb are below 2^32
+        g = q;
+        c = cfirst + (item - int64_t(q) * nper);
+        const unsigned b32 = q / unsigned(gpb);
+        bi = b32;
+        head0 = int(q - b32 * unsigned(gpb)) * lpw;
+    }
+};
+
 // Column `col` of a k x k row-major matrix in the workspace (bypassing L1).
 template <int K>
 __device__ __forceinline__ void ld_ws_col(const float *mat, int col, float (&x)[K]) {

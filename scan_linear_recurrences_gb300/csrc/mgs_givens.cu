@@ -30,8 +30,8 @@
 // enough blocks to fill the GPU).  Matrix scan: eight threads per lane,
 // thread j owning column j of P_t, four lanes per block.  Each stage of TS
 // steps arrives by tiled TMA loads into a per-block ring.
+#include "mgs_chunk.cuh"
 #include "mgs_ffsincos.cuh"
-#include "mgs_tiles.cuh"
 
 namespace mgs {
 namespace {
@@ -864,192 +864,682 @@ __global__ void __launch_bounds__(kBlockB)
 
 // ---------------------------------------------------------------- few lanes, long sequences
 // With few (batch, head) lanes and a long sequence, each lane of the kernels
-// above walks a long serial chain on one thread.  There the library instead
-// materialises A_t = G(theta_t) diag(a_t) in the caller's workspace (one
-// thread per step, fully parallel), runs the time-chunked matrix kernels on it,
-// and turns their output back into angle gradients (again one thread per step).
+// above walks a long serial chain on one thread.  There T is split into
+// chunks and the scan runs as the reduce-then-scan of mgs_chunk.cuh, still
+// from the angles: one warp per (group of 4 lanes, chunk) item, thread j of a
+// lane's 8-thread group holding column j of the chunk's aggregate (the mesh
+// applied to the columns of the identity) and, where a vector recurrence is
+// needed, the whole vector (every thread of the lane computes it, no
+// shuffles).  Each stage's angles are converted to cosines and sines in
+// shared memory by the whole warp.  Neither A_t nor dA_t is ever formed: the
+// workspace holds only the per-chunk aggregates and carries.
 
-// The per-column kernels (forming A, the matrix scan's angle gradients) take
-// kColSteps consecutive steps per block, eight threads per step, thread j on
-// column j.  Their angles are staged through shared memory: one coalesced
-// sweep of the block's 28 x kColSteps angles in, the conversion to cosines
-// and sines spread over all threads with consecutive threads on consecutive
-// words, and each thread then reads its step's 28 pairs back (the eight
-// threads of a step read the same words; the four steps of a warp are 112
-// bytes apart, in distinct banks).
-constexpr int kColSteps = 32;
-constexpr int kColBlock = kColSteps * GK;
+constexpr int kGcLanes = 4;                    // lanes per warp (8 threads each)
+constexpr int kGcTS = 4;                       // steps per stage
+constexpr int kGcNSmax = 4;                    // stages in flight (at most)
+constexpr int kGcThF = kGcTS * kGcLanes * GN;  // floats of one stage's angle box
+constexpr int kGcVecF = kGcTS * kGcLanes * GK; // floats of one stage's vector box
+using GcTile = MatTile<GK, true>;              // k x k boxes (swizzled), matrix scan backward
+constexpr int kGcMatF = kGcTS * GcTile::MF;
 
-__device__ __forceinline__ void stage_step_angles(const float *__restrict__ theta, int64_t s0, int nsteps,
-                                                  float *cs_sm, float *sn_sm) {
-    const int n = nsteps * GN;  // a multiple of 4; theta + s0 * GN is 16-byte aligned
-    const float4 *src = reinterpret_cast<const float4 *>(theta + s0 * GN);
-    for (int i = threadIdx.x; i < n / 4; i += blockDim.x) reinterpret_cast<float4 *>(cs_sm)[i] = __ldcs(src + i);
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += 4 * blockDim.x) {
-        float c[4], sv[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (i + q * blockDim.x < n) unbiased_cos_sin(cs_sm[i + q * blockDim.x], c[q], sv[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (i + q * blockDim.x < n) {
-                cs_sm[i + q * blockDim.x] = c[q];
-                sn_sm[i + q * blockDim.x] = sv[q];
-            }
+// Stage layout: [angles -> cosines][sines][nv vector boxes][nm k x k boxes].
+// Small stages, and fewer of them for the k x k boxes, keep a one-warp
+// block's shared memory low enough for many blocks per SM (these kernels are
+// latency bound; with 96 KB blocks only two fit on an SM).
+template <int NV, int NM>
+struct GcStage {
+    static constexpr int NS = NM > 0 ? 2 : kGcNSmax;
+    static constexpr int vec_off = 2 * kGcThF;
+    static constexpr int mat_off = int(align_up(size_t(vec_off + NV * kGcVecF), 256));
+    static constexpr int floats = int(align_up(size_t(mat_off + NM * kGcMatF), NM > 0 ? 256 : 32));
+    static constexpr uint32_t tx_bytes(int nv, int nm) { return uint32_t(kGcThF + nv * kGcVecF + nm * kGcMatF) * 4u; }
+    // dynamic shared memory: the ring, its barriers, slack to align the base to 1024 bytes
+    static constexpr int smem = int(size_t(NS) * floats * 4 + NS * sizeof(uint64_t) + 1024);
+};
+
+// The whole warp converts a landed stage's angles: cosines in place, sines
+// into the stage's sine area.
+__device__ __forceinline__ void gc_convert(float *st, int lane) {
+    float *sn = st + kGcThF;
+    for (int i = lane; i < kGcThF; i += 32) {
+        float c, sv;
+        unbiased_cos_sin(st[i], c, sv);
+        st[i] = c;
+        sn[i] = sv;
     }
-    __syncthreads();
+    __syncwarp();
 }
 
-// A_t = G(theta_t) diag(a_t) (a NULL: G(theta_t)), row-major 8 x 8 per step:
-// thread j of a step forms column j = a_j G(theta_t) e_j.
-__global__ void __launch_bounds__(kColBlock)
-    givens_materialise_kernel(const float *__restrict__ theta, const float *__restrict__ a, float *__restrict__ A,
-                              int64_t steps) {
-    __shared__ __align__(16) float cs_sm[kColSteps * GN], sn_sm[kColSteps * GN];
-    const int64_t s0 = int64_t(blockIdx.x) * kColSteps;
-    const int nsteps = int(min64(kColSteps, steps - s0));
-    stage_step_angles(theta, s0, nsteps, cs_sm, sn_sm);
-    const int u = threadIdx.x >> 3, j = threadIdx.x & 7;
-    if (u >= nsteps) return;
-    const int64_t st = s0 + u;
-    float cs[GN], sv[GN];
-    lds_vec<GN>(cs_sm + u * GN, cs);
-    lds_vec<GN>(sn_sm + u * GN, sv);
-    const float aj = a != nullptr ? a[st * GK + j] : 1.f;
-    float x[GK];
+// x <- G^T x (the transposed mesh: layer k first, each by its transposed rotations)
+__device__ __forceinline__ void mesh_apply_t(float (&x)[GK], const float (&cs)[GN], const float (&sn)[GN]) {
 #pragma unroll
-    for (int i = 0; i < GK; ++i) x[i] = (i == j) ? aj : 0.f;
-    mesh_apply(x, cs, sv);
-    // for each row, the step's eight threads write its 32 contiguous bytes
-    float *out = A + st * (GK * GK) + j;
-#pragma unroll
-    for (int i = 0; i < GK; ++i) st_cs(out + i * GK, x[i]);
-}
-
-// Angle (and gate) gradients of the affine scan from lambda_t (= db_t) and
-// h_{t-1}: the per-step body of gas_bwd_kernel without the carry.
-__global__ void __launch_bounds__(128)
-    gas_grad_kernel(const float *__restrict__ theta, const float *__restrict__ a, const float *__restrict__ lam_in,
-                    const float *__restrict__ h, const float *__restrict__ h0, float *__restrict__ dth,
-                    float *__restrict__ da, int64_t B, int64_t T, int64_t H) {
-    const int64_t st = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;  // (b, t, head)
-    if (st >= B * T * H) return;
-    int64_t hd, t, bi;
-    if (B * T * H <= 0x7fffffff) {  // 32-bit divisions where the index fits
-        const int s32 = int(st), q = s32 / int(H), b32 = q / int(T);
-        hd = s32 - q * int(H);
-        t = q - b32 * int(T);
-        bi = b32;
-    } else {
-        const int64_t q = st / H;
-        hd = st - q * H;
-        bi = q / T;
-        t = q - bi * T;
-    }
-    float cs[GN], sv[GN];
-#pragma unroll
-    for (int n = 0; n < GN; ++n) unbiased_cos_sin(theta[st * GN + n], cs[n], sv[n]);
-    float lam[GK], hp[GK], av[GK];
-    lds_vec<GK>(lam_in + st * GK, lam);
-    if (t >= 1) {
-        lds_vec<GK>(h + (st - H) * GK, hp);
-    } else if (h0 != nullptr) {
-        lds_vec<GK>(h0 + (bi * H + hd) * GK, hp);
-    } else {
-#pragma unroll
-        for (int i = 0; i < GK; ++i) hp[i] = 0.f;
-    }
-    if (a != nullptr) {
-        lds_vec<GK>(a + st * GK, av);
-    } else {
-#pragma unroll
-        for (int i = 0; i < GK; ++i) av[i] = 1.f;
-    }
-    float xl[GK][GK];
-#pragma unroll
-    for (int i = 0; i < GK; ++i) xl[0][i] = av[i] * hp[i];
-#pragma unroll
-    for (int l = 0; l < GK; ++l) {
-        if (l > 0) {
-#pragma unroll
-            for (int i = 0; i < GK; ++i) xl[l][i] = xl[l - 1][i];
-        }
+    for (int l = GK - 1; l >= 0; --l)
 #pragma unroll
         for (int q = 0; q < layer_pairs(l); ++q) {
             const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-            rot_fwd(xl[l][p], xl[l][p + 1], cs[n], sv[n]);
+            rot_bwd(x[p], x[p + 1], cs[n], sn[n]);
         }
-    }
-    float dthv[GN];
-#pragma unroll
-    for (int l = GK - 1; l >= 0; --l) {
-#pragma unroll
-        for (int q = 0; q < layer_pairs(l); ++q) {
-            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-            dthv[n] = fmaf(lam[p + 1], xl[l][p], -lam[p] * xl[l][p + 1]);
-            rot_bwd(lam[p], lam[p + 1], cs[n], sv[n]);
-        }
-    }
-    stg_vec_cs<GN>(dth + st * GN, dthv);
-    if (da != nullptr) {
-        float dav[GK];
-#pragma unroll
-        for (int i = 0; i < GK; ++i) dav[i] = lam[i] * hp[i];
-        stg_vec_cs<GK>(da + st * GK, dav);
-    }
 }
 
-// Angle gradients of the matrix scan from dA_t and A_t = G(theta_t) (both in
-// the workspace): d theta_n = <dA_t, dG/dtheta_n> = sum_j mu_j^T (dG/dtheta_n) e_j.
-// Thread j of a step takes column j back through the layers: x = A_t[:, j]
-// (= G e_j; each layer undone by its transposed rotations, exact up to
-// rounding since the mesh is orthogonal) and mu = dA_t[:, j], adding
-// mu_p+1 x_p - mu_p x_p+1 to angle n at its layer; the eight columns' shares
-// are summed by a butterfly reduce-scatter that leaves angles 4j .. 4j+3 with
-// thread j.  Threads past the last step carry zeros through the exchange.
-__global__ void __launch_bounds__(kColBlock)
-    gms_grad_kernel(const float *__restrict__ theta, const float *__restrict__ A, const float *__restrict__ dA,
-                    float *__restrict__ dth, int64_t steps) {
-    __shared__ __align__(16) float cs_sm[kColSteps * GN], sn_sm[kColSteps * GN];
-    const int64_t s0 = int64_t(blockIdx.x) * kColSteps;
-    const int nsteps = int(min64(kColSteps, steps - s0));
-    stage_step_angles(theta, s0, nsteps, cs_sm, sn_sm);
-    const int u = threadIdx.x >> 3, j = threadIdx.x & 7;
-    const bool valid = u < nsteps;
-    const int64_t st = s0 + (valid ? u : 0);
-    float cs[GN], sv[GN], x[GK], mu[GK];
-    lds_vec<GN>(cs_sm + (valid ? u : 0) * GN, cs);
-    lds_vec<GN>(sn_sm + (valid ? u : 0) * GN, sv);
+// Element j of a register vector, selected without dynamic indexing.
+__device__ __forceinline__ float pick8(const float (&v)[GK], int j) {
+    float r = v[0];
+#pragma unroll
+    for (int i = 1; i < GK; ++i) r = (i == j) ? v[i] : r;
+    return r;
+}
+
+// Common per-item set-up of the chunked Givens kernels: the ring and the item.
+struct GcItem {
+    ChunkItem it;
+    int sub, col, nl;
+    int64_t tb, te, len, nb;
+    __device__ GcItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int64_t T, int64_t H, int64_t Lc)
+        : it(item, nper, cfirst, gpb, kGcLanes) {
+        sub = int(threadIdx.x) >> 3;
+        col = int(threadIdx.x) & 7;
+        nl = int(min64(kGcLanes, H - it.head0));
+        tb = it.c * Lc;
+        te = min64(T, tb + Lc);
+        len = te - tb;
+        nb = (len + kGcTS - 1) / kGcTS;
+    }
+};
+
+#define MGS_GC_WAIT_OR_RETURN(rg, s)                          \
+    if (!(rg).wait(s, ctl)) {                                 \
+        if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);   \
+        (rg).drain(ctl, lane);                                \
+        return;                                               \
+    }
+
+// ---- affine scan, launch 1 forward: h_end = M h_in + c of chunks 0 .. C-2
+__global__ void __launch_bounds__(32)
+    gc_affine_fwd_agg_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, float *__restrict__ Ms, float *__restrict__ Cs,
+                             int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using L = GcStage<2, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C - 1, 0, gpb, T, H, Lc);
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.tb + j * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(2, 0));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off, &tmA, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off + kGcVecF, &tmB, 0, w.it.head0, r, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mcol[GK], cv[GK];  // column col of M; the whole offset c
 #pragma unroll
     for (int i = 0; i < GK; ++i) {
-        x[i] = valid ? A[st * (GK * GK) + i * GK + j] : 0.f;
-        mu[i] = valid ? __ldcs(dA + st * (GK * GK) + i * GK + j) : 0.f;
+        mcol[i] = (i == w.col) ? 1.f : 0.f;
+        cv[i] = 0.f;
     }
-    float d[32];
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int n = int(min64(kGcTS, w.len - j * kGcTS));
+        for (int u = 0; u < n; ++u) {
+            const int item = u * kGcLanes + w.sub;
+            float cs[GN], sv[GN], av[GK], bv[GK];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            lds_vec<GK>(st + L::vec_off + item * GK, av);
+            lds_vec<GK>(st + L::vec_off + kGcVecF + item * GK, bv);
 #pragma unroll
-    for (int l = GK - 1; l >= 0; --l) {
+            for (int i = 0; i < GK; ++i) {
+                mcol[i] *= av[i];
+                cv[i] *= av[i];
+            }
+            mesh_apply(mcol, cs, sv);
+            mesh_apply(cv, cs, sv);
 #pragma unroll
-        for (int q = 0; q < layer_pairs(l); ++q) {
-            const int p = (l & 1) + 2 * q, n = layer_base(l) + q;
-            d[n] = fmaf(mu[p + 1], x[p], -mu[p] * x[p + 1]);
-            rot_bwd(x[p], x[p + 1], cs[n], sv[n]);
-            rot_bwd(mu[p], mu[p + 1], cs[n], sv[n]);
+            for (int i = 0; i < GK; ++i) cv[i] += bv[i];
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
         }
     }
+    const int64_t itm = w.it.g * C + w.it.c;
+    st_ws_col<GK>(Ms + itm * (kGcLanes * GK * GK) + w.sub * GK * GK, w.col, mcol);
+    __stcg(Cs + itm * (kGcLanes * GK) + w.sub * GK + w.col, pick8(cv, w.col));
+}
+
+// ---- affine scan, launch 3 forward: h_t from each chunk's carry
+__global__ void __launch_bounds__(32)
+    gc_affine_fwd_out_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, float *__restrict__ h,
+                             const float *__restrict__ Es, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc,
+                             DevCtl ctl) {
+    using L = GcStage<2, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C, 0, gpb, T, H, Lc);
+    const bool active = w.sub < w.nl;
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.tb + j * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(2, 0));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off, &tmA, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off + kGcVecF, &tmB, 0, w.it.head0, r, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    pdl_wait();  // the carries of launch 2
+    float x[GK];
+    lds_row_global<GK>(Es + (w.it.g * C + w.it.c) * (kGcLanes * GK) + w.sub * GK, x);
+    float *hp = h + ((w.it.bi * T + w.tb) * H + w.it.head0 + w.sub) * GK + w.col;
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int n = int(min64(kGcTS, w.len - j * kGcTS));
+        for (int u = 0; u < n; ++u) {
+            const int item = u * kGcLanes + w.sub;
+            float cs[GN], sv[GN], av[GK], bv[GK];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            lds_vec<GK>(st + L::vec_off + item * GK, av);
+            lds_vec<GK>(st + L::vec_off + kGcVecF + item * GK, bv);
 #pragma unroll
-    for (int n = GN; n < 32; ++n) d[n] = 0.f;
+            for (int i = 0; i < GK; ++i) x[i] *= av[i];
+            mesh_apply(x, cs, sv);
 #pragma unroll
-    for (int o = 4, half = 16; o >= 1; o >>= 1, half >>= 1) {
-        const bool up = (j & o) != 0;
-#pragma unroll
-        for (int c = 0; c < half; ++c) {
-            const float send = up ? d[c] : d[c + half];
-            const float keep = up ? d[c + half] : d[c];
-            d[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            for (int i = 0; i < GK; ++i) x[i] += bv[i];
+            if (active) st_cs(hp, pick8(x, w.col));
+            hp += H * GK;
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
         }
     }
-    if (valid && j < GN / 4) st_cs4(dth + st * GN + 4 * j, make_float4(d[0], d[1], d[2], d[3]));
+}
+
+// ---- affine scan, launch 1 backward: mu_out = M mu_in + C of chunks 1 .. C-1
+// (per step lambda = g + mu, mu <- A^T lambda = a * G^T lambda)
+__global__ void __launch_bounds__(32)
+    gc_affine_bwd_agg_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmG, float *__restrict__ Ms, float *__restrict__ Cs,
+                             int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using L = GcStage<2, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C - 1, 1, gpb, T, H, Lc);
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    // block j covers t = te-1-j*TS down to max(tb, te-(j+1)*TS); boxes start at
+    // row te-(j+1)*TS, step u at box row TS-1-u
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.te - (j + 1) * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(2, 0));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off, &tmA, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off + kGcVecF, &tmG, 0, w.it.head0, r, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mcol[GK], mu[GK];  // column col of M; the whole offset C
+#pragma unroll
+    for (int i = 0; i < GK; ++i) {
+        mcol[i] = (i == w.col) ? 1.f : 0.f;
+        mu[i] = 0.f;
+    }
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int64_t tt = w.te - 1 - j * kGcTS;
+        const int n = int(min64(kGcTS, tt - w.tb + 1));
+        for (int u = 0; u < n; ++u) {
+            const int item = (kGcTS - 1 - u) * kGcLanes + w.sub;
+            float cs[GN], sv[GN], av[GK], gv[GK];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            lds_vec<GK>(st + L::vec_off + item * GK, av);
+            lds_vec<GK>(st + L::vec_off + kGcVecF + item * GK, gv);
+#pragma unroll
+            for (int i = 0; i < GK; ++i) mu[i] += gv[i];
+            mesh_apply_t(mu, cs, sv);
+            mesh_apply_t(mcol, cs, sv);
+#pragma unroll
+            for (int i = 0; i < GK; ++i) {
+                mu[i] *= av[i];
+                mcol[i] *= av[i];
+            }
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    const int64_t itm = w.it.g * C + w.it.c;
+    st_ws_col<GK>(Ms + itm * (kGcLanes * GK * GK) + w.sub * GK * GK, w.col, mcol);
+    __stcg(Cs + itm * (kGcLanes * GK) + w.sub * GK + w.col, pick8(mu, w.col));
+}
+
+// ---- affine scan, launch 3 backward: d theta, da, db (dh0 from chunk 0)
+__global__ void __launch_bounds__(32)
+    gc_affine_bwd_out_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmH,
+                             const float *__restrict__ h0, float *__restrict__ dth, float *__restrict__ da,
+                             float *__restrict__ db, float *__restrict__ dh0, const float *__restrict__ Es,
+                             int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using L = GcStage<3, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C, 0, gpb, T, H, Lc);
+    const bool active = w.sub < w.nl;
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    // as in launch 1; the h box starts one row earlier and holds h_{t-1}
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.te - (j + 1) * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(3, 0));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off, &tmA, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off + kGcVecF, &tmG, 0, w.it.head0, r, &bars[s], pol);
+        tma_load_3d(st + L::vec_off + 2 * kGcVecF, &tmH, 0, w.it.head0, r - 1, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float h0v[GK];
+#pragma unroll
+    for (int i = 0; i < GK; ++i) h0v[i] = 0.f;
+    if (h0 != nullptr && active) lds_row_global<GK>(h0 + (w.it.bi * H + w.it.head0 + w.sub) * GK, h0v);
+    pdl_wait();  // the carries of launch 2
+    float mu[GK];  // A_{t+1}^T lambda_{t+1} past the step, the whole vector
+    lds_row_global<GK>(Es + (w.it.g * C + w.it.c) * (kGcLanes * GK) + w.sub * GK, mu);
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int64_t tt = w.te - 1 - j * kGcTS;
+        const int n = int(min64(kGcTS, tt - w.tb + 1));
+        for (int u = 0; u < n; ++u) {
+            const int64_t t = tt - u;
+            const int item = (kGcTS - 1 - u) * kGcLanes + w.sub;
+            float cs[GN], sv[GN], av[GK], lam[GK], hp[GK];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            lds_vec<GK>(st + L::vec_off + item * GK, av);
+            lds_vec<GK>(st + L::vec_off + kGcVecF + item * GK, lam);
+            if (t >= 1) {
+                lds_vec<GK>(st + L::vec_off + 2 * kGcVecF + item * GK, hp);
+            } else {
+#pragma unroll
+                for (int i = 0; i < GK; ++i) hp[i] = h0v[i];
+            }
+#pragma unroll
+            for (int i = 0; i < GK; ++i) lam[i] += mu[i];
+            const int64_t o = (w.it.bi * T + t) * H + w.it.head0 + w.sub;
+            if (active) st_cs(db + o * GK + w.col, pick8(lam, w.col));
+            // forward through the layers from a * h_{t-1}, keeping each rotation's output pair
+            float x[GK], pr[2 * GN];
+#pragma unroll
+            for (int i = 0; i < GK; ++i) x[i] = av[i] * hp[i];
+#pragma unroll
+            for (int l = 0; l < GK; ++l)
+#pragma unroll
+                for (int q = 0; q < layer_pairs(l); ++q) {
+                    const int p = (l & 1) + 2 * q, nn = layer_base(l) + q;
+                    rot_fwd(x[p], x[p + 1], cs[nn], sv[nn]);
+                    pr[2 * nn] = x[p];
+                    pr[2 * nn + 1] = x[p + 1];
+                }
+            // lambda back through the layers; each angle's gradient on the way
+            float dthv[GN];
+#pragma unroll
+            for (int l = GK - 1; l >= 0; --l)
+#pragma unroll
+                for (int q = 0; q < layer_pairs(l); ++q) {
+                    const int p = (l & 1) + 2 * q, nn = layer_base(l) + q;
+                    dthv[nn] = fmaf(lam[p + 1], pr[2 * nn], -lam[p] * pr[2 * nn + 1]);
+                    rot_bwd(lam[p], lam[p + 1], cs[nn], sv[nn]);
+                }
+            if (active) {
+                // thread col < 7 stores angles 4 col .. 4 col + 3
+#pragma unroll
+                for (int c4 = 0; c4 < GN / 4; ++c4)
+                    if (c4 == w.col)
+                        st_cs4(dth + o * GN + 4 * c4,
+                               make_float4(dthv[4 * c4], dthv[4 * c4 + 1], dthv[4 * c4 + 2], dthv[4 * c4 + 3]));
+                if (da != nullptr) st_cs(da + o * GK + w.col, pick8(lam, w.col) * pick8(hp, w.col));
+            }
+#pragma unroll
+            for (int i = 0; i < GK; ++i) mu[i] = av[i] * lam[i];
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    if (w.it.c == 0 && dh0 != nullptr && active)
+        dh0[(w.it.bi * H + w.it.head0 + w.sub) * GK + w.col] = pick8(mu, w.col);
+}
+
+// ---- matrix scan, launch 1 forward: M = G_e ... G_s of chunks 0 .. C-2
+__global__ void __launch_bounds__(32)
+    gc_matrix_fwd_agg_kernel(const __grid_constant__ CUtensorMap tmTh, float *__restrict__ Ms, int64_t T, int64_t H,
+                             int64_t gpb, int64_t C, int64_t Lc, DevCtl ctl) {
+    using L = GcStage<0, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C - 1, 0, gpb, T, H, Lc);
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(0, 0));
+        tma_load_3d(ring + size_t(s) * L::floats, &tmTh, 0, w.it.head0, int(w.it.bi * T + w.tb + j * kGcTS), &bars[s],
+                    pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float v[GK];
+#pragma unroll
+    for (int i = 0; i < GK; ++i) v[i] = (i == w.col) ? 1.f : 0.f;
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int n = int(min64(kGcTS, w.len - j * kGcTS));
+        for (int u = 0; u < n; ++u) {
+            const int item = u * kGcLanes + w.sub;
+            float cs[GN], sv[GN];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            mesh_apply(v, cs, sv);
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    st_ws_col<GK>(Ms + (w.it.g * C + w.it.c) * GcTile::MF + w.sub * GK * GK, w.col, v);
+}
+
+// ---- matrix scan, launch 3 forward: P_t from each chunk's carry
+__global__ void __launch_bounds__(32)
+    gc_matrix_fwd_out_kernel(const __grid_constant__ CUtensorMap tmTh, float *__restrict__ P,
+                             const float *__restrict__ Es, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc,
+                             DevCtl ctl) {
+    using L = GcStage<0, 0>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C, 0, gpb, T, H, Lc);
+    const bool active = w.sub < w.nl;
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(0, 0));
+        tma_load_3d(ring + size_t(s) * L::floats, &tmTh, 0, w.it.head0, int(w.it.bi * T + w.tb + j * kGcTS), &bars[s],
+                    pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    pdl_wait();  // the carries of launch 2
+    float v[GK];
+    ld_ws_col<GK>(Es + (w.it.g * C + w.it.c) * GcTile::MF + w.sub * GK * GK, w.col, v);
+    float *pp = P + ((w.it.bi * T + w.tb) * H + w.it.head0 + w.sub) * (GK * GK) + w.col;
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int n = int(min64(kGcTS, w.len - j * kGcTS));
+        for (int u = 0; u < n; ++u) {
+            const int item = u * kGcLanes + w.sub;
+            float cs[GN], sv[GN];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+            mesh_apply(v, cs, sv);
+            if (active) {
+#pragma unroll
+                for (int i = 0; i < GK; ++i) st_cs(pp + i * GK, v[i]);
+            }
+            pp += H * GK * GK;
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
+}
+
+// ---- matrix scan, launch 1 backward: (M, C) of chunks 1 .. C-1, M = G_s^T ... G_e^T
+__global__ void __launch_bounds__(32)
+    gc_matrix_bwd_agg_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmG,
+                             float *__restrict__ Ms, float *__restrict__ Cs, int64_t T, int64_t H, int64_t gpb,
+                             int64_t C, int64_t Lc, DevCtl ctl) {
+    using L = GcStage<0, 1>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C - 1, 1, gpb, T, H, Lc);
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_last();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.te - (j + 1) * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(0, 1));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        GcTile::load(st + L::mat_off, &tmG, w.it.head0, r, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    float mcol[GK], mu[GK];  // columns col of M and of C
+#pragma unroll
+    for (int i = 0; i < GK; ++i) {
+        mcol[i] = (i == w.col) ? 1.f : 0.f;
+        mu[i] = 0.f;
+    }
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int64_t tt = w.te - 1 - j * kGcTS;
+        const int n = int(min64(kGcTS, tt - w.tb + 1));
+        for (int u = 0; u < n; ++u) {
+            const int q = kGcTS - 1 - u;
+            const int item = q * kGcLanes + w.sub;
+            const TileRef<GK, true> Gt{st + L::mat_off, q, w.sub};
+            float cs[GN], sv[GN];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+#pragma unroll
+            for (int i = 0; i < GK; ++i) mu[i] += Gt.at(i, w.col);
+            mesh_apply_t(mu, cs, sv);
+            mesh_apply_t(mcol, cs, sv);
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
+    const int64_t slot = (w.it.g * C + w.it.c) * GcTile::MF + w.sub * GK * GK;
+    st_ws_col<GK>(Ms + slot, w.col, mcol);
+    st_ws_col<GK>(Cs + slot, w.col, mu);
+}
+
+// ---- matrix scan, launch 3 backward: d theta from each chunk's carry; per
+// step and column j: Lambda = G_t[:, j] + carry, x = P_t[:, j], both back
+// through the layers (x recovers the pre-rotation columns), the eight
+// columns' shares of each angle summed by a butterfly reduce-scatter
+__global__ void __launch_bounds__(32)
+    gc_matrix_bwd_out_kernel(const __grid_constant__ CUtensorMap tmTh, const __grid_constant__ CUtensorMap tmP,
+                             const __grid_constant__ CUtensorMap tmG, float *__restrict__ dth,
+                             const float *__restrict__ Es, int64_t T, int64_t H, int64_t gpb, int64_t C, int64_t Lc,
+                             DevCtl ctl) {
+    using L = GcStage<0, 2>;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    float *ring = reinterpret_cast<float *>(align_smem(smem_raw, 1024));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + L::NS * L::floats);
+    const int lane = threadIdx.x;
+    const GcItem w(blockIdx.x, C, 0, gpb, T, H, Lc);
+    const bool active = w.sub < w.nl;
+    WarpRing<L::NS> rg;
+    rg.init(bars, lane);
+    const uint64_t pol = policy_evict_first();
+    auto issue = [&](int s, int64_t j) {  // lane 0 only
+        float *st = ring + size_t(s) * L::floats;
+        const int r = int(w.it.bi * T + w.te - (j + 1) * kGcTS);
+        mbar_arrive_expect_tx(&bars[s], L::tx_bytes(0, 2));
+        tma_load_3d(st, &tmTh, 0, w.it.head0, r, &bars[s], pol);
+        GcTile::load(st + L::mat_off, &tmP, w.it.head0, r, &bars[s], pol);
+        GcTile::load(st + L::mat_off + kGcMatF, &tmG, w.it.head0, r, &bars[s], pol);
+    };
+    const int npro = int(min64(L::NS, w.nb));
+    if (lane == 0)
+        for (int s = 0; s < npro; ++s) issue(s, s);
+    for (int s = 0; s < npro; ++s) rg.armed(s);
+
+    pdl_wait();  // the carries of launch 2
+    float carry[GK];
+    ld_ws_col<GK>(Es + (w.it.g * C + w.it.c) * GcTile::MF + w.sub * GK * GK, w.col, carry);
+    for (int64_t j = 0; j < w.nb; ++j) {
+        const int s = int(j % L::NS);
+        MGS_GC_WAIT_OR_RETURN(rg, s);
+        float *st = ring + size_t(s) * L::floats;
+        gc_convert(st, lane);
+        const int64_t tt = w.te - 1 - j * kGcTS;
+        const int n = int(min64(kGcTS, tt - w.tb + 1));
+        for (int u = 0; u < n; ++u) {
+            const int64_t t = tt - u;
+            const int q = kGcTS - 1 - u;
+            const int item = q * kGcLanes + w.sub;
+            const TileRef<GK, true> Pt{st + L::mat_off, q, w.sub}, Gt{st + L::mat_off + kGcMatF, q, w.sub};
+            float cs[GN], sv[GN], lam[GK], x[GK];
+            lds_vec<GN>(st + item * GN, cs);
+            lds_vec<GN>(st + kGcThF + item * GN, sv);
+#pragma unroll
+            for (int i = 0; i < GK; ++i) {
+                lam[i] = Gt.at(i, w.col) + carry[i];
+                x[i] = Pt.at(i, w.col);
+            }
+            float d[32];
+#pragma unroll
+            for (int l = GK - 1; l >= 0; --l)
+#pragma unroll
+                for (int qq = 0; qq < layer_pairs(l); ++qq) {
+                    const int p = (l & 1) + 2 * qq, nn = layer_base(l) + qq;
+                    d[nn] = fmaf(lam[p + 1], x[p], -lam[p] * x[p + 1]);
+                    rot_bwd(x[p], x[p + 1], cs[nn], sv[nn]);
+                    rot_bwd(lam[p], lam[p + 1], cs[nn], sv[nn]);
+                }
+#pragma unroll
+            for (int nn = GN; nn < 32; ++nn) d[nn] = 0.f;
+#pragma unroll
+            for (int o = 4, half = 16; o >= 1; o >>= 1, half >>= 1) {
+                const bool up = (w.col & o) != 0;
+#pragma unroll
+                for (int c = 0; c < half; ++c) {
+                    const float send = up ? d[c] : d[c + half];
+                    const float keep = up ? d[c + half] : d[c];
+                    d[c] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            if (active && w.col < GN / 4)
+                st_cs4(dth + ((w.it.bi * T + t) * H + w.it.head0 + w.sub) * GN + 4 * w.col,
+                       make_float4(d[0], d[1], d[2], d[3]));
+#pragma unroll
+            for (int i = 0; i < GK; ++i) carry[i] = lam[i];
+        }
+        __syncwarp();
+        if (j + L::NS < w.nb) {
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(s, j + L::NS);
+            }
+            rg.armed(s);
+        }
+    }
 }
 
 // Lanes per recurrence warp for the affine scan: as many as keep at least
@@ -1070,21 +1560,28 @@ int gas_lanes_per_block(int64_t B, int64_t H) {
 // chunks (fewer than 256 groups of 4 lanes) and T is at least 256.
 bool few_lane_path(int64_t B, int64_t T, int64_t H) { return T >= 256 && mas_workspace_bytes(B, T, H, GK) > 0; }
 
-size_t mat_bytes(int64_t B, int64_t T, int64_t H) { return align_up(size_t(B * T * H) * GK * GK * 4, 256); }
-
-inline unsigned grid_for(int64_t n, int block) { return unsigned((n + block - 1) / block); }
 
 }  // namespace
 
 size_t givens_workspace_bytes(int op, int64_t B, int64_t T, int64_t H) {
     if (!few_lane_path(B, T, H)) return 0;
+    // the chunk aggregates and carries only, laid out as matrix_affine_scan's
+    // (affine) and matrix_scan's (matrix) chunked paths lay out theirs
     switch (op) {
-        case 0: return mat_bytes(B, T, H) + mas_workspace_bytes(B, T, H, GK);             // affine fwd
-        case 1: return 2 * mat_bytes(B, T, H) + mas_workspace_bytes(B, T, H, GK);         // affine bwd
-        case 2: return mat_bytes(B, T, H) + ms_workspace_bytes(B, T, H, GK, false);       // matrix fwd
-        default: return 2 * mat_bytes(B, T, H) + ms_workspace_bytes(B, T, H, GK, true);   // matrix bwd
+        case 0:
+        case 1: return mas_workspace_bytes(B, T, H, GK);
+        case 2: return ms_workspace_bytes(B, T, H, GK, false);
+        default: return ms_workspace_bytes(B, T, H, GK, true);
     }
 }
+
+namespace {
+// Tensor maps of the chunked Givens kernels: angle and vector boxes of
+// kGcTS steps x kGcLanes heads.
+cudaError_t gc_vec_map(CUtensorMap *m, const float *base, int64_t B, int64_t T, int64_t H, int E) {
+    return make_head_map(m, base, B * T, H, E, kGcLanes, kGcTS);
+}
+}  // namespace
 
 const SinCosTable &sincos_table() {
     static const SinCosTable t = SinCosTable::build();
@@ -1098,12 +1595,24 @@ cudaError_t launch_gas_fwd(const float *theta, const float *a, const float *b, c
     // few-lane path's fp32 matrix kernels cannot carry the extra precision)
     const bool xo = a == nullptr;
     if (!xo && few_lane_path(B, T, H)) {
-        float *A = static_cast<float *>(ws);
-        const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, a, A, B * T * H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_mas_fwd(GK, A, b, h0, h, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
+        const ChunkPlan pl = plan_chunks(B, T, H, GK);
+        const int64_t gpb = (H + kGcLanes - 1) / kGcLanes;
+        const ScanWs w(static_cast<unsigned char *>(ws), pl, kGcLanes * GK * GK, kGcLanes * GK);
+        CUtensorMap tTh, tA, tB;
+        cudaError_t e;
+        if ((e = gc_vec_map(&tTh, theta, B, T, H, GN)) != cudaSuccess) return e;
+        if ((e = gc_vec_map(&tA, a, B, T, H, GK)) != cudaSuccess) return e;
+        if ((e = gc_vec_map(&tB, b, B, T, H, GK)) != cudaSuccess) return e;
+        constexpr int smem = GcStage<2, 0>::smem;
+        if ((e = ensure_smem_attr((const void *)gc_affine_fwd_agg_kernel, smem)) != cudaSuccess) return e;
+        if ((e = ensure_smem_attr((const void *)gc_affine_fwd_out_kernel, smem)) != cudaSuccess) return e;
+        gc_affine_fwd_agg_kernel<<<dim3(unsigned(pl.G * (pl.C - 1))), 32, smem, s>>>(tTh, tA, tB, w.M, w.Cv, T, H, gpb,
+                                                                                   pl.C, pl.L, ctl);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_chain<GK, false, true, +1>(w.M, w.Cv, w.E, h0, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess)
+            return e;
+        return launch_pdl(gc_affine_fwd_out_kernel, dim3(unsigned(pl.G * pl.C)), smem, s, tTh, tA, tB, h, w.E, T, H,
+                          gpb, pl.C, pl.L, ctl);
     }
     const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
@@ -1131,20 +1640,25 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
                            void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
     const bool xo = a == nullptr;  // as in the forward
     if (!xo && few_lane_path(B, T, H)) {
-        // lambda_t = db_t and dh0 come from the time-chunked matrix_affine_scan
-        // backward (dA goes to the workspace, unused); the angle and gate
-        // gradients then follow per step from lambda_t and h_{t-1}
-        float *A = static_cast<float *>(ws);
-        const size_t mb = mat_bytes(B, T, H);
-        float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, a, A, B * T * H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if ((e = launch_mas_bwd(GK, A, h0, h, gh, dA, db, dh0, B, T, H, static_cast<char *>(ws) + 2 * mb,
-                                ws_bytes - 2 * mb, ctl, s)) != cudaSuccess)
+        const ChunkPlan pl = plan_chunks(B, T, H, GK);
+        const int64_t gpb = (H + kGcLanes - 1) / kGcLanes;
+        const ScanWs w(static_cast<unsigned char *>(ws), pl, kGcLanes * GK * GK, kGcLanes * GK);
+        CUtensorMap tTh, tA, tG, tH;
+        cudaError_t e;
+        if ((e = gc_vec_map(&tTh, theta, B, T, H, GN)) != cudaSuccess) return e;
+        if ((e = gc_vec_map(&tA, a, B, T, H, GK)) != cudaSuccess) return e;
+        if ((e = gc_vec_map(&tG, gh, B, T, H, GK)) != cudaSuccess) return e;
+        if ((e = gc_vec_map(&tH, h, B, T, H, GK)) != cudaSuccess) return e;
+        constexpr int sa = GcStage<2, 0>::smem, so = GcStage<3, 0>::smem;
+        if ((e = ensure_smem_attr((const void *)gc_affine_bwd_agg_kernel, sa)) != cudaSuccess) return e;
+        if ((e = ensure_smem_attr((const void *)gc_affine_bwd_out_kernel, so)) != cudaSuccess) return e;
+        gc_affine_bwd_agg_kernel<<<dim3(unsigned(pl.G * (pl.C - 1))), 32, sa, s>>>(tTh, tA, tG, w.M, w.Cv, T, H, gpb,
+                                                                                 pl.C, pl.L, ctl);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_chain<GK, false, true, -1>(w.M, w.Cv, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) != cudaSuccess)
             return e;
-        gas_grad_kernel<<<grid_for(B * T * H, 128), 128, 0, s>>>(theta, a, db, h, h0, dth, da, B, T, H);
-        return cudaGetLastError();
+        return launch_pdl(gc_affine_bwd_out_kernel, dim3(unsigned(pl.G * pl.C)), so, s, tTh, tA, tG, tH, h0, dth, da,
+                          db, dh0, w.E, T, H, gpb, pl.C, pl.L, ctl);
     }
     const int lpw = gas_lanes_per_block(B, H), ts = kItems / lpw;
     const int64_t rows = B * T;
@@ -1171,12 +1685,23 @@ cudaError_t launch_gas_bwd(const float *theta, const float *a, const float *h0, 
 cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, int64_t H, void *ws,
                            size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
     if (few_lane_path(B, T, H)) {
-        float *A = static_cast<float *>(ws);
-        const size_t mb = mat_bytes(B, T, H);
-        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, nullptr, A, B * T * H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_ms_fwd(GK, A, P, B, T, H, static_cast<char *>(ws) + mb, ws_bytes - mb, ctl, s);
+        const ChunkPlan pl = plan_chunks(B, T, H, GK);
+        const int64_t gpb = (H + kGcLanes - 1) / kGcLanes;
+        const ScanWs w(static_cast<unsigned char *>(ws), pl, GcTile::MF, 0);
+        CUtensorMap tTh;
+        cudaError_t e;
+        if ((e = gc_vec_map(&tTh, theta, B, T, H, GN)) != cudaSuccess) return e;
+        constexpr int smem = GcStage<0, 0>::smem;
+        if ((e = ensure_smem_attr((const void *)gc_matrix_fwd_agg_kernel, smem)) != cudaSuccess) return e;
+        if ((e = ensure_smem_attr((const void *)gc_matrix_fwd_out_kernel, smem)) != cudaSuccess) return e;
+        gc_matrix_fwd_agg_kernel<<<dim3(unsigned(pl.G * (pl.C - 1))), 32, smem, s>>>(tTh, w.M, T, H, gpb, pl.C, pl.L,
+                                                                                   ctl);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_chain<GK, true, false, +1>(w.M, nullptr, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) !=
+            cudaSuccess)
+            return e;
+        return launch_pdl(gc_matrix_fwd_out_kernel, dim3(unsigned(pl.G * pl.C)), smem, s, tTh, P, w.E, T, H, gpb, pl.C,
+                          pl.L, ctl);
     }
     CUtensorMap tTh;
     cudaError_t e;
@@ -1193,17 +1718,25 @@ cudaError_t launch_gms_fwd(const float *theta, float *P, int64_t B, int64_t T, i
 cudaError_t launch_gms_bwd(const float *theta, const float *P, const float *G, float *dth, int64_t B, int64_t T,
                            int64_t H, void *ws, size_t ws_bytes, const DevCtl &ctl, cudaStream_t s) {
     if (few_lane_path(B, T, H)) {
-        float *A = static_cast<float *>(ws);
-        const size_t mb = mat_bytes(B, T, H);
-        float *dA = reinterpret_cast<float *>(static_cast<char *>(ws) + mb);
-        givens_materialise_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, nullptr, A, B * T * H);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        if ((e = launch_ms_bwd(GK, A, P, G, dA, B, T, H, static_cast<char *>(ws) + 2 * mb, ws_bytes - 2 * mb, ctl,
-                               s)) != cudaSuccess)
+        const ChunkPlan pl = plan_chunks(B, T, H, GK);
+        const int64_t gpb = (H + kGcLanes - 1) / kGcLanes;
+        const ScanWs w(static_cast<unsigned char *>(ws), pl, GcTile::MF, GcTile::MF);
+        CUtensorMap tTh, tP, tG;
+        cudaError_t e;
+        if ((e = gc_vec_map(&tTh, theta, B, T, H, GN)) != cudaSuccess) return e;
+        if ((e = GcTile::make(&tP, P, B * T, H, kGcTS)) != cudaSuccess) return e;
+        if ((e = GcTile::make(&tG, G, B * T, H, kGcTS)) != cudaSuccess) return e;
+        constexpr int sa = GcStage<0, 1>::smem, so = GcStage<0, 2>::smem;
+        if ((e = ensure_smem_attr((const void *)gc_matrix_bwd_agg_kernel, sa)) != cudaSuccess) return e;
+        if ((e = ensure_smem_attr((const void *)gc_matrix_bwd_out_kernel, so)) != cudaSuccess) return e;
+        gc_matrix_bwd_agg_kernel<<<dim3(unsigned(pl.G * (pl.C - 1))), 32, sa, s>>>(tTh, tG, w.M, w.Cv, T, H, gpb, pl.C,
+                                                                                 pl.L, ctl);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_chain<GK, true, true, -1>(w.M, w.Cv, w.E, nullptr, pl.G, pl.C, gpb, H, ctl, s)) !=
+            cudaSuccess)
             return e;
-        gms_grad_kernel<<<grid_for(B * T * H, kColSteps), kColBlock, 0, s>>>(theta, A, dA, dth, B * T * H);
-        return cudaGetLastError();
+        return launch_pdl(gc_matrix_bwd_out_kernel, dim3(unsigned(pl.G * pl.C)), so, s, tTh, tP, tG, dth, w.E, T, H,
+                          gpb, pl.C, pl.L, ctl);
     }
     using TM = MatTile<GK, true>;
     CUtensorMap tTh, tP, tG;

@@ -621,19 +621,6 @@ struct ChunkRing {
     static constexpr size_t warp_bytes = align_up(bar_offset + NS * sizeof(uint64_t), 128) + ALIGN;
 };
 
-// Item -> (lane group, chunk) and the lane group's place in the batch.
-struct ChunkItem {
-    int64_t g, c, bi;
-    int head0;
-    __device__ ChunkItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int lpw) {
-        const unsigned q = unsigned(item) / unsigned(nper);  // 32-bit: items, nper and gpb are below 2^32
-        g = q;
-        c = cfirst + (item - int64_t(q) * nper);
-        const unsigned b32 = q / unsigned(gpb);
-        bi = b32;
-        head0 = int(q - b32 * unsigned(gpb)) * lpw;
-    }
-};
 
 // The chunked path is the reduce-then-scan of mgs_chunk.cuh:
 //   forward:  aggregate h_end = M h_in + c of chunks 0 .. C-2 (M = A_e ... A_s

@@ -287,19 +287,6 @@ struct MsChunkShape {
     using TM = MatTile<K>;
 };
 
-// Item -> (lane group, chunk) and the lane group's place in the batch.
-struct ChunkItem {
-    int64_t g, c, bi;
-    int head0;
-    __device__ ChunkItem(int64_t item, int64_t nper, int64_t cfirst, int64_t gpb, int lpw) {
-        const unsigned q = unsigned(item) / unsigned(nper);  // 32-bit: items, nper and gpb are below 2^32
-        g = q;
-        c = cfirst + (item - int64_t(q) * nper);
-        const unsigned b32 = q / unsigned(gpb);
-        bi = b32;
-        head0 = int(q - b32 * unsigned(gpb)) * lpw;
-    }
-};
 
 // Launch 1, forward: the product of the chunk's A_t (chunks 0 .. C-2).
 template <int K>

@@ -147,10 +147,17 @@ def test_givens_workspace_only_for_few_lanes_and_long_T(L):
         assert b.mgs_workspace_size(op, 64, 1024, 64, 8) == 0    # many lanes
         assert b.mgs_workspace_size(op, 16, 128, 8, 8) == 0      # T < 256
         assert b.mgs_workspace_size(op, 16, 1024, 8, 4) == 0     # k != 8: the call reports it
-        n = b.mgs_workspace_size(op, 16, 1024, 8, 8)              # long-T shape: A formed in the workspace
-        assert n >= 16 * 1024 * 8 * 256
+    # long-T shape: time-chunked, still from the angles; the workspace holds only
+    # the chunk aggregates and carries (those of the matrix scans' chunked
+    # paths), never A_t or dA_t (256 bytes per step, 33.5 MB here)
     steps = 16 * 1024 * 8
-    assert b.mgs_workspace_size(b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, 16, 1024, 8, 8) >= 2 * steps * 256
+    for op, same in ((b.MGS_OP_GIVENS_AFFINE_SCAN_FWD, b.MGS_OP_MATRIX_AFFINE_SCAN_FWD),
+                     (b.MGS_OP_GIVENS_AFFINE_SCAN_BWD, b.MGS_OP_MATRIX_AFFINE_SCAN_BWD),
+                     (b.MGS_OP_GIVENS_MATRIX_SCAN_FWD, b.MGS_OP_MATRIX_SCAN_FWD),
+                     (b.MGS_OP_GIVENS_MATRIX_SCAN_BWD, b.MGS_OP_MATRIX_SCAN_BWD)):
+        n = b.mgs_workspace_size(op, 16, 1024, 8, 8)
+        assert 0 < n == b.mgs_workspace_size(same, 16, 1024, 8, 8)
+        assert n < steps * 256 // 8
     th, bb, h = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
     assert _st(b.mgs_givens_affine_scan_fwd, th, None, bb, None, h, 16, 1024, 8, 8) == b.MGS_ERR_WORKSPACE
 

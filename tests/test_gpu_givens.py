@@ -70,7 +70,7 @@ def test_givens_affine_scan(B, T, H, h0, with_a):
 
 
 @pytest.mark.parametrize("B,T,H,h0,with_a", [
-    (2, 300, 3, "normal", True),      # few lanes, long T: A formed in the workspace, time-chunked
+    (2, 300, 3, "normal", True),      # few lanes, long T: time-chunked from the angles
     (1, 517, 4, "none", False),       # ragged chunks, no gate, zero initial state
     (40, 300, 64, "normal", True),    # many lanes, long T: angle-fused kernels
 ])
