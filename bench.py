@@ -553,8 +553,11 @@ def run_gpu(args):
 
     kname, kms, kbytes, kw, kdir = dominant
     achieved = kbytes / (kms * 1e-3) / 1e9
-    chunked = kw.op == "ms" and b.mgs_workspace_size(b.MGS_OP_MATRIX_SCAN_FWD, kw.B, kw.T, kw.H, kw.k) > 0
-    kernel_symbol = f"{kw.op}_{kdir}_{'chunk_' if chunked else ''}kernel"
+    chunked = kw.op in ("ms", "mas") and b.mgs_workspace_size(
+        b.MGS_OP_MATRIX_SCAN_FWD if kw.op == "ms" else b.MGS_OP_MATRIX_AFFINE_SCAN_FWD, kw.B, kw.T, kw.H, kw.k) > 0
+    # the time-chunked path is three launches: aggregates, carry chain, outputs
+    kernel_symbol = (f"{kw.op}_{kdir}_agg_kernel+chain_kernel+{kw.op}_{kdir}_out_kernel" if chunked
+                     else f"{kw.op}_{kdir}_kernel")
     if kw.op == "delta":
         kernel_symbol = "delta_wy_kernel+delta_state_kernel"
     traffic = committed_traffic(kw.op, f"{kernel_symbol}@c{kw.cid}")
