@@ -311,16 +311,18 @@ mgs_status mgs_givens_matrix_scan_bwd(const float *theta, const float *P, const 
  * per (batch, head) lane with a D x D state S (S[i][j], i the value index):
  *     S_t = S_{t-1} + beta_t (v_t - S_{t-1} k_t) k_t^T,   o_t = S_t q_t,
  * S_0 = S0 (zeros when NULL).  Computed chunk by chunk (64 steps) in the WY
- * form: the chunks' W, U (the solve of (I + strict_tril(diag(beta) K K^T))
- * against diag(beta) [K | V]) and tril(Q K^T) first, all chunks at once, then
- * the state carried through the chunks in order.  Only D = 64 is supported
- * (else MGS_ERR_UNSUPPORTED).
+ * form: for every chunk at once, W, U (the solve of
+ * (I + strict_tril(diag(beta) K K^T)) against diag(beta) [K | V]) and
+ * P = tril(Q K^T), folded into the chunk's affine map of the state,
+ * S^T <- M S^T + N, O = R S^T + P U with M = I - K^T W, N = K^T U and
+ * R = Q - P W; then the state carried through the chunks in order.  Only
+ * D = 64 is supported (else MGS_ERR_UNSUPPORTED).
  * In: q, k, v [B][T][H][D]; beta [B][T][H] (4-byte aligned); S0 [B][H][D][D]
  *     (nullable).
  * Out: o [B][T][H][D]; S_T [B][H][D][D] (nullable: not written), the state
  *     after step T (S0, or zeros, when T = 0).
  * Workspace: mgs_workspace_size(MGS_OP_DELTA_SCAN_FWD, B, T, H, 64) bytes
- * (48 KiB per lane and 64-step chunk: W, U, tril(Q K^T) of every chunk),
+ * (64 KiB per lane and 64-step chunk: R, M, (P U)^T and N^T of every chunk),
  * disjoint from every other argument, else MGS_ERR_INVALID_ARG. */
 mgs_status mgs_delta_scan_fwd(const float *q, const float *k, const float *v, const float *beta,
                               const float *S0, float *o, float *S_T, int64_t B, int64_t T, int64_t H,

@@ -163,9 +163,9 @@ def test_givens_workspace_only_for_few_lanes_and_long_T(L):
 
 
 def test_delta_workspace_size(L):
-    # W, U and tril(Q K^T) of every lane's 64-step chunks, 64 x 64 floats each
+    # R, M, (P U)^T and N^T of every lane's 64-step chunks, 64 x 64 floats each
     op = b.MGS_OP_DELTA_SCAN_FWD
-    per_chunk = 3 * 64 * 64 * 4
+    per_chunk = 4 * 64 * 64 * 4
     assert b.mgs_workspace_size(op, 128, 64, 1, 64) == 128 * per_chunk
     assert b.mgs_workspace_size(op, 16, 1024, 1, 64) == 16 * 16 * per_chunk
     assert b.mgs_workspace_size(op, 2, 70, 3, 64) == 2 * 3 * 2 * per_chunk   # ragged tail: a whole chunk

@@ -80,7 +80,7 @@ def test_delta_degenerate_and_errors():
         b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], o, None, 2, 70, 2, 64)
     assert err.value.status == b.MGS_ERR_WORKSPACE
     ws, nws = api.workspace(b.MGS_OP_DELTA_SCAN_FWD, 2, 70, 2, 64, "cuda")
-    assert nws == 2 * 2 * 2 * 3 * 64 * 64 * 4
+    assert nws == 2 * 2 * 2 * 4 * 64 * 64 * 4
     with pytest.raises(b.MGSError) as err:
         b.mgs_delta_scan_fwd(d["q"], d["k"], d["v"], d["beta"], d["S0"], o, None, 2, 70, 2, 64, ws, nws // 2)
     assert err.value.status == b.MGS_ERR_WORKSPACE
