@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(kWyThreads, 2)
                 tma_store_2d(&tmO, 32 * p, row + 3 * CH, sm + L::on + p * PANEL);
             }
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read();
         }
     } while (false);
     // copies and products this block started are complete before its shared

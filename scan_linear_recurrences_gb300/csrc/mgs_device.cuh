@@ -167,8 +167,7 @@ __device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *m
 
 // Tiled TMA store shared -> global through a tensor map (2-D), tracked as a
 // bulk async-group of the issuing thread; the coordinates must not be
-// negative.  bulk_commit() closes the group, bulk_wait_all() waits until
-// every committed group of this thread has completed.
+// negative.  bulk_commit() closes the group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, const void *src_smem) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
@@ -176,7 +175,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int 
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until every committed group of this thread has finished reading its
+// shared-memory source (the source may then be reused or released; the
+// global writes complete on their own).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
