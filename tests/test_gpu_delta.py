@@ -48,6 +48,20 @@ def test_delta_shapes(B, T, H, S0):
     _run(d, T)
 
 
+@pytest.mark.parametrize("B,T,H", [
+    (76, 70, 1),    # 76 lanes: the 32-column state blocks, a ragged second chunk
+    (38, 130, 4),   # 152 lanes: the 64-column state blocks, ragged third chunk
+    (75, 1, 1),     # 75 lanes (the 16-column blocks), one step each
+    (19, 257, 8),   # 152 lanes over five chunks, the last one step long
+])
+def test_delta_state_block_widths(B, T, H):
+    # the state pass splits the value columns into blocks of 64, 32 or 16 by
+    # the lane count; each width, its boundary and a ragged last chunk
+    d = {k: (v.cuda() if v is not None else None)
+         for k, v in inputs.delta_inputs(B, T, H, 64, seed=1400 + B * T + H, with_S0=True).items()}
+    _run(d, T)
+
+
 @pytest.mark.parametrize("cid,rows", [(13, None), (14, [0, 9, 15]), (15, [0, 15])])
 def test_delta_workloads(cid, rows):
     w = inputs.EXTRA_WORKLOADS[cid]
