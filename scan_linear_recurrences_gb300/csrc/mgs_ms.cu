@@ -304,6 +304,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C - 1, 0, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
+    const QuadOffsets<K> qo(sub, col);  // this thread's offsets in a staged box
     const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
     const int64_t nb = (len + TS - 1) / TS;
 
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(32)
         for (int u = 0; u < TS; ++u) {
             if (u < n) {
                 float nm[K];
-                tile_matvec(TileRef<K>{st, u, sub}, m, nm);
+                tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
 #pragma unroll
                 for (int i = 0; i < K; ++i) m[i] = nm[i];
             }
@@ -369,6 +370,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
+    const QuadOffsets<K> qo(sub, col);  // this thread's offsets in a staged box
     const bool active = it.head0 + sub < H;
     const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
     const int64_t nb = (len + TS - 1) / TS;
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(32)
         for (int u = 0; u < TS; ++u) {
             if (u < n) {
                 float nm[K];
-                tile_matvec(TileRef<K>{st, u, sub}, m, nm);
+                tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
 #pragma unroll
                 for (int i = 0; i < K; ++i) m[i] = nm[i];
                 if (active) {
@@ -442,6 +444,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C - 1, 1, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
+    const QuadOffsets<K> qo(sub, col);  // this thread's offsets in a staged box
     const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
     const int64_t nb = (len + TS - 1) / TS;
 
@@ -486,12 +489,11 @@ __global__ void __launch_bounds__(32)
         for (int u = 0; u < TS; ++u) {
             if (u < n) {
                 const int q = TS - 1 - u;
-                const TileRef<K> At{st, q, sub}, Gt{st + BOXF, q, sub};
+                const TileRefQ<K> At{st + q * S::MF, qo}, Gt{st + BOXF + q * S::MF, qo};
                 float lc[K], nm[K];
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
-                tile_matvec_t(At, lc, mu);
-                tile_matvec_t(At, mm, nm);
+                for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
+                tile_matvec_t2(At, lc, mm, mu, nm);
 #pragma unroll
                 for (int i = 0; i < K; ++i) mm[i] = nm[i];
             }
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C, 0, gpb, S::LPW);
     const int sub = lane / K, col = lane % K;
+    const QuadOffsets<K> qo(sub, col);  // this thread's offsets in a staged box
     const bool active = it.head0 + sub < H;
     const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
     const int64_t nb = (len + TS - 1) / TS;
@@ -572,10 +575,11 @@ __global__ void __launch_bounds__(32)
             if (u < n) {
                 const int64_t t = tt - u;
                 const int q = TS - 1 - u;
-                const TileRef<K> At{st, q, sub}, Gt{st + BOXF, q, sub}, Pp{st + 2 * BOXF, q, sub};
+                const TileRefQ<K> At{st + q * S::MF, qo}, Gt{st + BOXF + q * S::MF, qo},
+                    Pp{st + 2 * BOXF + q * S::MF, qo};
                 float lc[K];
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt.at(i, col) + mu[i];
+                for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
 #pragma unroll
                 for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
                 __syncwarp();

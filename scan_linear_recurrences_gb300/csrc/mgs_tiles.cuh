@@ -118,6 +118,46 @@ struct TileRef {
     }
 };
 
+// Per-thread offsets (floats, from the start of a box row) of the 16-byte
+// quads of lane sub's k x k block.  The swizzle's XOR depends only on the
+// lane and the quad, so it is computed once per thread instead of at every
+// load of a step.
+template <int K>
+struct QuadOffsets {
+    int o[K][(K + 3) / 4];
+    int oc[K];  // element (i, col) of the thread's own column
+    __device__ __forceinline__ QuadOffsets(int sub, int col) {
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+#pragma unroll
+            for (int c = 0; c < (K + 3) / 4; ++c) o[i][c] = MatTile<K>::idx4(0, sub, i, 4 * c);
+            oc[i] = MatTile<K>::idx1(0, sub, i, col);
+        }
+    }
+};
+
+// One lane's k x k block inside a staged box, addressed through QuadOffsets
+// (for k < 4 the box is unswizzled and a row is K consecutive floats).
+template <int K>
+struct TileRefQ {
+    const float *box;  // the box row of this step
+    const QuadOffsets<K> &q;
+    // element (i, col) of the thread's own column
+    __device__ __forceinline__ float at_col(int i) const { return box[q.oc[i]]; }
+    __device__ __forceinline__ void row(int i, float (&r)[K]) const {
+        if constexpr (K >= 4) {
+#pragma unroll
+            for (int c = 0; c < K / 4; ++c) {
+                const float4 v = *reinterpret_cast<const float4 *>(box + q.o[i][c]);
+                r[4 * c] = v.x; r[4 * c + 1] = v.y; r[4 * c + 2] = v.z; r[4 * c + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < K; ++c) r[c] = box[q.o[i][0] + c];
+        }
+    }
+};
+
 // y = M x for a staged block.
 template <int K, bool SWZ>
 __device__ __forceinline__ void tile_matvec(const TileRef<K, SWZ> &M, const float (&x)[K], float (&y)[K]) {
@@ -146,6 +186,89 @@ __device__ __forceinline__ void tile_matvec_t(const TileRef<K, SWZ> &M, const fl
         M.row(i, r);
 #pragma unroll
         for (int m = 0; m < K; ++m) y[m] = fmaf(r[m], x[i], y[m]);
+    }
+}
+
+// y = M x and y = M^T x through TileRefQ: the same arithmetic, in the same
+// order, as above, with the even- and odd-indexed accumulators of a row (M x)
+// or adjacent outputs (M^T x) paired in one two-wide FMA (sm_100 and later;
+// each half rounds as fmaf), so the results are identical.
+template <int K>
+__device__ __forceinline__ void tile_matvec(const TileRefQ<K> &M, const float (&x)[K], float (&y)[K]) {
+    if constexpr (K >= 2) {
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            float r[K];
+            M.row(i, r);
+            float2 s = make_float2(0.f, 0.f);  // (even m, odd m)
+#pragma unroll
+            for (int m = 0; m < K; m += 2)
+                s = __ffma2_rn(make_float2(r[m], r[m + 1]), make_float2(x[m], x[m + 1]), s);
+            y[i] = s.x + s.y;
+        }
+    } else {
+        float r[1];
+        M.row(0, r);
+        y[0] = fmaf(r[0], x[0], 0.f) + 0.f;
+    }
+}
+template <int K>
+__device__ __forceinline__ void tile_matvec_t(const TileRefQ<K> &M, const float (&x)[K], float (&y)[K]) {
+    if constexpr (K >= 2) {
+        float2 acc[K / 2];
+#pragma unroll
+        for (int m = 0; m < K / 2; ++m) acc[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            float r[K];
+            M.row(i, r);
+            const float2 xi = make_float2(x[i], x[i]);
+#pragma unroll
+            for (int m = 0; m < K; m += 2) acc[m / 2] = __ffma2_rn(make_float2(r[m], r[m + 1]), xi, acc[m / 2]);
+        }
+#pragma unroll
+        for (int m = 0; m < K; m += 2) {
+            y[m] = acc[m / 2].x;
+            y[m + 1] = acc[m / 2].y;
+        }
+    } else {
+        float r[1];
+        M.row(0, r);
+        y[0] = fmaf(r[0], x[0], 0.f);
+    }
+}
+
+// y1 = M^T x1 and y2 = M^T x2 in one pass over M's rows (each row read once;
+// per output the same arithmetic and order as two tile_matvec_t calls).
+template <int K>
+__device__ __forceinline__ void tile_matvec_t2(const TileRefQ<K> &M, const float (&x1)[K], const float (&x2)[K],
+                                               float (&y1)[K], float (&y2)[K]) {
+    if constexpr (K >= 2) {
+        float2 a1[K / 2], a2[K / 2];
+#pragma unroll
+        for (int m = 0; m < K / 2; ++m) a1[m] = a2[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            float r[K];
+            M.row(i, r);
+            const float2 u1 = make_float2(x1[i], x1[i]), u2 = make_float2(x2[i], x2[i]);
+#pragma unroll
+            for (int m = 0; m < K; m += 2) {
+                const float2 rm = make_float2(r[m], r[m + 1]);
+                a1[m / 2] = __ffma2_rn(rm, u1, a1[m / 2]);
+                a2[m / 2] = __ffma2_rn(rm, u2, a2[m / 2]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < K; m += 2) {
+            y1[m] = a1[m / 2].x;
+            y1[m + 1] = a1[m / 2].y;
+            y2[m] = a2[m / 2].x;
+            y2[m + 1] = a2[m / 2].y;
+        }
+    } else {
+        tile_matvec_t(M, x1, y1);
+        tile_matvec_t(M, x2, y2);
     }
 }
 
