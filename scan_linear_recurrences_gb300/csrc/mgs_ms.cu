@@ -333,13 +333,37 @@ __global__ void __launch_bounds__(32)
         }
         const int n = int(min64(TS, len - j * TS));
         const float *st = ring + size_t(s) * BOXF;
+        if constexpr (K <= 8) {
+            // A of step u + 1 is loaded while step u computes (rows past n are
+            // staged box rows too, loaded and not used)
+            float a[K][K];
+            tile_load(TileRefQ<K>{st, qo}, a);
 #pragma unroll
-        for (int u = 0; u < TS; ++u) {
-            if (u < n) {
-                float nm[K];
-                tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
+            for (int u = 0; u < TS; ++u) {
+                float an[K][K];
+                if (u + 1 < TS) tile_load(TileRefQ<K>{st + (u + 1) * S::MF, qo}, an);
+                if (u < n) {
+                    float nm[K];
+                    reg_matvec(a, m, nm);
 #pragma unroll
-                for (int i = 0; i < K; ++i) m[i] = nm[i];
+                    for (int i = 0; i < K; ++i) m[i] = nm[i];
+                }
+                if (u + 1 < TS) {
+#pragma unroll
+                    for (int i = 0; i < K; ++i)
+#pragma unroll
+                        for (int c = 0; c < K; ++c) a[i][c] = an[i][c];
+                }
+            }
+        } else {  // k = 16: the block does not fit in registers twice
+#pragma unroll
+            for (int u = 0; u < TS; ++u) {
+                if (u < n) {
+                    float nm[K];
+                    tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) m[i] = nm[i];
+                }
             }
         }
         __syncwarp();
@@ -402,17 +426,43 @@ __global__ void __launch_bounds__(32)
         const int64_t t0 = tb + j * TS;
         const int n = int(min64(TS, len - j * TS));
         const float *st = ring + size_t(s) * BOXF;
+        auto put = [&](int u) {
+            if (active) {
+                float *dst = pout + (t0 + u) * H * K * K;
 #pragma unroll
-        for (int u = 0; u < TS; ++u) {
-            if (u < n) {
-                float nm[K];
-                tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
+                for (int i = 0; i < K; ++i) st_cs(dst + i * K, m[i]);
+            }
+        };
+        if constexpr (K <= 8) {
+            float a[K][K];  // A of step u; step u + 1's is loaded while u computes
+            tile_load(TileRefQ<K>{st, qo}, a);
 #pragma unroll
-                for (int i = 0; i < K; ++i) m[i] = nm[i];
-                if (active) {
-                    float *dst = pout + (t0 + u) * H * K * K;
+            for (int u = 0; u < TS; ++u) {
+                float an[K][K];
+                if (u + 1 < TS) tile_load(TileRefQ<K>{st + (u + 1) * S::MF, qo}, an);
+                if (u < n) {
+                    float nm[K];
+                    reg_matvec(a, m, nm);
 #pragma unroll
-                    for (int i = 0; i < K; ++i) st_cs(dst + i * K, m[i]);
+                    for (int i = 0; i < K; ++i) m[i] = nm[i];
+                    put(u);
+                }
+                if (u + 1 < TS) {
+#pragma unroll
+                    for (int i = 0; i < K; ++i)
+#pragma unroll
+                        for (int c = 0; c < K; ++c) a[i][c] = an[i][c];
+                }
+            }
+        } else {  // k = 16: the block does not fit in registers twice
+#pragma unroll
+            for (int u = 0; u < TS; ++u) {
+                if (u < n) {
+                    float nm[K];
+                    tile_matvec(TileRefQ<K>{st + u * S::MF, qo}, m, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) m[i] = nm[i];
+                    put(u);
                 }
             }
         }
@@ -485,17 +535,51 @@ __global__ void __launch_bounds__(32)
         const int64_t tt = te - 1 - j * TS;
         const int n = int(min64(TS, tt - tb + 1));
         const float *st = ring + size_t(s) * 2 * BOXF;
+        if constexpr (K <= 8) {
+            // A and the G column of step u + 1 are loaded while step u computes
+            float a[K][K], gc[K];
+            tile_load(TileRefQ<K>{st + (TS - 1) * S::MF, qo}, a);
+    #pragma unroll
+            for (int i = 0; i < K; ++i) gc[i] = TileRefQ<K>{st + BOXF + (TS - 1) * S::MF, qo}.at_col(i);
+    #pragma unroll
+            for (int u = 0; u < TS; ++u) {
+                float an[K][K], gn[K];
+                if (u + 1 < TS) {
+                    const int q1 = TS - 2 - u;
+                    tile_load(TileRefQ<K>{st + q1 * S::MF, qo}, an);
+    #pragma unroll
+                    for (int i = 0; i < K; ++i) gn[i] = TileRefQ<K>{st + BOXF + q1 * S::MF, qo}.at_col(i);
+                }
+                if (u < n) {
+                    float lc[K], nm[K];
+    #pragma unroll
+                    for (int i = 0; i < K; ++i) lc[i] = gc[i] + mu[i];
+                    reg_matvec_t2(a, lc, mm, mu, nm);
+    #pragma unroll
+                    for (int i = 0; i < K; ++i) mm[i] = nm[i];
+                }
+                if (u + 1 < TS) {
+    #pragma unroll
+                    for (int i = 0; i < K; ++i) {
+                        gc[i] = gn[i];
+    #pragma unroll
+                        for (int c = 0; c < K; ++c) a[i][c] = an[i][c];
+                    }
+                }
+            }
+        } else {  // k = 16: the block does not fit in registers twice
 #pragma unroll
-        for (int u = 0; u < TS; ++u) {
-            if (u < n) {
-                const int q = TS - 1 - u;
-                const TileRefQ<K> At{st + q * S::MF, qo}, Gt{st + BOXF + q * S::MF, qo};
-                float lc[K], nm[K];
+            for (int u = 0; u < TS; ++u) {
+                if (u < n) {
+                    const int q = TS - 1 - u;
+                    const TileRefQ<K> At{st + q * S::MF, qo}, Gt{st + BOXF + q * S::MF, qo};
+                    float lc[K], nm[K];
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
-                tile_matvec_t2(At, lc, mm, mu, nm);
+                    for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
+                    tile_matvec_t2(At, lc, mm, mu, nm);
 #pragma unroll
-                for (int i = 0; i < K; ++i) mm[i] = nm[i];
+                    for (int i = 0; i < K; ++i) mm[i] = nm[i];
+                }
             }
         }
         __syncwarp();
@@ -577,22 +661,43 @@ __global__ void __launch_bounds__(32)
                 const int q = TS - 1 - u;
                 const TileRefQ<K> At{st + q * S::MF, qo}, Gt{st + BOXF + q * S::MF, qo},
                     Pp{st + 2 * BOXF + q * S::MF, qo};
-                float lc[K];
+                float lc[K], lrow[K], darow[K];
+                if constexpr (K <= 8) {
+                    // both blocks of the step into registers, every load issued
+                    // before any use (the P box row of t = 0 is loaded, not used)
+                    float a[K][K], pp[K][K];
+                    tile_load(At, a);
+                    tile_load(Pp, pp);
 #pragma unroll
-                for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
+                    for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
 #pragma unroll
-                for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
-                __syncwarp();
-                float lrow[K], darow[K];
+                    for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
+                    __syncwarp();
 #pragma unroll
-                for (int x = 0; x < K; ++x) lrow[x] = xw[col * K + x];
-                if (t >= 1) {
-                    tile_matvec(Pp, lrow, darow);  // dA[row][m] = sum_j L[row][j] P_{t-1}[m][j]
+                    for (int x = 0; x < K; ++x) lrow[x] = xw[col * K + x];
+                    if (t >= 1) {
+                        reg_matvec(pp, lrow, darow);  // dA[row][m] = sum_j L[row][j] P_{t-1}[m][j]
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < K; ++x) darow[x] = lrow[x];  // P_0 = I
+                    }
+                    reg_matvec_t(a, lc, mu);
                 } else {
 #pragma unroll
-                    for (int x = 0; x < K; ++x) darow[x] = lrow[x];  // P_0 = I
+                    for (int i = 0; i < K; ++i) lc[i] = Gt.at_col(i) + mu[i];
+#pragma unroll
+                    for (int i = 0; i < K; ++i) xw[i * K + col] = lc[i];
+                    __syncwarp();
+#pragma unroll
+                    for (int x = 0; x < K; ++x) lrow[x] = xw[col * K + x];
+                    if (t >= 1) {
+                        tile_matvec(Pp, lrow, darow);
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < K; ++x) darow[x] = lrow[x];
+                    }
+                    tile_matvec_t(At, lc, mu);
                 }
-                tile_matvec_t(At, lc, mu);
                 __syncwarp();
                 if (active) {
                     float *dst = dA + ((it.bi * T + t) * H + it.head0 + sub) * K * K + col * K;

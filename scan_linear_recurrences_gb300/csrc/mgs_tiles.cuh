@@ -189,6 +189,84 @@ __device__ __forceinline__ void tile_matvec_t(const TileRef<K, SWZ> &M, const fl
     }
 }
 
+// The whole k x k block of one step into registers, row-major (every load
+// issued before any use, so a step's latency is one shared-memory round trip).
+template <int K>
+__device__ __forceinline__ void tile_load(const TileRefQ<K> &M, float (&a)[K][K]) {
+#pragma unroll
+    for (int i = 0; i < K; ++i) M.row(i, a[i]);
+}
+
+// y = A x, y = A^T x, and two of the latter, from a block in registers: the
+// arithmetic and order of tile_matvec / tile_matvec_t below (the even and odd
+// partial sums of a row, or adjacent outputs, paired in one two-wide FMA that
+// rounds each half as fmaf; sm_100 and later).
+template <int K>
+__device__ __forceinline__ void reg_matvec(const float (&a)[K][K], const float (&x)[K], float (&y)[K]) {
+    if constexpr (K >= 2) {
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            float2 s = make_float2(0.f, 0.f);  // (even m, odd m)
+#pragma unroll
+            for (int m = 0; m < K; m += 2)
+                s = __ffma2_rn(make_float2(a[i][m], a[i][m + 1]), make_float2(x[m], x[m + 1]), s);
+            y[i] = s.x + s.y;
+        }
+    } else {
+        y[0] = fmaf(a[0][0], x[0], 0.f) + 0.f;
+    }
+}
+template <int K>
+__device__ __forceinline__ void reg_matvec_t(const float (&a)[K][K], const float (&x)[K], float (&y)[K]) {
+    if constexpr (K >= 2) {
+        float2 acc[K / 2];
+#pragma unroll
+        for (int m = 0; m < K / 2; ++m) acc[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const float2 xi = make_float2(x[i], x[i]);
+#pragma unroll
+            for (int m = 0; m < K; m += 2) acc[m / 2] = __ffma2_rn(make_float2(a[i][m], a[i][m + 1]), xi, acc[m / 2]);
+        }
+#pragma unroll
+        for (int m = 0; m < K; m += 2) {
+            y[m] = acc[m / 2].x;
+            y[m + 1] = acc[m / 2].y;
+        }
+    } else {
+        y[0] = fmaf(a[0][0], x[0], 0.f);
+    }
+}
+template <int K>
+__device__ __forceinline__ void reg_matvec_t2(const float (&a)[K][K], const float (&x1)[K], const float (&x2)[K],
+                                              float (&y1)[K], float (&y2)[K]) {
+    if constexpr (K >= 2) {
+        float2 a1[K / 2], a2[K / 2];
+#pragma unroll
+        for (int m = 0; m < K / 2; ++m) a1[m] = a2[m] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            const float2 u1 = make_float2(x1[i], x1[i]), u2 = make_float2(x2[i], x2[i]);
+#pragma unroll
+            for (int m = 0; m < K; m += 2) {
+                const float2 rm = make_float2(a[i][m], a[i][m + 1]);
+                a1[m / 2] = __ffma2_rn(rm, u1, a1[m / 2]);
+                a2[m / 2] = __ffma2_rn(rm, u2, a2[m / 2]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < K; m += 2) {
+            y1[m] = a1[m / 2].x;
+            y1[m + 1] = a1[m / 2].y;
+            y2[m] = a2[m / 2].x;
+            y2[m + 1] = a2[m / 2].y;
+        }
+    } else {
+        y1[0] = fmaf(a[0][0], x1[0], 0.f);
+        y2[0] = fmaf(a[0][0], x2[0], 0.f);
+    }
+}
+
 // y = M x and y = M^T x through TileRefQ: the same arithmetic, in the same
 // order, as above, with the even- and odd-indexed accumulators of a row (M x)
 // or adjacent outputs (M^T x) paired in one two-wide FMA (sm_100 and later;
