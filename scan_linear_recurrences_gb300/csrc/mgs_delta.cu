@@ -93,9 +93,9 @@ constexpr uint32_t kWyD = 0, kWyAB = 128, kWyAS = 192, kWyCols = 256;
 
 // Shared memory of delta_state_kernel<NI>: NS stages of [R; M] (two swizzled
 // panels of 128 rows) and the block's rows of O_c^T and N^T (NI x 64 each,
-// swizzled, panels of NI rows); the B operand S as [S residuals; S] rows (two panels of 2 NI rows);
-// then full[NS], empty[NS], the product barrier, the TMEM address and the
-// abort word.
+// swizzled, panels of NI rows); the B operand S as [S residuals; S] rows (two
+// panels of 2 NI rows); then full[NS], empty[NS], the product barrier, the
+// TMEM address and the abort word.
 template <int NI>
 struct StLayout {
     static constexpr int NS = NI == 64 ? 3 : NI == 32 ? 4 : 5;
