@@ -247,6 +247,9 @@ __global__ void __launch_bounds__(kWyThreads, 2)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the state pass may be scheduled as soon as every block of this one has
+    // started (it waits for this grid's completion before reading its output)
+    pdl_trigger();
     const uint32_t tm = *slot;
     const uint32_t tq = tm + (uint32_t(32 * q4) << 16);
     if (tid == 0) {
@@ -640,6 +643,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
             const uint64_t pol = policy_evict_normal();
             prefetch_tmap(&tmA);
             prefetch_tmap(&tmS);
+            // launched as a programmatic dependent of the WY pass: its output is
+            // complete and visible after this wait
+            pdl_wait();
             int64_t last = -1;
             for (int64_t c = 0; c < nch; ++c) {
                 const int s = int(c % NS);
@@ -810,8 +816,19 @@ cudaError_t launch_state(float *w, int64_t chunks, const float *S0, float *o, fl
     if ((e = make_ws_map(&tS, w, chunks * WS_ROWS, 32, NI, true)) != cudaSuccess) return e;
     const int smem = int(StLayout<NI>::bytes);
     if ((e = ensure_smem_attr((const void *)delta_state_kernel<NI>, smem)) != cudaSuccess) return e;
-    delta_state_kernel<NI><<<dim3(unsigned(B * H * NVB)), kStateThreads, smem, s>>>(tA, tS, S0, o, ST, B, T, H, ctl);
-    return cudaGetLastError();
+    // programmatic dependent launch: the blocks set up (barriers, TMEM, the
+    // initial state) while the WY pass finishes; the copy warp waits for it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B * H * NVB));
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, delta_state_kernel<NI>, tA, tS, S0, o, ST, B, T, H, ctl);
 }
 
 }  // namespace
