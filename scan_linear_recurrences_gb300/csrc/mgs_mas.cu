@@ -649,6 +649,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C - 1, 0, gpb, S::LPW);
     const int sub = lane / K, r = lane % K, gbase = lane & ~(K - 1);
+    const QuadOffsets<K> qo(sub, r);  // this thread's offsets in a staged box
     const int64_t tb = it.c * Lc, len = min64(Lc, T - tb);
     const int64_t nb = (len + S::TS - 1) / S::TS;
 
@@ -684,24 +685,61 @@ __global__ void __launch_bounds__(32)
         }
         const int n = int(min64(S::TS, len - j * S::TS));
         const float *st = ring + size_t(s) * SSTR;
+        // one step: c <- A c + b (row r, from the group's shuffled c) and the
+        // column of M <- A M from the step's block in registers
+        auto step = [&](const float (&ablk)[K][K], int u) {
+            float a[K];
+            TileRef<K>{st, u, sub}.row(r, a);
+            float acc0 = st[A_STAGE + u * S::VF + sub * K + r], acc1 = 0.f;
 #pragma unroll
-        for (int u = 0; u < S::TS; ++u) {
-            if (u < n) {
-                const TileRef<K> Ablk{st, u, sub};
-                float a[K];
-                Ablk.row(r, a);
-                float acc0 = st[A_STAGE + u * S::VF + sub * K + r], acc1 = 0.f;
+            for (int jj = 0; jj < K; ++jj) {
+                const float x = __shfl_sync(0xffffffffu, cv, gbase + jj);
+                if (jj & 1) acc1 = fmaf(a[jj], x, acc1);
+                else acc0 = fmaf(a[jj], x, acc0);
+            }
+            cv = acc0 + acc1;
+            float nm[K];
+            reg_matvec(ablk, mcol, nm);
 #pragma unroll
-                for (int jj = 0; jj < K; ++jj) {
-                    const float x = __shfl_sync(0xffffffffu, cv, gbase + jj);
-                    if (jj & 1) acc1 = fmaf(a[jj], x, acc1);
-                    else acc0 = fmaf(a[jj], x, acc0);
+            for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+        };
+        if constexpr (K >= 4 && K <= 8) {
+            // step u + 1's block is loaded while step u computes (rows past n
+            // are staged box rows too, loaded and not used)
+            float ab[K][K];
+            tile_load(TileRefQ<K>{st, qo}, ab);
+#pragma unroll
+            for (int u = 0; u < S::TS; ++u) {
+                float an[K][K];
+                if (u + 1 < S::TS) tile_load(TileRefQ<K>{st + (u + 1) * S::AF, qo}, an);
+                if (u < n) step(ab, u);
+                if (u + 1 < S::TS) {
+#pragma unroll
+                    for (int i = 0; i < K; ++i)
+#pragma unroll
+                        for (int c = 0; c < K; ++c) ab[i][c] = an[i][c];
                 }
-                cv = acc0 + acc1;
-                float nm[K];
-                tile_matvec(Ablk, mcol, nm);
+            }
+        } else {
 #pragma unroll
-                for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+            for (int u = 0; u < S::TS; ++u) {
+                if (u < n) {
+                    const TileRef<K> Ablk{st, u, sub};
+                    float a[K];
+                    Ablk.row(r, a);
+                    float acc0 = st[A_STAGE + u * S::VF + sub * K + r], acc1 = 0.f;
+#pragma unroll
+                    for (int jj = 0; jj < K; ++jj) {
+                        const float x = __shfl_sync(0xffffffffu, cv, gbase + jj);
+                        if (jj & 1) acc1 = fmaf(a[jj], x, acc1);
+                        else acc0 = fmaf(a[jj], x, acc0);
+                    }
+                    cv = acc0 + acc1;
+                    float nm[K];
+                    tile_matvec(Ablk, mcol, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+                }
             }
         }
         __syncwarp();
@@ -819,6 +857,7 @@ __global__ void __launch_bounds__(32)
     const int lane = threadIdx.x;
     const ChunkItem it(blockIdx.x, C - 1, 1, gpb, S::LPW);
     const int sub = lane / K, r = lane % K;
+    const QuadOffsets<K> qo(sub, r);  // this thread's offsets in a staged box
     const int64_t tb = it.c * Lc, te = min64(T, tb + Lc), len = te - tb;
     const int64_t nb = (len + S::TS - 1) / S::TS;
 
@@ -857,20 +896,50 @@ __global__ void __launch_bounds__(32)
         const int64_t tt = te - 1 - j * S::TS;
         const int n = int(min64(S::TS, tt - tb + 1));
         const float *st = ring + size_t(s) * SSTR;
+        // one step (box row q): mu <- A^T (g + mu) by the group's reduce-scatter,
+        // and the column of M <- A^T M from the step's block in registers
+        auto bstep = [&](const float (&ablk)[K][K], int q) {
+            const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
+            float a[K], p[K], nm[K];
+            TileRef<K>{st, q, sub}.row(r, a);
 #pragma unroll
-        for (int u = 0; u < S::TS; ++u) {
-            if (u < n) {
-                const int q = S::TS - 1 - u;
-                const TileRef<K> Ablk{st, q, sub};
-                const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
-                float a[K], p[K], nm[K];
-                Ablk.row(r, a);
+            for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
+            mu = group_reduce_scatter<K>(p, r);
+            reg_matvec_t(ablk, mcol, nm);
 #pragma unroll
-                for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
-                mu = group_reduce_scatter<K>(p, r);
-                tile_matvec_t(Ablk, mcol, nm);
+            for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+        };
+        if constexpr (K >= 4 && K <= 8) {
+            float ab[K][K];
+            tile_load(TileRefQ<K>{st + (S::TS - 1) * S::AF, qo}, ab);
 #pragma unroll
-                for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+            for (int u = 0; u < S::TS; ++u) {
+                float an[K][K];
+                if (u + 1 < S::TS) tile_load(TileRefQ<K>{st + (S::TS - 2 - u) * S::AF, qo}, an);
+                if (u < n) bstep(ab, S::TS - 1 - u);
+                if (u + 1 < S::TS) {
+#pragma unroll
+                    for (int i = 0; i < K; ++i)
+#pragma unroll
+                        for (int c = 0; c < K; ++c) ab[i][c] = an[i][c];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < S::TS; ++u) {
+                if (u < n) {
+                    const int q = S::TS - 1 - u;
+                    const TileRef<K> Ablk{st, q, sub};
+                    const float lam = st[A_STAGE + q * S::VF + sub * K + r] + mu;
+                    float a[K], p[K], nm[K];
+                    Ablk.row(r, a);
+#pragma unroll
+                    for (int x = 0; x < K; ++x) p[x] = a[x] * lam;
+                    mu = group_reduce_scatter<K>(p, r);
+                    tile_matvec_t(Ablk, mcol, nm);
+#pragma unroll
+                    for (int i = 0; i < K; ++i) mcol[i] = nm[i];
+                }
             }
         }
         __syncwarp();
