@@ -226,7 +226,10 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
  *     h_t = a_t * h_{t-1} + b_t,   h_0 = h0 (zeros when NULL),
  * with signed coefficients allowed (the negative-eigenvalue gates of
  * SignedMinGRU, home page lineage paragraph).  It is matrix_affine_scan with
- * k = 1 and H = D, and runs on those kernels.
+ * k = 1 and H = D and validates as that op; T <= 1024 with fewer than 2048
+ * groups of 32 channels (B * ceil(D / 32)) runs as one time-parallel launch
+ * on thread-block clusters that uses no workspace, other shapes on the
+ * matrix_affine_scan kernels.  The workspace size is that op's either way.
  * In: a, b [B][T][D], h0 [B][D] (nullable).  Out: h [B][T][D].  D must be a
  * multiple of 4.  Workspace: mgs_workspace_size(MGS_OP_LINEAR_SCAN_FWD, ...). */
 mgs_status mgs_linear_scan_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B,

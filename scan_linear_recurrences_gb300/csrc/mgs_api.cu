@@ -282,6 +282,8 @@ mgs_status mgs_matrix_affine_scan_fwd(const float *A, const float *b, const floa
     if ((st = check_ws(mgs::mas_workspace_bytes(B, T, H, k), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    if (k == 1 && mgs::lin_supported(B, T, H))
+        return from_cuda(mgs::launch_lin_fwd(A, b, h0, h, B, T, H, reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(mgs::launch_mas_fwd(k, A, b, h0, h, B, T, H, workspace, workspace_bytes, ctl,
                                          reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -308,6 +310,9 @@ mgs_status mgs_matrix_affine_scan_bwd(const float *A, const float *h0, const flo
     if ((st = check_ws(mgs::mas_workspace_bytes(B, T, H, k), workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    if (k == 1 && mgs::lin_supported(B, T, H))
+        return from_cuda(mgs::launch_lin_bwd(A, h0, h, grad_h, dA, db, dh0, B, T, H,
+                                             reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(mgs::launch_mas_bwd(k, A, h0, h, grad_h, dA, db, dh0, B, T, H, workspace, workspace_bytes,
                                          ctl, reinterpret_cast<cudaStream_t>(stream)));
 }

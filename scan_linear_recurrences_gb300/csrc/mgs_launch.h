@@ -26,6 +26,14 @@ cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, cons
                                      float *dA, float *db, float *dh0, int64_t B, int64_t T, int64_t H, void *ws,
                                      const DevCtl &ctl, cudaStream_t s);
 
+// linear_scan (matrix_affine_scan with k = 1), time-parallel in one launch
+// for few channel groups and T <= 1024; no workspace.  h0 and dh0 may be null.
+bool lin_supported(int64_t B, int64_t T, int64_t D);
+cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
+                           int64_t D, cudaStream_t s);
+cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
+                           float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
+
 // matrix_scan
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);
 cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,

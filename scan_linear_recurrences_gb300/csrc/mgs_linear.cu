@@ -1,0 +1,236 @@
+// The diagonal linear recurrence (matrix_affine_scan with k = 1, which
+// linear_scan is; "mingru-scans" home page, scan-op table, linear_scan row)
+// scanned in parallel over time in one launch:
+//   h_t = a_t h_{t-1} + b_t                     (forward)
+//   lambda_t = g_t + a_{t+1} lambda_{t+1}       (backward; db_t = lambda_t,
+//   da_t = lambda_t h_{t-1}, dh0 = a_0 lambda_0)
+// One thread-block cluster of S CTAs owns 32 channels of one batch row
+// (thread = channel, so every load and store of a warp is 128 contiguous
+// bytes); CTA r holds the r-th segment of W*L steps and each of its W warps L
+// consecutive steps, with their inputs in registers (read once).  A warp
+// composes its steps into one affine map (x_end = m x_start + c), warp 0
+// composes the warps' maps into each warp's offset within the CTA and the
+// CTA's total, and after a cluster barrier every CTA applies the totals of
+// the CTAs before it (read from their shared memory) to h0 to get the state
+// entering its segment.  Each warp then walks its steps from its own entry
+// state.  No workspace; T <= S W L.
+#include "mgs_launch.h"
+#include "mgs_device.cuh"
+
+namespace mgs {
+namespace {
+
+constexpr int kLinWarps = 8;   // W
+constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
+constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;
+
+__device__ __forceinline__ unsigned cluster_rank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the float at address p in the shared memory of the cluster's CTA `rank`
+__device__ __forceinline__ float ld_dsmem(const float *p, unsigned rank) {
+    const unsigned local = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    unsigned remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+struct LinSmem {
+    float m[kLinWarps][32], c[kLinWarps][32];    // each warp's map
+    float pm[kLinWarps][32], pc[kLinWarps][32];  // each warp's offset within the CTA
+    float tm[32], tc[32];                        // the CTA's total map
+};
+
+// Warp 0: the warps' offsets within the CTA (in scan order: forward from warp
+// 0, backward from warp W-1) and the CTA's total.
+template <bool kRev>
+__device__ __forceinline__ void lin_cta_offsets(LinSmem &s, int lane) {
+    float pm = 1.f, pc = 0.f;
+    for (int i = 0; i < kLinWarps; ++i) {
+        const int k = kRev ? kLinWarps - 1 - i : i;
+        s.pm[k][lane] = pm;
+        s.pc[k][lane] = pc;
+        pc = fmaf(s.m[k][lane], pc, s.c[k][lane]);
+        pm *= s.m[k][lane];
+    }
+    s.tm[lane] = pm;
+    s.tc[lane] = pc;
+}
+
+// Steps of this warp inside [0, T) (none for a channel past D).
+__device__ __forceinline__ int lin_steps_here(bool act, int L, int64_t t0, int64_t T) {
+    return (!act || t0 >= T) ? 0 : int(min64(L, T - t0));
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps)
+    lin_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ h0,
+                   float *__restrict__ h, int64_t T, int64_t D, int64_t groups, int S) {
+    __shared__ LinSmem sm;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned r = cluster_rank();
+    const int64_t lg = blockIdx.x / S, bi = lg / groups;
+    const int64_t ch = (lg - bi * groups) * 32 + lane;
+    const bool act = ch < D;
+    const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
+    const int n = lin_steps_here(act, L, t0, T);
+    const int64_t base = (bi * T + t0) * D + ch;
+    float av[L], bv[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        av[u] = u < n ? a[base + u * D] : 1.f;
+        bv[u] = u < n ? b[base + u * D] : 0.f;
+    }
+    float m = 1.f, c = 0.f;
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        c = fmaf(av[u], c, bv[u]);
+        m *= av[u];
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<false>(sm, lane);
+    cluster_arrive();
+    cluster_wait();
+    // the state entering this CTA's segment: h0 through the CTAs before it
+    float x = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;
+    for (unsigned q = 0; q < r; ++q) x = fmaf(ld_dsmem(&sm.tm[lane], q), x, ld_dsmem(&sm.tc[lane], q));
+    cluster_arrive();  // done reading the other CTAs' shared memory
+    x = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        x = fmaf(av[u], x, bv[u]);
+        if (u < n) __stcs(h + base + u * D, x);
+    }
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps)
+    lin_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0, const float *__restrict__ h,
+                   const float *__restrict__ g, float *__restrict__ da, float *__restrict__ db,
+                   float *__restrict__ dh0, int64_t T, int64_t D, int64_t groups, int S) {
+    __shared__ LinSmem sm;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned r = cluster_rank();
+    const int64_t lg = blockIdx.x / S, bi = lg / groups;
+    const int64_t ch = (lg - bi * groups) * 32 + lane;
+    const bool act = ch < D;
+    const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
+    const int n = lin_steps_here(act, L, t0, T);
+    const int64_t base = (bi * T + t0) * D + ch;
+    const float hinit = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;
+    // step t's coefficient is a_{t+1} (none past the end: lambda_T = 0), and
+    // da_t needs h_{t-1} (h0, or zero, before the first step); steps past n
+    // are the identity
+    float an[L], gv[L], hp[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        an[u] = u < n ? (t0 + u + 1 < T ? a[base + (u + 1) * D] : 0.f) : 1.f;
+        gv[u] = u < n ? g[base + u * D] : 0.f;
+        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * D] : hinit) : 0.f;
+    }
+    float m = 1.f, c = 0.f;
+#pragma unroll
+    for (int u = L - 1; u >= 0; --u) {
+        c = fmaf(an[u], c, gv[u]);
+        m *= an[u];
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<true>(sm, lane);
+    cluster_arrive();
+    cluster_wait();
+    // lambda leaving this CTA's segment: zero past the end through the CTAs after it
+    float x = 0.f;
+    for (int q = S - 1; q > int(r); --q)
+        x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(q)), x, ld_dsmem(&sm.tc[lane], unsigned(q)));
+    cluster_arrive();
+    float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+#pragma unroll
+    for (int u = L - 1; u >= 0; --u) {
+        lam = fmaf(an[u], lam, gv[u]);
+        if (u < n) {
+            __stcs(db + base + u * D, lam);
+            __stcs(da + base + u * D, lam * hp[u]);
+        }
+    }
+    // lam is lambda_0 in the first warp of the first CTA
+    if (r == 0 && w == 0 && act && dh0 != nullptr) dh0[bi * D + ch] = a[bi * T * D + ch] * lam;
+    cluster_wait();
+}
+
+struct LinPlan {
+    int L, S;
+};
+// L = 8 steps a warp up to T = 512, 16 above; as many CTAs as the segments need.
+LinPlan lin_plan(int64_t T) {
+    LinPlan p;
+    p.L = T <= int64_t(8) * kLinWarps * kLinMaxCta ? 8 : 16;
+    p.S = int((T + int64_t(p.L) * kLinWarps - 1) / (int64_t(p.L) * kLinWarps));
+    return p;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t lin_launch(void (*kern)(KArgs...), int64_t blocks, int S, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(blocks));
+    cfg.blockDim = dim3(32 * kLinWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = unsigned(S);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, KArgs(args)...);
+}
+
+}  // namespace
+
+// Few channel groups (under 2048 warps of channels, where one thread walking
+// a channel's whole sequence leaves the GPU latency-bound) and T <= 1024.
+bool lin_supported(int64_t B, int64_t T, int64_t D) {
+    return T >= 1 && T <= kLinMaxT && B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048;
+}
+
+cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
+                           int64_t D, cudaStream_t s) {
+    const int64_t groups = (D + 31) / 32;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    const LinPlan p = lin_plan(T);
+    const int64_t blocks = B * groups * p.S;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
+    if (p.L == 8) return lin_launch(lin_fwd_kernel<8>, blocks, p.S, s, a, b, h0, h, T, D, groups, p.S);
+    return lin_launch(lin_fwd_kernel<16>, blocks, p.S, s, a, b, h0, h, T, D, groups, p.S);
+}
+
+cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
+                           float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
+    const int64_t groups = (D + 31) / 32;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    const LinPlan p = lin_plan(T);
+    const int64_t blocks = B * groups * p.S;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
+    if (p.L == 8)
+        return lin_launch(lin_bwd_kernel<8>, blocks, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
+    return lin_launch(lin_bwd_kernel<16>, blocks, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
+}
+
+}  // namespace mgs

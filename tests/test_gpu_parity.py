@@ -379,6 +379,10 @@ def test_psl_recompute_autograd_and_T0():
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 77, 132, True), (2, 300, 64, True), (1, 2000, 32, False), (4, 500, 1024, True),
     (16, 1024, 64, True), (128, 64, 64, True),
+    # edges of the one-launch time-parallel path: 8 -> 32 steps a warp past
+    # T = 256, sequential past T = 1024, and past 2048 channel groups
+    (3, 256, 36, True), (2, 257, 20, False), (1, 1024, 8, False), (1, 1025, 8, True),
+    (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_linear_scan(B, T, D, h0):
     d = _cuda(inputs.linear_inputs(B, T, D, seed=500 + B * T + D, with_h0=h0))
