@@ -270,6 +270,26 @@ def givens_peak_memory(torch, api, device, B=128, T=64, H=8, k=8):
 BASE_SEED_GIVENS_MEMORY = 20261202 + 99
 
 
+def copy_floor_us(torch, flush, stream, nbytes, reps):
+    """Median microseconds of a plain device copy moving `nbytes` (half read,
+    half written), timed as the L2-resident shapes' calls are: L2 flushed,
+    then CUDA events around the one call.  The floor those calls' times sit
+    on: launch, the first HBM round trip and the bytes."""
+    src = torch.empty(max(1, nbytes // 8), dtype=torch.float32, device=flush.device)
+    dst = torch.empty_like(src)
+    evs = []
+    for i in range(reps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dst.copy_(src)
+        e1.record(stream)
+        if i >= 3:
+            evs.append((e0, e1))
+    torch.cuda.synchronize()
+    return round(statistics.median(x.elapsed_time(y) for x, y in evs) * 1e3, 2)
+
+
 def delta_flops(w, C=64):
     """Floating-point operations of the chunked WY forward per call: per
     64-step chunk the products K K^T, Q K^T, the forward substitution for
@@ -547,6 +567,10 @@ def run_gpu(args):
             "fwd_bwd_pct_of_peak": round(100 * (fb + bb_) / ((fm + bm) * 1e-3) / 1e9 / peak, 1),
             "l2": "flushed" if small[w.cid] else "inputs larger than L2",
         }
+        if small[w.cid]:
+            # a plain copy of the same bytes, timed the same way (not part of the step)
+            ops[key]["same_bytes_copy_us"] = [copy_floor_us(torch, flush, stream, fb, args.steps),
+                                              copy_floor_us(torch, flush, stream, bb_, args.steps)]
         for direction, tms, nbytes in (("fwd", statistics.mean(f), fb), ("bwd", statistics.mean(bw), bb_)):
             if dominant is None or tms > dominant[1]:
                 dominant = (f"{w.op}_{direction}_c{w.cid}", tms, nbytes, w, direction)

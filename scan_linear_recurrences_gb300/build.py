@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmgscan.so")
 SOURCES = ["mgs_api.cu", "mgs_mas.cu", "mgs_ms.cu", "mgs_psl.cu", "mgs_givens.cu", "mgs_delta.cu", "mgs_linear.cu"]
-HEADERS = ["mgs_device.cuh", "mgs_launch.h", "mgs_tiles.cuh", "mgs_chunk.cuh", "mgs_ffsincos.cuh", "mgs_umma.cuh"]
+HEADERS = ["mgs_device.cuh", "mgs_launch.h", "mgs_tiles.cuh", "mgs_chunk.cuh", "mgs_ffsincos.cuh", "mgs_umma.cuh", "mgs_cluster.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", os.path.join(ROOT, "include")]

@@ -16,6 +16,7 @@
 // state.  No workspace; T <= S W L.
 #include "mgs_launch.h"
 #include "mgs_device.cuh"
+#include "mgs_cluster.cuh"
 
 namespace mgs {
 namespace {
@@ -23,27 +24,6 @@ namespace {
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
 constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;
-
-__device__ __forceinline__ unsigned cluster_rank() {
-    unsigned r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// the float at address p in the shared memory of the cluster's CTA `rank`
-__device__ __forceinline__ float ld_dsmem(const float *p, unsigned rank) {
-    const unsigned local = static_cast<unsigned>(__cvta_generic_to_shared(p));
-    unsigned remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
 
 struct LinSmem {
     float m[kLinWarps][32], c[kLinWarps][32];    // each warp's map
@@ -183,23 +163,6 @@ LinPlan lin_plan(int64_t T) {
     return p;
 }
 
-template <typename... KArgs, typename... Args>
-cudaError_t lin_launch(void (*kern)(KArgs...), int64_t blocks, int S, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(blocks));
-    cfg.blockDim = dim3(32 * kLinWarps);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = unsigned(S);
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, KArgs(args)...);
-}
-
 }  // namespace
 
 // Few channel groups (under 2048 warps of channels, where one thread walking
@@ -216,8 +179,8 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (blocks == 0) return cudaSuccess;
-    if (p.L == 8) return lin_launch(lin_fwd_kernel<8>, blocks, p.S, s, a, b, h0, h, T, D, groups, p.S);
-    return lin_launch(lin_fwd_kernel<16>, blocks, p.S, s, a, b, h0, h, T, D, groups, p.S);
+    if (p.L == 8) return launch_cluster(lin_fwd_kernel<8>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S);
+    return launch_cluster(lin_fwd_kernel<16>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S);
 }
 
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
@@ -229,8 +192,8 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (blocks == 0) return cudaSuccess;
     if (p.L == 8)
-        return lin_launch(lin_bwd_kernel<8>, blocks, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
-    return lin_launch(lin_bwd_kernel<16>, blocks, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
+        return launch_cluster(lin_bwd_kernel<8>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
+    return launch_cluster(lin_bwd_kernel<16>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
 }
 
 }  // namespace mgs

@@ -201,6 +201,8 @@ def test_ms_config2_full():
     (1, 1, 1, 8), (2, 13, 5, 8), (2, 21, 3, 4), (2, 17, 3, 16), (1, 40, 2, 2), (2, 30, 8, 1),
     # long sequences with few lanes take the time-chunked path
     (1, 333, 2, 8), (2, 1000, 3, 4), (1, 515, 3, 16), (1, 257, 4, 1), (1, 130, 2, 2), (3, 4099, 5, 8),
+    # 32 chunks with a ragged last one, and 33 chunks
+    (1, 1019, 3, 8), (1, 1056, 4, 8),
 ])
 def test_ms_shapes(B, T, H, k):
     _run_ms(B, T, H, k, seed=200 + B * T + H + k)
