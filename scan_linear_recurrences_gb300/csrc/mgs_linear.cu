@@ -47,18 +47,42 @@ __device__ __forceinline__ void lin_cta_offsets(LinSmem &s, int lane) {
     s.tc[lane] = pc;
 }
 
+// The two synchronisations of the kernels.  With one CTA (no cluster) the
+// first is a block barrier and the second is not needed.  Otherwise the first
+// is a full cluster barrier (release: warp 0's totals become visible to the
+// other CTAs), and the second is split: arrive (relaxed: the DSMEM loads have
+// completed, their values are used before it) once this CTA has read the
+// others' totals, wait just before exit.
+template <bool kCl>
+__device__ __forceinline__ void lin_sync1() {
+    if constexpr (kCl) {
+        cluster_arrive();
+        cluster_wait();
+    } else {
+        __syncthreads();
+    }
+}
+template <bool kCl>
+__device__ __forceinline__ void lin_arrive2() {
+    if constexpr (kCl) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+template <bool kCl>
+__device__ __forceinline__ void lin_wait2() {
+    if constexpr (kCl) cluster_wait();
+}
+
 // Steps of this warp inside [0, T) (none for a channel past D).
 __device__ __forceinline__ int lin_steps_here(bool act, int L, int64_t t0, int64_t T) {
     return (!act || t0 >= T) ? 0 : int(min64(L, T - t0));
 }
 
-template <int L>
+template <int L, bool kCl>
 __global__ void __launch_bounds__(32 * kLinWarps)
     lin_fwd_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ h0,
                    float *__restrict__ h, int64_t T, int64_t D, int64_t groups, int S) {
     __shared__ LinSmem sm;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned r = cluster_rank();
+    const unsigned r = kCl ? cluster_rank() : 0u;
     const int64_t lg = blockIdx.x / S, bi = lg / groups;
     const int64_t ch = (lg - bi * groups) * 32 + lane;
     const bool act = ch < D;
@@ -81,29 +105,29 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     sm.c[w][lane] = c;
     __syncthreads();
     if (w == 0) lin_cta_offsets<false>(sm, lane);
-    cluster_arrive();
-    cluster_wait();
+    lin_sync1<kCl>();
     // the state entering this CTA's segment: h0 through the CTAs before it
     float x = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;
-    for (unsigned q = 0; q < r; ++q) x = fmaf(ld_dsmem(&sm.tm[lane], q), x, ld_dsmem(&sm.tc[lane], q));
-    cluster_arrive();  // done reading the other CTAs' shared memory
+    if constexpr (kCl)
+        for (unsigned q = 0; q < r; ++q) x = fmaf(ld_dsmem(&sm.tm[lane], q), x, ld_dsmem(&sm.tc[lane], q));
+    lin_arrive2<kCl>();  // done reading the other CTAs' shared memory
     x = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
 #pragma unroll
     for (int u = 0; u < L; ++u) {
         x = fmaf(av[u], x, bv[u]);
         if (u < n) __stcs(h + base + u * D, x);
     }
-    cluster_wait();  // no CTA leaves while another may still read its shared memory
+    lin_wait2<kCl>();  // no CTA leaves while another may still read its shared memory
 }
 
-template <int L>
+template <int L, bool kCl>
 __global__ void __launch_bounds__(32 * kLinWarps)
     lin_bwd_kernel(const float *__restrict__ a, const float *__restrict__ h0, const float *__restrict__ h,
                    const float *__restrict__ g, float *__restrict__ da, float *__restrict__ db,
                    float *__restrict__ dh0, int64_t T, int64_t D, int64_t groups, int S) {
     __shared__ LinSmem sm;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned r = cluster_rank();
+    const unsigned r = kCl ? cluster_rank() : 0u;
     const int64_t lg = blockIdx.x / S, bi = lg / groups;
     const int64_t ch = (lg - bi * groups) * 32 + lane;
     const bool act = ch < D;
@@ -131,13 +155,13 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     sm.c[w][lane] = c;
     __syncthreads();
     if (w == 0) lin_cta_offsets<true>(sm, lane);
-    cluster_arrive();
-    cluster_wait();
+    lin_sync1<kCl>();
     // lambda leaving this CTA's segment: zero past the end through the CTAs after it
     float x = 0.f;
-    for (int q = S - 1; q > int(r); --q)
-        x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(q)), x, ld_dsmem(&sm.tc[lane], unsigned(q)));
-    cluster_arrive();
+    if constexpr (kCl)
+        for (int q = S - 1; q > int(r); --q)
+            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(q)), x, ld_dsmem(&sm.tc[lane], unsigned(q)));
+    lin_arrive2<kCl>();
     float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
 #pragma unroll
     for (int u = L - 1; u >= 0; --u) {
@@ -149,7 +173,7 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     }
     // lam is lambda_0 in the first warp of the first CTA
     if (r == 0 && w == 0 && act && dh0 != nullptr) dh0[bi * D + ch] = a[bi * T * D + ch] * lam;
-    cluster_wait();
+    lin_wait2<kCl>();
 }
 
 struct LinPlan {
@@ -179,8 +203,11 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (blocks == 0) return cudaSuccess;
-    if (p.L == 8) return launch_cluster(lin_fwd_kernel<8>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S);
-    return launch_cluster(lin_fwd_kernel<16>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S);
+#define LIN_FWD(L_, CL_) \
+    launch_cluster(lin_fwd_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S)
+    if (p.S == 1) return p.L == 8 ? LIN_FWD(8, false) : LIN_FWD(16, false);
+    return p.L == 8 ? LIN_FWD(8, true) : LIN_FWD(16, true);
+#undef LIN_FWD
 }
 
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
@@ -191,9 +218,12 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (blocks == 0) return cudaSuccess;
-    if (p.L == 8)
-        return launch_cluster(lin_bwd_kernel<8>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
-    return launch_cluster(lin_bwd_kernel<16>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, p.S);
+#define LIN_BWD(L_, CL_)                                                                                       \
+    launch_cluster(lin_bwd_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, \
+                   p.S)
+    if (p.S == 1) return p.L == 8 ? LIN_BWD(8, false) : LIN_BWD(16, false);
+    return p.L == 8 ? LIN_BWD(8, true) : LIN_BWD(16, true);
+#undef LIN_BWD
 }
 
 }  // namespace mgs
