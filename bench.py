@@ -497,7 +497,7 @@ def run_gpu(args):
         from dataclasses import replace
         ws = [replace(w, B=min(w.B, args.batch_rows)) for w in ws]
     runners = [Runner(w, torch, b, api, device) for w in ws]
-    small = {r.w.cid: (r.w.op != "psl" and r.w.B * r.w.T * r.w.H * r.w.k * r.w.k * 4 * 3 < (256 << 20)) for r in runners}
+    small = {r.w.cid: r.w.B * r.w.T * r.w.H * r.w.k * r.w.k * 4 * 3 < (256 << 20) for r in runners}
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream

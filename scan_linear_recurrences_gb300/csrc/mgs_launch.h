@@ -34,6 +34,13 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
                            float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
 
+// parallel_scan_log with the saved-h backward on the same time-parallel
+// kernels (lin_supported decides, D as the channel count); no workspace.
+cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
+                              int64_t T, int64_t D, cudaStream_t s);
+cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,
+                              float *dlc, float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
+
 // matrix_scan
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);
 cudaError_t launch_ms_fwd(int K, const float *A, float *P, int64_t B, int64_t T, int64_t H,

@@ -14,6 +14,20 @@
 // the CTAs before it (read from their shared memory) to h0 to get the state
 // entering its segment.  Each warp then walks its steps from its own entry
 // state.  No workspace; T <= S W L.
+//
+// parallel_scan_log with few lanes runs on the same skeleton (the
+// "mingru-scans" home page, scan-op table, parallel_scan_log row, at its lab
+// and long-T shapes).  In base 2 (a = log_coeffs log2 e, v = log_values
+// log2 e) a step is L_t = logaddexp2(a_t + L_{t-1}, v_t), and steps s..e
+// act on the state entering them as x -> logaddexp2(A + x, V) with
+// A = a_s + ... + a_e and V the steps run from L = -inf; two such maps, p
+// then q, compose to A = A_p + A_q, V = logaddexp2(A_q + V_p, V_q).  Every
+// step's own arithmetic is that of the one-warp-per-128-channels kernel.
+// Its backward is the linear recurrence lambda_t = g_t + a_{t+1} lambda_{t+1}
+// (a = exp(log_coeffs)), as above, with d_log_values = lambda_t exp(lv_t),
+// d_log_coeffs = a_t lambda_t h_{t-1}, d_log_h0 = a_0 lambda_0 h_0.
+#include <math_constants.h>
+
 #include "mgs_launch.h"
 #include "mgs_device.cuh"
 #include "mgs_cluster.cuh"
@@ -176,6 +190,138 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     lin_wait2<kCl>();
 }
 
+// ---------------------------------------------------------------- parallel_scan_log
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// log2(2^x + 2^y), max-shifted; both -inf gives -inf.
+__device__ __forceinline__ float lae2(float x, float y) {
+    const float m = fmaxf(x, y);
+    const float r = m + lg2_approx(1.f + ex2_approx(-fabsf(x - y)));
+    return (m == -CUDART_INF_F) ? m : r;
+}
+
+// Warp 0: the log-space maps' offsets within the CTA (forward order) and the total.
+__device__ __forceinline__ void psl_cta_offsets(LinSmem &s, int lane) {
+    float pa = 0.f, pv = -CUDART_INF_F;
+    for (int k = 0; k < kLinWarps; ++k) {
+        s.pm[k][lane] = pa;
+        s.pc[k][lane] = pv;
+        pv = lae2(s.m[k][lane] + pv, s.c[k][lane]);
+        pa += s.m[k][lane];
+    }
+    s.tm[lane] = pa;
+    s.tc[lane] = pv;
+}
+
+template <int L, bool kCl>
+__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
+    psl_fwd_cl_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
+                      float *__restrict__ h, float *__restrict__ logh, int64_t T, int64_t D, int64_t groups,
+                      int S) {
+    __shared__ LinSmem sm;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned r = kCl ? cluster_rank() : 0u;
+    const int64_t lg = blockIdx.x / S, bi = lg / groups;
+    const int64_t ch = (lg - bi * groups) * 32 + lane;
+    const bool act = ch < D;
+    const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
+    const int n = lin_steps_here(act, L, t0, T);
+    const int64_t base = (bi * T + t0) * D + ch;
+    // steps past n are the identity: log_coeffs 0, log_values -inf
+    float cv[L], vb[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        cv[u] = u < n ? lc[base + u * D] : 0.f;
+        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
+    }
+    float A = 0.f, V = -CUDART_INF_F;
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
+        A = fmaf(cv[u], kLog2e, A);
+    }
+    sm.m[w][lane] = A;
+    sm.c[w][lane] = V;
+    __syncthreads();
+    if (w == 0) psl_cta_offsets(sm, lane);
+    lin_sync1<kCl>();
+    // log2 h entering this CTA's segment: log h0 (or -inf) through the CTAs before it
+    float x = (lh0 != nullptr && act) ? lh0[bi * D + ch] * kLog2e : -CUDART_INF_F;
+    if constexpr (kCl)
+        for (unsigned q = 0; q < r; ++q) x = lae2(ld_dsmem(&sm.tm[lane], q) + x, ld_dsmem(&sm.tc[lane], q));
+    lin_arrive2<kCl>();
+    x = lae2(sm.pm[w][lane] + x, sm.pc[w][lane]);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
+        if (u < n) {
+            __stcs(h + base + u * D, ex2_approx(x));
+            if (logh != nullptr) __stcs(logh + base + u * D, x * kLn2);
+        }
+    }
+    lin_wait2<kCl>();
+}
+
+template <int L, bool kCl>
+__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
+    psl_bwd_cl_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
+                      const float *__restrict__ h, const float *__restrict__ g, float *__restrict__ dlc,
+                      float *__restrict__ dlv, float *__restrict__ dlh0, int64_t T, int64_t D, int64_t groups,
+                      int S) {
+    __shared__ LinSmem sm;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const unsigned r = kCl ? cluster_rank() : 0u;
+    const int64_t lg = blockIdx.x / S, bi = lg / groups;
+    const int64_t ch = (lg - bi * groups) * 32 + lane;
+    const bool act = ch < D;
+    const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
+    const int n = lin_steps_here(act, L, t0, T);
+    const int64_t base = (bi * T + t0) * D + ch;
+    const float h0v = (lh0 != nullptr && act) ? ex2_approx(lh0[bi * D + ch] * kLog2e) : 0.f;
+    // a_t, exp(lv_t), g_t, h_{t-1} (h0 before the first step) of this warp's
+    // steps, and a after its last step (zero past the end: lambda_T = 0)
+    float at[L], ev[L], gv[L], hp[L];
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        at[u] = u < n ? ex2_approx(lc[base + u * D] * kLog2e) : 1.f;
+        ev[u] = u < n ? ex2_approx(lv[base + u * D] * kLog2e) : 0.f;
+        gv[u] = u < n ? g[base + u * D] : 0.f;
+        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
+    }
+    const float aft = (n > 0 && t0 + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
+    // step t's coefficient a_{t+1}; steps past n are the identity
+    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
+    float m = 1.f, c = 0.f;
+#pragma unroll
+    for (int u = L - 1; u >= 0; --u) {
+        c = fmaf(coef(u), c, gv[u]);
+        m *= coef(u);
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<true>(sm, lane);
+    lin_sync1<kCl>();
+    float x = 0.f;  // lambda past this CTA's segment
+    if constexpr (kCl)
+        for (int q = S - 1; q > int(r); --q)
+            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(q)), x, ld_dsmem(&sm.tc[lane], unsigned(q)));
+    lin_arrive2<kCl>();
+    float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+#pragma unroll
+    for (int u = L - 1; u >= 0; --u) {
+        lam = fmaf(coef(u), lam, gv[u]);
+        if (u < n) {
+            __stcs(dlv + base + u * D, lam * ev[u]);
+            __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+        }
+    }
+    // lam is lambda_0 in the first warp of the first CTA
+    if (r == 0 && w == 0 && act && dlh0 != nullptr) dlh0[bi * D + ch] = at[0] * lam * h0v;
+    lin_wait2<kCl>();
+}
+
 struct LinPlan {
     int L, S;
 };
@@ -205,8 +351,8 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
     if (blocks == 0) return cudaSuccess;
 #define LIN_FWD(L_, CL_) \
     launch_cluster(lin_fwd_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, a, b, h0, h, T, D, groups, p.S)
-    if (p.S == 1) return p.L == 8 ? LIN_FWD(8, false) : LIN_FWD(16, false);
-    return p.L == 8 ? LIN_FWD(8, true) : LIN_FWD(16, true);
+    if (p.L == 16) return LIN_FWD(16, true);  // T > 512: always more than one CTA
+    return p.S == 1 ? LIN_FWD(8, false) : LIN_FWD(8, true);
 #undef LIN_FWD
 }
 
@@ -221,9 +367,41 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
 #define LIN_BWD(L_, CL_)                                                                                       \
     launch_cluster(lin_bwd_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, a, h0, h, g, da, db, dh0, T, D, groups, \
                    p.S)
-    if (p.S == 1) return p.L == 8 ? LIN_BWD(8, false) : LIN_BWD(16, false);
-    return p.L == 8 ? LIN_BWD(8, true) : LIN_BWD(16, true);
+    if (p.L == 16) return LIN_BWD(16, true);  // T > 512: always more than one CTA
+    return p.S == 1 ? LIN_BWD(8, false) : LIN_BWD(8, true);
 #undef LIN_BWD
+}
+
+cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
+                              int64_t T, int64_t D, cudaStream_t s) {
+    const int64_t groups = (D + 31) / 32;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    const LinPlan p = lin_plan(T);
+    const int64_t blocks = B * groups * p.S;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
+#define PSL_FWD(L_, CL_)                                                                                     \
+    launch_cluster(psl_fwd_cl_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, lc, lv, lh0, h, logh, T, D, \
+                   groups, p.S)
+    if (p.L == 16) return PSL_FWD(16, true);  // T > 512: always more than one CTA
+    return p.S == 1 ? PSL_FWD(8, false) : PSL_FWD(8, true);
+#undef PSL_FWD
+}
+
+cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,
+                              float *dlc, float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
+    const int64_t groups = (D + 31) / 32;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    const LinPlan p = lin_plan(T);
+    const int64_t blocks = B * groups * p.S;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
+#define PSL_BWD(L_, CL_)                                                                                     \
+    launch_cluster(psl_bwd_cl_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, lc, lv, lh0, h, g, dlc, dlv, \
+                   dlh0, T, D, groups, p.S)
+    if (p.L == 16) return PSL_BWD(16, true);  // T > 512: always more than one CTA
+    return p.S == 1 ? PSL_BWD(8, false) : PSL_BWD(8, true);
+#undef PSL_BWD
 }
 
 }  // namespace mgs

@@ -318,4 +318,7 @@ EXTRA_WORKLOADS = {
     13: Workload(13, "delta", "delta_scan lab B=128 T=64 H=1 D=64", 128, 64, 1, 64, "normal"),
     14: Workload(14, "delta", "delta_scan long-T B=16 T=1024 H=1 D=64", 16, 1024, 1, 64, "normal"),
     15: Workload(15, "delta", "delta_scan scaled B=16 T=4096 H=16 D=64", 16, 4096, 16, 64, "normal"),
+    # parallel_scan_log at the pages' lab and long-T shapes (64 channels)
+    16: Workload(16, "psl", "parallel_scan_log lab B=128 T=64 D=64", 128, 64, 64, 1, "log"),
+    17: Workload(17, "psl", "parallel_scan_log long-T B=16 T=1024 D=64", 16, 1024, 64, 1, "log"),
 }

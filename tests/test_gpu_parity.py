@@ -271,6 +271,11 @@ def _check_psl(d, T, rows=None):
 
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 50, 132, True), (2, 257, 1024, True), (2, 100, 260, False), (1, 2000, 128, True),
+    # the pages' lab and long-T shapes (one-launch time-parallel path), and
+    # the edges of that path: 8 -> 16 steps a warp past T = 512, sequential
+    # past T = 1024 and from 2048 groups of 32 channels
+    (128, 64, 64, True), (16, 1024, 64, True), (3, 512, 20, True), (2, 513, 20, False),
+    (1, 1024, 8, False), (1, 1025, 8, True), (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_psl_shapes(B, T, D, h0):
     _run_psl(B, T, D, seed=300 + B * T + D, with_h0=h0)
