@@ -663,9 +663,12 @@ def run_gpu(args):
                                          "l2": "flushed"}
             del r
         # parallel_scan_log backward in recompute mode (h not saved) on the
-        # minGRU shape: DRAM bytes are 28 per element (log_coeffs and
-        # log_values read by both passes, grad_h read, two gradients written)
-        for r in runners:
+        # minGRU shape and the pages' lab and long-T shapes: DRAM bytes are 28
+        # per element on the minGRU shape (log_coeffs and log_values read by
+        # both passes, grad_h read, two gradients written), 20 where h is
+        # recomputed in registers (few lanes)
+        psl_extra = [Runner(w, torch, b, api, device) for w in inputs.EXTRA_WORKLOADS.values() if w.op == "psl"]
+        for r in runners + psl_extra:
             w = r.w
             if w.op != "psl":
                 continue
@@ -683,12 +686,16 @@ def run_gpu(args):
                 if it >= args.warmup:
                     ts.append(e0.elapsed_time(e1))
             bm = statistics.median(ts)
-            nbytes = w.B * w.T * w.H * 28 + 2 * w.B * w.H * 4 + 2 * nws
+            # the library's rule for its one-launch diagonal-scan kernels
+            in_regs = 1 <= w.T <= 1024 and w.B * ((w.H + 31) // 32) < 2048
+            per_elem = 20 if in_regs else 28
+            nbytes = w.B * w.T * w.H * per_elem + 2 * w.B * w.H * 4 + (0 if in_regs else 2 * nws)
             extra[f"psl_c{w.cid}_bwd_recompute"] = {
                 "shape": w.name, "bwd_us": round(bm * 1e3, 2), "workspace_bytes": nws,
                 "GBps": round(nbytes / (bm * 1e-3) / 1e9, 1),
-                "bytes": "28 per element + checkpoints", "l2": "flushed"}
+                "bytes": f"{per_elem} per element" + ("" if in_regs else " + checkpoints"), "l2": "flushed"}
             del ws
+        del psl_extra
         # matrix_affine_scan backward in recompute mode (h not saved) on the
         # scaled shape: per step A and b read by both passes, grad_h read,
         # dA and db written (4 (2k^2 + 2k + k + k^2 + k) = 896 bytes at k = 8),

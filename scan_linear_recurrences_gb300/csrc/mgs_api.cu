@@ -455,6 +455,10 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
     if ((st = check_ws(need, workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
+    if (h == nullptr && mgs::lin_supported(B, T, D))
+        return from_cuda(mgs::launch_psl_bwd_rc_cl(log_coeffs, log_values, log_h0, grad_h, d_log_coeffs,
+                                                   d_log_values, d_log_h0, B, T, D,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
     if (h == nullptr)
         return from_cuda(mgs::launch_psl_bwd_recompute(log_coeffs, log_values, log_h0, grad_h, d_log_coeffs,
                                                        d_log_values, d_log_h0, workspace, B, T, D, ctl,

@@ -40,6 +40,9 @@ cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0
                               int64_t T, int64_t D, cudaStream_t s);
 cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,
                               float *dlc, float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
+// ... and its backward recomputing the forward in registers (h not saved)
+cudaError_t launch_psl_bwd_rc_cl(const float *lc, const float *lv, const float *lh0, const float *g, float *dlc,
+                                 float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
 
 // matrix_scan
 size_t ms_workspace_bytes(int64_t B, int64_t T, int64_t H, int K, bool bwd);

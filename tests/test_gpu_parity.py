@@ -321,10 +321,14 @@ def test_psl_zero_coefficients_and_empty():
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 15, 132, True), (2, 16, 8, False), (2, 17, 1024, True), (3, 50, 260, False),
     (2, 257, 1024, True), (1, 2000, 128, True), (5, 33, 36, True),
+    # the pages' long-T and lab shapes, on the one-launch cluster path
+    (16, 1024, 64, True), (128, 64, 64, False), (2, 600, 12, True),
 ])
 def test_psl_recompute_backward(B, T, D, h0):
-    """h == NULL: checkpoints every 16 steps, segments rebuilt in reverse; ragged
-    last segments, T below one segment and partial 128-channel groups."""
+    """h == NULL.  With many lanes: checkpoints every 16 steps, segments rebuilt
+    in reverse (ragged last segments, T below one segment, partial 128-channel
+    groups); with few lanes and T <= 1024: h recomputed in registers by the
+    one-launch cluster kernel."""
     d = _cuda(inputs.psl_inputs(B, T, D, seed=700 + B * T + D, with_h0=h0))
     lc, lv, l0, g = d["log_coeffs"], d["log_values"], d["log_h0"], d["grad_h"]
     h = api.parallel_scan_log_fwd(lc, lv, l0)
