@@ -188,7 +188,10 @@ mgs_status mgs_matrix_scan_bwd(const float *A, const float *P, const float *grad
  *     log h_0 = log_h0 (NULL: h_0 = 0),   h_t = exp(log h_t),
  * i.e. h_t = exp(a*_t + logcumsumexp_{s<=t}(log_values_s - a*_s)) with
  * a*_t = sum_{s<=t} log_coeffs_s, evaluated as a max-shifted log-sum-exp
- * recurrence so no cumulative sum loses precision.
+ * recurrence so no cumulative sum loses precision.  With T <= 1024 and
+ * fewer than 2048 groups of 32 channels (B * ceil(D / 32)) the call is one
+ * launch that is parallel over time (thread-block clusters), else one warp
+ * walks each 128 channels' sequence.
  * In: log_coeffs, log_values [B][T][D], log_h0 [B][D] (nullable).
  * Out: h [B][T][D]; log_h [B][T][D] (nullable: not written). */
 mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_values,
@@ -213,7 +216,10 @@ mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_v
  * sweep reaches it.  That needs mgs_workspace_size(MGS_OP_PARALLEL_SCAN_LOG_BWD,
  * B, T, D, 0) = 4 * B * ceil(T / 16) * D bytes, 256-byte aligned (else
  * MGS_ERR_WORKSPACE), reads log_coeffs and log_values twice, and gives the
- * same results as passing the h this library's forward wrote. */
+ * same results as passing the h this library's forward wrote.  On the
+ * time-parallel path (the forward's condition above) h is recomputed in
+ * registers instead and the workspace, still required at that size, is not
+ * touched. */
 mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_values,
                                      const float *log_h0, const float *h, const float *grad_h,
                                      float *d_log_coeffs, float *d_log_values, float *d_log_h0,
