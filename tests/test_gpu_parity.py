@@ -62,6 +62,8 @@ def test_mas_configs_full(cid):
     (2, 50, 6, 2, "normal"),
     (2, 81, 12, 1, "normal"),   # k = 1: the diagonal (linear_scan) case
     (1, 300, 4, 8, "none"),
+    # 256 or more lane groups (one pass per lane group), ragged head groups
+    (96, 200, 11, 8, "none"), (300, 90, 7, 4, "normal"), (64, 1100, 16, 8, "normal"),
     # few lanes, long sequences: the time-chunked path
     (1, 1000, 3, 16, "normal"), (2, 515, 5, 4, "normal"), (1, 2048, 8, 8, "none"), (3, 4099, 2, 2, "normal"),
 ])
