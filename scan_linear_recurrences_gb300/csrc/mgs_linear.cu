@@ -13,7 +13,12 @@
 // CTA's total, and after a cluster barrier every CTA applies the totals of
 // the CTAs before it (read from their shared memory) to h0 to get the state
 // entering its segment.  Each warp then walks its steps from its own entry
-// state.  No workspace; T <= S W L.
+// state.  No workspace; T <= S W L = 1024.
+//
+// Up to T = 8192 the *_mb_ kernels run the same scheme with each warp
+// holding R <= 8 blocks of L = 16 steps: the first walk composes all of them
+// (loading one block at a time), the second reads each block again (from
+// L2) as it reruns it.
 //
 // parallel_scan_log with few lanes runs on the same skeleton (the
 // "mingru-scans" home page, scan-op table, parallel_scan_log row, at its lab
@@ -37,7 +42,9 @@ namespace {
 
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
-constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;
+constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;  // one block a warp
+constexpr int kLinMaxBlocks = 8;                                           // R at most
+constexpr int64_t kLinMaxTBlocks = kLinMaxT * kLinMaxBlocks;
 
 struct LinSmem {
     float m[kLinWarps][32], c[kLinWarps][32];    // each warp's map
@@ -405,6 +412,414 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     lin_wait2<kCl>();
 }
 
+// ---------------------------------------------------------------- several blocks a warp
+// The kernels above with each warp holding R blocks of L steps (always a
+// cluster of several CTAs: T > 1024).  Kept apart from the one-block kernels,
+// whose inputs stay in registers between the two walks.
+// Where a thread's work lies: its channel's offset `cb` in a [B][T][D]
+// tensor (element t at cb + t D), whether the channel exists, and the first
+// step of its warp's R blocks.
+struct LinLane {
+    int lane, w;
+    unsigned r;
+    int64_t bi, ch, cb, t0;
+    bool act;
+};
+template <int L>
+__device__ __forceinline__ LinLane lin_lane(int64_t T, int64_t D, int64_t groups, int S, int R) {
+    LinLane q;
+    q.lane = threadIdx.x & 31;
+    q.w = threadIdx.x >> 5;
+    q.r = cluster_rank();
+    const int64_t lg = blockIdx.x / S;
+    q.bi = lg / groups;
+    q.ch = (lg - q.bi * groups) * 32 + q.lane;
+    q.act = q.ch < D;
+    q.cb = q.bi * T * D + q.ch;
+    q.t0 = (int64_t(q.r) * kLinWarps + q.w) * int64_t(R) * L;
+    return q;
+}
+
+// Block k of a warp's inputs into registers (steps past the block's end the
+// identity); returns the block's step count.  Plain functions with
+// restrict-qualified pointers, so the loads may be issued ahead of anything.
+template <int L>
+__device__ __forceinline__ int lin_fwd_block(const float *__restrict__ a, const float *__restrict__ b,
+                                             const LinLane &q, int k, int64_t T, int64_t D, float (&av)[L],
+                                             float (&bv)[L]) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        av[u] = u < n ? a[base + u * D] : 1.f;
+        bv[u] = u < n ? b[base + u * D] : 0.f;
+    }
+    return n;
+}
+// step t's coefficient is a_{t+1} (none past the end: lambda_T = 0), and
+// da_t needs h_{t-1} (h0, or zero, before the first step)
+template <int L>
+__device__ __forceinline__ int lin_bwd_block(const float *__restrict__ a, const float *__restrict__ h,
+                                             const float *__restrict__ g, const LinLane &q, int k, int64_t T,
+                                             int64_t D, float hinit, float (&an)[L], float (&gv)[L], float (&hp)[L]) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        an[u] = u < n ? (tk + u + 1 < T ? a[base + (u + 1) * D] : 0.f) : 1.f;
+        gv[u] = u < n ? g[base + u * D] : 0.f;
+        hp[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : hinit) : 0.f;
+    }
+    return n;
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps)
+    lin_fwd_mb_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ h0,
+                   float *__restrict__ h, int64_t T, int64_t D, int64_t groups, int S, int R) {
+    __shared__ LinSmem sm;
+    const LinLane q = lin_lane<L>(T, D, groups, S, R);
+    const int lane = q.lane, w = q.w;
+    const int RR = R;
+    float av[L], bv[L];
+    auto load = [&](int k) { return lin_fwd_block<L>(a, b, q, k, T, D, av, bv); };
+    float m = 1.f, c = 0.f;
+    int n = 0;
+    for (int k = 0; k < RR; ++k) {
+        n = load(k);
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            c = fmaf(av[u], c, bv[u]);
+            m *= av[u];
+        }
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<false>(sm, lane);
+    lin_sync1<true>();
+    // the state entering this CTA's segment: h0 through the CTAs before it
+    float x = (h0 != nullptr && q.act) ? h0[q.bi * D + q.ch] : 0.f;
+    for (unsigned p = 0; p < q.r; ++p) x = fmaf(ld_dsmem(&sm.tm[lane], p), x, ld_dsmem(&sm.tc[lane], p));
+    lin_arrive2<true>();  // done reading the other CTAs' shared memory
+    x = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+    for (int k = 0; k < RR; ++k) {
+        n = load(k);
+        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            x = fmaf(av[u], x, bv[u]);
+            if (u < n) __stcs(h + base + u * D, x);
+        }
+    }
+    lin_wait2<true>();  // no CTA leaves while another may still read its shared memory
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps)
+    lin_bwd_mb_kernel(const float *__restrict__ a, const float *__restrict__ h0, const float *__restrict__ h,
+                   const float *__restrict__ g, float *__restrict__ da, float *__restrict__ db,
+                   float *__restrict__ dh0, int64_t T, int64_t D, int64_t groups, int S, int R) {
+    __shared__ LinSmem sm;
+    const LinLane q = lin_lane<L>(T, D, groups, S, R);
+    const int lane = q.lane, w = q.w;
+    const int RR = R;
+    const float hinit = (h0 != nullptr && q.act) ? h0[q.bi * D + q.ch] : 0.f;
+    float an[L], gv[L], hp[L];
+    auto load = [&](int k) { return lin_bwd_block<L>(a, h, g, q, k, T, D, hinit, an, gv, hp); };
+    // the warp's map, right to left: lambda at its first step = m lambda past its last + c
+    float m = 1.f, c = 0.f;
+    int n = 0;
+    for (int k = RR - 1; k >= 0; --k) {
+        n = load(k);
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            c = fmaf(an[u], c, gv[u]);
+            m *= an[u];
+        }
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<true>(sm, lane);
+    lin_sync1<true>();
+    // lambda leaving this CTA's segment: zero past the end through the CTAs after it
+    float x = 0.f;
+    for (int p = S - 1; p > int(q.r); --p)
+            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(p)), x, ld_dsmem(&sm.tc[lane], unsigned(p)));
+    lin_arrive2<true>();
+    float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+    for (int k = RR - 1; k >= 0; --k) {
+        n = load(k);
+        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            lam = fmaf(an[u], lam, gv[u]);
+            if (u < n) {
+                __stcs(db + base + u * D, lam);
+                __stcs(da + base + u * D, lam * hp[u]);
+            }
+        }
+    }
+    // lam is lambda_0 in the first warp of the first CTA
+    if (q.r == 0 && w == 0 && q.act && dh0 != nullptr) dh0[q.bi * D + q.ch] = a[q.cb] * lam;
+    lin_wait2<true>();
+}
+
+
+// Block k of the log-space inputs (steps past the end the identity:
+// log_coeffs 0, log_values -inf); returns the block's step count.
+template <int L>
+__device__ __forceinline__ int psl_fwd_block(const float *__restrict__ lc, const float *__restrict__ lv,
+                                             const LinLane &q, int k, int64_t T, int64_t D, float (&cv)[L],
+                                             float (&vb)[L]) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        cv[u] = u < n ? lc[base + u * D] : 0.f;
+        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
+    }
+    return n;
+}
+// The saved-h backward's block: a_t, exp(lv_t), g_t, h_{t-1} (h0, or zero,
+// before t = 0), and a after the block's last step (zero past the end:
+// lambda_T = 0) in *aft; steps past the end are the identity.  Without
+// kOut only what the map needs (a, g).
+template <int L, bool kOut>
+__device__ __forceinline__ int psl_bwd_block(const float *__restrict__ lc, const float *__restrict__ lv,
+                                             const float *__restrict__ h, const float *__restrict__ g,
+                                             const LinLane &q, int k, int64_t T, int64_t D, float h0v, float (&at)[L],
+                                             float (&ev)[L], float (&gv)[L], float (&hp)[L], float *aft) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        at[u] = u < n ? ex2_approx(lc[base + u * D] * kLog2e) : 1.f;
+        gv[u] = u < n ? g[base + u * D] : 0.f;
+        if constexpr (kOut) {
+            ev[u] = u < n ? ex2_approx(lv[base + u * D] * kLog2e) : 0.f;
+            hp[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
+        }
+    }
+    *aft = (n > 0 && tk + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
+    return n;
+}
+// The recompute-mode backward's block: log_coeffs, log_values (base 2), g,
+// a = exp(log_coeffs) and a after the block (in *aft).
+template <int L>
+__device__ __forceinline__ int psl_rc_block(const float *__restrict__ lc, const float *__restrict__ lv,
+                                            const float *__restrict__ g, const LinLane &q, int k, int64_t T,
+                                            int64_t D, float (&cv)[L], float (&vb)[L], float (&gv)[L], float (&at)[L],
+                                            float *aft) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        cv[u] = u < n ? lc[base + u * D] : 0.f;
+        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
+        gv[u] = u < n ? g[base + u * D] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < L; ++u) at[u] = u < n ? ex2_approx(cv[u] * kLog2e) : 1.f;
+    *aft = (n > 0 && tk + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
+    return n;
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
+    psl_fwd_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
+                      float *__restrict__ h, float *__restrict__ logh, int64_t T, int64_t D, int64_t groups,
+                      int S, int R) {
+    __shared__ LinSmem sm;
+    const LinLane q = lin_lane<L>(T, D, groups, S, R);
+    const int lane = q.lane, w = q.w;
+    const int RR = R;
+    float cv[L], vb[L];
+    auto load = [&](int k) { return psl_fwd_block<L>(lc, lv, q, k, T, D, cv, vb); };
+    float A = 0.f, V = -CUDART_INF_F;
+    int n = 0;
+    for (int k = 0; k < RR; ++k) {
+        n = load(k);
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
+            A = fmaf(cv[u], kLog2e, A);
+        }
+    }
+    sm.m[w][lane] = A;
+    sm.c[w][lane] = V;
+    __syncthreads();
+    if (w == 0) psl_cta_offsets(sm, lane);
+    lin_sync1<true>();
+    // log2 h entering this CTA's segment: log h0 (or -inf) through the CTAs before it
+    float x = (lh0 != nullptr && q.act) ? lh0[q.bi * D + q.ch] * kLog2e : -CUDART_INF_F;
+    for (unsigned p = 0; p < q.r; ++p) x = lae2(ld_dsmem(&sm.tm[lane], p) + x, ld_dsmem(&sm.tc[lane], p));
+    lin_arrive2<true>();
+    x = lae2(sm.pm[w][lane] + x, sm.pc[w][lane]);
+    for (int k = 0; k < RR; ++k) {
+        n = load(k);
+        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
+            if (u < n) {
+                __stcs(h + base + u * D, ex2_approx(x));
+                if (logh != nullptr) __stcs(logh + base + u * D, x * kLn2);
+            }
+        }
+    }
+    lin_wait2<true>();
+}
+
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
+    psl_bwd_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
+                      const float *__restrict__ h, const float *__restrict__ g, float *__restrict__ dlc,
+                      float *__restrict__ dlv, float *__restrict__ dlh0, int64_t T, int64_t D, int64_t groups,
+                      int S, int R) {
+    __shared__ LinSmem sm;
+    const LinLane q = lin_lane<L>(T, D, groups, S, R);
+    const int lane = q.lane, w = q.w;
+    const int RR = R;
+    const float h0v = (lh0 != nullptr && q.act) ? ex2_approx(lh0[q.bi * D + q.ch] * kLog2e) : 0.f;
+    float at[L], ev[L], gv[L], hp[L], aft = 0.f;
+    int n = 0;
+    // the first pass needs only a and g when the second loads the blocks again
+    auto load_map = [&](int k) { n = psl_bwd_block<L, false>(lc, lv, h, g, q, k, T, D, h0v, at, ev, gv, hp, &aft); };
+    auto load = [&](int k) { n = psl_bwd_block<L, true>(lc, lv, h, g, q, k, T, D, h0v, at, ev, gv, hp, &aft); };
+    // step u's coefficient a_{t+1}
+    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
+    float m = 1.f, c = 0.f;
+    for (int k = RR - 1; k >= 0; --k) {
+        load_map(k);
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            c = fmaf(coef(u), c, gv[u]);
+            m *= coef(u);
+        }
+    }
+    sm.m[w][lane] = m;
+    sm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) lin_cta_offsets<true>(sm, lane);
+    lin_sync1<true>();
+    float x = 0.f;  // lambda past this CTA's segment
+    for (int p = S - 1; p > int(q.r); --p)
+            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(p)), x, ld_dsmem(&sm.tc[lane], unsigned(p)));
+    lin_arrive2<true>();
+    float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
+    for (int k = RR - 1; k >= 0; --k) {
+        load(k);
+        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            lam = fmaf(coef(u), lam, gv[u]);
+            if (u < n) {
+                __stcs(dlv + base + u * D, lam * ev[u]);
+                __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+            }
+        }
+    }
+    // lam is lambda_0 in the first warp of the first CTA
+    if (q.r == 0 && w == 0 && q.act && dlh0 != nullptr) dlh0[q.bi * D + q.ch] = at[0] * lam * h0v;
+    lin_wait2<true>();
+}
+
+// Backward without the saved h (the pages' log-space op recomputes its
+// forward): both recurrences' maps are composed in the first pass (the
+// forward's from log_coeffs and log_values, the backward's from a and g, none
+// of them needs h), both carries cross the CTA and the cluster together, and
+// each warp then reruns its forward steps from its entering state, keeping
+// h_{t-1} in registers (R > 1: the state entering each block in shared
+// memory, each block's h rebuilt from it), before walking its backward
+// steps.  h is never stored and no workspace is used.  The maps compose in
+// the order the other two kernels use, so the results equal the saved-h
+// backward's bit for bit.
+template <int L>
+__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
+    psl_bwd_rc_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
+                         const float *__restrict__ g, float *__restrict__ dlc, float *__restrict__ dlv,
+                         float *__restrict__ dlh0, int64_t T, int64_t D, int64_t groups, int S, int R) {
+    __shared__ LinSmem fm, bm;                           // the forward's maps, the backward's
+    __shared__ float xs[kLinMaxBlocks][32 * kLinWarps];  // log2 h entering each block
+    const LinLane q = lin_lane<L>(T, D, groups, S, R);
+    const int lane = q.lane, w = q.w;
+    const int RR = R;
+    const float l0 = (lh0 != nullptr && q.act) ? lh0[q.bi * D + q.ch] * kLog2e : -CUDART_INF_F;
+    float cv[L], vb[L], gv[L], at[L], aft = 0.f;
+    int n = 0;
+    auto load = [&](int k) { n = psl_rc_block<L>(lc, lv, g, q, k, T, D, cv, vb, gv, at, &aft); };
+    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
+    // forward map left to right, backward map right to left (block R-1 is
+    // still loaded after the first loop)
+    float A = 0.f, V = -CUDART_INF_F, m = 1.f, c = 0.f;
+    for (int k = 0; k < RR; ++k) {
+        load(k);
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
+            A = fmaf(cv[u], kLog2e, A);
+        }
+    }
+    for (int k = RR - 1; k >= 0; --k) {
+        if (k != RR - 1) load(k);
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            c = fmaf(coef(u), c, gv[u]);
+            m *= coef(u);
+        }
+    }
+    fm.m[w][lane] = A;
+    fm.c[w][lane] = V;
+    bm.m[w][lane] = m;
+    bm.c[w][lane] = c;
+    __syncthreads();
+    if (w == 0) {
+        psl_cta_offsets(fm, lane);
+        lin_cta_offsets<true>(bm, lane);
+    }
+    lin_sync1<true>();
+    float x = l0, y = 0.f;  // log2 h entering the CTA's segment, lambda past it
+    for (unsigned p = 0; p < q.r; ++p) x = lae2(ld_dsmem(&fm.tm[lane], p) + x, ld_dsmem(&fm.tc[lane], p));
+    for (int p = S - 1; p > int(q.r); --p)
+        y = fmaf(ld_dsmem(&bm.tm[lane], unsigned(p)), y, ld_dsmem(&bm.tc[lane], unsigned(p)));
+    lin_arrive2<true>();
+    x = lae2(fm.pm[w][lane] + x, fm.pc[w][lane]);
+    xs[0][threadIdx.x] = x;
+    for (int k = 0; k + 1 < RR; ++k) {  // the state entering each later block
+        load(k);
+#pragma unroll
+        for (int u = 0; u < L; ++u) x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
+        xs[k + 1][threadIdx.x] = x;
+    }
+    float lam = fmaf(bm.pm[w][lane], y, bm.pc[w][lane]);
+    for (int k = RR - 1; k >= 0; --k) {
+        load(k);
+        // the forward over this block: h_{t-1} of each step (h0, or zero, before t = 0)
+        float hp[L];
+        float xk = xs[k][threadIdx.x];
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            hp[u] = ex2_approx(xk);
+            xk = lae2(fmaf(cv[u], kLog2e, xk), vb[u]);
+        }
+        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+#pragma unroll
+        for (int u = L - 1; u >= 0; --u) {
+            lam = fmaf(coef(u), lam, gv[u]);
+            if (u < n) {
+                __stcs(dlv + base + u * D, lam * ex2_approx(vb[u]));
+                __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+            }
+        }
+        // lam is lambda_0 and hp[0] is h0 at block 0 of the first warp of the first CTA
+        if (k == 0 && q.r == 0 && w == 0 && q.act && dlh0 != nullptr)
+            dlh0[q.bi * D + q.ch] = at[0] * lam * hp[0];
+    }
+    lin_wait2<true>();
+}
+
 struct LinPlan {
     int L, S;
 };
@@ -416,18 +831,32 @@ LinPlan lin_plan(int64_t T) {
     return p;
 }
 
+// T in (1024, 8192]: R blocks of 16 steps a warp, S CTAs a cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_mb(void (*kern)(KArgs...), int64_t B, int64_t T, int64_t D, cudaStream_t s, Args... args) {
+    if (T > kLinMaxTBlocks) return cudaErrorInvalidConfiguration;
+    const int64_t groups = (D + 31) / 32, cta_steps = int64_t(16) * kLinWarps;
+    const int R = int((T + cta_steps * kLinMaxCta - 1) / (cta_steps * kLinMaxCta));
+    const int S = int((T + cta_steps * R - 1) / (cta_steps * R));
+    const int64_t blocks = B * groups * S;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (blocks == 0) return cudaSuccess;
+    return launch_cluster(kern, blocks, 32 * kLinWarps, 0, S, s, args..., T, D, groups, S, R);
+}
+
 }  // namespace
 
 // Few channel groups (under 2048 warps of channels, where one thread walking
-// a channel's whole sequence leaves the GPU latency-bound) and T <= 1024.
+// a channel's whole sequence leaves the GPU latency-bound) and T <= 8192.
 bool lin_supported(int64_t B, int64_t T, int64_t D) {
-    return T >= 1 && T <= kLinMaxT && B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048;
+    return T >= 1 && T <= kLinMaxTBlocks && B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048;
 }
 
 cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                            int64_t D, cudaStream_t s) {
+    if (T > kLinMaxT) return launch_mb(lin_fwd_mb_kernel<16>, B, T, D, s, a, b, h0, h);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -441,8 +870,9 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
 
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
                            float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
+    if (T > kLinMaxT) return launch_mb(lin_bwd_mb_kernel<16>, B, T, D, s, a, h0, h, g, da, db, dh0);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -457,8 +887,9 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
 
 cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
                               int64_t T, int64_t D, cudaStream_t s) {
+    if (T > kLinMaxT) return launch_mb(psl_fwd_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, h, logh);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -473,8 +904,9 @@ cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0
 
 cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,
                               float *dlc, float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
+    if (T > kLinMaxT) return launch_mb(psl_bwd_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, h, g, dlc, dlv, dlh0);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -489,8 +921,9 @@ cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0
 
 cudaError_t launch_psl_bwd_rc_cl(const float *lc, const float *lv, const float *lh0, const float *g, float *dlc,
                                  float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
+    if (T > kLinMaxT) return launch_mb(psl_bwd_rc_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, g, dlc, dlv, dlh0);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
+    if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;

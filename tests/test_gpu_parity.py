@@ -274,10 +274,11 @@ def _check_psl(d, T, rows=None):
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 50, 132, True), (2, 257, 1024, True), (2, 100, 260, False), (1, 2000, 128, True),
     # the pages' lab and long-T shapes (one-launch time-parallel path), and
-    # the edges of that path: 8 -> 16 steps a warp past T = 512, sequential
-    # past T = 1024 and from 2048 groups of 32 channels
+    # the edges of that path: 8 -> 16 steps a block past T = 512, 1 -> 2
+    # blocks a warp past T = 1024, its end at T = 8192, 2048 channel groups
     (128, 64, 64, True), (16, 1024, 64, True), (3, 512, 20, True), (2, 513, 20, False),
-    (1, 1024, 8, False), (1, 1025, 8, True), (63, 40, 1024, True), (64, 40, 1024, True),
+    (1, 1024, 8, False), (1, 1025, 8, True), (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
+    (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_psl_shapes(B, T, D, h0):
     _run_psl(B, T, D, seed=300 + B * T + D, with_h0=h0)
@@ -323,8 +324,11 @@ def test_psl_zero_coefficients_and_empty():
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 15, 132, True), (2, 16, 8, False), (2, 17, 1024, True), (3, 50, 260, False),
     (2, 257, 1024, True), (1, 2000, 128, True), (5, 33, 36, True),
-    # the pages' long-T and lab shapes, on the one-launch cluster path
-    (16, 1024, 64, True), (128, 64, 64, False), (2, 600, 12, True),
+    # the pages' long-T and lab shapes, on the one-launch cluster path (one
+    # and several blocks a warp)
+    (16, 1024, 64, True), (128, 64, 64, False), (2, 600, 12, True), (2, 2500, 36, True), (1, 8192, 8, False),
+    # 2048 channel groups, ragged last segment: the checkpointing kernel
+    (64, 33, 1024, True),
 ])
 def test_psl_recompute_backward(B, T, D, h0):
     """h == NULL.  With many lanes: checkpoints every 16 steps, segments rebuilt
@@ -392,9 +396,11 @@ def test_psl_recompute_autograd_and_T0():
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 77, 132, True), (2, 300, 64, True), (1, 2000, 32, False), (4, 500, 1024, True),
     (16, 1024, 64, True), (128, 64, 64, True),
-    # edges of the one-launch time-parallel path: 8 -> 32 steps a warp past
-    # T = 256, sequential past T = 1024, and past 2048 channel groups
-    (3, 256, 36, True), (2, 257, 20, False), (1, 1024, 8, False), (1, 1025, 8, True),
+    # edges of the one-launch time-parallel path: 8 -> 16 steps a block past
+    # T = 512, 1 -> 2 blocks a warp past T = 1024, its end at T = 8192, and
+    # 2048 channel groups
+    (3, 512, 36, True), (2, 513, 20, False), (1, 1024, 8, False), (1, 1025, 8, True),
+    (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
     (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_linear_scan(B, T, D, h0):
