@@ -232,7 +232,7 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
  *     h_t = a_t * h_{t-1} + b_t,   h_0 = h0 (zeros when NULL),
  * with signed coefficients allowed (the negative-eigenvalue gates of
  * SignedMinGRU, home page lineage paragraph).  It is matrix_affine_scan with
- * k = 1 and H = D and validates as that op; T <= 8192 with fewer than 2048
+ * k = 1 and H = D and validates as that op; T <= 1024 with fewer than 2048
  * groups of 32 channels (B * ceil(D / 32)) runs as one time-parallel launch
  * on thread-block clusters that uses no workspace, other shapes on the
  * matrix_affine_scan kernels.  The workspace size is that op's either way.

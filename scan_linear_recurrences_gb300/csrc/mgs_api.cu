@@ -421,7 +421,7 @@ mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_v
     if ((st = check_ws(0, workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    if (mgs::lin_supported(B, T, D))
+    if (mgs::psl_cl_supported(B, T, D))
         return from_cuda(mgs::launch_psl_fwd_cl(log_coeffs, log_values, log_h0, h, log_h, B, T, D,
                                                 reinterpret_cast<cudaStream_t>(stream)));
     return from_cuda(mgs::launch_psl_fwd(log_coeffs, log_values, log_h0, h, log_h, B, T, D, ctl,
@@ -455,7 +455,7 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
     if ((st = check_ws(need, workspace, workspace_bytes)) != MGS_OK) return st;
     mgs::DevCtl ctl;
     if ((st = current_ctl(&ctl)) != MGS_OK) return st;
-    if (h == nullptr && mgs::lin_supported(B, T, D))
+    if (h == nullptr && mgs::psl_cl_supported(B, T, D))
         return from_cuda(mgs::launch_psl_bwd_rc_cl(log_coeffs, log_values, log_h0, grad_h, d_log_coeffs,
                                                    d_log_values, d_log_h0, B, T, D,
                                                    reinterpret_cast<cudaStream_t>(stream)));
@@ -463,7 +463,7 @@ mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_v
         return from_cuda(mgs::launch_psl_bwd_recompute(log_coeffs, log_values, log_h0, grad_h, d_log_coeffs,
                                                        d_log_values, d_log_h0, workspace, B, T, D, ctl,
                                                        reinterpret_cast<cudaStream_t>(stream)));
-    if (mgs::lin_supported(B, T, D))
+    if (mgs::psl_cl_supported(B, T, D))
         return from_cuda(mgs::launch_psl_bwd_cl(log_coeffs, log_values, log_h0, h, grad_h, d_log_coeffs,
                                                 d_log_values, d_log_h0, B, T, D,
                                                 reinterpret_cast<cudaStream_t>(stream)));

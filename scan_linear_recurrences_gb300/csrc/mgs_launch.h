@@ -29,13 +29,15 @@ cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, cons
 // linear_scan (matrix_affine_scan with k = 1), time-parallel in one launch
 // for few channel groups and T <= 1024; no workspace.  h0 and dh0 may be null.
 bool lin_supported(int64_t B, int64_t T, int64_t D);
+// the same for parallel_scan_log, T <= 8192
+bool psl_cl_supported(int64_t B, int64_t T, int64_t D);
 cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                            int64_t D, cudaStream_t s);
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
                            float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s);
 
 // parallel_scan_log with the saved-h backward on the same time-parallel
-// kernels (lin_supported decides, D as the channel count); no workspace.
+// kernels (psl_cl_supported decides, D as the channel count); no workspace.
 cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
                               int64_t T, int64_t D, cudaStream_t s);
 cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,

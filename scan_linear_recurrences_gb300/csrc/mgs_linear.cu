@@ -15,10 +15,10 @@
 // entering its segment.  Each warp then walks its steps from its own entry
 // state.  No workspace; T <= S W L = 1024.
 //
-// Up to T = 8192 the *_mb_ kernels run the same scheme with each warp
-// holding R <= 8 blocks of L = 16 steps: the first walk composes all of them
-// (loading one block at a time), the second reads each block again (from
-// L2) as it reruns it.
+// parallel_scan_log runs up to T = 8192 with the *_mb_ kernels: the same
+// scheme with each warp holding R <= 8 blocks of L = 16 steps; the first walk
+// composes all of them (loading one block at a time), the second reads each
+// block again (from L2) as it reruns it.
 //
 // parallel_scan_log with few lanes runs on the same skeleton (the
 // "mingru-scans" home page, scan-op table, parallel_scan_log row, at its lab
@@ -443,129 +443,6 @@ __device__ __forceinline__ LinLane lin_lane(int64_t T, int64_t D, int64_t groups
 // Block k of a warp's inputs into registers (steps past the block's end the
 // identity); returns the block's step count.  Plain functions with
 // restrict-qualified pointers, so the loads may be issued ahead of anything.
-template <int L>
-__device__ __forceinline__ int lin_fwd_block(const float *__restrict__ a, const float *__restrict__ b,
-                                             const LinLane &q, int k, int64_t T, int64_t D, float (&av)[L],
-                                             float (&bv)[L]) {
-    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
-    const int n = lin_steps_here(q.act, L, tk, T);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        av[u] = u < n ? a[base + u * D] : 1.f;
-        bv[u] = u < n ? b[base + u * D] : 0.f;
-    }
-    return n;
-}
-// step t's coefficient is a_{t+1} (none past the end: lambda_T = 0), and
-// da_t needs h_{t-1} (h0, or zero, before the first step)
-template <int L>
-__device__ __forceinline__ int lin_bwd_block(const float *__restrict__ a, const float *__restrict__ h,
-                                             const float *__restrict__ g, const LinLane &q, int k, int64_t T,
-                                             int64_t D, float hinit, float (&an)[L], float (&gv)[L], float (&hp)[L]) {
-    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
-    const int n = lin_steps_here(q.act, L, tk, T);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        an[u] = u < n ? (tk + u + 1 < T ? a[base + (u + 1) * D] : 0.f) : 1.f;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-        hp[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : hinit) : 0.f;
-    }
-    return n;
-}
-
-template <int L>
-__global__ void __launch_bounds__(32 * kLinWarps)
-    lin_fwd_mb_kernel(const float *__restrict__ a, const float *__restrict__ b, const float *__restrict__ h0,
-                   float *__restrict__ h, int64_t T, int64_t D, int64_t groups, int S, int R) {
-    __shared__ LinSmem sm;
-    const LinLane q = lin_lane<L>(T, D, groups, S, R);
-    const int lane = q.lane, w = q.w;
-    const int RR = R;
-    float av[L], bv[L];
-    auto load = [&](int k) { return lin_fwd_block<L>(a, b, q, k, T, D, av, bv); };
-    float m = 1.f, c = 0.f;
-    int n = 0;
-    for (int k = 0; k < RR; ++k) {
-        n = load(k);
-#pragma unroll
-        for (int u = 0; u < L; ++u) {
-            c = fmaf(av[u], c, bv[u]);
-            m *= av[u];
-        }
-    }
-    sm.m[w][lane] = m;
-    sm.c[w][lane] = c;
-    __syncthreads();
-    if (w == 0) lin_cta_offsets<false>(sm, lane);
-    lin_sync1<true>();
-    // the state entering this CTA's segment: h0 through the CTAs before it
-    float x = (h0 != nullptr && q.act) ? h0[q.bi * D + q.ch] : 0.f;
-    for (unsigned p = 0; p < q.r; ++p) x = fmaf(ld_dsmem(&sm.tm[lane], p), x, ld_dsmem(&sm.tc[lane], p));
-    lin_arrive2<true>();  // done reading the other CTAs' shared memory
-    x = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
-    for (int k = 0; k < RR; ++k) {
-        n = load(k);
-        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
-#pragma unroll
-        for (int u = 0; u < L; ++u) {
-            x = fmaf(av[u], x, bv[u]);
-            if (u < n) __stcs(h + base + u * D, x);
-        }
-    }
-    lin_wait2<true>();  // no CTA leaves while another may still read its shared memory
-}
-
-template <int L>
-__global__ void __launch_bounds__(32 * kLinWarps)
-    lin_bwd_mb_kernel(const float *__restrict__ a, const float *__restrict__ h0, const float *__restrict__ h,
-                   const float *__restrict__ g, float *__restrict__ da, float *__restrict__ db,
-                   float *__restrict__ dh0, int64_t T, int64_t D, int64_t groups, int S, int R) {
-    __shared__ LinSmem sm;
-    const LinLane q = lin_lane<L>(T, D, groups, S, R);
-    const int lane = q.lane, w = q.w;
-    const int RR = R;
-    const float hinit = (h0 != nullptr && q.act) ? h0[q.bi * D + q.ch] : 0.f;
-    float an[L], gv[L], hp[L];
-    auto load = [&](int k) { return lin_bwd_block<L>(a, h, g, q, k, T, D, hinit, an, gv, hp); };
-    // the warp's map, right to left: lambda at its first step = m lambda past its last + c
-    float m = 1.f, c = 0.f;
-    int n = 0;
-    for (int k = RR - 1; k >= 0; --k) {
-        n = load(k);
-#pragma unroll
-        for (int u = L - 1; u >= 0; --u) {
-            c = fmaf(an[u], c, gv[u]);
-            m *= an[u];
-        }
-    }
-    sm.m[w][lane] = m;
-    sm.c[w][lane] = c;
-    __syncthreads();
-    if (w == 0) lin_cta_offsets<true>(sm, lane);
-    lin_sync1<true>();
-    // lambda leaving this CTA's segment: zero past the end through the CTAs after it
-    float x = 0.f;
-    for (int p = S - 1; p > int(q.r); --p)
-            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(p)), x, ld_dsmem(&sm.tc[lane], unsigned(p)));
-    lin_arrive2<true>();
-    float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
-    for (int k = RR - 1; k >= 0; --k) {
-        n = load(k);
-        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
-#pragma unroll
-        for (int u = L - 1; u >= 0; --u) {
-            lam = fmaf(an[u], lam, gv[u]);
-            if (u < n) {
-                __stcs(db + base + u * D, lam);
-                __stcs(da + base + u * D, lam * hp[u]);
-            }
-        }
-    }
-    // lam is lambda_0 in the first warp of the first CTA
-    if (q.r == 0 && w == 0 && q.act && dh0 != nullptr) dh0[q.bi * D + q.ch] = a[q.cb] * lam;
-    lin_wait2<true>();
-}
-
 
 // Block k of the log-space inputs (steps past the end the identity:
 // log_coeffs 0, log_values -inf); returns the block's step count.
@@ -847,16 +724,19 @@ cudaError_t launch_mb(void (*kern)(KArgs...), int64_t B, int64_t T, int64_t D, c
 }  // namespace
 
 // Few channel groups (under 2048 warps of channels, where one thread walking
-// a channel's whole sequence leaves the GPU latency-bound) and T <= 8192.
-bool lin_supported(int64_t B, int64_t T, int64_t D) {
-    return T >= 1 && T <= kLinMaxTBlocks && B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048;
+// a channel's whole sequence leaves the GPU latency-bound), and T <= 1024 for
+// linear_scan (past that the three-launch chunked k = 1 path measured faster
+// than several blocks a warp), T <= 8192 for parallel_scan_log.
+static bool few_channel_groups(int64_t B, int64_t D) { return B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048; }
+bool lin_supported(int64_t B, int64_t T, int64_t D) { return T >= 1 && T <= kLinMaxT && few_channel_groups(B, D); }
+bool psl_cl_supported(int64_t B, int64_t T, int64_t D) {
+    return T >= 1 && T <= kLinMaxTBlocks && few_channel_groups(B, D);
 }
 
 cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                            int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb(lin_fwd_mb_kernel<16>, B, T, D, s, a, b, h0, h);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1) return cudaErrorInvalidConfiguration;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -870,9 +750,8 @@ cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, floa
 
 cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, const float *g, float *da, float *db,
                            float *dh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb(lin_bwd_mb_kernel<16>, B, T, D, s, a, h0, h, g, da, db, dh0);
     const int64_t groups = (D + 31) / 32;
-    if (T < 1) return cudaErrorInvalidConfiguration;
+    if (T < 1 || T > kLinMaxT) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
     const int64_t blocks = B * groups * p.S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;

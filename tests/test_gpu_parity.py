@@ -396,9 +396,9 @@ def test_psl_recompute_autograd_and_T0():
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 77, 132, True), (2, 300, 64, True), (1, 2000, 32, False), (4, 500, 1024, True),
     (16, 1024, 64, True), (128, 64, 64, True),
-    # edges of the one-launch time-parallel path: 8 -> 16 steps a block past
-    # T = 512, 1 -> 2 blocks a warp past T = 1024, its end at T = 8192, and
-    # 2048 channel groups
+    # edges of the one-launch time-parallel path: 8 -> 16 steps a warp past
+    # T = 512, the three-launch chunked path past T = 1024, and 2048 channel
+    # groups
     (3, 512, 36, True), (2, 513, 20, False), (1, 1024, 8, False), (1, 1025, 8, True),
     (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
     (63, 40, 1024, True), (64, 40, 1024, True),
