@@ -687,7 +687,7 @@ def run_gpu(args):
                     ts.append(e0.elapsed_time(e1))
             bm = statistics.median(ts)
             # the library's rule for its one-launch diagonal-scan kernels
-            in_regs = 1 <= w.T <= 8192 and w.B * ((w.H + 31) // 32) < 2048
+            in_regs = 1 <= w.T <= 32768 and w.B * ((w.H + 31) // 32) < 2048
             per_elem = 20 if in_regs else 28
             nbytes = w.B * w.T * w.H * per_elem + 2 * w.B * w.H * 4 + (0 if in_regs else 2 * nws)
             extra[f"psl_c{w.cid}_bwd_recompute"] = {

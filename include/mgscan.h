@@ -188,7 +188,7 @@ mgs_status mgs_matrix_scan_bwd(const float *A, const float *P, const float *grad
  *     log h_0 = log_h0 (NULL: h_0 = 0),   h_t = exp(log h_t),
  * i.e. h_t = exp(a*_t + logcumsumexp_{s<=t}(log_values_s - a*_s)) with
  * a*_t = sum_{s<=t} log_coeffs_s, evaluated as a max-shifted log-sum-exp
- * recurrence so no cumulative sum loses precision.  With T <= 8192 and
+ * recurrence so no cumulative sum loses precision.  With T <= 32768 and
  * fewer than 2048 groups of 32 channels (B * ceil(D / 32)) the call is one
  * launch that is parallel over time (thread-block clusters), else one warp
  * walks each 128 channels' sequence.

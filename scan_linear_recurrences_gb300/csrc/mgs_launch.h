@@ -29,7 +29,7 @@ cudaError_t launch_mas_bwd_recompute(int K, const float *A, const float *b, cons
 // linear_scan (matrix_affine_scan with k = 1), time-parallel in one launch
 // for few channel groups and T <= 1024; no workspace.  h0 and dh0 may be null.
 bool lin_supported(int64_t B, int64_t T, int64_t D);
-// the same for parallel_scan_log, T <= 8192
+// the same for parallel_scan_log, T <= 32768
 bool psl_cl_supported(int64_t B, int64_t T, int64_t D);
 cudaError_t launch_lin_fwd(const float *a, const float *b, const float *h0, float *h, int64_t B, int64_t T,
                            int64_t D, cudaStream_t s);

@@ -15,8 +15,8 @@
 // entering its segment.  Each warp then walks its steps from its own entry
 // state.  No workspace; T <= S W L = 1024.
 //
-// parallel_scan_log runs up to T = 8192 with the *_mb_ kernels: the same
-// scheme with each warp holding R <= 8 blocks of L = 16 steps; the first walk
+// parallel_scan_log runs up to T = 32768 with the *_mb_ kernels: the same
+// scheme with each warp holding R <= 32 blocks of L = 16 steps; the first walk
 // composes all of them (loading one block at a time), the second reads each
 // block again (from L2) as it reruns it.
 //
@@ -43,7 +43,7 @@ namespace {
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
 constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;  // one block a warp
-constexpr int kLinMaxBlocks = 8;                                           // R at most
+constexpr int kLinMaxBlocks = 32;                                          // R at most
 constexpr int64_t kLinMaxTBlocks = kLinMaxT * kLinMaxBlocks;
 
 struct LinSmem {
@@ -708,7 +708,7 @@ LinPlan lin_plan(int64_t T) {
     return p;
 }
 
-// T in (1024, 8192]: R blocks of 16 steps a warp, S CTAs a cluster.
+// T in (1024, 32768]: R blocks of 16 steps a warp, S CTAs a cluster.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_mb(void (*kern)(KArgs...), int64_t B, int64_t T, int64_t D, cudaStream_t s, Args... args) {
     if (T > kLinMaxTBlocks) return cudaErrorInvalidConfiguration;
@@ -726,7 +726,7 @@ cudaError_t launch_mb(void (*kern)(KArgs...), int64_t B, int64_t T, int64_t D, c
 // Few channel groups (under 2048 warps of channels, where one thread walking
 // a channel's whole sequence leaves the GPU latency-bound), and T <= 1024 for
 // linear_scan (past that the three-launch chunked k = 1 path measured faster
-// than several blocks a warp), T <= 8192 for parallel_scan_log.
+// than several blocks a warp), T <= 32768 for parallel_scan_log.
 static bool few_channel_groups(int64_t B, int64_t D) { return B >= 0 && D >= 0 && B * ((D + 31) / 32) < 2048; }
 bool lin_supported(int64_t B, int64_t T, int64_t D) { return T >= 1 && T <= kLinMaxT && few_channel_groups(B, D); }
 bool psl_cl_supported(int64_t B, int64_t T, int64_t D) {

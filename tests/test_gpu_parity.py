@@ -275,9 +275,10 @@ def _check_psl(d, T, rows=None):
     (2, 1, 4, True), (3, 50, 132, True), (2, 257, 1024, True), (2, 100, 260, False), (1, 2000, 128, True),
     # the pages' lab and long-T shapes (one-launch time-parallel path), and
     # the edges of that path: 8 -> 16 steps a block past T = 512, 1 -> 2
-    # blocks a warp past T = 1024, its end at T = 8192, 2048 channel groups
+    # blocks a warp past T = 1024, its end at T = 32768, 2048 channel groups
     (128, 64, 64, True), (16, 1024, 64, True), (3, 512, 20, True), (2, 513, 20, False),
     (1, 1024, 8, False), (1, 1025, 8, True), (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
+    (1, 32768, 8, True), (1, 32769, 4, False),
     (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_psl_shapes(B, T, D, h0):
@@ -327,6 +328,7 @@ def test_psl_zero_coefficients_and_empty():
     # the pages' long-T and lab shapes, on the one-launch cluster path (one
     # and several blocks a warp)
     (16, 1024, 64, True), (128, 64, 64, False), (2, 600, 12, True), (2, 2500, 36, True), (1, 8192, 8, False),
+    (1, 30000, 4, True),
     # 2048 channel groups, ragged last segment: the checkpointing kernel
     (64, 33, 1024, True),
 ])
