@@ -321,4 +321,6 @@ EXTRA_WORKLOADS = {
     # parallel_scan_log at the pages' lab and long-T shapes (64 channels)
     16: Workload(16, "psl", "parallel_scan_log lab B=128 T=64 D=64", 128, 64, 64, 1, "log"),
     17: Workload(17, "psl", "parallel_scan_log long-T B=16 T=1024 D=64", 16, 1024, 64, 1, "log"),
+    # and at config 3's sequence length with the long-T shape's few lanes
+    18: Workload(18, "psl", "parallel_scan_log few-lane B=16 T=4096 D=64", 16, 4096, 64, 1, "log"),
 }
