@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
     const int n = lin_steps_here(act, L, t0, T);
     const int64_t base = (bi * T + t0) * D + ch;
+    const float hinit = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;  // loaded with the inputs
     float av[L], bv[L];
 #pragma unroll
     for (int u = 0; u < L; ++u) {
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     if (w == 0) lin_cta_offsets<false>(sm, lane);
     lin_sync1<kCl>();
     // the state entering this CTA's segment: h0 through the CTAs before it
-    float x = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;
+    float x = hinit;
     if constexpr (kCl)
         for (unsigned q = 0; q < r; ++q) x = fmaf(ld_dsmem(&sm.tm[lane], q), x, ld_dsmem(&sm.tc[lane], q));
     lin_arrive2<kCl>();  // done reading the other CTAs' shared memory
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
     const int n = lin_steps_here(act, L, t0, T);
     const int64_t base = (bi * T + t0) * D + ch;
+    const float linit = (lh0 != nullptr && act) ? lh0[bi * D + ch] * kLog2e : -CUDART_INF_F;
     // steps past n are the identity: log_coeffs 0, log_values -inf
     float cv[L], vb[L];
 #pragma unroll
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     if (w == 0) psl_cta_offsets(sm, lane);
     lin_sync1<kCl>();
     // log2 h entering this CTA's segment: log h0 (or -inf) through the CTAs before it
-    float x = (lh0 != nullptr && act) ? lh0[bi * D + ch] * kLog2e : -CUDART_INF_F;
+    float x = linit;
     if constexpr (kCl)
         for (unsigned q = 0; q < r; ++q) x = lae2(ld_dsmem(&sm.tm[lane], q) + x, ld_dsmem(&sm.tc[lane], q));
     lin_arrive2<kCl>();
