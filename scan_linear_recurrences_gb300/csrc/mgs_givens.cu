@@ -115,9 +115,19 @@ __device__ __forceinline__ float recip_nr(float x) {
     return fmaf(r0, fmaf(-x, r0, 1.f), r0);
 }
 
+// kFast: the half angle's sine and cosine from the hardware approximation
+// (__sincosf, absolute error about 2^-21 on [-pi, pi]) instead of sincosf.
+// The construction keeps c^2 + s^2 - 1 unbiased either way; what the faster
+// form adds is an angle error near 1e-6 rad.  The gated affine scan contracts
+// it (|a| < 1), so it takes kFast; the matrix scans, a product of T orthogonal
+// meshes with nothing to contract the errors, keep sincosf.
+template <bool kFast = false>
 __device__ __forceinline__ void unbiased_cos_sin(float theta, float &c, float &s) {
     float sh, ch;
-    sincosf(0.5f * theta, &sh, &ch);
+    if constexpr (kFast)
+        __sincosf(0.5f * theta, &sh, &ch);
+    else
+        sincosf(0.5f * theta, &sh, &ch);
     // |cos| of the half angle: at least 2^-100 away from a pole (theta = pi
     // mod 2 pi gives |t| <= 1e30, where c = -1 and s = 0 to fp32 precision)
     const float ach = fmaxf(fabsf(ch), 1e-30f);
@@ -132,7 +142,7 @@ __device__ __forceinline__ void unbiased_cos_sin(float theta, float &c, float &s
 // consecutive words.
 // Four angles per thread and round are independent chains, which the
 // scheduler interleaves (one chain alone is a long run of dependent ops).
-template <int NP>
+template <int NP, bool kFast = false>
 __device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi, int pt) {
     constexpr int kProd = NP;
     int i = lo + pt;
@@ -141,7 +151,7 @@ __device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi
 #pragma unroll
         for (int q = 0; q < 4; ++q) x[q] = th[i + q * kProd];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) unbiased_cos_sin(x[q], c[q], s[q]);
+        for (int q = 0; q < 4; ++q) unbiased_cos_sin<kFast>(x[q], c[q], s[q]);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             th[i + q * kProd] = c[q];
@@ -150,7 +160,7 @@ __device__ __forceinline__ void angle_range(float *th, float *sn, int lo, int hi
     }
     for (; i < hi; i += kProd) {
         float c, s;
-        unbiased_cos_sin(th[i], c, s);
+        unbiased_cos_sin<kFast>(th[i], c, s);
         th[i] = c;
         sn[i] = s;
     }
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(kBlockF)
                     angle_range_ff<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, lo, lo + L.sin_f,
                                            0, hi, tid - 32, tabs);
                 } else {
-                    angle_range<kProdF>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0, hi, tid - 32);
+                    angle_range<kProdF, true>(ring + size_t(s) * L.stage_f, snb + (it & 1) * L.sin_f, 0, hi, tid - 32);
                 }
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
@@ -489,7 +499,7 @@ __global__ void __launch_bounds__(kBlockB)
                     angle_range_ff<kProdB>(st, sn, lo, lo + L.sin_f, first_row(it) * lpw * GN, ts * lpw * GN,
                                            tid - 32, tabs);
                 } else {
-                    angle_range<kProdB>(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
+                    angle_range<kProdB, true>(st, sn, first_row(it) * lpw * GN, ts * lpw * GN, tid - 32);
                 }
             } else {
                 if (lane == 0) record_error(ctl, ERR_MBAR_TIMEOUT);
@@ -899,11 +909,12 @@ struct GcStage {
 
 // The whole warp converts a landed stage's angles: cosines in place, sines
 // into the stage's sine area.
+template <bool kFast>
 __device__ __forceinline__ void gc_convert(float *st, int lane) {
     float *sn = st + kGcThF;
     for (int i = lane; i < kGcThF; i += 32) {
         float c, sv;
-        unbiased_cos_sin(st[i], c, sv);
+        unbiased_cos_sin<kFast>(st[i], c, sv);
         st[i] = c;
         sn[i] = sv;
     }
@@ -990,7 +1001,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<true>(st, lane);
         const int n = int(min64(kGcTS, w.len - j * kGcTS));
         for (int u = 0; u < n; ++u) {
             const int item = u * kGcLanes + w.sub;
@@ -1060,7 +1071,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<true>(st, lane);
         const int n = int(min64(kGcTS, w.len - j * kGcTS));
         for (int u = 0; u < n; ++u) {
             const int item = u * kGcLanes + w.sub;
@@ -1128,7 +1139,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<true>(st, lane);
         const int64_t tt = w.te - 1 - j * kGcTS;
         const int n = int(min64(kGcTS, tt - w.tb + 1));
         for (int u = 0; u < n; ++u) {
@@ -1205,7 +1216,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<true>(st, lane);
         const int64_t tt = w.te - 1 - j * kGcTS;
         const int n = int(min64(kGcTS, tt - w.tb + 1));
         for (int u = 0; u < n; ++u) {
@@ -1304,7 +1315,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<false>(st, lane);
         const int n = int(min64(kGcTS, w.len - j * kGcTS));
         for (int u = 0; u < n; ++u) {
             const int item = u * kGcLanes + w.sub;
@@ -1358,7 +1369,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<false>(st, lane);
         const int n = int(min64(kGcTS, w.len - j * kGcTS));
         for (int u = 0; u < n; ++u) {
             const int item = u * kGcLanes + w.sub;
@@ -1419,7 +1430,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<false>(st, lane);
         const int64_t tt = w.te - 1 - j * kGcTS;
         const int n = int(min64(kGcTS, tt - w.tb + 1));
         for (int u = 0; u < n; ++u) {
@@ -1487,7 +1498,7 @@ __global__ void __launch_bounds__(32)
         const int s = int(j % L::NS);
         MGS_GC_WAIT_OR_RETURN(rg, s);
         float *st = ring + size_t(s) * L::floats;
-        gc_convert(st, lane);
+        gc_convert<false>(st, lane);
         const int64_t tt = w.te - 1 - j * kGcTS;
         const int n = int(min64(kGcTS, tt - w.tb + 1));
         for (int u = 0; u < n; ++u) {
