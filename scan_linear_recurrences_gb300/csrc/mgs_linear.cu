@@ -15,11 +15,6 @@
 // entering its segment.  Each warp then walks its steps from its own entry
 // state.  No workspace; T <= S W L = 1024.
 //
-// parallel_scan_log runs up to T = 32768 with the *_mb_ kernels: the same
-// scheme with each warp holding R <= 32 blocks of L = 16 steps; the first walk
-// composes all of them (loading one block at a time), the second reads each
-// block again (from L2) as it reruns it.
-//
 // parallel_scan_log with few lanes runs on the same skeleton (the
 // "mingru-scans" home page, scan-op table, parallel_scan_log row, at its lab
 // and long-T shapes).  In base 2 (a = log_coeffs log2 e, v = log_values
@@ -30,7 +25,11 @@
 // step's own arithmetic is that of the one-warp-per-128-channels kernel.
 // Its backward is the linear recurrence lambda_t = g_t + a_{t+1} lambda_{t+1}
 // (a = exp(log_coeffs)), as above, with d_log_values = lambda_t exp(lv_t),
-// d_log_coeffs = a_t lambda_t h_{t-1}, d_log_h0 = a_0 lambda_0 h_0.
+// d_log_coeffs = a_t lambda_t h_{t-1}, d_log_h0 = a_0 lambda_0 h_0.  It
+// runs up to T = 32768 with the *_mb_ kernels at the end of this file: the
+// same scheme with each warp holding R <= 32 blocks of L = 16 steps; the
+// first walk composes all of them (loading one block at a time), the second
+// reads each block again (from L2) as it reruns it.
 #include <math_constants.h>
 
 #include "mgs_launch.h"
