@@ -442,25 +442,8 @@ __device__ __forceinline__ LinLane lin_lane(int64_t T, int64_t D, int64_t groups
 }
 
 // Block k of a warp's inputs into registers (steps past the block's end the
-// identity); returns the block's step count.  Plain functions with
-// restrict-qualified pointers, so the loads may be issued ahead of anything.
-
-// Block k of the log-space inputs (steps past the end the identity:
-// log_coeffs 0, log_values -inf); returns the block's step count.
-template <int L>
-__device__ __forceinline__ int psl_fwd_block(const float *__restrict__ lc, const float *__restrict__ lv,
-                                             const LinLane &q, int k, int64_t T, int64_t D, float (&cv)[L],
-                                             float (&vb)[L]) {
-    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
-    const int n = lin_steps_here(q.act, L, tk, T);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        cv[u] = u < n ? lc[base + u * D] : 0.f;
-        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
-    }
-    return n;
-}
-// The saved-h backward's block: a_t, exp(lv_t), g_t, h_{t-1} (h0, or zero,
+// identity; plain functions with restrict-qualified pointers, so the loads
+// may be issued ahead of anything).  The saved-h backward's block: a_t, exp(lv_t), g_t, h_{t-1} (h0, or zero,
 // before t = 0), and a after the block's last step (zero past the end:
 // lambda_T = 0) in *aft; steps past the end are the identity.  Without
 // kOut only what the map needs (a, g).
@@ -504,6 +487,26 @@ __device__ __forceinline__ int psl_rc_block(const float *__restrict__ lc, const 
     return n;
 }
 
+// Block k's raw log_coeffs and log_values (the conversion to base 2 waits
+// until the values are used, so that loading the next block while this one
+// is composed stalls nothing); returns the block's step count.
+template <int L>
+__device__ __forceinline__ int psl_raw_block(const float *__restrict__ lc, const float *__restrict__ lv,
+                                             const LinLane &q, int k, int64_t T, int64_t D, float (&cv)[L],
+                                             float (&vr)[L]) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        cv[u] = u < n ? lc[base + u * D] : 0.f;
+        vr[u] = u < n ? lv[base + u * D] : -CUDART_INF_F;
+    }
+    return n;
+}
+
+// The blocks are double-buffered: block k+1's loads are issued before block
+// k is walked (the loop goes two blocks at a time so that the buffers are
+// fixed registers).
 template <int L>
 __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
     psl_fwd_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
@@ -512,17 +515,22 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     __shared__ LinSmem sm;
     const LinLane q = lin_lane<L>(T, D, groups, S, R);
     const int lane = q.lane, w = q.w;
-    const int RR = R;
-    float cv[L], vb[L];
-    auto load = [&](int k) { return psl_fwd_block<L>(lc, lv, q, k, T, D, cv, vb); };
+    float cv0[L], vr0[L], cv1[L], vr1[L];
     float A = 0.f, V = -CUDART_INF_F;
-    int n = 0;
-    for (int k = 0; k < RR; ++k) {
-        n = load(k);
+    auto compose = [&](const float (&cv)[L], const float (&vr)[L]) {
 #pragma unroll
         for (int u = 0; u < L; ++u) {
-            V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
+            V = lae2(fmaf(cv[u], kLog2e, V), vr[u] * kLog2e);
             A = fmaf(cv[u], kLog2e, A);
+        }
+    };
+    psl_raw_block<L>(lc, lv, q, 0, T, D, cv0, vr0);
+    for (int k = 0; k < R; k += 2) {
+        if (k + 1 < R) psl_raw_block<L>(lc, lv, q, k + 1, T, D, cv1, vr1);
+        compose(cv0, vr0);
+        if (k + 1 < R) {
+            if (k + 2 < R) psl_raw_block<L>(lc, lv, q, k + 2, T, D, cv0, vr0);
+            compose(cv1, vr1);
         }
     }
     sm.m[w][lane] = A;
@@ -535,16 +543,24 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     for (unsigned p = 0; p < q.r; ++p) x = lae2(ld_dsmem(&sm.tm[lane], p) + x, ld_dsmem(&sm.tc[lane], p));
     lin_arrive2<true>();
     x = lae2(sm.pm[w][lane] + x, sm.pc[w][lane]);
-    for (int k = 0; k < RR; ++k) {
-        n = load(k);
+    auto walk = [&](int k, int n, const float (&cv)[L], const float (&vr)[L]) {
         const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
 #pragma unroll
         for (int u = 0; u < L; ++u) {
-            x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
+            x = lae2(fmaf(cv[u], kLog2e, x), vr[u] * kLog2e);
             if (u < n) {
                 __stcs(h + base + u * D, ex2_approx(x));
                 if (logh != nullptr) __stcs(logh + base + u * D, x * kLn2);
             }
+        }
+    };
+    int n0 = psl_raw_block<L>(lc, lv, q, 0, T, D, cv0, vr0), n1 = 0;
+    for (int k = 0; k < R; k += 2) {
+        if (k + 1 < R) n1 = psl_raw_block<L>(lc, lv, q, k + 1, T, D, cv1, vr1);
+        walk(k, n0, cv0, vr0);
+        if (k + 1 < R) {
+            if (k + 2 < R) n0 = psl_raw_block<L>(lc, lv, q, k + 2, T, D, cv0, vr0);
+            walk(k + 1, n1, cv1, vr1);
         }
     }
     lin_wait2<true>();
