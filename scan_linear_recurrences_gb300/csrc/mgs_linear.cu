@@ -27,9 +27,10 @@
 // (a = exp(log_coeffs)), as above, with d_log_values = lambda_t exp(lv_t),
 // d_log_coeffs = a_t lambda_t h_{t-1}, d_log_h0 = a_0 lambda_0 h_0.  It
 // runs up to T = 32768 with the *_mb_ kernels at the end of this file: the
-// same scheme with each warp holding R <= 32 blocks of L = 16 steps; the
-// first walk composes all of them (loading one block at a time), the second
-// reads each block again (from L2) as it reruns it.
+// same scheme with each warp holding R blocks of L = 16 (forward) or 8
+// (backwards) steps; the first walk composes all of them, the second reads
+// each block again (from L2) as it reruns it, both loading the next block
+// while one is worked on.
 #include <math_constants.h>
 
 #include "mgs_launch.h"
@@ -42,8 +43,7 @@ namespace {
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
 constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;  // one block a warp
-constexpr int kLinMaxBlocks = 32;                                          // R at most
-constexpr int64_t kLinMaxTBlocks = kLinMaxT * kLinMaxBlocks;
+constexpr int64_t kLinMaxTBlocks = 32768;  // several blocks a warp: R <= 64 blocks of 8 steps or 32 of 16
 
 struct LinSmem {
     float m[kLinWarps][32], c[kLinWarps][32];    // each warp's map
@@ -441,55 +441,11 @@ __device__ __forceinline__ LinLane lin_lane(int64_t T, int64_t D, int64_t groups
     return q;
 }
 
-// Block k of a warp's inputs into registers (steps past the block's end the
-// identity; plain functions with restrict-qualified pointers, so the loads
-// may be issued ahead of anything).  The saved-h backward's block: a_t, exp(lv_t), g_t, h_{t-1} (h0, or zero,
-// before t = 0), and a after the block's last step (zero past the end:
-// lambda_T = 0) in *aft; steps past the end are the identity.  Without
-// kOut only what the map needs (a, g).
-template <int L, bool kOut>
-__device__ __forceinline__ int psl_bwd_block(const float *__restrict__ lc, const float *__restrict__ lv,
-                                             const float *__restrict__ h, const float *__restrict__ g,
-                                             const LinLane &q, int k, int64_t T, int64_t D, float h0v, float (&at)[L],
-                                             float (&ev)[L], float (&gv)[L], float (&hp)[L], float *aft) {
-    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
-    const int n = lin_steps_here(q.act, L, tk, T);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        at[u] = u < n ? ex2_approx(lc[base + u * D] * kLog2e) : 1.f;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-        if constexpr (kOut) {
-            ev[u] = u < n ? ex2_approx(lv[base + u * D] * kLog2e) : 0.f;
-            hp[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
-        }
-    }
-    *aft = (n > 0 && tk + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
-    return n;
-}
-// The recompute-mode backward's block: log_coeffs, log_values (base 2), g,
-// a = exp(log_coeffs) and a after the block (in *aft).
-template <int L>
-__device__ __forceinline__ int psl_rc_block(const float *__restrict__ lc, const float *__restrict__ lv,
-                                            const float *__restrict__ g, const LinLane &q, int k, int64_t T,
-                                            int64_t D, float (&cv)[L], float (&vb)[L], float (&gv)[L], float (&at)[L],
-                                            float *aft) {
-    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
-    const int n = lin_steps_here(q.act, L, tk, T);
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        cv[u] = u < n ? lc[base + u * D] : 0.f;
-        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < L; ++u) at[u] = u < n ? ex2_approx(cv[u] * kLog2e) : 1.f;
-    *aft = (n > 0 && tk + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
-    return n;
-}
-
-// Block k's raw log_coeffs and log_values (the conversion to base 2 waits
-// until the values are used, so that loading the next block while this one
-// is composed stalls nothing); returns the block's step count.
+// Block k's raw log_coeffs and log_values into registers (steps past the
+// block's end the identity; a plain function with restrict-qualified
+// pointers, so the loads may be issued ahead of anything; the conversion to
+// base 2 waits until the values are used, so that loading the next block
+// while this one is composed stalls nothing); returns the block's step count.
 template <int L>
 __device__ __forceinline__ int psl_raw_block(const float *__restrict__ lc, const float *__restrict__ lv,
                                              const LinLane &q, int k, int64_t T, int64_t D, float (&cv)[L],
@@ -566,6 +522,30 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     lin_wait2<true>();
 }
 
+// A backward's raw block: log_coeffs, g and the log_coeffs after the block
+// (in *lca), with kLv log_values, with kH h_{t-1} (h0, or zero, before
+// t = 0); pads give a = 1, exp(lv) = 0, g = 0.  h is read only with kH.
+template <int L, bool kLv, bool kH>
+__device__ __forceinline__ int psl_bwd_raw(const float *__restrict__ lc, const float *__restrict__ lv,
+                                           const float *__restrict__ h, const float *__restrict__ g, const LinLane &q,
+                                           int k, int64_t T, int64_t D, float h0v, float (&lcr)[L], float (&lvr)[L],
+                                           float (&gr)[L], float (&hr)[L], float *lca) {
+    const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
+    const int n = lin_steps_here(q.act, L, tk, T);
+#pragma unroll
+    for (int u = 0; u < L; ++u) {
+        lcr[u] = u < n ? lc[base + u * D] : 0.f;
+        gr[u] = u < n ? g[base + u * D] : 0.f;
+        if constexpr (kLv) lvr[u] = u < n ? lv[base + u * D] : -CUDART_INF_F;
+        if constexpr (kH) hr[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
+    }
+    *lca = (n > 0 && tk + n < T) ? lc[base + n * D] : -CUDART_INF_F;
+    return n;
+}
+
+// The saved-h backward with the blocks double-buffered as in the forward
+// (raw inputs of the next block loaded while a block is walked; 8-step
+// blocks, so that two buffers of four inputs fit the registers).
 template <int L>
 __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
     psl_bwd_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
@@ -575,22 +555,38 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     __shared__ LinSmem sm;
     const LinLane q = lin_lane<L>(T, D, groups, S, R);
     const int lane = q.lane, w = q.w;
-    const int RR = R;
     const float h0v = (lh0 != nullptr && q.act) ? ex2_approx(lh0[q.bi * D + q.ch] * kLog2e) : 0.f;
-    float at[L], ev[L], gv[L], hp[L], aft = 0.f;
-    int n = 0;
-    // the first pass needs only a and g when the second loads the blocks again
-    auto load_map = [&](int k) { n = psl_bwd_block<L, false>(lc, lv, h, g, q, k, T, D, h0v, at, ev, gv, hp, &aft); };
-    auto load = [&](int k) { n = psl_bwd_block<L, true>(lc, lv, h, g, q, k, T, D, h0v, at, ev, gv, hp, &aft); };
-    // step u's coefficient a_{t+1}
-    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
+    float lc0[L], lv0[L], g0[L], h0r[L], lc1[L], lv1[L], g1[L], h1r[L], lca0 = 0.f, lca1 = 0.f;
+    int n0 = 0, n1 = 0;
+    // a of a block's steps and a after it; step u's coefficient a_{t+1}
+    auto coefs = [&](const float (&lcr)[L], float lca, int n, float (&cf)[L], float (&at)[L]) {
+#pragma unroll
+        for (int u = 0; u < L; ++u) at[u] = ex2_approx(lcr[u] * kLog2e);
+        const float aft = ex2_approx(lca * kLog2e);
+#pragma unroll
+        for (int u = 0; u < L; ++u) cf[u] = u + 1 < n ? at[u + 1 < L ? u + 1 : L - 1] : (u + 1 == n ? aft : 1.f);
+    };
     float m = 1.f, c = 0.f;
-    for (int k = RR - 1; k >= 0; --k) {
-        load_map(k);
+    auto compose = [&](const float (&lcr)[L], const float (&gr)[L], float lca, int n) {
+        float cf[L], at[L];
+        coefs(lcr, lca, n, cf, at);
 #pragma unroll
         for (int u = L - 1; u >= 0; --u) {
-            c = fmaf(coef(u), c, gv[u]);
-            m *= coef(u);
+            c = fmaf(cf[u], c, gr[u]);
+            m *= cf[u];
+        }
+    };
+    auto load_map = [&](int k, float (&lcr)[L], float (&gr)[L], float (&lvr)[L], float (&hr)[L], float *lca) {
+        return psl_bwd_raw<L, false, false>(lc, lv, h, g, q, k, T, D, h0v, lcr, lvr, gr, hr, lca);
+    };
+    // blocks R-1 .. 0, two at a time
+    n0 = load_map(R - 1, lc0, g0, lv0, h0r, &lca0);
+    for (int k = R - 1; k >= 0; k -= 2) {
+        if (k >= 1) n1 = load_map(k - 1, lc1, g1, lv1, h1r, &lca1);
+        compose(lc0, g0, lca0, n0);
+        if (k >= 1) {
+            if (k >= 2) n0 = load_map(k - 2, lc0, g0, lv0, h0r, &lca0);
+            compose(lc1, g1, lca1, n1);
         }
     }
     sm.m[w][lane] = m;
@@ -600,68 +596,93 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     lin_sync1<true>();
     float x = 0.f;  // lambda past this CTA's segment
     for (int p = S - 1; p > int(q.r); --p)
-            x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(p)), x, ld_dsmem(&sm.tc[lane], unsigned(p)));
+        x = fmaf(ld_dsmem(&sm.tm[lane], unsigned(p)), x, ld_dsmem(&sm.tc[lane], unsigned(p)));
     lin_arrive2<true>();
     float lam = fmaf(sm.pm[w][lane], x, sm.pc[w][lane]);
-    for (int k = RR - 1; k >= 0; --k) {
-        load(k);
+    auto walk = [&](int k, int n, const float (&lcr)[L], const float (&lvr)[L], const float (&gr)[L],
+                    const float (&hr)[L], float lca) {
+        float cf[L], at[L];
+        coefs(lcr, lca, n, cf, at);
         const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
 #pragma unroll
         for (int u = L - 1; u >= 0; --u) {
-            lam = fmaf(coef(u), lam, gv[u]);
+            lam = fmaf(cf[u], lam, gr[u]);
             if (u < n) {
-                __stcs(dlv + base + u * D, lam * ev[u]);
-                __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+                __stcs(dlv + base + u * D, lam * ex2_approx(lvr[u] * kLog2e));
+                __stcs(dlc + base + u * D, at[u] * lam * hr[u]);
             }
         }
+        // lam is lambda_0 at block 0 of the first warp of the first CTA
+        if (k == 0 && q.r == 0 && w == 0 && q.act && dlh0 != nullptr) dlh0[q.bi * D + q.ch] = at[0] * lam * h0v;
+    };
+    auto load = [&](int k, float (&lcr)[L], float (&lvr)[L], float (&gr)[L], float (&hr)[L], float *lca) {
+        return psl_bwd_raw<L, true, true>(lc, lv, h, g, q, k, T, D, h0v, lcr, lvr, gr, hr, lca);
+    };
+    n0 = load(R - 1, lc0, lv0, g0, h0r, &lca0);
+    for (int k = R - 1; k >= 0; k -= 2) {
+        if (k >= 1) n1 = load(k - 1, lc1, lv1, g1, h1r, &lca1);
+        walk(k, n0, lc0, lv0, g0, h0r, lca0);
+        if (k >= 1) {
+            if (k >= 2) n0 = load(k - 2, lc0, lv0, g0, h0r, &lca0);
+            walk(k - 1, n1, lc1, lv1, g1, h1r, lca1);
+        }
     }
-    // lam is lambda_0 in the first warp of the first CTA
-    if (q.r == 0 && w == 0 && q.act && dlh0 != nullptr) dlh0[q.bi * D + q.ch] = at[0] * lam * h0v;
     lin_wait2<true>();
 }
 
-// Backward without the saved h (the pages' log-space op recomputes its
-// forward): both recurrences' maps are composed in the first pass (the
-// forward's from log_coeffs and log_values, the backward's from a and g, none
-// of them needs h), both carries cross the CTA and the cluster together, and
-// each warp then reruns its forward steps from its entering state, keeping
-// h_{t-1} in registers (R > 1: the state entering each block in shared
-// memory, each block's h rebuilt from it), before walking its backward
-// steps.  h is never stored and no workspace is used.  The maps compose in
-// the order the other two kernels use, so the results equal the saved-h
-// backward's bit for bit.
+// The recompute-mode backward with several blocks a warp, in two passes over
+// the blocks, each double-buffered as above.  The first (left to right)
+// composes the forward's log-space map and the backward's affine map
+// (lambda_first = m lambda_after + c, extended a step at a time on the
+// right: c += m g_t, m *= a_{t+1}) and keeps, per block, the forward map of
+// the warp's blocks before it in dynamic shared memory (2 R floats a
+// thread).  The second (right to left) turns that map and the state entering
+// the warp into the block's entering state, rebuilds the block's h_{t-1} in
+// registers and walks the backward through it.
 template <int L>
 __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
     psl_bwd_rc_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
                          const float *__restrict__ g, float *__restrict__ dlc, float *__restrict__ dlv,
                          float *__restrict__ dlh0, int64_t T, int64_t D, int64_t groups, int S, int R) {
-    __shared__ LinSmem fm, bm;                           // the forward's maps, the backward's
-    __shared__ float xs[kLinMaxBlocks][32 * kLinWarps];  // log2 h entering each block
+    __shared__ LinSmem fm, bm;  // the forward's maps, the backward's
+    extern __shared__ float pre[];  // [R][256] A then [R][256] V of the blocks before each block
+    float *preA = pre, *preV = pre + size_t(R) * (32 * kLinWarps);
     const LinLane q = lin_lane<L>(T, D, groups, S, R);
-    const int lane = q.lane, w = q.w;
-    const int RR = R;
+    const int lane = q.lane, w = q.w, tid = threadIdx.x;
     const float l0 = (lh0 != nullptr && q.act) ? lh0[q.bi * D + q.ch] * kLog2e : -CUDART_INF_F;
-    float cv[L], vb[L], gv[L], at[L], aft = 0.f;
-    int n = 0;
-    auto load = [&](int k) { n = psl_rc_block<L>(lc, lv, g, q, k, T, D, cv, vb, gv, at, &aft); };
-    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
-    // forward map left to right, backward map right to left (block R-1 is
-    // still loaded after the first loop)
+    float lc0[L], lv0[L], g0[L], lc1[L], lv1[L], g1[L], hd[L], lca0 = 0.f, lca1 = 0.f;
+    int n0 = 0, n1 = 0;
+    auto coefs = [&](const float (&lcr)[L], float lca, int n, float (&cf)[L], float (&at)[L]) {
+#pragma unroll
+        for (int u = 0; u < L; ++u) at[u] = ex2_approx(lcr[u] * kLog2e);
+        const float aft = ex2_approx(lca * kLog2e);
+#pragma unroll
+        for (int u = 0; u < L; ++u) cf[u] = u + 1 < n ? at[u + 1 < L ? u + 1 : L - 1] : (u + 1 == n ? aft : 1.f);
+    };
+    auto load = [&](int k, float (&lcr)[L], float (&lvr)[L], float (&gr)[L], float *lca) {
+        return psl_bwd_raw<L, true, false>(lc, lv, nullptr, g, q, k, T, D, 0.f, lcr, lvr, gr, hd, lca);
+    };
     float A = 0.f, V = -CUDART_INF_F, m = 1.f, c = 0.f;
-    for (int k = 0; k < RR; ++k) {
-        load(k);
+    auto compose = [&](int k, const float (&lcr)[L], const float (&lvr)[L], const float (&gr)[L], float lca, int n) {
+        preA[size_t(k) * (32 * kLinWarps) + tid] = A;
+        preV[size_t(k) * (32 * kLinWarps) + tid] = V;
+        float cf[L], at[L];
+        coefs(lcr, lca, n, cf, at);
 #pragma unroll
         for (int u = 0; u < L; ++u) {
-            V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
-            A = fmaf(cv[u], kLog2e, A);
+            V = lae2(fmaf(lcr[u], kLog2e, V), lvr[u] * kLog2e);
+            A = fmaf(lcr[u], kLog2e, A);
+            c = fmaf(m, gr[u], c);
+            m *= cf[u];
         }
-    }
-    for (int k = RR - 1; k >= 0; --k) {
-        if (k != RR - 1) load(k);
-#pragma unroll
-        for (int u = L - 1; u >= 0; --u) {
-            c = fmaf(coef(u), c, gv[u]);
-            m *= coef(u);
+    };
+    n0 = load(0, lc0, lv0, g0, &lca0);
+    for (int k = 0; k < R; k += 2) {
+        if (k + 1 < R) n1 = load(k + 1, lc1, lv1, g1, &lca1);
+        compose(k, lc0, lv0, g0, lca0, n0);
+        if (k + 1 < R) {
+            if (k + 2 < R) n0 = load(k + 2, lc0, lv0, g0, &lca0);
+            compose(k + 1, lc1, lv1, g1, lca1, n1);
         }
     }
     fm.m[w][lane] = A;
@@ -679,37 +700,39 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     for (int p = S - 1; p > int(q.r); --p)
         y = fmaf(ld_dsmem(&bm.tm[lane], unsigned(p)), y, ld_dsmem(&bm.tc[lane], unsigned(p)));
     lin_arrive2<true>();
-    x = lae2(fm.pm[w][lane] + x, fm.pc[w][lane]);
-    xs[0][threadIdx.x] = x;
-    for (int k = 0; k + 1 < RR; ++k) {  // the state entering each later block
-        load(k);
-#pragma unroll
-        for (int u = 0; u < L; ++u) x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
-        xs[k + 1][threadIdx.x] = x;
-    }
+    x = lae2(fm.pm[w][lane] + x, fm.pc[w][lane]);  // log2 h entering the warp's segment
     float lam = fmaf(bm.pm[w][lane], y, bm.pc[w][lane]);
-    for (int k = RR - 1; k >= 0; --k) {
-        load(k);
+    auto walk = [&](int k, int n, const float (&lcr)[L], const float (&lvr)[L], const float (&gr)[L], float lca) {
         // the forward over this block: h_{t-1} of each step (h0, or zero, before t = 0)
-        float hp[L];
-        float xk = xs[k][threadIdx.x];
+        float xk = k == 0 ? x
+                          : lae2(preA[size_t(k) * (32 * kLinWarps) + tid] + x, preV[size_t(k) * (32 * kLinWarps) + tid]);
+        float hp[L], cf[L], at[L];
 #pragma unroll
         for (int u = 0; u < L; ++u) {
             hp[u] = ex2_approx(xk);
-            xk = lae2(fmaf(cv[u], kLog2e, xk), vb[u]);
+            xk = lae2(fmaf(lcr[u], kLog2e, xk), lvr[u] * kLog2e);
         }
+        coefs(lcr, lca, n, cf, at);
         const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
 #pragma unroll
         for (int u = L - 1; u >= 0; --u) {
-            lam = fmaf(coef(u), lam, gv[u]);
+            lam = fmaf(cf[u], lam, gr[u]);
             if (u < n) {
-                __stcs(dlv + base + u * D, lam * ex2_approx(vb[u]));
+                __stcs(dlv + base + u * D, lam * ex2_approx(lvr[u] * kLog2e));
                 __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
             }
         }
         // lam is lambda_0 and hp[0] is h0 at block 0 of the first warp of the first CTA
-        if (k == 0 && q.r == 0 && w == 0 && q.act && dlh0 != nullptr)
-            dlh0[q.bi * D + q.ch] = at[0] * lam * hp[0];
+        if (k == 0 && q.r == 0 && w == 0 && q.act && dlh0 != nullptr) dlh0[q.bi * D + q.ch] = at[0] * lam * hp[0];
+    };
+    n0 = load(R - 1, lc0, lv0, g0, &lca0);
+    for (int k = R - 1; k >= 0; k -= 2) {
+        if (k >= 1) n1 = load(k - 1, lc1, lv1, g1, &lca1);
+        walk(k, n0, lc0, lv0, g0, lca0);
+        if (k >= 1) {
+            if (k >= 2) n0 = load(k - 2, lc0, lv0, g0, &lca0);
+            walk(k - 1, n1, lc1, lv1, g1, lca1);
+        }
     }
     lin_wait2<true>();
 }
@@ -725,17 +748,24 @@ LinPlan lin_plan(int64_t T) {
     return p;
 }
 
-// T in (1024, 32768]: R blocks of 16 steps a warp, S CTAs a cluster.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_mb(void (*kern)(KArgs...), int64_t B, int64_t T, int64_t D, cudaStream_t s, Args... args) {
+// T in (1024, 32768]: R blocks of L steps a warp, S CTAs a cluster, and
+// smem_per_block bytes of dynamic shared memory a CTA for each of the R.
+template <int L, typename... KArgs, typename... Args>
+cudaError_t launch_mb(void (*kern)(KArgs...), size_t smem_per_block, int64_t B, int64_t T, int64_t D,
+                      cudaStream_t s, Args... args) {
     if (T > kLinMaxTBlocks) return cudaErrorInvalidConfiguration;
-    const int64_t groups = (D + 31) / 32, cta_steps = int64_t(16) * kLinWarps;
+    const int64_t groups = (D + 31) / 32, cta_steps = int64_t(L) * kLinWarps;
     const int R = int((T + cta_steps * kLinMaxCta - 1) / (cta_steps * kLinMaxCta));
     const int S = int((T + cta_steps * R - 1) / (cta_steps * R));
     const int64_t blocks = B * groups * S;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     if (blocks == 0) return cudaSuccess;
-    return launch_cluster(kern, blocks, 32 * kLinWarps, 0, S, s, args..., T, D, groups, S, R);
+    const size_t smem = smem_per_block * size_t(R);
+    if (smem > 48 * 1024) {  // past the default limit (at most 128 KB: R <= 64)
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_cluster(kern, blocks, 32 * kLinWarps, smem, S, s, args..., T, D, groups, S, R);
 }
 
 }  // namespace
@@ -783,7 +813,7 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
 
 cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
                               int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb(psl_fwd_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, h, logh);
+    if (T > kLinMaxT) return launch_mb<16>(psl_fwd_cl_mb_kernel<16>, 0, B, T, D, s, lc, lv, lh0, h, logh);
     const int64_t groups = (D + 31) / 32;
     if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
@@ -800,7 +830,7 @@ cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0
 
 cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0, const float *h, const float *g,
                               float *dlc, float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb(psl_bwd_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, h, g, dlc, dlv, dlh0);
+    if (T > kLinMaxT) return launch_mb<8>(psl_bwd_cl_mb_kernel<8>, 0, B, T, D, s, lc, lv, lh0, h, g, dlc, dlv, dlh0);
     const int64_t groups = (D + 31) / 32;
     if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
@@ -817,7 +847,9 @@ cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0
 
 cudaError_t launch_psl_bwd_rc_cl(const float *lc, const float *lv, const float *lh0, const float *g, float *dlc,
                                  float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb(psl_bwd_rc_cl_mb_kernel<16>, B, T, D, s, lc, lv, lh0, g, dlc, dlv, dlh0);
+    if (T > kLinMaxT)
+        return launch_mb<8>(psl_bwd_rc_cl_mb_kernel<8>, 2 * sizeof(float) * 32 * kLinWarps, B, T, D, s, lc, lv, lh0, g,
+                            dlc, dlv, dlh0);
     const int64_t groups = (D + 31) / 32;
     if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);

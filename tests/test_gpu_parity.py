@@ -328,7 +328,7 @@ def test_psl_zero_coefficients_and_empty():
     # the pages' long-T and lab shapes, on the one-launch cluster path (one
     # and several blocks a warp)
     (16, 1024, 64, True), (128, 64, 64, False), (2, 600, 12, True), (2, 2500, 36, True), (1, 8192, 8, False),
-    (1, 30000, 4, True),
+    (1, 30000, 4, True), (2, 1025, 40, True), (1, 32768, 8, True),
     # 2048 channel groups, ragged last segment: the checkpointing kernel
     (64, 33, 1024, True),
 ])
