@@ -126,7 +126,9 @@ def test_guard_matrix_scan(B, T, H, k):
 # ---------------------------------------------------------------- parallel_scan_log (saved h and recompute)
 @pytest.mark.parametrize("B,T,D", [(3, 50, 132), (5, 33, 36), (2, 257, 1024), (2, 17, 8),
                                    # several blocks a warp; 2048 channel groups (one warp per 128 channels)
-                                   (2, 1500, 36), (64, 20, 1024)])
+                                   (2, 1500, 36), (64, 20, 1024),
+                                   # 40 blocks a warp: the recompute backward's 80 KB of dynamic shared memory
+                                   (1, 20000, 12)])
 def test_guard_parallel_scan_log(B, T, D):
     d = _cuda(inputs.psl_inputs(B, T, D, seed=51 + T + D, with_h0=True))
     h, lh = Guarded("h", (B, T, D)), Guarded("log_h", (B, T, D))
@@ -144,7 +146,8 @@ def test_guard_parallel_scan_log(B, T, D):
 
 
 # ---------------------------------------------------------------- linear_scan
-@pytest.mark.parametrize("B,T,D", [(3, 77, 132), (1, 2000, 32), (2, 45, 4), (64, 30, 1024)])
+@pytest.mark.parametrize("B,T,D", [(3, 77, 132), (1, 2000, 32), (2, 45, 4), (64, 30, 1024), (1, 20000, 12),
+                                   (1, 33000, 4)])
 def test_guard_linear_scan(B, T, D):
     d = _cuda(inputs.linear_inputs(B, T, D, seed=61 + T + D))
     h = Guarded("h", (B, T, D))

@@ -66,6 +66,8 @@ def test_mas_configs_full(cid):
     (96, 200, 11, 8, "none"), (300, 90, 7, 4, "normal"), (64, 1100, 16, 8, "normal"),
     # few lanes, long sequences: the time-chunked path
     (1, 1000, 3, 16, "normal"), (2, 515, 5, 4, "normal"), (1, 2048, 8, 8, "none"), (3, 4099, 2, 2, "normal"),
+    # k = 1, few lanes, past the one-launch path's T = 1024: time chunks
+    (2, 5000, 40, 1, "normal"), (1, 40000, 8, 1, "none"),
 ])
 def test_mas_shapes(B, T, H, k, h0):
     _run_mas(B, T, H, k, seed=100 + B * T + H + k, h0_mode=h0)
@@ -402,7 +404,7 @@ def test_psl_recompute_autograd_and_T0():
     # T = 512, the three-launch chunked path past T = 1024, and 2048 channel
     # groups
     (3, 512, 36, True), (2, 513, 20, False), (1, 1024, 8, False), (1, 1025, 8, True),
-    (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
+    (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True), (1, 32768, 8, True), (1, 32769, 4, False),
     (63, 40, 1024, True), (64, 40, 1024, True),
 ])
 def test_linear_scan(B, T, D, h0):
