@@ -218,7 +218,8 @@ mgs_status mgs_parallel_scan_log_fwd(const float *log_coeffs, const float *log_v
  * MGS_ERR_WORKSPACE), reads log_coeffs and log_values twice, and gives the
  * same results as passing the h this library's forward wrote.  On the
  * time-parallel path (the forward's condition above) h is recomputed in
- * registers instead and the workspace, still required at that size, is not
+ * registers instead (the gradients then equal the saved-h call's up to
+ * rounding) and the workspace, still required at that size, is not
  * touched. */
 mgs_status mgs_parallel_scan_log_bwd(const float *log_coeffs, const float *log_values,
                                      const float *log_h0, const float *h, const float *grad_h,
