@@ -276,8 +276,9 @@ def _check_psl(d, T, rows=None):
 @pytest.mark.parametrize("B,T,D,h0", [
     (2, 1, 4, True), (3, 50, 132, True), (2, 257, 1024, True), (2, 100, 260, False), (1, 2000, 128, True),
     # the pages' lab and long-T shapes (one-launch time-parallel path), and
-    # the edges of that path: 8 -> 16 steps a block past T = 512, 1 -> 2
-    # blocks a warp past T = 1024, its end at T = 32768, 2048 channel groups
+    # the edges of that path: 8 -> 16 steps a block past T = 512, one ->
+    # several blocks a warp past T = 1024 (odd block counts, ragged last
+    # blocks), its end at T = 32768, 2048 channel groups
     (128, 64, 64, True), (16, 1024, 64, True), (3, 512, 20, True), (2, 513, 20, False),
     (1, 1024, 8, False), (1, 1025, 8, True), (2, 3000, 20, True), (1, 8192, 64, False), (1, 8193, 8, True),
     (1, 32768, 8, True), (1, 32769, 4, False),
