@@ -30,7 +30,8 @@
 // same scheme with each warp holding R blocks of L = 16 (forward) or 8
 // (backwards) steps; the first walk composes all of them, the second reads
 // each block again (from L2) as it reruns it, both loading the next block
-// while one is worked on.
+// while one is worked on.  The backward without the saved h always runs
+// there, whatever T.
 #include <math_constants.h>
 
 #include "mgs_launch.h"
@@ -330,93 +331,11 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     lin_wait2<kCl>();
 }
 
-// Backward without the saved h (the pages' log-space op recomputes its
-// forward): both recurrences' maps are composed in the first pass (the
-// forward's from log_coeffs and log_values, the backward's from a and g, none
-// of them needs h), both carries cross the CTA and the cluster together, and
-// each warp then reruns its forward steps from its entering state, keeping
-// h_{t-1} in registers, before walking its backward steps.  h is never
-// stored and no workspace is used.
-template <int L, bool kCl>
-__global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
-    psl_bwd_rc_cl_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
-                         const float *__restrict__ g, float *__restrict__ dlc, float *__restrict__ dlv,
-                         float *__restrict__ dlh0, int64_t T, int64_t D, int64_t groups, int S) {
-    __shared__ LinSmem fm, bm;  // the forward's maps, the backward's
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const unsigned r = kCl ? cluster_rank() : 0u;
-    const int64_t lg = blockIdx.x / S, bi = lg / groups;
-    const int64_t ch = (lg - bi * groups) * 32 + lane;
-    const bool act = ch < D;
-    const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
-    const int n = lin_steps_here(act, L, t0, T);
-    const int64_t base = (bi * T + t0) * D + ch;
-    const float l0 = (lh0 != nullptr && act) ? lh0[bi * D + ch] * kLog2e : -CUDART_INF_F;
-    float cv[L], vb[L], gv[L], at[L];
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        cv[u] = u < n ? lc[base + u * D] : 0.f;
-        vb[u] = u < n ? lv[base + u * D] * kLog2e : -CUDART_INF_F;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-    }
-    const float aft = (n > 0 && t0 + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
-#pragma unroll
-    for (int u = 0; u < L; ++u) at[u] = u < n ? ex2_approx(cv[u] * kLog2e) : 1.f;
-    auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
-    float A = 0.f, V = -CUDART_INF_F, m = 1.f, c = 0.f;
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        V = lae2(fmaf(cv[u], kLog2e, V), vb[u]);
-        A = fmaf(cv[u], kLog2e, A);
-    }
-#pragma unroll
-    for (int u = L - 1; u >= 0; --u) {
-        c = fmaf(coef(u), c, gv[u]);
-        m *= coef(u);
-    }
-    fm.m[w][lane] = A;
-    fm.c[w][lane] = V;
-    bm.m[w][lane] = m;
-    bm.c[w][lane] = c;
-    __syncthreads();
-    if (w == 0) {
-        psl_cta_offsets(fm, lane);
-        lin_cta_offsets<true>(bm, lane);
-    }
-    lin_sync1<kCl>();
-    float x = l0, y = 0.f;  // log2 h entering the CTA's segment, lambda past it
-    if constexpr (kCl) {
-        for (unsigned q = 0; q < r; ++q) x = lae2(ld_dsmem(&fm.tm[lane], q) + x, ld_dsmem(&fm.tc[lane], q));
-        for (int q = S - 1; q > int(r); --q)
-            y = fmaf(ld_dsmem(&bm.tm[lane], unsigned(q)), y, ld_dsmem(&bm.tc[lane], unsigned(q)));
-    }
-    lin_arrive2<kCl>();
-    // the forward over this warp's steps: h_{t-1} of each (h0, or zero, before t = 0)
-    x = lae2(fm.pm[w][lane] + x, fm.pc[w][lane]);
-    float hp[L];
-#pragma unroll
-    for (int u = 0; u < L; ++u) {
-        hp[u] = ex2_approx(x);
-        x = lae2(fmaf(cv[u], kLog2e, x), vb[u]);
-    }
-    float lam = fmaf(bm.pm[w][lane], y, bm.pc[w][lane]);
-#pragma unroll
-    for (int u = L - 1; u >= 0; --u) {
-        lam = fmaf(coef(u), lam, gv[u]);
-        if (u < n) {
-            __stcs(dlv + base + u * D, lam * ex2_approx(vb[u]));
-            __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
-        }
-    }
-    // lam is lambda_0 and hp[0] is h0 in the first warp of the first CTA
-    if (r == 0 && w == 0 && act && dlh0 != nullptr) dlh0[bi * D + ch] = at[0] * lam * hp[0];
-    lin_wait2<kCl>();
-}
-
 // ---------------------------------------------------------------- several blocks a warp
-// The kernels above with each warp holding R blocks of L steps (always a
-// cluster of several CTAs: T > 1024).  Kept apart from the one-block kernels,
-// whose inputs stay in registers between the two walks.
+// The kernels above with each warp holding R blocks of L steps, always
+// launched as a cluster (of one CTA too, for short sequences in the
+// recompute backward).  Kept apart from the one-block kernels, whose inputs
+// stay in registers between the two walks.
 // Where a thread's work lies: its channel's offset `cb` in a [B][T][D]
 // tensor (element t at cb + t D), whether the channel exists, and the first
 // step of its warp's R blocks.
@@ -748,7 +667,7 @@ LinPlan lin_plan(int64_t T) {
     return p;
 }
 
-// T in (1024, 32768]: R blocks of L steps a warp, S CTAs a cluster, and
+// T in [1, 32768]: R blocks of L steps a warp, S CTAs a cluster, and
 // smem_per_block bytes of dynamic shared memory a CTA for each of the R.
 template <int L, typename... KArgs, typename... Args>
 cudaError_t launch_mb(void (*kern)(KArgs...), size_t smem_per_block, int64_t B, int64_t T, int64_t D,
@@ -847,21 +766,12 @@ cudaError_t launch_psl_bwd_cl(const float *lc, const float *lv, const float *lh0
 
 cudaError_t launch_psl_bwd_rc_cl(const float *lc, const float *lv, const float *lh0, const float *g, float *dlc,
                                  float *dlv, float *dlh0, int64_t B, int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT)
-        return launch_mb<8>(psl_bwd_rc_cl_mb_kernel<8>, 2 * sizeof(float) * 32 * kLinWarps, B, T, D, s, lc, lv, lh0, g,
-                            dlc, dlv, dlh0);
-    const int64_t groups = (D + 31) / 32;
+    // several-block kernel at every T (also where the forward and the saved-h
+    // backward take one block a warp: its two walks over 8-step blocks beat a
+    // one-block recompute kernel at every shape measured)
     if (T < 1) return cudaErrorInvalidConfiguration;
-    const LinPlan p = lin_plan(T);
-    const int64_t blocks = B * groups * p.S;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    if (blocks == 0) return cudaSuccess;
-#define PSL_RC(L_, CL_)                                                                                          \
-    launch_cluster(psl_bwd_rc_cl_kernel<L_, CL_>, blocks, 32 * kLinWarps, 0, p.S, s, lc, lv, lh0, g, dlc, dlv, \
-                   dlh0, T, D, groups, p.S)
-    if (p.L == 16) return PSL_RC(16, true);  // T > 512: always more than one CTA
-    return p.S == 1 ? PSL_RC(8, false) : PSL_RC(8, true);
-#undef PSL_RC
+    return launch_mb<8>(psl_bwd_rc_cl_mb_kernel<8>, 2 * sizeof(float) * 32 * kLinWarps, B, T, D, s, lc, lv, lh0, g,
+                        dlc, dlv, dlh0);
 }
 
 }  // namespace mgs
