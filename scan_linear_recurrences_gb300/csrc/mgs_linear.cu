@@ -27,10 +27,10 @@
 // (a = exp(log_coeffs)), as above, with d_log_values = lambda_t exp(lv_t),
 // d_log_coeffs = a_t lambda_t h_{t-1}, d_log_h0 = a_0 lambda_0 h_0.  It
 // runs up to T = 32768 with the *_mb_ kernels at the end of this file: the
-// same scheme with each warp holding R blocks of L = 16 (forward) or 8
-// (backwards) steps; the first walk composes all of them, the second reads
-// each block again (from L2) as it reruns it, both loading the next block
-// while one is worked on.  The backward without the saved h always runs
+// same scheme with each warp holding R blocks of L = 8 steps; the first walk
+// composes all of them, the second reads each block again (from L2) as it
+// reruns it, both loading the next block(s) while one (the forward: two side
+// by side) is worked on.  The backward without the saved h always runs
 // there, whatever T.
 #include <math_constants.h>
 
@@ -44,7 +44,7 @@ namespace {
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
 constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;  // one block a warp
-constexpr int64_t kLinMaxTBlocks = 32768;  // several blocks a warp: R <= 64 blocks of 8 steps or 32 of 16
+constexpr int64_t kLinMaxTBlocks = 32768;  // several blocks a warp: R <= 64 blocks of 8 steps
 
 struct LinSmem {
     float m[kLinWarps][32], c[kLinWarps][32];    // each warp's map
@@ -379,37 +379,76 @@ __device__ __forceinline__ int psl_raw_block(const float *__restrict__ lc, const
     return n;
 }
 
-// The blocks are double-buffered: block k+1's loads are issued before block
-// k is walked (the loop goes two blocks at a time so that the buffers are
-// fixed registers).
+// The forward in two walks over the warp's blocks, two blocks at a time,
+// with the next two loaded meanwhile (four block buffers).  The first walk
+// takes each block's own map from the identity (two independent chains at a
+// time) and chains those R maps into the map of the warp's blocks before
+// each block, kept in dynamic shared memory (2 R floats a thread); the second
+// turns that map and the state entering the warp into each block's entering
+// state, so that two blocks are walked side by side as well.
 template <int L>
 __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (clusters of 8 need them)
     psl_fwd_cl_mb_kernel(const float *__restrict__ lc, const float *__restrict__ lv, const float *__restrict__ lh0,
                       float *__restrict__ h, float *__restrict__ logh, int64_t T, int64_t D, int64_t groups,
                       int S, int R) {
     __shared__ LinSmem sm;
+    extern __shared__ float pre[];  // [R][256] A, then [R][256] V: the warp's map before block k
+    constexpr int NT = 32 * kLinWarps;
+    float *preA = pre, *preV = pre + size_t(R) * NT;
     const LinLane q = lin_lane<L>(T, D, groups, S, R);
-    const int lane = q.lane, w = q.w;
-    float cv0[L], vr0[L], cv1[L], vr1[L];
-    float A = 0.f, V = -CUDART_INF_F;
-    auto compose = [&](const float (&cv)[L], const float (&vr)[L]) {
+    const int lane = q.lane, w = q.w, tid = threadIdx.x;
+    float c0[L], v0[L], c1[L], v1[L], c2[L], v2[L], c3[L], v3[L];
+    // block k's raw inputs (identity steps past the warp's R blocks)
+    auto ld = [&](int k, float (&cv)[L], float (&vr)[L]) {
+        if (k < R) return psl_raw_block<L>(lc, lv, q, k, T, D, cv, vr);
 #pragma unroll
         for (int u = 0; u < L; ++u) {
-            V = lae2(fmaf(cv[u], kLog2e, V), vr[u] * kLog2e);
-            A = fmaf(cv[u], kLog2e, A);
+            cv[u] = 0.f;
+            vr[u] = -CUDART_INF_F;
+        }
+        return 0;
+    };
+    float WA = 0.f, WV = -CUDART_INF_F;  // the warp's map of the blocks composed so far
+    // blocks ka and ka + 1: their own maps side by side, then chained on
+    auto compose2 = [&](int ka, const float (&ca)[L], const float (&va)[L], const float (&cb)[L],
+                        const float (&vb)[L]) {
+        float Aa = 0.f, Va = -CUDART_INF_F, Ab = 0.f, Vb = -CUDART_INF_F;
+#pragma unroll
+        for (int u = 0; u < L; ++u) {
+            Va = lae2(fmaf(ca[u], kLog2e, Va), va[u] * kLog2e);
+            Aa = fmaf(ca[u], kLog2e, Aa);
+            Vb = lae2(fmaf(cb[u], kLog2e, Vb), vb[u] * kLog2e);
+            Ab = fmaf(cb[u], kLog2e, Ab);
+        }
+        preA[size_t(ka) * NT + tid] = WA;
+        preV[size_t(ka) * NT + tid] = WV;
+        WV = lae2(Aa + WV, Va);
+        WA += Aa;
+        if (ka + 1 < R) {
+            preA[size_t(ka + 1) * NT + tid] = WA;
+            preV[size_t(ka + 1) * NT + tid] = WV;
+            WV = lae2(Ab + WV, Vb);
+            WA += Ab;
         }
     };
-    psl_raw_block<L>(lc, lv, q, 0, T, D, cv0, vr0);
-    for (int k = 0; k < R; k += 2) {
-        if (k + 1 < R) psl_raw_block<L>(lc, lv, q, k + 1, T, D, cv1, vr1);
-        compose(cv0, vr0);
-        if (k + 1 < R) {
-            if (k + 2 < R) psl_raw_block<L>(lc, lv, q, k + 2, T, D, cv0, vr0);
-            compose(cv1, vr1);
+    ld(0, c0, v0);
+    ld(1, c1, v1);
+    for (int k = 0; k < R; k += 4) {
+        if (k + 2 < R) {
+            ld(k + 2, c2, v2);
+            ld(k + 3, c3, v3);
+        }
+        compose2(k, c0, v0, c1, v1);
+        if (k + 2 < R) {
+            if (k + 4 < R) {
+                ld(k + 4, c0, v0);
+                ld(k + 5, c1, v1);
+            }
+            compose2(k + 2, c2, v2, c3, v3);
         }
     }
-    sm.m[w][lane] = A;
-    sm.c[w][lane] = V;
+    sm.m[w][lane] = WA;
+    sm.c[w][lane] = WV;
     __syncthreads();
     if (w == 0) psl_cta_offsets(sm, lane);
     lin_sync1<true>();
@@ -417,25 +456,41 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     float x = (lh0 != nullptr && q.act) ? lh0[q.bi * D + q.ch] * kLog2e : -CUDART_INF_F;
     for (unsigned p = 0; p < q.r; ++p) x = lae2(ld_dsmem(&sm.tm[lane], p) + x, ld_dsmem(&sm.tc[lane], p));
     lin_arrive2<true>();
-    x = lae2(sm.pm[w][lane] + x, sm.pc[w][lane]);
-    auto walk = [&](int k, int n, const float (&cv)[L], const float (&vr)[L]) {
-        const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+    x = lae2(sm.pm[w][lane] + x, sm.pc[w][lane]);  // entering the warp's blocks
+    // blocks ka and ka + 1 (if any) side by side from their entering states
+    auto walk2 = [&](int ka, int na, const float (&ca)[L], const float (&va)[L], int nb, const float (&cb)[L],
+                     const float (&vb)[L]) {
+        float xa = lae2(preA[size_t(ka) * NT + tid] + x, preV[size_t(ka) * NT + tid]);
+        float xb = ka + 1 < R ? lae2(preA[size_t(ka + 1) * NT + tid] + x, preV[size_t(ka + 1) * NT + tid])
+                              : -CUDART_INF_F;
+        const int64_t ba = q.cb + (q.t0 + int64_t(ka) * L) * D, bb = ba + int64_t(L) * D;
 #pragma unroll
         for (int u = 0; u < L; ++u) {
-            x = lae2(fmaf(cv[u], kLog2e, x), vr[u] * kLog2e);
-            if (u < n) {
-                __stcs(h + base + u * D, ex2_approx(x));
-                if (logh != nullptr) __stcs(logh + base + u * D, x * kLn2);
+            xa = lae2(fmaf(ca[u], kLog2e, xa), va[u] * kLog2e);
+            xb = lae2(fmaf(cb[u], kLog2e, xb), vb[u] * kLog2e);
+            if (u < na) {
+                __stcs(h + ba + u * D, ex2_approx(xa));
+                if (logh != nullptr) __stcs(logh + ba + u * D, xa * kLn2);
+            }
+            if (u < nb) {
+                __stcs(h + bb + u * D, ex2_approx(xb));
+                if (logh != nullptr) __stcs(logh + bb + u * D, xb * kLn2);
             }
         }
     };
-    int n0 = psl_raw_block<L>(lc, lv, q, 0, T, D, cv0, vr0), n1 = 0;
-    for (int k = 0; k < R; k += 2) {
-        if (k + 1 < R) n1 = psl_raw_block<L>(lc, lv, q, k + 1, T, D, cv1, vr1);
-        walk(k, n0, cv0, vr0);
-        if (k + 1 < R) {
-            if (k + 2 < R) n0 = psl_raw_block<L>(lc, lv, q, k + 2, T, D, cv0, vr0);
-            walk(k + 1, n1, cv1, vr1);
+    int n0 = ld(0, c0, v0), n1 = ld(1, c1, v1), n2 = 0, n3 = 0;
+    for (int k = 0; k < R; k += 4) {
+        if (k + 2 < R) {
+            n2 = ld(k + 2, c2, v2);
+            n3 = ld(k + 3, c3, v3);
+        }
+        walk2(k, n0, c0, v0, n1, c1, v1);
+        if (k + 2 < R) {
+            if (k + 4 < R) {
+                n0 = ld(k + 4, c0, v0);
+                n1 = ld(k + 5, c1, v1);
+            }
+            walk2(k + 2, n2, c2, v2, n3, c3, v3);
         }
     }
     lin_wait2<true>();
@@ -732,7 +787,9 @@ cudaError_t launch_lin_bwd(const float *a, const float *h0, const float *h, cons
 
 cudaError_t launch_psl_fwd_cl(const float *lc, const float *lv, const float *lh0, float *h, float *logh, int64_t B,
                               int64_t T, int64_t D, cudaStream_t s) {
-    if (T > kLinMaxT) return launch_mb<16>(psl_fwd_cl_mb_kernel<16>, 0, B, T, D, s, lc, lv, lh0, h, logh);
+    if (T > kLinMaxT)
+        return launch_mb<8>(psl_fwd_cl_mb_kernel<8>, 2 * sizeof(float) * 32 * kLinWarps, B, T, D, s, lc, lv, lh0, h,
+                            logh);
     const int64_t groups = (D + 31) / 32;
     if (T < 1) return cudaErrorInvalidConfiguration;
     const LinPlan p = lin_plan(T);
