@@ -110,12 +110,13 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
     const int n = lin_steps_here(act, L, t0, T);
     const int64_t base = (bi * T + t0) * D + ch;
+    const int ds = int(D);  // steps apart: 32-bit offsets
     const float hinit = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;  // loaded with the inputs
     float av[L], bv[L];
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        av[u] = u < n ? a[base + u * D] : 1.f;
-        bv[u] = u < n ? b[base + u * D] : 0.f;
+        av[u] = u < n ? a[base + u * ds] : 1.f;
+        bv[u] = u < n ? b[base + u * ds] : 0.f;
     }
     float m = 1.f, c = 0.f;
 #pragma unroll
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(32 * kLinWarps)
 #pragma unroll
     for (int u = 0; u < L; ++u) {
         x = fmaf(av[u], x, bv[u]);
-        if (u < n) __stcs(h + base + u * D, x);
+        if (u < n) __stcs(h + base + u * ds, x);
     }
     lin_wait2<kCl>();  // no CTA leaves while another may still read its shared memory
 }
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
     const int n = lin_steps_here(act, L, t0, T);
     const int64_t base = (bi * T + t0) * D + ch;
+    const int ds = int(D);  // steps apart: 32-bit offsets
     const float hinit = (h0 != nullptr && act) ? h0[bi * D + ch] : 0.f;
     // step t's coefficient is a_{t+1} (none past the end: lambda_T = 0), and
     // da_t needs h_{t-1} (h0, or zero, before the first step); steps past n
@@ -163,9 +165,9 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     float an[L], gv[L], hp[L];
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        an[u] = u < n ? (t0 + u + 1 < T ? a[base + (u + 1) * D] : 0.f) : 1.f;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * D] : hinit) : 0.f;
+        an[u] = u < n ? (t0 + u + 1 < T ? a[base + (u + 1) * ds] : 0.f) : 1.f;
+        gv[u] = u < n ? g[base + u * ds] : 0.f;
+        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * ds] : hinit) : 0.f;
     }
     float m = 1.f, c = 0.f;
 #pragma unroll
@@ -189,8 +191,8 @@ __global__ void __launch_bounds__(32 * kLinWarps)
     for (int u = L - 1; u >= 0; --u) {
         lam = fmaf(an[u], lam, gv[u]);
         if (u < n) {
-            __stcs(db + base + u * D, lam);
-            __stcs(da + base + u * D, lam * hp[u]);
+            __stcs(db + base + u * ds, lam);
+            __stcs(da + base + u * ds, lam * hp[u]);
         }
     }
     // lam is lambda_0 in the first warp of the first CTA
@@ -287,18 +289,19 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     const int64_t t0 = (int64_t(r) * kLinWarps + w) * L;
     const int n = lin_steps_here(act, L, t0, T);
     const int64_t base = (bi * T + t0) * D + ch;
+    const int ds = int(D);  // steps apart: 32-bit offsets
     const float h0v = (lh0 != nullptr && act) ? ex2_approx(lh0[bi * D + ch] * kLog2e) : 0.f;
     // a_t, exp(lv_t), g_t, h_{t-1} (h0 before the first step) of this warp's
     // steps, and a after its last step (zero past the end: lambda_T = 0)
     float at[L], ev[L], gv[L], hp[L];
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        at[u] = u < n ? ex2_approx(lc[base + u * D] * kLog2e) : 1.f;
-        ev[u] = u < n ? ex2_approx(lv[base + u * D] * kLog2e) : 0.f;
-        gv[u] = u < n ? g[base + u * D] : 0.f;
-        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
+        at[u] = u < n ? ex2_approx(lc[base + u * ds] * kLog2e) : 1.f;
+        ev[u] = u < n ? ex2_approx(lv[base + u * ds] * kLog2e) : 0.f;
+        gv[u] = u < n ? g[base + u * ds] : 0.f;
+        hp[u] = u < n ? (t0 + u >= 1 ? h[base + (u - 1) * ds] : h0v) : 0.f;
     }
-    const float aft = (n > 0 && t0 + n < T) ? ex2_approx(lc[base + n * D] * kLog2e) : 0.f;
+    const float aft = (n > 0 && t0 + n < T) ? ex2_approx(lc[base + n * ds] * kLog2e) : 0.f;
     // step t's coefficient a_{t+1}; steps past n are the identity
     auto coef = [&](int u) { return u + 1 < n ? at[u + 1] : (u + 1 == n ? aft : 1.f); };
     float m = 1.f, c = 0.f;
@@ -322,8 +325,8 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
     for (int u = L - 1; u >= 0; --u) {
         lam = fmaf(coef(u), lam, gv[u]);
         if (u < n) {
-            __stcs(dlv + base + u * D, lam * ev[u]);
-            __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+            __stcs(dlv + base + u * ds, lam * ev[u]);
+            __stcs(dlc + base + u * ds, at[u] * lam * hp[u]);
         }
     }
     // lam is lambda_0 in the first warp of the first CTA
@@ -371,10 +374,12 @@ __device__ __forceinline__ int psl_raw_block(const float *__restrict__ lc, const
                                              float (&vr)[L]) {
     const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
     const int n = lin_steps_here(q.act, L, tk, T);
+    const int ds = int(D);  // steps apart within a block: 32-bit offsets
+    const float *pc = lc + base, *pv = lv + base;
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        cv[u] = u < n ? lc[base + u * D] : 0.f;
-        vr[u] = u < n ? lv[base + u * D] : -CUDART_INF_F;
+        cv[u] = u < n ? pc[u * ds] : 0.f;
+        vr[u] = u < n ? pv[u * ds] : -CUDART_INF_F;
     }
     return n;
 }
@@ -463,18 +468,20 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
         float xa = lae2(preA[size_t(ka) * NT + tid] + x, preV[size_t(ka) * NT + tid]);
         float xb = ka + 1 < R ? lae2(preA[size_t(ka + 1) * NT + tid] + x, preV[size_t(ka + 1) * NT + tid])
                               : -CUDART_INF_F;
-        const int64_t ba = q.cb + (q.t0 + int64_t(ka) * L) * D, bb = ba + int64_t(L) * D;
+        const int64_t ba = q.cb + (q.t0 + int64_t(ka) * L) * D;
+        const int ds = int(D);
+        float *ha = h + ba, *la = logh != nullptr ? logh + ba : nullptr;  // block ka + 1 at L * ds past them
 #pragma unroll
         for (int u = 0; u < L; ++u) {
             xa = lae2(fmaf(ca[u], kLog2e, xa), va[u] * kLog2e);
             xb = lae2(fmaf(cb[u], kLog2e, xb), vb[u] * kLog2e);
             if (u < na) {
-                __stcs(h + ba + u * D, ex2_approx(xa));
-                if (logh != nullptr) __stcs(logh + ba + u * D, xa * kLn2);
+                __stcs(ha + u * ds, ex2_approx(xa));
+                if (logh != nullptr) __stcs(la + u * ds, xa * kLn2);
             }
             if (u < nb) {
-                __stcs(h + bb + u * D, ex2_approx(xb));
-                if (logh != nullptr) __stcs(logh + bb + u * D, xb * kLn2);
+                __stcs(ha + (L + u) * ds, ex2_approx(xb));
+                if (logh != nullptr) __stcs(la + (L + u) * ds, xb * kLn2);
             }
         }
     };
@@ -506,14 +513,16 @@ __device__ __forceinline__ int psl_bwd_raw(const float *__restrict__ lc, const f
                                            float (&gr)[L], float (&hr)[L], float *lca) {
     const int64_t tk = q.t0 + int64_t(k) * L, base = q.cb + tk * D;
     const int n = lin_steps_here(q.act, L, tk, T);
+    const int ds = int(D);  // steps apart within a block: 32-bit offsets
+    const float *plc = lc + base, *pg = g + base;
 #pragma unroll
     for (int u = 0; u < L; ++u) {
-        lcr[u] = u < n ? lc[base + u * D] : 0.f;
-        gr[u] = u < n ? g[base + u * D] : 0.f;
-        if constexpr (kLv) lvr[u] = u < n ? lv[base + u * D] : -CUDART_INF_F;
-        if constexpr (kH) hr[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * D] : h0v) : 0.f;
+        lcr[u] = u < n ? plc[u * ds] : 0.f;
+        gr[u] = u < n ? pg[u * ds] : 0.f;
+        if constexpr (kLv) lvr[u] = u < n ? lv[base + u * ds] : -CUDART_INF_F;
+        if constexpr (kH) hr[u] = u < n ? (tk + u >= 1 ? h[base + (u - 1) * ds] : h0v) : 0.f;
     }
-    *lca = (n > 0 && tk + n < T) ? lc[base + n * D] : -CUDART_INF_F;
+    *lca = (n > 0 && tk + n < T) ? plc[n * ds] : -CUDART_INF_F;
     return n;
 }
 
@@ -578,12 +587,14 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
         float cf[L], at[L];
         coefs(lcr, lca, n, cf, at);
         const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+        const int ds = int(D);
+        float *pv = dlv + base, *pc = dlc + base;
 #pragma unroll
         for (int u = L - 1; u >= 0; --u) {
             lam = fmaf(cf[u], lam, gr[u]);
             if (u < n) {
-                __stcs(dlv + base + u * D, lam * ex2_approx(lvr[u] * kLog2e));
-                __stcs(dlc + base + u * D, at[u] * lam * hr[u]);
+                __stcs(pv + u * ds, lam * ex2_approx(lvr[u] * kLog2e));
+                __stcs(pc + u * ds, at[u] * lam * hr[u]);
             }
         }
         // lam is lambda_0 at block 0 of the first warp of the first CTA
@@ -688,12 +699,14 @@ __global__ void __launch_bounds__(32 * kLinWarps, 2)  // two CTAs per SM (cluste
         }
         coefs(lcr, lca, n, cf, at);
         const int64_t base = q.cb + (q.t0 + int64_t(k) * L) * D;
+        const int ds = int(D);
+        float *pv = dlv + base, *pc = dlc + base;
 #pragma unroll
         for (int u = L - 1; u >= 0; --u) {
             lam = fmaf(cf[u], lam, gr[u]);
             if (u < n) {
-                __stcs(dlv + base + u * D, lam * ex2_approx(lvr[u] * kLog2e));
-                __stcs(dlc + base + u * D, at[u] * lam * hp[u]);
+                __stcs(pv + u * ds, lam * ex2_approx(lvr[u] * kLog2e));
+                __stcs(pc + u * ds, at[u] * lam * hp[u]);
             }
         }
         // lam is lambda_0 and hp[0] is h0 at block 0 of the first warp of the first CTA
