@@ -318,6 +318,13 @@ def fp32_fma_peak_tflops():
 class Runner:
     """Holds one workload's device buffers and runs its fwd / bwd calls."""
 
+    def kernels_per_step(self):
+        """Kernel launches of one fwd + one bwd call: the time-chunked
+        matrix_affine_scan and matrix_scan paths (a nonzero workspace) run
+        three launches a call, every other step workload one."""
+        per_call = 3 if self.w.op in ("mas", "ms") and self.nf > 0 else 1
+        return 2 * per_call
+
     def __init__(self, w, torch, b, api, device):
         self.w = w
         self.t = torch
@@ -745,7 +752,7 @@ def run_gpu(args):
             # the report-only shapes first and the per-op lines of the step
             # last, so that a reader keeping only the end of the line keeps them
             "extra_ops_not_in_step": extra, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": args.steps * 2 * len(runners), "clocks": clocks,
+            "gpu_launches": args.steps * sum(r.kernels_per_step() for r in runners), "clocks": clocks,
             "impl": "libmgscan", "ops": ops,
         }
         print(json.dumps(line), flush=True)

@@ -11,6 +11,24 @@ import bench
 from scan_linear_recurrences_gb300 import inputs
 
 
+def test_kernel_launch_count_per_step():
+    """gpu_launches counts kernels: three a call on the time-chunked paths
+    (a nonzero workspace), one otherwise."""
+    from types import SimpleNamespace as NS
+    k = bench.Runner.kernels_per_step
+    assert k(NS(w=NS(op="ms"), nf=4096)) == 6
+    assert k(NS(w=NS(op="mas"), nf=4096)) == 6
+    assert k(NS(w=NS(op="mas"), nf=0)) == 2
+    assert k(NS(w=NS(op="psl"), nf=0)) == 2
+    # the step's four workloads: mas lab and scaled single-pass, ms long-T
+    # chunked, psl minGRU one launch a call
+    from scan_linear_recurrences_gb300 import _binding as b
+    plans = [(1, b.MGS_OP_MATRIX_AFFINE_SCAN_FWD), (2, b.MGS_OP_MATRIX_SCAN_FWD), (4, b.MGS_OP_MATRIX_AFFINE_SCAN_FWD)]
+    sizes = {cid: b.mgs_workspace_size(op, inputs.WORKLOADS[cid].B, inputs.WORKLOADS[cid].T,
+                                       inputs.WORKLOADS[cid].H, inputs.WORKLOADS[cid].k) for cid, op in plans}
+    assert sizes[1] == 0 and sizes[4] == 0 and sizes[2] > 0
+
+
 def test_algorithmic_bytes_per_unit():
     w1, w2, w3, w4 = (inputs.WORKLOADS[i] for i in (1, 2, 3, 4))
     # matrix_affine_scan: 320 B/step forward, 608 B/step backward (+ initial-state terms)
