@@ -43,6 +43,7 @@ namespace {
 
 constexpr int kLinWarps = 8;   // W
 constexpr int kLinMaxCta = 8;  // S at most: the portable cluster size limit
+constexpr int kLinMaxCtaWide = 16;  // S at most with few lane groups (non-portable cluster size)
 constexpr int64_t kLinMaxT = int64_t(16) * kLinWarps * kLinMaxCta;  // one block a warp
 constexpr int64_t kLinMaxTBlocks = 32768;  // several blocks a warp: R <= 64 blocks of 8 steps
 
@@ -737,22 +738,36 @@ LinPlan lin_plan(int64_t T) {
 
 // T in [1, 32768]: R blocks of L steps a warp, S CTAs a cluster, and
 // smem_per_block bytes of dynamic shared memory a CTA for each of the R.
+// With few lane groups (fewer than 128 CTAs at 8 a cluster) a long sequence
+// takes clusters of up to 16 CTAs (the non-portable size), twice the SMs;
+// if such a cluster cannot be launched the call falls back to 8.
 template <int L, typename... KArgs, typename... Args>
 cudaError_t launch_mb(void (*kern)(KArgs...), size_t smem_per_block, int64_t B, int64_t T, int64_t D,
                       cudaStream_t s, Args... args) {
     if (T > kLinMaxTBlocks) return cudaErrorInvalidConfiguration;
     const int64_t groups = (D + 31) / 32, cta_steps = int64_t(L) * kLinWarps;
-    const int R = int((T + cta_steps * kLinMaxCta - 1) / (cta_steps * kLinMaxCta));
-    const int S = int((T + cta_steps * R - 1) / (cta_steps * R));
-    const int64_t blocks = B * groups * S;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    if (blocks == 0) return cudaSuccess;
-    const size_t smem = smem_per_block * size_t(R);
-    if (smem > 48 * 1024) {  // past the default limit (at most 128 KB: R <= 64)
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
+    auto go = [&](int smax) -> cudaError_t {
+        const int R = int((T + cta_steps * smax - 1) / (cta_steps * smax));
+        const int S = int((T + cta_steps * R - 1) / (cta_steps * R));
+        const int64_t blocks = B * groups * S;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        if (blocks == 0) return cudaSuccess;
+        const size_t smem = smem_per_block * size_t(R);
+        cudaError_t e;
+        if (smem > 48 * 1024) {  // past the default limit (at most 128 KB: R <= 64)
+            if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
+                return e;
+        }
+        if (S > kLinMaxCta &&
+            (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+            return e;
+        return launch_cluster(kern, blocks, 32 * kLinWarps, smem, S, s, args..., T, D, groups, S, R);
+    };
+    if (B * groups * kLinMaxCta < 128 && T > cta_steps * kLinMaxCta) {
+        if (go(kLinMaxCtaWide) == cudaSuccess) return cudaSuccess;
+        (void)cudaGetLastError();  // a launch-configuration error: not sticky
     }
-    return launch_cluster(kern, blocks, 32 * kLinWarps, smem, S, s, args..., T, D, groups, S, R);
+    return go(kLinMaxCta);
 }
 
 }  // namespace
