@@ -738,8 +738,9 @@ LinPlan lin_plan(int64_t T) {
 
 // T in [1, 32768]: R blocks of L steps a warp, S CTAs a cluster, and
 // smem_per_block bytes of dynamic shared memory a CTA for each of the R.
-// With few lane groups (fewer than 128 CTAs at 8 a cluster) a long sequence
-// takes clusters of up to 16 CTAs (the non-portable size), twice the SMs;
+// With few lane groups (fewer than 16: fewer than 128 CTAs at 8 a cluster)
+// a long sequence takes clusters of up to 16 CTAs (the non-portable size),
+// twice the SMs (at 16 groups and more the wider clusters measured slower);
 // if such a cluster cannot be launched the call falls back to 8.
 template <int L, typename... KArgs, typename... Args>
 cudaError_t launch_mb(void (*kern)(KArgs...), size_t smem_per_block, int64_t B, int64_t T, int64_t D,
