@@ -43,10 +43,16 @@ __device__ __forceinline__ float4 ld_dsmem4(const float *p, unsigned rank) {
     return v;
 }
 
-// Launches kern on `blocks` CTAs (a multiple of S) in clusters of S along x.
+// Launches kern on `blocks` CTAs (a multiple of S) in clusters of S along x
+// (past the portable size of 8, up to 16, with the kernel's permission set
+// here first).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_cluster(void (*kern)(KArgs...), int64_t blocks, int threads, size_t smem, int S, cudaStream_t s,
                            Args... args) {
+    if (S > 8) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(blocks));
     cfg.blockDim = dim3(unsigned(threads));
